@@ -1,0 +1,118 @@
+"""fp64 CPU oracle for the Q8_0 decode matvec: test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+and reference legs may import this package.  The product library never loads
+it; if the CUDA library is missing, the product fails instead of falling back
+to anything here.
+
+The arithmetic lives in ``q8mv_oracle.c`` (plain C, fp64, no fused
+multiply-add contraction); this module only compiles it with gcc and
+marshals numpy arrays through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q8mv_oracle.c")
+_LIB = os.path.join(_HERE, "libq8mv_oracle.so")
+
+# -ffp-contract=off keeps every product and sum a separate IEEE operation on
+# both x86_64 and aarch64 (gcc contracts a*b+c into an fma by default).
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+_lib = None
+
+
+def build(src: str = _SRC, out: str = _LIB, force: bool = False) -> str:
+    """Compile the oracle into a shared library and return its path."""
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(src)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, src, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library."""
+
+    def __init__(self, path: str):
+        self.path = path
+        lib = ctypes.CDLL(path)
+        i64, p = ctypes.c_int64, ctypes.c_void_p
+        lib.q8mv_oracle_unfactored.argtypes = [i64, i64, p, p, p, p]
+        lib.q8mv_oracle_unfactored.restype = ctypes.c_int
+        lib.q8mv_oracle_factored.argtypes = [i64, i64, p, p, p, p, p]
+        lib.q8mv_oracle_factored.restype = ctypes.c_int
+        lib.q8mv_oracle_block_sums.argtypes = [i64, i64, p, p, p]
+        lib.q8mv_oracle_block_sums.restype = ctypes.c_int
+        self._lib = lib
+
+    @staticmethod
+    def _check(A, W, S):
+        A = np.ascontiguousarray(A, dtype=np.float32)
+        W = np.ascontiguousarray(W, dtype=np.int8)
+        K, N = W.shape
+        if A.size != K:
+            raise ValueError(f"A has {A.size} elements, W has K={K} rows")
+        if S is not None:
+            S = np.ascontiguousarray(S, dtype=np.float32)
+            KB = (K + 31) // 32
+            if S.shape != (KB, N):
+                raise ValueError(f"S has shape {S.shape}, expected {(KB, N)}")
+        return A, W, S, K, N
+
+    @staticmethod
+    def _ptr(x):
+        return x.ctypes.data if x is not None and x.size else None
+
+    def factored(self, A, W, S):
+        """Return (C, bound), both fp64 [N]: block-factored form and sum |A W S|."""
+        A, W, S, K, N = self._check(A, W, S)
+        # outputs start as NaN so that a result that is not fully written shows
+        C = np.full(N, np.nan, dtype=np.float64)
+        bound = np.full(N, np.nan, dtype=np.float64)
+        rc = self._lib.q8mv_oracle_factored(K, N, self._ptr(A), self._ptr(W), self._ptr(S),
+                                            self._ptr(C), self._ptr(bound))
+        if rc != 0:
+            raise RuntimeError(f"q8mv_oracle_factored returned {rc}")
+        return C, bound
+
+    def unfactored(self, A, W, S):
+        """Return C fp64 [N] from the per-weight sum of A W S."""
+        A, W, S, K, N = self._check(A, W, S)
+        C = np.full(N, np.nan, dtype=np.float64)
+        rc = self._lib.q8mv_oracle_unfactored(K, N, self._ptr(A), self._ptr(W), self._ptr(S),
+                                              self._ptr(C))
+        if rc != 0:
+            raise RuntimeError(f"q8mv_oracle_unfactored returned {rc}")
+        return C
+
+    def block_sums(self, A, W):
+        """Return the unscaled block sums, fp64 [KB, N]."""
+        A, W, _, K, N = self._check(A, W, None)
+        KB = (K + 31) // 32
+        P = np.full((KB, N), np.nan, dtype=np.float64)
+        rc = self._lib.q8mv_oracle_block_sums(K, N, self._ptr(A), self._ptr(W), self._ptr(P))
+        if rc != 0:
+            raise RuntimeError(f"q8mv_oracle_block_sums returned {rc}")
+        return P
+
+
+def load() -> Oracle:
+    """Build (if stale) and load the oracle library."""
+    global _lib
+    if _lib is None:
+        _lib = Oracle(build())
+    return _lib
+
+
+def tolerance(bound: np.ndarray) -> np.ndarray:
+    """Per-element acceptance bound for an f32 result: 1e-5 * sum|A W S| + 1e-6."""
+    return 1e-5 * bound + 1e-6

@@ -1,0 +1,149 @@
+/*
+ * Q8_0 decode matvec: CPU oracle in fp64.
+ *
+ * TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT.  Only the tests, the smoke
+ * check and the benchmark's CPU-baseline / reference legs load this file's
+ * library.  The GPU library never includes, links or calls it, and this file
+ * includes nothing from the GPU library.
+ *
+ * What it computes (Phobos docs, "Q8_0 matvec" example page):
+ *   - "The tensors": A is [1, K] f32 (one activation row), W is [K, N] signed
+ *     bytes (one column per output), S is [KB, N] f32 where row b of S scales
+ *     rows 32*b up to 32*b + 32 of W, and C is [1, N] f32.  The value a weight
+ *     stands for is W[k, n] * S[k / 32, n], so
+ *         C[0, n] = sum over k of A[0, k] * W[k, n] * S[k / 32, n].
+ *   - "Factoring out the scale": inside a block every weight of a column shares
+ *     one scale, so the block sum is taken on the raw bytes and scaled once:
+ *         sum_{k in b} A[k] W[k,n] S[b,n] = S[b,n] * sum_{k in b} A[k] W[k,n].
+ *   - "Bounds": K need not be a multiple of 32; the loop over K is whole blocks
+ *     plus one masked remainder, so the last block may hold fewer than 32 rows
+ *     and KB = ceil(K / 32).  Rows at or past K are never read.
+ *   - "Line by line": acc starts at 0 and C is assigned acc after the last
+ *     block, so C is overwritten (not accumulated into) and K = 0 gives C = 0.
+ *
+ * Readings where the pages are silent:
+ *   - Layout: every tensor is contiguous row-major, W[k, n] at k*N + n and
+ *     S[b, n] at b*N + n (the slices W[k :+ BLK, pn*TILE_N :+ TILE_N] of the
+ *     kernel listing index rows by k and columns by n).
+ *   - Precision: the pages fix f32 tiles for the GPU kernel but nothing for a
+ *     checker, so every product and sum here is taken in fp64.  Each product
+ *     A*W is exact in fp64 (24-bit by 8-bit significands); A*W*S rounds once.
+ *   - Signed bytes cover -128 .. 127; -128 is a legal weight.
+ *
+ * Both forms are pinned by CPU tests against exact rational brute force,
+ * closed forms, one-hot special cases, linearity and exact-integer inputs.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <math.h>
+
+#define Q8MV_ORACLE_BLK 32
+
+static int64_t oracle_num_blocks(int64_t K) {
+    return (K + Q8MV_ORACLE_BLK - 1) / Q8MV_ORACLE_BLK;
+}
+
+/* Return codes: 0 ok, -1 bad argument, -2 out of host memory. */
+
+/*
+ * Per-weight form ("The tensors"): C[n] = sum_k A[k] * W[k,n] * S[k/32, n],
+ * each term formed and added in fp64, k ascending.
+ */
+int q8mv_oracle_unfactored(int64_t K, int64_t N, const float *A, const int8_t *W,
+                           const float *S, double *C) {
+    if (K < 0 || N < 0) return -1;
+    if (N > 0 && C == NULL) return -1;
+    if (K > 0 && N > 0 && (A == NULL || W == NULL || S == NULL)) return -1;
+    for (int64_t n = 0; n < N; ++n) C[n] = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double a = (double)A[k];
+        const int8_t *w_row = W + k * N;
+        const float *s_row = S + (k / Q8MV_ORACLE_BLK) * N;
+        for (int64_t n = 0; n < N; ++n)
+            C[n] += a * (double)w_row[n] * (double)s_row[n];
+    }
+    return 0;
+}
+
+/*
+ * Block-factored form ("Factoring out the scale", "Line by line"): for each
+ * block b, part[n] = sum_{k in b, k < K} A[k] * W[k,n] on the raw bytes, then
+ * acc[n] += part[n] * S[b,n], one multiply per block and column.
+ *
+ * bound (nullable) receives sum_k |A[k] * W[k,n] * S[k/32,n]|, the magnitude
+ * against which a rounded result's error is judged.
+ */
+int q8mv_oracle_factored(int64_t K, int64_t N, const float *A, const int8_t *W,
+                         const float *S, double *C, double *bound) {
+    if (K < 0 || N < 0) return -1;
+    if (N > 0 && C == NULL) return -1;
+    if (K > 0 && N > 0 && (A == NULL || W == NULL || S == NULL)) return -1;
+    for (int64_t n = 0; n < N; ++n) {
+        C[n] = 0.0;
+        if (bound) bound[n] = 0.0;
+    }
+    if (K == 0 || N == 0) return 0;
+
+    double *part = (double *)malloc((size_t)N * sizeof(double));
+    double *mag = (double *)malloc((size_t)N * sizeof(double));
+    if (part == NULL || mag == NULL) {
+        free(part);
+        free(mag);
+        return -2;
+    }
+    const int64_t KB = oracle_num_blocks(K);
+    for (int64_t b = 0; b < KB; ++b) {
+        const int64_t k_begin = b * Q8MV_ORACLE_BLK;
+        int64_t k_end = k_begin + Q8MV_ORACLE_BLK;
+        if (k_end > K) k_end = K; /* masked remainder of the last block */
+        for (int64_t n = 0; n < N; ++n) {
+            part[n] = 0.0;
+            mag[n] = 0.0;
+        }
+        /* the block's dot product on the unscaled bytes */
+        for (int64_t k = k_begin; k < k_end; ++k) {
+            const double a = (double)A[k];
+            const int8_t *w_row = W + k * N;
+            for (int64_t n = 0; n < N; ++n) {
+                const double aw = a * (double)w_row[n];
+                part[n] += aw;
+                mag[n] += fabs(aw);
+            }
+        }
+        /* the block's scale, applied once per column */
+        const float *s_row = S + b * N;
+        for (int64_t n = 0; n < N; ++n) {
+            const double s = (double)s_row[n];
+            C[n] += part[n] * s;
+            if (bound) bound[n] += mag[n] * fabs(s);
+        }
+    }
+    free(part);
+    free(mag);
+    return 0;
+}
+
+/*
+ * The unscaled block sums themselves, part[b, n] = sum_{k in b, k < K}
+ * A[k] * W[k, n], as a [KB, N] fp64 array.  With integer-valued A these are
+ * integers, which is what a bit-exact check of a kernel's block sums needs.
+ */
+int q8mv_oracle_block_sums(int64_t K, int64_t N, const float *A, const int8_t *W,
+                           double *part) {
+    if (K < 0 || N < 0) return -1;
+    const int64_t KB = oracle_num_blocks(K);
+    if (KB > 0 && N > 0 && (A == NULL || W == NULL || part == NULL)) return -1;
+    for (int64_t b = 0; b < KB; ++b) {
+        double *p_row = part + b * N;
+        for (int64_t n = 0; n < N; ++n) p_row[n] = 0.0;
+        const int64_t k_begin = b * Q8MV_ORACLE_BLK;
+        int64_t k_end = k_begin + Q8MV_ORACLE_BLK;
+        if (k_end > K) k_end = K;
+        for (int64_t k = k_begin; k < k_end; ++k) {
+            const double a = (double)A[k];
+            const int8_t *w_row = W + k * N;
+            for (int64_t n = 0; n < N; ++n) p_row[n] += a * (double)w_row[n];
+        }
+    }
+    return 0;
+}

@@ -1,0 +1,253 @@
+"""Pins for the fp64 oracle: checks against what the pages and arithmetic fix.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises ``AssertionError`` when
+the oracle disagrees with an independent fact:
+
+- exact rational brute force (Python ``fractions``), written with its own loop
+  order and its own indexing of the scale row, on tiny ragged shapes;
+- the closed form A = 1, W = 1, S = s  =>  C[n] = K * s;
+- one-hot activations and one-hot weights, which isolate a single term and so
+  pin the block <-> scale-row mapping, including the partial last block;
+- linearity in A and, block by block, in S;
+- exact-integer inputs checked against numpy int64 arithmetic;
+- the factoring identity of "Factoring out the scale" (both forms agree);
+- the scale-row rule printed in "The tensors", read from a golden fixture.
+
+The pins are shared by ``test_oracle_pins.py`` (the real oracle must pass all)
+and ``test_oracle_mutants.py`` (each planted mistake must fail at least one).
+"""
+from __future__ import annotations
+
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+EPS64 = 2.0 ** -53
+
+
+def _rng(seed):
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def exact_matvec(A, W, S):
+    """C[n] = sum_k A[k] W[k,n] S[floor(k/32), n] in exact rational arithmetic."""
+    K, N = W.shape
+    out = []
+    for n in range(N):
+        total = Fraction(0)
+        for k in range(K):
+            total += Fraction(float(A.flat[k])) * int(W[k, n]) * Fraction(float(S[k // 32, n]))
+        out.append(total)
+    return out
+
+
+def exact_abs_sum(A, W, S):
+    K, N = W.shape
+    return [sum(abs(Fraction(float(A.flat[k])) * int(W[k, n]) * Fraction(float(S[k // 32, n])))
+                for k in range(K)) for n in range(N)]
+
+
+def pin_exact_rational(orc):
+    shapes = [(1, 1), (5, 3), (31, 2), (32, 4), (33, 3), (37, 5), (64, 2), (70, 3)]
+    for i, (K, N) in enumerate(shapes):
+        A, W, S = workloads.make_random(K, N, seed=100 + i)
+        W[0, 0] = -128  # the most negative byte is a legal weight
+        exact = exact_matvec(A, W, S)
+        mag = exact_abs_sum(A, W, S)
+        C, bound = orc.factored(A, W, S)
+        Cu = orc.unfactored(A, W, S)
+        for n in range(N):
+            tol = 4 * (K + 2) * EPS64 * float(mag[n]) + 1e-300
+            assert abs(C[n] - float(exact[n])) <= tol, ("factored", K, N, n, C[n], float(exact[n]))
+            assert abs(Cu[n] - float(exact[n])) <= tol, ("unfactored", K, N, n, Cu[n], float(exact[n]))
+            assert abs(bound[n] - float(mag[n])) <= tol, ("bound", K, N, n, bound[n], float(mag[n]))
+
+
+def pin_closed_form_ones(orc):
+    for K in (1, 31, 32, 33, 100, 4100):
+        for s in (np.float32(2.0 ** -7), np.float32(0.0123)):
+            N = 5
+            A = np.ones((1, K), np.float32)
+            W = np.ones((K, N), np.int8)
+            S = np.full((workloads.num_blocks(K), N), s, np.float32)
+            C, bound = orc.factored(A, W, S)
+            Cu = orc.unfactored(A, W, S)
+            expect = K * float(s)
+            tol = 4 * K * EPS64 * expect
+            assert np.all(np.abs(C - expect) <= tol), ("factored", K, float(s), C[:2], expect)
+            assert np.all(np.abs(Cu - expect) <= tol), ("unfactored", K, float(s), Cu[:2], expect)
+            assert np.all(np.abs(bound - expect) <= tol), ("bound", K, float(s))
+            if float(s) == 2.0 ** -7:  # every partial sum is exact
+                assert np.all(C == expect) and np.all(Cu == expect)
+
+
+def pin_one_hot_a(orc):
+    K, N = 100, 7  # KB = 4, last block holds rows 96..99
+    A0, W, S = workloads.make_random(K, N, seed=7)
+    W[99, 3] = -128
+    for k in (0, 1, 31, 32, 33, 63, 64, 95, 96, 98, 99):
+        A = np.zeros((1, K), np.float32)
+        A[0, k] = A0[0, k]
+        expect = np.array([float(A[0, k]) * int(W[k, n]) * float(S[k // 32, n]) for n in range(N)])
+        C, _ = orc.factored(A, W, S)
+        Cu = orc.unfactored(A, W, S)
+        assert np.array_equal(C, expect), ("factored", k, C, expect)
+        assert np.array_equal(Cu, expect), ("unfactored", k, Cu, expect)
+
+
+def pin_one_hot_w(orc):
+    K, N = 70, 9
+    A, _, S = workloads.make_random(K, N, seed=8)
+    for (k0, n0) in ((0, 0), (31, 8), (32, 4), (69, 2), (64, 0)):
+        W = np.zeros((K, N), np.int8)
+        W[k0, n0] = -128
+        C, _ = orc.factored(A, W, S)
+        Cu = orc.unfactored(A, W, S)
+        expect = np.zeros(N)
+        expect[n0] = float(A[0, k0]) * -128.0 * float(S[k0 // 32, n0])
+        assert np.array_equal(C, expect), ("factored", k0, n0, C, expect)
+        assert np.array_equal(Cu, expect), ("unfactored", k0, n0, Cu, expect)
+
+
+def pin_linearity_a(orc):
+    K, N = 97, 11
+    rng = _rng(9)
+    A1 = rng.integers(-8, 9, size=(1, K)).astype(np.float32)
+    A2 = rng.integers(-8, 9, size=(1, K)).astype(np.float32)
+    _, W, S = workloads.make_random(K, N, seed=10)
+    alpha, beta = 2.0, -3.0
+    A3 = (alpha * A1 + beta * A2).astype(np.float32)  # exact: small integers
+    C1, b1 = orc.factored(A1, W, S)
+    C2, b2 = orc.factored(A2, W, S)
+    C3, b3 = orc.factored(A3, W, S)
+    tol = 8 * K * EPS64 * (abs(alpha) * b1 + abs(beta) * b2 + b3) + 1e-300
+    assert np.all(np.abs(C3 - (alpha * C1 + beta * C2)) <= tol)
+    for fn in (orc.unfactored,):
+        D1, D2, D3 = fn(A1, W, S), fn(A2, W, S), fn(A3, W, S)
+        assert np.all(np.abs(D3 - (alpha * D1 + beta * D2)) <= tol)
+
+
+def pin_linearity_s_blocks(orc):
+    K, N = 100, 6  # blocks of 32, 32, 32 and 4 rows
+    A, W, S = workloads.make_random(K, N, seed=11)
+    C, bound = orc.factored(A, W, S)
+    total = np.zeros(N)
+    for b in range(workloads.num_blocks(K)):
+        Sb = np.zeros_like(S)
+        Sb[b] = S[b]
+        Cb, _ = orc.factored(A, W, Sb)
+        Cbu = orc.unfactored(A, W, Sb)
+        # only rows of block b may contribute
+        rows = slice(32 * b, min(K, 32 * b + 32))
+        expect = [sum(float(A[0, k]) * int(W[k, n]) for k in range(rows.start, rows.stop))
+                  * float(S[b, n]) for n in range(N)]
+        tol = 4 * 33 * EPS64 * bound + 1e-300
+        assert np.all(np.abs(Cb - expect) <= tol), ("block", b)
+        assert np.all(np.abs(Cbu - expect) <= tol), ("block unfactored", b)
+        # doubling one scale row doubles exactly that block's contribution
+        S2 = S.copy()
+        S2[b] *= np.float32(2.0)
+        C2, _ = orc.factored(A, W, S2)
+        assert np.all(np.abs((C2 - C) - Cb) <= 4 * K * EPS64 * 3 * bound + 1e-300), ("double", b)
+        total += Cb
+    assert np.all(np.abs(total - C) <= 4 * K * EPS64 * bound + 1e-300)
+
+
+def pin_integer_exact(orc):
+    for (K, N, seed) in ((100, 13, 12), (4100, 40, 13), (512, 200, 14)):
+        A, W, S = workloads.make_integer_exact(K, N, seed)
+        Ai = A.astype(np.int64).reshape(K)
+        Wi = W.astype(np.int64)
+        KB = workloads.num_blocks(K)
+        scale = float(S[0, 0])
+        blocks = np.stack([Ai[32 * b:32 * b + 32] @ Wi[32 * b:32 * b + 32] for b in range(KB)])
+        expect = blocks.sum(axis=0).astype(np.float64) * scale
+        C, _ = orc.factored(A, W, S)
+        Cu = orc.unfactored(A, W, S)
+        P = orc.block_sums(A, W)
+        assert np.array_equal(C, expect), ("factored", K, N)
+        assert np.array_equal(Cu, expect), ("unfactored", K, N)
+        assert np.array_equal(P, blocks.astype(np.float64)), ("block sums", K, N)
+
+
+def pin_factoring_identity(orc):
+    for (K, N, seed) in ((300, 40, 15), (4100, 17, 16)):
+        A, W, S = workloads.make_random(K, N, seed)
+        C, bound = orc.factored(A, W, S)
+        Cu = orc.unfactored(A, W, S)
+        assert np.all(np.abs(C - Cu) <= 1e-12 * bound), (K, N)
+
+
+def pin_block_sums(orc):
+    for (K, N, seed) in ((33, 4, 17), (70, 3, 18)):
+        A, W, _ = workloads.make_random(K, N, seed)
+        P = orc.block_sums(A, W)
+        KB = workloads.num_blocks(K)
+        assert P.shape == (KB, N)
+        for b in range(KB):
+            for n in range(N):
+                exact = sum(Fraction(float(A[0, k])) * int(W[k, n])
+                            for k in range(32 * b, min(K, 32 * b + 32)))
+                assert abs(P[b, n] - float(exact)) <= 4 * 33 * EPS64 * float(
+                    sum(abs(Fraction(float(A[0, k])) * int(W[k, n]))
+                        for k in range(32 * b, min(K, 32 * b + 32)))) + 1e-300, (K, b, n)
+
+
+def pin_empty(orc):
+    A = np.zeros((1, 0), np.float32)
+    W = np.zeros((0, 5), np.int8)
+    S = np.zeros((0, 5), np.float32)
+    C, bound = orc.factored(A, W, S)
+    assert np.array_equal(C, np.zeros(5)) and np.array_equal(bound, np.zeros(5))
+    assert np.array_equal(orc.unfactored(A, W, S), np.zeros(5))
+    A, W, S = workloads.make_random(40, 0, seed=19)
+    C, bound = orc.factored(A, W, S)
+    assert C.shape == (0,) and bound.shape == (0,)
+
+
+def read_scale_row_fixture():
+    """Rows ``K k b`` of the golden fixture: row k of W is scaled by S row b."""
+    rows = []
+    with open(os.path.join(GOLDEN, "scale_rows.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                K, k, b = (int(x) for x in line.split())
+                rows.append((K, k, b))
+    return rows
+
+
+def pin_scale_rows_golden(orc):
+    """One-hot A at row k picks exactly scale row b, as printed in the fixture."""
+    N = 3
+    for (K, k, b) in read_scale_row_fixture():
+        KB = workloads.num_blocks(K)
+        A = np.zeros((1, K), np.float32)
+        A[0, k] = 1.0
+        W = np.zeros((K, N), np.int8)
+        W[k, :] = 1
+        S = np.zeros((KB, N), np.float32)
+        S[b, :] = 1.0  # only the printed row is non-zero
+        C, _ = orc.factored(A, W, S)
+        Cu = orc.unfactored(A, W, S)
+        assert np.array_equal(C, np.ones(N)), ("factored", K, k, b, C)
+        assert np.array_equal(Cu, np.ones(N)), ("unfactored", K, k, b, Cu)
+
+
+ALL_PINS = [
+    pin_exact_rational,
+    pin_closed_form_ones,
+    pin_one_hot_a,
+    pin_one_hot_w,
+    pin_linearity_a,
+    pin_linearity_s_blocks,
+    pin_integer_exact,
+    pin_factoring_identity,
+    pin_block_sums,
+    pin_empty,
+    pin_scale_rows_golden,
+]

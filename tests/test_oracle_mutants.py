@@ -1,0 +1,59 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin.
+
+Every mutant below is a plausible slip (a dropped term, a wrong sign, a wrong
+index, a transposed operand, a dropped partial block, a missing absolute
+value, a missing initialisation).  The mistake is planted in a private copy
+of the C source, compiled on the CPU and run against the pin suite; all
+mutants keep every memory access inside the caller's arrays.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "q8mv_oracle.c")
+
+MUTANTS = {
+    "scale_row_mod": ("const float *s_row = S + (k / Q8MV_ORACLE_BLK) * N;",
+                      "const float *s_row = S + ((k % Q8MV_ORACLE_BLK) % ((K + 31) / 32)) * N;"),
+    "scale_row_64": ("const float *s_row = S + (k / Q8MV_ORACLE_BLK) * N;",
+                     "const float *s_row = S + (k / 64) * N;"),
+    "factored_prev_scale_row": ("const float *s_row = S + b * N;",
+                                "const float *s_row = S + (b > 0 ? b - 1 : 0) * N;"),
+    "drop_partial_block": ("return (K + Q8MV_ORACLE_BLK - 1) / Q8MV_ORACLE_BLK;",
+                           "return K / Q8MV_ORACLE_BLK;"),
+    "drop_first_row_of_block": ("for (int64_t k = k_begin; k < k_end; ++k) {\n            const double a = (double)A[k];\n            const int8_t *w_row = W + k * N;\n            for (int64_t n = 0; n < N; ++n) {\n                const double aw",
+                                "for (int64_t k = k_begin + 1; k < k_end; ++k) {\n            const double a = (double)A[k];\n            const int8_t *w_row = W + k * N;\n            for (int64_t n = 0; n < N; ++n) {\n                const double aw"),
+    "wrong_sign": ("C[n] += part[n] * s;", "C[n] -= part[n] * s;"),
+    "transposed_w_factored": ("const double aw = a * (double)w_row[n];",
+                              "const double aw = a * (double)W[n * K + k];"),
+    "transposed_w_unfactored": ("C[n] += a * (double)w_row[n] * (double)s_row[n];",
+                                "C[n] += a * (double)W[n * K + k] * (double)s_row[n];"),
+    "bound_without_abs": ("mag[n] += fabs(aw);", "mag[n] += aw;"),
+    "unsigned_bytes": ("const double aw = a * (double)w_row[n];",
+                       "const double aw = a * (double)(uint8_t)w_row[n];"),
+    "no_zero_init": ("        C[n] = 0.0;\n        if (bound) bound[n] = 0.0;",
+                     "        if (bound) bound[n] = 0.0;"),
+    "block_sums_missing_mask": ("        if (k_end > K) k_end = K;\n        for (int64_t k = k_begin; k < k_end; ++k) {\n            const double a = (double)A[k];\n            const int8_t *w_row = W + k * N;\n            for (int64_t n = 0; n < N; ++n) p_row[n] += a * (double)w_row[n];",
+                                "        if (k_end > K) k_end = K;\n        for (int64_t k = k_begin; k < k_end; ++k) {\n            const double a = (double)A[k];\n            const int8_t *w_row = W + k * N;\n            for (int64_t n = 0; n < N; ++n) p_row[n] += a * (double)w_row[n] * (k + 1 < k_end);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new, 1))
+    lib = oracle.build(str(mutated), str(tmp_path / "libmutant.so"), force=True)
+    orc = oracle.Oracle(lib)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, RuntimeError, ValueError) as e:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {name} passed every pin"
