@@ -1,0 +1,150 @@
+/*
+ * q8mv: Q8_0 decode matrix-vector product on one NVIDIA GB300 (sm_103a).
+ *
+ * Operation (Phobos docs, "Q8_0 matvec" example page, "The tensors" and
+ * "Factoring out the scale"):
+ *
+ *     C[0, n] = sum over blocks b of  S[b, n] * ( sum over k in block b of A[0, k] * W[k, n] )
+ *
+ * with blocks of 32 rows along K: block b holds rows 32*b .. 32*b+31 of W and
+ * is scaled by row b of S.  K need not be a multiple of 32 ("Bounds"): the
+ * last block then holds K - 32*(KB-1) rows and rows at or past K are never
+ * read.  N need not be a multiple of anything: columns at or past N are
+ * neither read nor written.
+ *
+ * Tensors (all contiguous, row-major, in device memory of the plan's GPU):
+ *     A  f32  [1, K]        activation row                         (4*K bytes)
+ *     W  i8   [K, N]        quantized weights, W[k, n] at k*N + n  (K*N bytes)
+ *     S  f32  [KB, N]       block scales, KB = ceil(K / 32),
+ *                           S[b, n] at b*N + n                     (4*KB*N bytes)
+ *     C  f32  [1, N]        output row, overwritten                (4*N bytes)
+ *
+ * Arithmetic: each weight byte is converted to f32 exactly (every value in
+ * -128 .. 127), each block's dot product is accumulated in f32 on the raw
+ * bytes, and the block's scale is applied once per block and column with a
+ * fused multiply-add into an f32 accumulator.  Summation order is fixed by
+ * the plan, so a plan gives bit-identical results run after run.
+ *
+ * Ownership: the caller owns A, W, S and C.  A plan owns a small device
+ * workspace (split-K partial sums and per-tile counters) that it allocates in
+ * q8mv_plan and frees in q8mv_destroy; q8mv_run never allocates.
+ *
+ * Concurrency: q8mv_run is asynchronous on the given stream.  Calls on one
+ * plan share its workspace, so they must be ordered (same stream, or
+ * otherwise serialised); use one plan per concurrent stream.
+ *
+ * Errors: every call returns a q8mv_status_t.  Arguments are validated on the
+ * host before anything is launched; q8mv_run reports launch-time errors only
+ * (it does not synchronise).  No kernel in this library waits on a flag, so
+ * none can hang.
+ */
+#ifndef Q8MV_H
+#define Q8MV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    Q8MV_OK = 0,
+    Q8MV_ERR_INVALID_ARG = 1,        /* null/misaligned/overlapping pointer, bad size, bad option */
+    Q8MV_ERR_UNSUPPORTED_DEVICE = 2, /* no device, or not an sm_103 GPU this library was built for */
+    Q8MV_ERR_OUT_OF_MEMORY = 3,      /* host or device allocation for the plan failed */
+    Q8MV_ERR_CUDA = 4                /* any other CUDA runtime error (see q8mv_last_cuda_error) */
+} q8mv_status_t;
+
+/* Kernel families a plan can pick. */
+enum {
+    Q8MV_KERNEL_AUTO = 0,
+    Q8MV_KERNEL_REGS = 1  /* weights streamed through registers with vector loads; any alignment */
+};
+
+/*
+ * Optional overrides for tuning sweeps and tests.  Zero means "let the plan
+ * choose".  An override that cannot apply to the shape gives INVALID_ARG.
+ */
+typedef struct {
+    int32_t kernel;    /* Q8MV_KERNEL_* */
+    int32_t vec_bytes; /* widest weight load per thread and row: 16, 8, 4, 2 or 1 */
+    int32_t threads_n; /* threads along N in one CTA: 32, 64, 128 or 256 */
+    int32_t split_k;   /* CTAs sharing one column tile along K (>= 1) */
+} q8mv_opts_t;
+
+/* What a plan chose, for the widest weight load the shape allows. */
+typedef struct {
+    int32_t kernel;           /* Q8MV_KERNEL_REGS */
+    int32_t vec_bytes;        /* weight bytes per thread per row */
+    int32_t threads_n;        /* threads along N per CTA */
+    int32_t groups_k;         /* thread groups along K per CTA (threads per CTA / threads_n) */
+    int32_t threads_per_cta;
+    int32_t split_k;          /* CTAs per column tile along K */
+    int32_t blocks_per_split; /* 32-row blocks each of those CTAs covers */
+    int64_t tile_n;           /* output columns per CTA */
+    int64_t grid_x;           /* column tiles */
+    int64_t grid_y;           /* = split_k */
+    int64_t workspace_bytes;  /* device workspace the plan owns */
+    int32_t sm_count;
+    int32_t ctas_per_sm;      /* resident CTAs per SM for the chosen kernel */
+} q8mv_plan_info_t;
+
+typedef struct q8mv_plan_s *q8mv_plan_t;
+
+/*
+ * Create a plan for C[1,N] = A[1,K] x (W[K,N], S[KB,N]) on `device`
+ * (-1 = the current device).  Queries the SM count, picks the kernel, tile
+ * and split, and allocates the workspace.  K >= 0, N >= 0, K < 2^31,
+ * N < 2^31 and K*N < 2^62; otherwise INVALID_ARG.  `opts` may be NULL.
+ * On success *out holds the plan; on failure *out is set to NULL.
+ * The calling thread's current device is left unchanged.
+ */
+q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device,
+                        const q8mv_opts_t *opts);
+
+/*
+ * Enqueue C = matvec(A, W, S) on `stream` (0 = the legacy default stream).
+ * The plan's device must be current.  A, S and C must be 4-byte aligned;
+ * W may have any alignment (narrower loads are used when W, S or N do not
+ * allow 16-byte ones).  C must not overlap A, W or S.  Null pointers are
+ * allowed only for tensors of zero size.  K == 0 writes C = 0; N == 0 is a
+ * no-op.  Returns after the launch; errors inside the kernel surface on the
+ * next synchronising call, as for any CUDA kernel.
+ */
+q8mv_status_t q8mv_run(q8mv_plan_t plan, const float *A, const int8_t *W, const float *S,
+                       float *C, cudaStream_t stream);
+
+/* Release the plan and its workspace.  NULL is accepted.  Synchronises the
+ * plan's device first so that no launch still uses the workspace. */
+q8mv_status_t q8mv_destroy(q8mv_plan_t plan);
+
+/* Fill *info with the plan's choices (for the widest legal weight load). */
+q8mv_status_t q8mv_plan_info(q8mv_plan_t plan, q8mv_plan_info_t *info);
+
+/*
+ * Host-only planning, no GPU needed: the configuration q8mv_plan would pick
+ * for K, N on a GPU with `sm_count` SMs, `ctas_per_sm` resident CTAs of the
+ * register kernel, and weight loads of `vec_bytes` (which must divide N).
+ * Used by tests of the planner; fills *info (workspace_bytes included).
+ */
+q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t ctas_per_sm,
+                                 int32_t vec_bytes, const q8mv_opts_t *opts,
+                                 q8mv_plan_info_t *info);
+
+/* Static, human-readable text for a status code. */
+const char *q8mv_status_string(q8mv_status_t status);
+
+/* The last CUDA runtime error code this library saw on the calling thread
+ * (0 if none), for diagnosing Q8MV_ERR_CUDA. */
+int q8mv_last_cuda_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int q8mv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q8MV_H */

@@ -1,0 +1,213 @@
+"""Q8_0 decode matvec on GB300: Python binding of the q8mv C library.
+
+    C[0, n] = sum_b S[b, n] * sum_{k in block b} A[0, k] * W[k, n]
+
+(Phobos docs, "Q8_0 matvec" example page, "The tensors".)  This module only
+marshals arguments: it checks dtypes, shapes and devices of torch tensors and
+passes raw device pointers and the current CUDA stream to ``libq8mv.so``.
+Every step of the computation runs in the library's CUDA kernels; if the
+library is missing, importing the binding raises instead of computing
+anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB, build_library  # noqa: F401  (build step for users)
+
+BLK = 32
+
+Q8MV_OK = 0
+Q8MV_ERR_INVALID_ARG = 1
+Q8MV_ERR_UNSUPPORTED_DEVICE = 2
+Q8MV_ERR_OUT_OF_MEMORY = 3
+Q8MV_ERR_CUDA = 4
+
+KERNEL_AUTO = 0
+KERNEL_REGS = 1
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
+                ("threads_n", ctypes.c_int32), ("split_k", ctypes.c_int32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
+                ("threads_n", ctypes.c_int32), ("groups_k", ctypes.c_int32),
+                ("threads_per_cta", ctypes.c_int32), ("split_k", ctypes.c_int32),
+                ("blocks_per_split", ctypes.c_int32),
+                ("tile_n", ctypes.c_int64), ("grid_x", ctypes.c_int64), ("grid_y", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64), ("sm_count", ctypes.c_int32),
+                ("ctas_per_sm", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class Q8mvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        text = _lib.q8mv_status_string(status).decode() if _lib is not None else str(status)
+        extra = ""
+        if status == Q8MV_ERR_CUDA:
+            extra = f" (cudaError {_lib.q8mv_last_cuda_error()})"
+        super().__init__(f"{what}: {text}{extra}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB):
+        raise ImportError(
+            f"{LIB} is missing: build it with `python -m q8_matrix_vector_gb300._build` "
+            "(the Q8_0 matvec has no implementation other than this CUDA library)")
+    lib = ctypes.CDLL(LIB)
+    i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    lib.q8mv_plan.argtypes = [ctypes.POINTER(p), i64, i64, ctypes.c_int, ctypes.POINTER(Opts)]
+    lib.q8mv_plan.restype = ctypes.c_int
+    lib.q8mv_run.argtypes = [p, p, p, p, p, p]
+    lib.q8mv_run.restype = ctypes.c_int
+    lib.q8mv_destroy.argtypes = [p]
+    lib.q8mv_destroy.restype = ctypes.c_int
+    lib.q8mv_plan_info.argtypes = [p, ctypes.POINTER(PlanInfo)]
+    lib.q8mv_plan_info.restype = ctypes.c_int
+    lib.q8mv_choose_config.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(Opts),
+                                       ctypes.POINTER(PlanInfo)]
+    lib.q8mv_choose_config.restype = ctypes.c_int
+    lib.q8mv_status_string.argtypes = [ctypes.c_int]
+    lib.q8mv_status_string.restype = ctypes.c_char_p
+    lib.q8mv_last_cuda_error.argtypes = []
+    lib.q8mv_last_cuda_error.restype = ctypes.c_int
+    lib.q8mv_version.argtypes = []
+    lib.q8mv_version.restype = ctypes.c_int
+    return lib
+
+
+_lib = _load()
+
+
+def library() -> ctypes.CDLL:
+    """The loaded ``libq8mv.so`` (for callers that use the C entry points directly)."""
+    return _lib
+
+
+def _opts(kernel=0, vec_bytes=0, threads_n=0, split_k=0):
+    if not (kernel or vec_bytes or threads_n or split_k):
+        return None
+    return Opts(kernel, vec_bytes, threads_n, split_k)
+
+
+def choose_config(K: int, N: int, sm_count: int, ctas_per_sm: int, vec_bytes: int, **opts) -> dict:
+    """Host-only planner: what a plan would pick on a GPU with ``sm_count`` SMs."""
+    info = PlanInfo()
+    o = _opts(**opts)
+    st = _lib.q8mv_choose_config(K, N, sm_count, ctas_per_sm, vec_bytes,
+                                 ctypes.byref(o) if o else None, ctypes.byref(info))
+    if st != Q8MV_OK:
+        raise Q8mvError(st, "q8mv_choose_config")
+    return info.as_dict()
+
+
+def num_blocks(K: int) -> int:
+    return (K + BLK - 1) // BLK
+
+
+class Plan:
+    """A q8mv plan for fixed (K, N) on one device; owns the split-K workspace."""
+
+    def __init__(self, K: int, N: int, device: int = -1, **opts):
+        self.K, self.N, self.KB = int(K), int(N), num_blocks(int(K))
+        handle = ctypes.c_void_p()
+        o = _opts(**opts)
+        st = _lib.q8mv_plan(ctypes.byref(handle), self.K, self.N, int(device),
+                            ctypes.byref(o) if o else None)
+        if st != Q8MV_OK:
+            raise Q8mvError(st, f"q8mv_plan(K={K}, N={N})")
+        self._h = handle
+        info = PlanInfo()
+        st = _lib.q8mv_plan_info(self._h, ctypes.byref(info))
+        if st != Q8MV_OK:
+            raise Q8mvError(st, "q8mv_plan_info")
+        self.info = info.as_dict()
+
+    @property
+    def handle(self) -> int:
+        return self._h.value
+
+    def run_ptr(self, A: int, W: int, S: int, C: int, stream: int = 0) -> None:
+        """Enqueue the matvec on raw device pointers (integers) and a raw stream."""
+        st = _lib.q8mv_run(self._h, A, W, S, C, stream)
+        if st != Q8MV_OK:
+            raise Q8mvError(st, "q8mv_run")
+
+    def __call__(self, A, W, S, out=None, stream=None):
+        """C = matvec(A, W, S) on torch CUDA tensors, enqueued on the current stream."""
+        import torch
+
+        _check(A, torch.float32, (1, self.K), "A")
+        _check(W, torch.int8, (self.K, self.N), "W")
+        _check(S, torch.float32, (self.KB, self.N), "S")
+        dev = W.device
+        for name, t in (("A", A), ("S", S)):
+            if t.device != dev:
+                raise ValueError(f"{name} is on {t.device}, W is on {dev}")
+        if out is None:
+            out = torch.empty((1, self.N), dtype=torch.float32, device=dev)
+        else:
+            _check(out, torch.float32, (1, self.N), "out")
+            if out.device != dev:
+                raise ValueError(f"out is on {out.device}, W is on {dev}")
+        if stream is None:
+            stream = torch.cuda.current_stream(dev)
+        with torch.cuda.device(dev):
+            self.run_ptr(A.data_ptr(), W.data_ptr(), S.data_ptr(), out.data_ptr(), stream.cuda_stream)
+        return out
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            st = _lib.q8mv_destroy(self._h)
+            self._h = ctypes.c_void_p()
+            if st != Q8MV_OK:
+                raise Q8mvError(st, "q8mv_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _check(t, dtype, shape, name):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape) and not (name == "A" and t.dim() == 1 and t.numel() == shape[1]) \
+            and not (name == "out" and t.dim() == 1 and t.numel() == shape[1]):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+_plans: dict = {}
+
+
+def matvec(A, W, S, out=None):
+    """C[1, N] = Q8_0 matvec of A [1, K] f32 with W [K, N] int8 and S [KB, N] f32.
+
+    Plans are cached per (K, N, device).  Runs on the current CUDA stream.
+    """
+    K, N = W.shape
+    key = (int(K), int(N), W.device.index)
+    plan = _plans.get(key)
+    if plan is None:
+        plan = _plans[key] = Plan(K, N, device=W.device.index)
+    return plan(A, W, S, out=out)
+
+
+def version() -> int:
+    return _lib.q8mv_version()

@@ -1,0 +1,160 @@
+"""Host-side checks of the C boundary: no GPU, no kernel launches."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q8mv.h")
+
+
+@pytest.fixture(scope="session")
+def q8():
+    import __graft_entry__
+
+    __graft_entry__._load_build_module().build_library()
+    import q8_matrix_vector_gb300 as q8mv
+
+    return q8mv
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q8mv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for required in ("q8mv_plan", "q8mv_run", "q8mv_destroy", "q8mv_plan_info", "q8mv_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(q8):
+    out = subprocess.run(["nm", "-D", "--defined-only", q8.LIB], check=True, capture_output=True, text=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    lib = q8.library()
+    for n in declared_functions():
+        assert getattr(lib, n) is not None
+
+
+def test_library_exports_nothing_undeclared(q8):
+    out = subprocess.run(["nm", "-D", "--defined-only", q8.LIB], check=True, capture_output=True, text=True).stdout
+    ours = sorted(s for s in (line.split()[-1] for line in out.splitlines() if line.strip())
+                  if s.startswith("q8mv_"))
+    assert ours == declared_functions()
+
+
+def test_status_strings(q8):
+    lib = q8.library()
+    seen = set()
+    for s in range(5):
+        text = lib.q8mv_status_string(s).decode()
+        assert text and text not in seen
+        seen.add(text)
+    assert lib.q8mv_status_string(99).decode() == "unknown status"
+    assert q8.version() >= 100
+
+
+def test_plan_rejects_bad_sizes_before_touching_a_device(q8):
+    lib = q8.library()
+    h = ctypes.c_void_p(1234)
+    assert lib.q8mv_plan(ctypes.byref(h), -1, 10, -1, None) == q8.Q8MV_ERR_INVALID_ARG
+    assert h.value is None
+    assert lib.q8mv_plan(ctypes.byref(h), 10, -1, -1, None) == q8.Q8MV_ERR_INVALID_ARG
+    assert lib.q8mv_plan(ctypes.byref(h), 1 << 31, 10, -1, None) == q8.Q8MV_ERR_INVALID_ARG
+    assert lib.q8mv_plan(None, 10, 10, -1, None) == q8.Q8MV_ERR_INVALID_ARG
+    bad = q8.Opts(0, 3, 0, 0)  # 3-byte loads do not exist
+    assert lib.q8mv_plan(ctypes.byref(h), 10, 12, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+    bad = q8.Opts(0, 0, 48, 0)
+    assert lib.q8mv_plan(ctypes.byref(h), 10, 12, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+    bad = q8.Opts(7, 0, 0, 0)
+    assert lib.q8mv_plan(ctypes.byref(h), 10, 12, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+
+
+def test_run_and_info_reject_null_plan(q8):
+    lib = q8.library()
+    assert lib.q8mv_run(None, None, None, None, None, None) == q8.Q8MV_ERR_INVALID_ARG
+    info = q8.PlanInfo()
+    assert lib.q8mv_plan_info(None, ctypes.byref(info)) == q8.Q8MV_ERR_INVALID_ARG
+    assert lib.q8mv_destroy(None) == q8.Q8MV_OK
+
+
+def test_plan_without_gpu_reports_unsupported_device(q8):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    lib = q8.library()
+    h = ctypes.c_void_p()
+    st = lib.q8mv_plan(ctypes.byref(h), 64, 64, -1, None)
+    assert st in (q8.Q8MV_ERR_UNSUPPORTED_DEVICE, q8.Q8MV_ERR_CUDA)
+    assert h.value is None
+
+
+def test_missing_library_fails_loudly(q8, monkeypatch):
+    monkeypatch.setattr(q8, "LIB", os.path.join(ROOT, "does-not-exist", "libq8mv.so"))
+    with pytest.raises(ImportError):
+        q8._load()
+
+
+# ----------------------------------------------------------------------------
+# planner (pure host function)
+# ----------------------------------------------------------------------------
+SHAPES = [(512, 200), (4096, 4096), (4096, 11008), (11008, 4096), (8192, 28672), (4100, 128256),
+          (1, 1), (33, 17), (0, 64), (64, 0), (100000, 16)]
+
+
+def legal_vecs(N):
+    return [v for v in (16, 8, 4, 2, 1) if N == 0 or N % v == 0]
+
+
+@pytest.mark.parametrize("K,N", SHAPES)
+def test_planner_covers_every_column_and_block(q8, K, N):
+    KB = (K + 31) // 32
+    for sms in (148, 152, 160):
+        for vec in legal_vecs(N):
+            c = q8.choose_config(K, N, sms, 1, vec)
+            assert c["vec_bytes"] == vec
+            assert c["threads_n"] * c["groups_k"] == c["threads_per_cta"] == 256
+            assert c["tile_n"] == c["threads_n"] * vec
+            assert c["grid_x"] * c["tile_n"] >= N
+            assert (c["grid_x"] - 1) * c["tile_n"] < max(N, 1)
+            assert c["grid_y"] == c["split_k"] >= 1
+            if KB:
+                # the splits cover every block exactly once
+                assert c["split_k"] * c["blocks_per_split"] >= KB
+                assert (c["split_k"] - 1) * c["blocks_per_split"] < KB
+            assert c["split_k"] <= 65535
+            if c["split_k"] > 1:
+                assert c["workspace_bytes"] == 4 * c["split_k"] * N
+            else:
+                assert c["workspace_bytes"] == 0
+
+
+def test_planner_fills_the_gpu_for_the_attention_projection(q8):
+    # 4096 x 4096 has only 8 tiles of 512 columns: split-K must spread it over the SMs
+    c = q8.choose_config(4096, 4096, 152, 1, 16)
+    assert c["grid_x"] * c["grid_y"] >= 128
+    assert c["split_k"] > 1
+
+
+def test_planner_honours_overrides(q8):
+    c = q8.choose_config(4096, 4096, 152, 1, 16, threads_n=128, split_k=4)
+    assert c["threads_n"] == 128 and c["split_k"] == 4 and c["blocks_per_split"] == 32
+    # a split larger than the number of blocks is clamped to one block per split
+    c = q8.choose_config(64, 4096, 152, 1, 16, split_k=9)
+    assert c["split_k"] == 2 and c["blocks_per_split"] == 1
+
+
+def test_planner_rejects_illegal_requests(q8):
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config(64, 200, 152, 1, 16)  # 16 does not divide 200
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config(64, 256, 0, 1, 16)
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config(64, 256, 152, 1, 16, threads_n=96)
