@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the Q8_0 decode matvec on GB300.
+
+One step is one call of the whole path, C = matvec(A, W, S), on the 7B-class
+attention projection (K = 4096, N = 4096) unless ``--workload`` says
+otherwise.  The timed region replays CUDA graphs of back-to-back calls that
+rotate over enough distinct copies of the inputs to exceed twice the L2, so
+every call streams its weights from HBM.
+
+Printed (rank 0, one JSON line): effective HBM GB/s over the algorithmic
+bytes K*N + 4*KB*N + 4*K + 4*N per call, microseconds per call, the roofline
+of the kernel against the measured HBM copy bandwidth, the fp64 CPU oracle
+timed on the host cores, an end-to-end figure with host buffers, the SM
+clocks seen during the timed region and the number of kernel launches.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload attn]
+    python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+With N > 1 (under torchrun) every rank runs an independent replica on its own
+GPU: the matvec has no exchange step, so there is no collective on the data
+path; the process group only provides the barrier and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "Q8_0 matvec effective HBM GB/s and % of GB300 peak; µs per call"
+UNIT = "GB/s"
+KERNEL_SRC = os.path.join(ROOT, "q8_matrix_vector_gb300", "csrc", "q8mv.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+GRAPH_CALLS = 1000  # calls captured per CUDA graph (rounded to the rotation length)
+CPU_BASELINE_SECONDS = 10.0
+
+
+# ----------------------------------------------------------------------------
+# process group (replicas only: barrier and max/sum over ranks)
+# ----------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return rank, local_rank, world
+
+
+def init_group(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(group):
+    if group is not None:
+        group.barrier()
+
+
+def reduce_over_ranks(group, value: float, op: str, device=None) -> float:
+    """max or sum of a float over all ranks (the identity with one rank)."""
+    if group is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    group.all_reduce(t, op=group.ReduceOp.MAX if op == "max" else group.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# peaks, clocks, profile data
+# ----------------------------------------------------------------------------
+def read_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel is unchanged."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get("workloads", {}).get(workload)
+    if not entry or rec.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs."""
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(CLOCK_FIELDS)}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # let it start before the timed region
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        return parse_clock_samples(out)
+
+
+def parse_clock_samples(text: str):
+    sm, sm_max, power = [], [], []
+    reasons = set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in text.splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) != len(CLOCK_FIELDS):
+            continue
+        try:
+            sm.append(float(parts[1]))
+            sm_max.append(float(parts[2]))
+            power.append(float(parts[3]))
+        except ValueError:
+            continue
+        for name, val in zip(names, parts[5:9]):
+            if val.lower().startswith("active"):
+                reasons.add(name)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(sm_max), "samples": len(sm),
+            "power_w_max": max(power), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, rank, local_rank, world):
+    import torch
+
+    import q8_matrix_vector_gb300 as q8mv
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for the q8mv arm")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    group = init_group(world, "nccl")
+    wl = workloads.WORKLOADS[args.workload]
+    K, N, KB = wl.K, wl.N, wl.KB
+    bytes_per_call = wl.algorithmic_bytes()
+
+    A, W, S = workloads.make_inputs(wl)
+    plan = q8mv.Plan(K, N, device=local_rank)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0)) or 126 * 1024 * 1024
+    # distinct copies so that a copy is reused only after > 2 x L2 of other traffic
+    copies = max(2, math.ceil(2 * l2 / bytes_per_call) + 1)
+    Ah, Wh, Sh = torch.from_numpy(A), torch.from_numpy(W), torch.from_numpy(S)
+    bufs = []
+    for _ in range(copies):
+        bufs.append((Ah.to(dev), Wh.to(dev), Sh.to(dev), torch.empty((1, N), dtype=torch.float32, device=dev)))
+    ptrs = [(a.data_ptr(), w.data_ptr(), s.data_ptr(), c.data_ptr()) for a, w, s, c in bufs]
+    stream = torch.cuda.Stream(dev)
+
+    # warm-up steps (eager launches through the C library)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            plan.run_ptr(*ptrs[i % copies], stream.cuda_stream)
+    stream.synchronize()
+
+    # graphs of back-to-back calls; the rotation restarts at copy 0 in each graph
+    chunk = max(copies, (min(GRAPH_CALLS, max(args.steps, 1)) // copies) * copies)
+    full, rest = divmod(args.steps, chunk)
+
+    def capture(ncalls):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            s = torch.cuda.current_stream().cuda_stream
+            for i in range(ncalls):
+                plan.run_ptr(*ptrs[i % copies], s)
+        return g
+
+    g_full = capture(chunk) if full else None
+    g_rest = capture(rest) if rest else None
+    with torch.cuda.stream(stream):  # one untimed replay uploads the graphs
+        if g_full:
+            g_full.replay()
+        if g_rest:
+            g_rest.replay()
+    stream.synchronize()
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(group)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local_rank)
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rest:
+            g_rest.replay()
+        end.record(stream)
+    end.synchronize()
+    wall = time.perf_counter() - wall0
+    torch.cuda.synchronize(dev)
+    barrier(group)
+    clocks = sampler.stop()
+    ms = start.elapsed_time(end)
+    ms_max = reduce_over_ranks(group, ms, "max", dev)
+    total_bytes = reduce_over_ranks(group, float(bytes_per_call) * args.steps, "sum", dev)
+    value = total_bytes / (ms_max * 1e-3) / 1e9 if ms_max > 0 else 0.0
+
+    # roofline of the one kernel each call launches
+    per_launch_s = ms * 1e-3 / max(args.steps, 1)
+    achieved = bytes_per_call / per_launch_s / 1e9 if per_launch_s > 0 else 0.0
+    peak, peak_kind = read_hbm_peak()
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} copy bandwidth",
+                "traffic": recorded_traffic(args.workload),
+                "algorithmic_bytes_per_launch": bytes_per_call}
+
+    # end to end through the public binding: pinned host inputs in, result out
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    Ap, Wp, Sp = Ah.pin_memory(), Wh.pin_memory(), Sh.pin_memory()
+    Cp = torch.empty((1, N), dtype=torch.float32).pin_memory()
+    Ad, Wd, Sd, Cd = bufs[0]
+    with torch.cuda.stream(stream):
+        for _ in range(2):  # warm-up
+            Ad.copy_(Ap, non_blocking=True)
+            Wd.copy_(Wp, non_blocking=True)
+            Sd.copy_(Sp, non_blocking=True)
+            plan(Ad, Wd, Sd, out=Cd, stream=stream)
+            Cp.copy_(Cd, non_blocking=True)
+    stream.synchronize()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    barrier(group)
+    with torch.cuda.stream(stream):
+        e_start.record(stream)
+        for _ in range(e2e_steps):
+            Ad.copy_(Ap, non_blocking=True)
+            Wd.copy_(Wp, non_blocking=True)
+            Sd.copy_(Sp, non_blocking=True)
+            plan(Ad, Wd, Sd, out=Cd, stream=stream)
+            Cp.copy_(Cd, non_blocking=True)
+        e_end.record(stream)
+    e_end.synchronize()
+    e_ms = reduce_over_ranks(group, e_start.elapsed_time(e_end), "max", dev)
+    e_bytes = reduce_over_ranks(group, float(bytes_per_call) * e2e_steps, "sum", dev)
+    h2d = 4 * K + K * N + 4 * KB * N
+    e2e = {"value": round(e_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * N, "steps": e2e_steps,
+           "what": "pinned host A, W, S copied in, q8mv_run, C copied out, every step"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(A, W, S, bytes_per_call, args.cpu_seconds, wl)
+
+    if rank != 0:
+        return None
+    info = plan.info
+    us = ms * 1e3 / max(args.steps, 1)
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / max(args.steps, 1), 6),
+        "us_per_call": round(us, 3), "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {wl.description}", "K": K, "N": N, "KB": KB,
+                   "weights": "Q8_0: int8 W [K,N], f32 scales [KB,N], f32 A and C",
+                   "bytes_per_call": bytes_per_call,
+                   "l2": f"inputs larger than L2: {copies} rotating input copies "
+                         f"({copies * bytes_per_call / 1e6:.0f} MB) vs {l2 / 1e6:.0f} MB L2",
+                   "timing": f"CUDA events around graph replays of {chunk} back-to-back calls",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "plan": {k: info[k] for k in ("kernel", "vec_bytes", "threads_n", "groups_k", "split_k",
+                                                 "blocks_per_split", "grid_x", "grid_y", "ctas_per_sm")}},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "wall_s_timed_region": round(wall, 4),
+    }
+
+
+def cpu_baseline(A, W, S, bytes_per_call, seconds, wl):
+    """The fp64 oracle, as it stands, on the host cores: full calls for ~seconds."""
+    import oracle
+
+    orc = oracle.load()
+    orc.factored(A, W, S)  # page in
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        orc.factored(A, W, S)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return {"value": round(reps * bytes_per_call / dt / 1e9, 4), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{reps} full {wl.name} calls (K={wl.K}, N={wl.N}) in {dt:.1f} s, single thread, fp64"}
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the CPU oracle on the same workload and metric
+# ----------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    import numpy as np
+
+    import oracle
+
+    if rank != 0:
+        return None  # rank 0 alone runs the reference arm
+    wl = workloads.WORKLOADS[args.workload]
+    A, W, S = workloads.make_inputs(wl)
+    orc = oracle.load()
+    t0 = time.perf_counter()
+    orc.factored(A, W, S)
+    t_full = time.perf_counter() - t0
+    # each step is a bounded sample of the workload: the first n_s columns
+    budget = args.reference_seconds
+    total_steps = args.steps + args.warmup
+    n_s = wl.N
+    if total_steps * t_full > budget:
+        n_s = max(1, int(wl.N * budget / (total_steps * t_full)))
+    Ws = np.ascontiguousarray(W[:, :n_s])
+    Ss = np.ascontiguousarray(S[:, :n_s])
+    step_bytes = wl.K * n_s + 4 * wl.KB * n_s + 4 * wl.K + 4 * n_s
+    for _ in range(args.warmup):
+        orc.factored(A, Ws, Ss)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.factored(A, Ws, Ss)
+    dt = time.perf_counter() - t0
+    value = args.steps * step_bytes / dt / 1e9 if dt > 0 else 0.0
+    sample = (f"first {n_s} of {wl.N} columns of {wl.name} (K={wl.K}) per step, "
+              f"fp64 oracle, single thread")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / max(args.steps, 1), 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.name}: {wl.description}", "K": wl.K, "N": wl.N, "KB": wl.KB},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=workloads.HEADLINE)
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=CPU_BASELINE_SECONDS)
+    ap.add_argument("--reference-seconds", type=float, default=60.0,
+                    help="CPU budget of the reference arm's timed steps")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, local_rank, world = dist_env()
+    if world != args.gpus and args.gpus != 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, local_rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
