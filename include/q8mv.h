@@ -54,7 +54,9 @@ typedef enum {
     Q8MV_ERR_INVALID_ARG = 1,        /* null/misaligned/overlapping pointer, bad size, bad option */
     Q8MV_ERR_UNSUPPORTED_DEVICE = 2, /* no device, or not an sm_103 GPU this library was built for */
     Q8MV_ERR_OUT_OF_MEMORY = 3,      /* host or device allocation for the plan failed */
-    Q8MV_ERR_CUDA = 4                /* any other CUDA runtime error (see q8mv_last_cuda_error) */
+    Q8MV_ERR_CUDA = 4,               /* any other CUDA runtime error (see q8mv_last_cuda_error) */
+    Q8MV_ERR_SCRATCH_TOO_SMALL = 5   /* q8mv_run_noalloc: the shape needs more split-K scratch than
+                                        Q8MV_NOALLOC_SCRATCH_BYTES */
 } q8mv_status_t;
 
 /* Kernel families a plan can pick. */
@@ -142,6 +144,46 @@ int q8mv_last_cuda_error(void);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int q8mv_version(void);
+
+/*
+ * Allocation-free matvec.  The pages have no counterpart to this call: it
+ * exists only for callers that cannot allocate device memory and therefore
+ * cannot own a plan.  Examples are an engine that reserves the GPU's memory for
+ * its own pool at start-up (a cudaMalloc would fail, or bypass the pool's
+ * accounting), code on a latency-critical path that must not call cudaMalloc
+ * (it can synchronise the device and its latency is unbounded), and plug-in
+ * hosts that let an extension enqueue work on a given stream but not create
+ * resources.
+ *
+ * It computes exactly what q8mv_run computes with a default plan for (K, N)
+ * on the current device: same kernel, same tile and split, same summation
+ * order.  The split-K partial sums and counters live in one static device
+ * array of Q8MV_NOALLOC_SCRATCH_BYTES bytes inside this library (4 MiB, held
+ * by every GPU that loads the library until the process exits) instead of a
+ * plan's workspace.
+ *
+ *   - Arguments, alignment and overlap rules are those of q8mv_run; the current
+ *     device is used.
+ *   - Returns Q8MV_ERR_SCRATCH_TOO_SMALL, before launching anything, when the
+ *     split the planner picks needs more than that scratch: split_k * N floats
+ *     of partial sums beyond the first 64 KiB, or more than 16384 column tiles
+ *     of counters.  The 7B- and 70B-class projections and a 128256-row LM head
+ *     all fit.
+ *   - The first call on each device looks up the scratch array's device
+ *     address and the device's SM count and occupancy; make that first call
+ *     before any stream capture begins on that device.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.  Each
+ *     call clears the counters it uses with cudaMemsetAsync on `stream` before
+ *     its kernel, so a call never depends on what an earlier call left behind.
+ *   - All calls on a device share the one scratch array, and it keeps the last
+ *     call's contents.  Calls whose kernels may overlap on the GPU (other
+ *     streams, other host threads) race on it: order them, for example by
+ *     issuing them on one stream.
+ */
+#define Q8MV_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+q8mv_status_t q8mv_run_noalloc(int64_t K, int64_t N, const float *A, const int8_t *W,
+                               const float *S, float *C, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

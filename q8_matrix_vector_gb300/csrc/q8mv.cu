@@ -33,6 +33,8 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <functional>
+#include <mutex>
 #include <new>
 
 namespace {
@@ -443,6 +445,8 @@ const char *q8mv_status_string(q8mv_status_t s) {
         case Q8MV_ERR_UNSUPPORTED_DEVICE: return "unsupported or missing device (needs sm_103)";
         case Q8MV_ERR_OUT_OF_MEMORY: return "out of memory";
         case Q8MV_ERR_CUDA: return "CUDA runtime error";
+        case Q8MV_ERR_SCRATCH_TOO_SMALL:
+            return "shape needs more split-K scratch than the allocation-free entry point holds";
     }
     return "unknown status";
 }
@@ -646,3 +650,140 @@ q8mv_status_t q8mv_destroy(q8mv_plan_t p) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point
+//
+// For callers that cannot allocate device memory (and so cannot own a plan):
+// the register kernel's split-K scratch lives in one static device array of
+// this library instead of a plan's workspace.  Layout of the array:
+//   [0, 64 KiB)        one u32 arrival counter per column tile
+//   [64 KiB, 4 MiB)    split_k x N f32 partial sums
+// The host never dereferences the array's name: it is a host-side stand-in
+// for the symbol, so the device address is looked up with
+// cudaGetSymbolAddress, once per device, with that device current.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoallocBytes = Q8MV_NOALLOC_SCRATCH_BYTES;
+constexpr size_t kNoallocCounterBytes = 64 * 1024;
+constexpr int kNoallocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
+
+struct NoallocDevice {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    bool supported = false;
+    unsigned char *scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int sm_count = 0;
+    int cps = 1;
+};
+
+NoallocDevice g_noalloc_devices[kNoallocMaxDevices];
+
+// Set-up for one device (must be current): the scratch address, and the SM
+// count and occupancy the planner needs, queried the same way q8mv_plan does.
+void noalloc_setup(NoallocDevice &d, int device) {
+    int major = 0, minor = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) {
+        d.err = e;
+        return;
+    }
+    d.supported = (major == 10 && minor == 3);
+    if (!d.supported) return;
+    void *addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+    if (e != cudaSuccess || addr == nullptr) {
+        d.err = (e != cudaSuccess) ? e : cudaErrorInvalidSymbol;
+        return;
+    }
+    d.scratch = static_cast<unsigned char *>(addr);
+    int cps = 1;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cps, q8mv_regs_kernel<16, true>, kCtaThreads,
+                                                      static_cast<size_t>(16384));
+    if (e != cudaSuccess) {
+        d.err = e;
+        return;
+    }
+    d.cps = std::max(1, cps);
+}
+
+}  // namespace
+
+extern "C" q8mv_status_t q8mv_run_noalloc(int64_t K, int64_t N, const float *A, const int8_t *W,
+                                          const float *S, float *C, cudaStream_t stream) {
+    if (K < 0 || N < 0 || K >= (1LL << 31) || N >= (1LL << 31)) return Q8MV_ERR_INVALID_ARG;
+    if (N > 0 && K > ((1LL << 62) / N)) return Q8MV_ERR_INVALID_ARG;
+    if (N == 0) return Q8MV_OK;
+    if (C == nullptr || (reinterpret_cast<uintptr_t>(C) & 3u)) return Q8MV_ERR_INVALID_ARG;
+
+    int dev = -1;
+    q8mv_status_t st = cuda_status(cudaGetDevice(&dev));
+    if (st != Q8MV_OK) return st;
+    if (dev < 0 || dev >= kNoallocMaxDevices) return Q8MV_ERR_UNSUPPORTED_DEVICE;
+    NoallocDevice &d = g_noalloc_devices[dev];
+    std::call_once(d.once, noalloc_setup, std::ref(d), dev);
+    if (d.err != cudaSuccess) return cuda_status(d.err);
+    if (!d.supported) return Q8MV_ERR_UNSUPPORTED_DEVICE;
+
+    if (K == 0) return cuda_status(cudaMemsetAsync(C, 0, static_cast<size_t>(N) * sizeof(float), stream));
+    if (A == nullptr || W == nullptr || S == nullptr) return Q8MV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(S) & 3u))
+        return Q8MV_ERR_INVALID_ARG;
+    const int64_t KB = ceil_div(K, kBlk);
+    const int64_t c_bytes = 4 * N;
+    if (overlaps(C, c_bytes, A, 4 * K) || overlaps(C, c_bytes, W, K * N) || overlaps(C, c_bytes, S, 4 * KB * N))
+        return Q8MV_ERR_INVALID_ARG;
+
+    // the widest weight load N and W's address allow, as q8mv_run picks it
+    const uintptr_t waddr = reinterpret_cast<uintptr_t>(W);
+    int vec = 1;
+    for (int i = 0; i < 5; ++i) {
+        if (N % kVecs[i] == 0 && waddr % static_cast<uintptr_t>(kVecs[i]) == 0) {
+            vec = kVecs[i];
+            break;
+        }
+    }
+    Config c;
+    st = choose(K, N, d.sm_count, d.cps, vec, nullptr, &c);
+    if (st != Q8MV_OK) return st;
+
+    float *ws = nullptr;
+    unsigned *tickets = nullptr;
+    if (c.split > 1) {
+        const size_t counter_bytes = static_cast<size_t>(c.tiles) * sizeof(unsigned);
+        const size_t partial_bytes = static_cast<size_t>(c.split) * static_cast<size_t>(N) * sizeof(float);
+        if (counter_bytes > kNoallocCounterBytes || partial_bytes > kNoallocBytes - kNoallocCounterBytes)
+            return Q8MV_ERR_SCRATCH_TOO_SMALL;
+        tickets = reinterpret_cast<unsigned *>(d.scratch);
+        ws = reinterpret_cast<float *>(d.scratch + kNoallocCounterBytes);
+        // the counters must start at zero; clear them on this call's stream
+        st = cuda_status(cudaMemsetAsync(tickets, 0, counter_bytes, stream));
+        if (st != Q8MV_OK) return st;
+    }
+
+    const uintptr_t saddr = reinterpret_cast<uintptr_t>(S);
+    const bool svec = (c.vec >= 4 && saddr % 16 == 0) || (c.vec == 2 && saddr % 8 == 0);
+    Params prm;
+    prm.A = A;
+    prm.W = W;
+    prm.S = S;
+    prm.C = C;
+    prm.ws = ws;
+    prm.tickets = tickets;
+    prm.K = K;
+    prm.N = N;
+    prm.KB = static_cast<int>(KB);
+    prm.tn = c.tn;
+    prm.tn_log2 = log2_pow2(c.tn);
+    prm.gk = c.gk;
+    prm.split = c.split;
+    prm.bps = c.bps;
+    const dim3 grid(static_cast<unsigned>(c.tiles), static_cast<unsigned>(c.split));
+    kernel_for(c.vec, svec)<<<grid, kCtaThreads, smem_bytes(c), stream>>>(prm);
+    return cuda_status(cudaGetLastError());
+}

@@ -1,0 +1,116 @@
+"""The allocation-free entry point, q8mv_run_noalloc, called through the C ABI.
+
+Some callers cannot allocate device memory (an engine whose memory pool owns
+the GPU, a latency-critical path that must not call cudaMalloc, a plug-in host
+that only hands out a stream), so they cannot own a plan and its workspace.
+q8mv_run_noalloc serves them with a static scratch array inside the library.
+These tests check that it agrees with the plan-based entry point, call after
+call, and that it refuses shapes whose split-K scratch would not fit.
+
+This file is collected last on purpose: if it fails, a run that stops at the
+first failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import workloads
+from gpu_util import assert_close
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 4 * 1024 * 1024
+COUNTER_BYTES = 64 * 1024
+ERR_SCRATCH_TOO_SMALL = 5
+
+
+@pytest.fixture(scope="module")
+def q8():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import q8_matrix_vector_gb300 as q8mv
+
+    lib = q8mv.library()
+    p, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.q8mv_run_noalloc.argtypes = [i64, i64, p, p, p, p, p]
+    lib.q8mv_run_noalloc.restype = ctypes.c_int
+    return q8mv
+
+
+def run_noalloc(q8, A, W, S, C):
+    import torch
+
+    K, N = W.shape
+    stream = torch.cuda.current_stream().cuda_stream
+    return q8.library().q8mv_run_noalloc(K, N, A.data_ptr(), W.data_ptr(), S.data_ptr(), C.data_ptr(), stream)
+
+
+@pytest.mark.parametrize("name,w_offset", [("attn", 0), ("tiny", 0), ("lm_head", 0), ("ffn_down", 3)])
+def test_noalloc_matches_plan_entry_point_twice(q8, orc, name, w_offset):
+    import torch
+
+    A, W, S = workloads.make_inputs(name)
+    K, N = W.shape
+    dev = torch.device("cuda")
+    Ad = torch.from_numpy(A).to(dev)
+    wbuf = torch.empty(K * N + w_offset, dtype=torch.int8, device=dev)
+    Wd = wbuf[w_offset:].view(K, N)
+    Wd.copy_(torch.from_numpy(W))
+    Sd = torch.from_numpy(S).to(dev)
+
+    plan = q8.Plan(K, N)
+    C_plan = plan(Ad, Wd, Sd)
+    torch.cuda.synchronize()
+    ref_plan = C_plan.cpu().numpy().reshape(N).astype(np.float64)
+    _, bound = orc.factored(A, W, S)
+
+    # two calls in a row share the static scratch; both must match
+    for call in range(2):
+        C = torch.full((1, N), float("nan"), device=dev)
+        st = run_noalloc(q8, Ad, Wd, Sd, C)
+        assert st == 0, q8.library().q8mv_status_string(st)
+        torch.cuda.synchronize()
+        got = C.cpu().numpy().reshape(N).astype(np.float64)
+        assert_close(got, ref_plan, bound, f"{name} call {call}")
+    plan.close()
+
+
+def test_noalloc_rejects_a_shape_whose_scratch_does_not_fit(q8):
+    import torch
+
+    # the planner's choice for this shape needs more partial sums than the
+    # static array holds; buffers are real and full-size all the same
+    K, N = 16384, 131072
+    probe = q8.Plan(64, 64)
+    cfg = q8.choose_config(K, N, probe.info["sm_count"], probe.info["ctas_per_sm"], 16)
+    probe.close()
+    assert cfg["split_k"] > 1 and cfg["split_k"] * N * 4 > SCRATCH_BYTES - COUNTER_BYTES
+    dev = torch.device("cuda")
+    A = torch.zeros((1, K), device=dev)
+    W = torch.empty((K, N), dtype=torch.int8, device=dev)
+    S = torch.zeros(((K + 31) // 32, N), device=dev)
+    C = torch.zeros((1, N), device=dev)
+    assert run_noalloc(q8, A, W, S, C) == ERR_SCRATCH_TOO_SMALL
+    text = q8.library().q8mv_status_string(ERR_SCRATCH_TOO_SMALL).decode()
+    assert "scratch" in text
+    del A, W, S, C
+    torch.cuda.empty_cache()
+
+
+def test_noalloc_edge_sizes(q8):
+    import torch
+
+    dev = torch.device("cuda")
+    C = torch.full((1, 300), float("nan"), device=dev)
+    empty_a = torch.empty((1, 0), device=dev)
+    empty_w = torch.empty((0, 300), dtype=torch.int8, device=dev)
+    empty_s = torch.empty((0, 300), device=dev)
+    assert run_noalloc(q8, empty_a, empty_w, empty_s, C) == 0  # K == 0 writes zeros
+    torch.cuda.synchronize()
+    assert torch.equal(C.cpu(), torch.zeros(1, 300))
+    lib = q8.library()
+    assert lib.q8mv_run_noalloc(-1, 4, None, None, None, None, None) == 1
+    assert lib.q8mv_run_noalloc(4, 4, None, None, None, None, None) == 1  # null C
