@@ -186,7 +186,10 @@ def run_ours(args, rank, local_rank, world):
     bytes_per_call = wl.algorithmic_bytes()
 
     A, W, S = workloads.make_inputs(wl)
-    plan = q8mv.Plan(K, N, device=local_rank)
+    kernel = {"auto": q8mv.KERNEL_AUTO, "regs": q8mv.KERNEL_REGS, "tma": q8mv.KERNEL_TMA,
+              "async": q8mv.KERNEL_ASYNC}[args.kernel]
+    plan = q8mv.Plan(K, N, device=local_rank, kernel=kernel, split_k=args.split, stages=args.stages,
+                     threads_n=args.threads_n, overlap=int(args.overlap), cta_threads=args.cta_threads)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0)) or 126 * 1024 * 1024
     # distinct copies so that a copy is reused only after > 2 x L2 of other traffic
@@ -311,8 +314,10 @@ def run_ours(args, rank, local_rank, world):
                          f"({copies * bytes_per_call / 1e6:.0f} MB) vs {l2 / 1e6:.0f} MB L2",
                    "timing": f"CUDA events around graph replays of {chunk} back-to-back calls",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "plan": {k: info[k] for k in ("kernel", "vec_bytes", "threads_n", "groups_k", "split_k",
-                                                 "blocks_per_split", "grid_x", "grid_y", "ctas_per_sm")}},
+                   "plan": {k: info[k] for k in ("kernel", "vec_bytes", "threads_per_cta", "threads_n",
+                                                 "groups_k", "split_k",
+                                                 "blocks_per_split", "stages", "overlap", "grid_x",
+                                                 "grid_y", "ctas_per_sm")}},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -399,6 +404,14 @@ def parse_args(argv=None):
     ap.add_argument("--reference-seconds", type=float, default=60.0,
                     help="CPU budget of the reference arm's timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["auto", "regs", "tma", "async"], default="auto",
+                    help="plan override: kernel family (default: the plan's choice)")
+    ap.add_argument("--split", type=int, default=0, help="plan override: K ranges per column tile")
+    ap.add_argument("--stages", type=int, default=0, help="plan override: TMA ring depth")
+    ap.add_argument("--threads-n", type=int, default=0, help="plan override: threads along N per CTA")
+    ap.add_argument("--cta-threads", type=int, default=0, help="plan override: threads per CTA (128 or 256)")
+    ap.add_argument("--overlap", action="store_true",
+                    help="plan option: programmatic dependent launch (weights constant across calls)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

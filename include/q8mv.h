@@ -62,7 +62,11 @@ typedef enum {
 /* Kernel families a plan can pick. */
 enum {
     Q8MV_KERNEL_AUTO = 0,
-    Q8MV_KERNEL_REGS = 1  /* weights streamed through registers with vector loads; any alignment */
+    Q8MV_KERNEL_REGS = 1, /* weights streamed through registers with vector loads; any alignment */
+    Q8MV_KERNEL_TMA = 2,  /* weights streamed by the tensor-memory accelerator into a shared-memory
+                             ring; needs N % 16 == 0, N >= 256, K >= 32 and 16-byte aligned A, W, S */
+    Q8MV_KERNEL_ASYNC = 3 /* each thread streams its weight strip through its own shared-memory ring
+                             with asynchronous 16-byte copies; needs N % 16 == 0 and 16-byte aligned W, S */
 };
 
 /*
@@ -71,20 +75,36 @@ enum {
  */
 typedef struct {
     int32_t kernel;    /* Q8MV_KERNEL_* */
-    int32_t vec_bytes; /* widest weight load per thread and row: 16, 8, 4, 2 or 1 */
+    int32_t vec_bytes; /* weight load per thread and row: 16, 8, 4, 2 or 1, used whenever W's
+                          address allows it (narrower loads only as a fallback); 0 lets the
+                          planner pick the width it expects to be fastest */
     int32_t threads_n; /* threads along N in one CTA: 32, 64, 128 or 256 */
-    int32_t split_k;   /* CTAs sharing one column tile along K (>= 1) */
+    int32_t split_k;   /* K ranges per column tile, each summed by one CTA (>= 1) */
+    int32_t stages;    /* ring depth: TMA kernel a multiple of 8 in 8 .. 32 stages of one block;
+                          async kernel 2, 3, 4 or 6 stages of 8 rows per thread */
+    int32_t overlap;   /* 1: launch with programmatic dependent launch, so a call starts while the
+                          previous kernel in its stream finishes and reads W and S before that kernel
+                          has completed (A is read and C written only after it).  Only for weights
+                          that the preceding work in the stream does not write.  Register and
+                          async kernels. */
+    int32_t cta_threads; /* register and async kernels: 128 or 256 threads per CTA */
 } q8mv_opts_t;
 
-/* What a plan chose, for the widest weight load the shape allows. */
+/* What a plan chose for 16-byte aligned tensors: the kernel family asked for
+ * (the register kernel by default) and, for the register kernel, the weight
+ * load width the planner expects to be fastest. */
 typedef struct {
-    int32_t kernel;           /* Q8MV_KERNEL_REGS */
+    int32_t kernel;           /* Q8MV_KERNEL_REGS, _TMA or _ASYNC */
     int32_t vec_bytes;        /* weight bytes per thread per row */
     int32_t threads_n;        /* threads along N per CTA */
     int32_t groups_k;         /* thread groups along K per CTA (threads per CTA / threads_n) */
     int32_t threads_per_cta;
-    int32_t split_k;          /* CTAs per column tile along K */
-    int32_t blocks_per_split; /* 32-row blocks each of those CTAs covers */
+    int32_t split_k;          /* K ranges per column tile (partial rows summed in range order) */
+    int32_t blocks_per_split; /* 32-row blocks in each K range */
+    int32_t stages;           /* TMA or async ring depth (0 for the register kernel) */
+    int32_t overlap;          /* programmatic dependent launch enabled */
+    int32_t cluster;          /* split-K partial rows summed through a thread-block cluster's
+                                 distributed shared memory (no workspace) */
     int64_t tile_n;           /* output columns per CTA */
     int64_t grid_x;           /* column tiles */
     int64_t grid_y;           /* = split_k */
@@ -118,6 +138,16 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device,
 q8mv_status_t q8mv_run(q8mv_plan_t plan, const float *A, const int8_t *W, const float *S,
                        float *C, cudaStream_t stream);
 
+/*
+ * Synchronise the plan's device and report in *device_error the error bits
+ * its kernels recorded since the last check (0 = none; 1 = a weight stage
+ * did not arrive in time, 2 = a ring slot was not released in time, 4 = a
+ * copy in flight did not land in time).  A kernel that records an error stops
+ * waiting and finishes; its output is then undefined.  The bits are cleared,
+ * and the plan's split-K counters are reset when any was set.
+ */
+q8mv_status_t q8mv_check(q8mv_plan_t plan, int32_t *device_error);
+
 /* Release the plan and its workspace.  NULL is accepted.  Synchronises the
  * plan's device first so that no launch still uses the workspace. */
 q8mv_status_t q8mv_destroy(q8mv_plan_t plan);
@@ -127,9 +157,10 @@ q8mv_status_t q8mv_plan_info(q8mv_plan_t plan, q8mv_plan_info_t *info);
 
 /*
  * Host-only planning, no GPU needed: the configuration q8mv_plan would pick
- * for K, N on a GPU with `sm_count` SMs, `ctas_per_sm` resident CTAs of the
- * register kernel, and weight loads of `vec_bytes` (which must divide N).
- * Used by tests of the planner; fills *info (workspace_bytes included).
+ * for K, N on a GPU with `sm_count` SMs.  For the register kernel (opts NULL
+ * or kernel REGS/AUTO): `ctas_per_sm` resident CTAs and weight loads of
+ * `vec_bytes` (which must divide N).  For opts->kernel == Q8MV_KERNEL_TMA the
+ * last two are ignored.  Fills *info (workspace_bytes of partial rows).
  */
 q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t ctas_per_sm,
                                  int32_t vec_bytes, const q8mv_opts_t *opts,
@@ -158,7 +189,7 @@ int q8mv_version(void);
  * It computes exactly what q8mv_run computes with a default plan for (K, N)
  * on the current device: same kernel, same tile and split, same summation
  * order.  The split-K partial sums and counters live in one static device
- * array of Q8MV_NOALLOC_SCRATCH_BYTES bytes inside this library (4 MiB, held
+ * array of Q8MV_NOALLOC_SCRATCH_BYTES bytes inside this library (2 MiB, held
  * by every GPU that loads the library until the process exits) instead of a
  * plan's workspace.
  *
@@ -168,7 +199,8 @@ int q8mv_version(void);
  *     split the planner picks needs more than that scratch: split_k * N floats
  *     of partial sums beyond the first 64 KiB, or more than 16384 column tiles
  *     of counters.  The 7B- and 70B-class projections and a 128256-row LM head
- *     all fit.
+ *     all fit with aligned weights; 1-byte-aligned weights of 16 MiB or more
+ *     can be refused.
  *   - The first call on each device looks up the scratch array's device
  *     address and the device's SM count and occupancy; make that first call
  *     before any stream capture begins on that device.
@@ -180,7 +212,7 @@ int q8mv_version(void);
  *     streams, other host threads) race on it: order them, for example by
  *     issuing them on one stream.
  */
-#define Q8MV_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+#define Q8MV_NOALLOC_SCRATCH_BYTES (2u * 1024u * 1024u)
 
 q8mv_status_t q8mv_run_noalloc(int64_t K, int64_t N, const float *A, const int8_t *W,
                                const float *S, float *C, cudaStream_t stream);

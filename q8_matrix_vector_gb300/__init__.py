@@ -26,18 +26,23 @@ Q8MV_ERR_CUDA = 4
 
 KERNEL_AUTO = 0
 KERNEL_REGS = 1
+KERNEL_TMA = 2
+KERNEL_ASYNC = 3
 
 
 class Opts(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
-                ("threads_n", ctypes.c_int32), ("split_k", ctypes.c_int32)]
+                ("threads_n", ctypes.c_int32), ("split_k", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("overlap", ctypes.c_int32),
+                ("cta_threads", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
                 ("threads_n", ctypes.c_int32), ("groups_k", ctypes.c_int32),
                 ("threads_per_cta", ctypes.c_int32), ("split_k", ctypes.c_int32),
-                ("blocks_per_split", ctypes.c_int32),
+                ("blocks_per_split", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("overlap", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("tile_n", ctypes.c_int64), ("grid_x", ctypes.c_int64), ("grid_y", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("sm_count", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32)]
@@ -67,6 +72,8 @@ def _load() -> ctypes.CDLL:
     lib.q8mv_plan.restype = ctypes.c_int
     lib.q8mv_run.argtypes = [p, p, p, p, p, p]
     lib.q8mv_run.restype = ctypes.c_int
+    lib.q8mv_check.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
+    lib.q8mv_check.restype = ctypes.c_int
     lib.q8mv_destroy.argtypes = [p]
     lib.q8mv_destroy.restype = ctypes.c_int
     lib.q8mv_plan_info.argtypes = [p, ctypes.POINTER(PlanInfo)]
@@ -91,10 +98,10 @@ def library() -> ctypes.CDLL:
     return _lib
 
 
-def _opts(kernel=0, vec_bytes=0, threads_n=0, split_k=0):
-    if not (kernel or vec_bytes or threads_n or split_k):
+def _opts(kernel=0, vec_bytes=0, threads_n=0, split_k=0, stages=0, overlap=0, cta_threads=0):
+    if not (kernel or vec_bytes or threads_n or split_k or stages or overlap or cta_threads):
         return None
-    return Opts(kernel, vec_bytes, threads_n, split_k)
+    return Opts(kernel, vec_bytes, threads_n, split_k, stages, overlap, cta_threads)
 
 
 def choose_config(K: int, N: int, sm_count: int, ctas_per_sm: int, vec_bytes: int, **opts) -> dict:
@@ -162,6 +169,14 @@ class Plan:
         with torch.cuda.device(dev):
             self.run_ptr(A.data_ptr(), W.data_ptr(), S.data_ptr(), out.data_ptr(), stream.cuda_stream)
         return out
+
+    def check(self) -> int:
+        """Synchronise and return (and clear) the error bits the plan's kernels recorded."""
+        word = ctypes.c_int32()
+        st = _lib.q8mv_check(self._h, ctypes.byref(word))
+        if st != Q8MV_OK:
+            raise Q8mvError(st, "q8mv_check")
+        return word.value
 
     def close(self) -> None:
         if getattr(self, "_h", None) is not None and self._h.value:

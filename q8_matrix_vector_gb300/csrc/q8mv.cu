@@ -26,6 +26,9 @@
 //     fold use packed f32x2 fused multiply-adds, round-to-nearest, no flush.
 #include "../../include/q8mv.h"
 
+#include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -37,10 +40,12 @@
 #include <mutex>
 #include <new>
 
+#include "async_stream.cuh"
+#include "tma_stream.cuh"
+
 namespace {
 
 constexpr int kBlk = 32;            // Q8_0 block length along K
-constexpr int kCtaThreads = 256;    // threads per CTA of the register kernel
 constexpr int kStageBlocks = 64;    // activation blocks staged in shared memory at a time
 constexpr int kMaxSplit = 65535;    // gridDim.y limit
 constexpr int kVersion = 100;       // 0.1.0
@@ -73,7 +78,7 @@ struct Params {
     int KB;
     int tn;               // threads along N (power of two, 32..256)
     int tn_log2;
-    int gk;               // thread groups along K = kCtaThreads / tn
+    int gk;               // thread groups along K = threads per CTA / tn
     int split;            // CTAs per tile along K
     int bps;              // blocks per split
 };
@@ -187,10 +192,36 @@ __device__ __forceinline__ void fold_scale(const float (&part)[V], const float (
 // ---------------------------------------------------------------------------
 // Register-streaming kernel
 // ---------------------------------------------------------------------------
-template <int V, bool SVEC>
-__global__ void __launch_bounds__(kCtaThreads, 1) q8mv_regs_kernel(const Params p) {
+// Weight loads of a thread's first block are issued before anything else, and
+// in particular before griddepcontrol.wait: under programmatic dependent launch
+// the kernel may start while the previous kernel in the stream is finishing,
+// so its weight stream overlaps that kernel's tail.  The activations, the
+// workspace and C are touched only after the wait.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <int V>
+__device__ __forceinline__ void load_w_volatile(const int8_t *p, uint32_t (&w)[(V + 3) / 4]) {
+    // same loads as load_w, but kept in program order so that a block's 32
+    // rows are all in flight before the first one is used
+    if constexpr (V == 16) {
+        asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "l"(p));
+    } else if constexpr (V == 8) {
+        asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p));
+    } else {
+        load_w<V>(p, w);
+    }
+}
+
+template <int V, bool SVEC, int TPB, bool CLUSTER>
+__global__ void __launch_bounds__(TPB, 1) q8mv_regs_kernel(const Params p) {
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_is_last;
+    constexpr int VW = (V + 3) / 4;
 
     const int tid = threadIdx.x;
     const int tn_i = tid & (p.tn - 1);
@@ -204,6 +235,19 @@ __global__ void __launch_bounds__(kCtaThreads, 1) q8mv_regs_kernel(const Params 
     const int b_begin = blockIdx.y * p.bps;
     const int b_end = min(p.KB, b_begin + p.bps);
 
+    // the first block of this thread, if it is whole, is loaded right away
+    uint32_t w[kBlk][VW];
+    int b = b_begin + gk_i;
+    bool prefetched = false;
+    if (active && b < b_end && static_cast<int64_t>(b + 1) * kBlk <= p.K) {
+        const int8_t *w_ptr = p.W + static_cast<int64_t>(b) * kBlk * p.N + n0;
+#pragma unroll
+        for (int r = 0; r < kBlk; ++r) load_w_volatile<V>(w_ptr + r * p.N, w[r]);
+        prefetched = true;
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+
     float acc[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) acc[j] = 0.0f;
@@ -214,11 +258,11 @@ __global__ void __launch_bounds__(kCtaThreads, 1) q8mv_regs_kernel(const Params 
         const int64_t k0 = static_cast<int64_t>(c_begin) * kBlk;
         const int nk = static_cast<int>(min(static_cast<int64_t>(c_end) * kBlk, p.K) - k0);
         __syncthreads();
-        for (int i = tid; i < nk; i += kCtaThreads) smem[i] = __ldg(p.A + k0 + i);
+        for (int i = tid; i < nk; i += TPB) smem[i] = __ldg(p.A + k0 + i);
         __syncthreads();
         if (!active) continue;
 
-        for (int b = c_begin + gk_i; b < c_end; b += p.gk) {
+        for (; b < c_end; b += p.gk) {
             const float *a_blk = smem + (b - c_begin) * kBlk;
             const int8_t *w_ptr = p.W + static_cast<int64_t>(b) * kBlk * p.N + n0;
             const int64_t rows = min(static_cast<int64_t>(kBlk), p.K - static_cast<int64_t>(b) * kBlk);
@@ -228,10 +272,12 @@ __global__ void __launch_bounds__(kCtaThreads, 1) q8mv_regs_kernel(const Params 
             for (int j = 0; j < V; ++j) part[j] = 0.0f;
 
             if (rows == kBlk) {
-                // whole block: issue all 32 row loads before the arithmetic
-                uint32_t w[kBlk][(V + 3) / 4];
+                // whole block: all 32 row loads are issued before the arithmetic
+                if (!prefetched) {
 #pragma unroll
-                for (int r = 0; r < kBlk; ++r) load_w<V>(w_ptr + r * p.N, w[r]);
+                    for (int r = 0; r < kBlk; ++r) load_w_volatile<V>(w_ptr + r * p.N, w[r]);
+                }
+                prefetched = false;
 #pragma unroll
                 for (int r = 0; r < kBlk; r += 4) {
                     const float4 a4 = *reinterpret_cast<const float4 *>(a_blk + r);
@@ -243,9 +289,9 @@ __global__ void __launch_bounds__(kCtaThreads, 1) q8mv_regs_kernel(const Params 
             } else {
                 // masked remainder: rows at or past K are never read
                 for (int r = 0; r < rows; ++r) {
-                    uint32_t w[(V + 3) / 4];
-                    load_w<V>(w_ptr + r * p.N, w);
-                    fma_row<V>(a_blk[r], w, part);
+                    uint32_t wr[VW];
+                    load_w<V>(w_ptr + r * p.N, wr);
+                    fma_row<V>(a_blk[r], wr, part);
                 }
             }
             float s[V];
@@ -261,8 +307,35 @@ __global__ void __launch_bounds__(kCtaThreads, 1) q8mv_regs_kernel(const Params 
     for (int j = 0; j < V; ++j) red[gk_i * tile_cols + tn_i * V + j] = acc[j];
     __syncthreads();
 
+    if constexpr (CLUSTER) {
+        // The split_k CTAs of this tile form one thread-block cluster.  Each
+        // keeps its column sums in its own shared memory; after a cluster
+        // barrier CTA r adds up slice r of the columns over all the cluster's
+        // CTAs, in rank order, reading their shared memory directly.
+        namespace cg = cooperative_groups;
+        float *mine = smem + p.gk * tile_cols;  // [tile_cols]
+        for (int c = tid; c < tile_cols; c += TPB) {
+            float v = red[c];
+            for (int g = 1; g < p.gk; ++g) v += red[g * tile_cols + c];
+            mine[c] = v;
+        }
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        const int rank = static_cast<int>(blockIdx.y);
+        const int per = (tile_cols + p.split - 1) / p.split;
+        const int c_end = min(tile_cols, (rank + 1) * per);
+        for (int c = rank * per + tid; c < c_end; c += TPB) {
+            const int64_t n = col0 + c;
+            float v = *cluster.map_shared_rank(mine + c, 0);
+            for (int q = 1; q < p.split; ++q) v += *cluster.map_shared_rank(mine + c, q);
+            if (n < p.N) p.C[n] = v;
+        }
+        cluster.sync();  // keep this CTA's sums alive until every CTA has read them
+        return;
+    }
+
     const bool split = p.split > 1;
-    for (int c = tid; c < tile_cols; c += kCtaThreads) {
+    for (int c = tid; c < tile_cols; c += TPB) {
         const int64_t n = col0 + c;
         if (n >= p.N) break;
         float v = red[c];
@@ -285,11 +358,11 @@ __global__ void __launch_bounds__(kCtaThreads, 1) q8mv_regs_kernel(const Params 
     __syncthreads();
     if (!s_is_last) return;
     __threadfence();
-    for (int c = tid; c < tile_cols; c += kCtaThreads) {
+    for (int c = tid; c < tile_cols; c += TPB) {
         const int64_t n = col0 + c;
         if (n >= p.N) break;
         float v = __ldcg(p.ws + n);
-        for (int s = 1; s < p.split; ++s) v += __ldcg(p.ws + static_cast<int64_t>(s) * p.N + n);
+        for (int q = 1; q < p.split; ++q) v += __ldcg(p.ws + static_cast<int64_t>(q) * p.N + n);
         p.C[n] = v;
     }
     if (tid == 0) p.tickets[tile] = 0u;  // ready for the next call
@@ -300,6 +373,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1) q8mv_regs_kernel(const Params 
 // ---------------------------------------------------------------------------
 struct Config {
     int vec = 0;
+    int tpb = 256;  // threads per CTA
+    bool cluster = false;  // split-K sums through distributed shared memory (no workspace)
     int tn = 0;
     int gk = 0;
     int split = 0;
@@ -307,10 +382,12 @@ struct Config {
     int64_t tiles = 0;
     int64_t tile_n = 0;
     int64_t ws_floats = 0;
+    double cost_us = 0.0;  // planner's estimate
 };
 
 bool valid_vec(int v) { return v == 16 || v == 8 || v == 4 || v == 2 || v == 1; }
-bool valid_tn(int t) { return t == 32 || t == 64 || t == 128 || t == 256; }
+bool cluster_capable(int vec) { return vec == 16 || vec == 8; }
+bool valid_tn(int t) { return t == 8 || t == 16 || t == 32 || t == 64 || t == 128 || t == 256; }
 
 int log2_pow2(int x) {
     int l = 0;
@@ -318,52 +395,101 @@ int log2_pow2(int x) {
     return l;
 }
 
-// Cost model: the kernel is bound by HBM, so estimate the weight bytes the
-// busiest SM must pull (CTAs spread evenly over SMs) plus the split-K
-// workspace traffic spread over all SMs.  Ties go to fewer splits.
-q8mv_status_t choose(int64_t K, int64_t N, int sm_count, int cps, int vec, const q8mv_opts_t *o,
-                     Config *out) {
-    if (K < 0 || N < 0 || sm_count <= 0 || cps <= 0 || !valid_vec(vec)) return Q8MV_ERR_INVALID_ARG;
+// Resident CTAs per SM of the register kernel, per weight-load width (16, 8,
+// 4, 2, 1 bytes) and CTA size (128, 256 threads).
+struct Occupancy {
+    int cps[5][2] = {{2, 1}, {4, 2}, {4, 2}, {4, 2}, {4, 2}};
+    int get(int vec_idx, int tpb) const { return cps[vec_idx][tpb == 128 ? 0 : 1]; }
+};
+
+int vec_idx_of(int v) { return v == 16 ? 0 : v == 8 ? 1 : v == 4 ? 2 : v == 2 ? 3 : 4; }
+
+// Cost model, in microseconds, fitted to measurements of this kernel on
+// GB300 over the decode shapes.  The time to stream the bytes is set by the
+// bytes in flight: each resident thread with a block requests 32 rows at
+// once, and between blocks it spends the block's arithmetic (about 0.1 us per
+// byte of load width) with nothing in flight; with about 1.5 us of loaded DRAM
+// latency that gives the achievable bandwidth, capped at 7.2 TB/s.  A partial
+// last wave of CTAs costs as much as a full one.  A split adds its reduction
+// at the end: ~0.3 us through a cluster, ~3 us through the workspace.  The
+// last block's arithmetic is added once.
+double model_us(int64_t K, int64_t N, int sm_count, int cps, int vec, int tpb, int tn, int64_t split, int64_t bps,
+                int64_t tiles, bool cluster) {
+    constexpr double kBw = 7.2e6;   // bytes per microsecond
+    constexpr double kLat = 1.5;    // microseconds
+    const int gk = tpb / tn;
+    const int64_t ctas = tiles * split;
+    const double total = static_cast<double>(ceil_div(K, kBlk)) * kBlk * N * 1.125;
+    const double slots = static_cast<double>(sm_count) * cps;
+    const double resident = std::min(static_cast<double>(ctas), slots);
+    const double busy = static_cast<double>(std::min<int64_t>(gk, bps));
+    const int64_t blocks_per_thread = ceil_div(bps, gk);
+    const double t_comp = 0.1 * vec;
+    const double duty = blocks_per_thread <= 1 ? 1.0 : kLat / (kLat + t_comp);
+    const double inflight = resident * busy * tn * kBlk * vec * duty;
+    const double bw = std::min(kBw, inflight / kLat);
+    double t = total / bw;
+    const double waves = static_cast<double>(ctas) / slots;
+    if (waves > 1.0) t *= std::ceil(waves) / waves;
+    const double tail = split <= 1 ? 0.0 : (cluster ? 0.3 : 3.0);
+    return t + tail + t_comp;
+}
+
+q8mv_status_t choose(int64_t K, int64_t N, int sm_count, const Occupancy &occ, int vec, const q8mv_opts_t *o,
+                     Config *out, int max_cluster = 8) {
+    if (K < 0 || N < 0 || sm_count <= 0 || !valid_vec(vec)) return Q8MV_ERR_INVALID_ARG;
     if (N % vec != 0) return Q8MV_ERR_INVALID_ARG;
     const int want_tn = o ? o->threads_n : 0;
     const int want_split = o ? o->split_k : 0;
+    const int want_tpb = o ? o->cta_threads : 0;
     if (want_tn != 0 && !valid_tn(want_tn)) return Q8MV_ERR_INVALID_ARG;
     if (want_split < 0 || want_split > kMaxSplit) return Q8MV_ERR_INVALID_ARG;
+    if (want_tpb != 0 && want_tpb != 128 && want_tpb != 256) return Q8MV_ERR_INVALID_ARG;
 
     const int64_t KB = ceil_div(K, kBlk);
     const int64_t strips = N / vec;
+    // a row segment of a thread group should cover whole 128-byte lines
+    const int min_tn = std::max(8, 128 / vec);
     Config best;
     double best_cost = -1.0;
-    for (int tn = 32; tn <= 256; tn *= 2) {
-        if (want_tn != 0 && tn != want_tn) continue;
-        const int gk = kCtaThreads / tn;
-        const int64_t tile_n = static_cast<int64_t>(tn) * vec;
-        const int64_t tiles = std::max<int64_t>(1, ceil_div(strips, tn));
-        if (tiles > 0x7fffffffLL) continue;
-        int64_t max_split = std::max<int64_t>(1, KB);
-        max_split = std::min<int64_t>(max_split, kMaxSplit);
-        // more than ~8 waves of CTAs never helps a bandwidth-bound kernel
-        max_split = std::min<int64_t>(max_split, std::max<int64_t>(1, 8LL * sm_count * cps / tiles));
-        int64_t lo = 1, hi = max_split;
-        if (want_split != 0) lo = hi = std::min<int64_t>(want_split, std::max<int64_t>(1, KB));
-        for (int64_t split = lo; split <= hi; ++split) {
-            const int64_t bps = std::max<int64_t>(1, ceil_div(KB, split));
-            const int64_t split_eff = std::max<int64_t>(1, ceil_div(KB, bps));
-            if (split_eff != split && want_split == 0) continue;  // same as a smaller split
-            const int64_t ctas = tiles * split_eff;
-            const double per_sm = static_cast<double>(ceil_div(ctas, sm_count)) * bps * kBlk * tile_n;
-            const double ws = split_eff > 1 ? 8.0 * split_eff * N / sm_count : 0.0;
-            const double cost = per_sm + ws;
-            if (best_cost < 0 || cost < best_cost * (1.0 - 1e-9)) {
-                best_cost = cost;
-                best.vec = vec;
-                best.tn = tn;
-                best.gk = gk;
-                best.split = static_cast<int>(split_eff);
-                best.bps = static_cast<int>(bps);
-                best.tiles = tiles;
-                best.tile_n = tile_n;
-                best.ws_floats = split_eff > 1 ? split_eff * N : 0;
+    for (int tpb = 128; tpb <= 256; tpb *= 2) {
+        if (want_tpb != 0 && tpb != want_tpb) continue;
+        const int cps = std::max(1, occ.get(vec_idx_of(vec), tpb));
+        for (int tn = 8; tn <= tpb; tn *= 2) {
+            if (want_tn != 0 && tn != want_tn) continue;
+            if (want_tn == 0 && tn < min_tn) continue;
+            const int gk = tpb / tn;
+            const int64_t tile_n = static_cast<int64_t>(tn) * vec;
+            const int64_t tiles = std::max<int64_t>(1, ceil_div(strips, tn));
+            if (tiles > 0x7fffffffLL) continue;
+            int64_t max_split = std::max<int64_t>(1, KB);
+            max_split = std::min<int64_t>(max_split, kMaxSplit);
+            // more than ~8 waves of CTAs never helps a bandwidth-bound kernel
+            max_split = std::min<int64_t>(max_split, std::max<int64_t>(1, 8LL * sm_count * cps / tiles));
+            int64_t lo = 1, hi = max_split;
+            if (want_split != 0) lo = hi = std::min<int64_t>(want_split, std::max<int64_t>(1, KB));
+            for (int64_t split = lo; split <= hi; ++split) {
+                const int64_t bps = std::max<int64_t>(1, ceil_div(KB, split));
+                const int64_t split_eff = std::max<int64_t>(1, ceil_div(KB, bps));
+                if (split_eff != split && want_split == 0) continue;  // same as a smaller split
+                const int64_t ctas = tiles * split_eff;
+                const bool one_wave = ctas <= static_cast<int64_t>(sm_count) * cps;
+                const bool cluster = split_eff > 1 && split_eff <= max_cluster && cluster_capable(vec) && one_wave;
+                const double cost = model_us(K, N, sm_count, cps, vec, tpb, tn, split_eff, bps, tiles, cluster);
+                if (best_cost < 0 || cost < best_cost * (1.0 - 1e-9)) {
+                    best_cost = cost;
+                    best.cost_us = cost;
+                    best.cluster = cluster;
+                    best.vec = vec;
+                    best.tpb = tpb;
+                    best.tn = tn;
+                    best.gk = gk;
+                    best.split = static_cast<int>(split_eff);
+                    best.bps = static_cast<int>(bps);
+                    best.tiles = tiles;
+                    best.tile_n = tile_n;
+                    best.ws_floats = (split_eff > 1 && !cluster) ? split_eff * N : 0;
+                }
             }
         }
     }
@@ -378,7 +504,7 @@ void fill_info(const Config &c, int sm_count, int cps, int64_t ws_bytes, q8mv_pl
     info->vec_bytes = c.vec;
     info->threads_n = c.tn;
     info->groups_k = c.gk;
-    info->threads_per_cta = kCtaThreads;
+    info->threads_per_cta = c.tpb;
     info->split_k = c.split;
     info->blocks_per_split = c.bps;
     info->tile_n = c.tile_n;
@@ -387,6 +513,7 @@ void fill_info(const Config &c, int sm_count, int cps, int64_t ws_bytes, q8mv_pl
     info->workspace_bytes = ws_bytes;
     info->sm_count = sm_count;
     info->ctas_per_sm = cps;
+    info->cluster = c.cluster ? 1 : 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -394,20 +521,103 @@ void fill_info(const Config &c, int sm_count, int cps, int64_t ws_bytes, q8mv_pl
 // ---------------------------------------------------------------------------
 using KernelFn = void (*)(Params);
 
-KernelFn kernel_for(int vec, bool svec) {
+template <int TPB>
+KernelFn kernel_for_tpb(int vec, bool svec) {
     switch (vec) {
-        case 16: return svec ? q8mv_regs_kernel<16, true> : q8mv_regs_kernel<16, false>;
-        case 8: return svec ? q8mv_regs_kernel<8, true> : q8mv_regs_kernel<8, false>;
-        case 4: return svec ? q8mv_regs_kernel<4, true> : q8mv_regs_kernel<4, false>;
-        case 2: return svec ? q8mv_regs_kernel<2, true> : q8mv_regs_kernel<2, false>;
-        default: return q8mv_regs_kernel<1, false>;
+        case 16: return svec ? q8mv_regs_kernel<16, true, TPB, false> : q8mv_regs_kernel<16, false, TPB, false>;
+        case 8: return svec ? q8mv_regs_kernel<8, true, TPB, false> : q8mv_regs_kernel<8, false, TPB, false>;
+        case 4: return svec ? q8mv_regs_kernel<4, true, TPB, false> : q8mv_regs_kernel<4, false, TPB, false>;
+        case 2: return svec ? q8mv_regs_kernel<2, true, TPB, false> : q8mv_regs_kernel<2, false, TPB, false>;
+        default: return q8mv_regs_kernel<1, false, TPB, false>;
     }
 }
 
+// cluster-reduced variants exist for the 16- and 8-byte loads (the decode shapes)
+template <int TPB>
+KernelFn cluster_kernel_for_tpb(int vec, bool svec) {
+    if (vec == 16) return svec ? q8mv_regs_kernel<16, true, TPB, true> : q8mv_regs_kernel<16, false, TPB, true>;
+    return svec ? q8mv_regs_kernel<8, true, TPB, true> : q8mv_regs_kernel<8, false, TPB, true>;
+}
+
+KernelFn kernel_for(int vec, bool svec, int tpb, bool cluster = false) {
+    if (cluster) return tpb == 128 ? cluster_kernel_for_tpb<128>(vec, svec) : cluster_kernel_for_tpb<256>(vec, svec);
+    return tpb == 128 ? kernel_for_tpb<128>(vec, svec) : kernel_for_tpb<256>(vec, svec);
+}
+
+// Largest split the register kernel reduces through a cluster: the portable
+// cluster size, 8, when the device can schedule such clusters of this kernel.
+int query_max_cluster() {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(8, 8);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 17 * 1024;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 1;
+    attr.val.clusterDim.y = 8;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, q8mv_regs_kernel<16, true, 256, true>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    return clusters >= 1 ? 8 : 1;
+}
+
+// Resident CTAs per SM of every register-kernel variant on the current device.
+cudaError_t query_occupancy(Occupancy *occ) {
+    const int vecs[5] = {16, 8, 4, 2, 1};
+    for (int i = 0; i < 5; ++i) {
+        for (int t = 0; t < 2; ++t) {
+            const int tpb = t == 0 ? 128 : 256;
+            const size_t smem = std::max<size_t>(static_cast<size_t>(kStageBlocks) * kBlk * sizeof(float),
+                                                 static_cast<size_t>(tpb) * vecs[i] * sizeof(float) + 4096);
+            int cps = 1;
+            const cudaError_t e =
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cps, kernel_for(vecs[i], true, tpb), tpb, smem);
+            if (e != cudaSuccess) return e;
+            occ->cps[i][t] = std::max(1, cps);
+        }
+    }
+    return cudaSuccess;
+}
+
+// Launch the register kernel, with programmatic dependent launch if asked.
+cudaError_t launch_regs(const Config &c, bool svec, size_t smem, const Params &prm, cudaStream_t stream,
+                        bool overlap);
+
 size_t smem_bytes(const Config &c) {
     const size_t stage = static_cast<size_t>(kStageBlocks) * kBlk * sizeof(float);
-    const size_t red = static_cast<size_t>(c.gk) * c.tile_n * sizeof(float);
+    const size_t red = static_cast<size_t>(c.gk + (c.cluster ? 1 : 0)) * c.tile_n * sizeof(float);
     return std::max(stage, red);
+}
+
+cudaError_t launch_regs(const Config &c, bool svec, size_t smem, const Params &prm, cudaStream_t stream,
+                        bool overlap) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(c.tiles), static_cast<unsigned>(c.split));
+    cfg.blockDim = dim3(static_cast<unsigned>(c.tpb));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n_attr = 0;
+    if (overlap) {
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attr;
+    }
+    if (c.cluster) {
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = 1;
+        attr[n_attr].val.clusterDim.y = static_cast<unsigned>(c.split);
+        attr[n_attr].val.clusterDim.z = 1;
+        ++n_attr;
+    }
+    cfg.attrs = n_attr ? attr : nullptr;
+    cfg.numAttrs = n_attr;
+    return cudaLaunchKernelEx(&cfg, kernel_for(c.vec, svec, c.tpb, c.cluster), prm);
 }
 
 constexpr int kVecs[5] = {16, 8, 4, 2, 1};
@@ -421,6 +631,239 @@ int vec_index(int v) {
 }  // namespace
 
 // ---------------------------------------------------------------------------
+// TMA-stream kernel: host side
+// ---------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode_tiled;
+}
+
+// Small direct-mapped cache of encoded tensor maps, keyed by base address.
+struct MapCache {
+    static constexpr int kSlots = 32;
+    const void *key[kSlots] = {};
+    CUtensorMap map[kSlots];
+    const CUtensorMap *find(const void *ptr) const {
+        const int i = static_cast<int>((reinterpret_cast<uintptr_t>(ptr) >> 8) % kSlots);
+        return key[i] == ptr ? &map[i] : nullptr;
+    }
+    CUtensorMap *slot(const void *ptr) {
+        const int i = static_cast<int>((reinterpret_cast<uintptr_t>(ptr) >> 8) % kSlots);
+        key[i] = nullptr;
+        return &map[i];
+    }
+    void commit(const void *ptr) {
+        const int i = static_cast<int>((reinterpret_cast<uintptr_t>(ptr) >> 8) % kSlots);
+        key[i] = ptr;
+    }
+};
+
+// A failed encode is reported through q8mv_last_cuda_error as
+// -(1000 * which + CUresult), which = 1 for W, 2 for S, 3 for A.
+bool encode_result(int which, CUresult r) {
+    if (r == CUDA_SUCCESS) return true;
+    g_last_cuda_error = -(1000 * which + static_cast<int>(r));
+    return false;
+}
+
+// W as a 2D map [K rows][N bytes], box 32 rows x 256 columns.
+bool encode_w(CUtensorMap *m, const int8_t *W, int64_t K, int64_t N) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N)};
+    const cuuint32_t box[2] = {tmak::kUnitN, tmak::kBlk};
+    const cuuint32_t elem[2] = {1, 1};
+    return encode_result(1, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(W), dims, strides,
+                                        box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+}
+
+// S as a 2D map [KB rows][N floats], box 1 row x 256 columns.
+bool encode_s(CUtensorMap *m, const float *S, int64_t KB, int64_t N) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(KB)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
+    const cuuint32_t box[2] = {tmak::kUnitN, 1};
+    const cuuint32_t elem[2] = {1, 1};
+    return encode_result(2, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(S), dims, strides,
+                                        box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+}
+
+// A as a 1D map [K floats], box 32.
+bool encode_a(CUtensorMap *m, const float *A, int64_t K) {
+    const cuuint64_t dims[1] = {static_cast<cuuint64_t>(K)};
+    const cuuint64_t strides[1] = {0};  // unused for rank 1, but the encoder rejects a null array
+    const cuuint32_t box[1] = {tmak::kBlk};
+    const cuuint32_t elem[1] = {1};
+    return encode_result(3, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float *>(A), dims, strides,
+                                        box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+}
+
+size_t tma_smem_bytes(int stages) {
+    return static_cast<size_t>(stages) * tmak::kStageBytes + tmak::kRedBytes +
+           2 * tmak::kMaxStages * sizeof(uint64_t);
+}
+
+struct TmaConfig {
+    int64_t tiles = 0;
+    int split = 1;
+    int bps = 1;
+    int64_t items = 0;
+    int grid = 0;
+    int64_t ws_floats = 0;
+};
+
+// Split of each tile's K range for the TMA kernel.  Cost model as for the
+// register kernel: the weight bytes the busiest CTA (one per SM) streams, plus
+// the partial-row traffic of the split spread over all SMs.  Ties go to the
+// smaller split.
+TmaConfig choose_tma(int64_t K, int64_t N, int sm_count, int want_split) {
+    TmaConfig c;
+    const int64_t KB = ceil_div(K, kBlk);
+    c.tiles = ceil_div(N, tmak::kUnitN);
+    const int64_t unit_bytes = static_cast<int64_t>(kBlk) * tmak::kUnitN;
+    int64_t lo = 1, hi = std::min<int64_t>(KB, std::max<int64_t>(1, 16LL * sm_count));
+    if (want_split > 0) lo = hi = std::min<int64_t>(want_split, KB);
+    double best = -1.0;
+    for (int64_t split = lo; split <= hi; ++split) {
+        const int64_t bps = ceil_div(KB, split);
+        const int64_t split_eff = ceil_div(KB, bps);
+        if (split_eff != split && want_split <= 0) continue;
+        const int64_t items = c.tiles * split_eff;
+        const int64_t grid = std::min<int64_t>(sm_count, items);
+        const double per_cta = static_cast<double>(ceil_div(items, grid)) * bps * unit_bytes;
+        const double ws = split_eff > 1 ? 8.0 * split_eff * N / grid : 0.0;
+        const double cost = per_cta + ws;
+        if (best < 0 || cost < best * (1.0 - 1e-9)) {
+            best = cost;
+            c.split = static_cast<int>(split_eff);
+            c.bps = static_cast<int>(bps);
+            c.items = items;
+            c.grid = static_cast<int>(grid);
+            c.ws_floats = split_eff > 1 ? split_eff * N : 0;
+        }
+    }
+    return c;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Async-ring kernel: host side
+// ---------------------------------------------------------------------------
+namespace {
+
+
+using AsyncFn = void (*)(asyk::Params);
+
+AsyncFn async_kernel(int depth, int tpb) {
+    if (tpb == 128) {
+        switch (depth) {
+            case 2: return asyk::q8mv_async_kernel<2, 128>;
+            case 3: return asyk::q8mv_async_kernel<3, 128>;
+            case 4: return asyk::q8mv_async_kernel<4, 128>;
+            default: return asyk::q8mv_async_kernel<6, 128>;
+        }
+    }
+    switch (depth) {
+        case 2: return asyk::q8mv_async_kernel<2, 256>;
+        case 3: return asyk::q8mv_async_kernel<3, 256>;
+        case 4: return asyk::q8mv_async_kernel<4, 256>;
+        default: return asyk::q8mv_async_kernel<6, 256>;
+    }
+}
+
+size_t async_smem(int depth, int tpb) {
+    return static_cast<size_t>(depth) * asyk::kRows * tpb * asyk::kV + asyk::kABytes;
+}
+
+bool valid_async_depth(int d) { return d == 2 || d == 3 || d == 4 || d == 6; }
+
+// CTAs of this footprint that fit on one SM by shared memory (228 KiB, 1 KiB reserved per CTA)
+int async_cps(int depth, int tpb) {
+    return std::max(1, static_cast<int>((228 * 1024) / (async_smem(depth, tpb) + 1024)));
+}
+
+// Same cost model as the register kernel, over CTAs of 128 or 256 threads,
+// tiles of 8 .. 64 strips of 16 columns and ring depths 2 .. 6, with at most
+// kMaxBps blocks per CTA so that the CTA's activations fit in shared memory.
+// The depth is the smallest that keeps a thread's whole block (4 stages), or
+// 6 stages of a longer run, in flight.
+q8mv_status_t choose_async(int64_t K, int64_t N, int sm_count, const q8mv_opts_t *o, Config *out, int *depth_out) {
+    if (K < 1 || N < 16 || N % 16 != 0 || sm_count <= 0) return Q8MV_ERR_INVALID_ARG;
+    const int want_tn = o ? o->threads_n : 0;
+    const int want_split = o ? o->split_k : 0;
+    const int want_depth = o ? o->stages : 0;
+    const int want_tpb = o ? o->cta_threads : 0;
+    if (want_depth != 0 && !valid_async_depth(want_depth)) return Q8MV_ERR_INVALID_ARG;
+    const int64_t KB = ceil_div(K, kBlk);
+    const int64_t strips = N / asyk::kV;
+    Config best;
+    int best_depth = 0;
+    double best_cost = -1.0;
+    for (int tpb = 128; tpb <= 256; tpb *= 2) {
+        if (want_tpb != 0 && tpb != want_tpb) continue;
+        for (int tn = 8; tn <= 64; tn *= 2) {
+            if (want_tn != 0 && tn != want_tn) continue;
+            const int gk = tpb / tn;
+            const int64_t tile_n = static_cast<int64_t>(tn) * asyk::kV;
+            const int64_t tiles = ceil_div(strips, tn);
+            const int64_t min_split = ceil_div(KB, asyk::kMaxBps);
+            int64_t max_split = std::min<int64_t>(std::max<int64_t>(KB, 1), kMaxSplit);
+            max_split = std::min<int64_t>(max_split, std::max<int64_t>(min_split, 16LL * sm_count / tiles));
+            int64_t lo = min_split, hi = max_split;
+            if (want_split != 0) lo = hi = std::max<int64_t>(min_split, std::min<int64_t>(want_split, KB));
+            for (int64_t split = lo; split <= hi; ++split) {
+                const int64_t bps = ceil_div(KB, split);
+                const int64_t split_eff = ceil_div(KB, bps);
+                if (split_eff != split && want_split == 0) continue;
+                if (bps > asyk::kMaxBps) continue;
+                const int64_t blocks_per_thread = ceil_div(bps, gk);
+                const int depth = want_depth ? want_depth : (blocks_per_thread <= 1 ? 4 : 6);
+                const int cps = async_cps(depth, tpb);
+                const int64_t ctas = tiles * split_eff;
+                const int64_t busy = std::min<int64_t>(gk, bps) * blocks_per_thread;
+                const double per_sm = static_cast<double>(ceil_div(ctas, sm_count)) * std::max(bps, busy) * kBlk * tile_n;
+                const double ws = split_eff > 1 ? 8.0 * split_eff * N / sm_count : 0.0;
+                const double waves = static_cast<double>(ceil_div(ctas, static_cast<int64_t>(sm_count) * cps));
+                const double cost = per_sm + ws + 48.0 * 1024 * (waves - 1);
+                if (best_cost < 0 || cost < best_cost * (1.0 - 1e-9)) {
+                    best_cost = cost;
+                    best.vec = asyk::kV;
+                    best.tpb = tpb;
+                    best.tn = tn;
+                    best.gk = gk;
+                    best.split = static_cast<int>(split_eff);
+                    best.bps = static_cast<int>(bps);
+                    best.tiles = tiles;
+                    best.tile_n = tile_n;
+                    best.ws_floats = split_eff > 1 ? split_eff * N : 0;
+                    best_depth = depth;
+                }
+            }
+        }
+    }
+    if (best_cost < 0) return Q8MV_ERR_INVALID_ARG;
+    *out = best;
+    *depth_out = best_depth;
+    return Q8MV_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
 // Plan object
 // ---------------------------------------------------------------------------
 struct q8mv_plan_s {
@@ -428,11 +871,27 @@ struct q8mv_plan_s {
     int KB = 0;
     int device = 0;
     int sm_count = 0;
-    int cps = 1;
+    Occupancy occ;          // resident register-kernel CTAs per SM
+    int max_cluster = 8;    // largest split reduced through a cluster
     int max_vec = 16;       // cap from opts
-    Config cfg[5];          // per weight-load width (16, 8, 4, 2, 1); vec == 0 if unusable
+    bool forced_vec = false;  // opts named a width: use the widest legal one up to it
+    Config cfg[5];          // register kernel, per weight-load width (16, 8, 4, 2, 1); vec == 0 if unusable
+    // TMA-stream kernel (used when enabled and A, W, S are 16-byte aligned)
+    bool async = false;     // async-ring kernel for 16-byte aligned W and S
+    bool overlap = false;   // programmatic dependent launch
+    Config acfg;
+    int adepth = 0;         // async ring depth
+    bool tma = false;
+    TmaConfig tcfg;
+    int tma_stages = 0;
+    size_t tma_smem = 0;
+    MapCache wmaps, smaps, amaps;
+    // device memory owned by the plan
     float *ws = nullptr;
     unsigned *tickets = nullptr;
+    int *err = nullptr;
+    int64_t ws_floats = 0;
+    int64_t n_tickets = 0;
     int64_t ws_bytes = 0;
 };
 
@@ -458,10 +917,48 @@ int q8mv_version(void) { return kVersion; }
 q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t ctas_per_sm,
                                  int32_t vec_bytes, const q8mv_opts_t *opts, q8mv_plan_info_t *info) {
     if (info == nullptr) return Q8MV_ERR_INVALID_ARG;
-    if (opts && opts->kernel != Q8MV_KERNEL_AUTO && opts->kernel != Q8MV_KERNEL_REGS)
+    if (opts && opts->kernel != Q8MV_KERNEL_AUTO && opts->kernel != Q8MV_KERNEL_REGS &&
+        opts->kernel != Q8MV_KERNEL_TMA && opts->kernel != Q8MV_KERNEL_ASYNC)
         return Q8MV_ERR_INVALID_ARG;
+    if (opts && opts->kernel == Q8MV_KERNEL_ASYNC) {
+        Config c;
+        int depth = 0;
+        const q8mv_status_t st = choose_async(K, N, sm_count, opts, &c, &depth);
+        if (st != Q8MV_OK) return st;
+        fill_info(c, sm_count, async_cps(depth, c.tpb), c.ws_floats * static_cast<int64_t>(sizeof(float)), info);
+        info->kernel = Q8MV_KERNEL_ASYNC;
+        info->stages = depth;
+        return Q8MV_OK;
+    }
+    if (opts && opts->kernel == Q8MV_KERNEL_TMA) {
+        if (K < kBlk || N < tmak::kUnitN || N % 16 != 0 || sm_count <= 0 || opts->split_k < 0)
+            return Q8MV_ERR_INVALID_ARG;
+        const TmaConfig t = choose_tma(K, N, sm_count, opts->split_k);
+        std::memset(info, 0, sizeof(*info));
+        info->kernel = Q8MV_KERNEL_TMA;
+        info->vec_bytes = tmak::kLaneCols;
+        info->threads_n = 32;
+        info->groups_k = tmak::kConsumerWarps;
+        info->threads_per_cta = tmak::kThreads;
+        info->split_k = t.split;
+        info->blocks_per_split = t.bps;
+        info->tile_n = tmak::kUnitN;
+        info->grid_x = t.grid;
+        info->grid_y = 1;
+        info->workspace_bytes = t.ws_floats * static_cast<int64_t>(sizeof(float));
+        info->sm_count = sm_count;
+        info->ctas_per_sm = 1;
+        return Q8MV_OK;
+    }
     Config c;
-    const q8mv_status_t st = choose(K, N, sm_count, ctas_per_sm, vec_bytes, opts, &c);
+    // ctas_per_sm counts 256-thread CTAs of the chosen load width; twice as many 128-thread CTAs fit
+    if (ctas_per_sm <= 0) return Q8MV_ERR_INVALID_ARG;
+    Occupancy occ;
+    for (auto &row : occ.cps) {
+        row[0] = 2 * ctas_per_sm;
+        row[1] = ctas_per_sm;
+    }
+    const q8mv_status_t st = choose(K, N, sm_count, occ, vec_bytes, opts, &c);
     if (st != Q8MV_OK) return st;
     fill_info(c, sm_count, ctas_per_sm, c.ws_floats * static_cast<int64_t>(sizeof(float)), info);
     return Q8MV_OK;
@@ -472,12 +969,33 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
     *out = nullptr;
     if (K < 0 || N < 0 || K >= (1LL << 31) || N >= (1LL << 31)) return Q8MV_ERR_INVALID_ARG;
     if (N > 0 && K > ((1LL << 62) / N)) return Q8MV_ERR_INVALID_ARG;
+    const int want_kernel = opts ? opts->kernel : Q8MV_KERNEL_AUTO;
     if (opts) {
-        if (opts->kernel != Q8MV_KERNEL_AUTO && opts->kernel != Q8MV_KERNEL_REGS) return Q8MV_ERR_INVALID_ARG;
+        if (want_kernel != Q8MV_KERNEL_AUTO && want_kernel != Q8MV_KERNEL_REGS && want_kernel != Q8MV_KERNEL_TMA &&
+            want_kernel != Q8MV_KERNEL_ASYNC)
+            return Q8MV_ERR_INVALID_ARG;
+        if (opts->overlap != 0 && opts->overlap != 1) return Q8MV_ERR_INVALID_ARG;
         if (opts->vec_bytes != 0 && !valid_vec(opts->vec_bytes)) return Q8MV_ERR_INVALID_ARG;
-        if (opts->threads_n != 0 && !valid_tn(opts->threads_n)) return Q8MV_ERR_INVALID_ARG;
+        if (opts->threads_n != 0 && !valid_tn(opts->threads_n) && opts->threads_n != 8 && opts->threads_n != 16)
+            return Q8MV_ERR_INVALID_ARG;
         if (opts->split_k < 0 || opts->split_k > kMaxSplit) return Q8MV_ERR_INVALID_ARG;
+        if (opts->cta_threads != 0 && opts->cta_threads != 128 && opts->cta_threads != 256)
+            return Q8MV_ERR_INVALID_ARG;
+        if (opts->stages != 0) {
+            const bool tma_ok = opts->stages >= tmak::kConsumerWarps && opts->stages <= tmak::kMaxStages &&
+                                opts->stages % tmak::kConsumerWarps == 0;
+            if (want_kernel == Q8MV_KERNEL_TMA && !tma_ok) return Q8MV_ERR_INVALID_ARG;
+            if (want_kernel == Q8MV_KERNEL_ASYNC && !valid_async_depth(opts->stages)) return Q8MV_ERR_INVALID_ARG;
+            if (want_kernel != Q8MV_KERNEL_TMA && want_kernel != Q8MV_KERNEL_ASYNC) return Q8MV_ERR_INVALID_ARG;
+        }
     }
+    // the TMA kernel needs 16-byte row pitches and whole boxes along each axis
+    const int64_t KBl = ceil_div(K, kBlk);
+    const int64_t tma_tiles = ceil_div(N, tmak::kUnitN);
+    const bool tma_shape = (N % 16 == 0) && N >= tmak::kUnitN && K >= kBlk && (tma_tiles * KBl) < (1LL << 40);
+    if (want_kernel == Q8MV_KERNEL_TMA && !tma_shape) return Q8MV_ERR_INVALID_ARG;
+    const bool async_shape = (N % 16 == 0) && N >= 16 && K >= 1;
+    if (want_kernel == Q8MV_KERNEL_ASYNC && !async_shape) return Q8MV_ERR_INVALID_ARG;
 
     int prev = 0;
     q8mv_status_t st = cuda_status(cudaGetDevice(&prev));
@@ -500,6 +1018,7 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
     auto fail = [&](q8mv_status_t s) {
         if (p->ws) cudaFree(p->ws);
         if (p->tickets) cudaFree(p->tickets);
+        if (p->err) cudaFree(p->err);
         delete p;
         if (device != prev) cudaSetDevice(prev);
         return s;
@@ -507,41 +1026,98 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
 
     p->K = K;
     p->N = N;
-    p->KB = static_cast<int>(ceil_div(K, kBlk));
+    p->KB = static_cast<int>(KBl);
     p->device = device;
     p->max_vec = (opts && opts->vec_bytes) ? opts->vec_bytes : 16;
+    p->forced_vec = opts && opts->vec_bytes != 0;
+    p->overlap = opts && opts->overlap == 1;
 
-    int major = 0, minor = 0;
+    int major = 0, minor = 0, smem_optin = 0;
     st = cuda_status(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device));
     if (st == Q8MV_OK) st = cuda_status(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device));
     if (st == Q8MV_OK) st = cuda_status(cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, device));
+    if (st == Q8MV_OK)
+        st = cuda_status(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device));
     if (st != Q8MV_OK) return fail(st);
     if (major != 10 || minor != 3) return fail(Q8MV_ERR_UNSUPPORTED_DEVICE);
 
-    // resident CTAs per SM of the widest kernel (the narrower ones use fewer registers)
+    // the library must hold a kernel image for this device
     cudaFuncAttributes fa;
-    st = cuda_status(cudaFuncGetAttributes(&fa, q8mv_regs_kernel<16, true>));
+    st = cuda_status(cudaFuncGetAttributes(&fa, q8mv_regs_kernel<16, true, 256, false>));
     if (st != Q8MV_OK) return fail(st == Q8MV_ERR_CUDA ? Q8MV_ERR_UNSUPPORTED_DEVICE : st);
-    int cps = 1;
-    st = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &cps, q8mv_regs_kernel<16, true>, kCtaThreads,
-        static_cast<size_t>(kStageBlocks) * kBlk * sizeof(float) > 16384
-            ? static_cast<size_t>(kStageBlocks) * kBlk * sizeof(float)
-            : 16384));
+    st = cuda_status(query_occupancy(&p->occ));
     if (st != Q8MV_OK) return fail(st);
-    p->cps = std::max(1, cps);
+    p->max_cluster = query_max_cluster();
+
+    // overrides each kernel family understands (the register kernel is also the
+    // fallback for unaligned pointers, so it is planned whatever kernel is asked for)
+    q8mv_opts_t regs_opts = {};
+    q8mv_opts_t async_opts = {};
+    if (opts) {
+        regs_opts = *opts;
+        async_opts = *opts;
+        if (!valid_tn(opts->threads_n)) regs_opts.threads_n = 0;
+        if (opts->threads_n > 64) async_opts.threads_n = 0;
+        if (want_kernel != Q8MV_KERNEL_REGS && want_kernel != Q8MV_KERNEL_AUTO) regs_opts.threads_n = 0;
+    }
+    if (want_kernel == Q8MV_KERNEL_REGS && opts && opts->threads_n != 0 && !valid_tn(opts->threads_n))
+        return fail(Q8MV_ERR_INVALID_ARG);
+    if (want_kernel == Q8MV_KERNEL_ASYNC && opts && opts->threads_n > 64) return fail(Q8MV_ERR_INVALID_ARG);
 
     int64_t ws_floats = 0, max_tiles = 0;
     for (int i = 0; i < 5; ++i) {
         const int v = kVecs[i];
         if (v > p->max_vec || (N > 0 && N % v != 0)) continue;
         Config c;
-        if (choose(K, N, p->sm_count, p->cps, v, opts, &c) != Q8MV_OK) return fail(Q8MV_ERR_INVALID_ARG);
+        if (choose(K, N, p->sm_count, p->occ, v, &regs_opts, &c, p->max_cluster) != Q8MV_OK)
+            return fail(Q8MV_ERR_INVALID_ARG);
         p->cfg[i] = c;
         ws_floats = std::max(ws_floats, c.ws_floats);
         max_tiles = std::max(max_tiles, c.tiles);
     }
     if (p->cfg[vec_index(1)].vec == 0 && N > 0) return fail(Q8MV_ERR_INVALID_ARG);  // needs the fallback
+
+    // async-ring kernel, on request (the register kernel measures faster on the decode shapes)
+    if (async_shape && want_kernel == Q8MV_KERNEL_ASYNC) {
+        if (choose_async(K, N, p->sm_count, &async_opts, &p->acfg, &p->adepth) != Q8MV_OK)
+            return fail(Q8MV_ERR_INVALID_ARG);
+        const size_t smem = async_smem(p->adepth, p->acfg.tpb);
+        if (smem + 1024 > static_cast<size_t>(smem_optin)) return fail(Q8MV_ERR_UNSUPPORTED_DEVICE);
+        st = cuda_status(cudaFuncSetAttribute(async_kernel(p->adepth, p->acfg.tpb),
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+        if (st != Q8MV_OK) return fail(st);
+        p->async = true;
+        ws_floats = std::max(ws_floats, p->acfg.ws_floats);
+        if (p->acfg.split > 1) max_tiles = std::max(max_tiles, p->acfg.tiles);
+    }
+
+    // TMA-stream kernel: one persistent CTA per SM, ring as deep as shared memory allows
+    if (tma_shape && want_kernel == Q8MV_KERNEL_TMA && encode_fn() != nullptr) {
+        int stages = opts && opts->stages ? opts->stages : 0;
+        if (stages == 0) {
+            for (int r = tmak::kMaxStages; r >= tmak::kConsumerWarps; r -= tmak::kConsumerWarps) {
+                if (tma_smem_bytes(r) + 1024 <= static_cast<size_t>(smem_optin)) {
+                    stages = r;
+                    break;
+                }
+            }
+        }
+        if (stages != 0 && tma_smem_bytes(stages) + 1024 <= static_cast<size_t>(smem_optin)) {
+            p->tma_stages = stages;
+            p->tma_smem = tma_smem_bytes(stages);
+            p->tcfg = choose_tma(K, N, p->sm_count, opts ? opts->split_k : 0);
+            st = cuda_status(cudaFuncSetAttribute(tmak::q8mv_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(p->tma_smem)));
+            if (st != Q8MV_OK) return fail(st);
+            p->tma = true;
+            ws_floats = std::max<int64_t>(ws_floats, p->tcfg.ws_floats);
+            if (p->tcfg.split > 1) max_tiles = std::max(max_tiles, p->tcfg.tiles);
+        } else if (want_kernel == Q8MV_KERNEL_TMA) {
+            return fail(Q8MV_ERR_INVALID_ARG);
+        }
+    } else if (want_kernel == Q8MV_KERNEL_TMA) {
+        return fail(encode_fn() == nullptr ? Q8MV_ERR_UNSUPPORTED_DEVICE : Q8MV_ERR_INVALID_ARG);
+    }
 
     if (ws_floats > 0) {
         st = cuda_status(cudaMalloc(&p->ws, static_cast<size_t>(ws_floats) * sizeof(float)));
@@ -549,10 +1125,15 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
         st = cuda_status(cudaMalloc(&p->tickets, static_cast<size_t>(max_tiles) * sizeof(unsigned)));
         if (st != Q8MV_OK) return fail(st);
         st = cuda_status(cudaMemset(p->tickets, 0, static_cast<size_t>(max_tiles) * sizeof(unsigned)));
-        if (st == Q8MV_OK) st = cuda_status(cudaDeviceSynchronize());
         if (st != Q8MV_OK) return fail(st);
     }
-    p->ws_bytes = ws_floats * static_cast<int64_t>(sizeof(float)) + (ws_floats > 0 ? max_tiles * 4 : 0);
+    st = cuda_status(cudaMalloc(&p->err, sizeof(int)));
+    if (st == Q8MV_OK) st = cuda_status(cudaMemset(p->err, 0, sizeof(int)));
+    if (st == Q8MV_OK) st = cuda_status(cudaDeviceSynchronize());
+    if (st != Q8MV_OK) return fail(st);
+    p->ws_floats = ws_floats;
+    p->n_tickets = ws_floats > 0 ? max_tiles : 0;
+    p->ws_bytes = ws_floats * static_cast<int64_t>(sizeof(float)) + p->n_tickets * 4 + 4;
 
     if (device != prev) cudaSetDevice(prev);
     *out = p;
@@ -561,16 +1142,43 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
 
 q8mv_status_t q8mv_plan_info(q8mv_plan_t p, q8mv_plan_info_t *info) {
     if (p == nullptr || info == nullptr) return Q8MV_ERR_INVALID_ARG;
-    for (int i = 0; i < 5; ++i) {
-        if (p->cfg[i].vec != 0) {
-            fill_info(p->cfg[i], p->sm_count, p->cps, p->ws_bytes, info);
-            return Q8MV_OK;
-        }
-    }
     std::memset(info, 0, sizeof(*info));
+    if (p->async) {
+        fill_info(p->acfg, p->sm_count, async_cps(p->adepth, p->acfg.tpb), p->ws_bytes, info);
+        info->kernel = Q8MV_KERNEL_ASYNC;
+        info->stages = p->adepth;
+        info->overlap = p->overlap ? 1 : 0;
+        return Q8MV_OK;
+    }
+    if (p->tma) {
+        info->kernel = Q8MV_KERNEL_TMA;
+        info->vec_bytes = tmak::kLaneCols;
+        info->threads_n = 32;
+        info->groups_k = tmak::kConsumerWarps;
+        info->threads_per_cta = tmak::kThreads;
+        info->split_k = p->tcfg.split;
+        info->blocks_per_split = p->tcfg.bps;
+        info->stages = p->tma_stages;
+        info->tile_n = tmak::kUnitN;
+        info->grid_x = p->tcfg.grid;
+        info->grid_y = 1;
+        info->workspace_bytes = p->ws_bytes;
+        info->sm_count = p->sm_count;
+        info->ctas_per_sm = 1;
+        return Q8MV_OK;
+    }
+    int idx = -1;
+    for (int i = 0; i < 5; ++i)
+        if (p->cfg[i].vec != 0 && (idx < 0 || (!p->forced_vec && p->cfg[i].cost_us < p->cfg[idx].cost_us))) idx = i;
+    if (idx >= 0) {
+        fill_info(p->cfg[idx], p->sm_count, p->occ.get(vec_idx_of(p->cfg[idx].vec), p->cfg[idx].tpb), p->ws_bytes,
+                  info);
+        info->overlap = p->overlap ? 1 : 0;
+        return Q8MV_OK;
+    }
     info->kernel = Q8MV_KERNEL_REGS;
     info->sm_count = p->sm_count;
-    info->ctas_per_sm = p->cps;
+    info->ctas_per_sm = p->occ.get(0, 256);
     return Q8MV_OK;
 }
 
@@ -578,6 +1186,80 @@ static bool overlaps(const void *a, int64_t a_bytes, const void *b, int64_t b_by
     if (a_bytes <= 0 || b_bytes <= 0) return false;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
     return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
+}
+
+static q8mv_status_t run_tma(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
+                             cudaStream_t stream) {
+    const CUtensorMap *mw = p->wmaps.find(W);
+    if (mw == nullptr) {
+        CUtensorMap *m = p->wmaps.slot(W);
+        if (!encode_w(m, W, p->K, p->N)) return Q8MV_ERR_CUDA;
+        p->wmaps.commit(W);
+        mw = m;
+    }
+    const CUtensorMap *ms = p->smaps.find(S);
+    if (ms == nullptr) {
+        CUtensorMap *m = p->smaps.slot(S);
+        if (!encode_s(m, S, p->KB, p->N)) return Q8MV_ERR_CUDA;
+        p->smaps.commit(S);
+        ms = m;
+    }
+    const CUtensorMap *ma = p->amaps.find(A);
+    if (ma == nullptr) {
+        CUtensorMap *m = p->amaps.slot(A);
+        if (!encode_a(m, A, p->K)) return Q8MV_ERR_CUDA;
+        p->amaps.commit(A);
+        ma = m;
+    }
+    tmak::Params prm;
+    prm.C = C;
+    prm.ws = p->ws;
+    prm.tickets = p->tickets;
+    prm.err = p->err;
+    prm.N = p->N;
+    prm.KB = p->KB;
+    prm.tiles = p->tcfg.tiles;
+    prm.items = p->tcfg.items;
+    prm.split = p->tcfg.split;
+    prm.bps = p->tcfg.bps;
+    prm.grid = p->tcfg.grid;
+    prm.stages = p->tma_stages;
+    prm.wait_ns = tmak::kWaitNs;
+    tmak::q8mv_tma_kernel<<<p->tcfg.grid, tmak::kThreads, p->tma_smem, stream>>>(*mw, *ms, *ma, prm);
+    return cuda_status(cudaGetLastError());
+}
+
+static q8mv_status_t run_async(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
+                               cudaStream_t stream) {
+    const Config &c = p->acfg;
+    asyk::Params prm;
+    prm.A = A;
+    prm.W = W;
+    prm.S = S;
+    prm.C = C;
+    prm.ws = p->ws;
+    prm.tickets = p->tickets;
+    prm.K = p->K;
+    prm.N = p->N;
+    prm.KB = p->KB;
+    prm.tn = c.tn;
+    prm.tn_log2 = log2_pow2(c.tn);
+    prm.gk = c.gk;
+    prm.split = c.split;
+    prm.bps = c.bps;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(c.tiles), static_cast<unsigned>(c.split));
+    cfg.blockDim = dim3(static_cast<unsigned>(c.tpb));
+    cfg.dynamicSmemBytes = async_smem(p->adepth, c.tpb);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p->overlap) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cuda_status(cudaLaunchKernelEx(&cfg, async_kernel(p->adepth, c.tpb), prm));
 }
 
 q8mv_status_t q8mv_run(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
@@ -600,16 +1282,20 @@ q8mv_status_t q8mv_run(q8mv_plan_t p, const float *A, const int8_t *W, const flo
         overlaps(C, c_bytes, S, 4 * static_cast<int64_t>(p->KB) * N))
         return Q8MV_ERR_INVALID_ARG;
 
-    // widest weight load that N, W's address and the plan's cap allow
     const uintptr_t waddr = reinterpret_cast<uintptr_t>(W);
     const uintptr_t saddr = reinterpret_cast<uintptr_t>(S);
+    const uintptr_t aaddr = reinterpret_cast<uintptr_t>(A);
+    if (p->async && waddr % 16 == 0 && saddr % 16 == 0) return run_async(p, A, W, S, C, stream);
+    if (p->tma && waddr % 16 == 0 && saddr % 16 == 0 && aaddr % 16 == 0) return run_tma(p, A, W, S, C, stream);
+
+    // register kernel: of the weight-load widths that N, W's address and the
+    // plan's cap allow, the one the planner expects to be fastest
     int idx = -1;
     for (int i = 0; i < 5; ++i) {
         const int v = kVecs[i];
         if (p->cfg[i].vec == 0) continue;
         if (waddr % static_cast<uintptr_t>(v) != 0) continue;
-        idx = i;
-        break;
+        if (idx < 0 || (!p->forced_vec && p->cfg[i].cost_us < p->cfg[idx].cost_us)) idx = i;
     }
     if (idx < 0) return Q8MV_ERR_INVALID_ARG;
     const Config &c = p->cfg[idx];
@@ -631,9 +1317,32 @@ q8mv_status_t q8mv_run(q8mv_plan_t p, const float *A, const int8_t *W, const flo
     prm.split = c.split;
     prm.bps = c.bps;
 
-    const dim3 grid(static_cast<unsigned>(c.tiles), static_cast<unsigned>(c.split));
-    kernel_for(c.vec, svec)<<<grid, kCtaThreads, smem_bytes(c), stream>>>(prm);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_regs(c, svec, smem_bytes(c), prm, stream, p->overlap));
+}
+
+q8mv_status_t q8mv_check(q8mv_plan_t p, int32_t *device_error) {
+    if (p == nullptr || device_error == nullptr) return Q8MV_ERR_INVALID_ARG;
+    *device_error = 0;
+    int prev = 0;
+    q8mv_status_t st = cuda_status(cudaGetDevice(&prev));
+    if (st != Q8MV_OK) return st;
+    if (prev != p->device) {
+        st = cuda_status(cudaSetDevice(p->device));
+        if (st != Q8MV_OK) return st;
+    }
+    int word = 0;
+    st = cuda_status(cudaDeviceSynchronize());
+    if (st == Q8MV_OK) st = cuda_status(cudaMemcpy(&word, p->err, sizeof(int), cudaMemcpyDeviceToHost));
+    if (st == Q8MV_OK && word != 0) {
+        // an interrupted launch may have left counters behind: start clean
+        st = cuda_status(cudaMemset(p->err, 0, sizeof(int)));
+        if (st == Q8MV_OK && p->tickets)
+            st = cuda_status(cudaMemset(p->tickets, 0, static_cast<size_t>(p->n_tickets) * sizeof(unsigned)));
+        if (st == Q8MV_OK) st = cuda_status(cudaDeviceSynchronize());
+    }
+    *device_error = word;
+    if (prev != p->device) cudaSetDevice(prev);
+    return st;
 }
 
 q8mv_status_t q8mv_destroy(q8mv_plan_t p) {
@@ -644,6 +1353,7 @@ q8mv_status_t q8mv_destroy(q8mv_plan_t p) {
     q8mv_status_t st = cuda_status(cudaDeviceSynchronize());
     if (p->ws) cudaFree(p->ws);
     if (p->tickets) cudaFree(p->tickets);
+    if (p->err) cudaFree(p->err);
     if (prev != p->device) cudaSetDevice(prev);
     delete p;
     return st;
@@ -658,7 +1368,7 @@ q8mv_status_t q8mv_destroy(q8mv_plan_t p) {
 // the register kernel's split-K scratch lives in one static device array of
 // this library instead of a plan's workspace.  Layout of the array:
 //   [0, 64 KiB)        one u32 arrival counter per column tile
-//   [64 KiB, 4 MiB)    split_k x N f32 partial sums
+//   [64 KiB, 2 MiB)    split_k x N f32 partial sums
 // The host never dereferences the array's name: it is a host-side stand-in
 // for the symbol, so the device address is looked up with
 // cudaGetSymbolAddress, once per device, with that device current.
@@ -677,7 +1387,8 @@ struct NoallocDevice {
     bool supported = false;
     unsigned char *scratch = nullptr;  // device address of g_noalloc_scratch on this device
     int sm_count = 0;
-    int cps = 1;
+    Occupancy occ;   // resident register-kernel CTAs per SM
+    int max_cluster = 8;
 };
 
 NoallocDevice g_noalloc_devices[kNoallocMaxDevices];
@@ -702,14 +1413,12 @@ void noalloc_setup(NoallocDevice &d, int device) {
         return;
     }
     d.scratch = static_cast<unsigned char *>(addr);
-    int cps = 1;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cps, q8mv_regs_kernel<16, true>, kCtaThreads,
-                                                      static_cast<size_t>(16384));
+    e = query_occupancy(&d.occ);
     if (e != cudaSuccess) {
         d.err = e;
         return;
     }
-    d.cps = std::max(1, cps);
+    d.max_cluster = query_max_cluster();
 }
 
 }  // namespace
@@ -739,22 +1448,24 @@ extern "C" q8mv_status_t q8mv_run_noalloc(int64_t K, int64_t N, const float *A, 
     if (overlaps(C, c_bytes, A, 4 * K) || overlaps(C, c_bytes, W, K * N) || overlaps(C, c_bytes, S, 4 * KB * N))
         return Q8MV_ERR_INVALID_ARG;
 
-    // the widest weight load N and W's address allow, as q8mv_run picks it
+    // the register-kernel configuration q8mv_run would use for these pointers:
+    // the cheapest of the weight-load widths that N and W's address allow
     const uintptr_t waddr = reinterpret_cast<uintptr_t>(W);
-    int vec = 1;
-    for (int i = 0; i < 5; ++i) {
-        if (N % kVecs[i] == 0 && waddr % static_cast<uintptr_t>(kVecs[i]) == 0) {
-            vec = kVecs[i];
-            break;
-        }
-    }
     Config c;
-    st = choose(K, N, d.sm_count, d.cps, vec, nullptr, &c);
-    if (st != Q8MV_OK) return st;
+    bool have = false;
+    for (int i = 0; i < 5; ++i) {
+        if (N % kVecs[i] != 0 || waddr % static_cast<uintptr_t>(kVecs[i]) != 0) continue;
+        Config ci;
+        st = choose(K, N, d.sm_count, d.occ, kVecs[i], nullptr, &ci, d.max_cluster);
+        if (st != Q8MV_OK) return st;
+        if (!have || ci.cost_us < c.cost_us) c = ci;
+        have = true;
+    }
+    if (!have) return Q8MV_ERR_INVALID_ARG;
 
     float *ws = nullptr;
     unsigned *tickets = nullptr;
-    if (c.split > 1) {
+    if (c.split > 1 && !c.cluster) {
         const size_t counter_bytes = static_cast<size_t>(c.tiles) * sizeof(unsigned);
         const size_t partial_bytes = static_cast<size_t>(c.split) * static_cast<size_t>(N) * sizeof(float);
         if (counter_bytes > kNoallocCounterBytes || partial_bytes > kNoallocBytes - kNoallocCounterBytes)
@@ -783,7 +1494,5 @@ extern "C" q8mv_status_t q8mv_run_noalloc(int64_t K, int64_t N, const float *A, 
     prm.gk = c.gk;
     prm.split = c.split;
     prm.bps = c.bps;
-    const dim3 grid(static_cast<unsigned>(c.tiles), static_cast<unsigned>(c.split));
-    kernel_for(c.vec, svec)<<<grid, kCtaThreads, smem_bytes(c), stream>>>(prm);
-    return cuda_status(cudaGetLastError());
+    return cuda_status(launch_regs(c, svec, smem_bytes(c), prm, stream, false));
 }

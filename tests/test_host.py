@@ -68,12 +68,18 @@ def test_plan_rejects_bad_sizes_before_touching_a_device(q8):
     assert lib.q8mv_plan(ctypes.byref(h), 10, -1, -1, None) == q8.Q8MV_ERR_INVALID_ARG
     assert lib.q8mv_plan(ctypes.byref(h), 1 << 31, 10, -1, None) == q8.Q8MV_ERR_INVALID_ARG
     assert lib.q8mv_plan(None, 10, 10, -1, None) == q8.Q8MV_ERR_INVALID_ARG
-    bad = q8.Opts(0, 3, 0, 0)  # 3-byte loads do not exist
+    bad = q8.Opts(0, 3, 0, 0, 0)  # 3-byte loads do not exist
     assert lib.q8mv_plan(ctypes.byref(h), 10, 12, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
-    bad = q8.Opts(0, 0, 48, 0)
+    bad = q8.Opts(0, 0, 48, 0, 0)
     assert lib.q8mv_plan(ctypes.byref(h), 10, 12, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
-    bad = q8.Opts(7, 0, 0, 0)
+    bad = q8.Opts(7, 0, 0, 0, 0)
     assert lib.q8mv_plan(ctypes.byref(h), 10, 12, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+    bad = q8.Opts(2, 0, 0, 0, 12)  # ring depth must be a multiple of 8
+    assert lib.q8mv_plan(ctypes.byref(h), 10, 12, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+    bad = q8.Opts(0, 0, 0, 0, 0, 2)  # overlap is 0 or 1
+    assert lib.q8mv_plan(ctypes.byref(h), 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+    bad = q8.Opts(2, 0, 0, 0, 0)  # the TMA kernel cannot stream N = 12
+    assert lib.q8mv_plan(ctypes.byref(h), 64, 12, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
 
 
 def test_run_and_info_reject_null_plan(q8):
@@ -82,6 +88,8 @@ def test_run_and_info_reject_null_plan(q8):
     info = q8.PlanInfo()
     assert lib.q8mv_plan_info(None, ctypes.byref(info)) == q8.Q8MV_ERR_INVALID_ARG
     assert lib.q8mv_destroy(None) == q8.Q8MV_OK
+    word = ctypes.c_int32(7)
+    assert lib.q8mv_check(None, ctypes.byref(word)) == q8.Q8MV_ERR_INVALID_ARG
 
 
 def test_plan_without_gpu_reports_unsupported_device(q8):
@@ -120,7 +128,7 @@ def test_planner_covers_every_column_and_block(q8, K, N):
         for vec in legal_vecs(N):
             c = q8.choose_config(K, N, sms, 1, vec)
             assert c["vec_bytes"] == vec
-            assert c["threads_n"] * c["groups_k"] == c["threads_per_cta"] == 256
+            assert c["threads_n"] * c["groups_k"] == c["threads_per_cta"] in (128, 256)
             assert c["tile_n"] == c["threads_n"] * vec
             assert c["grid_x"] * c["tile_n"] >= N
             assert (c["grid_x"] - 1) * c["tile_n"] < max(N, 1)
@@ -130,17 +138,20 @@ def test_planner_covers_every_column_and_block(q8, K, N):
                 assert c["split_k"] * c["blocks_per_split"] >= KB
                 assert (c["split_k"] - 1) * c["blocks_per_split"] < KB
             assert c["split_k"] <= 65535
-            if c["split_k"] > 1:
+            if c["split_k"] > 1 and not c["cluster"]:
                 assert c["workspace_bytes"] == 4 * c["split_k"] * N
             else:
                 assert c["workspace_bytes"] == 0
+            if c["cluster"]:
+                assert 2 <= c["split_k"] <= 8 and vec in (16, 8)
 
 
 def test_planner_fills_the_gpu_for_the_attention_projection(q8):
-    # 4096 x 4096 has only 8 tiles of 512 columns: split-K must spread it over the SMs
+    # 4096 x 4096 is 16 MiB of weights: split-K must spread it over the SMs, and a
+    # split that fits a cluster is summed through distributed shared memory
     c = q8.choose_config(4096, 4096, 152, 1, 16)
     assert c["grid_x"] * c["grid_y"] >= 128
-    assert c["split_k"] > 1
+    assert c["split_k"] > 1 and c["cluster"] == 1 and c["workspace_bytes"] == 0
 
 
 def test_planner_honours_overrides(q8):
@@ -158,3 +169,49 @@ def test_planner_rejects_illegal_requests(q8):
         q8.choose_config(64, 256, 0, 1, 16)
     with pytest.raises(q8.Q8mvError):
         q8.choose_config(64, 256, 152, 1, 16, threads_n=96)
+
+
+TMA_SHAPES = [(4096, 4096), (4096, 11008), (11008, 4096), (8192, 28672), (4100, 128256),
+              (32, 256), (33, 272), (100000, 256), (64, 1 << 20)]
+
+
+@pytest.mark.parametrize("K,N", TMA_SHAPES)
+def test_tma_planner_covers_and_balances(q8, K, N):
+    KB = (K + 31) // 32
+    tiles = -(-N // 256)
+    for sms in (148, 152, 160):
+        c = q8.choose_config(K, N, sms, 0, 0, kernel=q8.KERNEL_TMA)
+        assert c["kernel"] == q8.KERNEL_TMA and c["tile_n"] == 256 and c["threads_per_cta"] == 288
+        split, bps = c["split_k"], c["blocks_per_split"]
+        assert split * bps >= KB and (split - 1) * bps < KB  # every block in exactly one K range
+        items = tiles * split
+        assert c["grid_x"] == min(sms, items)
+        assert c["workspace_bytes"] == (4 * split * N if split > 1 else 0)
+        # the busiest CTA streams at most ~6% more units than an even share (or one item)
+        busiest = -(-items // c["grid_x"]) * bps
+        assert busiest <= max(1.06 * tiles * KB / c["grid_x"], bps) + bps
+
+
+def test_tma_planner_rejects_shapes_it_cannot_stream(q8):
+    for K, N in ((31, 4096), (4096, 200), (4096, 128)):
+        with pytest.raises(q8.Q8mvError):
+            q8.choose_config(K, N, 152, 0, 0, kernel=q8.KERNEL_TMA)
+
+
+@pytest.mark.parametrize("K,N", [(4096, 4096), (4096, 11008), (11008, 4096), (8192, 28672), (4100, 128256),
+                                 (1, 16), (33, 48), (100000, 256)])
+def test_async_planner_covers_every_block(q8, K, N):
+    KB = (K + 31) // 32
+    for sms in (148, 152, 160):
+        c = q8.choose_config(K, N, sms, 0, 0, kernel=q8.KERNEL_ASYNC)
+        assert c["kernel"] == q8.KERNEL_ASYNC and c["vec_bytes"] == 16 and c["threads_per_cta"] in (128, 256)
+        assert c["threads_n"] in (8, 16, 32, 64) and c["tile_n"] == 16 * c["threads_n"]
+        assert c["stages"] in (2, 3, 4, 6)
+        assert c["grid_x"] * c["tile_n"] >= N and (c["grid_x"] - 1) * c["tile_n"] < N
+        assert c["blocks_per_split"] <= 128  # the CTA's activations fit in shared memory
+        assert c["split_k"] * c["blocks_per_split"] >= KB and (c["split_k"] - 1) * c["blocks_per_split"] < KB
+
+
+def test_async_planner_rejects_unaligned_rows(q8):
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config(64, 200, 152, 0, 0, kernel=q8.KERNEL_ASYNC)

@@ -20,7 +20,7 @@ from gpu_util import assert_close
 
 pytestmark = pytest.mark.gpu
 
-SCRATCH_BYTES = 4 * 1024 * 1024
+SCRATCH_BYTES = 2 * 1024 * 1024
 COUNTER_BYTES = 64 * 1024
 ERR_SCRATCH_TOO_SMALL = 5
 
@@ -81,22 +81,29 @@ def test_noalloc_matches_plan_entry_point_twice(q8, orc, name, w_offset):
 def test_noalloc_rejects_a_shape_whose_scratch_does_not_fit(q8):
     import torch
 
-    # the planner's choice for this shape needs more partial sums than the
-    # static array holds; buffers are real and full-size all the same
-    K, N = 16384, 131072
-    probe = q8.Plan(64, 64)
-    cfg = q8.choose_config(K, N, probe.info["sm_count"], probe.info["ctas_per_sm"], 16)
-    probe.close()
-    assert cfg["split_k"] > 1 and cfg["split_k"] * N * 4 > SCRATCH_BYTES - COUNTER_BYTES
+    # With W one byte off 16-byte alignment only 1-byte loads apply, and their
+    # split-K partial sums go through the scratch.  A plan forced to 1-byte
+    # loads shows the configuration the entry point picks for such a W; take
+    # the first shape whose partial sums would overflow the static array.
+    chosen = None
+    for K, N in ((4096, 4096), (2048, 8192), (1024, 16384), (16384, 16384), (4096, 65536)):
+        info = q8.Plan(K, N, vec_bytes=1).info
+        if info["split_k"] > 1 and not info["cluster"] and info["split_k"] * N * 4 > SCRATCH_BYTES - COUNTER_BYTES:
+            chosen = (K, N)
+            break
+    assert chosen is not None, "no candidate shape needs more scratch than the static array"
+    K, N = chosen
     dev = torch.device("cuda")
+    # buffers are real and full-size all the same
     A = torch.zeros((1, K), device=dev)
-    W = torch.empty((K, N), dtype=torch.int8, device=dev)
+    wbuf = torch.empty(K * N + 1, dtype=torch.int8, device=dev)
+    W = wbuf[1:].view(K, N)
     S = torch.zeros(((K + 31) // 32, N), device=dev)
     C = torch.zeros((1, N), device=dev)
     assert run_noalloc(q8, A, W, S, C) == ERR_SCRATCH_TOO_SMALL
     text = q8.library().q8mv_status_string(ERR_SCRATCH_TOO_SMALL).decode()
     assert "scratch" in text
-    del A, W, S, C
+    del A, W, wbuf, S, C
     torch.cuda.empty_cache()
 
 
