@@ -217,8 +217,15 @@ __device__ __forceinline__ void load_w_volatile(const int8_t *p, uint32_t (&w)[(
     }
 }
 
+// Narrow loads keep a block in at most 64 registers, so those variants are held
+// to 128 registers a thread: two 256-thread or four 128-thread CTAs per SM.
+template <int V, int TPB>
+constexpr int regs_min_blocks() {
+    return V >= 16 ? 1 : (TPB == 256 ? 2 : 4);
+}
+
 template <int V, bool SVEC, int TPB, bool CLUSTER>
-__global__ void __launch_bounds__(TPB, 1) q8mv_regs_kernel(const Params p) {
+__global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kernel(const Params p) {
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_is_last;
     constexpr int VW = (V + 3) / 4;
@@ -235,14 +242,17 @@ __global__ void __launch_bounds__(TPB, 1) q8mv_regs_kernel(const Params p) {
     const int b_begin = blockIdx.y * p.bps;
     const int b_end = min(p.KB, b_begin + p.bps);
 
-    // the first block of this thread, if it is whole, is loaded right away
+    // the first block of this thread, if it is whole, is loaded right away,
+    // weights and scales
     uint32_t w[kBlk][VW];
+    float s[V];
     int b = b_begin + gk_i;
     bool prefetched = false;
     if (active && b < b_end && static_cast<int64_t>(b + 1) * kBlk <= p.K) {
         const int8_t *w_ptr = p.W + static_cast<int64_t>(b) * kBlk * p.N + n0;
 #pragma unroll
         for (int r = 0; r < kBlk; ++r) load_w_volatile<V>(w_ptr + r * p.N, w[r]);
+        load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
         prefetched = true;
     }
     pdl_launch_dependents();
@@ -271,6 +281,7 @@ __global__ void __launch_bounds__(TPB, 1) q8mv_regs_kernel(const Params p) {
 #pragma unroll
             for (int j = 0; j < V; ++j) part[j] = 0.0f;
 
+            const bool had_prefetch = prefetched;
             if (rows == kBlk) {
                 // whole block: all 32 row loads are issued before the arithmetic
                 if (!prefetched) {
@@ -294,17 +305,32 @@ __global__ void __launch_bounds__(TPB, 1) q8mv_regs_kernel(const Params p) {
                     fma_row<V>(a_blk[r], wr, part);
                 }
             }
-            float s[V];
-            load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
+            if (!had_prefetch) load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
             fold_scale<V>(part, s, acc);
         }
     }
 
-    // sum the K groups of this CTA in group order
-    __syncthreads();
-    float *red = smem;  // [gk][tile_cols]
+    // sum the K groups of this CTA: first the groups that share a warp, by a
+    // butterfly of shuffles over the lane bits that number them (each pairwise
+    // sum is commutative, so every lane ends with the same bits), then the
+    // warps' rows in shared memory in row order
+    const int lane = tid & 31;
+    int rows = p.gk;       // rows of partial sums left for shared memory
+    int row = gk_i;
+    if (p.tn < 32) {
+        for (int off = p.tn; off < 32; off <<= 1) {
 #pragma unroll
-    for (int j = 0; j < V; ++j) red[gk_i * tile_cols + tn_i * V + j] = acc[j];
+            for (int j = 0; j < V; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
+        }
+        rows = TPB / 32;
+        row = tid >> 5;
+    }
+    __syncthreads();
+    float *red = smem;  // [rows][tile_cols]
+    if (p.tn >= 32 || lane < p.tn) {
+#pragma unroll
+        for (int j = 0; j < V; ++j) red[row * tile_cols + tn_i * V + j] = acc[j];
+    }
     __syncthreads();
 
     if constexpr (CLUSTER) {
@@ -313,10 +339,10 @@ __global__ void __launch_bounds__(TPB, 1) q8mv_regs_kernel(const Params p) {
         // barrier CTA r adds up slice r of the columns over all the cluster's
         // CTAs, in rank order, reading their shared memory directly.
         namespace cg = cooperative_groups;
-        float *mine = smem + p.gk * tile_cols;  // [tile_cols]
+        float *mine = smem + rows * tile_cols;  // [tile_cols]
         for (int c = tid; c < tile_cols; c += TPB) {
             float v = red[c];
-            for (int g = 1; g < p.gk; ++g) v += red[g * tile_cols + c];
+            for (int g = 1; g < rows; ++g) v += red[g * tile_cols + c];
             mine[c] = v;
         }
         cg::cluster_group cluster = cg::this_cluster();
@@ -339,7 +365,7 @@ __global__ void __launch_bounds__(TPB, 1) q8mv_regs_kernel(const Params p) {
         const int64_t n = col0 + c;
         if (n >= p.N) break;
         float v = red[c];
-        for (int g = 1; g < p.gk; ++g) v += red[g * tile_cols + c];
+        for (int g = 1; g < rows; ++g) v += red[g * tile_cols + c];
         if (split)
             p.ws[static_cast<int64_t>(blockIdx.y) * p.N + n] = v;
         else
@@ -1316,7 +1342,6 @@ q8mv_status_t q8mv_run(q8mv_plan_t p, const float *A, const int8_t *W, const flo
     prm.gk = c.gk;
     prm.split = c.split;
     prm.bps = c.bps;
-
     return cuda_status(launch_regs(c, svec, smem_bytes(c), prm, stream, p->overlap));
 }
 
