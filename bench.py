@@ -188,8 +188,10 @@ def run_ours(args, rank, local_rank, world):
     A, W, S = workloads.make_inputs(wl)
     kernel = {"auto": q8mv.KERNEL_AUTO, "regs": q8mv.KERNEL_REGS, "tma": q8mv.KERNEL_TMA,
               "async": q8mv.KERNEL_ASYNC}[args.kernel]
-    plan = q8mv.Plan(K, N, device=local_rank, kernel=kernel, split_k=args.split, stages=args.stages,
-                     threads_n=args.threads_n, overlap=int(args.overlap), cta_threads=args.cta_threads)
+    overlap = not args.no_overlap
+    plan_opts = dict(kernel=kernel, split_k=args.split, stages=args.stages, threads_n=args.threads_n,
+                     cta_threads=args.cta_threads)
+    plan = q8mv.Plan(K, N, device=local_rank, overlap=int(overlap), **plan_opts)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0)) or 126 * 1024 * 1024
     # distinct copies so that a copy is reused only after > 2 x L2 of other traffic
@@ -293,6 +295,18 @@ def run_ours(args, rank, local_rank, world):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * N, "steps": e2e_steps,
            "what": "pinned host A, W, S copied in, q8mv_run, C copied out, every step"}
 
+    # the same workload with plain launches, for comparison with the overlapped headline
+    plain = None
+    if overlap:
+        plan_plain = q8mv.Plan(K, N, device=local_rank, overlap=0, **plan_opts)
+        us_plain = time_calls(plan_plain, ptrs, stream, min(args.steps, 20000))
+        pinfo = plan_plain.info
+        plain = {"us_per_call": round(us_plain, 3), "value": round(bytes_per_call / us_plain / 1e3, 2),
+                 "unit": UNIT, "what": "same workload and timing, launched without programmatic dependent launch",
+                 "plan": {k: pinfo[k] for k in ("vec_bytes", "threads_per_cta", "threads_n", "split_k", "cluster",
+                                                "grid_x", "grid_y")}}
+        plan_plain.close()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(A, W, S, bytes_per_call, args.cpu_seconds, wl)
@@ -312,19 +326,51 @@ def run_ours(args, rank, local_rank, world):
                    "bytes_per_call": bytes_per_call,
                    "l2": f"inputs larger than L2: {copies} rotating input copies "
                          f"({copies * bytes_per_call / 1e6:.0f} MB) vs {l2 / 1e6:.0f} MB L2",
-                   "timing": f"CUDA events around graph replays of {chunk} back-to-back calls",
+                   "timing": f"CUDA events around graph replays of {chunk} back-to-back calls"
+                             + (", programmatic dependent launch (each call reads A and writes C only after the "
+                                "previous call completes)" if overlap else ""),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "plan": {k: info[k] for k in ("kernel", "vec_bytes", "threads_per_cta", "threads_n",
                                                  "groups_k", "split_k",
-                                                 "blocks_per_split", "stages", "overlap", "grid_x",
-                                                 "grid_y", "ctas_per_sm")}},
+                                                 "blocks_per_split", "stages", "overlap", "cluster",
+                                                 "grid_x", "grid_y", "ctas_per_sm")}},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "plain_launch": plain,
         "clocks": clocks,
         "gpu_launches": args.steps,
         "wall_s_timed_region": round(wall, 4),
     }
+
+
+def time_calls(plan, ptrs, stream, calls, reps=3):
+    """Microseconds per call of back-to-back graph-captured calls (best of reps)."""
+    import torch
+
+    copies = len(ptrs)
+    chunk = max(copies, (min(GRAPH_CALLS, calls) // copies) * copies)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        s = torch.cuda.current_stream().cuda_stream
+        for i in range(chunk):
+            plan.run_ptr(*ptrs[i % copies], s)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    replays = max(1, calls // chunk)
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(replays):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (replays * chunk)
+        best = us if best is None else min(best, us)
+    return best
 
 
 def cpu_baseline(A, W, S, bytes_per_call, seconds, wl):
@@ -410,8 +456,9 @@ def parse_args(argv=None):
     ap.add_argument("--stages", type=int, default=0, help="plan override: TMA ring depth")
     ap.add_argument("--threads-n", type=int, default=0, help="plan override: threads along N per CTA")
     ap.add_argument("--cta-threads", type=int, default=0, help="plan override: threads per CTA (128 or 256)")
-    ap.add_argument("--overlap", action="store_true",
-                    help="plan option: programmatic dependent launch (weights constant across calls)")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="plain launches instead of programmatic dependent launch (the plan's overlap option, "
+                         "on by default: decode weights are constant across calls)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -431,18 +431,28 @@ struct Occupancy {
 int vec_idx_of(int v) { return v == 16 ? 0 : v == 8 ? 1 : v == 4 ? 2 : v == 2 ? 3 : 4; }
 
 // Cost model, in microseconds, fitted to measurements of this kernel on
-// GB300 over the decode shapes.  The time to stream the bytes is set by the
-// bytes in flight: each resident thread with a block requests 32 rows at
-// once, and between blocks it spends the block's arithmetic (about 0.1 us per
-// byte of load width) with nothing in flight; with about 1.5 us of loaded DRAM
-// latency that gives the achievable bandwidth, capped at 7.2 TB/s.  A partial
-// last wave of CTAs costs as much as a full one.  A split adds its reduction
-// at the end: ~0.3 us through a cluster, ~3 us through the workspace.  The
-// last block's arithmetic is added once.
+// GB300 over the decode shapes (about 1,400 timed configurations).  The time
+// to stream the bytes is set by the bytes in flight: each resident thread with
+// a block requests 32 rows at once, and between blocks it spends the block's
+// arithmetic with nothing in flight; with the loaded DRAM latency that gives
+// the achievable bandwidth, capped at the sustained rate.  A partial last wave
+// of CTAs costs as much as a full one.  A split adds its reduction at the
+// end, through a cluster or (much slower) through the workspace.  The last
+// block's arithmetic is added once.  Launches that overlap the previous
+// kernel (programmatic dependent launch) see more latency and less of the
+// arithmetic on the critical path, hence their own constants.
+struct ModelConsts {
+    double bw;          // bytes per microsecond
+    double lat;         // microseconds
+    double comp;        // microseconds of a block's arithmetic per byte of load width
+    double tail_cluster;
+    double tail_ws;
+};
+constexpr ModelConsts kModelPlain = {7.2e6, 1.5, 0.10, 0.3, 3.0};
+constexpr ModelConsts kModelOverlap = {6.8e6, 2.0, 0.05, 0.6, 3.0};
+
 double model_us(int64_t K, int64_t N, int sm_count, int cps, int vec, int tpb, int tn, int64_t split, int64_t bps,
-                int64_t tiles, bool cluster) {
-    constexpr double kBw = 7.2e6;   // bytes per microsecond
-    constexpr double kLat = 1.5;    // microseconds
+                int64_t tiles, bool cluster, const ModelConsts &m) {
     const int gk = tpb / tn;
     const int64_t ctas = tiles * split;
     const double total = static_cast<double>(ceil_div(K, kBlk)) * kBlk * N * 1.125;
@@ -450,14 +460,14 @@ double model_us(int64_t K, int64_t N, int sm_count, int cps, int vec, int tpb, i
     const double resident = std::min(static_cast<double>(ctas), slots);
     const double busy = static_cast<double>(std::min<int64_t>(gk, bps));
     const int64_t blocks_per_thread = ceil_div(bps, gk);
-    const double t_comp = 0.1 * vec;
-    const double duty = blocks_per_thread <= 1 ? 1.0 : kLat / (kLat + t_comp);
+    const double t_comp = m.comp * vec;
+    const double duty = blocks_per_thread <= 1 ? 1.0 : m.lat / (m.lat + t_comp);
     const double inflight = resident * busy * tn * kBlk * vec * duty;
-    const double bw = std::min(kBw, inflight / kLat);
+    const double bw = std::min(m.bw, inflight / m.lat);
     double t = total / bw;
     const double waves = static_cast<double>(ctas) / slots;
     if (waves > 1.0) t *= std::ceil(waves) / waves;
-    const double tail = split <= 1 ? 0.0 : (cluster ? 0.3 : 3.0);
+    const double tail = split <= 1 ? 0.0 : (cluster ? m.tail_cluster : m.tail_ws);
     return t + tail + t_comp;
 }
 
@@ -501,7 +511,8 @@ q8mv_status_t choose(int64_t K, int64_t N, int sm_count, const Occupancy &occ, i
                 const int64_t ctas = tiles * split_eff;
                 const bool one_wave = ctas <= static_cast<int64_t>(sm_count) * cps;
                 const bool cluster = split_eff > 1 && split_eff <= max_cluster && cluster_capable(vec) && one_wave;
-                const double cost = model_us(K, N, sm_count, cps, vec, tpb, tn, split_eff, bps, tiles, cluster);
+                const double cost = model_us(K, N, sm_count, cps, vec, tpb, tn, split_eff, bps, tiles, cluster,
+                                             (o && o->overlap == 1) ? kModelOverlap : kModelPlain);
                 if (best_cost < 0 || cost < best_cost * (1.0 - 1e-9)) {
                     best_cost = cost;
                     best.cost_us = cost;
