@@ -52,6 +52,8 @@ class Oracle:
         lib.q8mv_oracle_factored.restype = ctypes.c_int
         lib.q8mv_oracle_block_sums.argtypes = [i64, i64, p, p, p]
         lib.q8mv_oracle_block_sums.restype = ctypes.c_int
+        lib.q8mv_oracle_batched.argtypes = [i64, i64, i64, p, p, p, p, p]
+        lib.q8mv_oracle_batched.restype = ctypes.c_int
         self._lib = lib
 
     @staticmethod
@@ -93,6 +95,25 @@ class Oracle:
         if rc != 0:
             raise RuntimeError(f"q8mv_oracle_unfactored returned {rc}")
         return C
+
+    def batched(self, A, W, S):
+        """Return (C, bound), both fp64 [M, N], for the M rows of A [M, K]."""
+        W = np.ascontiguousarray(W, dtype=np.int8)
+        K, N = W.shape
+        A = np.ascontiguousarray(A, dtype=np.float32)
+        if A.ndim != 2 or A.shape[1] != K:
+            raise ValueError(f"A has shape {A.shape}, expected (M, {K})")
+        S = np.ascontiguousarray(S, dtype=np.float32)
+        if S.shape != ((K + 31) // 32, N):
+            raise ValueError(f"S has shape {S.shape}, expected {((K + 31) // 32, N)}")
+        M = A.shape[0]
+        C = np.full((M, N), np.nan, dtype=np.float64)
+        bound = np.full((M, N), np.nan, dtype=np.float64)
+        rc = self._lib.q8mv_oracle_batched(M, K, N, self._ptr(A), self._ptr(W), self._ptr(S),
+                                           self._ptr(C), self._ptr(bound))
+        if rc != 0:
+            raise RuntimeError(f"q8mv_oracle_batched returned {rc}")
+        return C, bound
 
     def block_sums(self, A, W):
         """Return the unscaled block sums, fp64 [KB, N]."""

@@ -147,3 +147,21 @@ int q8mv_oracle_block_sums(int64_t K, int64_t N, const float *A, const int8_t *W
     }
     return 0;
 }
+
+/*
+ * Several activation rows against the same weights: A is [M, K] and C, bound
+ * are [M, N], all row-major.  Row m of C is the block-factored matvec above of
+ * row m of A; rows never mix.  The Q8_0 matvec example page ("The tensors")
+ * defines one activation row; a decode step of M sequences applies it to each.
+ */
+int q8mv_oracle_batched(int64_t M, int64_t K, int64_t N, const float *A, const int8_t *W,
+                        const float *S, double *C, double *bound) {
+    if (M < 0 || K < 0 || N < 0) return -1;
+    if (M > 0 && N > 0 && C == NULL) return -1;
+    if (M > 0 && K > 0 && A == NULL) return -1;
+    for (int64_t m = 0; m < M; ++m) {
+        const int rc = q8mv_oracle_factored(K, N, A + m * K, W, S, C + m * N, bound ? bound + m * N : NULL);
+        if (rc != 0) return rc;
+    }
+    return 0;
+}

@@ -11,7 +11,10 @@ the oracle disagrees with an independent fact:
 - linearity in A and, block by block, in S;
 - exact-integer inputs checked against numpy int64 arithmetic;
 - the factoring identity of "Factoring out the scale" (both forms agree);
-- the scale-row rule printed in "The tensors", read from a golden fixture.
+- the scale-row rule printed in "The tensors", read from a golden fixture;
+- for several activation rows at once: exact rational brute force per row,
+  one-hot rows, a closed form with a different constant per row, and row
+  permutations (rows of C follow rows of A and never mix).
 
 The pins are shared by ``test_oracle_pins.py`` (the real oracle must pass all)
 and ``test_oracle_mutants.py`` (each planted mistake must fail at least one).
@@ -238,6 +241,63 @@ def pin_scale_rows_golden(orc):
         assert np.array_equal(Cu, np.ones(N)), ("unfactored", K, k, b, Cu)
 
 
+def pin_batched_exact_rational(orc):
+    for i, (M, K, N) in enumerate(((2, 5, 3), (3, 33, 4), (5, 70, 3), (4, 32, 1))):
+        rng = _rng(200 + i)
+        A = rng.uniform(-1, 1, size=(M, K)).astype(np.float32)
+        _, W, S = workloads.make_random(K, N, seed=210 + i)
+        W[K - 1, N - 1] = -128
+        C, bound = orc.batched(A, W, S)
+        assert C.shape == (M, N) and bound.shape == (M, N)
+        for m in range(M):
+            exact = exact_matvec(A[m], W, S)
+            mag = exact_abs_sum(A[m], W, S)
+            for n in range(N):
+                tol = 4 * (K + 2) * EPS64 * float(mag[n]) + 1e-300
+                assert abs(C[m, n] - float(exact[n])) <= tol, ("batched", M, K, N, m, n)
+                assert abs(bound[m, n] - float(mag[n])) <= tol, ("batched bound", M, K, N, m, n)
+
+
+def pin_batched_one_hot_rows(orc):
+    K, N = 100, 5
+    ks = (0, 31, 32, 63, 96, 99)  # one row of A per k, last block partial
+    _, W, S = workloads.make_random(K, N, seed=220)
+    A = np.zeros((len(ks), K), np.float32)
+    for m, k in enumerate(ks):
+        A[m, k] = np.float32(m + 1)
+    C, _ = orc.batched(A, W, S)
+    for m, k in enumerate(ks):
+        expect = np.array([(m + 1) * int(W[k, n]) * float(S[k // 32, n]) for n in range(N)])
+        assert np.array_equal(C[m], expect), ("one-hot row", m, k, C[m], expect)
+
+
+def pin_batched_closed_form(orc):
+    for (M, K) in ((3, 1), (4, 33), (7, 4100)):
+        N = 6
+        c = np.arange(1, M + 1, dtype=np.float32) * np.float32(0.5)  # 0.5, 1.0, 1.5, ...
+        A = np.repeat(c[:, None], K, axis=1)
+        W = np.ones((K, N), np.int8)
+        S = np.full((workloads.num_blocks(K), N), np.float32(2.0 ** -5), np.float32)
+        C, _ = orc.batched(A, W, S)
+        expect = (c.astype(np.float64) * K * 2.0 ** -5)[:, None] * np.ones((1, N))
+        assert np.array_equal(C, expect), ("closed form", M, K)
+
+
+def pin_batched_row_permutation(orc):
+    M, K, N = 6, 97, 8
+    rng = _rng(230)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    _, W, S = workloads.make_random(K, N, seed=231)
+    C, bound = orc.batched(A, W, S)
+    perm = np.array([3, 0, 5, 1, 4, 2])
+    Cp, bp = orc.batched(A[perm], W, S)
+    assert np.array_equal(Cp, C[perm]) and np.array_equal(bp, bound[perm])
+    # a row on its own gives the same bits as inside the batch
+    for m in range(M):
+        Cm, bm = orc.factored(A[m:m + 1], W, S)
+        assert np.array_equal(Cm, C[m]) and np.array_equal(bm, bound[m]), m
+
+
 ALL_PINS = [
     pin_exact_rational,
     pin_closed_form_ones,
@@ -250,4 +310,8 @@ ALL_PINS = [
     pin_block_sums,
     pin_empty,
     pin_scale_rows_golden,
+    pin_batched_exact_rational,
+    pin_batched_one_hot_rows,
+    pin_batched_closed_form,
+    pin_batched_row_permutation,
 ]

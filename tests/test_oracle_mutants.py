@@ -38,6 +38,14 @@ MUTANTS = {
                      "        if (bound) bound[n] = 0.0;"),
     "block_sums_missing_mask": ("        if (k_end > K) k_end = K;\n        for (int64_t k = k_begin; k < k_end; ++k) {\n            const double a = (double)A[k];\n            const int8_t *w_row = W + k * N;\n            for (int64_t n = 0; n < N; ++n) p_row[n] += a * (double)w_row[n];",
                                 "        if (k_end > K) k_end = K;\n        for (int64_t k = k_begin; k < k_end; ++k) {\n            const double a = (double)A[k];\n            const int8_t *w_row = W + k * N;\n            for (int64_t n = 0; n < N; ++n) p_row[n] += a * (double)w_row[n] * (k + 1 < k_end);"),
+    "batched_row_stride_n": ("q8mv_oracle_factored(K, N, A + m * K, W, S, C + m * N, bound ? bound + m * N : NULL)",
+                             "q8mv_oracle_factored(K, N, A + m * (N < K ? N : K), W, S, C + m * N, bound ? bound + m * N : NULL)"),
+    "batched_first_row_only": ("q8mv_oracle_factored(K, N, A + m * K, W, S, C + m * N, bound ? bound + m * N : NULL)",
+                               "q8mv_oracle_factored(K, N, A, W, S, C + m * N, bound ? bound + m * N : NULL)"),
+    "batched_rows_reversed": ("q8mv_oracle_factored(K, N, A + m * K, W, S, C + m * N, bound ? bound + m * N : NULL)",
+                              "q8mv_oracle_factored(K, N, A + (M - 1 - m) * K, W, S, C + m * N, bound ? bound + m * N : NULL)"),
+    "batched_skip_last_row": ("for (int64_t m = 0; m < M; ++m) {\n        const int rc",
+                              "for (int64_t m = 0; m + 1 < M; ++m) {\n        const int rc"),
 }
 
 

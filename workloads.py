@@ -147,3 +147,29 @@ def make_integer_exact(K: int, N: int, seed: int, scale_exp: int = 6):
     W = rng.integers(-128, 128, size=(K, N), dtype=np.int8)
     S = np.full((num_blocks(K), N), np.float32(2.0 ** -scale_exp), dtype=np.float32)
     return np.ascontiguousarray(A), np.ascontiguousarray(W), np.ascontiguousarray(S)
+
+
+def make_rows(w: Workload | str, M: int, seed: int | None = None) -> np.ndarray:
+    """M activation rows [M, K] f32 for a batched decode step of workload ``w``.
+
+    The rows are drawn with the workload's activation distribution from their
+    own generator (seed + 7919 * M, so batches of different sizes differ), row
+    after row; the workload's W and S come from ``make_inputs`` unchanged.
+    """
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    base = w.seed if seed is None else seed
+    rng = np.random.Generator(np.random.PCG64(base + 7919 * M))
+    return np.ascontiguousarray(np.concatenate([draw_a(rng, w.K, w.a_dist) for _ in range(M)], axis=0))
+
+
+def make_integer_rows(K: int, M: int, seed: int) -> np.ndarray:
+    """M rows of activations in {-1, 0, 1}: with the exact-integer W and S of
+    ``make_integer_exact`` every row's result is exact in f32 in any order."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return np.ascontiguousarray(rng.integers(-1, 2, size=(M, K)).astype(np.float32))
+
+
+def batched_bytes(K: int, N: int, M: int) -> int:
+    """Bytes one batched call must move at least: W + S once, M rows of A and C."""
+    return K * N + 4 * num_blocks(K) * N + 4 * M * K + 4 * M * N
