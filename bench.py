@@ -3,7 +3,8 @@
 
 One step is one call of the whole path, C = matvec(A, W, S), on the 7B-class
 attention projection (K = 4096, N = 4096) unless ``--workload`` says
-otherwise.  The timed region replays CUDA graphs of back-to-back calls that
+otherwise; with ``--rows M`` a step is one batched call of M activation rows
+against the same weights.  The timed region replays CUDA graphs of back-to-back calls that
 rotate over enough distinct copies of the inputs to exceed twice the L2, so
 every call streams its weights from HBM.
 
@@ -40,7 +41,7 @@ import workloads  # noqa: E402
 
 METRIC = "Q8_0 matvec effective HBM GB/s and % of GB300 peak; µs per call"
 UNIT = "GB/s"
-KERNEL_SRC = os.path.join(ROOT, "q8_matrix_vector_gb300", "csrc", "q8mv.cu")
+CSRC = os.path.join(ROOT, "q8_matrix_vector_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 GRAPH_CALLS = 1000  # calls captured per CUDA graph (rounded to the rotation length)
@@ -96,20 +97,29 @@ def read_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
+def kernel_source_hash(name: str) -> str:
+    with open(os.path.join(CSRC, name), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch from a committed ncu capture, if the kernel is unchanged."""
+def traffic_key(workload: str, rows: int) -> str:
+    return workload if rows == 1 else f"{workload}_m{rows}"
+
+
+def recorded_traffic(key: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    entry = rec.get("workloads", {}).get(workload)
-    if not entry or rec.get("kernel_source_sha256") != kernel_source_hash():
+    entry = rec.get("workloads", {}).get(key)
+    if not entry:
+        return None
+    try:
+        if kernel_source_hash(entry["kernel_source"]) != entry["kernel_source_sha256"]:
+            return None
+    except (OSError, KeyError):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -183,15 +193,18 @@ def run_ours(args, rank, local_rank, world):
     group = init_group(world, "nccl")
     wl = workloads.WORKLOADS[args.workload]
     K, N, KB = wl.K, wl.N, wl.KB
-    bytes_per_call = wl.algorithmic_bytes()
+    M = args.rows
+    bytes_per_call = workloads.batched_bytes(K, N, M)
 
     A, W, S = workloads.make_inputs(wl)
+    if M > 1:
+        A = workloads.make_rows(wl, M)
     kernel = {"auto": q8mv.KERNEL_AUTO, "regs": q8mv.KERNEL_REGS, "tma": q8mv.KERNEL_TMA,
               "async": q8mv.KERNEL_ASYNC}[args.kernel]
     overlap = not args.no_overlap
     plan_opts = dict(kernel=kernel, split_k=args.split, stages=args.stages, threads_n=args.threads_n,
                      cta_threads=args.cta_threads)
-    plan = q8mv.Plan(K, N, device=local_rank, overlap=int(overlap), **plan_opts)
+    plan = q8mv.Plan(K, N, device=local_rank, rows=M, overlap=int(overlap), **plan_opts)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0)) or 126 * 1024 * 1024
     # distinct copies so that a copy is reused only after > 2 x L2 of other traffic
@@ -199,7 +212,7 @@ def run_ours(args, rank, local_rank, world):
     Ah, Wh, Sh = torch.from_numpy(A), torch.from_numpy(W), torch.from_numpy(S)
     bufs = []
     for _ in range(copies):
-        bufs.append((Ah.to(dev), Wh.to(dev), Sh.to(dev), torch.empty((1, N), dtype=torch.float32, device=dev)))
+        bufs.append((Ah.to(dev), Wh.to(dev), Sh.to(dev), torch.empty((M, N), dtype=torch.float32, device=dev)))
     ptrs = [(a.data_ptr(), w.data_ptr(), s.data_ptr(), c.data_ptr()) for a, w, s, c in bufs]
     stream = torch.cuda.Stream(dev)
 
@@ -259,13 +272,13 @@ def run_ours(args, rank, local_rank, world):
     peak, peak_kind = read_hbm_peak()
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} copy bandwidth",
-                "traffic": recorded_traffic(args.workload),
+                "traffic": recorded_traffic(traffic_key(args.workload, M)),
                 "algorithmic_bytes_per_launch": bytes_per_call}
 
     # end to end through the public binding: pinned host inputs in, result out
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     Ap, Wp, Sp = Ah.pin_memory(), Wh.pin_memory(), Sh.pin_memory()
-    Cp = torch.empty((1, N), dtype=torch.float32).pin_memory()
+    Cp = torch.empty((M, N), dtype=torch.float32).pin_memory()
     Ad, Wd, Sd, Cd = bufs[0]
     with torch.cuda.stream(stream):
         for _ in range(2):  # warm-up
@@ -290,15 +303,15 @@ def run_ours(args, rank, local_rank, world):
     e_end.synchronize()
     e_ms = reduce_over_ranks(group, e_start.elapsed_time(e_end), "max", dev)
     e_bytes = reduce_over_ranks(group, float(bytes_per_call) * e2e_steps, "sum", dev)
-    h2d = 4 * K + K * N + 4 * KB * N
+    h2d = 4 * M * K + K * N + 4 * KB * N
     e2e = {"value": round(e_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * N, "steps": e2e_steps,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * M * N, "steps": e2e_steps,
            "what": "pinned host A, W, S copied in, q8mv_run, C copied out, every step"}
 
     # the same workload with plain launches, for comparison with the overlapped headline
     plain = None
     if overlap:
-        plan_plain = q8mv.Plan(K, N, device=local_rank, overlap=0, **plan_opts)
+        plan_plain = q8mv.Plan(K, N, device=local_rank, rows=M, overlap=0, **plan_opts)
         us_plain = time_calls(plan_plain, ptrs, stream, min(args.steps, 20000))
         pinfo = plan_plain.info
         plain = {"us_per_call": round(us_plain, 3), "value": round(bytes_per_call / us_plain / 1e3, 2),
@@ -309,7 +322,7 @@ def run_ours(args, rank, local_rank, world):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(A, W, S, bytes_per_call, args.cpu_seconds, wl)
+        cpu = cpu_baseline(A, W, S, bytes_per_call, args.cpu_seconds, wl, M)
 
     if rank != 0:
         return None
@@ -321,8 +334,9 @@ def run_ours(args, rank, local_rank, world):
         "us_per_call": round(us, 3), "pct_of_peak": round(100.0 * achieved / peak, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: {wl.description}", "K": K, "N": N, "KB": KB,
-                   "weights": "Q8_0: int8 W [K,N], f32 scales [KB,N], f32 A and C",
+        "config": {"workload": f"{wl.name}: {wl.description}" + (f", batched decode of M={M} rows" if M > 1 else ""),
+                   "K": K, "N": N, "KB": KB, "M": M,
+                   "weights": "Q8_0: int8 W [K,N], f32 scales [KB,N], f32 A [M,K] and C [M,N]",
                    "bytes_per_call": bytes_per_call,
                    "l2": f"inputs larger than L2: {copies} rotating input copies "
                          f"({copies * bytes_per_call / 1e6:.0f} MB) vs {l2 / 1e6:.0f} MB L2",
@@ -333,7 +347,8 @@ def run_ours(args, rank, local_rank, world):
                    "plan": {k: info[k] for k in ("kernel", "vec_bytes", "threads_per_cta", "threads_n",
                                                  "groups_k", "split_k",
                                                  "blocks_per_split", "stages", "overlap", "cluster",
-                                                 "grid_x", "grid_y", "ctas_per_sm")}},
+                                                 "grid_x", "grid_y", "ctas_per_sm", "rows_per_pass",
+                                                 "grid_z")}},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -373,22 +388,24 @@ def time_calls(plan, ptrs, stream, calls, reps=3):
     return best
 
 
-def cpu_baseline(A, W, S, bytes_per_call, seconds, wl):
+def cpu_baseline(A, W, S, bytes_per_call, seconds, wl, M=1):
     """The fp64 oracle, as it stands, on the host cores: full calls for ~seconds."""
     import oracle
 
     orc = oracle.load()
-    orc.factored(A, W, S)  # page in
+    run = (lambda: orc.factored(A, W, S)) if M == 1 else (lambda: orc.batched(A, W, S))
+    run()  # page in
     reps, t0 = 0, time.perf_counter()
     while True:
-        orc.factored(A, W, S)
+        run()
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= seconds:
             break
+    rows = "" if M == 1 else f" of M={M} rows"
     return {"value": round(reps * bytes_per_call / dt / 1e9, 4), "unit": UNIT, "cores": 1,
             "kind": "oracle",
-            "sample": f"{reps} full {wl.name} calls (K={wl.K}, N={wl.N}) in {dt:.1f} s, single thread, fp64"}
+            "sample": f"{reps} full {wl.name} calls{rows} (K={wl.K}, N={wl.N}) in {dt:.1f} s, single thread, fp64"}
 
 
 # ----------------------------------------------------------------------------
@@ -402,10 +419,16 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None  # rank 0 alone runs the reference arm
     wl = workloads.WORKLOADS[args.workload]
+    M = args.rows
     A, W, S = workloads.make_inputs(wl)
     orc = oracle.load()
+    if M > 1:
+        A = workloads.make_rows(wl, M)
+        call = orc.batched
+    else:
+        call = orc.factored
     t0 = time.perf_counter()
-    orc.factored(A, W, S)
+    call(A, W, S)
     t_full = time.perf_counter() - t0
     # each step is a bounded sample of the workload: the first n_s columns
     budget = args.reference_seconds
@@ -415,23 +438,24 @@ def run_reference(args, rank, world):
         n_s = max(1, int(wl.N * budget / (total_steps * t_full)))
     Ws = np.ascontiguousarray(W[:, :n_s])
     Ss = np.ascontiguousarray(S[:, :n_s])
-    step_bytes = wl.K * n_s + 4 * wl.KB * n_s + 4 * wl.K + 4 * n_s
+    step_bytes = workloads.batched_bytes(wl.K, n_s, M)
     for _ in range(args.warmup):
-        orc.factored(A, Ws, Ss)
+        call(A, Ws, Ss)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        orc.factored(A, Ws, Ss)
+        call(A, Ws, Ss)
     dt = time.perf_counter() - t0
     value = args.steps * step_bytes / dt / 1e9 if dt > 0 else 0.0
-    sample = (f"first {n_s} of {wl.N} columns of {wl.name} (K={wl.K}) per step, "
-              f"fp64 oracle, single thread")
+    sample = (f"first {n_s} of {wl.N} columns of {wl.name} (K={wl.K}"
+              + (f", M={M} rows" if M > 1 else "") + ") per step, fp64 oracle, single thread")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / max(args.steps, 1), 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: {wl.description}", "K": wl.K, "N": wl.N, "KB": wl.KB},
+        "config": {"workload": f"{wl.name}: {wl.description}" + (f", batched decode of M={M} rows" if M > 1 else ""),
+                   "K": wl.K, "N": wl.N, "KB": wl.KB, "M": M},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -445,6 +469,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=workloads.HEADLINE)
+    ap.add_argument("--rows", type=int, default=1,
+                    help="activation rows per call (batched decode; 1 = the single-row matvec)")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=CPU_BASELINE_SECONDS)
     ap.add_argument("--reference-seconds", type=float, default=60.0,
@@ -464,6 +490,8 @@ def parse_args(argv=None):
         ap.error("--warmup must be at least 3")
     if args.steps < 1:
         ap.error("--steps must be at least 1")
+    if not 1 <= args.rows <= 1 << 19:
+        ap.error("--rows must be in 1 .. 2^19")
     return args
 
 

@@ -111,6 +111,9 @@ typedef struct {
     int64_t workspace_bytes;  /* device workspace the plan owns */
     int32_t sm_count;
     int32_t ctas_per_sm;      /* resident CTAs per SM for the chosen kernel */
+    int32_t rows;             /* activation rows M of the plan (1 for q8mv_plan) */
+    int32_t rows_per_pass;    /* activation rows one CTA serves (1, or 2, 4, 8, 16 when batched) */
+    int64_t grid_z;           /* passes of rows_per_pass rows: ceil(rows / rows_per_pass) */
 } q8mv_plan_info_t;
 
 typedef struct q8mv_plan_s *q8mv_plan_t;
@@ -127,7 +130,31 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device,
                         const q8mv_opts_t *opts);
 
 /*
+ * Batched decode: a plan for C[M,N] = A[M,K] x (W[K,N], S[KB,N]), each row of
+ * C the matvec above of the same row of A (A and C contiguous, row-major:
+ * A[m, k] at m*K + k, C[m, n] at m*N + n).  The Q8_0 matvec example page
+ * ("The tensors") defines one activation row, A[1, K]; here M rows share one
+ * pass over the weights, as a decode step of M sequences does.
+ *
+ * 1 <= M <= 2^19, otherwise INVALID_ARG; the other limits and the ownership
+ * rules are those of q8mv_plan.  M == 1 gives exactly the plan of q8mv_plan.
+ * For M >= 2 the plan uses the batched register kernel: rows are served
+ * 2, 4, 8 or 16 at a time (M rounded up to one of them, or ceil(M/16) passes
+ * of 16 that each stream the weights again).  Accepted overrides: vec_bytes
+ * (8, 4 or 1; 8-byte loads exist for up to 4 rows per pass), threads_n,
+ * split_k, overlap; any other non-zero field gives INVALID_ARG.
+ *
+ * Per element the arithmetic is that of q8mv_plan: exact byte conversion,
+ * the block's 32 products summed in f32 in row order, one scale fold per
+ * block, column and activation row, and split-K partial sums added in range
+ * order, so a row's result does not depend on the other rows.
+ */
+q8mv_status_t q8mv_plan_batched(q8mv_plan_t *out, int64_t M, int64_t K, int64_t N, int device,
+                                const q8mv_opts_t *opts);
+
+/*
  * Enqueue C = matvec(A, W, S) on `stream` (0 = the legacy default stream).
+ * For a batched plan A is [M, K] and C is [M, N] (see q8mv_plan_batched).
  * The plan's device must be current.  A, S and C must be 4-byte aligned;
  * W may have any alignment (narrower loads are used when W, S or N do not
  * allow 16-byte ones).  C must not overlap A, W or S.  Null pointers are
@@ -165,6 +192,16 @@ q8mv_status_t q8mv_plan_info(q8mv_plan_t plan, q8mv_plan_info_t *info);
 q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t ctas_per_sm,
                                  int32_t vec_bytes, const q8mv_opts_t *opts,
                                  q8mv_plan_info_t *info);
+
+/*
+ * Host-only planning for a batched plan of M rows: the configuration
+ * q8mv_plan_batched would pick on a GPU with `sm_count` SMs, where registers
+ * allow `ctas_per_sm` resident CTAs of the batched kernel, with weight loads
+ * of `vec_bytes` (8, 4 or 1, dividing N).  Fills *info.
+ */
+q8mv_status_t q8mv_choose_config_batched(int64_t M, int64_t K, int64_t N, int32_t sm_count,
+                                         int32_t ctas_per_sm, int32_t vec_bytes,
+                                         const q8mv_opts_t *opts, q8mv_plan_info_t *info);
 
 /* Static, human-readable text for a status code. */
 const char *q8mv_status_string(q8mv_status_t status);

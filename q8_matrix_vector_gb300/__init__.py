@@ -1,8 +1,9 @@
 """Q8_0 decode matvec on GB300: Python binding of the q8mv C library.
 
-    C[0, n] = sum_b S[b, n] * sum_{k in block b} A[0, k] * W[k, n]
+    C[m, n] = sum_b S[b, n] * sum_{k in block b} A[m, k] * W[k, n]
 
-(Phobos docs, "Q8_0 matvec" example page, "The tensors".)  This module only
+(Phobos docs, "Q8_0 matvec" example page, "The tensors", for one activation
+row m = 0; a batched plan serves M rows with one pass over W.)  This module only
 marshals arguments: it checks dtypes, shapes and devices of torch tensors and
 passes raw device pointers and the current CUDA stream to ``libq8mv.so``.
 Every step of the computation runs in the library's CUDA kernels; if the
@@ -45,7 +46,8 @@ class PlanInfo(ctypes.Structure):
                 ("overlap", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("tile_n", ctypes.c_int64), ("grid_x", ctypes.c_int64), ("grid_y", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("sm_count", ctypes.c_int32),
-                ("ctas_per_sm", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("rows", ctypes.c_int32),
+                ("rows_per_pass", ctypes.c_int32), ("grid_z", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -70,6 +72,8 @@ def _load() -> ctypes.CDLL:
     i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
     lib.q8mv_plan.argtypes = [ctypes.POINTER(p), i64, i64, ctypes.c_int, ctypes.POINTER(Opts)]
     lib.q8mv_plan.restype = ctypes.c_int
+    lib.q8mv_plan_batched.argtypes = [ctypes.POINTER(p), i64, i64, i64, ctypes.c_int, ctypes.POINTER(Opts)]
+    lib.q8mv_plan_batched.restype = ctypes.c_int
     lib.q8mv_run.argtypes = [p, p, p, p, p, p]
     lib.q8mv_run.restype = ctypes.c_int
     lib.q8mv_check.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
@@ -81,6 +85,9 @@ def _load() -> ctypes.CDLL:
     lib.q8mv_choose_config.argtypes = [i64, i64, i32, i32, i32, ctypes.POINTER(Opts),
                                        ctypes.POINTER(PlanInfo)]
     lib.q8mv_choose_config.restype = ctypes.c_int
+    lib.q8mv_choose_config_batched.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(Opts),
+                                               ctypes.POINTER(PlanInfo)]
+    lib.q8mv_choose_config_batched.restype = ctypes.c_int
     lib.q8mv_status_string.argtypes = [ctypes.c_int]
     lib.q8mv_status_string.restype = ctypes.c_char_p
     lib.q8mv_last_cuda_error.argtypes = []
@@ -115,21 +122,41 @@ def choose_config(K: int, N: int, sm_count: int, ctas_per_sm: int, vec_bytes: in
     return info.as_dict()
 
 
+def choose_config_batched(M: int, K: int, N: int, sm_count: int, ctas_per_sm: int, vec_bytes: int,
+                          **opts) -> dict:
+    """Host-only planner for a batched plan of ``M`` activation rows."""
+    info = PlanInfo()
+    o = _opts(**opts)
+    st = _lib.q8mv_choose_config_batched(M, K, N, sm_count, ctas_per_sm, vec_bytes,
+                                         ctypes.byref(o) if o else None, ctypes.byref(info))
+    if st != Q8MV_OK:
+        raise Q8mvError(st, "q8mv_choose_config_batched")
+    return info.as_dict()
+
+
 def num_blocks(K: int) -> int:
     return (K + BLK - 1) // BLK
 
 
 class Plan:
-    """A q8mv plan for fixed (K, N) on one device; owns the split-K workspace."""
+    """A q8mv plan for fixed (M, K, N) on one device; owns the split-K workspace.
 
-    def __init__(self, K: int, N: int, device: int = -1, **opts):
+    ``rows`` is the number M of activation rows per call (1: the single-row
+    matvec of ``q8mv_plan``; more: ``q8mv_plan_batched``)."""
+
+    def __init__(self, K: int, N: int, device: int = -1, rows: int = 1, **opts):
         self.K, self.N, self.KB = int(K), int(N), num_blocks(int(K))
+        self.M = int(rows)
         handle = ctypes.c_void_p()
         o = _opts(**opts)
-        st = _lib.q8mv_plan(ctypes.byref(handle), self.K, self.N, int(device),
-                            ctypes.byref(o) if o else None)
+        if self.M == 1:
+            st = _lib.q8mv_plan(ctypes.byref(handle), self.K, self.N, int(device),
+                                ctypes.byref(o) if o else None)
+        else:
+            st = _lib.q8mv_plan_batched(ctypes.byref(handle), self.M, self.K, self.N, int(device),
+                                        ctypes.byref(o) if o else None)
         if st != Q8MV_OK:
-            raise Q8mvError(st, f"q8mv_plan(K={K}, N={N})")
+            raise Q8mvError(st, f"q8mv_plan(M={rows}, K={K}, N={N})")
         self._h = handle
         info = PlanInfo()
         st = _lib.q8mv_plan_info(self._h, ctypes.byref(info))
@@ -151,7 +178,7 @@ class Plan:
         """C = matvec(A, W, S) on torch CUDA tensors, enqueued on the current stream."""
         import torch
 
-        _check(A, torch.float32, (1, self.K), "A")
+        _check(A, torch.float32, (self.M, self.K), "A")
         _check(W, torch.int8, (self.K, self.N), "W")
         _check(S, torch.float32, (self.KB, self.N), "S")
         dev = W.device
@@ -159,9 +186,9 @@ class Plan:
             if t.device != dev:
                 raise ValueError(f"{name} is on {t.device}, W is on {dev}")
         if out is None:
-            out = torch.empty((1, self.N), dtype=torch.float32, device=dev)
+            out = torch.empty((self.M, self.N), dtype=torch.float32, device=dev)
         else:
-            _check(out, torch.float32, (1, self.N), "out")
+            _check(out, torch.float32, (self.M, self.N), "out")
             if out.device != dev:
                 raise ValueError(f"out is on {out.device}, W is on {dev}")
         if stream is None:
@@ -199,8 +226,8 @@ def _check(t, dtype, shape, name):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if tuple(t.shape) != tuple(shape) and not (name == "A" and t.dim() == 1 and t.numel() == shape[1]) \
-            and not (name == "out" and t.dim() == 1 and t.numel() == shape[1]):
+    one_row = shape[0] == 1 and name in ("A", "out") and t.dim() == 1 and t.numel() == shape[1]
+    if tuple(t.shape) != tuple(shape) and not one_row:
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -212,15 +239,17 @@ _plans: dict = {}
 
 
 def matvec(A, W, S, out=None):
-    """C[1, N] = Q8_0 matvec of A [1, K] f32 with W [K, N] int8 and S [KB, N] f32.
+    """C[M, N] = Q8_0 matvec of every row of A [M, K] f32 (or [K]) with W [K, N] int8
+    and S [KB, N] f32.
 
-    Plans are cached per (K, N, device).  Runs on the current CUDA stream.
+    Plans are cached per (M, K, N, device).  Runs on the current CUDA stream.
     """
     K, N = W.shape
-    key = (int(K), int(N), W.device.index)
+    M = A.shape[0] if A.dim() == 2 else 1
+    key = (int(M), int(K), int(N), W.device.index)
     plan = _plans.get(key)
     if plan is None:
-        plan = _plans[key] = Plan(K, N, device=W.device.index)
+        plan = _plans[key] = Plan(K, N, device=W.device.index, rows=M)
     return plan(A, W, S, out=out)
 
 

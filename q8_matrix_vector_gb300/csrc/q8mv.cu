@@ -41,12 +41,16 @@
 #include <new>
 
 #include "async_stream.cuh"
+#include "batched.h"
+#include "regs_kernel.cuh"
 #include "tma_stream.cuh"
 
 namespace {
 
-constexpr int kBlk = 32;            // Q8_0 block length along K
-constexpr int kStageBlocks = 64;    // activation blocks staged in shared memory at a time
+using rk::kBlk;
+using rk::kStageBlocks;
+using rk::Params;
+using rk::q8mv_regs_kernel;
 constexpr int kMaxSplit = 65535;    // gridDim.y limit
 constexpr int kVersion = 100;       // 0.1.0
 
@@ -63,336 +67,6 @@ q8mv_status_t cuda_status(cudaError_t e) {
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-// ---------------------------------------------------------------------------
-// Kernel parameters
-// ---------------------------------------------------------------------------
-struct Params {
-    const float *A;
-    const int8_t *W;
-    const float *S;
-    float *C;
-    float *ws;            // [split, N] partial rows (split > 1)
-    unsigned *tickets;    // [tiles] arrival counters, zero between calls
-    int64_t K, N;
-    int KB;
-    int tn;               // threads along N (power of two, 32..256)
-    int tn_log2;
-    int gk;               // thread groups along K = threads per CTA / tn
-    int split;            // CTAs per tile along K
-    int bps;              // blocks per split
-};
-
-// ---------------------------------------------------------------------------
-// Device helpers
-// ---------------------------------------------------------------------------
-
-// Weight loads: read-only, streamed once, so no L1 allocation; ask L2 to fetch
-// 256-byte lines since neighbouring lanes read the rest of the line.
-template <int V>
-__device__ __forceinline__ void load_w(const int8_t *p, uint32_t (&w)[(V + 3) / 4]) {
-    if constexpr (V == 16) {
-        asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-            : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-            : "l"(p));
-    } else if constexpr (V == 8) {
-        asm("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p));
-    } else if constexpr (V == 4) {
-        asm("ld.global.nc.L1::no_allocate.L2::256B.u32 %0, [%1];" : "=r"(w[0]) : "l"(p));
-    } else if constexpr (V == 2) {
-        unsigned short h;
-        asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(h) : "l"(p));
-        w[0] = h;
-    } else {
-        asm("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=r"(w[0]) : "l"(p));
-    }
-}
-
-// Exact signed-byte -> f32 for two bytes of a word (selectors pick bytes i, j).
-// u = w ^ 0x80 lies in 0..255; the float with bits 0x4B0000uu is 2^23 + u,
-// exactly; subtracting 2^23 + 128 leaves w, exactly.
-__device__ __forceinline__ float2 bytes_to_f32x2(uint32_t flipped, uint32_t sel_lo, uint32_t sel_hi) {
-    const float2 t = make_float2(__uint_as_float(__byte_perm(flipped, 0x4B000000u, sel_lo)),
-                                 __uint_as_float(__byte_perm(flipped, 0x4B000000u, sel_hi)));
-    return __fadd2_rn(t, make_float2(-8388736.0f, -8388736.0f));
-}
-
-__device__ __forceinline__ float byte_to_f32(uint32_t raw) {
-    return __uint_as_float(0x4B000000u | ((raw ^ 0x80u) & 0xFFu)) - 8388736.0f;
-}
-
-// part[0..V) += a * W-row (V bytes held in w).  Packed pairs for V >= 2.
-template <int V>
-__device__ __forceinline__ void fma_row(float a, const uint32_t (&w)[(V + 3) / 4], float (&part)[V]) {
-    if constexpr (V >= 4) {
-        const float2 a2 = make_float2(a, a);
-#pragma unroll
-        for (int q = 0; q < V / 4; ++q) {
-            const uint32_t u = w[q] ^ 0x80808080u;
-            const float2 f01 = bytes_to_f32x2(u, 0x7440u, 0x7441u);
-            const float2 f23 = bytes_to_f32x2(u, 0x7442u, 0x7443u);
-            float2 p01 = make_float2(part[4 * q + 0], part[4 * q + 1]);
-            float2 p23 = make_float2(part[4 * q + 2], part[4 * q + 3]);
-            p01 = __ffma2_rn(a2, f01, p01);
-            p23 = __ffma2_rn(a2, f23, p23);
-            part[4 * q + 0] = p01.x;
-            part[4 * q + 1] = p01.y;
-            part[4 * q + 2] = p23.x;
-            part[4 * q + 3] = p23.y;
-        }
-    } else if constexpr (V == 2) {
-        const float2 f01 = bytes_to_f32x2(w[0] ^ 0x8080u, 0x7440u, 0x7441u);
-        float2 p01 = make_float2(part[0], part[1]);
-        p01 = __ffma2_rn(make_float2(a, a), f01, p01);
-        part[0] = p01.x;
-        part[1] = p01.y;
-    } else {
-        part[0] = fmaf(a, byte_to_f32(w[0]), part[0]);
-    }
-}
-
-// S[b, n0 .. n0+V): vector loads when S and N allow them.
-template <int V, bool SVEC>
-__device__ __forceinline__ void load_s(const float *p, float (&s)[V]) {
-    if constexpr (SVEC && V >= 4) {
-#pragma unroll
-        for (int q = 0; q < V / 4; ++q) {
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(p) + q);
-            s[4 * q + 0] = v.x;
-            s[4 * q + 1] = v.y;
-            s[4 * q + 2] = v.z;
-            s[4 * q + 3] = v.w;
-        }
-    } else if constexpr (SVEC && V == 2) {
-        const float2 v = __ldg(reinterpret_cast<const float2 *>(p));
-        s[0] = v.x;
-        s[1] = v.y;
-    } else {
-#pragma unroll
-        for (int j = 0; j < V; ++j) s[j] = __ldg(p + j);
-    }
-}
-
-// acc += part * s, one fused multiply-add per column ("Factoring out the scale").
-template <int V>
-__device__ __forceinline__ void fold_scale(const float (&part)[V], const float (&s)[V], float (&acc)[V]) {
-    if constexpr (V >= 2) {
-#pragma unroll
-        for (int j = 0; j < V; j += 2) {
-            const float2 r = __ffma2_rn(make_float2(part[j], part[j + 1]), make_float2(s[j], s[j + 1]),
-                                        make_float2(acc[j], acc[j + 1]));
-            acc[j] = r.x;
-            acc[j + 1] = r.y;
-        }
-    } else {
-        acc[0] = fmaf(part[0], s[0], acc[0]);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Register-streaming kernel
-// ---------------------------------------------------------------------------
-// Weight loads of a thread's first block are issued before anything else, and
-// in particular before griddepcontrol.wait: under programmatic dependent launch
-// the kernel may start while the previous kernel in the stream is finishing,
-// so its weight stream overlaps that kernel's tail.  The activations, the
-// workspace and C are touched only after the wait.
-__device__ __forceinline__ void pdl_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-template <int V>
-__device__ __forceinline__ void load_w_volatile(const int8_t *p, uint32_t (&w)[(V + 3) / 4]) {
-    // same loads as load_w, but kept in program order so that a block's 32
-    // rows are all in flight before the first one is used
-    if constexpr (V == 16) {
-        asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                     : "l"(p));
-    } else if constexpr (V == 8) {
-        asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p));
-    } else {
-        load_w<V>(p, w);
-    }
-}
-
-// Narrow loads keep a block in at most 64 registers, so those variants are held
-// to 128 registers a thread: two 256-thread or four 128-thread CTAs per SM.
-template <int V, int TPB>
-constexpr int regs_min_blocks() {
-    return V >= 16 ? 1 : (TPB == 256 ? 2 : 4);
-}
-
-template <int V, bool SVEC, int TPB, bool CLUSTER>
-__global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kernel(const Params p) {
-    extern __shared__ __align__(16) float smem[];
-    __shared__ unsigned s_is_last;
-    constexpr int VW = (V + 3) / 4;
-
-    const int tid = threadIdx.x;
-    const int tn_i = tid & (p.tn - 1);
-    const int gk_i = tid >> p.tn_log2;
-    const int64_t tile = blockIdx.x;
-    const int tile_cols = p.tn * V;
-    const int64_t col0 = tile * tile_cols;
-    const int64_t n0 = col0 + static_cast<int64_t>(tn_i) * V;
-    const bool active = n0 < p.N;  // V divides N, so an active strip is whole
-
-    const int b_begin = blockIdx.y * p.bps;
-    const int b_end = min(p.KB, b_begin + p.bps);
-
-    // the first block of this thread, if it is whole, is loaded right away,
-    // weights and scales
-    uint32_t w[kBlk][VW];
-    float s[V];
-    int b = b_begin + gk_i;
-    bool prefetched = false;
-    if (active && b < b_end && static_cast<int64_t>(b + 1) * kBlk <= p.K) {
-        const int8_t *w_ptr = p.W + static_cast<int64_t>(b) * kBlk * p.N + n0;
-#pragma unroll
-        for (int r = 0; r < kBlk; ++r) load_w_volatile<V>(w_ptr + r * p.N, w[r]);
-        load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
-        prefetched = true;
-    }
-    pdl_launch_dependents();
-    pdl_wait();
-
-    float acc[V];
-#pragma unroll
-    for (int j = 0; j < V; ++j) acc[j] = 0.0f;
-
-    for (int c_begin = b_begin; c_begin < b_end; c_begin += kStageBlocks) {
-        const int c_end = min(b_end, c_begin + kStageBlocks);
-        // stage the activation rows of this chunk of blocks (rows < K only)
-        const int64_t k0 = static_cast<int64_t>(c_begin) * kBlk;
-        const int nk = static_cast<int>(min(static_cast<int64_t>(c_end) * kBlk, p.K) - k0);
-        __syncthreads();
-        for (int i = tid; i < nk; i += TPB) smem[i] = __ldg(p.A + k0 + i);
-        __syncthreads();
-        if (!active) continue;
-
-        for (; b < c_end; b += p.gk) {
-            const float *a_blk = smem + (b - c_begin) * kBlk;
-            const int8_t *w_ptr = p.W + static_cast<int64_t>(b) * kBlk * p.N + n0;
-            const int64_t rows = min(static_cast<int64_t>(kBlk), p.K - static_cast<int64_t>(b) * kBlk);
-
-            float part[V];
-#pragma unroll
-            for (int j = 0; j < V; ++j) part[j] = 0.0f;
-
-            const bool had_prefetch = prefetched;
-            if (rows == kBlk) {
-                // whole block: all 32 row loads are issued before the arithmetic
-                if (!prefetched) {
-#pragma unroll
-                    for (int r = 0; r < kBlk; ++r) load_w_volatile<V>(w_ptr + r * p.N, w[r]);
-                }
-                prefetched = false;
-#pragma unroll
-                for (int r = 0; r < kBlk; r += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(a_blk + r);
-                    fma_row<V>(a4.x, w[r + 0], part);
-                    fma_row<V>(a4.y, w[r + 1], part);
-                    fma_row<V>(a4.z, w[r + 2], part);
-                    fma_row<V>(a4.w, w[r + 3], part);
-                }
-            } else {
-                // masked remainder: rows at or past K are never read
-                for (int r = 0; r < rows; ++r) {
-                    uint32_t wr[VW];
-                    load_w<V>(w_ptr + r * p.N, wr);
-                    fma_row<V>(a_blk[r], wr, part);
-                }
-            }
-            if (!had_prefetch) load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
-            fold_scale<V>(part, s, acc);
-        }
-    }
-
-    // sum the K groups of this CTA: first the groups that share a warp, by a
-    // butterfly of shuffles over the lane bits that number them (each pairwise
-    // sum is commutative, so every lane ends with the same bits), then the
-    // warps' rows in shared memory in row order
-    const int lane = tid & 31;
-    int rows = p.gk;       // rows of partial sums left for shared memory
-    int row = gk_i;
-    if (p.tn < 32) {
-        for (int off = p.tn; off < 32; off <<= 1) {
-#pragma unroll
-            for (int j = 0; j < V; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
-        }
-        rows = TPB / 32;
-        row = tid >> 5;
-    }
-    __syncthreads();
-    float *red = smem;  // [rows][tile_cols]
-    if (p.tn >= 32 || lane < p.tn) {
-#pragma unroll
-        for (int j = 0; j < V; ++j) red[row * tile_cols + tn_i * V + j] = acc[j];
-    }
-    __syncthreads();
-
-    if constexpr (CLUSTER) {
-        // The split_k CTAs of this tile form one thread-block cluster.  Each
-        // keeps its column sums in its own shared memory; after a cluster
-        // barrier CTA r adds up slice r of the columns over all the cluster's
-        // CTAs, in rank order, reading their shared memory directly.
-        namespace cg = cooperative_groups;
-        float *mine = smem + rows * tile_cols;  // [tile_cols]
-        for (int c = tid; c < tile_cols; c += TPB) {
-            float v = red[c];
-            for (int g = 1; g < rows; ++g) v += red[g * tile_cols + c];
-            mine[c] = v;
-        }
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        const int rank = static_cast<int>(blockIdx.y);
-        const int per = (tile_cols + p.split - 1) / p.split;
-        const int c_end = min(tile_cols, (rank + 1) * per);
-        for (int c = rank * per + tid; c < c_end; c += TPB) {
-            const int64_t n = col0 + c;
-            float v = *cluster.map_shared_rank(mine + c, 0);
-            for (int q = 1; q < p.split; ++q) v += *cluster.map_shared_rank(mine + c, q);
-            if (n < p.N) p.C[n] = v;
-        }
-        cluster.sync();  // keep this CTA's sums alive until every CTA has read them
-        return;
-    }
-
-    const bool split = p.split > 1;
-    for (int c = tid; c < tile_cols; c += TPB) {
-        const int64_t n = col0 + c;
-        if (n >= p.N) break;
-        float v = red[c];
-        for (int g = 1; g < rows; ++g) v += red[g * tile_cols + c];
-        if (split)
-            p.ws[static_cast<int64_t>(blockIdx.y) * p.N + n] = v;
-        else
-            p.C[n] = v;
-    }
-    if (!split) return;
-
-    // split-K: the CTA that arrives last for this tile sums the partial rows
-    // in split order.  Fence, count, and only the last arrival reads.
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned ticket = atomicAdd(p.tickets + tile, 1u);
-        s_is_last = (ticket == static_cast<unsigned>(p.split - 1)) ? 1u : 0u;
-    }
-    __syncthreads();
-    if (!s_is_last) return;
-    __threadfence();
-    for (int c = tid; c < tile_cols; c += TPB) {
-        const int64_t n = col0 + c;
-        if (n >= p.N) break;
-        float v = __ldcg(p.ws + n);
-        for (int q = 1; q < p.split; ++q) v += __ldcg(p.ws + static_cast<int64_t>(q) * p.N + n);
-        p.C[n] = v;
-    }
-    if (tid == 0) p.tickets[tile] = 0u;  // ready for the next call
-}
 
 // ---------------------------------------------------------------------------
 // Host-side planning (pure; no CUDA calls)
@@ -551,6 +225,9 @@ void fill_info(const Config &c, int sm_count, int cps, int64_t ws_bytes, q8mv_pl
     info->sm_count = sm_count;
     info->ctas_per_sm = cps;
     info->cluster = c.cluster ? 1 : 0;
+    info->rows = 1;
+    info->rows_per_pass = 1;
+    info->grid_z = 1;
 }
 
 // ---------------------------------------------------------------------------
@@ -923,6 +600,11 @@ struct q8mv_plan_s {
     int tma_stages = 0;
     size_t tma_smem = 0;
     MapCache wmaps, smaps, amaps;
+    // batched plans (q8mv_plan_batched with M >= 2): rows per pass, and one
+    // configuration per weight-load width (8, 4, 1 bytes; vec == 0 if unusable)
+    int64_t M = 1;
+    int mb = 0;
+    bk::Config bcfg[bk::kNumVec];
     // device memory owned by the plan
     float *ws = nullptr;
     unsigned *tickets = nullptr;
@@ -985,6 +667,9 @@ q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t
         info->workspace_bytes = t.ws_floats * static_cast<int64_t>(sizeof(float));
         info->sm_count = sm_count;
         info->ctas_per_sm = 1;
+        info->rows = 1;
+        info->rows_per_pass = 1;
+        info->grid_z = 1;
         return Q8MV_OK;
     }
     Config c;
@@ -1177,9 +862,50 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
     return Q8MV_OK;
 }
 
+// Of the batched configurations whose load width W's address allows, the one
+// the planner expects to be fastest (or, when the width was named, the widest).
+static int batched_index(q8mv_plan_t p, uintptr_t waddr) {
+    int idx = -1;
+    for (int i = 0; i < bk::kNumVec; ++i) {
+        const bk::Config &c = p->bcfg[i];
+        if (c.vec == 0 || waddr % static_cast<uintptr_t>(c.vec) != 0) continue;
+        if (idx < 0 || (!p->forced_vec && c.cost_us < p->bcfg[idx].cost_us)) idx = i;
+    }
+    return idx;
+}
+
+static void fill_batched_info(const bk::Config &c, int sm_count, int64_t M, int64_t ws_bytes,
+                              q8mv_plan_info_t *info) {
+    std::memset(info, 0, sizeof(*info));
+    info->kernel = Q8MV_KERNEL_REGS;
+    info->vec_bytes = c.vec;
+    info->threads_n = c.tn;
+    info->groups_k = c.gk;
+    info->threads_per_cta = c.tpb;
+    info->split_k = c.split;
+    info->blocks_per_split = c.bps;
+    info->cluster = c.cluster ? 1 : 0;
+    info->tile_n = c.tile_n;
+    info->grid_x = c.tiles;
+    info->grid_y = c.split;
+    info->workspace_bytes = ws_bytes;
+    info->sm_count = sm_count;
+    info->ctas_per_sm = c.cps;
+    info->rows = static_cast<int32_t>(M);
+    info->rows_per_pass = c.mb;
+    info->grid_z = c.groups;
+}
+
 q8mv_status_t q8mv_plan_info(q8mv_plan_t p, q8mv_plan_info_t *info) {
     if (p == nullptr || info == nullptr) return Q8MV_ERR_INVALID_ARG;
     std::memset(info, 0, sizeof(*info));
+    if (p->mb > 0) {
+        const int idx = batched_index(p, 0);
+        if (idx < 0) return Q8MV_ERR_INVALID_ARG;
+        fill_batched_info(p->bcfg[idx], p->sm_count, p->M, p->ws_bytes, info);
+        info->overlap = p->overlap ? 1 : 0;
+        return Q8MV_OK;
+    }
     if (p->async) {
         fill_info(p->acfg, p->sm_count, async_cps(p->adepth, p->acfg.tpb), p->ws_bytes, info);
         info->kernel = Q8MV_KERNEL_ASYNC;
@@ -1202,6 +928,9 @@ q8mv_status_t q8mv_plan_info(q8mv_plan_t p, q8mv_plan_info_t *info) {
         info->workspace_bytes = p->ws_bytes;
         info->sm_count = p->sm_count;
         info->ctas_per_sm = 1;
+        info->rows = 1;
+        info->rows_per_pass = 1;
+        info->grid_z = 1;
         return Q8MV_OK;
     }
     int idx = -1;
@@ -1216,6 +945,9 @@ q8mv_status_t q8mv_plan_info(q8mv_plan_t p, q8mv_plan_info_t *info) {
     info->kernel = Q8MV_KERNEL_REGS;
     info->sm_count = p->sm_count;
     info->ctas_per_sm = p->occ.get(0, 256);
+    info->rows = 1;
+    info->rows_per_pass = 1;
+    info->grid_z = 1;
     return Q8MV_OK;
 }
 
@@ -1299,25 +1031,34 @@ static q8mv_status_t run_async(q8mv_plan_t p, const float *A, const int8_t *W, c
     return cuda_status(cudaLaunchKernelEx(&cfg, async_kernel(p->adepth, c.tpb), prm));
 }
 
+static q8mv_status_t run_batched(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
+                                 cudaStream_t stream) {
+    const int idx = batched_index(p, reinterpret_cast<uintptr_t>(W));
+    if (idx < 0) return Q8MV_ERR_INVALID_ARG;
+    return cuda_status(
+        bk::launch(p->bcfg[idx], A, W, S, C, p->ws, p->tickets, p->M, p->K, p->N, stream, p->overlap));
+}
+
 q8mv_status_t q8mv_run(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
                        cudaStream_t stream) {
     if (p == nullptr) return Q8MV_ERR_INVALID_ARG;
-    const int64_t K = p->K, N = p->N;
+    const int64_t K = p->K, N = p->N, M = p->M;
     if (N == 0) return Q8MV_OK;
     if (C == nullptr || (reinterpret_cast<uintptr_t>(C) & 3u)) return Q8MV_ERR_INVALID_ARG;
     int dev = -1;
     q8mv_status_t st = cuda_status(cudaGetDevice(&dev));
     if (st != Q8MV_OK) return st;
     if (dev != p->device) return Q8MV_ERR_INVALID_ARG;
-    if (K == 0) return cuda_status(cudaMemsetAsync(C, 0, static_cast<size_t>(N) * sizeof(float), stream));
+    if (K == 0) return cuda_status(cudaMemsetAsync(C, 0, static_cast<size_t>(M * N) * sizeof(float), stream));
 
     if (A == nullptr || W == nullptr || S == nullptr) return Q8MV_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(S) & 3u))
         return Q8MV_ERR_INVALID_ARG;
-    const int64_t c_bytes = 4 * N;
-    if (overlaps(C, c_bytes, A, 4 * K) || overlaps(C, c_bytes, W, K * N) ||
+    const int64_t c_bytes = 4 * M * N;
+    if (overlaps(C, c_bytes, A, 4 * M * K) || overlaps(C, c_bytes, W, K * N) ||
         overlaps(C, c_bytes, S, 4 * static_cast<int64_t>(p->KB) * N))
         return Q8MV_ERR_INVALID_ARG;
+    if (p->mb > 0) return run_batched(p, A, W, S, C, stream);
 
     const uintptr_t waddr = reinterpret_cast<uintptr_t>(W);
     const uintptr_t saddr = reinterpret_cast<uintptr_t>(S);
@@ -1393,6 +1134,135 @@ q8mv_status_t q8mv_destroy(q8mv_plan_t p) {
     if (prev != p->device) cudaSetDevice(prev);
     delete p;
     return st;
+}
+
+// Overrides a batched plan understands: vec_bytes (8, 4, 1; 8 only for up to
+// 4 rows per pass), threads_n, split_k, overlap.
+static bool batched_opts_ok(int mb, const q8mv_opts_t *o) {
+    if (o == nullptr) return true;
+    if (o->kernel != Q8MV_KERNEL_AUTO && o->kernel != Q8MV_KERNEL_REGS) return false;
+    if (o->stages != 0 || (o->cta_threads != 0 && o->cta_threads != bk::kThreads)) return false;
+    if (o->overlap != 0 && o->overlap != 1) return false;
+    if (o->vec_bytes != 0 && !((o->vec_bytes == 8 || o->vec_bytes == 4 || o->vec_bytes == 1) &&
+                               bk::vec_built(mb, o->vec_bytes)))
+        return false;
+    const int tn = o->threads_n;
+    if (tn != 0 && (tn < 8 || tn > bk::kThreads || (tn & (tn - 1)) != 0)) return false;
+    return o->split_k >= 0 && o->split_k <= kMaxSplit;
+}
+
+q8mv_status_t q8mv_plan_batched(q8mv_plan_t *out, int64_t M, int64_t K, int64_t N, int device,
+                                const q8mv_opts_t *opts) {
+    if (out == nullptr) return Q8MV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (M < 1 || M > bk::kMaxRows) return Q8MV_ERR_INVALID_ARG;
+    if (M == 1) return q8mv_plan(out, K, N, device, opts);
+    if (K < 0 || N < 0 || K >= (1LL << 31) || N >= (1LL << 31)) return Q8MV_ERR_INVALID_ARG;
+    if (N > 0 && K > ((1LL << 62) / N)) return Q8MV_ERR_INVALID_ARG;
+    const int mb = bk::rows_per_pass(M);
+    if (!batched_opts_ok(mb, opts)) return Q8MV_ERR_INVALID_ARG;
+
+    int prev = 0;
+    q8mv_status_t st = cuda_status(cudaGetDevice(&prev));
+    if (st != Q8MV_OK) return st;
+    if (device < 0) device = prev;
+    int ndev = 0;
+    st = cuda_status(cudaGetDeviceCount(&ndev));
+    if (st != Q8MV_OK) return st;
+    if (device >= ndev) return Q8MV_ERR_INVALID_ARG;
+    if (device != prev) {
+        st = cuda_status(cudaSetDevice(device));
+        if (st != Q8MV_OK) return st;
+    }
+    q8mv_plan_s *p = new (std::nothrow) q8mv_plan_s();
+    if (p == nullptr) {
+        if (device != prev) cudaSetDevice(prev);
+        return Q8MV_ERR_OUT_OF_MEMORY;
+    }
+    auto fail = [&](q8mv_status_t s) {
+        if (p->ws) cudaFree(p->ws);
+        if (p->tickets) cudaFree(p->tickets);
+        if (p->err) cudaFree(p->err);
+        delete p;
+        if (device != prev) cudaSetDevice(prev);
+        return s;
+    };
+    p->K = K;
+    p->N = N;
+    p->M = M;
+    p->mb = mb;
+    p->KB = static_cast<int>(ceil_div(K, kBlk));
+    p->device = device;
+    p->max_vec = (opts && opts->vec_bytes) ? opts->vec_bytes : 16;
+    p->forced_vec = opts && opts->vec_bytes != 0;
+    p->overlap = opts && opts->overlap == 1;
+
+    int major = 0, minor = 0;
+    bk::Device dev;
+    st = cuda_status(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device));
+    if (st == Q8MV_OK) st = cuda_status(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device));
+    if (st == Q8MV_OK) st = cuda_status(cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, device));
+    if (st == Q8MV_OK)
+        st = cuda_status(cudaDeviceGetAttribute(&dev.smem_per_cta, cudaDevAttrMaxSharedMemoryPerBlockOptin, device));
+    if (st == Q8MV_OK)
+        st = cuda_status(
+            cudaDeviceGetAttribute(&dev.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device));
+    if (st != Q8MV_OK) return fail(st);
+    if (major != 10 || minor != 3) return fail(Q8MV_ERR_UNSUPPORTED_DEVICE);
+    dev.sm_count = p->sm_count;
+    st = cuda_status(bk::query_device(mb, &dev));
+    if (st != Q8MV_OK) return fail(st == Q8MV_ERR_CUDA ? Q8MV_ERR_UNSUPPORTED_DEVICE : st);
+
+    int64_t ws_floats = 0, n_tickets = 0;
+    for (int i = 0; i < bk::kNumVec; ++i) {
+        const int v = bk::kVecs[i];
+        if (v > p->max_vec || !bk::vec_built(mb, v) || (N > 0 && N % v != 0)) continue;
+        bk::Config c;
+        if (bk::choose(M, K, N, dev, v, opts, &c) != Q8MV_OK) return fail(Q8MV_ERR_INVALID_ARG);
+        st = cuda_status(bk::prepare(c));
+        if (st != Q8MV_OK) return fail(st);
+        p->bcfg[i] = c;
+        ws_floats = std::max(ws_floats, c.ws_floats);
+        n_tickets = std::max(n_tickets, c.n_tickets);
+    }
+    if (p->bcfg[bk::kNumVec - 1].vec == 0 && N > 0) return fail(Q8MV_ERR_INVALID_ARG);  // needs the fallback
+
+    if (ws_floats > 0) {
+        st = cuda_status(cudaMalloc(&p->ws, static_cast<size_t>(ws_floats) * sizeof(float)));
+        if (st != Q8MV_OK) return fail(st);
+        st = cuda_status(cudaMalloc(&p->tickets, static_cast<size_t>(n_tickets) * sizeof(unsigned)));
+        if (st != Q8MV_OK) return fail(st);
+        st = cuda_status(cudaMemset(p->tickets, 0, static_cast<size_t>(n_tickets) * sizeof(unsigned)));
+        if (st != Q8MV_OK) return fail(st);
+    }
+    st = cuda_status(cudaMalloc(&p->err, sizeof(int)));
+    if (st == Q8MV_OK) st = cuda_status(cudaMemset(p->err, 0, sizeof(int)));
+    if (st == Q8MV_OK) st = cuda_status(cudaDeviceSynchronize());
+    if (st != Q8MV_OK) return fail(st);
+    p->ws_floats = ws_floats;
+    p->n_tickets = ws_floats > 0 ? n_tickets : 0;
+    p->ws_bytes = ws_floats * static_cast<int64_t>(sizeof(float)) + p->n_tickets * 4 + 4;
+
+    if (device != prev) cudaSetDevice(prev);
+    *out = p;
+    return Q8MV_OK;
+}
+
+q8mv_status_t q8mv_choose_config_batched(int64_t M, int64_t K, int64_t N, int32_t sm_count, int32_t ctas_per_sm,
+                                         int32_t vec_bytes, const q8mv_opts_t *opts, q8mv_plan_info_t *info) {
+    if (info == nullptr || M < 1 || M > bk::kMaxRows || sm_count <= 0 || ctas_per_sm <= 0)
+        return Q8MV_ERR_INVALID_ARG;
+    const int mb = bk::rows_per_pass(M);
+    if (!batched_opts_ok(mb, opts)) return Q8MV_ERR_INVALID_ARG;
+    bk::Device dev;
+    dev.sm_count = sm_count;
+    for (int i = 0; i < bk::kNumVec; ++i) dev.cps_regs[i] = ctas_per_sm;
+    bk::Config c;
+    const q8mv_status_t st = bk::choose(M, K, N, dev, vec_bytes, opts, &c);
+    if (st != Q8MV_OK) return st;
+    fill_batched_info(c, sm_count, M, c.ws_floats * static_cast<int64_t>(sizeof(float)), info);
+    info->overlap = opts && opts->overlap == 1 ? 1 : 0;
+    return Q8MV_OK;
 }
 
 }  // extern "C"

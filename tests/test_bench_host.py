@@ -91,15 +91,23 @@ def test_clock_parsing():
 
 
 def test_traffic_ignored_when_kernel_changed(tmp_path, monkeypatch):
-    rec = {"kernel_source_sha256": "0" * 64, "workloads": {"attn": {"dram_bytes_per_launch": 123}}}
+    rec = {"workloads": {
+        "attn": {"dram_bytes_per_launch": 123, "kernel_source": "regs_kernel.cuh",
+                 "kernel_source_sha256": "0" * 64},
+        "attn_m4": {"dram_bytes_per_launch": 456, "kernel_source": "batched.cuh",
+                    "kernel_source_sha256": bench.kernel_source_hash("batched.cuh")},
+        "tiny": {"dram_bytes_per_launch": 789, "kernel_source": "no_such_file.cuh",
+                 "kernel_source_sha256": "0" * 64}}}
     p = tmp_path / "traffic.json"
     p.write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(p))
-    assert bench.recorded_traffic("attn") is None
-    rec["kernel_source_sha256"] = bench.kernel_source_hash()
-    p.write_text(json.dumps(rec))
-    assert bench.recorded_traffic("attn") == 123
+    assert bench.recorded_traffic("attn") is None  # the kernel changed since the capture
+    assert bench.recorded_traffic(bench.traffic_key("attn", 4)) == 456
     assert bench.recorded_traffic("tiny") is None
+    assert bench.recorded_traffic("ffn_up") is None
+    rec["workloads"]["attn"]["kernel_source_sha256"] = bench.kernel_source_hash("regs_kernel.cuh")
+    p.write_text(json.dumps(rec))
+    assert bench.recorded_traffic(bench.traffic_key("attn", 1)) == 123
 
 
 def test_bench_rejects_short_warmup():

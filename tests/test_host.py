@@ -215,3 +215,94 @@ def test_async_planner_covers_every_block(q8, K, N):
 def test_async_planner_rejects_unaligned_rows(q8):
     with pytest.raises(q8.Q8mvError):
         q8.choose_config(64, 200, 152, 0, 0, kernel=q8.KERNEL_ASYNC)
+
+
+# ----------------------------------------------------------------------------
+# batched planner (M activation rows; pure host function)
+# ----------------------------------------------------------------------------
+BATCH_SHAPES = [(512, 200), (4096, 4096), (4096, 11008), (11008, 4096), (8192, 28672), (4100, 128256),
+                (1, 1), (33, 17), (0, 64), (64, 0)]
+BATCH_ROWS = [2, 3, 4, 5, 8, 9, 16, 17, 40]
+
+
+def batched_vecs(M, N):
+    mb = 2 if M <= 2 else 4 if M <= 4 else 8 if M <= 8 else 16
+    return mb, [v for v in ((8,) if mb <= 4 else ()) + (4, 1) if N == 0 or N % v == 0]
+
+
+@pytest.mark.parametrize("K,N", BATCH_SHAPES)
+@pytest.mark.parametrize("M", BATCH_ROWS)
+def test_batched_planner_covers_every_row_column_and_block(q8, M, K, N):
+    KB = (K + 31) // 32
+    mb, vecs = batched_vecs(M, N)
+    for vec in vecs:
+        c = q8.choose_config_batched(M, K, N, 152, 2, vec)
+        assert c["vec_bytes"] == vec and c["rows"] == M and c["rows_per_pass"] == mb
+        assert c["grid_z"] * mb >= M and (c["grid_z"] - 1) * mb < M
+        assert c["threads_n"] * c["groups_k"] == c["threads_per_cta"] == 256
+        assert c["tile_n"] == c["threads_n"] * vec
+        assert c["grid_x"] * c["tile_n"] >= N and (c["grid_x"] - 1) * c["tile_n"] < max(N, 1)
+        assert c["grid_y"] == c["split_k"] >= 1
+        if KB:
+            assert c["split_k"] * c["blocks_per_split"] >= KB
+            assert (c["split_k"] - 1) * c["blocks_per_split"] < KB
+        if c["split_k"] > 1 and not c["cluster"]:
+            # partial rows of every pass: [passes, split, rows per pass, N]
+            assert c["workspace_bytes"] == 4 * c["grid_z"] * c["split_k"] * mb * N
+        else:
+            assert c["workspace_bytes"] == 0
+        if c["cluster"]:
+            assert 2 <= c["split_k"] <= 8 and vec in (8, 4)
+            # the whole grid is resident at once
+            assert c["grid_x"] * c["split_k"] * c["grid_z"] <= 152 * c["ctas_per_sm"]
+
+
+def test_batched_planner_spreads_the_attention_projection(q8):
+    for M in (2, 4, 8, 16):
+        c = q8.choose_config_batched(M, 4096, 4096, 152, 2, 4)
+        assert c["grid_x"] * c["grid_y"] >= 152, M
+
+
+def test_batched_planner_honours_overrides(q8):
+    c = q8.choose_config_batched(4, 4096, 4096, 152, 2, 8, threads_n=64, split_k=3)
+    assert c["threads_n"] == 64 and c["split_k"] == 3 and c["blocks_per_split"] == 43
+    c = q8.choose_config_batched(16, 64, 4096, 152, 2, 4, split_k=9)
+    assert c["split_k"] == 2 and c["blocks_per_split"] == 1
+
+
+def test_batched_planner_rejects_illegal_requests(q8):
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config_batched(8, 64, 256, 152, 2, 8)  # 8-byte loads only up to 4 rows per pass
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config_batched(2, 64, 200, 152, 2, 16)  # no 16-byte batched kernel
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config_batched(2, 64, 202, 152, 2, 4)  # 4 does not divide 202
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config_batched(0, 64, 256, 152, 2, 4)
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config_batched((1 << 19) + 1, 64, 256, 152, 2, 4)
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config_batched(4, 64, 256, 152, 2, 4, stages=4)
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config_batched(4, 64, 256, 152, 2, 4, cta_threads=128)
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config_batched(4, 64, 256, 152, 2, 4, kernel=q8.KERNEL_TMA)
+
+
+def test_batched_plan_rejects_bad_arguments_before_touching_a_device(q8):
+    lib = q8.library()
+    h = ctypes.c_void_p(1234)
+    assert lib.q8mv_plan_batched(ctypes.byref(h), 0, 64, 64, -1, None) == q8.Q8MV_ERR_INVALID_ARG
+    assert h.value is None
+    assert lib.q8mv_plan_batched(ctypes.byref(h), -3, 64, 64, -1, None) == q8.Q8MV_ERR_INVALID_ARG
+    assert lib.q8mv_plan_batched(ctypes.byref(h), 4, -1, 64, -1, None) == q8.Q8MV_ERR_INVALID_ARG
+    assert lib.q8mv_plan_batched(ctypes.byref(h), 4, 64, 1 << 31, -1, None) == q8.Q8MV_ERR_INVALID_ARG
+    assert lib.q8mv_plan_batched(None, 4, 64, 64, -1, None) == q8.Q8MV_ERR_INVALID_ARG
+    bad = q8.Opts(0, 16, 0, 0, 0)
+    assert lib.q8mv_plan_batched(ctypes.byref(h), 4, 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+    bad = q8.Opts(0, 8, 0, 0, 0)  # 8-byte loads need at most 4 rows per pass
+    assert lib.q8mv_plan_batched(ctypes.byref(h), 5, 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+    bad = q8.Opts(3, 0, 0, 0, 0)
+    assert lib.q8mv_plan_batched(ctypes.byref(h), 4, 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+    bad = q8.Opts(0, 0, 0, 0, 0, 0, 128)
+    assert lib.q8mv_plan_batched(ctypes.byref(h), 4, 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
