@@ -54,6 +54,9 @@ class Oracle:
         lib.q8mv_oracle_block_sums.restype = ctypes.c_int
         lib.q8mv_oracle_batched.argtypes = [i64, i64, i64, p, p, p, p, p]
         lib.q8mv_oracle_batched.restype = ctypes.c_int
+        lib.q8mv_oracle_epilogue.argtypes = [i64, i64, p, p, p, p, ctypes.c_double, ctypes.c_double,
+                                             ctypes.c_int, p, p]
+        lib.q8mv_oracle_epilogue.restype = ctypes.c_int
         self._lib = lib
 
     @staticmethod
@@ -115,6 +118,33 @@ class Oracle:
             raise RuntimeError(f"q8mv_oracle_batched returned {rc}")
         return C, bound
 
+    def epilogue(self, x, c_old=None, bias=None, residual=None, alpha=1.0, beta=0.0, act=0):
+        """Apply the fused epilogue to the fp64 product x [M, N]: return (out, mag), fp64 [M, N]."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        if x.ndim == 1:
+            x = x.reshape(1, -1)
+        M, N = x.shape
+
+        def f32(a, shape):
+            if a is None:
+                return None
+            a = np.ascontiguousarray(a, dtype=np.float32)
+            if a.size != int(np.prod(shape)):
+                raise ValueError(f"expected {shape}, got {a.shape}")
+            return a
+
+        c_old = f32(c_old, (M, N))
+        bias = f32(bias, (N,))
+        residual = f32(residual, (M, N))
+        out = np.full((M, N), np.nan)
+        mag = np.full((M, N), np.nan)
+        rc = self._lib.q8mv_oracle_epilogue(M, N, self._ptr(x), self._ptr(c_old), self._ptr(bias),
+                                            self._ptr(residual), float(alpha), float(beta), int(act),
+                                            self._ptr(out), self._ptr(mag))
+        if rc != 0:
+            raise RuntimeError(f"q8mv_oracle_epilogue returned {rc}")
+        return out, mag
+
     def block_sums(self, A, W):
         """Return the unscaled block sums, fp64 [KB, N]."""
         A, W, _, K, N = self._check(A, W, None)
@@ -137,3 +167,14 @@ def load() -> Oracle:
 def tolerance(bound: np.ndarray) -> np.ndarray:
     """Per-element acceptance bound for an f32 result: 1e-5 * sum|A W S| + 1e-6."""
     return 1e-5 * bound + 1e-6
+
+
+def epilogue_tolerance(bound: np.ndarray, mag: np.ndarray, alpha: float = 1.0) -> np.ndarray:
+    """Acceptance bound after the fused epilogue, per element.
+
+    The product's own error (1e-5 * sum|A W S| + 1e-6) is scaled by |alpha| and
+    by 1.13, the largest slope of the activations (gelu's tanh form; relu and
+    silu stay below 1.1); the f32 evaluation of the statement (a few roundings,
+    expf / tanhf within a few ulps) adds 1e-6 of the magnitude of its terms.
+    """
+    return 1.13 * abs(alpha) * (1e-5 * bound + 1e-6) + 1e-6 * mag + 1e-6

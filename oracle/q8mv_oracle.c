@@ -165,3 +165,51 @@ int q8mv_oracle_batched(int64_t M, int64_t K, int64_t N, const float *A, const i
     }
     return 0;
 }
+
+/*
+ * Fused epilogue ("dot and tensor cores" page, "The fused epilogue"): an
+ * elementwise statement right after the product is applied to each output as
+ * it is written, instead of storing the product and sweeping it again.  The
+ * page's two forms are a scale of the product (s = s * scale) and an update
+ * of the target that reads its previous value (acc = acc * corr + dot(p, v)).
+ * The statement here covers both, plus the bias, activation and residual of a
+ * decode layer, in this order, for output (m, n) of an [M, N] result:
+ *
+ *     y = alpha * x[m,n] + beta * c_old[m,n] + bias[n]
+ *     y = act(y)                       (0 none, 1 relu, 2 silu, 3 gelu tanh)
+ *     out[m,n] = y + residual[m,n]
+ *
+ * with x the fp64 product, c_old (read only when beta != 0), bias and residual
+ * optional f32 arrays.  silu(y) = y / (1 + exp(-y)); the tanh form of gelu is
+ * 0.5 y (1 + tanh(sqrt(2/pi) (y + 0.044715 y^3))) (Hendrycks and Gimpel).
+ * mag (nullable) receives |alpha x| + |beta c_old| + |bias| + |act(y)| +
+ * |residual|, the magnitude a rounded result's error is judged against.
+ */
+int q8mv_oracle_epilogue(int64_t M, int64_t N, const double *x, const float *c_old, const float *bias,
+                         const float *residual, double alpha, double beta, int act, double *out,
+                         double *mag) {
+    if (M < 0 || N < 0 || act < 0 || act > 3) return -1;
+    if (M > 0 && N > 0 && (x == NULL || out == NULL)) return -1;
+    if (M > 0 && N > 0 && beta != 0.0 && c_old == NULL) return -1;
+    const double k_gelu = 0.79788456080286535588; /* sqrt(2 / pi) */
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            const int64_t i = m * N + n;
+            const double ax = alpha * x[i];
+            const double bc = beta != 0.0 ? beta * (double)c_old[i] : 0.0;
+            const double b = bias ? (double)bias[n] : 0.0;
+            double y = ax + bc + b;
+            if (act == 1) {
+                y = y > 0.0 ? y : 0.0;
+            } else if (act == 2) {
+                y = y / (1.0 + exp(-y));
+            } else if (act == 3) {
+                y = 0.5 * y * (1.0 + tanh(k_gelu * (y + 0.044715 * y * y * y)));
+            }
+            const double r = residual ? (double)residual[i] : 0.0;
+            out[i] = y + r;
+            if (mag) mag[i] = fabs(ax) + fabs(bc) + fabs(b) + fabs(y) + fabs(r);
+        }
+    }
+    return 0;
+}

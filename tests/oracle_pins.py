@@ -14,7 +14,10 @@ the oracle disagrees with an independent fact:
 - the scale-row rule printed in "The tensors", read from a golden fixture;
 - for several activation rows at once: exact rational brute force per row,
   one-hot rows, a closed form with a different constant per row, and row
-  permutations (rows of C follow rows of A and never mix).
+  permutations (rows of C follow rows of A and never mix);
+- for the fused epilogue: the page's two statement forms on integers (exact),
+  bias per column and residual per element, their order around the
+  activation, and the activations against scipy's expit and torch's gelu.
 
 The pins are shared by ``test_oracle_pins.py`` (the real oracle must pass all)
 and ``test_oracle_mutants.py`` (each planted mistake must fail at least one).
@@ -298,6 +301,65 @@ def pin_batched_row_permutation(orc):
         assert np.array_equal(Cm, C[m]) and np.array_equal(bm, bound[m]), m
 
 
+def pin_epilogue_identity_and_page_forms(orc):
+    """Defaults leave the product alone; the page's two forms, s = s * scale and
+    acc = acc * corr + dot(p, v), on integer data are exact closed forms."""
+    rng = _rng(300)
+    x = rng.integers(-1000, 1000, size=(3, 7)).astype(np.float64)
+    out, _ = orc.epilogue(x)
+    assert np.array_equal(out, x)
+    out, _ = orc.epilogue(x, alpha=0.125)
+    assert np.array_equal(out, x / 8)
+    c_old = rng.integers(-50, 50, size=(3, 7)).astype(np.float32)
+    out, _ = orc.epilogue(x, c_old=c_old, beta=0.5)
+    assert np.array_equal(out, c_old.astype(np.float64) / 2 + x)
+    # beta = 0 never reads c_old
+    out, _ = orc.epilogue(x, c_old=None, beta=0.0, alpha=-2.0)
+    assert np.array_equal(out, -2 * x)
+
+
+def pin_epilogue_bias_and_residual_indexing(orc):
+    """bias is per column and shared by every row; residual is per element."""
+    M, N = 3, 4
+    x = np.zeros((M, N))
+    bias = np.arange(1, N + 1, dtype=np.float32)
+    residual = (10 * np.arange(M)[:, None] + 100 * np.arange(N)[None, :]).astype(np.float32)
+    out, mag = orc.epilogue(x, bias=bias, residual=residual)
+    expect = np.array([[(n + 1) + 10 * m + 100 * n for n in range(N)] for m in range(M)], dtype=np.float64)
+    assert np.array_equal(out, expect)
+    assert np.array_equal(mag, np.array([[2 * (n + 1) + 10 * m + 100 * n for n in range(N)] for m in range(M)],
+                                        dtype=np.float64))
+
+
+def pin_epilogue_order(orc):
+    """Bias before the activation, residual after it (relu tells them apart)."""
+    x = np.array([[-1.0, -5.0, 2.0]])
+    out, _ = orc.epilogue(x, bias=np.array([3, 0, 0], np.float32), act=1)
+    assert np.array_equal(out, [[2.0, 0.0, 2.0]])
+    out, _ = orc.epilogue(x, residual=np.array([[0, 4, 0]], np.float32), act=1)
+    assert np.array_equal(out, [[0.0, 4.0, 2.0]])
+
+
+def pin_epilogue_activations_against_libraries(orc):
+    """relu is max(y, 0); silu is y * expit(y) (scipy); the tanh form of gelu is
+    torch's gelu(approximate='tanh'), all in fp64."""
+    from scipy.special import expit
+
+    y = np.concatenate([np.linspace(-30, 30, 241), [0.0, 1e-8, -1e-8, 80.0, -80.0]]).reshape(1, -1)
+    out, _ = orc.epilogue(y, act=1)
+    assert np.array_equal(out, np.maximum(y, 0.0))
+    out, _ = orc.epilogue(y, act=2)
+    ref = y * expit(y)
+    assert np.all(np.abs(out - ref) <= 1e-14 * np.abs(ref) + 1e-300)
+    try:
+        import torch
+    except ImportError:
+        return
+    ref = torch.nn.functional.gelu(torch.from_numpy(y.copy()), approximate="tanh").numpy()
+    out, _ = orc.epilogue(y, act=3)
+    assert np.all(np.abs(out - ref) <= 1e-13 * np.abs(ref) + 1e-300), np.max(np.abs(out - ref))
+
+
 ALL_PINS = [
     pin_exact_rational,
     pin_closed_form_ones,
@@ -314,4 +376,8 @@ ALL_PINS = [
     pin_batched_one_hot_rows,
     pin_batched_closed_form,
     pin_batched_row_permutation,
+    pin_epilogue_identity_and_page_forms,
+    pin_epilogue_bias_and_residual_indexing,
+    pin_epilogue_order,
+    pin_epilogue_activations_against_libraries,
 ]

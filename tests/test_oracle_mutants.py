@@ -46,6 +46,17 @@ MUTANTS = {
                               "q8mv_oracle_factored(K, N, A + (M - 1 - m) * K, W, S, C + m * N, bound ? bound + m * N : NULL)"),
     "batched_skip_last_row": ("for (int64_t m = 0; m < M; ++m) {\n        const int rc",
                               "for (int64_t m = 0; m + 1 < M; ++m) {\n        const int rc"),
+    "epi_bias_by_row": ("const double b = bias ? (double)bias[n] : 0.0;",
+                        "const double b = bias ? (double)bias[m % N] : 0.0;"),
+    "epi_residual_by_column": ("const double r = residual ? (double)residual[i] : 0.0;",
+                               "const double r = residual ? (double)residual[n] : 0.0;"),
+    "epi_beta_ignored": ("const double bc = beta != 0.0 ? beta * (double)c_old[i] : 0.0;",
+                         "const double bc = 0.0;"),
+    "epi_silu_sign": ("y = y / (1.0 + exp(-y));", "y = y / (1.0 + exp(y));"),
+    "epi_gelu_cubic": ("(y + 0.044715 * y * y * y)", "(y + 0.0044715 * y * y * y)"),
+    "epi_relu_leaky": ("y = y > 0.0 ? y : 0.0;", "y = y > 0.0 ? y : 0.01 * y;"),
+    "epi_residual_dropped": ("out[i] = y + r;", "out[i] = y;"),
+    "epi_alpha_ignored": ("const double ax = alpha * x[i];", "const double ax = x[i];"),
 }
 
 
