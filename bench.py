@@ -4,7 +4,8 @@
 One step is one call of the whole path, C = matvec(A, W, S), on the 7B-class
 attention projection (K = 4096, N = 4096) unless ``--workload`` says
 otherwise; with ``--rows M`` a step is one batched call of M activation rows
-against the same weights.  The timed region replays CUDA graphs of back-to-back calls that
+against the same weights, and with ``--epilogue ACT`` the call also applies the
+fused epilogue C = act(product + bias) + residual as it writes C.  The timed region replays CUDA graphs of back-to-back calls that
 rotate over enough distinct copies of the inputs to exceed twice the L2, so
 every call streams its weights from HBM.
 
@@ -195,10 +196,14 @@ def run_ours(args, rank, local_rank, world):
     K, N, KB = wl.K, wl.N, wl.KB
     M = args.rows
     bytes_per_call = workloads.batched_bytes(K, N, M)
+    fused = args.epilogue != "none"
+    if fused:
+        bytes_per_call += 4 * N + 4 * M * N  # bias and residual read once per call
 
     A, W, S = workloads.make_inputs(wl)
     if M > 1:
         A = workloads.make_rows(wl, M)
+    bias_h, res_h = epilogue_inputs(N, M) if fused else (None, None)
     kernel = {"auto": q8mv.KERNEL_AUTO, "regs": q8mv.KERNEL_REGS, "tma": q8mv.KERNEL_TMA,
               "async": q8mv.KERNEL_ASYNC}[args.kernel]
     overlap = not args.no_overlap
@@ -214,12 +219,18 @@ def run_ours(args, rank, local_rank, world):
     for _ in range(copies):
         bufs.append((Ah.to(dev), Wh.to(dev), Sh.to(dev), torch.empty((M, N), dtype=torch.float32, device=dev)))
     ptrs = [(a.data_ptr(), w.data_ptr(), s.data_ptr(), c.data_ptr()) for a, w, s, c in bufs]
+    epis = None
+    if fused:
+        epi_bufs = [(torch.from_numpy(bias_h).to(dev), torch.from_numpy(res_h).to(dev)) for _ in range(copies)]
+        epis = [q8mv.Epilogue(1.0, 0.0, b.data_ptr(), r.data_ptr(), EPILOGUE_ACTS[args.epilogue])
+                for b, r in epi_bufs]
+    launch = make_launcher(plan, ptrs, epis)
     stream = torch.cuda.Stream(dev)
 
     # warm-up steps (eager launches through the C library)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            plan.run_ptr(*ptrs[i % copies], stream.cuda_stream)
+            launch(i, stream.cuda_stream)
     stream.synchronize()
 
     # graphs of back-to-back calls; the rotation restarts at copy 0 in each graph
@@ -231,7 +242,7 @@ def run_ours(args, rank, local_rank, world):
         with torch.cuda.graph(g, stream=stream):
             s = torch.cuda.current_stream().cuda_stream
             for i in range(ncalls):
-                plan.run_ptr(*ptrs[i % copies], s)
+                launch(i, s)
         return g
 
     g_full = capture(chunk) if full else None
@@ -280,12 +291,20 @@ def run_ours(args, rank, local_rank, world):
     Ap, Wp, Sp = Ah.pin_memory(), Wh.pin_memory(), Sh.pin_memory()
     Cp = torch.empty((M, N), dtype=torch.float32).pin_memory()
     Ad, Wd, Sd, Cd = bufs[0]
+    epi_kw, epi_copies = {}, []
+    if fused:
+        bias_p, res_p = torch.from_numpy(bias_h).pin_memory(), torch.from_numpy(res_h).pin_memory()
+        bias_d, res_d = epi_bufs[0]
+        epi_copies = [(bias_d, bias_p), (res_d, res_p)]
+        epi_kw = dict(bias=bias_d, residual=res_d, act=args.epilogue)
     with torch.cuda.stream(stream):
         for _ in range(2):  # warm-up
             Ad.copy_(Ap, non_blocking=True)
             Wd.copy_(Wp, non_blocking=True)
             Sd.copy_(Sp, non_blocking=True)
-            plan(Ad, Wd, Sd, out=Cd, stream=stream)
+            for dst, src in epi_copies:
+                dst.copy_(src, non_blocking=True)
+            plan(Ad, Wd, Sd, out=Cd, stream=stream, **epi_kw)
             Cp.copy_(Cd, non_blocking=True)
     stream.synchronize()
     e_start = torch.cuda.Event(enable_timing=True)
@@ -297,22 +316,25 @@ def run_ours(args, rank, local_rank, world):
             Ad.copy_(Ap, non_blocking=True)
             Wd.copy_(Wp, non_blocking=True)
             Sd.copy_(Sp, non_blocking=True)
-            plan(Ad, Wd, Sd, out=Cd, stream=stream)
+            for dst, src in epi_copies:
+                dst.copy_(src, non_blocking=True)
+            plan(Ad, Wd, Sd, out=Cd, stream=stream, **epi_kw)
             Cp.copy_(Cd, non_blocking=True)
         e_end.record(stream)
     e_end.synchronize()
     e_ms = reduce_over_ranks(group, e_start.elapsed_time(e_end), "max", dev)
     e_bytes = reduce_over_ranks(group, float(bytes_per_call) * e2e_steps, "sum", dev)
-    h2d = 4 * M * K + K * N + 4 * KB * N
+    h2d = 4 * M * K + K * N + 4 * KB * N + ((4 * N + 4 * M * N) if fused else 0)
     e2e = {"value": round(e_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * M * N, "steps": e2e_steps,
-           "what": "pinned host A, W, S copied in, q8mv_run, C copied out, every step"}
+           "what": "pinned host A, W, S" + (", bias, residual" if fused else "")
+                   + " copied in, " + ("q8mv_run_fused" if fused else "q8mv_run") + ", C copied out, every step"}
 
     # the same workload with plain launches, for comparison with the overlapped headline
     plain = None
     if overlap:
         plan_plain = q8mv.Plan(K, N, device=local_rank, rows=M, overlap=0, **plan_opts)
-        us_plain = time_calls(plan_plain, ptrs, stream, min(args.steps, 20000))
+        us_plain = time_calls(plan_plain, ptrs, stream, min(args.steps, 20000), epis=epis)
         pinfo = plan_plain.info
         plain = {"us_per_call": round(us_plain, 3), "value": round(bytes_per_call / us_plain / 1e3, 2),
                  "unit": UNIT, "what": "same workload and timing, launched without programmatic dependent launch",
@@ -322,7 +344,8 @@ def run_ours(args, rank, local_rank, world):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(A, W, S, bytes_per_call, args.cpu_seconds, wl, M)
+        cpu = cpu_baseline(A, W, S, bytes_per_call, args.cpu_seconds, wl, M,
+                           (bias_h, res_h, EPILOGUE_ACTS[args.epilogue]) if fused else None)
 
     if rank != 0:
         return None
@@ -334,8 +357,9 @@ def run_ours(args, rank, local_rank, world):
         "us_per_call": round(us, 3), "pct_of_peak": round(100.0 * achieved / peak, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: {wl.description}" + (f", batched decode of M={M} rows" if M > 1 else ""),
-                   "K": K, "N": N, "KB": KB, "M": M,
+        "config": {"workload": f"{wl.name}: {wl.description}" + (f", batched decode of M={M} rows" if M > 1 else "")
+                               + (f", fused epilogue act({args.epilogue})(x + bias) + residual" if fused else ""),
+                   "K": K, "N": N, "KB": KB, "M": M, "epilogue": args.epilogue,
                    "weights": "Q8_0: int8 W [K,N], f32 scales [KB,N], f32 A [M,K] and C [M,N]",
                    "bytes_per_call": bytes_per_call,
                    "l2": f"inputs larger than L2: {copies} rotating input copies "
@@ -359,17 +383,38 @@ def run_ours(args, rank, local_rank, world):
     }
 
 
-def time_calls(plan, ptrs, stream, calls, reps=3):
+EPILOGUE_ACTS = {"none": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
+
+
+def epilogue_inputs(N, M):
+    """Seeded bias [N] and residual [M, N] for a fused-epilogue run."""
+    import numpy as np
+
+    rng = np.random.Generator(np.random.PCG64(4242))
+    return (rng.standard_normal(N).astype(np.float32),
+            np.ascontiguousarray(rng.standard_normal((M, N)).astype(np.float32)))
+
+
+def make_launcher(plan, ptrs, epis=None):
+    """launch(i, stream): call i of the rotation, with its epilogue if any."""
+    copies = len(ptrs)
+    if epis is None:
+        return lambda i, s: plan.run_ptr(*ptrs[i % copies], s)
+    return lambda i, s: plan.run_fused_ptr(*ptrs[i % copies], epis[i % copies], s)
+
+
+def time_calls(plan, ptrs, stream, calls, reps=3, epis=None):
     """Microseconds per call of back-to-back graph-captured calls (best of reps)."""
     import torch
 
     copies = len(ptrs)
+    launch = make_launcher(plan, ptrs, epis)
     chunk = max(copies, (min(GRAPH_CALLS, calls) // copies) * copies)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         s = torch.cuda.current_stream().cuda_stream
         for i in range(chunk):
-            plan.run_ptr(*ptrs[i % copies], s)
+            launch(i, s)
     with torch.cuda.stream(stream):
         g.replay()
     stream.synchronize()
@@ -388,12 +433,19 @@ def time_calls(plan, ptrs, stream, calls, reps=3):
     return best
 
 
-def cpu_baseline(A, W, S, bytes_per_call, seconds, wl, M=1):
+def cpu_baseline(A, W, S, bytes_per_call, seconds, wl, M=1, epilogue=None):
     """The fp64 oracle, as it stands, on the host cores: full calls for ~seconds."""
     import oracle
 
     orc = oracle.load()
-    run = (lambda: orc.factored(A, W, S)) if M == 1 else (lambda: orc.batched(A, W, S))
+    product = (lambda: orc.factored(A, W, S)) if M == 1 else (lambda: orc.batched(A, W, S))
+    if epilogue is None:
+        run = product
+    else:
+        bias, residual, act = epilogue
+
+        def run():
+            orc.epilogue(product()[0], bias=bias, residual=residual, act=act)
     run()  # page in
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -424,9 +476,19 @@ def run_reference(args, rank, world):
     orc = oracle.load()
     if M > 1:
         A = workloads.make_rows(wl, M)
-        call = orc.batched
+        product = orc.batched
     else:
-        call = orc.factored
+        product = orc.factored
+    fused = args.epilogue != "none"
+    bias_h, res_h = epilogue_inputs(wl.N, M) if fused else (None, None)
+    act = EPILOGUE_ACTS[args.epilogue]
+
+    def call(A, W, S):
+        x = product(A, W, S)[0]
+        if fused:
+            n = W.shape[1]
+            orc.epilogue(x, bias=bias_h[:n], residual=np.ascontiguousarray(res_h[:, :n]), act=act)
+
     t0 = time.perf_counter()
     call(A, W, S)
     t_full = time.perf_counter() - t0
@@ -438,7 +500,7 @@ def run_reference(args, rank, world):
         n_s = max(1, int(wl.N * budget / (total_steps * t_full)))
     Ws = np.ascontiguousarray(W[:, :n_s])
     Ss = np.ascontiguousarray(S[:, :n_s])
-    step_bytes = workloads.batched_bytes(wl.K, n_s, M)
+    step_bytes = workloads.batched_bytes(wl.K, n_s, M) + ((4 * n_s + 4 * M * n_s) if fused else 0)
     for _ in range(args.warmup):
         call(A, Ws, Ss)
     t0 = time.perf_counter()
@@ -447,15 +509,17 @@ def run_reference(args, rank, world):
     dt = time.perf_counter() - t0
     value = args.steps * step_bytes / dt / 1e9 if dt > 0 else 0.0
     sample = (f"first {n_s} of {wl.N} columns of {wl.name} (K={wl.K}"
-              + (f", M={M} rows" if M > 1 else "") + ") per step, fp64 oracle, single thread")
+              + (f", M={M} rows" if M > 1 else "") + (f", epilogue {args.epilogue}" if fused else "")
+              + ") per step, fp64 oracle, single thread")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt * 1e3 / max(args.steps, 1), 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: {wl.description}" + (f", batched decode of M={M} rows" if M > 1 else ""),
-                   "K": wl.K, "N": wl.N, "KB": wl.KB, "M": M},
+        "config": {"workload": f"{wl.name}: {wl.description}" + (f", batched decode of M={M} rows" if M > 1 else "")
+                               + (f", fused epilogue act({args.epilogue})(x + bias) + residual" if fused else ""),
+                   "K": wl.K, "N": wl.N, "KB": wl.KB, "M": M, "epilogue": args.epilogue},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -471,6 +535,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=workloads.HEADLINE)
     ap.add_argument("--rows", type=int, default=1,
                     help="activation rows per call (batched decode; 1 = the single-row matvec)")
+    ap.add_argument("--epilogue", choices=sorted(EPILOGUE_ACTS), default="none",
+                    help="fused epilogue: C = act(product + bias) + residual as C is written")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=CPU_BASELINE_SECONDS)
     ap.add_argument("--reference-seconds", type=float, default=60.0,

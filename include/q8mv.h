@@ -166,6 +166,50 @@ q8mv_status_t q8mv_run(q8mv_plan_t plan, const float *A, const int8_t *W, const 
                        float *C, cudaStream_t stream);
 
 /*
+ * Fused epilogue ("dot and tensor cores" page, "The fused epilogue"): an
+ * elementwise statement applied to each output as it is written, instead of
+ * storing the product and sweeping it again.  For output (m, n) of a call
+ * whose product is x[m, n]:
+ *
+ *     y = alpha * x[m, n] + beta * C[m, n] + bias[n]     (f32; C's previous
+ *                                                         contents are read only
+ *                                                         if beta != 0)
+ *     y = act(y)
+ *     C[m, n] = y + residual[m, n]
+ *
+ * The page's two forms are alpha (s = s * scale) and beta (acc = acc * corr +
+ * dot(p, v)); bias, activation and residual are those of a decode layer.
+ * act: none, relu = max(y, 0), silu = y / (1 + exp(-y)), or the tanh form of
+ * gelu, 0.5 y (1 + tanh(sqrt(2/pi) (y + 0.044715 y^3))), with CUDA's expf and
+ * tanhf.
+ */
+enum {
+    Q8MV_ACT_NONE = 0,
+    Q8MV_ACT_RELU = 1,
+    Q8MV_ACT_SILU = 2,
+    Q8MV_ACT_GELU_TANH = 3
+};
+
+typedef struct {
+    float alpha;           /* scale of the product (1 = the product itself) */
+    float beta;            /* scale of C's previous contents (0 = C is not read) */
+    const float *bias;     /* [N], the same for every row, added before the activation; NULL = none */
+    const float *residual; /* [M, N] (M = 1 for q8mv_plan), added after the activation; NULL = none */
+    int32_t act;           /* Q8MV_ACT_* */
+} q8mv_epilogue_t;
+
+/*
+ * q8mv_run with the fused epilogue `epi` (NULL = q8mv_run).  Same rules as
+ * q8mv_run; in addition bias and residual are 4-byte aligned device arrays of
+ * the plan's device that do not overlap C, and act is one of Q8MV_ACT_*.
+ * The register kernel (or, for a batched plan, the batched kernel) runs even
+ * when the plan was made for the TMA or async kernel, and also when K == 0
+ * (the product is then 0, so C = act(beta * C + bias) + residual).
+ */
+q8mv_status_t q8mv_run_fused(q8mv_plan_t plan, const float *A, const int8_t *W, const float *S,
+                             float *C, const q8mv_epilogue_t *epi, cudaStream_t stream);
+
+/*
  * Synchronise the plan's device and report in *device_error the error bits
  * its kernels recorded since the last check (0 = none; 1 = a weight stage
  * did not arrive in time, 2 = a ring slot was not released in time, 4 = a

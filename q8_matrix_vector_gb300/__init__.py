@@ -30,12 +30,24 @@ KERNEL_REGS = 1
 KERNEL_TMA = 2
 KERNEL_ASYNC = 3
 
+ACT_NONE = 0
+ACT_RELU = 1
+ACT_SILU = 2
+ACT_GELU_TANH = 3
+_ACTS = {None: ACT_NONE, "none": ACT_NONE, "relu": ACT_RELU, "silu": ACT_SILU, "gelu_tanh": ACT_GELU_TANH}
+
 
 class Opts(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
                 ("threads_n", ctypes.c_int32), ("split_k", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("overlap", ctypes.c_int32),
                 ("cta_threads", ctypes.c_int32)]
+
+
+class Epilogue(ctypes.Structure):
+    """q8mv_epilogue_t: y = alpha x + beta C_old + bias[n]; y = act(y); C = y + residual."""
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p), ("act", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -76,6 +88,8 @@ def _load() -> ctypes.CDLL:
     lib.q8mv_plan_batched.restype = ctypes.c_int
     lib.q8mv_run.argtypes = [p, p, p, p, p, p]
     lib.q8mv_run.restype = ctypes.c_int
+    lib.q8mv_run_fused.argtypes = [p, p, p, p, p, ctypes.POINTER(Epilogue), p]
+    lib.q8mv_run_fused.restype = ctypes.c_int
     lib.q8mv_check.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
     lib.q8mv_check.restype = ctypes.c_int
     lib.q8mv_destroy.argtypes = [p]
@@ -174,14 +188,27 @@ class Plan:
         if st != Q8MV_OK:
             raise Q8mvError(st, "q8mv_run")
 
-    def __call__(self, A, W, S, out=None, stream=None):
-        """C = matvec(A, W, S) on torch CUDA tensors, enqueued on the current stream."""
+    def run_fused_ptr(self, A: int, W: int, S: int, C: int, epilogue: "Epilogue", stream: int = 0) -> None:
+        """Enqueue the matvec with a fused epilogue on raw device pointers."""
+        st = _lib.q8mv_run_fused(self._h, A, W, S, C, ctypes.byref(epilogue), stream)
+        if st != Q8MV_OK:
+            raise Q8mvError(st, "q8mv_run_fused")
+
+    def __call__(self, A, W, S, out=None, stream=None, *, alpha=None, beta=None, bias=None, residual=None,
+                 act=None):
+        """C = matvec(A, W, S) on torch CUDA tensors, enqueued on the current stream.
+
+        Any of alpha, beta, bias, residual, act turns on the fused epilogue:
+        C = act(alpha * matvec + beta * C_old + bias) + residual, with act one of
+        None, "relu", "silu", "gelu_tanh" (beta != 0 reads ``out``'s contents).
+        """
         import torch
 
         _check(A, torch.float32, (self.M, self.K), "A")
         _check(W, torch.int8, (self.K, self.N), "W")
         _check(S, torch.float32, (self.KB, self.N), "S")
         dev = W.device
+        out_given = out is not None
         for name, t in (("A", A), ("S", S)):
             if t.device != dev:
                 raise ValueError(f"{name} is on {t.device}, W is on {dev}")
@@ -193,8 +220,28 @@ class Plan:
                 raise ValueError(f"out is on {out.device}, W is on {dev}")
         if stream is None:
             stream = torch.cuda.current_stream(dev)
+        fused = not (alpha is None and beta is None and bias is None and residual is None and act is None)
+        if fused:
+            if act not in _ACTS:
+                raise ValueError(f"act must be one of {sorted(k for k in _ACTS if k)} or None, got {act!r}")
+            if beta not in (None, 0, 0.0) and not out_given:
+                raise ValueError("beta != 0 reads C's previous contents: pass out=")
+            if bias is not None:
+                _check(bias, torch.float32, (self.N,), "bias")
+            if residual is not None:
+                _check(residual, torch.float32, (self.M, self.N), "residual")
+            for name, t in (("bias", bias), ("residual", residual)):
+                if t is not None and t.device != dev:
+                    raise ValueError(f"{name} is on {t.device}, W is on {dev}")
+            epi = Epilogue(1.0 if alpha is None else float(alpha), 0.0 if beta is None else float(beta),
+                           bias.data_ptr() if bias is not None else None,
+                           residual.data_ptr() if residual is not None else None, _ACTS[act])
         with torch.cuda.device(dev):
-            self.run_ptr(A.data_ptr(), W.data_ptr(), S.data_ptr(), out.data_ptr(), stream.cuda_stream)
+            if fused:
+                self.run_fused_ptr(A.data_ptr(), W.data_ptr(), S.data_ptr(), out.data_ptr(), epi,
+                                   stream.cuda_stream)
+            else:
+                self.run_ptr(A.data_ptr(), W.data_ptr(), S.data_ptr(), out.data_ptr(), stream.cuda_stream)
         return out
 
     def check(self) -> int:
@@ -226,7 +273,8 @@ def _check(t, dtype, shape, name):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    one_row = shape[0] == 1 and name in ("A", "out") and t.dim() == 1 and t.numel() == shape[1]
+    one_row = len(shape) == 2 and shape[0] == 1 and name in ("A", "out", "residual") and t.dim() == 1 \
+        and t.numel() == shape[1]
     if tuple(t.shape) != tuple(shape) and not one_row:
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_cuda:
@@ -238,11 +286,13 @@ def _check(t, dtype, shape, name):
 _plans: dict = {}
 
 
-def matvec(A, W, S, out=None):
+def matvec(A, W, S, out=None, **epilogue):
     """C[M, N] = Q8_0 matvec of every row of A [M, K] f32 (or [K]) with W [K, N] int8
     and S [KB, N] f32.
 
     Plans are cached per (M, K, N, device).  Runs on the current CUDA stream.
+    Keyword arguments alpha, beta, bias, residual, act select the fused epilogue
+    (see ``Plan.__call__``).
     """
     K, N = W.shape
     M = A.shape[0] if A.dim() == 2 else 1
@@ -250,7 +300,7 @@ def matvec(A, W, S, out=None):
     plan = _plans.get(key)
     if plan is None:
         plan = _plans[key] = Plan(K, N, device=W.device.index, rows=M)
-    return plan(A, W, S, out=out)
+    return plan(A, W, S, out=out, **epilogue)
 
 
 def version() -> int:

@@ -297,7 +297,8 @@ cudaError_t prepare(const Config &c) {
 }
 
 cudaError_t launch(const Config &c, const float *A, const int8_t *W, const float *S, float *C, float *ws,
-                   unsigned *tickets, int64_t M, int64_t K, int64_t N, cudaStream_t stream, bool overlap) {
+                   unsigned *tickets, int64_t M, int64_t K, int64_t N, const q8epi::Epilogue &epi,
+                   cudaStream_t stream, bool overlap) {
     Params prm;
     prm.A = A;
     prm.W = W;
@@ -315,6 +316,7 @@ cudaError_t launch(const Config &c, const float *A, const int8_t *W, const float
     prm.split = c.split;
     prm.bps = c.bps;
     prm.cb = c.cb;
+    prm.epi = epi;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(c.tiles), static_cast<unsigned>(c.split), static_cast<unsigned>(c.groups));
     cfg.blockDim = dim3(static_cast<unsigned>(c.tpb));

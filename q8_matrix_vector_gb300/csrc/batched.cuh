@@ -25,6 +25,8 @@
 #include <cooperative_groups.h>
 #include <cstdint>
 
+#include "epilogue.cuh"
+
 namespace bk {
 
 constexpr int kBlk = 32;
@@ -43,6 +45,7 @@ struct Params {
     int split;
     int bps;
     int cb;          // blocks of activations staged in shared memory at a time
+    q8epi::Epilogue epi;  // applied as C is written (off by default)
 };
 
 // Weight loads, kept in program order (asm volatile) and, through the memory
@@ -367,7 +370,8 @@ __global__ void __launch_bounds__(TPB, min_blocks<MB, V>()) q8mv_batched_kernel(
             if (m >= mrows || n >= p.N) continue;
             float v = *cluster.map_shared_rank(mine + i, 0);
             for (int q = 1; q < p.split; ++q) v += *cluster.map_shared_rank(mine + i, q);
-            p.C[static_cast<int64_t>(m0 + m) * p.N + n] = v;
+            const int64_t idx = static_cast<int64_t>(m0 + m) * p.N + n;
+            p.C[idx] = q8epi::apply(p.epi, v, p.C, idx, n);
         }
         cluster.sync();  // keep this CTA's sums alive until every CTA has read them
         return;
@@ -390,11 +394,18 @@ __global__ void __launch_bounds__(TPB, min_blocks<MB, V>()) q8mv_batched_kernel(
             v.z += t.z;
             v.w += t.w;
         }
-        float *dst = split ? ws_row + static_cast<int64_t>(m) * p.N : p.C + static_cast<int64_t>(m0 + m) * p.N;
         const float vals[4] = {v.x, v.y, v.z, v.w};
+        if (split) {
+            float *dst = ws_row + static_cast<int64_t>(m) * p.N;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (n + q < p.N) dst[n + q] = vals[q];
+            for (int q = 0; q < 4; ++q)
+                if (n + q < p.N) dst[n + q] = vals[q];
+        } else {
+            const int64_t row = static_cast<int64_t>(m0 + m) * p.N;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (n + q < p.N) p.C[row + n + q] = q8epi::apply(p.epi, vals[q], p.C, row + n + q, n + q);
+        }
     }
     if (!split) return;
 
@@ -414,7 +425,8 @@ __global__ void __launch_bounds__(TPB, min_blocks<MB, V>()) q8mv_batched_kernel(
         if (m >= mrows || n >= p.N) continue;
         float v = __ldcg(ws_group + static_cast<int64_t>(m) * p.N + n);
         for (int q = 1; q < p.split; ++q) v += __ldcg(ws_group + (static_cast<int64_t>(q) * MB + m) * p.N + n);
-        p.C[static_cast<int64_t>(m0 + m) * p.N + n] = v;
+        const int64_t idx = static_cast<int64_t>(m0 + m) * p.N + n;
+        p.C[idx] = q8epi::apply(p.epi, v, p.C, idx, n);
     }
     if (tid == 0) *ticket = 0u;  // ready for the next call
 }

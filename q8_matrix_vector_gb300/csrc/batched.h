@@ -4,6 +4,7 @@
 #pragma once
 
 #include "../../include/q8mv.h"
+#include "epilogue.cuh"
 
 #include <cstddef>
 #include <cstdint>
@@ -67,6 +68,7 @@ cudaError_t query_device(int mb, Device *dev);
 cudaError_t prepare(const Config &c);
 
 cudaError_t launch(const Config &c, const float *A, const int8_t *W, const float *S, float *C, float *ws,
-                   unsigned *tickets, int64_t M, int64_t K, int64_t N, cudaStream_t stream, bool overlap);
+                   unsigned *tickets, int64_t M, int64_t K, int64_t N, const q8epi::Epilogue &epi,
+                   cudaStream_t stream, bool overlap);
 
 }  // namespace bk

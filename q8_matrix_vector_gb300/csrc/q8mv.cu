@@ -1032,15 +1032,17 @@ static q8mv_status_t run_async(q8mv_plan_t p, const float *A, const int8_t *W, c
 }
 
 static q8mv_status_t run_batched(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
-                                 cudaStream_t stream) {
+                                 const q8epi::Epilogue &epi, cudaStream_t stream) {
     const int idx = batched_index(p, reinterpret_cast<uintptr_t>(W));
     if (idx < 0) return Q8MV_ERR_INVALID_ARG;
     return cuda_status(
-        bk::launch(p->bcfg[idx], A, W, S, C, p->ws, p->tickets, p->M, p->K, p->N, stream, p->overlap));
+        bk::launch(p->bcfg[idx], A, W, S, C, p->ws, p->tickets, p->M, p->K, p->N, epi, stream, p->overlap));
 }
 
-q8mv_status_t q8mv_run(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
-                       cudaStream_t stream) {
+// The run path of q8mv_run and q8mv_run_fused.  With an epilogue the register
+// (or batched) kernel always runs, also for K == 0 (the product is then 0).
+static q8mv_status_t run_impl(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
+                              const q8epi::Epilogue &epi, cudaStream_t stream) {
     if (p == nullptr) return Q8MV_ERR_INVALID_ARG;
     const int64_t K = p->K, N = p->N, M = p->M;
     if (N == 0) return Q8MV_OK;
@@ -1049,22 +1051,26 @@ q8mv_status_t q8mv_run(q8mv_plan_t p, const float *A, const int8_t *W, const flo
     q8mv_status_t st = cuda_status(cudaGetDevice(&dev));
     if (st != Q8MV_OK) return st;
     if (dev != p->device) return Q8MV_ERR_INVALID_ARG;
-    if (K == 0) return cuda_status(cudaMemsetAsync(C, 0, static_cast<size_t>(M * N) * sizeof(float), stream));
+    if (K == 0 && !epi.on)
+        return cuda_status(cudaMemsetAsync(C, 0, static_cast<size_t>(M * N) * sizeof(float), stream));
 
-    if (A == nullptr || W == nullptr || S == nullptr) return Q8MV_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(S) & 3u))
-        return Q8MV_ERR_INVALID_ARG;
-    const int64_t c_bytes = 4 * M * N;
-    if (overlaps(C, c_bytes, A, 4 * M * K) || overlaps(C, c_bytes, W, K * N) ||
-        overlaps(C, c_bytes, S, 4 * static_cast<int64_t>(p->KB) * N))
-        return Q8MV_ERR_INVALID_ARG;
-    if (p->mb > 0) return run_batched(p, A, W, S, C, stream);
+    if (K > 0) {
+        if (A == nullptr || W == nullptr || S == nullptr) return Q8MV_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(S) & 3u))
+            return Q8MV_ERR_INVALID_ARG;
+        const int64_t c_bytes = 4 * M * N;
+        if (overlaps(C, c_bytes, A, 4 * M * K) || overlaps(C, c_bytes, W, K * N) ||
+            overlaps(C, c_bytes, S, 4 * static_cast<int64_t>(p->KB) * N))
+            return Q8MV_ERR_INVALID_ARG;
+    }
+    if (p->mb > 0) return run_batched(p, A, W, S, C, epi, stream);
 
     const uintptr_t waddr = reinterpret_cast<uintptr_t>(W);
     const uintptr_t saddr = reinterpret_cast<uintptr_t>(S);
     const uintptr_t aaddr = reinterpret_cast<uintptr_t>(A);
-    if (p->async && waddr % 16 == 0 && saddr % 16 == 0) return run_async(p, A, W, S, C, stream);
-    if (p->tma && waddr % 16 == 0 && saddr % 16 == 0 && aaddr % 16 == 0) return run_tma(p, A, W, S, C, stream);
+    if (!epi.on && p->async && waddr % 16 == 0 && saddr % 16 == 0) return run_async(p, A, W, S, C, stream);
+    if (!epi.on && p->tma && waddr % 16 == 0 && saddr % 16 == 0 && aaddr % 16 == 0)
+        return run_tma(p, A, W, S, C, stream);
 
     // register kernel: of the weight-load widths that N, W's address and the
     // plan's cap allow, the one the planner expects to be fastest
@@ -1094,7 +1100,32 @@ q8mv_status_t q8mv_run(q8mv_plan_t p, const float *A, const int8_t *W, const flo
     prm.gk = c.gk;
     prm.split = c.split;
     prm.bps = c.bps;
+    prm.epi = epi;
     return cuda_status(launch_regs(c, svec, smem_bytes(c), prm, stream, p->overlap));
+}
+
+q8mv_status_t q8mv_run(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
+                       cudaStream_t stream) {
+    return run_impl(p, A, W, S, C, q8epi::Epilogue{}, stream);
+}
+
+q8mv_status_t q8mv_run_fused(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
+                             const q8mv_epilogue_t *epi, cudaStream_t stream) {
+    if (epi == nullptr) return q8mv_run(p, A, W, S, C, stream);
+    if (p == nullptr || epi->act < Q8MV_ACT_NONE || epi->act > Q8MV_ACT_GELU_TANH) return Q8MV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(epi->bias) & 3u) || (reinterpret_cast<uintptr_t>(epi->residual) & 3u))
+        return Q8MV_ERR_INVALID_ARG;
+    const int64_t c_bytes = 4 * p->M * p->N;
+    if (overlaps(C, c_bytes, epi->bias, 4 * p->N) || overlaps(C, c_bytes, epi->residual, c_bytes))
+        return Q8MV_ERR_INVALID_ARG;
+    q8epi::Epilogue e;
+    e.on = 1;
+    e.alpha = epi->alpha;
+    e.beta = epi->beta;
+    e.bias = epi->bias;
+    e.residual = epi->residual;
+    e.act = epi->act;
+    return run_impl(p, A, W, S, C, e, stream);
 }
 
 q8mv_status_t q8mv_check(q8mv_plan_t p, int32_t *device_error) {

@@ -10,6 +10,8 @@
 #include <cooperative_groups.h>
 #include <cstdint>
 
+#include "epilogue.cuh"
+
 namespace rk {
 
 constexpr int kBlk = 32;            // Q8_0 block length along K
@@ -32,6 +34,7 @@ struct Params {
     int gk;               // thread groups along K = threads per CTA / tn
     int split;            // CTAs per tile along K
     int bps;              // blocks per split
+    q8epi::Epilogue epi;  // applied as C is written (off by default)
 };
 
 // ---------------------------------------------------------------------------
@@ -305,7 +308,7 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
             const int64_t n = col0 + c;
             float v = *cluster.map_shared_rank(mine + c, 0);
             for (int q = 1; q < p.split; ++q) v += *cluster.map_shared_rank(mine + c, q);
-            if (n < p.N) p.C[n] = v;
+            if (n < p.N) p.C[n] = q8epi::apply(p.epi, v, p.C, n, n);
         }
         cluster.sync();  // keep this CTA's sums alive until every CTA has read them
         return;
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
         if (split)
             p.ws[static_cast<int64_t>(blockIdx.y) * p.N + n] = v;
         else
-            p.C[n] = v;
+            p.C[n] = q8epi::apply(p.epi, v, p.C, n, n);
     }
     if (!split) return;
 
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
         if (n >= p.N) break;
         float v = __ldcg(p.ws + n);
         for (int q = 1; q < p.split; ++q) v += __ldcg(p.ws + static_cast<int64_t>(q) * p.N + n);
-        p.C[n] = v;
+        p.C[n] = q8epi::apply(p.epi, v, p.C, n, n);
     }
     if (tid == 0) p.tickets[tile] = 0u;  // ready for the next call
 }
