@@ -57,6 +57,8 @@ class Oracle:
         lib.q8mv_oracle_epilogue.argtypes = [i64, i64, p, p, p, p, ctypes.c_double, ctypes.c_double,
                                              ctypes.c_int, p, p]
         lib.q8mv_oracle_epilogue.restype = ctypes.c_int
+        lib.q8mv_oracle_transposed.argtypes = [i64, i64, p, p, p, p, p]
+        lib.q8mv_oracle_transposed.restype = ctypes.c_int
         self._lib = lib
 
     @staticmethod
@@ -144,6 +146,25 @@ class Oracle:
         if rc != 0:
             raise RuntimeError(f"q8mv_oracle_epilogue returned {rc}")
         return out, mag
+
+    def transposed(self, A, Wt, St):
+        """Return (C, bound), fp64 [N], for weights stored one output row per row:
+        Wt [N, K] int8, St [N, KB] f32."""
+        Wt = np.ascontiguousarray(Wt, dtype=np.int8)
+        N, K = Wt.shape
+        A = np.ascontiguousarray(A, dtype=np.float32)
+        if A.size != K:
+            raise ValueError(f"A has {A.size} elements, Wt has K={K} columns")
+        St = np.ascontiguousarray(St, dtype=np.float32)
+        if St.shape != (N, (K + 31) // 32):
+            raise ValueError(f"St has shape {St.shape}, expected {(N, (K + 31) // 32)}")
+        C = np.full(N, np.nan)
+        bound = np.full(N, np.nan)
+        rc = self._lib.q8mv_oracle_transposed(K, N, self._ptr(A), self._ptr(Wt), self._ptr(St),
+                                              self._ptr(C), self._ptr(bound))
+        if rc != 0:
+            raise RuntimeError(f"q8mv_oracle_transposed returned {rc}")
+        return C, bound
 
     def block_sums(self, A, W):
         """Return the unscaled block sums, fp64 [KB, N]."""

@@ -213,3 +213,44 @@ int q8mv_oracle_epilogue(int64_t M, int64_t N, const double *x, const float *c_o
     }
     return 0;
 }
+
+/*
+ * Weights stored one output row per row ("dot and tensor cores" page: dot_t
+ * contracts the last axis of both operands, the layout of a linear layer's
+ * weights).  Wt is [N, K] with Wt[n, k] at n*K + k, and St is [N, KB] with
+ * St[n, b] at n*KB + b: row n holds output n's bytes and its block scales.
+ * The product is the Q8_0 matvec of the "Q8_0 matvec" page with W = Wt^T and
+ * S = St^T:
+ *     C[n] = sum_b St[n, b] * ( sum_{k in b, k < K} A[k] * Wt[n, k] )
+ * written directly over the transposed indexing, blocks in order, fp64.
+ * bound (nullable) receives sum_k |A[k] Wt[n,k] St[n, k/32]|.
+ */
+int q8mv_oracle_transposed(int64_t K, int64_t N, const float *A, const int8_t *Wt, const float *St,
+                           double *C, double *bound) {
+    if (K < 0 || N < 0) return -1;
+    if (N > 0 && C == NULL) return -1;
+    if (K > 0 && N > 0 && (A == NULL || Wt == NULL || St == NULL)) return -1;
+    const int64_t KB = oracle_num_blocks(K);
+    for (int64_t n = 0; n < N; ++n) {
+        const int8_t *w_row = Wt + n * K;
+        const float *s_row = St + n * KB;
+        double acc = 0.0, mag = 0.0;
+        for (int64_t b = 0; b < KB; ++b) {
+            const int64_t k_begin = b * Q8MV_ORACLE_BLK;
+            int64_t k_end = k_begin + Q8MV_ORACLE_BLK;
+            if (k_end > K) k_end = K;
+            double part = 0.0, part_mag = 0.0;
+            for (int64_t k = k_begin; k < k_end; ++k) {
+                const double aw = (double)A[k] * (double)w_row[k];
+                part += aw;
+                part_mag += fabs(aw);
+            }
+            const double s = (double)s_row[b];
+            acc += part * s;
+            mag += part_mag * fabs(s);
+        }
+        C[n] = acc;
+        if (bound) bound[n] = mag;
+    }
+    return 0;
+}

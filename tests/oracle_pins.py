@@ -17,7 +17,9 @@ the oracle disagrees with an independent fact:
   permutations (rows of C follow rows of A and never mix);
 - for the fused epilogue: the page's two statement forms on integers (exact),
   bias per column and residual per element, their order around the
-  activation, and the activations against scipy's expit and torch's gelu.
+  activation, and the activations against scipy's expit and torch's gelu;
+- for weights stored one output row per row (Wt [N, K], St [N, KB]): exact
+  rational brute force, bit-equality with the column layout, one-hot cases.
 
 The pins are shared by ``test_oracle_pins.py`` (the real oracle must pass all)
 and ``test_oracle_mutants.py`` (each planted mistake must fail at least one).
@@ -360,6 +362,52 @@ def pin_epilogue_activations_against_libraries(orc):
     assert np.all(np.abs(out - ref) <= 1e-13 * np.abs(ref) + 1e-300), np.max(np.abs(out - ref))
 
 
+def pin_transposed_exact_rational(orc):
+    """Rows-of-outputs layout: exact rational brute force over Wt[n, k], St[n, b]."""
+    for i, (K, N) in enumerate(((1, 1), (5, 3), (33, 4), (64, 2), (70, 3))):
+        A, W, S = workloads.make_random(K, N, seed=400 + i)
+        W[-1, 0] = -128
+        Wt, St = np.ascontiguousarray(W.T), np.ascontiguousarray(S.T)
+        C, bound = orc.transposed(A, Wt, St)
+        for n in range(N):
+            exact = sum(Fraction(float(A.flat[k])) * int(Wt[n, k]) * Fraction(float(St[n, k // 32]))
+                        for k in range(K))
+            mag = sum(abs(Fraction(float(A.flat[k])) * int(Wt[n, k]) * Fraction(float(St[n, k // 32])))
+                      for k in range(K))
+            tol = 4 * (K + 2) * EPS64 * float(mag) + 1e-300
+            assert abs(C[n] - float(exact)) <= tol, (K, N, n)
+            assert abs(bound[n] - float(mag)) <= tol, (K, N, n)
+
+
+def pin_transposed_matches_column_layout(orc):
+    """The same numbers laid out as W [K, N], S [KB, N] give the same result, bit
+    for bit (both sum each block's products in k order, then blocks in order)."""
+    for (K, N, seed) in ((100, 13, 410), (4100, 37, 411), (512, 200, 412)):
+        A, W, S = workloads.make_random(K, N, seed)
+        C, bound = orc.factored(A, W, S)
+        Ct, bt = orc.transposed(A, np.ascontiguousarray(W.T), np.ascontiguousarray(S.T))
+        assert np.array_equal(C, Ct) and np.array_equal(bound, bt), (K, N)
+
+
+def pin_transposed_one_hot(orc):
+    """One-hot A picks Wt[n, k] * St[n, k/32] exactly, across block edges and the
+    partial last block; a single non-zero row of Wt isolates one output."""
+    K, N = 100, 6
+    _, W, S = workloads.make_random(K, N, seed=420)
+    Wt, St = np.ascontiguousarray(W.T), np.ascontiguousarray(S.T)
+    for k in (0, 31, 32, 63, 96, 99):
+        A = np.zeros((1, K), np.float32)
+        A[0, k] = 3.0
+        C, _ = orc.transposed(A, Wt, St)
+        assert np.array_equal(C, [3.0 * int(Wt[n, k]) * float(St[n, k // 32]) for n in range(N)]), k
+    A = np.ones((1, K), np.float32)
+    Wz = np.zeros_like(Wt)
+    Wz[4] = 1
+    Sz = np.ones_like(St)
+    C, _ = orc.transposed(A, Wz, Sz)
+    assert np.array_equal(C, [0, 0, 0, 0, K, 0])
+
+
 ALL_PINS = [
     pin_exact_rational,
     pin_closed_form_ones,
@@ -380,4 +428,7 @@ ALL_PINS = [
     pin_epilogue_bias_and_residual_indexing,
     pin_epilogue_order,
     pin_epilogue_activations_against_libraries,
+    pin_transposed_exact_rational,
+    pin_transposed_matches_column_layout,
+    pin_transposed_one_hot,
 ]

@@ -57,6 +57,13 @@ MUTANTS = {
     "epi_relu_leaky": ("y = y > 0.0 ? y : 0.0;", "y = y > 0.0 ? y : 0.01 * y;"),
     "epi_residual_dropped": ("out[i] = y + r;", "out[i] = y;"),
     "epi_alpha_ignored": ("const double ax = alpha * x[i];", "const double ax = x[i];"),
+    "t_row_stride": ("const int8_t *w_row = Wt + n * K;", "const int8_t *w_row = Wt + n * (K > 1 ? K - 1 : K);"),
+    "t_scale_row_of_next_output": ("const float *s_row = St + n * KB;",
+                                   "const float *s_row = St + ((n + 1) % N) * KB;"),
+    "t_scale_by_k_not_block": ("const double s = (double)s_row[b];",
+                               "const double s = (double)s_row[b == 0 ? 0 : b - 1];"),
+    "t_drop_masked_rows": ("            if (k_end > K) k_end = K;\n            double part = 0.0, part_mag = 0.0;",
+                           "            if (k_end > K) k_end = k_begin;\n            double part = 0.0, part_mag = 0.0;"),
 }
 
 
