@@ -4,8 +4,10 @@
 One step is one call of the whole path, C = matvec(A, W, S), on the 7B-class
 attention projection (K = 4096, N = 4096) unless ``--workload`` says
 otherwise; with ``--rows M`` a step is one batched call of M activation rows
-against the same weights, and with ``--epilogue ACT`` the call also applies the
-fused epilogue C = act(product + bias) + residual as it writes C.  The timed region replays CUDA graphs of back-to-back calls that
+against the same weights, with ``--epilogue ACT`` the call also applies the
+fused epilogue C = act(product + bias) + residual as it writes C, and with
+``--transposed`` the weights are stored one output row per row (Wt [N, K],
+St [N, KB]).  The timed region replays CUDA graphs of back-to-back calls that
 rotate over enough distinct copies of the inputs to exceed twice the L2, so
 every call streams its weights from HBM.
 
@@ -103,7 +105,9 @@ def kernel_source_hash(name: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def traffic_key(workload: str, rows: int) -> str:
+def traffic_key(workload: str, rows: int, transposed: bool = False) -> str:
+    if transposed:
+        return f"{workload}_t"
     return workload if rows == 1 else f"{workload}_m{rows}"
 
 
@@ -183,6 +187,7 @@ def parse_clock_samples(text: str):
 # our arm
 # ----------------------------------------------------------------------------
 def run_ours(args, rank, local_rank, world):
+    import numpy as np
     import torch
 
     import q8_matrix_vector_gb300 as q8mv
@@ -203,13 +208,17 @@ def run_ours(args, rank, local_rank, world):
     A, W, S = workloads.make_inputs(wl)
     if M > 1:
         A = workloads.make_rows(wl, M)
+    if args.transposed:
+        W, S = np.ascontiguousarray(W.T), np.ascontiguousarray(S.T)
     bias_h, res_h = epilogue_inputs(N, M) if fused else (None, None)
     kernel = {"auto": q8mv.KERNEL_AUTO, "regs": q8mv.KERNEL_REGS, "tma": q8mv.KERNEL_TMA,
               "async": q8mv.KERNEL_ASYNC}[args.kernel]
     overlap = not args.no_overlap
     plan_opts = dict(kernel=kernel, split_k=args.split, stages=args.stages, threads_n=args.threads_n,
                      cta_threads=args.cta_threads)
-    plan = q8mv.Plan(K, N, device=local_rank, rows=M, overlap=int(overlap), **plan_opts)
+    if args.transposed:
+        plan_opts = dict(vec_bytes=0)
+    plan = q8mv.Plan(K, N, device=local_rank, rows=M, transposed=args.transposed, overlap=int(overlap), **plan_opts)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0)) or 126 * 1024 * 1024
     # distinct copies so that a copy is reused only after > 2 x L2 of other traffic
@@ -283,7 +292,7 @@ def run_ours(args, rank, local_rank, world):
     peak, peak_kind = read_hbm_peak()
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} copy bandwidth",
-                "traffic": recorded_traffic(traffic_key(args.workload, M)),
+                "traffic": recorded_traffic(traffic_key(args.workload, M, args.transposed)),
                 "algorithmic_bytes_per_launch": bytes_per_call}
 
     # end to end through the public binding: pinned host inputs in, result out
@@ -333,7 +342,7 @@ def run_ours(args, rank, local_rank, world):
     # the same workload with plain launches, for comparison with the overlapped headline
     plain = None
     if overlap:
-        plan_plain = q8mv.Plan(K, N, device=local_rank, rows=M, overlap=0, **plan_opts)
+        plan_plain = q8mv.Plan(K, N, device=local_rank, rows=M, transposed=args.transposed, overlap=0, **plan_opts)
         us_plain = time_calls(plan_plain, ptrs, stream, min(args.steps, 20000), epis=epis)
         pinfo = plan_plain.info
         plain = {"us_per_call": round(us_plain, 3), "value": round(bytes_per_call / us_plain / 1e3, 2),
@@ -345,7 +354,7 @@ def run_ours(args, rank, local_rank, world):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(A, W, S, bytes_per_call, args.cpu_seconds, wl, M,
-                           (bias_h, res_h, EPILOGUE_ACTS[args.epilogue]) if fused else None)
+                           (bias_h, res_h, EPILOGUE_ACTS[args.epilogue]) if fused else None, args.transposed)
 
     if rank != 0:
         return None
@@ -358,8 +367,10 @@ def run_ours(args, rank, local_rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{wl.name}: {wl.description}" + (f", batched decode of M={M} rows" if M > 1 else "")
-                               + (f", fused epilogue act({args.epilogue})(x + bias) + residual" if fused else ""),
+                               + (f", fused epilogue act({args.epilogue})(x + bias) + residual" if fused else "")
+                               + (", weights stored one output row per row" if args.transposed else ""),
                    "K": K, "N": N, "KB": KB, "M": M, "epilogue": args.epilogue,
+                   "layout": "Wt [N,K], St [N,KB]" if args.transposed else "W [K,N], S [KB,N]",
                    "weights": "Q8_0: int8 W [K,N], f32 scales [KB,N], f32 A [M,K] and C [M,N]",
                    "bytes_per_call": bytes_per_call,
                    "l2": f"inputs larger than L2: {copies} rotating input copies "
@@ -433,12 +444,15 @@ def time_calls(plan, ptrs, stream, calls, reps=3, epis=None):
     return best
 
 
-def cpu_baseline(A, W, S, bytes_per_call, seconds, wl, M=1, epilogue=None):
+def cpu_baseline(A, W, S, bytes_per_call, seconds, wl, M=1, epilogue=None, transposed=False):
     """The fp64 oracle, as it stands, on the host cores: full calls for ~seconds."""
     import oracle
 
     orc = oracle.load()
-    product = (lambda: orc.factored(A, W, S)) if M == 1 else (lambda: orc.batched(A, W, S))
+    if transposed:
+        product = lambda: orc.transposed(A, W, S)  # noqa: E731
+    else:
+        product = (lambda: orc.factored(A, W, S)) if M == 1 else (lambda: orc.batched(A, W, S))
     if epilogue is None:
         run = product
     else:
@@ -479,6 +493,9 @@ def run_reference(args, rank, world):
         product = orc.batched
     else:
         product = orc.factored
+    if args.transposed:
+        W, S = np.ascontiguousarray(W.T), np.ascontiguousarray(S.T)
+        product = orc.transposed
     fused = args.epilogue != "none"
     bias_h, res_h = epilogue_inputs(wl.N, M) if fused else (None, None)
     act = EPILOGUE_ACTS[args.epilogue]
@@ -486,7 +503,7 @@ def run_reference(args, rank, world):
     def call(A, W, S):
         x = product(A, W, S)[0]
         if fused:
-            n = W.shape[1]
+            n = W.shape[0] if args.transposed else W.shape[1]
             orc.epilogue(x, bias=bias_h[:n], residual=np.ascontiguousarray(res_h[:, :n]), act=act)
 
     t0 = time.perf_counter()
@@ -498,8 +515,10 @@ def run_reference(args, rank, world):
     n_s = wl.N
     if total_steps * t_full > budget:
         n_s = max(1, int(wl.N * budget / (total_steps * t_full)))
-    Ws = np.ascontiguousarray(W[:, :n_s])
-    Ss = np.ascontiguousarray(S[:, :n_s])
+    if args.transposed:
+        Ws, Ss = np.ascontiguousarray(W[:n_s]), np.ascontiguousarray(S[:n_s])
+    else:
+        Ws, Ss = np.ascontiguousarray(W[:, :n_s]), np.ascontiguousarray(S[:, :n_s])
     step_bytes = workloads.batched_bytes(wl.K, n_s, M) + ((4 * n_s + 4 * M * n_s) if fused else 0)
     for _ in range(args.warmup):
         call(A, Ws, Ss)
@@ -518,7 +537,8 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{wl.name}: {wl.description}" + (f", batched decode of M={M} rows" if M > 1 else "")
-                               + (f", fused epilogue act({args.epilogue})(x + bias) + residual" if fused else ""),
+                               + (f", fused epilogue act({args.epilogue})(x + bias) + residual" if fused else "")
+                               + (", weights stored one output row per row" if args.transposed else ""),
                    "K": wl.K, "N": wl.N, "KB": wl.KB, "M": M, "epilogue": args.epilogue},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
@@ -537,6 +557,8 @@ def parse_args(argv=None):
                     help="activation rows per call (batched decode; 1 = the single-row matvec)")
     ap.add_argument("--epilogue", choices=sorted(EPILOGUE_ACTS), default="none",
                     help="fused epilogue: C = act(product + bias) + residual as C is written")
+    ap.add_argument("--transposed", action="store_true",
+                    help="weights stored one output row per row: Wt [N, K], St [N, KB] (dot_t layout)")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=CPU_BASELINE_SECONDS)
     ap.add_argument("--reference-seconds", type=float, default=60.0,
@@ -558,6 +580,8 @@ def parse_args(argv=None):
         ap.error("--steps must be at least 1")
     if not 1 <= args.rows <= 1 << 19:
         ap.error("--rows must be in 1 .. 2^19")
+    if args.transposed and args.rows != 1:
+        ap.error("--transposed takes one activation row")
     return args
 
 

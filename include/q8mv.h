@@ -65,8 +65,10 @@ enum {
     Q8MV_KERNEL_REGS = 1, /* weights streamed through registers with vector loads; any alignment */
     Q8MV_KERNEL_TMA = 2,  /* weights streamed by the tensor-memory accelerator into a shared-memory
                              ring; needs N % 16 == 0, N >= 256, K >= 32 and 16-byte aligned A, W, S */
-    Q8MV_KERNEL_ASYNC = 3 /* each thread streams its weight strip through its own shared-memory ring
-                             with asynchronous 16-byte copies; needs N % 16 == 0 and 16-byte aligned W, S */
+    Q8MV_KERNEL_ASYNC = 3, /* each thread streams its weight strip through its own shared-memory ring
+                              with asynchronous 16-byte copies; needs N % 16 == 0 and 16-byte aligned W, S */
+    Q8MV_KERNEL_ROWS = 4   /* weights stored one output row per row (q8mv_plan_transposed): a CTA owns
+                              rows_per_cta outputs, its warps split K, lanes read 16 bytes of a row */
 };
 
 /*
@@ -88,6 +90,7 @@ typedef struct {
                           that the preceding work in the stream does not write.  Register and
                           async kernels. */
     int32_t cta_threads; /* register and async kernels: 128 or 256 threads per CTA */
+    int32_t rows_per_cta; /* transposed plans: output rows per CTA, 8 or 16 */
 } q8mv_opts_t;
 
 /* What a plan chose for 16-byte aligned tensors: the kernel family asked for
@@ -128,6 +131,25 @@ typedef struct q8mv_plan_s *q8mv_plan_t;
  */
 q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device,
                         const q8mv_opts_t *opts);
+
+/*
+ * Weights stored one output row per row: a plan for C[1,N] = A[1,K] x (Wt, St)
+ * where Wt is i8 [N, K] (Wt[n, k] at n*K + k, output n's bytes in row n) and
+ * St is f32 [N, KB] (St[n, b] at n*KB + b, output n's block scales):
+ *
+ *     C[0, n] = sum_b St[n, b] * ( sum_{k in block b} A[0, k] * Wt[n, k] )
+ *
+ * the Q8_0 product above with W = Wt^T and S = St^T, in the layout that dot_t
+ * contracts ("dot and tensor cores" page: the last axis of both operands, as a
+ * linear layer stores its weights).  q8mv_run and q8mv_run_fused then take Wt
+ * and St in place of W and S.  Limits as for q8mv_plan.  Accepted overrides:
+ * vec_bytes (16, 4 or 1: load per lane and step, used when K and Wt's address
+ * allow it, narrower loads as the fallback), rows_per_cta (8 or 16), overlap;
+ * any other non-zero field gives INVALID_ARG.  Each output's blocks are summed
+ * in order within a fixed interleave, so a plan is bitwise repeatable.
+ */
+q8mv_status_t q8mv_plan_transposed(q8mv_plan_t *out, int64_t K, int64_t N, int device,
+                                   const q8mv_opts_t *opts);
 
 /*
  * Batched decode: a plan for C[M,N] = A[M,K] x (W[K,N], S[KB,N]), each row of
@@ -231,7 +253,10 @@ q8mv_status_t q8mv_plan_info(q8mv_plan_t plan, q8mv_plan_info_t *info);
  * for K, N on a GPU with `sm_count` SMs.  For the register kernel (opts NULL
  * or kernel REGS/AUTO): `ctas_per_sm` resident CTAs and weight loads of
  * `vec_bytes` (which must divide N).  For opts->kernel == Q8MV_KERNEL_TMA the
- * last two are ignored.  Fills *info (workspace_bytes of partial rows).
+ * last two are ignored.  For opts->kernel == Q8MV_KERNEL_ROWS: the transposed
+ * plan's rows per CTA and warps along K, for `ctas_per_sm` resident CTAs of 16
+ * rows and loads of `vec_bytes` (16, 4 or 1).  Fills *info (workspace_bytes of
+ * partial rows).
  */
 q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t ctas_per_sm,
                                  int32_t vec_bytes, const q8mv_opts_t *opts,

@@ -29,6 +29,7 @@ KERNEL_AUTO = 0
 KERNEL_REGS = 1
 KERNEL_TMA = 2
 KERNEL_ASYNC = 3
+KERNEL_ROWS = 4
 
 ACT_NONE = 0
 ACT_RELU = 1
@@ -41,7 +42,7 @@ class Opts(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
                 ("threads_n", ctypes.c_int32), ("split_k", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("overlap", ctypes.c_int32),
-                ("cta_threads", ctypes.c_int32)]
+                ("cta_threads", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32)]
 
 
 class Epilogue(ctypes.Structure):
@@ -86,6 +87,8 @@ def _load() -> ctypes.CDLL:
     lib.q8mv_plan.restype = ctypes.c_int
     lib.q8mv_plan_batched.argtypes = [ctypes.POINTER(p), i64, i64, i64, ctypes.c_int, ctypes.POINTER(Opts)]
     lib.q8mv_plan_batched.restype = ctypes.c_int
+    lib.q8mv_plan_transposed.argtypes = [ctypes.POINTER(p), i64, i64, ctypes.c_int, ctypes.POINTER(Opts)]
+    lib.q8mv_plan_transposed.restype = ctypes.c_int
     lib.q8mv_run.argtypes = [p, p, p, p, p, p]
     lib.q8mv_run.restype = ctypes.c_int
     lib.q8mv_run_fused.argtypes = [p, p, p, p, p, ctypes.POINTER(Epilogue), p]
@@ -119,10 +122,10 @@ def library() -> ctypes.CDLL:
     return _lib
 
 
-def _opts(kernel=0, vec_bytes=0, threads_n=0, split_k=0, stages=0, overlap=0, cta_threads=0):
-    if not (kernel or vec_bytes or threads_n or split_k or stages or overlap or cta_threads):
+def _opts(kernel=0, vec_bytes=0, threads_n=0, split_k=0, stages=0, overlap=0, cta_threads=0, rows_per_cta=0):
+    if not (kernel or vec_bytes or threads_n or split_k or stages or overlap or cta_threads or rows_per_cta):
         return None
-    return Opts(kernel, vec_bytes, threads_n, split_k, stages, overlap, cta_threads)
+    return Opts(kernel, vec_bytes, threads_n, split_k, stages, overlap, cta_threads, rows_per_cta)
 
 
 def choose_config(K: int, N: int, sm_count: int, ctas_per_sm: int, vec_bytes: int, **opts) -> dict:
@@ -156,14 +159,22 @@ class Plan:
     """A q8mv plan for fixed (M, K, N) on one device; owns the split-K workspace.
 
     ``rows`` is the number M of activation rows per call (1: the single-row
-    matvec of ``q8mv_plan``; more: ``q8mv_plan_batched``)."""
+    matvec of ``q8mv_plan``; more: ``q8mv_plan_batched``).  ``transposed=True``
+    makes a plan for weights stored one output row per row
+    (``q8mv_plan_transposed``): W is then [N, K] and S is [N, KB]."""
 
-    def __init__(self, K: int, N: int, device: int = -1, rows: int = 1, **opts):
+    def __init__(self, K: int, N: int, device: int = -1, rows: int = 1, transposed: bool = False, **opts):
         self.K, self.N, self.KB = int(K), int(N), num_blocks(int(K))
         self.M = int(rows)
+        self.transposed = bool(transposed)
         handle = ctypes.c_void_p()
         o = _opts(**opts)
-        if self.M == 1:
+        if self.transposed:
+            if self.M != 1:
+                raise ValueError("transposed plans take one activation row")
+            st = _lib.q8mv_plan_transposed(ctypes.byref(handle), self.K, self.N, int(device),
+                                           ctypes.byref(o) if o else None)
+        elif self.M == 1:
             st = _lib.q8mv_plan(ctypes.byref(handle), self.K, self.N, int(device),
                                 ctypes.byref(o) if o else None)
         else:
@@ -205,8 +216,12 @@ class Plan:
         import torch
 
         _check(A, torch.float32, (self.M, self.K), "A")
-        _check(W, torch.int8, (self.K, self.N), "W")
-        _check(S, torch.float32, (self.KB, self.N), "S")
+        if self.transposed:
+            _check(W, torch.int8, (self.N, self.K), "W")
+            _check(S, torch.float32, (self.N, self.KB), "S")
+        else:
+            _check(W, torch.int8, (self.K, self.N), "W")
+            _check(S, torch.float32, (self.KB, self.N), "S")
         dev = W.device
         out_given = out is not None
         for name, t in (("A", A), ("S", S)):
@@ -301,6 +316,17 @@ def matvec(A, W, S, out=None, **epilogue):
     if plan is None:
         plan = _plans[key] = Plan(K, N, device=W.device.index, rows=M)
     return plan(A, W, S, out=out, **epilogue)
+
+
+def matvec_t(A, Wt, St, out=None, **epilogue):
+    """C[1, N] = Q8_0 matvec of A [1, K] with weights stored one output row per row:
+    Wt [N, K] int8 and St [N, KB] f32.  Plans are cached per (K, N, device)."""
+    N, K = Wt.shape
+    key = ("t", int(K), int(N), Wt.device.index)
+    plan = _plans.get(key)
+    if plan is None:
+        plan = _plans[key] = Plan(K, N, device=Wt.device.index, transposed=True)
+    return plan(A, Wt, St, out=out, **epilogue)
 
 
 def version() -> int:

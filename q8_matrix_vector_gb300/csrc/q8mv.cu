@@ -43,6 +43,7 @@
 #include "async_stream.cuh"
 #include "batched.h"
 #include "regs_kernel.cuh"
+#include "rows_kernel.cuh"
 #include "tma_stream.cuh"
 
 namespace {
@@ -578,6 +579,70 @@ q8mv_status_t choose_async(int64_t K, int64_t N, int sm_count, const q8mv_opts_t
 }  // namespace
 
 // ---------------------------------------------------------------------------
+// Rows kernel: weights stored one output row per row
+// ---------------------------------------------------------------------------
+namespace {
+
+using RowsFn = void (*)(tk::Params);
+
+RowsFn rows_kernel(int lv, int r) {
+    if (r == 16)
+        return lv == 16 ? tk::q8mv_rows_kernel<16, 16> : lv == 4 ? tk::q8mv_rows_kernel<4, 16>
+                                                                : tk::q8mv_rows_kernel<1, 16>;
+    return lv == 16 ? tk::q8mv_rows_kernel<16, 8> : lv == 4 ? tk::q8mv_rows_kernel<4, 8> : tk::q8mv_rows_kernel<1, 8>;
+}
+
+struct RowsConfig {
+    int r = 0;         // output rows per CTA
+    int wk = 0;        // warps per CTA along K
+    int64_t ctas = 0;  // grid
+};
+
+// One warp per 512-wide step of K, at most 8 (warps then take every 8th step).
+// 8 rows per CTA unless asked otherwise: three 8-row CTAs per SM measured
+// faster than one 16-row CTA on every decode shape (e.g. 70B FFN up 54 us vs
+// 83 us).
+RowsConfig choose_rows(int64_t K, int64_t N, int sm_count, int cps16, int want_r) {
+    (void)sm_count;
+    (void)cps16;
+    RowsConfig c;
+    c.wk = static_cast<int>(std::min<int64_t>(tk::kMaxWarps, std::max<int64_t>(1, ceil_div(K, tk::kStepK))));
+    c.r = want_r != 0 ? want_r : 8;
+    c.ctas = std::max<int64_t>(1, ceil_div(N, c.r));
+    return c;
+}
+
+// Widest load per lane that Wt's address, the row pitch K and the cap allow.
+int rows_lv(uintptr_t waddr, int64_t K, int cap) {
+    if (cap >= 16 && waddr % 16 == 0 && K % 16 == 0) return 16;
+    if (cap >= 4 && waddr % 4 == 0 && K % 4 == 0) return 4;
+    return 1;
+}
+
+void fill_rows_info(const RowsConfig &c, int64_t K, int lv, int sm_count, int cps, int64_t ws_bytes,
+                           q8mv_plan_info_t *info) {
+    std::memset(info, 0, sizeof(*info));
+    info->kernel = Q8MV_KERNEL_ROWS;
+    info->vec_bytes = lv;
+    info->threads_n = 32;
+    info->groups_k = c.wk;
+    info->threads_per_cta = 32 * c.wk;
+    info->split_k = 1;
+    info->blocks_per_split = static_cast<int32_t>(ceil_div(K, kBlk));
+    info->tile_n = c.r;
+    info->grid_x = c.ctas;
+    info->grid_y = 1;
+    info->workspace_bytes = ws_bytes;
+    info->sm_count = sm_count;
+    info->ctas_per_sm = cps;
+    info->rows = 1;
+    info->rows_per_pass = 1;
+    info->grid_z = 1;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
 // Plan object
 // ---------------------------------------------------------------------------
 struct q8mv_plan_s {
@@ -605,6 +670,10 @@ struct q8mv_plan_s {
     int64_t M = 1;
     int mb = 0;
     bk::Config bcfg[bk::kNumVec];
+    // transposed plans (q8mv_plan_transposed): weights stored one output row per row
+    bool rows = false;
+    RowsConfig rcfg;
+    int rows_cps = 0;
     // device memory owned by the plan
     float *ws = nullptr;
     unsigned *tickets = nullptr;
@@ -636,6 +705,15 @@ int q8mv_version(void) { return kVersion; }
 q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t ctas_per_sm,
                                  int32_t vec_bytes, const q8mv_opts_t *opts, q8mv_plan_info_t *info) {
     if (info == nullptr) return Q8MV_ERR_INVALID_ARG;
+    if (opts && opts->kernel == Q8MV_KERNEL_ROWS) {
+        if (K < 0 || N < 0 || sm_count <= 0 || ctas_per_sm <= 0) return Q8MV_ERR_INVALID_ARG;
+        if (vec_bytes != 16 && vec_bytes != 4 && vec_bytes != 1) return Q8MV_ERR_INVALID_ARG;
+        if (opts->rows_per_cta != 0 && opts->rows_per_cta != 8 && opts->rows_per_cta != 16)
+            return Q8MV_ERR_INVALID_ARG;
+        const RowsConfig c = choose_rows(K, N, sm_count, ctas_per_sm, opts->rows_per_cta);
+        fill_rows_info(c, K, vec_bytes, sm_count, ctas_per_sm, 0, info);
+        return Q8MV_OK;
+    }
     if (opts && opts->kernel != Q8MV_KERNEL_AUTO && opts->kernel != Q8MV_KERNEL_REGS &&
         opts->kernel != Q8MV_KERNEL_TMA && opts->kernel != Q8MV_KERNEL_ASYNC)
         return Q8MV_ERR_INVALID_ARG;
@@ -703,6 +781,7 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
         if (opts->split_k < 0 || opts->split_k > kMaxSplit) return Q8MV_ERR_INVALID_ARG;
         if (opts->cta_threads != 0 && opts->cta_threads != 128 && opts->cta_threads != 256)
             return Q8MV_ERR_INVALID_ARG;
+        if (opts->rows_per_cta != 0) return Q8MV_ERR_INVALID_ARG;
         if (opts->stages != 0) {
             const bool tma_ok = opts->stages >= tmak::kConsumerWarps && opts->stages <= tmak::kMaxStages &&
                                 opts->stages % tmak::kConsumerWarps == 0;
@@ -899,6 +978,11 @@ static void fill_batched_info(const bk::Config &c, int sm_count, int64_t M, int6
 q8mv_status_t q8mv_plan_info(q8mv_plan_t p, q8mv_plan_info_t *info) {
     if (p == nullptr || info == nullptr) return Q8MV_ERR_INVALID_ARG;
     std::memset(info, 0, sizeof(*info));
+    if (p->rows) {
+        fill_rows_info(p->rcfg, p->K, rows_lv(0, p->K, p->max_vec), p->sm_count, p->rows_cps, p->ws_bytes, info);
+        info->overlap = p->overlap ? 1 : 0;
+        return Q8MV_OK;
+    }
     if (p->mb > 0) {
         const int idx = batched_index(p, 0);
         if (idx < 0) return Q8MV_ERR_INVALID_ARG;
@@ -1041,6 +1125,34 @@ static q8mv_status_t run_batched(q8mv_plan_t p, const float *A, const int8_t *W,
 
 // The run path of q8mv_run and q8mv_run_fused.  With an epilogue the register
 // (or batched) kernel always runs, also for K == 0 (the product is then 0).
+static q8mv_status_t run_rows(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
+                              const q8epi::Epilogue &epi, cudaStream_t stream) {
+    const RowsConfig &c = p->rcfg;
+    tk::Params prm;
+    prm.A = A;
+    prm.W = W;
+    prm.S = S;
+    prm.C = C;
+    prm.K = p->K;
+    prm.N = p->N;
+    prm.KB = p->KB;
+    prm.wk = c.wk;
+    prm.epi = epi;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(c.ctas));
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * c.wk));
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p->overlap) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    const int lv = rows_lv(reinterpret_cast<uintptr_t>(W), p->K, p->max_vec);
+    return cuda_status(cudaLaunchKernelEx(&cfg, rows_kernel(lv, c.r), prm));
+}
+
 static q8mv_status_t run_impl(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
                               const q8epi::Epilogue &epi, cudaStream_t stream) {
     if (p == nullptr) return Q8MV_ERR_INVALID_ARG;
@@ -1063,6 +1175,7 @@ static q8mv_status_t run_impl(q8mv_plan_t p, const float *A, const int8_t *W, co
             overlaps(C, c_bytes, S, 4 * static_cast<int64_t>(p->KB) * N))
             return Q8MV_ERR_INVALID_ARG;
     }
+    if (p->rows) return run_rows(p, A, W, S, C, epi, stream);
     if (p->mb > 0) return run_batched(p, A, W, S, C, epi, stream);
 
     const uintptr_t waddr = reinterpret_cast<uintptr_t>(W);
@@ -1173,6 +1286,7 @@ static bool batched_opts_ok(int mb, const q8mv_opts_t *o) {
     if (o == nullptr) return true;
     if (o->kernel != Q8MV_KERNEL_AUTO && o->kernel != Q8MV_KERNEL_REGS) return false;
     if (o->stages != 0 || (o->cta_threads != 0 && o->cta_threads != bk::kThreads)) return false;
+    if (o->rows_per_cta != 0) return false;
     if (o->overlap != 0 && o->overlap != 1) return false;
     if (o->vec_bytes != 0 && !((o->vec_bytes == 8 || o->vec_bytes == 4 || o->vec_bytes == 1) &&
                                bk::vec_built(mb, o->vec_bytes)))
@@ -1274,6 +1388,78 @@ q8mv_status_t q8mv_plan_batched(q8mv_plan_t *out, int64_t M, int64_t K, int64_t 
     p->n_tickets = ws_floats > 0 ? n_tickets : 0;
     p->ws_bytes = ws_floats * static_cast<int64_t>(sizeof(float)) + p->n_tickets * 4 + 4;
 
+    if (device != prev) cudaSetDevice(prev);
+    *out = p;
+    return Q8MV_OK;
+}
+
+q8mv_status_t q8mv_plan_transposed(q8mv_plan_t *out, int64_t K, int64_t N, int device, const q8mv_opts_t *opts) {
+    if (out == nullptr) return Q8MV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (K < 0 || N < 0 || K >= (1LL << 31) || N >= (1LL << 31)) return Q8MV_ERR_INVALID_ARG;
+    if (N > 0 && K > ((1LL << 62) / N)) return Q8MV_ERR_INVALID_ARG;
+    if (opts) {
+        if (opts->kernel != Q8MV_KERNEL_AUTO && opts->kernel != Q8MV_KERNEL_ROWS) return Q8MV_ERR_INVALID_ARG;
+        if (opts->vec_bytes != 0 && opts->vec_bytes != 16 && opts->vec_bytes != 4 && opts->vec_bytes != 1)
+            return Q8MV_ERR_INVALID_ARG;
+        if (opts->rows_per_cta != 0 && opts->rows_per_cta != 8 && opts->rows_per_cta != 16)
+            return Q8MV_ERR_INVALID_ARG;
+        if (opts->overlap != 0 && opts->overlap != 1) return Q8MV_ERR_INVALID_ARG;
+        if (opts->threads_n != 0 || opts->split_k != 0 || opts->stages != 0 || opts->cta_threads != 0)
+            return Q8MV_ERR_INVALID_ARG;
+    }
+    int prev = 0;
+    q8mv_status_t st = cuda_status(cudaGetDevice(&prev));
+    if (st != Q8MV_OK) return st;
+    if (device < 0) device = prev;
+    int ndev = 0;
+    st = cuda_status(cudaGetDeviceCount(&ndev));
+    if (st != Q8MV_OK) return st;
+    if (device >= ndev) return Q8MV_ERR_INVALID_ARG;
+    if (device != prev) {
+        st = cuda_status(cudaSetDevice(device));
+        if (st != Q8MV_OK) return st;
+    }
+    q8mv_plan_s *p = new (std::nothrow) q8mv_plan_s();
+    if (p == nullptr) {
+        if (device != prev) cudaSetDevice(prev);
+        return Q8MV_ERR_OUT_OF_MEMORY;
+    }
+    auto fail = [&](q8mv_status_t s) {
+        if (p->err) cudaFree(p->err);
+        delete p;
+        if (device != prev) cudaSetDevice(prev);
+        return s;
+    };
+    p->K = K;
+    p->N = N;
+    p->KB = static_cast<int>(ceil_div(K, kBlk));
+    p->device = device;
+    p->rows = true;
+    p->max_vec = (opts && opts->vec_bytes) ? opts->vec_bytes : 16;
+    p->forced_vec = opts && opts->vec_bytes != 0;
+    p->overlap = opts && opts->overlap == 1;
+
+    int major = 0, minor = 0;
+    st = cuda_status(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device));
+    if (st == Q8MV_OK) st = cuda_status(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device));
+    if (st == Q8MV_OK) st = cuda_status(cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, device));
+    if (st != Q8MV_OK) return fail(st);
+    if (major != 10 || minor != 3) return fail(Q8MV_ERR_UNSUPPORTED_DEVICE);
+    int cps16 = 1;
+    st = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cps16, rows_kernel(16, 16), 256, 0));
+    if (st != Q8MV_OK) return fail(st == Q8MV_ERR_CUDA ? Q8MV_ERR_UNSUPPORTED_DEVICE : st);
+    p->rcfg = choose_rows(K, N, p->sm_count, cps16, opts ? opts->rows_per_cta : 0);
+    int cps = 1;
+    st = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cps, rows_kernel(16, p->rcfg.r),
+                                                                   32 * p->rcfg.wk, 0));
+    if (st != Q8MV_OK) return fail(st);
+    p->rows_cps = cps;
+    st = cuda_status(cudaMalloc(&p->err, sizeof(int)));
+    if (st == Q8MV_OK) st = cuda_status(cudaMemset(p->err, 0, sizeof(int)));
+    if (st == Q8MV_OK) st = cuda_status(cudaDeviceSynchronize());
+    if (st != Q8MV_OK) return fail(st);
+    p->ws_bytes = 4;
     if (device != prev) cudaSetDevice(prev);
     *out = p;
     return Q8MV_OK;

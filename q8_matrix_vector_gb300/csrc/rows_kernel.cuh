@@ -1,0 +1,212 @@
+// q8mv rows kernel: Q8_0 weights stored one output row per row (sm_103a).
+//
+//   C[n] = sum_b St[n, b] * ( sum_{k in block b} A[k] * Wt[n, k] )
+//
+// Wt [N, K] holds output n's bytes in row n and St [N, KB] its block scales:
+// the layout dot_t contracts ("dot and tensor cores" page: the last axis of
+// both operands, as a linear layer stores its weights), applied to the Q8_0
+// product of the "Q8_0 matvec" page ("The tensors", "Factoring out the
+// scale", "Bounds").
+//
+// Mapping: a CTA owns R consecutive output rows.  Its warps split K into steps
+// of 512 (16 blocks), warp w taking steps w, w + wk, ...; within a step lane l
+// covers the 16 consecutive k of half a block, so one 16-byte load per lane and
+// row reads 512 contiguous bytes per warp.  The lane converts its bytes exactly
+// (byte permute into the mantissa of 2^23, packed subtract) and multiplies them
+// with its 16 activations in packed f32x2 FMAs; the two lanes of a block add
+// their halves with one shuffle, and the even lane applies the block's scale
+// once.  After its steps each warp sums its lanes per row (fixed butterfly), and
+// the CTA adds the warps in order in shared memory before writing C.
+#pragma once
+
+#include <cstdint>
+
+#include "epilogue.cuh"
+
+namespace tk {
+
+constexpr int kBlk = 32;
+constexpr int kLaneK = 16;             // k per lane and step: half a block
+constexpr int kStepK = 32 * kLaneK;    // k per warp and step: 16 blocks
+constexpr int kMaxWarps = 8;
+
+struct Params {
+    const float *A;  // [K]
+    const int8_t *W; // [N, K]
+    const float *S;  // [N, KB]
+    float *C;        // [N]
+    int64_t K, N;
+    int KB;
+    int wk;          // warps per CTA along K
+    q8epi::Epilogue epi;
+};
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ float2 cvt2(uint32_t flipped, uint32_t sel_lo, uint32_t sel_hi) {
+    const float2 t = make_float2(__uint_as_float(__byte_perm(flipped, 0x4B000000u, sel_lo)),
+                                 __uint_as_float(__byte_perm(flipped, 0x4B000000u, sel_hi)));
+    return __fadd2_rn(t, make_float2(-8388736.0f, -8388736.0f));
+}
+
+__device__ __forceinline__ uint32_t load_byte(const int8_t *p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v & 0xFFu;
+}
+
+// The 16 bytes of `row` from byte k (k < K) into w, little-endian words;
+// bytes at or past K are 0 (they convert to 0) and are not read.
+//   LV = 16: one 16-byte load (rows 16-byte aligned), streamed past L1.
+//   LV = 4:  four 4-byte loads (rows 4-byte aligned), through L1 so that the
+//            warp's four loads of a 512-byte span reach L2 once.
+//   LV = 1:  sixteen byte loads (any alignment), through L1 likewise.
+template <int LV>
+__device__ __forceinline__ void load_chunk(const int8_t *row, int64_t k, int64_t K, uint32_t (&w)[4]) {
+    const int8_t *p = row + k;
+    if (k + kLaneK <= K) {
+        if constexpr (LV == 16) {
+            asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                         : "l"(p)
+                         : "memory");
+        } else if constexpr (LV == 4) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(w[q]) : "l"(p + 4 * q) : "memory");
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                w[q] = load_byte(p + 4 * q) | (load_byte(p + 4 * q + 1) << 8) | (load_byte(p + 4 * q + 2) << 16) |
+                       (load_byte(p + 4 * q + 3) << 24);
+        }
+    } else {
+        // the row's ragged end: only bytes below K (unrolled, so that w stays in registers)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) w[q] = 0u;
+#pragma unroll
+        for (int i = 0; i < kLaneK; ++i)
+            if (k + i < K) w[i / 4] |= load_byte(p + i) << (8 * (i % 4));
+    }
+}
+
+// A step's loads: the lane's 16 bytes of each of the CTA's rows and, on the
+// even lane of each block pair, the rows' scales of that block; zeros past the
+// CTA's rows or past K.  W and S are never written by overlapped work.
+template <int LV, int R>
+__device__ __forceinline__ void load_step(const Params &p, const int8_t *w_base, const float *s_base, int nrows,
+                                          int64_t k, bool even, uint32_t (&w)[R][4], float (&s)[R]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        if (r < nrows && k < p.K) {
+            load_chunk<LV>(w_base + r * p.K, k, p.K, w[r]);
+            s[r] = even ? __ldg(s_base + r * p.KB + k / kBlk) : 0.0f;
+        } else {
+            w[r][0] = w[r][1] = w[r][2] = w[r][3] = 0u;
+            s[r] = 0.0f;
+        }
+    }
+}
+
+// The lane's 16 activations from k, zeros at or past K.
+__device__ __forceinline__ void load_a(const Params &p, int64_t k, float2 (&a2)[8]) {
+    if (k + kLaneK <= p.K && (reinterpret_cast<uintptr_t>(p.A + k) & 15u) == 0) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 t = __ldg(reinterpret_cast<const float4 *>(p.A + k) + q);
+            a2[2 * q] = make_float2(t.x, t.y);
+            a2[2 * q + 1] = make_float2(t.z, t.w);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float lo = k + 2 * i < p.K ? __ldg(p.A + k + 2 * i) : 0.0f;
+            const float hi = k + 2 * i + 1 < p.K ? __ldg(p.A + k + 2 * i + 1) : 0.0f;
+            a2[i] = make_float2(lo, hi);
+        }
+    }
+}
+
+// 8-row CTAs fit three per SM in registers (measured best); 16-row CTAs hold
+// twice the loads in flight per thread and take the register file of one CTA
+// per SM.
+template <int R>
+constexpr int rows_min_blocks() {
+    return R <= 8 ? 3 : 1;
+}
+
+template <int LV, int R>
+__global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_rows_kernel(const Params p) {
+    __shared__ float part[kMaxWarps][R];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const bool even = (lane & 1) == 0;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * R;
+    const int nrows = static_cast<int>(min(static_cast<int64_t>(R), p.N - n0));
+    const int64_t step = static_cast<int64_t>(p.wk) * kStepK;
+    const int8_t *w_base = p.W + n0 * p.K;
+    const float *s_base = p.S + n0 * p.KB;
+
+    // the first step's weights and scales before the dependency wait, its
+    // activations after it; a later step's loads follow the arithmetic of the
+    // step before it (three CTAs per SM keep other warps' loads in flight)
+    uint32_t w[R][4];
+    float s[R];
+    int64_t k0 = static_cast<int64_t>(warp) * kStepK;
+    load_step<LV, R>(p, w_base, s_base, nrows, k0 + lane * kLaneK, even, w, s);
+    pdl_launch_dependents();
+    pdl_wait();
+    float2 a2[8];
+    load_a(p, k0 + lane * kLaneK, a2);
+
+    float acc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = 0.0f;
+
+    for (; k0 < p.K; k0 += step) {
+        // per row: 16 products per lane in two packed lanes (k in order within
+        // each), the block's other half by one shuffle, then one scale per
+        // block (the even lane's s; 0 on the odd lane)
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            float2 s2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t u = w[r][q] ^ 0x80808080u;
+                s2 = __ffma2_rn(a2[2 * q], cvt2(u, 0x7440u, 0x7441u), s2);
+                s2 = __ffma2_rn(a2[2 * q + 1], cvt2(u, 0x7442u, 0x7443u), s2);
+            }
+            float blk = s2.x + s2.y;
+            blk += __shfl_xor_sync(0xffffffffu, blk, 1);
+            acc[r] = fmaf(blk, s[r], acc[r]);
+        }
+        // the next step's loads, once this step's registers are free
+        const int64_t kn = k0 + step + lane * kLaneK;
+        if (k0 + step < p.K) {
+            load_step<LV, R>(p, w_base, s_base, nrows, kn, even, w, s);
+            load_a(p, kn, a2);
+        }
+    }
+
+    // lanes of the warp per row (fixed butterfly), then the warps in order
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        float v = acc[r];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) part[warp][r] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < nrows) {
+        const int t = threadIdx.x;
+        float v = part[0][t];
+        for (int q = 1; q < p.wk; ++q) v += part[q][t];
+        const int64_t n = n0 + t;
+        p.C[n] = q8epi::apply(p.epi, v, p.C, n, n);
+    }
+}
+
+}  // namespace tk

@@ -306,3 +306,50 @@ def test_batched_plan_rejects_bad_arguments_before_touching_a_device(q8):
     assert lib.q8mv_plan_batched(ctypes.byref(h), 4, 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
     bad = q8.Opts(0, 0, 0, 0, 0, 0, 128)
     assert lib.q8mv_plan_batched(ctypes.byref(h), 4, 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+
+
+# ----------------------------------------------------------------------------
+# rows planner (weights stored one output row per row; pure host function)
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("K,N", [(4096, 4096), (4096, 11008), (11008, 4096), (4100, 128256), (1, 1), (513, 17),
+                                 (0, 64), (64, 0)])
+def test_rows_planner_covers_every_row_and_step(q8, K, N):
+    for vec in (16, 4, 1):
+        for r in (0, 8, 16):
+            c = q8.choose_config(K, N, 152, 2, vec, kernel=q8.KERNEL_ROWS, rows_per_cta=r)
+            assert c["kernel"] == q8.KERNEL_ROWS and c["vec_bytes"] == vec
+            assert c["tile_n"] in (8, 16) and (r == 0 or c["tile_n"] == r)
+            assert c["grid_x"] * c["tile_n"] >= N and (c["grid_x"] - 1) * c["tile_n"] < max(N, 1)
+            # one warp per 512-wide step of K, at most 8
+            steps = max(1, (K + 511) // 512)
+            assert c["groups_k"] == min(8, steps) and c["threads_per_cta"] == 32 * c["groups_k"]
+            assert c["split_k"] == 1 and c["workspace_bytes"] == 0
+
+
+def test_rows_planner_picks_rows_per_cta(q8):
+    # 8 rows per CTA by default (measured faster than 16 on every decode shape)
+    for N in (200, 4096, 128256):
+        assert q8.choose_config(4096, N, 152, 3, 16, kernel=q8.KERNEL_ROWS)["tile_n"] == 8
+    assert q8.choose_config(4096, 4096, 152, 3, 16, kernel=q8.KERNEL_ROWS, rows_per_cta=16)["tile_n"] == 16
+
+
+def test_rows_planner_rejects_illegal_requests(q8):
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config(64, 64, 152, 2, 8, kernel=q8.KERNEL_ROWS)  # no 8-byte lane load
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config(64, 64, 152, 2, 16, kernel=q8.KERNEL_ROWS, rows_per_cta=12)
+
+
+def test_transposed_plan_rejects_bad_arguments_before_touching_a_device(q8):
+    lib = q8.library()
+    h = ctypes.c_void_p(1234)
+    assert lib.q8mv_plan_transposed(ctypes.byref(h), -1, 64, -1, None) == q8.Q8MV_ERR_INVALID_ARG
+    assert h.value is None
+    assert lib.q8mv_plan_transposed(None, 64, 64, -1, None) == q8.Q8MV_ERR_INVALID_ARG
+    for bad in (q8.Opts(0, 8, 0, 0, 0, 0, 0, 0), q8.Opts(0, 0, 32, 0, 0, 0, 0, 0), q8.Opts(0, 0, 0, 2, 0, 0, 0, 0),
+                q8.Opts(0, 0, 0, 0, 0, 0, 0, 12), q8.Opts(q8.KERNEL_TMA, 0, 0, 0, 0, 0, 0, 0)):
+        assert lib.q8mv_plan_transposed(ctypes.byref(h), 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+    # rows_per_cta belongs to transposed plans only
+    bad = q8.Opts(0, 0, 0, 0, 0, 0, 0, 8)
+    assert lib.q8mv_plan(ctypes.byref(h), 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+    assert lib.q8mv_plan_batched(ctypes.byref(h), 4, 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
