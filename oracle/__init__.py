@@ -59,6 +59,10 @@ class Oracle:
         lib.q8mv_oracle_epilogue.restype = ctypes.c_int
         lib.q8mv_oracle_transposed.argtypes = [i64, i64, p, p, p, p, p]
         lib.q8mv_oracle_transposed.restype = ctypes.c_int
+        lib.q8mv_oracle_quantize.argtypes = [i64, p, p, p]
+        lib.q8mv_oracle_quantize.restype = ctypes.c_int
+        lib.q8mv_oracle_i8.argtypes = [i64, i64, p, p, p, p, p, p]
+        lib.q8mv_oracle_i8.restype = ctypes.c_int
         self._lib = lib
 
     @staticmethod
@@ -164,6 +168,40 @@ class Oracle:
                                               self._ptr(C), self._ptr(bound))
         if rc != 0:
             raise RuntimeError(f"q8mv_oracle_transposed returned {rc}")
+        return C, bound
+
+    def quantize(self, A):
+        """Per-32-block int8 codes of A [K] (or [M, K], row by row): return (q int8, d f32 [.., KB])."""
+        A = np.ascontiguousarray(A, dtype=np.float32)
+        rows = A.reshape(-1, A.shape[-1]) if A.ndim == 2 else A.reshape(1, -1)
+        M, K = rows.shape
+        KB = (K + 31) // 32
+        q = np.zeros((M, K), np.int8)
+        d = np.full((M, KB), np.nan, np.float32)
+        for m in range(M):
+            qm = np.zeros(K, np.int8)
+            dm = np.zeros(KB, np.float32)
+            rc = self._lib.q8mv_oracle_quantize(K, self._ptr(rows[m]), self._ptr(qm), self._ptr(dm))
+            if rc != 0:
+                raise RuntimeError(f"q8mv_oracle_quantize returned {rc}")
+            q[m], d[m] = qm, dm
+        if A.ndim != 2:
+            return q[0], d[0]
+        return q, d
+
+    def i8(self, q, d, Wt, St):
+        """Return (C, bound), fp64 [N]: int8 activations (q, d) against Wt [N, K], St [N, KB]."""
+        Wt = np.ascontiguousarray(Wt, dtype=np.int8)
+        N, K = Wt.shape
+        q = np.ascontiguousarray(q, dtype=np.int8).reshape(K)
+        d = np.ascontiguousarray(d, dtype=np.float32).reshape((K + 31) // 32)
+        St = np.ascontiguousarray(St, dtype=np.float32)
+        C = np.full(N, np.nan)
+        bound = np.full(N, np.nan)
+        rc = self._lib.q8mv_oracle_i8(K, N, self._ptr(q), self._ptr(d), self._ptr(Wt), self._ptr(St),
+                                      self._ptr(C), self._ptr(bound))
+        if rc != 0:
+            raise RuntimeError(f"q8mv_oracle_i8 returned {rc}")
         return C, bound
 
     def block_sums(self, A, W):

@@ -254,3 +254,79 @@ int q8mv_oracle_transposed(int64_t K, int64_t N, const float *A, const int8_t *W
     }
     return 0;
 }
+
+/*
+ * Int8 activations ("dot and tensor cores" page, "Hardware paths": an i8
+ * dot_t accumulates in i32, and a single row takes dp4a).  The pages do not
+ * say how an f32 activation row becomes i8; the reading used here quantizes
+ * each 32-element block b of A on its own, in f32 arithmetic:
+ *     amax_b = max_{k in b} |A[k]|
+ *     d_b    = amax_b / 127                    (f32 division)
+ *     q[k]   = rint(A[k] * (127 / amax_b))     (f32 division once, f32 product,
+ *                                               round half to even, clamped to
+ *                                               -127 .. 127; q = 0 if amax_b = 0)
+ * so that A[k] is approximately q[k] * d_b.  Every operation is a single IEEE
+ * f32 operation (no contraction), so any IEEE implementation gets the same q.
+ */
+int q8mv_oracle_quantize(int64_t K, const float *A, int8_t *q, float *d) {
+    if (K < 0) return -1;
+    if (K > 0 && (A == NULL || q == NULL || d == NULL)) return -1;
+    const int64_t KB = oracle_num_blocks(K);
+    for (int64_t b = 0; b < KB; ++b) {
+        const int64_t k_begin = b * Q8MV_ORACLE_BLK;
+        int64_t k_end = k_begin + Q8MV_ORACLE_BLK;
+        if (k_end > K) k_end = K;
+        float amax = 0.0f;
+        for (int64_t k = k_begin; k < k_end; ++k) {
+            const float a = fabsf(A[k]);
+            if (a > amax) amax = a;
+        }
+        const float db = amax / 127.0f;
+        const float id = amax > 0.0f ? 127.0f / amax : 0.0f;
+        d[b] = db;
+        for (int64_t k = k_begin; k < k_end; ++k) {
+            const float x = A[k] * id;
+            float r = rintf(x);
+            if (r > 127.0f) r = 127.0f;
+            if (r < -127.0f) r = -127.0f;
+            q[k] = (int8_t)r;
+        }
+    }
+    return 0;
+}
+
+/*
+ * The Q8_0 product with int8 activations, weights stored one output row per
+ * row (Wt [N, K], St [N, KB]): each block's dot product of codes is an exact
+ * integer, scaled once by the activation block's d_b and the weight block's
+ * scale:
+ *     C[n] = sum_b (d_b * St[n, b]) * ( sum_{k in b} q[k] * Wt[n, k] )
+ * in fp64.  bound (nullable) receives sum_b |d_b St[n, b]| * sum_k |q[k] Wt[n, k]|.
+ */
+int q8mv_oracle_i8(int64_t K, int64_t N, const int8_t *q, const float *d, const int8_t *Wt, const float *St,
+                   double *C, double *bound) {
+    if (K < 0 || N < 0) return -1;
+    if (N > 0 && C == NULL) return -1;
+    if (K > 0 && N > 0 && (q == NULL || d == NULL || Wt == NULL || St == NULL)) return -1;
+    const int64_t KB = oracle_num_blocks(K);
+    for (int64_t n = 0; n < N; ++n) {
+        double acc = 0.0, mag = 0.0;
+        for (int64_t b = 0; b < KB; ++b) {
+            const int64_t k_begin = b * Q8MV_ORACLE_BLK;
+            int64_t k_end = k_begin + Q8MV_ORACLE_BLK;
+            if (k_end > K) k_end = K;
+            int64_t isum = 0, iabs = 0;
+            for (int64_t k = k_begin; k < k_end; ++k) {
+                const int64_t p = (int64_t)q[k] * (int64_t)Wt[n * K + k];
+                isum += p;
+                iabs += p < 0 ? -p : p;
+            }
+            const double scale = (double)d[b] * (double)St[n * KB + b];
+            acc += scale * (double)isum;
+            mag += fabs(scale) * (double)iabs;
+        }
+        C[n] = acc;
+        if (bound) bound[n] = mag;
+    }
+    return 0;
+}

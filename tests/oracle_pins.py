@@ -19,7 +19,11 @@ the oracle disagrees with an independent fact:
   bias per column and residual per element, their order around the
   activation, and the activations against scipy's expit and torch's gelu;
 - for weights stored one output row per row (Wt [N, K], St [N, KB]): exact
-  rational brute force, bit-equality with the column layout, one-hot cases.
+  rational brute force, bit-equality with the column layout, one-hot cases;
+- for int8 activations: the codes of amax = 127 blocks against Python's
+  round-half-even, reconstruction within d/2 with the block maximum at +-127,
+  power-of-two scale invariance, the integer product against numpy int64
+  block dots, and equality with the f32 product when the codes are exact.
 
 The pins are shared by ``test_oracle_pins.py`` (the real oracle must pass all)
 and ``test_oracle_mutants.py`` (each planted mistake must fail at least one).
@@ -408,6 +412,80 @@ def pin_transposed_one_hot(orc):
     assert np.array_equal(C, [0, 0, 0, 0, K, 0])
 
 
+def pin_quantize_rounding_and_extremes(orc):
+    """With amax = 127 the reciprocal is exactly 1, so q = rint(a): half to even."""
+    a = np.array([2.5, 3.5, -2.5, 126.5, 127.0, -127.0, 0.5, 1.5, -0.5, 0.49, 100.25, -3.75] + [0.0] * 20,
+                 np.float32)
+    q, d = orc.quantize(a)
+    assert d.tolist() == [1.0]
+    assert q.tolist() == [round(float(x)) for x in a]  # Python rounds half to even
+    q, d = orc.quantize(np.zeros(40, np.float32))
+    assert not q.any() and d.tolist() == [0.0, 0.0]
+
+
+def pin_quantize_reconstruction(orc):
+    """|q d - a| <= d/2 (plus f32 rounding), the largest |a| of a block maps to +-127,
+    and no code leaves -127 .. 127; blocks are independent (K = 100: 32, 32, 32, 4)."""
+    rng = _rng(500)
+    a = (rng.standard_normal(100) * np.exp(rng.uniform(-8, 8, size=100))).astype(np.float32)
+    q, d = orc.quantize(a)
+    assert q.dtype == np.int8 and d.shape == (4,)
+    for b in range(4):
+        blk = a[32 * b:32 * b + 32].astype(np.float64)
+        qb = q[32 * b:32 * b + 32].astype(np.float64)
+        amax = np.max(np.abs(blk))
+        assert d[b] == np.float32(np.float32(amax) / np.float32(127))
+        assert np.all(np.abs(qb * float(d[b]) - blk) <= 0.5 * float(d[b]) * (1 + 1e-6) + 1e-7 * amax)
+        i = int(np.argmax(np.abs(blk)))
+        assert abs(int(qb[i])) == 127 and np.sign(qb[i]) == np.sign(blk[i])
+    assert np.all(np.abs(q.astype(int)) <= 127)
+
+
+def pin_quantize_scale_invariance(orc):
+    """Scaling A by a power of two scales d by it and leaves every code alone."""
+    rng = _rng(501)
+    a = rng.uniform(-3, 3, 96).astype(np.float32)
+    q, d = orc.quantize(a)
+    for j in (-20, -3, 5, 30):
+        qj, dj = orc.quantize((a * np.float32(2.0 ** j)).astype(np.float32))
+        assert np.array_equal(qj, q) and np.array_equal(dj, (d * np.float32(2.0 ** j)).astype(np.float32)), j
+
+
+def pin_i8_integer_closed_form(orc):
+    """Power-of-two d and St make every term exact: compare with numpy int64 block dots."""
+    rng = _rng(502)
+    K, N = 100, 9
+    q = rng.integers(-127, 128, K).astype(np.int8)
+    Wt = rng.integers(-128, 128, (N, K)).astype(np.int8)
+    KB = 4
+    d = (2.0 ** rng.integers(-6, 3, KB)).astype(np.float32)
+    St = (2.0 ** rng.integers(-9, 1, (N, KB))).astype(np.float32)
+    C, bound = orc.i8(q, d, Wt, St)
+    for n in range(N):
+        isums = [int(np.dot(q[32 * b:32 * b + 32].astype(np.int64), Wt[n, 32 * b:32 * b + 32].astype(np.int64)))
+                 for b in range(KB)]
+        assert C[n] == sum(float(d[b]) * float(St[n, b]) * isums[b] for b in range(KB)), n
+        iabs = [int(np.sum(np.abs(q[32 * b:32 * b + 32].astype(np.int64) * Wt[n, 32 * b:32 * b + 32])))
+                for b in range(KB)]
+        assert bound[n] == sum(float(d[b]) * float(St[n, b]) * iabs[b] for b in range(KB)), n
+
+
+def pin_i8_equals_f32_product_when_codes_are_exact(orc):
+    """Integer activations whose every block reaches |a| = 127 quantize to themselves
+    with d = 1, so the int8 product equals the f32-activation product bit for bit."""
+    rng = _rng(503)
+    K, N = 4100, 12
+    A = rng.integers(-126, 127, K).astype(np.float32)
+    A[::32] = 127.0  # every block, including the partial last one, holds 127
+    _, W, S = workloads.make_random(K, N, seed=504)
+    Wt, St = np.ascontiguousarray(W.T), np.ascontiguousarray(S.T)
+    q, d = orc.quantize(A)
+    assert np.array_equal(q.astype(np.float32), A) and np.all(d == 1.0)
+    C8, _ = orc.i8(q, d, Wt, St)
+    C32, _ = orc.transposed(A, Wt, St)
+    assert np.array_equal(C8, C32)
+
+
 ALL_PINS = [
     pin_exact_rational,
     pin_closed_form_ones,
@@ -431,4 +509,9 @@ ALL_PINS = [
     pin_transposed_exact_rational,
     pin_transposed_matches_column_layout,
     pin_transposed_one_hot,
+    pin_quantize_rounding_and_extremes,
+    pin_quantize_reconstruction,
+    pin_quantize_scale_invariance,
+    pin_i8_integer_closed_form,
+    pin_i8_equals_f32_product_when_codes_are_exact,
 ]

@@ -64,6 +64,14 @@ MUTANTS = {
                                "const double s = (double)s_row[b == 0 ? 0 : b - 1];"),
     "t_drop_masked_rows": ("            if (k_end > K) k_end = K;\n            double part = 0.0, part_mag = 0.0;",
                            "            if (k_end > K) k_end = k_begin;\n            double part = 0.0, part_mag = 0.0;"),
+    "qa_no_abs": ("const float a = fabsf(A[k]);", "const float a = A[k];"),
+    "qa_d_by_128": ("const float db = amax / 127.0f;", "const float db = amax / 128.0f;"),
+    "qa_truncate": ("float r = rintf(x);", "float r = truncf(x);"),
+    "qa_round_half_away": ("float r = rintf(x);", "float r = roundf(x);"),
+    "i8_next_scale": ("const double scale = (double)d[b] * (double)St[n * KB + b];",
+                      "const double scale = (double)d[b] * (double)St[n * KB + (b + 1) % KB];"),
+    "i8_unsigned_codes": ("const int64_t p = (int64_t)q[k] * (int64_t)Wt[n * K + k];",
+                          "const int64_t p = (int64_t)(uint8_t)q[k] * (int64_t)Wt[n * K + k];"),
 }
 
 
