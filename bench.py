@@ -7,7 +7,8 @@ otherwise; with ``--rows M`` a step is one batched call of M activation rows
 against the same weights, with ``--epilogue ACT`` the call also applies the
 fused epilogue C = act(product + bias) + residual as it writes C, and with
 ``--transposed`` the weights are stored one output row per row (Wt [N, K],
-St [N, KB]).  The timed region replays CUDA graphs of back-to-back calls that
+St [N, KB]); ``--a-int8`` (with ``--transposed``) quantizes the activations
+to int8 per 32-element block inside the kernel and multiplies with dp4a.  The timed region replays CUDA graphs of back-to-back calls that
 rotate over enough distinct copies of the inputs to exceed twice the L2, so
 every call streams its weights from HBM.
 
@@ -105,9 +106,9 @@ def kernel_source_hash(name: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def traffic_key(workload: str, rows: int, transposed: bool = False) -> str:
+def traffic_key(workload: str, rows: int, transposed: bool = False, a_int8: bool = False) -> str:
     if transposed:
-        return f"{workload}_t"
+        return f"{workload}_t" + ("8" if a_int8 else "")
     return workload if rows == 1 else f"{workload}_m{rows}"
 
 
@@ -217,7 +218,7 @@ def run_ours(args, rank, local_rank, world):
     plan_opts = dict(kernel=kernel, split_k=args.split, stages=args.stages, threads_n=args.threads_n,
                      cta_threads=args.cta_threads)
     if args.transposed:
-        plan_opts = dict(vec_bytes=0)
+        plan_opts = dict(kernel=q8mv.KERNEL_ROWS_I8 if args.a_int8 else 0)
     plan = q8mv.Plan(K, N, device=local_rank, rows=M, transposed=args.transposed, overlap=int(overlap), **plan_opts)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0)) or 126 * 1024 * 1024
@@ -292,7 +293,7 @@ def run_ours(args, rank, local_rank, world):
     peak, peak_kind = read_hbm_peak()
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} copy bandwidth",
-                "traffic": recorded_traffic(traffic_key(args.workload, M, args.transposed)),
+                "traffic": recorded_traffic(traffic_key(args.workload, M, args.transposed, args.a_int8)),
                 "algorithmic_bytes_per_launch": bytes_per_call}
 
     # end to end through the public binding: pinned host inputs in, result out
@@ -354,7 +355,8 @@ def run_ours(args, rank, local_rank, world):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(A, W, S, bytes_per_call, args.cpu_seconds, wl, M,
-                           (bias_h, res_h, EPILOGUE_ACTS[args.epilogue]) if fused else None, args.transposed)
+                           (bias_h, res_h, EPILOGUE_ACTS[args.epilogue]) if fused else None, args.transposed,
+                           args.a_int8)
 
     if rank != 0:
         return None
@@ -368,7 +370,8 @@ def run_ours(args, rank, local_rank, world):
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{wl.name}: {wl.description}" + (f", batched decode of M={M} rows" if M > 1 else "")
                                + (f", fused epilogue act({args.epilogue})(x + bias) + residual" if fused else "")
-                               + (", weights stored one output row per row" if args.transposed else ""),
+                               + (", weights stored one output row per row" if args.transposed else "")
+                               + (", int8 activations (dp4a)" if args.a_int8 else ""),
                    "K": K, "N": N, "KB": KB, "M": M, "epilogue": args.epilogue,
                    "layout": "Wt [N,K], St [N,KB]" if args.transposed else "W [K,N], S [KB,N]",
                    "weights": "Q8_0: int8 W [K,N], f32 scales [KB,N], f32 A [M,K] and C [M,N]",
@@ -444,12 +447,14 @@ def time_calls(plan, ptrs, stream, calls, reps=3, epis=None):
     return best
 
 
-def cpu_baseline(A, W, S, bytes_per_call, seconds, wl, M=1, epilogue=None, transposed=False):
+def cpu_baseline(A, W, S, bytes_per_call, seconds, wl, M=1, epilogue=None, transposed=False, a_int8=False):
     """The fp64 oracle, as it stands, on the host cores: full calls for ~seconds."""
     import oracle
 
     orc = oracle.load()
-    if transposed:
+    if a_int8:
+        product = lambda: orc.i8(*orc.quantize(A.reshape(-1)), W, S)  # noqa: E731
+    elif transposed:
         product = lambda: orc.transposed(A, W, S)  # noqa: E731
     else:
         product = (lambda: orc.factored(A, W, S)) if M == 1 else (lambda: orc.batched(A, W, S))
@@ -496,6 +501,9 @@ def run_reference(args, rank, world):
     if args.transposed:
         W, S = np.ascontiguousarray(W.T), np.ascontiguousarray(S.T)
         product = orc.transposed
+    if args.a_int8:
+        def product(A, W, S):
+            return orc.i8(*orc.quantize(A.reshape(-1)), W, S)
     fused = args.epilogue != "none"
     bias_h, res_h = epilogue_inputs(wl.N, M) if fused else (None, None)
     act = EPILOGUE_ACTS[args.epilogue]
@@ -538,7 +546,8 @@ def run_reference(args, rank, world):
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{wl.name}: {wl.description}" + (f", batched decode of M={M} rows" if M > 1 else "")
                                + (f", fused epilogue act({args.epilogue})(x + bias) + residual" if fused else "")
-                               + (", weights stored one output row per row" if args.transposed else ""),
+                               + (", weights stored one output row per row" if args.transposed else "")
+                               + (", int8 activations (dp4a)" if args.a_int8 else ""),
                    "K": wl.K, "N": wl.N, "KB": wl.KB, "M": M, "epilogue": args.epilogue},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
@@ -559,6 +568,8 @@ def parse_args(argv=None):
                     help="fused epilogue: C = act(product + bias) + residual as C is written")
     ap.add_argument("--transposed", action="store_true",
                     help="weights stored one output row per row: Wt [N, K], St [N, KB] (dot_t layout)")
+    ap.add_argument("--a-int8", action="store_true",
+                    help="with --transposed: int8 activations per 32-element block, dp4a products")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=CPU_BASELINE_SECONDS)
     ap.add_argument("--reference-seconds", type=float, default=60.0,
@@ -582,6 +593,8 @@ def parse_args(argv=None):
         ap.error("--rows must be in 1 .. 2^19")
     if args.transposed and args.rows != 1:
         ap.error("--transposed takes one activation row")
+    if args.a_int8 and not args.transposed:
+        ap.error("--a-int8 needs --transposed (weights stored one output row per row)")
     return args
 
 

@@ -67,8 +67,10 @@ enum {
                              ring; needs N % 16 == 0, N >= 256, K >= 32 and 16-byte aligned A, W, S */
     Q8MV_KERNEL_ASYNC = 3, /* each thread streams its weight strip through its own shared-memory ring
                               with asynchronous 16-byte copies; needs N % 16 == 0 and 16-byte aligned W, S */
-    Q8MV_KERNEL_ROWS = 4   /* weights stored one output row per row (q8mv_plan_transposed): a CTA owns
+    Q8MV_KERNEL_ROWS = 4,  /* weights stored one output row per row (q8mv_plan_transposed): a CTA owns
                               rows_per_cta outputs, its warps split K, lanes read 16 bytes of a row */
+    Q8MV_KERNEL_ROWS_I8 = 5 /* as ROWS, with int8 activations: each 32-element block of A is quantized
+                               in the kernel (q8mv_quantize_rows) and multiplied with dp4a */
 };
 
 /*
@@ -144,12 +146,34 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device,
  * linear layer stores its weights).  q8mv_run and q8mv_run_fused then take Wt
  * and St in place of W and S.  Limits as for q8mv_plan.  Accepted overrides:
  * vec_bytes (16, 4 or 1: load per lane and step, used when K and Wt's address
- * allow it, narrower loads as the fallback), rows_per_cta (8 or 16), overlap;
- * any other non-zero field gives INVALID_ARG.  Each output's blocks are summed
- * in order within a fixed interleave, so a plan is bitwise repeatable.
+ * allow it, narrower loads as the fallback), rows_per_cta (8 or 16), overlap,
+ * and kernel = Q8MV_KERNEL_ROWS_I8 for int8 activations (below); any other
+ * non-zero field gives INVALID_ARG.  Each output's blocks are summed in order
+ * within a fixed interleave, so a plan is bitwise repeatable.
+ *
+ * Int8 activations (kernel = Q8MV_KERNEL_ROWS_I8; "dot and tensor cores" page,
+ * "Hardware paths": an i8 dot_t accumulates in i32, a single row takes dp4a):
+ * the kernel quantizes each 32-element block b of A as q8mv_quantize_rows does
+ * and computes
+ *     C[0, n] = sum_b (d_b * St[n, b]) * ( sum_{k in block b} q[k] * Wt[n, k] )
+ * with the block's dot product exact in i32 (four dp4a per 16 bytes) and one
+ * f32 fold per block.  This is an approximation of the f32 product: the codes
+ * carry about 7 bits of each activation.
  */
 q8mv_status_t q8mv_plan_transposed(q8mv_plan_t *out, int64_t K, int64_t N, int device,
                                    const q8mv_opts_t *opts);
+
+/*
+ * Int8 codes of M activation rows: for each 32-element block b of row m (the
+ * last block may be partial), in IEEE f32 arithmetic,
+ *     amax = max |A[m, k]|,  d[m, b] = amax / 127,
+ *     q[m, k] = rint(A[m, k] * (127 / amax))   (ties to even; 0 when amax = 0)
+ * so that A[m, k] ~ q[m, k] * d[m, b].  A f32 [M, K], q i8 [M, K], d f32
+ * [M, KB], all device memory, row-major; A and d 4-byte aligned, no overlaps.
+ * 0 <= M <= 65535.  Asynchronous on `stream`; the current device is used.
+ */
+q8mv_status_t q8mv_quantize_rows(int64_t M, int64_t K, const float *A, int8_t *q, float *d,
+                                 cudaStream_t stream);
 
 /*
  * Batched decode: a plan for C[M,N] = A[M,K] x (W[K,N], S[KB,N]), each row of

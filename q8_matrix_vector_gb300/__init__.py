@@ -30,6 +30,7 @@ KERNEL_REGS = 1
 KERNEL_TMA = 2
 KERNEL_ASYNC = 3
 KERNEL_ROWS = 4
+KERNEL_ROWS_I8 = 5
 
 ACT_NONE = 0
 ACT_RELU = 1
@@ -105,6 +106,8 @@ def _load() -> ctypes.CDLL:
     lib.q8mv_choose_config_batched.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(Opts),
                                                ctypes.POINTER(PlanInfo)]
     lib.q8mv_choose_config_batched.restype = ctypes.c_int
+    lib.q8mv_quantize_rows.argtypes = [i64, i64, p, p, p, p]
+    lib.q8mv_quantize_rows.restype = ctypes.c_int
     lib.q8mv_status_string.argtypes = [ctypes.c_int]
     lib.q8mv_status_string.restype = ctypes.c_char_p
     lib.q8mv_last_cuda_error.argtypes = []
@@ -327,6 +330,24 @@ def matvec_t(A, Wt, St, out=None, **epilogue):
     if plan is None:
         plan = _plans[key] = Plan(K, N, device=Wt.device.index, transposed=True)
     return plan(A, Wt, St, out=out, **epilogue)
+
+
+def quantize_rows(A):
+    """Int8 codes of the rows of A [M, K] f32 per 32-element block: (q int8 [M, K], d f32 [M, KB])."""
+    import torch
+
+    if A.dim() == 1:
+        A = A.reshape(1, -1)
+    _check(A, torch.float32, tuple(A.shape), "A")
+    M, K = A.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=A.device)
+    d = torch.empty((M, num_blocks(K)), dtype=torch.float32, device=A.device)
+    with torch.cuda.device(A.device):
+        st = _lib.q8mv_quantize_rows(M, K, A.data_ptr(), q.data_ptr(), d.data_ptr(),
+                                     torch.cuda.current_stream(A.device).cuda_stream)
+    if st != Q8MV_OK:
+        raise Q8mvError(st, "q8mv_quantize_rows")
+    return q, d
 
 
 def version() -> int:

@@ -585,11 +585,17 @@ namespace {
 
 using RowsFn = void (*)(tk::Params);
 
-RowsFn rows_kernel(int lv, int r) {
+template <bool I8A>
+RowsFn rows_kernel_for(int lv, int r) {
     if (r == 16)
-        return lv == 16 ? tk::q8mv_rows_kernel<16, 16> : lv == 4 ? tk::q8mv_rows_kernel<4, 16>
-                                                                : tk::q8mv_rows_kernel<1, 16>;
-    return lv == 16 ? tk::q8mv_rows_kernel<16, 8> : lv == 4 ? tk::q8mv_rows_kernel<4, 8> : tk::q8mv_rows_kernel<1, 8>;
+        return lv == 16 ? tk::q8mv_rows_kernel<16, 16, I8A>
+                        : lv == 4 ? tk::q8mv_rows_kernel<4, 16, I8A> : tk::q8mv_rows_kernel<1, 16, I8A>;
+    return lv == 16 ? tk::q8mv_rows_kernel<16, 8, I8A>
+                    : lv == 4 ? tk::q8mv_rows_kernel<4, 8, I8A> : tk::q8mv_rows_kernel<1, 8, I8A>;
+}
+
+RowsFn rows_kernel(int lv, int r, bool i8a = false) {
+    return i8a ? rows_kernel_for<true>(lv, r) : rows_kernel_for<false>(lv, r);
 }
 
 struct RowsConfig {
@@ -672,6 +678,7 @@ struct q8mv_plan_s {
     bk::Config bcfg[bk::kNumVec];
     // transposed plans (q8mv_plan_transposed): weights stored one output row per row
     bool rows = false;
+    bool rows_i8 = false;   // int8 activations, dp4a
     RowsConfig rcfg;
     int rows_cps = 0;
     // device memory owned by the plan
@@ -705,13 +712,14 @@ int q8mv_version(void) { return kVersion; }
 q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t ctas_per_sm,
                                  int32_t vec_bytes, const q8mv_opts_t *opts, q8mv_plan_info_t *info) {
     if (info == nullptr) return Q8MV_ERR_INVALID_ARG;
-    if (opts && opts->kernel == Q8MV_KERNEL_ROWS) {
+    if (opts && (opts->kernel == Q8MV_KERNEL_ROWS || opts->kernel == Q8MV_KERNEL_ROWS_I8)) {
         if (K < 0 || N < 0 || sm_count <= 0 || ctas_per_sm <= 0) return Q8MV_ERR_INVALID_ARG;
         if (vec_bytes != 16 && vec_bytes != 4 && vec_bytes != 1) return Q8MV_ERR_INVALID_ARG;
         if (opts->rows_per_cta != 0 && opts->rows_per_cta != 8 && opts->rows_per_cta != 16)
             return Q8MV_ERR_INVALID_ARG;
         const RowsConfig c = choose_rows(K, N, sm_count, ctas_per_sm, opts->rows_per_cta);
         fill_rows_info(c, K, vec_bytes, sm_count, ctas_per_sm, 0, info);
+        info->kernel = opts->kernel;
         return Q8MV_OK;
     }
     if (opts && opts->kernel != Q8MV_KERNEL_AUTO && opts->kernel != Q8MV_KERNEL_REGS &&
@@ -980,6 +988,7 @@ q8mv_status_t q8mv_plan_info(q8mv_plan_t p, q8mv_plan_info_t *info) {
     std::memset(info, 0, sizeof(*info));
     if (p->rows) {
         fill_rows_info(p->rcfg, p->K, rows_lv(0, p->K, p->max_vec), p->sm_count, p->rows_cps, p->ws_bytes, info);
+        if (p->rows_i8) info->kernel = Q8MV_KERNEL_ROWS_I8;
         info->overlap = p->overlap ? 1 : 0;
         return Q8MV_OK;
     }
@@ -1150,7 +1159,7 @@ static q8mv_status_t run_rows(q8mv_plan_t p, const float *A, const int8_t *W, co
         cfg.numAttrs = 1;
     }
     const int lv = rows_lv(reinterpret_cast<uintptr_t>(W), p->K, p->max_vec);
-    return cuda_status(cudaLaunchKernelEx(&cfg, rows_kernel(lv, c.r), prm));
+    return cuda_status(cudaLaunchKernelEx(&cfg, rows_kernel(lv, c.r, p->rows_i8), prm));
 }
 
 static q8mv_status_t run_impl(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
@@ -1399,7 +1408,9 @@ q8mv_status_t q8mv_plan_transposed(q8mv_plan_t *out, int64_t K, int64_t N, int d
     if (K < 0 || N < 0 || K >= (1LL << 31) || N >= (1LL << 31)) return Q8MV_ERR_INVALID_ARG;
     if (N > 0 && K > ((1LL << 62) / N)) return Q8MV_ERR_INVALID_ARG;
     if (opts) {
-        if (opts->kernel != Q8MV_KERNEL_AUTO && opts->kernel != Q8MV_KERNEL_ROWS) return Q8MV_ERR_INVALID_ARG;
+        if (opts->kernel != Q8MV_KERNEL_AUTO && opts->kernel != Q8MV_KERNEL_ROWS &&
+            opts->kernel != Q8MV_KERNEL_ROWS_I8)
+            return Q8MV_ERR_INVALID_ARG;
         if (opts->vec_bytes != 0 && opts->vec_bytes != 16 && opts->vec_bytes != 4 && opts->vec_bytes != 1)
             return Q8MV_ERR_INVALID_ARG;
         if (opts->rows_per_cta != 0 && opts->rows_per_cta != 8 && opts->rows_per_cta != 16)
@@ -1436,6 +1447,7 @@ q8mv_status_t q8mv_plan_transposed(q8mv_plan_t *out, int64_t K, int64_t N, int d
     p->KB = static_cast<int>(ceil_div(K, kBlk));
     p->device = device;
     p->rows = true;
+    p->rows_i8 = opts && opts->kernel == Q8MV_KERNEL_ROWS_I8;
     p->max_vec = (opts && opts->vec_bytes) ? opts->vec_bytes : 16;
     p->forced_vec = opts && opts->vec_bytes != 0;
     p->overlap = opts && opts->overlap == 1;
@@ -1451,7 +1463,7 @@ q8mv_status_t q8mv_plan_transposed(q8mv_plan_t *out, int64_t K, int64_t N, int d
     if (st != Q8MV_OK) return fail(st == Q8MV_ERR_CUDA ? Q8MV_ERR_UNSUPPORTED_DEVICE : st);
     p->rcfg = choose_rows(K, N, p->sm_count, cps16, opts ? opts->rows_per_cta : 0);
     int cps = 1;
-    st = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cps, rows_kernel(16, p->rcfg.r),
+    st = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cps, rows_kernel(16, p->rcfg.r, p->rows_i8),
                                                                    32 * p->rcfg.wk, 0));
     if (st != Q8MV_OK) return fail(st);
     p->rows_cps = cps;
@@ -1463,6 +1475,20 @@ q8mv_status_t q8mv_plan_transposed(q8mv_plan_t *out, int64_t K, int64_t N, int d
     if (device != prev) cudaSetDevice(prev);
     *out = p;
     return Q8MV_OK;
+}
+
+q8mv_status_t q8mv_quantize_rows(int64_t M, int64_t K, const float *A, int8_t *q, float *d, cudaStream_t stream) {
+    if (M < 0 || K < 0 || M > 65535 || K >= (1LL << 31)) return Q8MV_ERR_INVALID_ARG;
+    if (M == 0 || K == 0) return Q8MV_OK;
+    if (A == nullptr || q == nullptr || d == nullptr) return Q8MV_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) & 3u) || (reinterpret_cast<uintptr_t>(d) & 3u)) return Q8MV_ERR_INVALID_ARG;
+    const int64_t KB = ceil_div(K, kBlk);
+    if (overlaps(q, M * K, A, 4 * M * K) || overlaps(d, 4 * M * KB, A, 4 * M * K) || overlaps(q, M * K, d, 4 * M * KB))
+        return Q8MV_ERR_INVALID_ARG;
+    const int64_t grid_x = ceil_div(K, 8LL * tk::kStepK);
+    tk::q8mv_quantize_kernel<<<dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(M)), 256, 0, stream>>>(
+        A, q, d, K, static_cast<int>(KB));
+    return cuda_status(cudaGetLastError());
 }
 
 q8mv_status_t q8mv_choose_config_batched(int64_t M, int64_t K, int64_t N, int32_t sm_count, int32_t ctas_per_sm,

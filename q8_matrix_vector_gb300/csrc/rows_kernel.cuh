@@ -17,6 +17,15 @@
 // their halves with one shuffle, and the even lane applies the block's scale
 // once.  After its steps each warp sums its lanes per row (fixed butterfly), and
 // the CTA adds the warps in order in shared memory before writing C.
+//
+// With int8 activations (I8A) the lane first turns its 16 activations into
+// codes of their 32-element block (the block's two lanes agree on its largest
+// magnitude through one shuffle): d = amax / 127, q = rint(a * (127 / amax)),
+// each an IEEE f32 operation; the row's 16 products are then four dp4a into an
+// exact i32 sum, the block's halves are joined by one integer shuffle-add, and
+// the even lane folds the block once with d * St[n, b] ("dot and tensor cores"
+// page, "Hardware paths": an i8 dot_t accumulates in i32; a single row takes
+// dp4a).
 #pragma once
 
 #include <cstdint>
@@ -138,7 +147,29 @@ constexpr int rows_min_blocks() {
     return R <= 8 ? 3 : 1;
 }
 
-template <int LV, int R>
+// The int8 codes of a lane's 16 activations (half a block) and the block's d.
+// Both lanes of the block (lane ^ 1) must call this together.  rint is taken
+// by adding 1.5 * 2^23, whose f32 sum rounds the product to the nearest
+// integer, ties to even; the code is the low byte of that sum's bits.
+__device__ __forceinline__ void quantize_half_block(const float2 (&a2)[8], uint32_t (&qa)[4], float &d) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(a2[i].x), fabsf(a2[i].y)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    d = __fdiv_rn(amax, 127.0f);
+    const float id = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t c0 = __float_as_uint(__fadd_rn(__fmul_rn(a2[2 * q].x, id), kRound));
+        const uint32_t c1 = __float_as_uint(__fadd_rn(__fmul_rn(a2[2 * q].y, id), kRound));
+        const uint32_t c2 = __float_as_uint(__fadd_rn(__fmul_rn(a2[2 * q + 1].x, id), kRound));
+        const uint32_t c3 = __float_as_uint(__fadd_rn(__fmul_rn(a2[2 * q + 1].y, id), kRound));
+        qa[q] = __byte_perm(__byte_perm(c0, c1, 0x0040u), __byte_perm(c2, c3, 0x0040u), 0x5410u);
+    }
+}
+
+template <int LV, int R, bool I8A>
 __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_rows_kernel(const Params p) {
     __shared__ float part[kMaxWarps][R];
     const int lane = threadIdx.x & 31;
@@ -167,21 +198,38 @@ __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_row
     for (int r = 0; r < R; ++r) acc[r] = 0.0f;
 
     for (; k0 < p.K; k0 += step) {
-        // per row: 16 products per lane in two packed lanes (k in order within
-        // each), the block's other half by one shuffle, then one scale per
-        // block (the even lane's s; 0 on the odd lane)
+        if constexpr (I8A) {
+            // per row: four dp4a into the exact i32 sum of the lane's 16
+            // products, the block's other half by one shuffle, one fold with
+            // d * St[n, b] (0 on the odd lane)
+            uint32_t qa[4];
+            float d;
+            quantize_half_block(a2, qa, d);
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float2 s2 = make_float2(0.0f, 0.0f);
+            for (int r = 0; r < R; ++r) {
+                int isum = 0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint32_t u = w[r][q] ^ 0x80808080u;
-                s2 = __ffma2_rn(a2[2 * q], cvt2(u, 0x7440u, 0x7441u), s2);
-                s2 = __ffma2_rn(a2[2 * q + 1], cvt2(u, 0x7442u, 0x7443u), s2);
+                for (int q = 0; q < 4; ++q) isum = __dp4a(static_cast<int>(qa[q]), static_cast<int>(w[r][q]), isum);
+                isum += __shfl_xor_sync(0xffffffffu, isum, 1);
+                acc[r] = fmaf(static_cast<float>(isum), __fmul_rn(d, s[r]), acc[r]);
             }
-            float blk = s2.x + s2.y;
-            blk += __shfl_xor_sync(0xffffffffu, blk, 1);
-            acc[r] = fmaf(blk, s[r], acc[r]);
+        } else {
+            // per row: 16 products per lane in two packed lanes (k in order
+            // within each), the block's other half by one shuffle, then one
+            // scale per block (the even lane's s; 0 on the odd lane)
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float2 s2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t u = w[r][q] ^ 0x80808080u;
+                    s2 = __ffma2_rn(a2[2 * q], cvt2(u, 0x7440u, 0x7441u), s2);
+                    s2 = __ffma2_rn(a2[2 * q + 1], cvt2(u, 0x7442u, 0x7443u), s2);
+                }
+                float blk = s2.x + s2.y;
+                blk += __shfl_xor_sync(0xffffffffu, blk, 1);
+                acc[r] = fmaf(blk, s[r], acc[r]);
+            }
         }
         // the next step's loads, once this step's registers are free
         const int64_t kn = k0 + step + lane * kLaneK;
@@ -207,6 +255,30 @@ __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_row
         const int64_t n = n0 + t;
         p.C[n] = q8epi::apply(p.epi, v, p.C, n, n);
     }
+}
+
+// Int8 codes of M activation rows, per 32-element block: q [M, K] and d [M, KB]
+// (the quantization of the int8-activation rows kernel, on its own).  Grid
+// (ceil(K / 512), M), 256 threads: a warp takes one 512-wide step of a row.
+__global__ void __launch_bounds__(256) q8mv_quantize_kernel(const float *A, int8_t *q, float *d, int64_t K, int KB) {
+    const int lane = threadIdx.x & 31;
+    const int64_t k = (static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kStepK + lane * kLaneK;
+    const int64_t m = blockIdx.y;
+    if (k - lane * kLaneK >= K) return;  // the whole warp is past K
+    Params p{};
+    p.A = A + m * K;
+    p.K = K;
+    float2 a2[8];
+    load_a(p, k, a2);
+    uint32_t qa[4];
+    float dd;
+    quantize_half_block(a2, qa, dd);
+    if (k >= K) return;
+    int8_t *qrow = q + m * K;
+#pragma unroll
+    for (int i = 0; i < kLaneK; ++i)
+        if (k + i < K) qrow[k + i] = static_cast<int8_t>((qa[i / 4] >> (8 * (i % 4))) & 0xFFu);
+    if ((lane & 1) == 0) d[m * KB + k / kBlk] = dd;
 }
 
 }  // namespace tk

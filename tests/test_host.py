@@ -353,3 +353,18 @@ def test_transposed_plan_rejects_bad_arguments_before_touching_a_device(q8):
     bad = q8.Opts(0, 0, 0, 0, 0, 0, 0, 8)
     assert lib.q8mv_plan(ctypes.byref(h), 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
     assert lib.q8mv_plan_batched(ctypes.byref(h), 4, 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+
+
+def test_int8_activation_planner_and_quantize_arguments(q8):
+    c = q8.choose_config(4096, 4096, 152, 3, 16, kernel=q8.KERNEL_ROWS_I8)
+    assert c["kernel"] == q8.KERNEL_ROWS_I8 and c["tile_n"] == 8 and c["groups_k"] == 8
+    lib = q8.library()
+    assert lib.q8mv_quantize_rows(-1, 64, None, None, None, None) == q8.Q8MV_ERR_INVALID_ARG
+    assert lib.q8mv_quantize_rows(2, -1, None, None, None, None) == q8.Q8MV_ERR_INVALID_ARG
+    assert lib.q8mv_quantize_rows(1 << 16, 64, None, None, None, None) == q8.Q8MV_ERR_INVALID_ARG
+    assert lib.q8mv_quantize_rows(2, 64, None, None, None, None) == q8.Q8MV_ERR_INVALID_ARG  # null pointers
+    assert lib.q8mv_quantize_rows(0, 64, None, None, None, None) == q8.Q8MV_OK  # nothing to do
+    assert lib.q8mv_quantize_rows(3, 0, None, None, None, None) == q8.Q8MV_OK
+    h = ctypes.c_void_p()
+    bad = q8.Opts(q8.KERNEL_ROWS_I8, 0, 0, 0, 0, 0, 0, 0)  # the int8 kernel belongs to transposed plans
+    assert lib.q8mv_plan(ctypes.byref(h), 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
