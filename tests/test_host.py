@@ -227,7 +227,8 @@ BATCH_ROWS = [2, 3, 4, 5, 8, 9, 16, 17, 40]
 
 def batched_vecs(M, N):
     mb = 2 if M <= 2 else 4 if M <= 4 else 8 if M <= 8 else 16
-    return mb, [v for v in ((8,) if mb <= 4 else ()) + (4, 1) if N == 0 or N % v == 0]
+    widths = ((8,) if mb <= 4 else ()) + (4, 1)
+    return mb, [v for v in widths if N == 0 or N % v == 0]
 
 
 @pytest.mark.parametrize("K,N", BATCH_SHAPES)
@@ -275,6 +276,8 @@ def test_batched_planner_rejects_illegal_requests(q8):
         q8.choose_config_batched(8, 64, 256, 152, 2, 8)  # 8-byte loads only up to 4 rows per pass
     with pytest.raises(q8.Q8mvError):
         q8.choose_config_batched(2, 64, 200, 152, 2, 16)  # no 16-byte batched kernel
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config_batched(16, 64, 256, 152, 2, 2)  # no 2-byte batched kernel
     with pytest.raises(q8.Q8mvError):
         q8.choose_config_batched(2, 64, 202, 152, 2, 4)  # 4 does not divide 202
     with pytest.raises(q8.Q8mvError):
