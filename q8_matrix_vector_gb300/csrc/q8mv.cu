@@ -1132,8 +1132,7 @@ static q8mv_status_t run_batched(q8mv_plan_t p, const float *A, const int8_t *W,
         bk::launch(p->bcfg[idx], A, W, S, C, p->ws, p->tickets, p->M, p->K, p->N, epi, stream, p->overlap));
 }
 
-// The run path of q8mv_run and q8mv_run_fused.  With an epilogue the register
-// (or batched) kernel always runs, also for K == 0 (the product is then 0).
+// Launch the rows kernel of a transposed plan (weights one output row per row).
 static q8mv_status_t run_rows(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
                               const q8epi::Epilogue &epi, cudaStream_t stream) {
     const RowsConfig &c = p->rcfg;
@@ -1162,6 +1161,8 @@ static q8mv_status_t run_rows(q8mv_plan_t p, const float *A, const int8_t *W, co
     return cuda_status(cudaLaunchKernelEx(&cfg, rows_kernel(lv, c.r, p->rows_i8), prm));
 }
 
+// The run path of q8mv_run and q8mv_run_fused.  With an epilogue the register
+// (or batched) kernel always runs, also for K == 0 (the product is then 0).
 static q8mv_status_t run_impl(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
                               const q8epi::Epilogue &epi, cudaStream_t stream) {
     if (p == nullptr) return Q8MV_ERR_INVALID_ARG;
