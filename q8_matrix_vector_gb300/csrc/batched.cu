@@ -8,6 +8,7 @@
 // outputs while the arithmetic grows with M.
 #include "batched.cuh"
 #include "batched.h"
+#include "mma_kernel.cuh"
 
 #include <cuda_runtime.h>
 
@@ -294,6 +295,137 @@ cudaError_t prepare(const Config &c) {
     if (e != cudaSuccess) return e;
     if (static_cast<size_t>(fa.maxDynamicSharedSizeBytes) >= c.smem) return cudaSuccess;
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(c.smem));
+}
+
+// ---------------------------------------------------------------------------
+// tensor-core kernel
+// ---------------------------------------------------------------------------
+using MmaFn = void (*)(mk::Params);
+
+MmaFn mma_kernel(bool cluster) { return cluster ? mk::q8mv_mma_kernel<true> : mk::q8mv_mma_kernel<false>; }
+
+cudaError_t query_mma(int *cps, int (&clusters)[9]) {
+    cudaError_t e = cudaFuncSetAttribute(mk::q8mv_mma_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         64 * 1024);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mk::q8mv_mma_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    if (e != cudaSuccess) return e;
+    *cps = 1;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(cps, mk::q8mv_mma_kernel<false>, mk::kThreads, 50 * 1024);
+    if (e != cudaSuccess) return e;
+    for (int s = 0; s < 9; ++s) clusters[s] = 0;
+    for (int s = 2; s <= 8; ++s) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, s);
+        cfg.blockDim = dim3(mk::kThreads);
+        cfg.dynamicSmemBytes = 50 * 1024;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 1;
+        attr.val.clusterDim.y = s;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mk::q8mv_mma_kernel<true>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        clusters[s] = n;
+    }
+    return cudaSuccess;
+}
+
+// Column tiles of 128, passes of 16 rows; the split fills one wave: as many
+// K ranges per tile as the resident slots allow, summed through a cluster
+// when at most 8 and every cluster is resident at once, else through the
+// workspace.  Activations are staged 16 blocks at a time (a multiple of the
+// weight ring's depth).
+q8mv_status_t choose_mma(int64_t M, int64_t K, int64_t N, const Device &dev, int cps, const int *resident_clusters,
+                         const q8mv_opts_t *o, MmaConfig *out) {
+    MmaConfig c;
+    if (M < 1 || K < 0 || N < 0 || dev.sm_count <= 0) return Q8MV_ERR_INVALID_ARG;
+    if (N % 4 != 0) {
+        *out = c;
+        return Q8MV_OK;
+    }
+    const int64_t KB = ceil_div(K, kBlk);
+    c.tiles = std::max<int64_t>(1, ceil_div(N, mk::kTileN));
+    c.groups = ceil_div(M, mk::kRows);
+    c.cps = std::max(1, cps);
+    const int64_t slots = static_cast<int64_t>(dev.sm_count) * c.cps;
+    int64_t split = std::max<int64_t>(1, slots / (c.tiles * c.groups));
+    split = std::min<int64_t>(split, std::max<int64_t>(1, KB));
+    const int want = o ? o->split_k : 0;
+    if (want > 0) split = std::min<int64_t>(want, std::max<int64_t>(1, KB));
+    c.bps = static_cast<int>(std::max<int64_t>(1, ceil_div(KB, split)));
+    c.split = static_cast<int>(std::max<int64_t>(1, ceil_div(KB, c.bps)));
+    c.cluster = c.split > 1 && c.split <= 8 && resident_clusters != nullptr &&
+                c.tiles * c.groups <= resident_clusters[c.split];
+    if (c.split > 1 && !c.cluster && want == 0 && c.split > 8) {
+        // prefer the cluster form: fewer, longer K ranges
+        int s8 = 8;
+        while (s8 > 1 && !(resident_clusters && c.tiles * c.groups <= resident_clusters[s8])) --s8;
+        if (s8 > 1) {
+            c.bps = static_cast<int>(ceil_div(KB, s8));
+            c.split = static_cast<int>(ceil_div(KB, c.bps));
+            c.cluster = c.split <= 8 && c.tiles * c.groups <= resident_clusters[c.split];
+        }
+    }
+    c.cb = static_cast<int>(std::min<int64_t>(16, ceil_div(c.bps, mk::kDepth) * mk::kDepth));
+    c.smem = std::max<size_t>(3 * mk::kRows * (c.cb * kBlk + mk::kPad) * 2, mk::kRows * mk::kTileN * 4);
+    c.ws_floats = (c.split > 1 && !c.cluster) ? c.groups * c.split * mk::kRows * N : 0;
+    c.n_tickets = (c.split > 1 && !c.cluster) ? c.groups * c.tiles : 0;
+    c.usable = true;
+    *out = c;
+    return Q8MV_OK;
+}
+
+cudaError_t prepare_mma(const MmaConfig &c) {
+    (void)c;
+    return cudaSuccess;  // query_mma raised the kernels' shared-memory limit to 64 KiB
+}
+
+cudaError_t launch_mma(const MmaConfig &c, const float *A, const int8_t *W, const float *S, float *C, float *ws,
+                       unsigned *tickets, int64_t M, int64_t K, int64_t N, const q8epi::Epilogue &epi,
+                       cudaStream_t stream, bool overlap) {
+    mk::Params prm;
+    prm.A = A;
+    prm.W = W;
+    prm.S = S;
+    prm.C = C;
+    prm.ws = ws;
+    prm.tickets = tickets;
+    prm.K = K;
+    prm.N = N;
+    prm.M = static_cast<int>(M);
+    prm.KB = static_cast<int>(ceil_div(K, kBlk));
+    prm.split = c.split;
+    prm.bps = c.bps;
+    prm.cb = c.cb;
+    prm.epi = epi;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(c.tiles), static_cast<unsigned>(c.split), static_cast<unsigned>(c.groups));
+    cfg.blockDim = dim3(mk::kThreads);
+    cfg.dynamicSmemBytes = c.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n_attr = 0;
+    if (overlap) {
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attr;
+    }
+    if (c.cluster) {
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = 1;
+        attr[n_attr].val.clusterDim.y = static_cast<unsigned>(c.split);
+        attr[n_attr].val.clusterDim.z = 1;
+        ++n_attr;
+    }
+    cfg.attrs = n_attr ? attr : nullptr;
+    cfg.numAttrs = n_attr;
+    return cudaLaunchKernelEx(&cfg, mma_kernel(c.cluster), prm);
 }
 
 cudaError_t launch(const Config &c, const float *A, const int8_t *W, const float *S, float *C, float *ws,

@@ -55,6 +55,31 @@ struct Device {
     int max_clusters[kNumVec][9] = {};
 };
 
+// The tensor-core kernel (up to 16 rows per pass on mma.sync): its planner's
+// choice, or vec == 0 when the shape cannot use it (N % 4 != 0).
+struct MmaConfig {
+    int split = 0, bps = 0, cb = 0;
+    bool cluster = false;
+    int64_t tiles = 0, groups = 0;
+    size_t smem = 0;
+    int cps = 0;
+    int64_t ws_floats = 0, n_tickets = 0;
+    bool usable = false;
+};
+
+q8mv_status_t choose_mma(int64_t M, int64_t K, int64_t N, const Device &dev, int cps, const int *resident_clusters,
+                         const q8mv_opts_t *o, MmaConfig *out);
+
+// Resident CTAs per SM of the tensor-core kernel and resident clusters of it
+// per cluster size 2 .. 8 (index = size).  Current device.
+cudaError_t query_mma(int *cps, int (&clusters)[9]);
+
+cudaError_t prepare_mma(const MmaConfig &c);
+
+cudaError_t launch_mma(const MmaConfig &c, const float *A, const int8_t *W, const float *S, float *C, float *ws,
+                       unsigned *tickets, int64_t M, int64_t K, int64_t N, const q8epi::Epilogue &epi,
+                       cudaStream_t stream, bool overlap);
+
 // Pick tile, split and staging for M x K x N with `vec`-byte weight loads.
 // Pure host code.  INVALID_ARG when the override cannot apply.
 q8mv_status_t choose(int64_t M, int64_t K, int64_t N, const Device &dev, int vec, const q8mv_opts_t *o,

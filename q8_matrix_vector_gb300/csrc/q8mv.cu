@@ -42,6 +42,7 @@
 
 #include "async_stream.cuh"
 #include "batched.h"
+#include "mma_kernel.cuh"
 #include "regs_kernel.cuh"
 #include "rows_kernel.cuh"
 #include "tma_stream.cuh"
@@ -676,6 +677,8 @@ struct q8mv_plan_s {
     int64_t M = 1;
     int mb = 0;
     bk::Config bcfg[bk::kNumVec];
+    bk::MmaConfig mcfg;      // tensor-core batched kernel (usable == false if the shape cannot use it)
+    bool mma = false;        // batched calls with a 4-byte aligned W run the tensor-core kernel
     // transposed plans (q8mv_plan_transposed): weights stored one output row per row
     bool rows = false;
     bool rows_i8 = false;   // int8 activations, dp4a
@@ -961,6 +964,27 @@ static int batched_index(q8mv_plan_t p, uintptr_t waddr) {
     return idx;
 }
 
+static void fill_mma_info(const bk::MmaConfig &c, int sm_count, int64_t M, int64_t ws_bytes, q8mv_plan_info_t *info) {
+    std::memset(info, 0, sizeof(*info));
+    info->kernel = Q8MV_KERNEL_MMA;
+    info->vec_bytes = 4;
+    info->threads_n = 32;
+    info->groups_k = 1;
+    info->threads_per_cta = mk::kThreads;
+    info->split_k = c.split;
+    info->blocks_per_split = c.bps;
+    info->cluster = c.cluster ? 1 : 0;
+    info->tile_n = mk::kTileN;
+    info->grid_x = c.tiles;
+    info->grid_y = c.split;
+    info->workspace_bytes = ws_bytes;
+    info->sm_count = sm_count;
+    info->ctas_per_sm = c.cps;
+    info->rows = static_cast<int32_t>(M);
+    info->rows_per_pass = mk::kRows;
+    info->grid_z = c.groups;
+}
+
 static void fill_batched_info(const bk::Config &c, int sm_count, int64_t M, int64_t ws_bytes,
                               q8mv_plan_info_t *info) {
     std::memset(info, 0, sizeof(*info));
@@ -989,6 +1013,11 @@ q8mv_status_t q8mv_plan_info(q8mv_plan_t p, q8mv_plan_info_t *info) {
     if (p->rows) {
         fill_rows_info(p->rcfg, p->K, rows_lv(0, p->K, p->max_vec), p->sm_count, p->rows_cps, p->ws_bytes, info);
         if (p->rows_i8) info->kernel = Q8MV_KERNEL_ROWS_I8;
+        info->overlap = p->overlap ? 1 : 0;
+        return Q8MV_OK;
+    }
+    if (p->mb > 0 && p->mma && p->mcfg.usable) {
+        fill_mma_info(p->mcfg, p->sm_count, p->M, p->ws_bytes, info);
         info->overlap = p->overlap ? 1 : 0;
         return Q8MV_OK;
     }
@@ -1126,6 +1155,9 @@ static q8mv_status_t run_async(q8mv_plan_t p, const float *A, const int8_t *W, c
 
 static q8mv_status_t run_batched(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
                                  const q8epi::Epilogue &epi, cudaStream_t stream) {
+    if (p->mma && p->mcfg.usable && reinterpret_cast<uintptr_t>(W) % 4 == 0)
+        return cuda_status(bk::launch_mma(p->mcfg, A, W, S, C, p->ws, p->tickets, p->M, p->K, p->N, epi, stream,
+                                          p->overlap));
     const int idx = batched_index(p, reinterpret_cast<uintptr_t>(W));
     if (idx < 0) return Q8MV_ERR_INVALID_ARG;
     return cuda_status(
@@ -1294,7 +1326,7 @@ q8mv_status_t q8mv_destroy(q8mv_plan_t p) {
 // 4 rows per pass), threads_n, split_k, overlap.
 static bool batched_opts_ok(int mb, const q8mv_opts_t *o) {
     if (o == nullptr) return true;
-    if (o->kernel != Q8MV_KERNEL_AUTO && o->kernel != Q8MV_KERNEL_REGS) return false;
+    if (o->kernel != Q8MV_KERNEL_AUTO && o->kernel != Q8MV_KERNEL_REGS && o->kernel != Q8MV_KERNEL_MMA) return false;
     if (o->stages != 0 || (o->cta_threads != 0 && o->cta_threads != bk::kThreads)) return false;
     if (o->rows_per_cta != 0) return false;
     if (o->overlap != 0 && o->overlap != 1) return false;
@@ -1368,12 +1400,19 @@ q8mv_status_t q8mv_plan_batched(q8mv_plan_t *out, int64_t M, int64_t K, int64_t 
     st = cuda_status(bk::query_device(mb, &dev));
     if (st != Q8MV_OK) return fail(st == Q8MV_ERR_CUDA ? Q8MV_ERR_UNSUPPORTED_DEVICE : st);
 
+    // the register kernel is planned in every case: it is also the fallback of
+    // the tensor-core kernel for weights that are not 4-byte aligned
+    q8mv_opts_t regs_opts = {};
+    if (opts) {
+        regs_opts = *opts;
+        regs_opts.kernel = Q8MV_KERNEL_AUTO;
+    }
     int64_t ws_floats = 0, n_tickets = 0;
     for (int i = 0; i < bk::kNumVec; ++i) {
         const int v = bk::kVecs[i];
         if (v > p->max_vec || !bk::vec_built(mb, v) || (N > 0 && N % v != 0)) continue;
         bk::Config c;
-        if (bk::choose(M, K, N, dev, v, opts, &c) != Q8MV_OK) return fail(Q8MV_ERR_INVALID_ARG);
+        if (bk::choose(M, K, N, dev, v, opts ? &regs_opts : nullptr, &c) != Q8MV_OK) return fail(Q8MV_ERR_INVALID_ARG);
         st = cuda_status(bk::prepare(c));
         if (st != Q8MV_OK) return fail(st);
         p->bcfg[i] = c;
@@ -1381,6 +1420,21 @@ q8mv_status_t q8mv_plan_batched(q8mv_plan_t *out, int64_t M, int64_t K, int64_t 
         n_tickets = std::max(n_tickets, c.n_tickets);
     }
     if (p->bcfg[bk::kNumVec - 1].vec == 0 && N > 0) return fail(Q8MV_ERR_INVALID_ARG);  // needs the fallback
+
+    // tensor-core kernel: on request, and by default for 16 rows per pass on
+    // large weights (K * N >= 2^27), where it measured faster than the
+    // register kernel (70B FFN up, 16 rows: 204 us vs 308 us; LM head 445 vs 532)
+    p->mma = (opts && opts->kernel == Q8MV_KERNEL_MMA) ||
+             ((!opts || opts->kernel == Q8MV_KERNEL_AUTO) && mb == 16 && K * N >= (1LL << 27));
+    if (p->mma && N > 0 && N % 4 == 0) {
+        int mcps = 1;
+        int clusters[9];
+        st = cuda_status(bk::query_mma(&mcps, clusters));
+        if (st != Q8MV_OK) return fail(st);
+        if (bk::choose_mma(M, K, N, dev, mcps, clusters, opts, &p->mcfg) != Q8MV_OK) return fail(Q8MV_ERR_INVALID_ARG);
+        ws_floats = std::max(ws_floats, p->mcfg.ws_floats);
+        n_tickets = std::max(n_tickets, p->mcfg.n_tickets);
+    }
 
     if (ws_floats > 0) {
         st = cuda_status(cudaMalloc(&p->ws, static_cast<size_t>(ws_floats) * sizeof(float)));
@@ -1501,6 +1555,19 @@ q8mv_status_t q8mv_choose_config_batched(int64_t M, int64_t K, int64_t N, int32_
     bk::Device dev;
     dev.sm_count = sm_count;
     for (int i = 0; i < bk::kNumVec; ++i) dev.cps_regs[i] = ctas_per_sm;
+    if (opts && opts->kernel == Q8MV_KERNEL_MMA) {
+        // resident clusters estimated for GPCs of 19 SMs
+        int clusters[9] = {};
+        const int gpcs = std::max(1, sm_count / 19);
+        for (int s = 2; s <= 8; ++s) clusters[s] = gpcs * ((sm_count / gpcs) * ctas_per_sm / s);
+        bk::MmaConfig mc;
+        const q8mv_status_t st = bk::choose_mma(M, K, N, dev, ctas_per_sm, clusters, opts, &mc);
+        if (st != Q8MV_OK) return st;
+        if (!mc.usable) return Q8MV_ERR_INVALID_ARG;
+        fill_mma_info(mc, sm_count, M, mc.ws_floats * static_cast<int64_t>(sizeof(float)), info);
+        info->overlap = opts->overlap == 1 ? 1 : 0;
+        return Q8MV_OK;
+    }
     bk::Config c;
     const q8mv_status_t st = bk::choose(M, K, N, dev, vec_bytes, opts, &c);
     if (st != Q8MV_OK) return st;

@@ -225,3 +225,103 @@ def test_batched_overlapped_launches_respect_the_chain(q8):
         over = chain(overlapped_plan)
         for i in range(calls):
             assert torch.equal(plain[i], over[i]), i
+
+
+# ----------------------------------------------------------------------------
+# the tensor-core kernel (kernel = MMA): 16 rows per pass on mma.sync
+# ----------------------------------------------------------------------------
+MMA_CASES = [(name, M) for name in ("tiny", "attn", "ffn_down") for M in (2, 5, 16)]
+MMA_CASES += [("ffn_up", 8), ("up70b", 16), ("lm_head", 4), ("attn", 17), ("attn", 40)]
+
+
+@pytest.mark.parametrize("name,M", MMA_CASES)
+def test_mma_workload_parity_full_size(q8, orc, name, M):
+    _, W, S = workloads.make_inputs(name)
+    A = workloads.make_rows(name, M)
+    K, N = W.shape
+    plan = q8.Plan(K, N, rows=M, kernel=q8.KERNEL_MMA)
+    assert plan.info["kernel"] == q8.KERNEL_MMA and plan.info["rows_per_pass"] == 16
+    got, guards = run_batched(plan, A, W, S)
+    ref, bound = orc.batched(A, W, S)
+    assert guards
+    check_rows(got, ref, bound, f"mma {name} M={M}")
+
+
+@pytest.mark.parametrize("name,M", [("attn", 3), ("ffn_down", 16), ("lm_head", 9), ("tiny", 16)])
+def test_mma_integer_inputs_bit_exact(q8, orc, name, M):
+    """A in {-1, 0, 1}: the bf16 split is exact (hi = A), every product and sum is
+    an integer below 2^24 times a power of two, so the tensor cores are exact."""
+    w = workloads.WORKLOADS[name]
+    _, W, S = workloads.make_integer_exact(w.K, w.N, seed=5000 + w.seed)
+    A = workloads.make_integer_rows(w.K, M, seed=6000 + w.seed)
+    plan = q8.Plan(w.K, w.N, rows=M, kernel=q8.KERNEL_MMA)
+    got, _ = run_batched(plan, A, W, S)
+    ref, _ = orc.batched(A, W, S)
+    assert np.array_equal(got, ref), np.argwhere(got != ref)[:10]
+
+
+@pytest.mark.parametrize("K", [1, 31, 33, 100, 4100])
+@pytest.mark.parametrize("N", [4, 36, 200, 1028])
+@pytest.mark.parametrize("M", [2, 16])
+def test_mma_tail_sweep(q8, orc, K, N, M):
+    _, W, S = workloads.make_random(K, N, seed=K * 31 + N)
+    A = np.random.Generator(np.random.PCG64(K + 3 * N + M)).standard_normal((M, K)).astype(np.float32)
+    plan = q8.Plan(K, N, rows=M, kernel=q8.KERNEL_MMA)
+    got, guards = run_batched(plan, A, W, S)
+    ref, bound = orc.batched(A, W, S)
+    assert guards
+    check_rows(got, ref, bound, f"mma K={K} N={N} M={M}")
+
+
+@pytest.mark.parametrize("split_k", [1, 3, 12])
+def test_mma_every_split_form(q8, orc, split_k):
+    """Direct writes (1), cluster sums (3) and the workspace ticket (12)."""
+    K, N, M = 4100, 1024, 7
+    _, W, S = workloads.make_random(K, N, seed=97)
+    A = np.random.Generator(np.random.PCG64(98)).standard_normal((M, K)).astype(np.float32)
+    plan = q8.Plan(K, N, rows=M, kernel=q8.KERNEL_MMA, split_k=split_k)
+    info = plan.info
+    assert (info["split_k"] == 1) == (split_k == 1)
+    assert info["cluster"] == (1 if split_k == 3 else 0)
+    got, _ = run_batched(plan, A, W, S)
+    ref, bound = orc.batched(A, W, S)
+    check_rows(got, ref, bound, f"mma split={split_k}")
+
+
+def test_mma_falls_back_for_unaligned_weights_and_odd_n(q8, orc):
+    K, N, M = 1000, 300, 4
+    _, W, S = workloads.make_random(K, N, seed=99)
+    A = np.random.Generator(np.random.PCG64(100)).standard_normal((M, K)).astype(np.float32)
+    plan = q8.Plan(K, N, rows=M, kernel=q8.KERNEL_MMA)
+    for off in (1, 2):  # the register kernel runs
+        got, _ = run_batched(plan, A, W, S, w_offset=off)
+        ref, bound = orc.batched(A, W, S)
+        check_rows(got, ref, bound, f"w+{off}")
+    _, W3, S3 = workloads.make_random(K, 301, seed=101)
+    plan = q8.Plan(K, 301, rows=M, kernel=q8.KERNEL_MMA)  # N % 4 != 0
+    got, _ = run_batched(plan, A, W3, S3)
+    ref, bound = orc.batched(A, W3, S3)
+    check_rows(got, ref, bound, "N=301")
+
+
+def test_mma_fused_epilogue_and_repeatability(q8, orc):
+    import oracle
+    import torch
+
+    _, W, S = workloads.make_inputs("ffn_up")
+    M = 6
+    A = workloads.make_rows("ffn_up", M)
+    K, N = W.shape
+    rng = np.random.Generator(np.random.PCG64(102))
+    bias = (20 * rng.standard_normal(N)).astype(np.float32)
+    plan = q8.Plan(K, N, rows=M, kernel=q8.KERNEL_MMA)
+    dev = torch.device("cuda")
+    Ad, Wd, Sd, bd = (torch.from_numpy(x).to(dev) for x in (A, W, S, bias))
+    C1 = plan(Ad, Wd, Sd, bias=bd, act="gelu_tanh")
+    C2 = plan(Ad, Wd, Sd, bias=bd, act="gelu_tanh")
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+    x, bound = orc.batched(A, W, S)
+    ref, mag = orc.epilogue(x, bias=bias, act=3)
+    got = C1.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= oracle.epilogue_tolerance(bound, mag))
