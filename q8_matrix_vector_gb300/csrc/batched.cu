@@ -336,11 +336,14 @@ cudaError_t query_mma(int *cps, int (&clusters)[9]) {
     return cudaSuccess;
 }
 
-// Column tiles of 128, passes of 16 rows; the split fills one wave: as many
-// K ranges per tile as the resident slots allow, summed through a cluster
-// when at most 8 and every cluster is resident at once, else through the
-// workspace.  Activations are staged 16 blocks at a time (a multiple of the
-// weight ring's depth).
+// Column tiles of 128, passes of 16 rows.  A warp's time grows with the blocks
+// its CTA takes in turn (measured about linear: attention at 16 rows runs
+// 134, 102, 55, 30 us at 128, 64, 32, 16 blocks per CTA), so the split gives
+// each CTA about 32 blocks (70B FFN up, 16 rows: 198 us at split 8 against
+// 231 us at split 2); the K ranges are summed through a cluster when at most
+// 8 and every cluster is resident at once, else through the workspace.
+// Activations are staged 16 blocks at a time (a multiple of the weight
+// ring's depth).
 q8mv_status_t choose_mma(int64_t M, int64_t K, int64_t N, const Device &dev, int cps, const int *resident_clusters,
                          const q8mv_opts_t *o, MmaConfig *out) {
     MmaConfig c;
@@ -353,25 +356,13 @@ q8mv_status_t choose_mma(int64_t M, int64_t K, int64_t N, const Device &dev, int
     c.tiles = std::max<int64_t>(1, ceil_div(N, mk::kTileN));
     c.groups = ceil_div(M, mk::kRows);
     c.cps = std::max(1, cps);
-    const int64_t slots = static_cast<int64_t>(dev.sm_count) * c.cps;
-    int64_t split = std::max<int64_t>(1, slots / (c.tiles * c.groups));
-    split = std::min<int64_t>(split, std::max<int64_t>(1, KB));
+    int64_t split = std::max<int64_t>(1, ceil_div(KB, 32));
     const int want = o ? o->split_k : 0;
     if (want > 0) split = std::min<int64_t>(want, std::max<int64_t>(1, KB));
     c.bps = static_cast<int>(std::max<int64_t>(1, ceil_div(KB, split)));
     c.split = static_cast<int>(std::max<int64_t>(1, ceil_div(KB, c.bps)));
     c.cluster = c.split > 1 && c.split <= 8 && resident_clusters != nullptr &&
                 c.tiles * c.groups <= resident_clusters[c.split];
-    if (c.split > 1 && !c.cluster && want == 0 && c.split > 8) {
-        // prefer the cluster form: fewer, longer K ranges
-        int s8 = 8;
-        while (s8 > 1 && !(resident_clusters && c.tiles * c.groups <= resident_clusters[s8])) --s8;
-        if (s8 > 1) {
-            c.bps = static_cast<int>(ceil_div(KB, s8));
-            c.split = static_cast<int>(ceil_div(KB, c.bps));
-            c.cluster = c.split <= 8 && c.tiles * c.groups <= resident_clusters[c.split];
-        }
-    }
     c.cb = static_cast<int>(std::min<int64_t>(16, ceil_div(c.bps, mk::kDepth) * mk::kDepth));
     c.smem = std::max<size_t>(3 * mk::kRows * (c.cb * kBlk + mk::kPad) * 2, mk::kRows * mk::kTileN * 4);
     c.ws_floats = (c.split > 1 && !c.cluster) ? c.groups * c.split * mk::kRows * N : 0;

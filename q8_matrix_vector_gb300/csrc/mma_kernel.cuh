@@ -122,14 +122,26 @@ __device__ __forceinline__ void split3(float a, __nv_bfloat16 &hi, __nv_bfloat16
 // The weights of one block for this lane (rows 4c .. 4c+3 of both 16-row
 // slices, its 4 columns; 0 past K or past N) and the block's scale of column
 // `lane` of the warp's 32 (the fold gathers the ones it needs by shuffles).
-__device__ __forceinline__ void load_block(const Params &p, int b, int64_t nb, int64_t n_lane, int c, uint32_t (&w)[8],
-                                           float &s) {
+// w_lane points at row 4c of block 0 of this lane's columns; rows of a block
+// are at constant offsets from it.  Only a block that reaches past K checks
+// its rows.
+__device__ __forceinline__ void load_block(const Params &p, int b, const int8_t *w_lane, bool cols_ok,
+                                           int64_t n_lane, int c, uint32_t (&w)[8], float &s) {
+    const int8_t *blk = w_lane + static_cast<int64_t>(b) * kBlk * p.N;
+    const bool whole = static_cast<int64_t>(b + 1) * kBlk <= p.K;
+    if (cols_ok && whole) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t row = static_cast<int64_t>(b) * kBlk + 16 * h + 4 * c + j;
-            w[4 * h + j] = (nb < p.N && row < p.K) ? ld_w32(p.W + row * p.N + nb) : 0u;
+            for (int j = 0; j < 4; ++j) w[4 * h + j] = ld_w32(blk + (16 * h + j) * p.N);
+    } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t row = static_cast<int64_t>(b) * kBlk + 16 * h + 4 * c + j;
+                w[4 * h + j] = (cols_ok && row < p.K) ? ld_w32(blk + (16 * h + j) * p.N) : 0u;
+            }
         }
     }
     s = n_lane < p.N ? __ldg(p.S + static_cast<int64_t>(b) * p.N + n_lane) : 0.0f;
@@ -197,11 +209,13 @@ __global__ void __launch_bounds__(kThreads, 4) q8mv_mma_kernel(const Params p) {
 
     // the first kDepth blocks' weights and scales before the dependency wait
     const int64_t n_lane = col0 + lane;
+    const bool cols_ok = nb < p.N;  // N % 4 == 0: the lane's 4 columns are whole or absent
+    const int8_t *w_lane = p.W + static_cast<int64_t>(4 * c) * p.N + (cols_ok ? nb : 0);
     uint32_t ring_w[kDepth][8];
     float ring_s[kDepth];
 #pragma unroll
     for (int d = 0; d < kDepth; ++d)
-        if (d < nblocks) load_block(p, b_begin + d, nb, n_lane, c, ring_w[d], ring_s[d]);
+        if (d < nblocks) load_block(p, b_begin + d, w_lane, cols_ok, n_lane, c, ring_w[d], ring_s[d]);
     pdl_launch_dependents();
     pdl_wait();
 
@@ -245,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 4) q8mv_mma_kernel(const Params p) {
             const int i = i0 + d;
             if (i < nblocks) {
                 block_product(apart, pitch, i - chunk_begin, g, c, ring_w[d], ring_s[d], acc);
-                if (i + kDepth < nblocks) load_block(p, b_begin + i + kDepth, nb, n_lane, c, ring_w[d], ring_s[d]);
+                if (i + kDepth < nblocks)
+                    load_block(p, b_begin + i + kDepth, w_lane, cols_ok, n_lane, c, ring_w[d], ring_s[d]);
             }
         }
     }
