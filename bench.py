@@ -213,7 +213,8 @@ def run_ours(args, rank, local_rank, world):
         W, S = np.ascontiguousarray(W.T), np.ascontiguousarray(S.T)
     bias_h, res_h = epilogue_inputs(N, M) if fused else (None, None)
     kernel = {"auto": q8mv.KERNEL_AUTO, "regs": q8mv.KERNEL_REGS, "tma": q8mv.KERNEL_TMA,
-              "async": q8mv.KERNEL_ASYNC, "mma": q8mv.KERNEL_MMA}[args.kernel]
+              "async": q8mv.KERNEL_ASYNC, "mma": q8mv.KERNEL_MMA,
+              "tc": q8mv.KERNEL_TC}[args.kernel]
     overlap = not args.no_overlap
     plan_opts = dict(kernel=kernel, split_k=args.split, stages=args.stages, threads_n=args.threads_n,
                      cta_threads=args.cta_threads)
@@ -575,7 +576,7 @@ def parse_args(argv=None):
     ap.add_argument("--reference-seconds", type=float, default=60.0,
                     help="CPU budget of the reference arm's timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["auto", "regs", "tma", "async", "mma"], default="auto",
+    ap.add_argument("--kernel", choices=["auto", "regs", "tma", "async", "mma", "tc"], default="auto",
                     help="plan override: kernel family (default: the plan's choice)")
     ap.add_argument("--split", type=int, default=0, help="plan override: K ranges per column tile")
     ap.add_argument("--stages", type=int, default=0, help="plan override: TMA ring depth")

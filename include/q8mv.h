@@ -71,9 +71,14 @@ enum {
                               rows_per_cta outputs, its warps split K, lanes read 16 bytes of a row */
     Q8MV_KERNEL_ROWS_I8 = 5, /* as ROWS, with int8 activations: each 32-element block of A is quantized
                                 in the kernel (q8mv_quantize_rows) and multiplied with dp4a */
-    Q8MV_KERNEL_MMA = 6      /* batched plans: the block products of 16 activation rows on the tensor
+    Q8MV_KERNEL_MMA = 6,     /* batched plans: the block products of 16 activation rows on the tensor
                                 cores (mma.sync bf16, A split into three bf16 parts); needs N % 4 == 0
                                 and a 4-byte aligned W, else the batched register kernel runs */
+    Q8MV_KERNEL_TC = 7       /* batched plans: the block products of 16 activation rows on the
+                                5th-generation tensor cores (tcgen05.mma bf16, accumulators in tensor
+                                memory, A split once per call into three bf16 parts); needs
+                                N % 16 == 0 and a 16-byte aligned W, else the batched register kernel
+                                runs */
 };
 
 /*
@@ -191,8 +196,8 @@ q8mv_status_t q8mv_quantize_rows(int64_t M, int64_t K, const float *A, int8_t *q
  * 2, 4, 8 or 16 at a time (M rounded up to one of them, or ceil(M/16) passes
  * of 16 that each stream the weights again).  Accepted overrides: vec_bytes
  * (8, 4 or 1; 8-byte loads exist for up to 4 rows per pass), threads_n,
- * split_k, overlap, and kernel = Q8MV_KERNEL_MMA for the tensor-core kernel
- * (which takes split_k and overlap); any other non-zero field gives
+ * split_k, overlap, and kernel = Q8MV_KERNEL_MMA or Q8MV_KERNEL_TC for the
+ * tensor-core kernels (which take split_k and overlap); any other non-zero field gives
  * INVALID_ARG.  Without a kernel named, 16 rows per pass on weights of
  * K * N >= 2^27 use the tensor-core kernel, everything else the register
  * kernel.

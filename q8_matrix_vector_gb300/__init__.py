@@ -32,6 +32,7 @@ KERNEL_ASYNC = 3
 KERNEL_ROWS = 4
 KERNEL_ROWS_I8 = 5
 KERNEL_MMA = 6
+KERNEL_TC = 7
 
 ACT_NONE = 0
 ACT_RELU = 1

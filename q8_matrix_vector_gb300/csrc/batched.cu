@@ -9,6 +9,7 @@
 #include "batched.cuh"
 #include "batched.h"
 #include "mma_kernel.cuh"
+#include "tc_kernel.cuh"
 
 #include <cuda_runtime.h>
 
@@ -417,6 +418,113 @@ cudaError_t launch_mma(const MmaConfig &c, const float *A, const int8_t *W, cons
     cfg.attrs = n_attr ? attr : nullptr;
     cfg.numAttrs = n_attr;
     return cudaLaunchKernelEx(&cfg, mma_kernel(c.cluster), prm);
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 kernel
+// ---------------------------------------------------------------------------
+static_assert(kTcThreads == tck::kThreads && kTcTileN == tck::kTileN && kTcRows == tck::kRows,
+              "the tcgen05 kernel's shape as the library reports it");
+
+cudaError_t query_tc(int *cps) {
+    cudaError_t e =
+        cudaFuncSetAttribute(tck::q8mv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tck::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    *cps = 1;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(cps, tck::q8mv_tc_kernel, tck::kThreads, tck::kSmemBytes);
+}
+
+// Column tiles of 128, passes of 16 rows.  The split balances waves against
+// the workspace: with `cps` CTAs resident per SM, an SM streams one block
+// (4 KiB of weights per CTA) in about kBlockUs * cps, and every K range past
+// the first costs a write and a read of its 16 x N partial rows.
+q8mv_status_t choose_tc(int64_t M, int64_t K, int64_t N, const Device &dev, int cps, const q8mv_opts_t *o,
+                        TcConfig *out) {
+    TcConfig c;
+    if (M < 1 || K < 0 || N < 0 || dev.sm_count <= 0) return Q8MV_ERR_INVALID_ARG;
+    if (N % 16 != 0 || N == 0) {
+        *out = c;
+        return Q8MV_OK;
+    }
+    constexpr double kBlockUs = 0.1;    // one block of one CTA with the SM to itself
+    constexpr double kBytesPerUs = 6.0e6;
+    const int64_t KB = std::max<int64_t>(1, ceil_div(K, kBlk));
+    c.tiles = ceil_div(N, tck::kTileN);
+    c.groups = ceil_div(M, tck::kRows);
+    c.cps = std::max(1, cps);
+    const int64_t slots = static_cast<int64_t>(dev.sm_count) * c.cps;
+    const int want = o ? o->split_k : 0;
+    int best = 1;
+    double best_us = 0.0;
+    const int64_t top = want > 0 ? std::min<int64_t>(want, KB) : std::min<int64_t>(KB, 64);
+    for (int64_t s = want > 0 ? top : 1; s <= top; ++s) {
+        const int64_t bps = ceil_div(KB, s);
+        const int64_t split = ceil_div(KB, bps);
+        if (split != s && want == 0) continue;  // the same ranges as a smaller split
+        const int64_t ctas = c.tiles * c.groups * split;
+        const int64_t waves = ceil_div(ctas, slots);
+        const double per_cta = bps * kBlockUs * std::min<int64_t>(c.cps, ceil_div(ctas, dev.sm_count));
+        const double ws = split > 1 ? 2.0 * split * c.groups * tck::kRows * N * 4 / kBytesPerUs : 0.0;
+        const double us = waves * per_cta + ws;
+        if (s == (want > 0 ? top : 1) || us < best_us) {
+            best = static_cast<int>(split);
+            best_us = us;
+        }
+    }
+    c.bps = static_cast<int>(ceil_div(KB, best));
+    c.split = static_cast<int>(ceil_div(KB, c.bps));
+    c.cost_us = best_us;
+    c.ws_floats = c.split > 1 ? c.groups * c.split * tck::kRows * N : 0;
+    c.n_tickets = c.split > 1 ? c.groups * c.tiles : 0;
+    c.parts_bytes = c.groups * KB * tck::kPartBytes;
+    c.usable = true;
+    *out = c;
+    return Q8MV_OK;
+}
+
+cudaError_t launch_tc(const TcConfig &c, const float *A, const int8_t *W, const float *S, float *C, float *ws,
+                      unsigned *tickets, void *parts, int *err, int64_t M, int64_t K, int64_t N,
+                      const q8epi::Epilogue &epi, cudaStream_t stream, bool overlap) {
+    const int KB = static_cast<int>(std::max<int64_t>(1, ceil_div(K, kBlk)));
+    const int64_t total = c.groups * KB * 64;
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3(static_cast<unsigned>(ceil_div(total, 256)));
+    pc.blockDim = dim3(256);
+    pc.stream = stream;
+    pc.attrs = overlap ? &pdl : nullptr;
+    pc.numAttrs = overlap ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&pc, tck::q8mv_tc_parts_kernel, A, static_cast<uint8_t *>(parts), K,
+                                       static_cast<int>(M), KB, total);
+    if (e != cudaSuccess) return e;
+
+    tck::Params prm;
+    prm.W = W;
+    prm.S = S;
+    prm.P = static_cast<const uint8_t *>(parts);
+    prm.C = C;
+    prm.ws = ws;
+    prm.tickets = tickets;
+    prm.err = err;
+    prm.K = K;
+    prm.N = N;
+    prm.M = static_cast<int>(M);
+    prm.KB = KB;
+    prm.split = c.split;
+    prm.bps = c.bps;
+    prm.wait_ns = tck::kWaitNs;
+    prm.epi = epi;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(c.tiles), static_cast<unsigned>(c.split), static_cast<unsigned>(c.groups));
+    cfg.blockDim = dim3(tck::kThreads);
+    cfg.dynamicSmemBytes = tck::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = &pdl;  // its prologue overlaps the parts kernel; it waits for it before reading the parts
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tck::q8mv_tc_kernel, prm);
 }
 
 cudaError_t launch(const Config &c, const float *A, const int8_t *W, const float *S, float *C, float *ws,

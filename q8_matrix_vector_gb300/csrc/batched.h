@@ -67,6 +67,34 @@ struct MmaConfig {
     bool usable = false;
 };
 
+// The tcgen05 kernel (16 rows per pass, accumulators in tensor memory): its
+// planner's choice, usable == false when the shape cannot use it (N % 16 != 0).
+constexpr int kTcThreads = 128;  // threads per CTA of the tcgen05 kernel
+constexpr int kTcTileN = 128;    // its columns per CTA
+constexpr int kTcRows = 16;      // its activation rows per pass
+
+struct TcConfig {
+    int split = 0, bps = 0;
+    int64_t tiles = 0, groups = 0;
+    int cps = 0;                 // resident CTAs per SM
+    int64_t ws_floats = 0, n_tickets = 0;
+    int64_t parts_bytes = 0;     // the activation parts buffer
+    double cost_us = 0.0;        // planner's estimate
+    bool usable = false;
+};
+
+q8mv_status_t choose_tc(int64_t M, int64_t K, int64_t N, const Device &dev, int cps, const q8mv_opts_t *o,
+                        TcConfig *out);
+
+// Resident CTAs per SM of the tcgen05 kernel (and raise its shared-memory
+// limit).  Current device.
+cudaError_t query_tc(int *cps);
+
+// Two launches: the activation parts into `parts`, then the product.
+cudaError_t launch_tc(const TcConfig &c, const float *A, const int8_t *W, const float *S, float *C, float *ws,
+                      unsigned *tickets, void *parts, int *err, int64_t M, int64_t K, int64_t N,
+                      const q8epi::Epilogue &epi, cudaStream_t stream, bool overlap);
+
 q8mv_status_t choose_mma(int64_t M, int64_t K, int64_t N, const Device &dev, int cps, const int *resident_clusters,
                          const q8mv_opts_t *o, MmaConfig *out);
 

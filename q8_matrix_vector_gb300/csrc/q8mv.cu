@@ -679,6 +679,9 @@ struct q8mv_plan_s {
     bk::Config bcfg[bk::kNumVec];
     bk::MmaConfig mcfg;      // tensor-core batched kernel (usable == false if the shape cannot use it)
     bool mma = false;        // batched calls with a 4-byte aligned W run the tensor-core kernel
+    bk::TcConfig tcc;        // tcgen05 batched kernel (usable == false if the shape cannot use it)
+    bool tc = false;         // batched calls with K > 0 and a 16-byte aligned W run the tcgen05 kernel
+    void *parts = nullptr;   // its activation parts, [passes][KB][3 KiB]
     // transposed plans (q8mv_plan_transposed): weights stored one output row per row
     bool rows = false;
     bool rows_i8 = false;   // int8 activations, dp4a
@@ -831,6 +834,7 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
         if (p->ws) cudaFree(p->ws);
         if (p->tickets) cudaFree(p->tickets);
         if (p->err) cudaFree(p->err);
+        if (p->parts) cudaFree(p->parts);
         delete p;
         if (device != prev) cudaSetDevice(prev);
         return s;
@@ -985,6 +989,27 @@ static void fill_mma_info(const bk::MmaConfig &c, int sm_count, int64_t M, int64
     info->grid_z = c.groups;
 }
 
+static void fill_tc_info(const bk::TcConfig &c, int sm_count, int64_t M, int64_t ws_bytes, q8mv_plan_info_t *info) {
+    std::memset(info, 0, sizeof(*info));
+    info->kernel = Q8MV_KERNEL_TC;
+    info->vec_bytes = 16;
+    info->threads_n = 32;
+    info->groups_k = 1;
+    info->threads_per_cta = bk::kTcThreads;
+    info->split_k = c.split;
+    info->blocks_per_split = c.bps;
+    info->cluster = 0;
+    info->tile_n = bk::kTcTileN;
+    info->grid_x = c.tiles;
+    info->grid_y = c.split;
+    info->workspace_bytes = ws_bytes;
+    info->sm_count = sm_count;
+    info->ctas_per_sm = c.cps;
+    info->rows = static_cast<int32_t>(M);
+    info->rows_per_pass = bk::kTcRows;
+    info->grid_z = c.groups;
+}
+
 static void fill_batched_info(const bk::Config &c, int sm_count, int64_t M, int64_t ws_bytes,
                               q8mv_plan_info_t *info) {
     std::memset(info, 0, sizeof(*info));
@@ -1013,6 +1038,11 @@ q8mv_status_t q8mv_plan_info(q8mv_plan_t p, q8mv_plan_info_t *info) {
     if (p->rows) {
         fill_rows_info(p->rcfg, p->K, rows_lv(0, p->K, p->max_vec), p->sm_count, p->rows_cps, p->ws_bytes, info);
         if (p->rows_i8) info->kernel = Q8MV_KERNEL_ROWS_I8;
+        info->overlap = p->overlap ? 1 : 0;
+        return Q8MV_OK;
+    }
+    if (p->mb > 0 && p->tc && p->tcc.usable) {
+        fill_tc_info(p->tcc, p->sm_count, p->M, p->ws_bytes, info);
         info->overlap = p->overlap ? 1 : 0;
         return Q8MV_OK;
     }
@@ -1155,6 +1185,9 @@ static q8mv_status_t run_async(q8mv_plan_t p, const float *A, const int8_t *W, c
 
 static q8mv_status_t run_batched(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
                                  const q8epi::Epilogue &epi, cudaStream_t stream) {
+    if (p->tc && p->tcc.usable && p->K > 0 && reinterpret_cast<uintptr_t>(W) % 16 == 0)
+        return cuda_status(bk::launch_tc(p->tcc, A, W, S, C, p->ws, p->tickets, p->parts, p->err, p->M, p->K, p->N,
+                                         epi, stream, p->overlap));
     if (p->mma && p->mcfg.usable && reinterpret_cast<uintptr_t>(W) % 4 == 0)
         return cuda_status(bk::launch_mma(p->mcfg, A, W, S, C, p->ws, p->tickets, p->M, p->K, p->N, epi, stream,
                                           p->overlap));
@@ -1317,6 +1350,7 @@ q8mv_status_t q8mv_destroy(q8mv_plan_t p) {
     if (p->ws) cudaFree(p->ws);
     if (p->tickets) cudaFree(p->tickets);
     if (p->err) cudaFree(p->err);
+    if (p->parts) cudaFree(p->parts);
     if (prev != p->device) cudaSetDevice(prev);
     delete p;
     return st;
@@ -1326,7 +1360,9 @@ q8mv_status_t q8mv_destroy(q8mv_plan_t p) {
 // 4 rows per pass), threads_n, split_k, overlap.
 static bool batched_opts_ok(int mb, const q8mv_opts_t *o) {
     if (o == nullptr) return true;
-    if (o->kernel != Q8MV_KERNEL_AUTO && o->kernel != Q8MV_KERNEL_REGS && o->kernel != Q8MV_KERNEL_MMA) return false;
+    if (o->kernel != Q8MV_KERNEL_AUTO && o->kernel != Q8MV_KERNEL_REGS && o->kernel != Q8MV_KERNEL_MMA &&
+        o->kernel != Q8MV_KERNEL_TC)
+        return false;
     if (o->stages != 0 || (o->cta_threads != 0 && o->cta_threads != bk::kThreads)) return false;
     if (o->rows_per_cta != 0) return false;
     if (o->overlap != 0 && o->overlap != 1) return false;
@@ -1370,6 +1406,7 @@ q8mv_status_t q8mv_plan_batched(q8mv_plan_t *out, int64_t M, int64_t K, int64_t 
         if (p->ws) cudaFree(p->ws);
         if (p->tickets) cudaFree(p->tickets);
         if (p->err) cudaFree(p->err);
+        if (p->parts) cudaFree(p->parts);
         delete p;
         if (device != prev) cudaSetDevice(prev);
         return s;
@@ -1436,6 +1473,19 @@ q8mv_status_t q8mv_plan_batched(q8mv_plan_t *out, int64_t M, int64_t K, int64_t 
         n_tickets = std::max(n_tickets, p->mcfg.n_tickets);
     }
 
+    // tcgen05 kernel: on request
+    p->tc = opts && opts->kernel == Q8MV_KERNEL_TC;
+    if (p->tc && N > 0 && N % 16 == 0 && K > 0) {
+        int tcps = 1;
+        st = cuda_status(bk::query_tc(&tcps));
+        if (st != Q8MV_OK) return fail(st);
+        if (bk::choose_tc(M, K, N, dev, tcps, opts, &p->tcc) != Q8MV_OK) return fail(Q8MV_ERR_INVALID_ARG);
+        ws_floats = std::max(ws_floats, p->tcc.ws_floats);
+        n_tickets = std::max(n_tickets, p->tcc.n_tickets);
+        st = cuda_status(cudaMalloc(&p->parts, static_cast<size_t>(p->tcc.parts_bytes)));
+        if (st != Q8MV_OK) return fail(st);
+    }
+
     if (ws_floats > 0) {
         st = cuda_status(cudaMalloc(&p->ws, static_cast<size_t>(ws_floats) * sizeof(float)));
         if (st != Q8MV_OK) return fail(st);
@@ -1493,6 +1543,7 @@ q8mv_status_t q8mv_plan_transposed(q8mv_plan_t *out, int64_t K, int64_t N, int d
     }
     auto fail = [&](q8mv_status_t s) {
         if (p->err) cudaFree(p->err);
+        if (p->parts) cudaFree(p->parts);
         delete p;
         if (device != prev) cudaSetDevice(prev);
         return s;
@@ -1555,6 +1606,15 @@ q8mv_status_t q8mv_choose_config_batched(int64_t M, int64_t K, int64_t N, int32_
     bk::Device dev;
     dev.sm_count = sm_count;
     for (int i = 0; i < bk::kNumVec; ++i) dev.cps_regs[i] = ctas_per_sm;
+    if (opts && opts->kernel == Q8MV_KERNEL_TC) {
+        bk::TcConfig tc;
+        const q8mv_status_t st = bk::choose_tc(M, K, N, dev, ctas_per_sm, opts, &tc);
+        if (st != Q8MV_OK) return st;
+        if (!tc.usable) return Q8MV_ERR_INVALID_ARG;
+        fill_tc_info(tc, sm_count, M, tc.ws_floats * static_cast<int64_t>(sizeof(float)), info);
+        info->overlap = opts->overlap == 1 ? 1 : 0;
+        return Q8MV_OK;
+    }
     if (opts && opts->kernel == Q8MV_KERNEL_MMA) {
         // resident clusters estimated for GPCs of 19 SMs
         int clusters[9] = {};
