@@ -429,9 +429,24 @@ static_assert(kTcThreads == tck::kThreads && kTcTileN == tck::kTileN && kTcRows 
 cudaError_t query_tc(int *cps) {
     cudaError_t e =
         cudaFuncSetAttribute(tck::q8mv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tck::kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tck::q8mv_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    *cps = 1;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(cps, tck::q8mv_tc_kernel, tck::kThreads, tck::kSmemBytes);
+    // shared memory decides (registers and threads allow more); the runtime's
+    // occupancy query reports one CTA per SM for this kernel where the
+    // hardware runs two (ncu: occupancy limit 2 by shared memory)
+    int dev = 0, smem_sm = 0, reserved = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, tck::q8mv_tc_kernel);
+    if (e != cudaSuccess) return e;
+    const size_t per_cta = tck::kSmemBytes + fa.sharedSizeBytes + static_cast<size_t>(reserved);
+    *cps = std::max(1, std::min(2, static_cast<int>(static_cast<size_t>(smem_sm) / per_cta)));
+    return cudaSuccess;
 }
 
 // Column tiles of 128, passes of 16 rows.  The split balances waves against
@@ -482,8 +497,8 @@ q8mv_status_t choose_tc(int64_t M, int64_t K, int64_t N, const Device &dev, int 
     return Q8MV_OK;
 }
 
-cudaError_t launch_tc(const TcConfig &c, const float *A, const int8_t *W, const float *S, float *C, float *ws,
-                      unsigned *tickets, void *parts, int *err, int64_t M, int64_t K, int64_t N,
+cudaError_t launch_tc(const TcConfig &c, const float *A, const CUtensorMap *wmap, const CUtensorMap *smap, float *C,
+                      float *ws, unsigned *tickets, void *parts, int *err, int64_t M, int64_t K, int64_t N,
                       const q8epi::Epilogue &epi, cudaStream_t stream, bool overlap) {
     const int KB = static_cast<int>(std::max<int64_t>(1, ceil_div(K, kBlk)));
     const int64_t total = c.groups * KB * 64;
@@ -502,8 +517,6 @@ cudaError_t launch_tc(const TcConfig &c, const float *A, const int8_t *W, const 
     if (e != cudaSuccess) return e;
 
     tck::Params prm;
-    prm.W = W;
-    prm.S = S;
     prm.P = static_cast<const uint8_t *>(parts);
     prm.C = C;
     prm.ws = ws;
@@ -524,7 +537,7 @@ cudaError_t launch_tc(const TcConfig &c, const float *A, const int8_t *W, const 
     cfg.stream = stream;
     cfg.attrs = &pdl;  // its prologue overlaps the parts kernel; it waits for it before reading the parts
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tck::q8mv_tc_kernel, prm);
+    return cudaLaunchKernelEx(&cfg, tck::q8mv_tc_kernel, *wmap, *smap, prm);
 }
 
 cudaError_t launch(const Config &c, const float *A, const int8_t *W, const float *S, float *C, float *ws,

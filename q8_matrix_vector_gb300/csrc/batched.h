@@ -8,6 +8,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime_api.h>
 
 namespace bk {
@@ -69,7 +70,7 @@ struct MmaConfig {
 
 // The tcgen05 kernel (16 rows per pass, accumulators in tensor memory): its
 // planner's choice, usable == false when the shape cannot use it (N % 16 != 0).
-constexpr int kTcThreads = 128;  // threads per CTA of the tcgen05 kernel
+constexpr int kTcThreads = 320;  // threads per CTA of the tcgen05 kernel
 constexpr int kTcTileN = 128;    // its columns per CTA
 constexpr int kTcRows = 16;      // its activation rows per pass
 
@@ -90,9 +91,11 @@ q8mv_status_t choose_tc(int64_t M, int64_t K, int64_t N, const Device &dev, int 
 // limit).  Current device.
 cudaError_t query_tc(int *cps);
 
-// Two launches: the activation parts into `parts`, then the product.
-cudaError_t launch_tc(const TcConfig &c, const float *A, const int8_t *W, const float *S, float *C, float *ws,
-                      unsigned *tickets, void *parts, int *err, int64_t M, int64_t K, int64_t N,
+// Two launches: the activation parts into `parts`, then the product.  wmap:
+// W as a 2D tensor map [K rows][N bytes], box 32 rows x 128 columns, 128-byte
+// swizzle; smap: S [KB rows][N floats], box 1 row x 128 columns.
+cudaError_t launch_tc(const TcConfig &c, const float *A, const CUtensorMap *wmap, const CUtensorMap *smap, float *C,
+                      float *ws, unsigned *tickets, void *parts, int *err, int64_t M, int64_t K, int64_t N,
                       const q8epi::Epilogue &epi, cudaStream_t stream, bool overlap);
 
 q8mv_status_t choose_mma(int64_t M, int64_t K, int64_t N, const Device &dev, int cps, const int *resident_clusters,

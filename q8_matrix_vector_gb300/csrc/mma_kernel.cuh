@@ -120,31 +120,22 @@ __device__ __forceinline__ void split3(float a, __nv_bfloat16 &hi, __nv_bfloat16
 }
 
 // The weights of one block for this lane (rows 4c .. 4c+3 of both 16-row
-// slices, its 4 columns; 0 past K or past N) and the block's scale of column
-// `lane` of the warp's 32 (the fold gathers the ones it needs by shuffles).
-// w_lane points at row 4c of block 0 of this lane's columns; rows of a block
-// are at constant offsets from it.  Only a block that reaches past K checks
-// its rows.
-__device__ __forceinline__ void load_block(const Params &p, int b, const int8_t *w_lane, bool cols_ok,
-                                           int64_t n_lane, int c, uint32_t (&w)[8], float &s) {
-    const int8_t *blk = w_lane + static_cast<int64_t>(b) * kBlk * p.N;
-    const bool whole = static_cast<int64_t>(b + 1) * kBlk <= p.K;
-    if (cols_ok && whole) {
+// slices, its 4 columns at w_col) and the block's scale of column `lane` of
+// the warp's 32 (the fold gathers the ones it needs by shuffles; s_lane is
+// column 0 for lanes past N, whose sums are never stored).  Always eight
+// loads, from addresses clamped into W (rows past K read row K - 1); rows
+// past K and columns past N are zeroed where the words are used.  No value
+// of a load is selected on here: an instruction that reads a load's
+// destination waits for the load, which would cost a memory latency per
+// block.
+__device__ __forceinline__ void load_block(const Params &p, int b, const int8_t *w_col, const float *s_lane, int c,
+                                           uint32_t (&w)[8], float &s) {
+    const int64_t k0 = static_cast<int64_t>(b) * kBlk + 4 * c;
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) w[4 * h + j] = ld_w32(blk + (16 * h + j) * p.N);
-    } else {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t row = static_cast<int64_t>(b) * kBlk + 16 * h + 4 * c + j;
-                w[4 * h + j] = (cols_ok && row < p.K) ? ld_w32(blk + (16 * h + j) * p.N) : 0u;
-            }
-        }
-    }
-    s = n_lane < p.N ? __ldg(p.S + static_cast<int64_t>(b) * p.N + n_lane) : 0.0f;
+        for (int j = 0; j < 4; ++j) w[4 * h + j] = ld_w32(w_col + min(k0 + 16 * h + j, p.K - 1) * p.N);
+    s = __ldg(s_lane + static_cast<int64_t>(b) * p.N);
 }
 
 // The 16 x 32 x 32 product of one block into the four column tiles' f32
@@ -210,12 +201,13 @@ __global__ void __launch_bounds__(kThreads, 4) q8mv_mma_kernel(const Params p) {
     // the first kDepth blocks' weights and scales before the dependency wait
     const int64_t n_lane = col0 + lane;
     const bool cols_ok = nb < p.N;  // N % 4 == 0: the lane's 4 columns are whole or absent
-    const int8_t *w_lane = p.W + static_cast<int64_t>(4 * c) * p.N + (cols_ok ? nb : 0);
+    const int8_t *w_col = p.W + (cols_ok ? nb : 0);
+    const float *s_lane = p.S + (n_lane < p.N ? n_lane : 0);
     uint32_t ring_w[kDepth][8];
     float ring_s[kDepth];
 #pragma unroll
     for (int d = 0; d < kDepth; ++d)
-        if (d < nblocks) load_block(p, b_begin + d, w_lane, cols_ok, n_lane, c, ring_w[d], ring_s[d]);
+        if (d < nblocks) load_block(p, b_begin + d, w_col, s_lane, c, ring_w[d], ring_s[d]);
     pdl_launch_dependents();
     pdl_wait();
 
@@ -258,9 +250,16 @@ __global__ void __launch_bounds__(kThreads, 4) q8mv_mma_kernel(const Params p) {
         for (int d = 0; d < kDepth; ++d) {
             const int i = i0 + d;
             if (i < nblocks) {
-                block_product(apart, pitch, i - chunk_begin, g, c, ring_w[d], ring_s[d], acc);
-                if (i + kDepth < nblocks)
-                    load_block(p, b_begin + i + kDepth, w_lane, cols_ok, n_lane, c, ring_w[d], ring_s[d]);
+                // rows past K and columns past N count as zero bytes
+                const int64_t k0 = static_cast<int64_t>(b_begin + i) * kBlk + 4 * c;
+                uint32_t wm[8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        wm[4 * h + j] = (cols_ok && k0 + 16 * h + j < p.K) ? ring_w[d][4 * h + j] : 0u;
+                block_product(apart, pitch, i - chunk_begin, g, c, wm, ring_s[d], acc);
+                if (i + kDepth < nblocks) load_block(p, b_begin + i + kDepth, w_col, s_lane, c, ring_w[d], ring_s[d]);
             }
         }
     }

@@ -416,6 +416,29 @@ bool encode_s(CUtensorMap *m, const float *S, int64_t KB, int64_t N) {
                                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
 }
 
+// The tcgen05 batched kernel's maps: W [K rows][N bytes], box 32 rows x 128
+// columns, 128-byte swizzle (the kernel reads each row's 16-byte chunks at
+// chunk ^ (row % 8)); S [KB rows][N floats], box 1 row x 128 columns.
+bool encode_w_tc(CUtensorMap *m, const int8_t *W, int64_t K, int64_t N) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N)};
+    const cuuint32_t box[2] = {128, 32};
+    const cuuint32_t elem[2] = {1, 1};
+    return encode_result(1, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(W), dims, strides,
+                                        box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+}
+
+bool encode_s_tc(CUtensorMap *m, const float *S, int64_t KB, int64_t N) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(KB)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
+    const cuuint32_t box[2] = {128, 1};
+    const cuuint32_t elem[2] = {1, 1};
+    return encode_result(2, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(S), dims, strides,
+                                        box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
+}
+
 // A as a 1D map [K floats], box 32.
 bool encode_a(CUtensorMap *m, const float *A, int64_t K) {
     const cuuint64_t dims[1] = {static_cast<cuuint64_t>(K)};
@@ -682,6 +705,7 @@ struct q8mv_plan_s {
     bk::TcConfig tcc;        // tcgen05 batched kernel (usable == false if the shape cannot use it)
     bool tc = false;         // batched calls with K > 0 and a 16-byte aligned W run the tcgen05 kernel
     void *parts = nullptr;   // its activation parts, [passes][KB][3 KiB]
+    MapCache tc_wmaps, tc_smaps;  // its tensor maps of W and S
     // transposed plans (q8mv_plan_transposed): weights stored one output row per row
     bool rows = false;
     bool rows_i8 = false;   // int8 activations, dp4a
@@ -1185,9 +1209,25 @@ static q8mv_status_t run_async(q8mv_plan_t p, const float *A, const int8_t *W, c
 
 static q8mv_status_t run_batched(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
                                  const q8epi::Epilogue &epi, cudaStream_t stream) {
-    if (p->tc && p->tcc.usable && p->K > 0 && reinterpret_cast<uintptr_t>(W) % 16 == 0)
-        return cuda_status(bk::launch_tc(p->tcc, A, W, S, C, p->ws, p->tickets, p->parts, p->err, p->M, p->K, p->N,
-                                         epi, stream, p->overlap));
+    if (p->tc && p->tcc.usable && p->K > 0 && reinterpret_cast<uintptr_t>(W) % 16 == 0 &&
+        reinterpret_cast<uintptr_t>(S) % 16 == 0 && encode_fn() != nullptr) {
+        const CUtensorMap *mw = p->tc_wmaps.find(W);
+        if (mw == nullptr) {
+            CUtensorMap *m = p->tc_wmaps.slot(W);
+            if (!encode_w_tc(m, W, p->K, p->N)) return Q8MV_ERR_CUDA;
+            p->tc_wmaps.commit(W);
+            mw = m;
+        }
+        const CUtensorMap *ms = p->tc_smaps.find(S);
+        if (ms == nullptr) {
+            CUtensorMap *m = p->tc_smaps.slot(S);
+            if (!encode_s_tc(m, S, p->KB, p->N)) return Q8MV_ERR_CUDA;
+            p->tc_smaps.commit(S);
+            ms = m;
+        }
+        return cuda_status(bk::launch_tc(p->tcc, A, mw, ms, C, p->ws, p->tickets, p->parts, p->err, p->M, p->K,
+                                         p->N, epi, stream, p->overlap));
+    }
     if (p->mma && p->mcfg.usable && reinterpret_cast<uintptr_t>(W) % 4 == 0)
         return cuda_status(bk::launch_mma(p->mcfg, A, W, S, C, p->ws, p->tickets, p->M, p->K, p->N, epi, stream,
                                           p->overlap));

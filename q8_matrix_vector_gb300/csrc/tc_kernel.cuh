@@ -23,21 +23,34 @@
 //   * q8mv_tc_parts_kernel splits A into P once, in the shared-memory order
 //     the MMA reads (K-major core matrices of 8 rows x 8 k), 3 KiB per block
 //     of 32 k and pass of 16 rows, zero past M and past K.
-//   * q8mv_tc_kernel: one CTA per (128-column tile, K range, pass), 4 warps.
-//     Per block of 32 rows of W:
-//       - every thread loads its 2 x 16 bytes of the block's 32 x 128 weight
-//         bytes into a register ring kRing blocks ahead, converts them to
-//         bf16 exactly and stores them into a shared-memory tile laid out as
-//         MN-major core matrices (8 k x 8 n);
-//       - one thread waits for the block's activation parts (a bulk copy into
-//         a kStages-deep shared ring), issues two tcgen05.mma (k 0..15,
-//         16..31) of M = 128, N = 48, K = 16 into a TMEM accumulator slot and
-//         commits them to the slot's mbarrier;
-//       - kLag blocks later every thread waits for that mbarrier, reads its
-//         TMEM lane (one column n) with tcgen05.ld and folds the block with
-//         S[b, n].
-//     The weight tiles and accumulator slots rotate over kSlots = kLag + 1:
-//     a tile is rewritten only after the MMA that read it has completed.
+//   * q8mv_tc_kernel: one CTA per (128-column tile, K range, pass), ten
+//     warps with fixed roles, handing work over through mbarriers only:
+//       - the load warp keeps a kStages-deep shared-memory ring filled: per
+//         block, a 2D tensor copy of its 32 x 128 weight bytes (128-byte
+//         swizzle), one of its 128 scales and a bulk copy of its 3 KiB of
+//         activation parts, all completing on the stage's "full" mbarrier
+//         (rows past K and columns past N arrive as zeros); a stage is
+//         refilled once every compute warp has folded its block ("empty");
+//       - eight compute warps convert each block's weight bytes to bf16
+//         exactly (16 bytes a thread) into a tile laid out as MN-major core
+//         matrices (8 k x 8 n) and mark the tile converted ("conv"); kLag
+//         blocks later they wait for the block's MMAs ("done"), read 8 rows
+//         of their TMEM lane (one column n) with tcgen05.ld and fold the
+//         block with S[b, n] from the stage;
+//       - the MMA warp waits for a block's stage and converted tile, issues
+//         two tcgen05.mma (k 0..15, 16..31) of M = 128, N = 48, K = 16 into
+//         the tile's TMEM accumulator slot and commits them to "done".
+//     The bf16 tiles and accumulator slots rotate over kSlots = kLag + 1: a
+//     compute warp rewrites a tile only after folding the block whose MMA
+//     read it, and marks it converted only after that fold's TMEM reads.
+//
+// The weights come through the tensor-memory accelerator rather than a
+// register ring of per-thread loads: with loads issued eight blocks ahead
+// into registers, each block still cost a full memory latency (about 1 us per
+// block and CTA, measured on the attention projection).  The roles are split
+// because one thread issuing the MMAs and copies between CTA barriers put
+// about 500 cycles per block on every warp's path (measured with clock
+// stamps).
 //
 // Split-K CTAs of a column tile are summed in range order through the
 // workspace by the CTA that takes the tile's last ticket.  Every mbarrier wait
@@ -46,6 +59,7 @@
 // issued, frees its tensor memory and returns.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -58,28 +72,37 @@ constexpr int kRows = 16;               // activation rows per pass
 constexpr int kParts = 3;               // bf16 parts of each activation
 constexpr int kMmaN = kParts * kRows;   // 48: the MMA's N
 constexpr int kTileN = 128;             // weight columns per CTA: the MMA's M, one TMEM lane each
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kRing = 8;                // blocks of weights in flight in registers
+constexpr int kWarps = 8;              // compute warps; w and w + 4 share TMEM lane quarter w % 4
+constexpr int kMmaWarp = kWarps;        // issues the MMAs (and owns the TMEM allocation)
+constexpr int kLoadWarp = kWarps + 1;   // keeps the shared-memory ring filled
+constexpr int kThreads = (kWarps + 2) * 32;
 constexpr int kLag = 2;                 // blocks between an MMA's issue and its fold
 constexpr int kSlots = kLag + 1;        // bf16 weight tiles and TMEM accumulator slots
-constexpr int kStages = 8;              // activation-part stages in shared memory
+constexpr int kStages = 10;             // shared-memory ring of copied blocks
 constexpr int kSlotCols = 64;           // TMEM columns per accumulator slot (48 used)
 constexpr uint32_t kTmemCols = 256;     // allocated: a power of two >= kSlots * kSlotCols
 constexpr int kWTileBytes = kBlk * kTileN * 2;   // 8192: one block of bf16 weights
+constexpr int kWStageBytes = kBlk * kTileN;      // 4096: one block of weight bytes
+constexpr int kSStageBytes = kTileN * 4;         // 512: one block of scales
 constexpr int kPartBytes = kBlk * kMmaN * 2;     // 3072: one block of activation parts
-// Shared memory: the weight tiles, the part stages, then padding that keeps
-// every operand read of the MMA inside the allocation and holds the CTA to two
-// per SM (two accumulator allocations fill the SM's 512 TMEM columns).
-constexpr int kSmemBytes = 80 * 1024;
+constexpr uint32_t kStageTx = kWStageBytes + kSStageBytes + kPartBytes;
+// shared memory (offsets from a 1024-byte aligned base): bf16 tiles, weight
+// stages (1024-byte aligned for the swizzle), part stages, scale stages
+constexpr int kTilesOff = 0;
+constexpr int kWRingOff = kTilesOff + kSlots * kWTileBytes;
+constexpr int kPartsOff = kWRingOff + kStages * kWStageBytes;
+constexpr int kSRingOff = kPartsOff + kStages * kPartBytes;
+constexpr int kSmemUsed = kSRingOff + kStages * kSStageBytes;
+constexpr int kSmemBytes = kSmemUsed + 1024;     // + alignment slack; two CTAs fit an SM
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 static_assert(kSlots * kSlotCols <= static_cast<int>(kTmemCols), "accumulator slots exceed the allocation");
-static_assert(kSlots * kWTileBytes + kStages * kPartBytes + 32 * 1024 <= kSmemBytes, "shared-memory budget");
-static_assert(kRing > kLag, "the scale ring must outlast the fold lag");
+static_assert(kWRingOff % 1024 == 0 && kWStageBytes % 1024 == 0, "swizzled stages need 1024-byte alignment");
+static_assert(2 * (kSmemBytes + 2048) <= 228 * 1024, "two CTAs per SM (their TMEM fills the SM's 512 columns)");
+static_assert(kStages > kLag + 1, "a stage is refilled one block after its fold");
 
 // error codes recorded in the device error word
-constexpr int kErrPartsTimeout = 8;
+constexpr int kErrStageTimeout = 8;
 constexpr int kErrMmaTimeout = 16;
 constexpr int kErrDrainTimeout = 32;
 
@@ -91,8 +114,6 @@ constexpr int kWCoreK = (kTileN / 8) * 128;  // 2048
 constexpr int kPCoreK = (kMmaN / 8) * 128;   // 768
 
 struct Params {
-    const int8_t *W;       // [K, N]
-    const float *S;        // [KB, N]
     const uint8_t *P;      // [passes][KB][kPartBytes] activation parts
     float *C;              // [M, N]
     float *ws;             // [passes][split][16][N] partial rows (split > 1)
@@ -129,6 +150,10 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
@@ -199,29 +224,26 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                  : "memory");
 }
 
-// 16 consecutive 32-bit TMEM columns of this thread's lane
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
+// 8 consecutive 32-bit TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ uint4 ld_w128(const int8_t *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p)
-                 : "memory");
-    return v;
+// 2D tensor copy of the box at (x, y) into shared dst, completing on bar
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // Two signed bytes of `flipped` (selectors lo, hi) -> packed bf16x2 (lo in
@@ -303,32 +325,38 @@ __global__ void __launch_bounds__(256) q8mv_tc_parts_kernel(const float *A, uint
     }
 }
 
-// This thread's 2 x 16 weight bytes of block b: rows r and r + 16 of the
-// block, columns col .. col + 15 (zeros past K or past N).
-__device__ __forceinline__ void load_w(const Params &p, int64_t b, const int8_t *w_thread, bool cols_ok, int r,
-                                       uint4 (&w)[2]) {
-    const int8_t *blk = w_thread + b * kBlk * p.N;
-    if (cols_ok && (b + 1) * kBlk <= p.K) {
-        w[0] = ld_w128(blk);
-        w[1] = ld_w128(blk + 16 * p.N);
-    } else {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int64_t row = b * kBlk + r + 16 * j;
-            w[j] = (cols_ok && row < p.K) ? ld_w128(blk + 16 * j * p.N) : make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
+// One thread: fill stage `st` with block b of the CTA's range: weights and
+// scales by tensor copies (before the dependency wait they are inputs no
+// earlier kernel writes), the activation parts by a bulk copy (only after it,
+// when `parts` is set).
+__device__ __forceinline__ void issue_inputs(const CUtensorMap *tmW, const CUtensorMap *tmS, uint32_t base,
+                                             uint64_t *full, int st, int64_t tile, int64_t b) {
+    mbar_arrive_expect_tx(full + st, kStageTx);
+    tma_load_2d(base + kWRingOff + st * kWStageBytes, tmW, static_cast<int>(tile * kTileN), static_cast<int>(b * kBlk),
+                full + st);
+    tma_load_2d(base + kSRingOff + st * kSStageBytes, tmS, static_cast<int>(tile * kTileN), static_cast<int>(b),
+                full + st);
+}
+__device__ __forceinline__ void issue_parts(const Params &p, unsigned char *smem_base, uint64_t *full, int st, int z,
+                                            int64_t b) {
+    bulk_load(smem_base + kPartsOff + st * kPartBytes, p.P + (static_cast<int64_t>(z) * p.KB + b) * kPartBytes,
+              kPartBytes, full + st);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) q8mv_tc_kernel(const Params p) {
-    extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) uint64_t s_pfull[kStages];
-    __shared__ __align__(8) uint64_t s_done[kSlots];
+__global__ void __launch_bounds__(kThreads, 2)
+    q8mv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS, const Params p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t s_full[kStages];   // stage landed (copies' transaction count)
+    __shared__ __align__(8) uint64_t s_empty[kStages];  // stage folded by every compute warp
+    __shared__ __align__(8) uint64_t s_conv[kSlots];    // tile converted by every compute warp
+    __shared__ __align__(8) uint64_t s_done[kSlots];    // the tile's MMAs completed
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     __shared__ unsigned s_is_last;
-    unsigned char *wtile = smem;                               // [kSlots][kWTileBytes]
-    unsigned char *parts = smem + kSlots * kWTileBytes;        // [kStages][kPartBytes]
+    // a 1024-byte aligned base (the swizzled weight stages need it)
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t base = smem_u32(smem);
     const volatile int *abort_flag = &s_abort;
 
     const int tid = threadIdx.x;
@@ -341,40 +369,35 @@ __global__ void __launch_bounds__(kThreads, 2) q8mv_tc_kernel(const Params p) {
     const int64_t b_end = b_begin + p.bps < p.KB ? b_begin + p.bps : static_cast<int64_t>(p.KB);
     const int nblocks = b_end > b_begin ? static_cast<int>(b_end - b_begin) : 0;
 
-    // conversion: rows r, r + 16 of a block, 16 columns from col_c
-    const int r = lane & 15;
-    const int half = lane >> 4;
-    const int64_t col_c = tile * kTileN + warp * 32 + half * 16;
-    const bool cols_ok = col_c < p.N;  // N % 16 == 0: the 16 columns are whole or absent
-    const int8_t *w_thread = p.W + static_cast<int64_t>(r) * p.N + (cols_ok ? col_c : 0);
-    const int ng = warp * 4 + half * 2;  // the first of the two core-matrix columns this thread fills
-    // fold: TMEM lane = tid = column n of the tile
-    const int64_t n = tile * kTileN + tid;
-    const bool n_ok = n < p.N;
+    // compute warps.  conversion: row k = lane of a block, the 16 columns of
+    // chunk c16 = warp; fold: TMEM lane quarter q (column n of the tile), rows
+    // 8 rh .. 8 rh + 7
+    const int c16 = warp;
+    const int ng = c16 * 2;  // the first of the two core-matrix columns this thread fills
+    const int q = warp & 3, rh = (warp >> 2) & 1;
+    const int nl = q * 32 + lane;
+    const int64_t n = tile * kTileN + nl;
+    const bool n_ok = warp < kWarps && n < p.N;
 
-    if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(s_pfull + s, 1);
-        for (int s = 0; s < kSlots; ++s) mbar_init(s_done + s, 1);
+    if (warp == kLoadWarp && lane == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(s_full + s, 1);
+            mbar_init(s_empty + s, kWarps);
+        }
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(s_conv + s, kWarps);
+            mbar_init(s_done + s, 1);
+        }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (int i = 0; i < kStages && i < nblocks; ++i) issue_inputs(&tmW, &tmS, base, s_full, i, tile, b_begin + i);
     }
-    __syncwarp();
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
                      "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-
-    // the first kRing blocks of weights and scales: inputs no earlier kernel writes
-    uint4 ring_w[kRing][2];
-    float ring_s[kRing];
-#pragma unroll
-    for (int d = 0; d < kRing; ++d) {
-        if (d < nblocks) {
-            load_w(p, b_begin + d, w_thread, cols_ok, r, ring_w[d]);
-            ring_s[d] = n_ok ? __ldg(p.S + (b_begin + d) * p.N + n) : 0.0f;
-        }
     }
     tc_fence_before();
     __syncthreads();
@@ -383,115 +406,158 @@ __global__ void __launch_bounds__(kThreads, 2) q8mv_tc_kernel(const Params p) {
     pdl_launch_dependents();
     pdl_wait();  // the activation parts come from the kernel launched just before
 
-    int issued_parts = 0;  // thread 0: part copies issued
-    int issued_mma = 0;    // thread 0: blocks whose MMAs were issued
-    if (tid == 0) {
-        for (int i = 0; i < kStages && i < nblocks; ++i) {
-            mbar_arrive_expect_tx(s_pfull + i, kPartBytes);
-            bulk_load(parts + i * kPartBytes, p.P + ((static_cast<int64_t>(z) * p.KB + b_begin + i) * kPartBytes),
-                      kPartBytes, s_pfull + i);
-            ++issued_parts;
+    float2 acc[4];  // compute warps: rows 8 rh + 2 j, 8 rh + 2 j + 1 of column n
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.0f, 0.0f);
+    bool bad = false;  // warp-uniform
+    int last_issue[kStages];  // load warp: the last block issued into each stage (-1: none)
+    int issued_mma = 0;       // MMA warp: blocks whose MMAs were issued
+
+    if (warp == kLoadWarp) {
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) last_issue[s] = s < nblocks ? s : -1;
+            for (int i = 0; i < kStages && i < nblocks; ++i) issue_parts(p, smem, s_full, i, z, b_begin + i);
+            // block j into stage j % kStages once the compute warps folded block j - kStages
+            int st = 0;
+            uint32_t ph = 0;
+            for (int j = kStages; j < nblocks; ++j) {
+                if (!mbar_wait(s_empty + st, ph, abort_flag, p.wait_ns)) {
+                    bad = true;
+                    s_abort = 1;
+                    atomicOr(p.err, kErrStageTimeout);
+                    break;
+                }
+                issue_inputs(&tmW, &tmS, base, s_full, st, tile, b_begin + j);
+                issue_parts(p, smem, s_full, st, z, b_begin + j);
+                last_issue[st] = j;
+                if (++st == kStages) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            }
         }
-    }
-
-    float2 acc[kRows / 2];
-#pragma unroll
-    for (int q = 0; q < kRows / 2; ++q) acc[q] = make_float2(0.0f, 0.0f);
-    bool bad = false;
-
-    for (int i0 = 0; i0 < nblocks + kLag; i0 += kRing) {
-#pragma unroll
-        for (int d = 0; d < kRing; ++d) {
-            const int i = i0 + d;
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            int st = 0, sl = 0;
+            uint32_t st_ph = 0, sl_ph = 0;
+            for (int i = 0; i < nblocks; ++i) {
+                // the block's parts landed, and every compute warp converted its weights
+                // (after folding the block that last used this accumulator slot)
+                if (!mbar_wait(s_full + st, st_ph, abort_flag, p.wait_ns) ||
+                    !mbar_wait(s_conv + sl, sl_ph, abort_flag, p.wait_ns)) {
+                    bad = true;
+                    s_abort = 1;
+                    atomicOr(p.err, kErrStageTimeout);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = base + kTilesOff + sl * kWTileBytes;
+                const uint32_t b0 = base + kPartsOff + st * kPartBytes;
+                const uint32_t dt = tmem + sl * kSlotCols;
+                mma_bf16(dt, smem_desc(a0, kWCoreK, 128), smem_desc(b0, kPCoreK, 128), 0u);
+                mma_bf16(dt, smem_desc(a0 + 2 * kWCoreK, kWCoreK, 128), smem_desc(b0 + 2 * kPCoreK, kPCoreK, 128), 1u);
+                mma_commit(s_done + sl);
+                issued_mma = i + 1;
+                if (++sl == kSlots) {
+                    sl = 0;
+                    sl_ph ^= 1u;
+                }
+                if (++st == kStages) {
+                    st = 0;
+                    st_ph ^= 1u;
+                }
+            }
+        }
+    } else {
+        // stage and phase of block i; slot of block i; stage, slot and phase of
+        // the folded block f = i - kLag
+        int st = 0, sl = 0, f_st = 0, f_sl = 0;
+        uint32_t st_ph = 0, f_ph = 0;
+        for (int i = 0; i < nblocks + kLag && !bad; ++i) {
             if (i < nblocks) {
-                // weights of block i -> bf16 tile i % kSlots (its last reader, the MMA of block
-                // i - kSlots, was seen complete by every thread at that block's fold)
-                unsigned char *wt = wtile + (i % kSlots) * kWTileBytes;
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    uint4 lo, hi;
-                    convert16(ring_w[d][j], lo, hi);
-                    const int k = r + 16 * j;
-                    unsigned char *row = wt + (k >> 3) * kWCoreK + (k & 7) * 16;
-                    *reinterpret_cast<uint4 *>(row + ng * 128) = lo;
-                    *reinterpret_cast<uint4 *>(row + (ng + 1) * 128) = hi;
+                const bool waited = mbar_wait(s_full + st, st_ph, abort_flag, p.wait_ns);
+                if (!__all_sync(0xffffffffu, waited)) {
+                    bad = true;
+                    s_abort = 1;
+                    if (lane == 0) atomicOr(p.err, kErrStageTimeout);
+                    break;
                 }
+                // weights of block i -> bf16 tile sl (its last reader, the MMA of block
+                // i - kSlots, was seen complete by this warp at that block's fold)
+                const unsigned char *ws = smem + kWRingOff + st * kWStageBytes;
+                unsigned char *wt = smem + kTilesOff + sl * kWTileBytes;
+                const int k = lane;
+                const uint4 w = *reinterpret_cast<const uint4 *>(ws + k * 128 + ((c16 ^ (k & 7)) << 4));
+                uint4 lo, hi;
+                convert16(w, lo, hi);
+                unsigned char *row = wt + (k >> 3) * kWCoreK + (k & 7) * 16;
+                *reinterpret_cast<uint4 *>(row + ng * 128) = lo;
+                *reinterpret_cast<uint4 *>(row + (ng + 1) * 128) = hi;
                 fence_proxy_async_smem();
-                if (i + kRing < nblocks) load_w(p, b_begin + i + kRing, w_thread, cols_ok, r, ring_w[d]);
-                if (__syncthreads_or(bad)) goto drain;
-                if (tid == 0) {
-                    if (!mbar_wait(s_pfull + i % kStages, (i / kStages) & 1, abort_flag, p.wait_ns)) {
-                        bad = true;
-                        s_abort = 1;
-                        atomicOr(p.err, kErrPartsTimeout);
-                    } else {
-                        tc_fence_after();
-                        const uint32_t a0 = smem_u32(wt);
-                        const uint32_t b0 = smem_u32(parts + (i % kStages) * kPartBytes);
-                        const uint32_t dt = tmem + (i % kSlots) * kSlotCols;
-                        mma_bf16(dt, smem_desc(a0, kWCoreK, 128), smem_desc(b0, kPCoreK, 128), 0u);
-                        mma_bf16(dt, smem_desc(a0 + 2 * kWCoreK, kWCoreK, 128), smem_desc(b0 + 2 * kPCoreK, kPCoreK, 128),
-                                 1u);
-                        mma_commit(s_done + i % kSlots);
-                        issued_mma = i + 1;
-                    }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_conv + sl);
+                if (++sl == kSlots) sl = 0;
+                if (++st == kStages) {
+                    st = 0;
+                    st_ph ^= 1u;
                 }
-                bad = __any_sync(0xffffffffu, bad);  // warp-uniform: tcgen05.ld below is .sync.aligned
             }
             const int f = i - kLag;  // the block folded now
-            if (f >= 0 && f < nblocks && !bad) {
-                const bool waited = mbar_wait(s_done + f % kSlots, (f / kSlots) & 1, abort_flag, p.wait_ns);
+            if (f >= 0 && f < nblocks) {
+                const bool waited = mbar_wait(s_done + f_sl, f_ph, abort_flag, p.wait_ns);
                 if (!__all_sync(0xffffffffu, waited)) {
                     bad = true;
                     s_abort = 1;
                     if (lane == 0) atomicOr(p.err, kErrMmaTimeout);
-                } else {
-                    tc_fence_after();
-                    const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) + (f % kSlots) * kSlotCols;
-                    float dh[16], dm[16], dl[16];
-                    tmem_ld16(ta, dh);
-                    tmem_ld16(ta + 16, dm);
-                    tmem_ld16(ta + 32, dl);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    const int ds = (d - kLag + kRing) % kRing;
-                    const float2 s2 = make_float2(ring_s[ds], ring_s[ds]);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + f_sl * kSlotCols + rh * 8;
+                float dh[8], dm[8], dl[8];
+                tmem_ld8(ta, dh);
+                tmem_ld8(ta + kRows, dm);
+                tmem_ld8(ta + 2 * kRows, dl);
+                const float sv = reinterpret_cast<const float *>(smem + kSRingOff + f_st * kSStageBytes)[nl];
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_empty + f_st);  // the stage's last reader
+                const float2 s2 = make_float2(sv, sv);
 #pragma unroll
-                    for (int q = 0; q < kRows / 2; ++q) {
-                        const float2 x = __fadd2_rn(__fadd2_rn(make_float2(dh[2 * q], dh[2 * q + 1]),
-                                                               make_float2(dm[2 * q], dm[2 * q + 1])),
-                                                    make_float2(dl[2 * q], dl[2 * q + 1]));
-                        acc[q] = __ffma2_rn(x, s2, acc[q]);
-                    }
-                    if (f + kRing < nblocks) ring_s[ds] = n_ok ? __ldg(p.S + (b_begin + f + kRing) * p.N + n) : 0.0f;
-                    if (tid == 0 && f + kStages < nblocks) {
-                        const int s = f % kStages;
-                        mbar_arrive_expect_tx(s_pfull + s, kPartBytes);
-                        bulk_load(parts + s * kPartBytes,
-                                  p.P + ((static_cast<int64_t>(z) * p.KB + b_begin + f + kStages) * kPartBytes),
-                                  kPartBytes, s_pfull + s);
-                        ++issued_parts;
-                    }
+                for (int j = 0; j < 4; ++j) {
+                    const float2 x = __fadd2_rn(__fadd2_rn(make_float2(dh[2 * j], dh[2 * j + 1]),
+                                                           make_float2(dm[2 * j], dm[2 * j + 1])),
+                                                make_float2(dl[2 * j], dl[2 * j + 1]));
+                    acc[j] = __ffma2_rn(x, s2, acc[j]);
+                }
+            }
+            if (f >= 0) {
+                if (++f_st == kStages) f_st = 0;
+                if (++f_sl == kSlots) {
+                    f_sl = 0;
+                    f_ph ^= 1u;
                 }
             }
         }
     }
-drain:
+
     if (__syncthreads_or(bad)) {
         // let what this CTA issued land before its memory goes away
-        if (tid == 0) {
-            bool ok = true;
-            if (issued_mma > 0)
-                ok = mbar_wait(s_done + (issued_mma - 1) % kSlots, ((issued_mma - 1) / kSlots) & 1, nullptr,
-                               p.wait_ns);
-            for (int i = issued_mma; i < issued_parts && ok; ++i)
-                ok = mbar_wait(s_pfull + i % kStages, (i / kStages) & 1, nullptr, p.wait_ns);
-            if (!ok) atomicOr(p.err, kErrDrainTimeout);
+        bool ok = true;
+        if (warp == kMmaWarp && lane == 0 && issued_mma > 0)
+            ok = mbar_wait(s_done + (issued_mma - 1) % kSlots, ((issued_mma - 1) / kSlots) & 1, nullptr, p.wait_ns);
+        if (warp == kLoadWarp && lane == 0) {
+            for (int s = 0; s < kStages && ok; ++s)
+                if (last_issue[s] >= 0)
+                    ok = mbar_wait(s_full + s, (last_issue[s] / kStages) & 1, nullptr, p.wait_ns);
         }
+        if (!ok) atomicOr(p.err, kErrDrainTimeout);
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (warp == 0)
+        if (warp == kMmaWarp)
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                          : "memory");
         return;
@@ -499,20 +565,20 @@ drain:
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 0)
+    if (warp == kMmaWarp)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 
-    // acc[q] holds rows 2q, 2q + 1 of column n
+    // acc[j] holds rows 8 rh + 2 j, 8 rh + 2 j + 1 of column n
     if (p.split == 1) {
         if (n_ok) {
 #pragma unroll
-            for (int q = 0; q < kRows / 2; ++q) {
+            for (int j = 0; j < 4; ++j) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int m = 2 * q + h;
+                    const int m = rh * 8 + 2 * j + h;
                     if (m < mrows) {
                         const int64_t idx = static_cast<int64_t>(m0 + m) * p.N + n;
-                        p.C[idx] = q8epi::apply(p.epi, h ? acc[q].y : acc[q].x, p.C, idx, n);
+                        p.C[idx] = q8epi::apply(p.epi, h ? acc[j].y : acc[j].x, p.C, idx, n);
                     }
                 }
             }
@@ -525,9 +591,10 @@ drain:
     float *ws_row = p.ws + (static_cast<int64_t>(z) * p.split + blockIdx.y) * kRows * p.N;
     if (n_ok) {
 #pragma unroll
-        for (int q = 0; q < kRows / 2; ++q) {
-            if (2 * q < mrows) ws_row[static_cast<int64_t>(2 * q) * p.N + n] = acc[q].x;
-            if (2 * q + 1 < mrows) ws_row[static_cast<int64_t>(2 * q + 1) * p.N + n] = acc[q].y;
+        for (int j = 0; j < 4; ++j) {
+            const int m = rh * 8 + 2 * j;
+            if (m < mrows) ws_row[static_cast<int64_t>(m) * p.N + n] = acc[j].x;
+            if (m + 1 < mrows) ws_row[static_cast<int64_t>(m + 1) * p.N + n] = acc[j].y;
         }
     }
     unsigned *ticket = p.tickets + static_cast<int64_t>(z) * gridDim.x + tile;
@@ -539,9 +606,9 @@ drain:
     __threadfence();
     const float *ws_group = p.ws + static_cast<int64_t>(z) * p.split * kRows * p.N;
     if (n_ok) {
-        for (int m = 0; m < mrows; ++m) {
+        for (int m = rh * 8; m < min(mrows, rh * 8 + 8); ++m) {
             float v = __ldcg(ws_group + static_cast<int64_t>(m) * p.N + n);
-            for (int q = 1; q < p.split; ++q) v += __ldcg(ws_group + (static_cast<int64_t>(q) * kRows + m) * p.N + n);
+            for (int y = 1; y < p.split; ++y) v += __ldcg(ws_group + (static_cast<int64_t>(y) * kRows + m) * p.N + n);
             const int64_t idx = static_cast<int64_t>(m0 + m) * p.N + n;
             p.C[idx] = q8epi::apply(p.epi, v, p.C, idx, n);
         }
