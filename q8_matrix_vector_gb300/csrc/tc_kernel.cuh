@@ -76,10 +76,12 @@ constexpr int kWarps = 8;              // compute warps; w and w + 4 share TMEM 
 constexpr int kMmaWarp = kWarps;        // issues the MMAs (and owns the TMEM allocation)
 constexpr int kLoadWarp = kWarps + 1;   // keeps the shared-memory ring filled
 constexpr int kThreads = (kWarps + 2) * 32;
-constexpr int kLag = 2;                 // blocks between an MMA's issue and its fold
-constexpr int kSlots = kLag + 1;        // bf16 weight tiles and TMEM accumulator slots
-constexpr int kStages = 10;             // shared-memory ring of copied blocks
-constexpr int kSlotCols = 64;           // TMEM columns per accumulator slot (48 used)
+constexpr int kPair = 2;                // blocks per step of the compute and MMA warps
+constexpr int kLag = 1;                 // steps between a step's MMAs and its fold
+constexpr int kSlots = kLag + 1;        // steps of bf16 tiles and TMEM accumulators in flight
+constexpr int kStages = 10;             // shared-memory ring of copied blocks (a multiple of kPair)
+constexpr int kBlockCols = 64;          // TMEM columns per block's accumulator (48 used)
+constexpr int kSlotCols = kPair * kBlockCols;
 constexpr uint32_t kTmemCols = 256;     // allocated: a power of two >= kSlots * kSlotCols
 constexpr int kWTileBytes = kBlk * kTileN * 2;   // 8192: one block of bf16 weights
 constexpr int kWStageBytes = kBlk * kTileN;      // 4096: one block of weight bytes
@@ -89,7 +91,7 @@ constexpr uint32_t kStageTx = kWStageBytes + kSStageBytes + kPartBytes;
 // shared memory (offsets from a 1024-byte aligned base): bf16 tiles, weight
 // stages (1024-byte aligned for the swizzle), part stages, scale stages
 constexpr int kTilesOff = 0;
-constexpr int kWRingOff = kTilesOff + kSlots * kWTileBytes;
+constexpr int kWRingOff = kTilesOff + kSlots * kPair * kWTileBytes;
 constexpr int kPartsOff = kWRingOff + kStages * kWStageBytes;
 constexpr int kSRingOff = kPartsOff + kStages * kPartBytes;
 constexpr int kSmemUsed = kSRingOff + kStages * kSStageBytes;
@@ -99,7 +101,8 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 static_assert(kSlots * kSlotCols <= static_cast<int>(kTmemCols), "accumulator slots exceed the allocation");
 static_assert(kWRingOff % 1024 == 0 && kWStageBytes % 1024 == 0, "swizzled stages need 1024-byte alignment");
 static_assert(2 * (kSmemBytes + 2048) <= 228 * 1024, "two CTAs per SM (their TMEM fills the SM's 512 columns)");
-static_assert(kStages > kLag + 1, "a stage is refilled one block after its fold");
+static_assert(kStages % kPair == 0 && kStages >= (kLag + 2) * kPair, "a step's stages share a phase");
+static_assert(kSlots == 2, "slot arithmetic below takes two slots");
 
 // error codes recorded in the device error word
 constexpr int kErrStageTimeout = 8;
@@ -411,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.0f, 0.0f);
     bool bad = false;  // warp-uniform
     int last_issue[kStages];  // load warp: the last block issued into each stage (-1: none)
-    int issued_mma = 0;       // MMA warp: blocks whose MMAs were issued
+    int issued_mma = 0;       // MMA warp: steps whose MMAs were issued
 
     if (warp == kLoadWarp) {
         if (lane == 0) {
@@ -441,10 +444,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             int st = 0, sl = 0;
             uint32_t st_ph = 0, sl_ph = 0;
-            for (int i = 0; i < nblocks; ++i) {
-                // the block's parts landed, and every compute warp converted its weights
-                // (after folding the block that last used this accumulator slot)
+            const int nsteps = (nblocks + kPair - 1) / kPair;
+            for (int t = 0; t < nsteps; ++t) {
+                const bool two = kPair * t + 1 < nblocks;
+                // the step's parts landed, and every compute warp converted its weights
+                // (after folding the step that last used this accumulator slot)
                 if (!mbar_wait(s_full + st, st_ph, abort_flag, p.wait_ns) ||
+                    (two && !mbar_wait(s_full + st + 1, st_ph, abort_flag, p.wait_ns)) ||
                     !mbar_wait(s_conv + sl, sl_ph, abort_flag, p.wait_ns)) {
                     bad = true;
                     s_abort = 1;
@@ -452,60 +458,70 @@ __global__ void __launch_bounds__(kThreads, 2)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a0 = base + kTilesOff + sl * kWTileBytes;
-                const uint32_t b0 = base + kPartsOff + st * kPartBytes;
-                const uint32_t dt = tmem + sl * kSlotCols;
-                mma_bf16(dt, smem_desc(a0, kWCoreK, 128), smem_desc(b0, kPCoreK, 128), 0u);
-                mma_bf16(dt, smem_desc(a0 + 2 * kWCoreK, kWCoreK, 128), smem_desc(b0 + 2 * kPCoreK, kPCoreK, 128), 1u);
-                mma_commit(s_done + sl);
-                issued_mma = i + 1;
-                if (++sl == kSlots) {
-                    sl = 0;
-                    sl_ph ^= 1u;
+                for (int h = 0; h < (two ? 2 : 1); ++h) {
+                    const uint32_t a0 = base + kTilesOff + (sl * kPair + h) * kWTileBytes;
+                    const uint32_t b0 = base + kPartsOff + (st + h) * kPartBytes;
+                    const uint32_t dt = tmem + sl * kSlotCols + h * kBlockCols;
+                    mma_bf16(dt, smem_desc(a0, kWCoreK, 128), smem_desc(b0, kPCoreK, 128), 0u);
+                    mma_bf16(dt, smem_desc(a0 + 2 * kWCoreK, kWCoreK, 128), smem_desc(b0 + 2 * kPCoreK, kPCoreK, 128),
+                             1u);
                 }
-                if (++st == kStages) {
+                mma_commit(s_done + sl);
+                issued_mma = t + 1;
+                sl ^= 1;
+                if (sl == 0) sl_ph ^= 1u;
+                st += kPair;
+                if (st == kStages) {
                     st = 0;
                     st_ph ^= 1u;
                 }
             }
         }
     } else {
-        // stage and phase of block i; slot of block i; stage, slot and phase of
-        // the folded block f = i - kLag
+        // stage and phase of step t's first block, slot of step t; stage, slot and
+        // phase of the folded step f = t - kLag
         int st = 0, sl = 0, f_st = 0, f_sl = 0;
         uint32_t st_ph = 0, f_ph = 0;
-        for (int i = 0; i < nblocks + kLag && !bad; ++i) {
-            if (i < nblocks) {
-                const bool waited = mbar_wait(s_full + st, st_ph, abort_flag, p.wait_ns);
+        const int nsteps = (nblocks + kPair - 1) / kPair;
+        const int k = lane;
+        const int w_off = k * 128 + ((c16 ^ (k & 7)) << 4);                       // in a weight stage
+        const int t_off = (k >> 3) * kWCoreK + (k & 7) * 16 + ng * 128;            // in a bf16 tile
+        for (int t = 0; t < nsteps + kLag && !bad; ++t) {
+            if (t < nsteps) {
+                const bool two = kPair * t + 1 < nblocks;
+                bool waited = mbar_wait(s_full + st, st_ph, abort_flag, p.wait_ns);
+                if (two && waited) waited = mbar_wait(s_full + st + 1, st_ph, abort_flag, p.wait_ns);
                 if (!__all_sync(0xffffffffu, waited)) {
                     bad = true;
                     s_abort = 1;
                     if (lane == 0) atomicOr(p.err, kErrStageTimeout);
                     break;
                 }
-                // weights of block i -> bf16 tile sl (its last reader, the MMA of block
-                // i - kSlots, was seen complete by this warp at that block's fold)
-                const unsigned char *ws = smem + kWRingOff + st * kWStageBytes;
-                unsigned char *wt = smem + kTilesOff + sl * kWTileBytes;
-                const int k = lane;
-                const uint4 w = *reinterpret_cast<const uint4 *>(ws + k * 128 + ((c16 ^ (k & 7)) << 4));
-                uint4 lo, hi;
-                convert16(w, lo, hi);
-                unsigned char *row = wt + (k >> 3) * kWCoreK + (k & 7) * 16;
-                *reinterpret_cast<uint4 *>(row + ng * 128) = lo;
-                *reinterpret_cast<uint4 *>(row + (ng + 1) * 128) = hi;
+                // weights of the step's blocks -> bf16 tiles of slot sl (their last reader, the
+                // MMAs of step t - kSlots, was seen complete by this warp at that step's fold)
+                for (int h = 0; h < (two ? 2 : 1); ++h) {
+                    const uint4 w =
+                        *reinterpret_cast<const uint4 *>(smem + kWRingOff + (st + h) * kWStageBytes + w_off);
+                    uint4 lo, hi;
+                    convert16(w, lo, hi);
+                    unsigned char *row = smem + kTilesOff + (sl * kPair + h) * kWTileBytes + t_off;
+                    *reinterpret_cast<uint4 *>(row) = lo;
+                    *reinterpret_cast<uint4 *>(row + 128) = hi;
+                }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(s_conv + sl);
-                if (++sl == kSlots) sl = 0;
-                if (++st == kStages) {
+                sl ^= 1;
+                st += kPair;
+                if (st == kStages) {
                     st = 0;
                     st_ph ^= 1u;
                 }
             }
-            const int f = i - kLag;  // the block folded now
-            if (f >= 0 && f < nblocks) {
+            const int f = t - kLag;  // the step folded now
+            if (f >= 0 && f < nsteps) {
+                const bool two = kPair * f + 1 < nblocks;
                 const bool waited = mbar_wait(s_done + f_sl, f_ph, abort_flag, p.wait_ns);
                 if (!__all_sync(0xffffffffu, waited)) {
                     bad = true;
@@ -515,30 +531,50 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc_fence_after();
                 const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + f_sl * kSlotCols + rh * 8;
-                float dh[8], dm[8], dl[8];
-                tmem_ld8(ta, dh);
-                tmem_ld8(ta + kRows, dm);
-                tmem_ld8(ta + 2 * kRows, dl);
-                const float sv = reinterpret_cast<const float *>(smem + kSRingOff + f_st * kSStageBytes)[nl];
+                const float *sring = reinterpret_cast<const float *>(smem + kSRingOff);
+                float d0[3][8], d1[3][8];
+                tmem_ld8(ta, d0[0]);
+                tmem_ld8(ta + kRows, d0[1]);
+                tmem_ld8(ta + 2 * kRows, d0[2]);
+                const float s0 = sring[f_st * (kSStageBytes / 4) + nl];
+                float s1 = 0.0f;
+                if (two) {
+                    tmem_ld8(ta + kBlockCols, d1[0]);
+                    tmem_ld8(ta + kBlockCols + kRows, d1[1]);
+                    tmem_ld8(ta + kBlockCols + 2 * kRows, d1[2]);
+                    s1 = sring[(f_st + 1) * (kSStageBytes / 4) + nl];
+                }
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(s_empty + f_st);  // the stage's last reader
-                const float2 s2 = make_float2(sv, sv);
+                if (lane == 0) {  // the stages' last readers
+                    mbar_arrive(s_empty + f_st);
+                    if (two) mbar_arrive(s_empty + f_st + 1);
+                }
+                const float2 s02 = make_float2(s0, s0);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float2 x = __fadd2_rn(__fadd2_rn(make_float2(dh[2 * j], dh[2 * j + 1]),
-                                                           make_float2(dm[2 * j], dm[2 * j + 1])),
-                                                make_float2(dl[2 * j], dl[2 * j + 1]));
-                    acc[j] = __ffma2_rn(x, s2, acc[j]);
+                    const float2 x = __fadd2_rn(__fadd2_rn(make_float2(d0[0][2 * j], d0[0][2 * j + 1]),
+                                                           make_float2(d0[1][2 * j], d0[1][2 * j + 1])),
+                                                make_float2(d0[2][2 * j], d0[2][2 * j + 1]));
+                    acc[j] = __ffma2_rn(x, s02, acc[j]);
+                }
+                if (two) {
+                    const float2 s12 = make_float2(s1, s1);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 x = __fadd2_rn(__fadd2_rn(make_float2(d1[0][2 * j], d1[0][2 * j + 1]),
+                                                               make_float2(d1[1][2 * j], d1[1][2 * j + 1])),
+                                                    make_float2(d1[2][2 * j], d1[2][2 * j + 1]));
+                        acc[j] = __ffma2_rn(x, s12, acc[j]);
+                    }
                 }
             }
             if (f >= 0) {
-                if (++f_st == kStages) f_st = 0;
-                if (++f_sl == kSlots) {
-                    f_sl = 0;
-                    f_ph ^= 1u;
-                }
+                f_st += kPair;
+                if (f_st == kStages) f_st = 0;
+                f_sl ^= 1;
+                if (f_sl == 0) f_ph ^= 1u;
             }
         }
     }
@@ -548,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         bool ok = true;
         if (warp == kMmaWarp && lane == 0 && issued_mma > 0)
             ok = mbar_wait(s_done + (issued_mma - 1) % kSlots, ((issued_mma - 1) / kSlots) & 1, nullptr, p.wait_ns);
+        // (issued_mma counts steps; each step committed once)
         if (warp == kLoadWarp && lane == 0) {
             for (int s = 0; s < kStages && ok; ++s)
                 if (last_issue[s] >= 0)
