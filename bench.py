@@ -106,10 +106,21 @@ def kernel_source_hash(name: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-def traffic_key(workload: str, rows: int, transposed: bool = False, a_int8: bool = False) -> str:
+KERNEL_NAMES = {1: "regs", 2: "tma", 3: "async", 4: "rows", 5: "rows_i8", 6: "mma", 7: "tc"}
+
+
+def traffic_key(workload: str, rows: int, transposed: bool = False, a_int8: bool = False, kernel: int = 1) -> str:
+    """Key of a recorded ncu capture: workload, activation rows (or the
+    transposed layout) and, for batched calls, the kernel that ran."""
     if transposed:
         return f"{workload}_t" + ("8" if a_int8 else "")
-    return workload if rows == 1 else f"{workload}_m{rows}"
+    return workload if rows == 1 else f"{workload}_m{rows}_{KERNEL_NAMES.get(kernel, str(kernel))}"
+
+
+def launches_per_call(info) -> int:
+    """Kernels one call launches: the tcgen05 path splits the activations into
+    bf16 parts first."""
+    return 2 if info.get("kernel") == 7 else 1
 
 
 def recorded_traffic(key: str):
@@ -288,13 +299,14 @@ def run_ours(args, rank, local_rank, world):
     total_bytes = reduce_over_ranks(group, float(bytes_per_call) * args.steps, "sum", dev)
     value = total_bytes / (ms_max * 1e-3) / 1e9 if ms_max > 0 else 0.0
 
-    # roofline of the one kernel each call launches
+    # roofline of the call (for the tcgen05 path: its parts kernel and product kernel)
     per_launch_s = ms * 1e-3 / max(args.steps, 1)
     achieved = bytes_per_call / per_launch_s / 1e9 if per_launch_s > 0 else 0.0
     peak, peak_kind = read_hbm_peak()
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} copy bandwidth",
-                "traffic": recorded_traffic(traffic_key(args.workload, M, args.transposed, args.a_int8)),
+                "traffic": recorded_traffic(traffic_key(args.workload, M, args.transposed, args.a_int8,
+                                                        plan.info["kernel"])),
                 "algorithmic_bytes_per_launch": bytes_per_call}
 
     # end to end through the public binding: pinned host inputs in, result out
@@ -393,7 +405,7 @@ def run_ours(args, rank, local_rank, world):
         "e2e": e2e,
         "plain_launch": plain,
         "clocks": clocks,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_call(plan.info),
         "wall_s_timed_region": round(wall, 4),
     }
 

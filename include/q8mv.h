@@ -198,8 +198,10 @@ q8mv_status_t q8mv_quantize_rows(int64_t M, int64_t K, const float *A, int8_t *q
  * (8, 4 or 1; 8-byte loads exist for up to 4 rows per pass), threads_n,
  * split_k, overlap, and kernel = Q8MV_KERNEL_MMA or Q8MV_KERNEL_TC for the
  * tensor-core kernels (which take split_k and overlap); any other non-zero field gives
- * INVALID_ARG.  Without a kernel named, 16 rows per pass on weights of
- * K * N >= 2^27 use the tensor-core kernel, everything else the register
+ * INVALID_ARG.  Without a kernel named (and without vec_bytes or
+ * threads_n, which tune the register kernel), 16 rows per pass, and 8 rows
+ * per pass on weights of K * N >= 2^27, use the tcgen05 kernel when N % 16
+ * == 0 and W and S are 16-byte aligned; everything else uses the register
  * kernel.
  *
  * Per element the arithmetic is that of q8mv_plan: exact byte conversion,

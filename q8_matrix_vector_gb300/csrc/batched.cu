@@ -449,10 +449,16 @@ cudaError_t query_tc(int *cps) {
     return cudaSuccess;
 }
 
-// Column tiles of 128, passes of 16 rows.  The split balances waves against
-// the workspace: with `cps` CTAs resident per SM, an SM streams one block
-// (4 KiB of weights per CTA) in about kBlockUs * cps, and every K range past
-// the first costs a write and a read of its 16 x N partial rows.
+// Column tiles of 128, passes of 16 rows.  The split balances the SMs' load
+// against the workspace, with costs fitted to split sweeps on GB300 (16 rows;
+// attention 4096 x 4096, FFN 4096 x 11008 and 11008 x 4096, 70B FFN up
+// 8192 x 28672, LM head 4100 x 128256): a CTA alone on its SM takes about
+// kAloneUs per block, an SM holding several CTAs about kSharedUs per block of
+// any of them, a call about kFixedUs, and each K range past the first a
+// write and a read of its 16 x N partial rows plus a share of the last CTA's
+// serial sum; every wave of resident CTAs starts with a set-up of about
+// kStartUs.  Picks: attention split 8, FFN up 3, FFN down 9, 70B FFN up 2,
+// LM head 1 (within 6% of the best measured split).
 q8mv_status_t choose_tc(int64_t M, int64_t K, int64_t N, const Device &dev, int cps, const q8mv_opts_t *o,
                         TcConfig *out) {
     TcConfig c;
@@ -461,13 +467,16 @@ q8mv_status_t choose_tc(int64_t M, int64_t K, int64_t N, const Device &dev, int 
         *out = c;
         return Q8MV_OK;
     }
-    constexpr double kBlockUs = 0.1;    // one block of one CTA with the SM to itself
-    constexpr double kBytesPerUs = 6.0e6;
+    constexpr double kAloneUs = 0.36;
+    constexpr double kSharedUs = 0.25;
+    constexpr double kFixedUs = 9.0;
+    constexpr double kSumUs = 0.6;       // per four K ranges summed by the last CTA
+    constexpr double kStartUs = 2.5;     // per wave of resident CTAs: set-up and the first copies
+    constexpr double kBytesPerUs = 5.0e6;
     const int64_t KB = std::max<int64_t>(1, ceil_div(K, kBlk));
     c.tiles = ceil_div(N, tck::kTileN);
     c.groups = ceil_div(M, tck::kRows);
     c.cps = std::max(1, cps);
-    const int64_t slots = static_cast<int64_t>(dev.sm_count) * c.cps;
     const int want = o ? o->split_k : 0;
     int best = 1;
     double best_us = 0.0;
@@ -477,10 +486,16 @@ q8mv_status_t choose_tc(int64_t M, int64_t K, int64_t N, const Device &dev, int 
         const int64_t split = ceil_div(KB, bps);
         if (split != s && want == 0) continue;  // the same ranges as a smaller split
         const int64_t ctas = c.tiles * c.groups * split;
-        const int64_t waves = ceil_div(ctas, slots);
-        const double per_cta = bps * kBlockUs * std::min<int64_t>(c.cps, ceil_div(ctas, dev.sm_count));
-        const double ws = split > 1 ? 2.0 * split * c.groups * tck::kRows * N * 4 / kBytesPerUs : 0.0;
-        const double us = waves * per_cta + ws;
+        // CTAs per SM: the busiest SM's count while the grid is under three per
+        // SM, the average beyond (CTAs then fill SMs as earlier ones finish)
+        const double avg = static_cast<double>(ctas) / dev.sm_count;
+        const double load = avg < 3.0 ? static_cast<double>(ceil_div(ctas, dev.sm_count)) : avg;
+        const double stream = std::max(bps * kAloneUs, load * bps * kSharedUs);
+        const double ws = split > 1 ? kSumUs * ceil_div(split, 4) +
+                                          2.0 * split * c.groups * tck::kRows * N * 4 / kBytesPerUs
+                                    : 0.0;
+        const double waves = std::ceil(load / c.cps);
+        const double us = kFixedUs + stream + ws + kStartUs * waves;
         if (s == (want > 0 ? top : 1) || us < best_us) {
             best = static_cast<int>(split);
             best_us = us;

@@ -1498,11 +1498,9 @@ q8mv_status_t q8mv_plan_batched(q8mv_plan_t *out, int64_t M, int64_t K, int64_t 
     }
     if (p->bcfg[bk::kNumVec - 1].vec == 0 && N > 0) return fail(Q8MV_ERR_INVALID_ARG);  // needs the fallback
 
-    // tensor-core kernel: on request, and by default for 16 rows per pass on
-    // large weights (K * N >= 2^27), where it measured faster than the
-    // register kernel (70B FFN up, 16 rows: 204 us vs 308 us; LM head 445 vs 532)
-    p->mma = (opts && opts->kernel == Q8MV_KERNEL_MMA) ||
-             ((!opts || opts->kernel == Q8MV_KERNEL_AUTO) && mb == 16 && K * N >= (1LL << 27));
+    // mma.sync tensor-core kernel: on request only (the tcgen05 kernel below
+    // measured faster on every shape)
+    p->mma = opts && opts->kernel == Q8MV_KERNEL_MMA;
     if (p->mma && N > 0 && N % 4 == 0) {
         int mcps = 1;
         int clusters[9];
@@ -1513,8 +1511,15 @@ q8mv_status_t q8mv_plan_batched(q8mv_plan_t *out, int64_t M, int64_t K, int64_t 
         n_tickets = std::max(n_tickets, p->mcfg.n_tickets);
     }
 
-    // tcgen05 kernel: on request
-    p->tc = opts && opts->kernel == Q8MV_KERNEL_TC;
+    // tcgen05 kernel: on request, and by default for 16 rows per pass and for 8
+    // rows on large weights (K * N >= 2^27), where it measured faster than the
+    // register kernel (16 rows: attention 22.6 us vs 23.7, 70B FFN up 107 vs
+    // 315, LM head 214 vs 536; 8 rows: 70B FFN up 106 vs 114, LM head 213 vs 229)
+    // (unless the options tune the register kernel: a load width or threads along N)
+    const bool regs_tuned = opts && (opts->vec_bytes != 0 || opts->threads_n != 0);
+    p->tc = (opts && opts->kernel == Q8MV_KERNEL_TC) ||
+            ((!opts || opts->kernel == Q8MV_KERNEL_AUTO) && !regs_tuned &&
+             (mb == 16 || (mb == 8 && K * N >= (1LL << 27))));
     if (p->tc && N > 0 && N % 16 == 0 && K > 0) {
         int tcps = 1;
         st = cuda_status(bk::query_tc(&tcps));

@@ -645,6 +645,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (n_ok) {
         for (int m = rh * 8; m < min(mrows, rh * 8 + 8); ++m) {
             float v = __ldcg(ws_group + static_cast<int64_t>(m) * p.N + n);
+#pragma unroll 4
             for (int y = 1; y < p.split; ++y) v += __ldcg(ws_group + (static_cast<int64_t>(y) * kRows + m) * p.N + n);
             const int64_t idx = static_cast<int64_t>(m0 + m) * p.N + n;
             p.C[idx] = q8epi::apply(p.epi, v, p.C, idx, n);

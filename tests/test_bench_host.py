@@ -94,7 +94,7 @@ def test_traffic_ignored_when_kernel_changed(tmp_path, monkeypatch):
     rec = {"workloads": {
         "attn": {"dram_bytes_per_launch": 123, "kernel_source": "regs_kernel.cuh",
                  "kernel_source_sha256": "0" * 64},
-        "attn_m4": {"dram_bytes_per_launch": 456, "kernel_source": "batched.cuh",
+        "attn_m4_regs": {"dram_bytes_per_launch": 456, "kernel_source": "batched.cuh",
                     "kernel_source_sha256": bench.kernel_source_hash("batched.cuh")},
         "tiny": {"dram_bytes_per_launch": 789, "kernel_source": "no_such_file.cuh",
                  "kernel_source_sha256": "0" * 64}}}
@@ -102,12 +102,19 @@ def test_traffic_ignored_when_kernel_changed(tmp_path, monkeypatch):
     p.write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(p))
     assert bench.recorded_traffic("attn") is None  # the kernel changed since the capture
-    assert bench.recorded_traffic(bench.traffic_key("attn", 4)) == 456
+    assert bench.recorded_traffic(bench.traffic_key("attn", 4, kernel=1)) == 456
+    assert bench.recorded_traffic(bench.traffic_key("attn", 4, kernel=7)) is None  # another kernel's capture
     assert bench.recorded_traffic("tiny") is None
     assert bench.recorded_traffic("ffn_up") is None
     rec["workloads"]["attn"]["kernel_source_sha256"] = bench.kernel_source_hash("regs_kernel.cuh")
     p.write_text(json.dumps(rec))
     assert bench.recorded_traffic(bench.traffic_key("attn", 1)) == 123
+
+
+def test_tc_calls_count_two_launches():
+    assert bench.launches_per_call({"kernel": 7}) == 2
+    assert bench.launches_per_call({"kernel": 1}) == 1
+    assert bench.traffic_key("up70b", 16, kernel=7) == "up70b_m16_tc"
 
 
 def test_bench_rejects_short_warmup():

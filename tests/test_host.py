@@ -371,3 +371,30 @@ def test_int8_activation_planner_and_quantize_arguments(q8):
     h = ctypes.c_void_p()
     bad = q8.Opts(q8.KERNEL_ROWS_I8, 0, 0, 0, 0, 0, 0, 0)  # the int8 kernel belongs to transposed plans
     assert lib.q8mv_plan(ctypes.byref(h), 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("K,N", [(4096, 4096), (4096, 11008), (11008, 4096), (8192, 28672), (4100, 128256),
+                                 (1, 16), (33, 48), (4100, 1040)])
+@pytest.mark.parametrize("M", [2, 8, 16, 17, 40])
+def test_tc_planner_covers_every_row_column_and_block(q8, M, K, N):
+    """The tcgen05 kernel: 16 rows per pass, 128-column tiles, K ranges that
+    cover every block exactly once, the workspace only for a split."""
+    KB = (K + 31) // 32
+    c = q8.choose_config_batched(M, K, N, 152, 2, 4, kernel=q8.KERNEL_TC)
+    assert c["kernel"] == q8.KERNEL_TC and c["rows_per_pass"] == 16 and c["rows"] == M
+    assert c["threads_per_cta"] == 320 and c["tile_n"] == 128 and c["vec_bytes"] == 16
+    assert c["grid_z"] * 16 >= M and (c["grid_z"] - 1) * 16 < M
+    assert c["grid_x"] * 128 >= N and (c["grid_x"] - 1) * 128 < N
+    assert c["split_k"] * c["blocks_per_split"] >= KB and (c["split_k"] - 1) * c["blocks_per_split"] < KB
+    assert c["workspace_bytes"] == (4 * c["grid_z"] * c["split_k"] * 16 * N if c["split_k"] > 1 else 0)
+
+
+def test_tc_planner_picks_and_limits(q8):
+    """Splits the fitted cost model picks on 152 SMs, and the shapes the kernel
+    cannot take (N % 16 != 0)."""
+    picks = {(4096, 4096): 8, (4096, 11008): 3, (11008, 4096): 9, (8192, 28672): 2, (4100, 128256): 1}
+    for (K, N), split in picks.items():
+        assert q8.choose_config_batched(16, K, N, 152, 2, 4, kernel=q8.KERNEL_TC)["split_k"] == split
+    assert q8.choose_config_batched(16, 4096, 4096, 152, 2, 4, kernel=q8.KERNEL_TC, split_k=5)["split_k"] == 5
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config_batched(16, 4096, 4100, 152, 2, 4, kernel=q8.KERNEL_TC)
