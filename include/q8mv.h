@@ -200,7 +200,7 @@ q8mv_status_t q8mv_quantize_rows(int64_t M, int64_t K, const float *A, int8_t *q
  * tensor-core kernels (which take split_k and overlap); any other non-zero field gives
  * INVALID_ARG.  Without a kernel named (and without vec_bytes or
  * threads_n, which tune the register kernel), 16 rows per pass, and 8 rows
- * per pass on weights of K * N >= 2^27, use the tcgen05 kernel when N % 16
+ * per pass on weights of K * N >= 2^25, use the tcgen05 kernel when N % 16
  * == 0 and W and S are 16-byte aligned; everything else uses the register
  * kernel.
  *

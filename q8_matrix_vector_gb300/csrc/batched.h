@@ -70,7 +70,7 @@ struct MmaConfig {
 
 // The tcgen05 kernel (16 rows per pass, accumulators in tensor memory): its
 // planner's choice, usable == false when the shape cannot use it (N % 16 != 0).
-constexpr int kTcThreads = 320;  // threads per CTA of the tcgen05 kernel
+constexpr int kTcThreads = 448;  // threads per CTA of the tcgen05 kernel
 constexpr int kTcTileN = 128;    // its columns per CTA
 constexpr int kTcRows = 16;      // its activation rows per pass
 

@@ -1512,14 +1512,15 @@ q8mv_status_t q8mv_plan_batched(q8mv_plan_t *out, int64_t M, int64_t K, int64_t 
     }
 
     // tcgen05 kernel: on request, and by default for 16 rows per pass and for 8
-    // rows on large weights (K * N >= 2^27), where it measured faster than the
-    // register kernel (16 rows: attention 22.6 us vs 23.7, 70B FFN up 107 vs
-    // 315, LM head 214 vs 536; 8 rows: 70B FFN up 106 vs 114, LM head 213 vs 229)
+    // rows on weights of K * N >= 2^25, where it measured faster than the
+    // register kernel (16 rows: attention 20.2 us vs 23.6, FFN up 28.9 vs 51.3,
+    // 70B FFN up 100.5 vs 311.5, LM head 196.7 vs 532.6; 8 rows: FFN up 26.0 vs
+    // 27.7, 70B FFN up 97.3 vs 112.9, LM head 195.4 vs 227.9)
     // (unless the options tune the register kernel: a load width or threads along N)
     const bool regs_tuned = opts && (opts->vec_bytes != 0 || opts->threads_n != 0);
     p->tc = (opts && opts->kernel == Q8MV_KERNEL_TC) ||
             ((!opts || opts->kernel == Q8MV_KERNEL_AUTO) && !regs_tuned &&
-             (mb == 16 || (mb == 8 && K * N >= (1LL << 27))));
+             (mb == 16 || (mb == 8 && K * N >= (1LL << 25))));
     if (p->tc && N > 0 && N % 16 == 0 && K > 0) {
         int tcps = 1;
         st = cuda_status(bk::query_tc(&tcps));

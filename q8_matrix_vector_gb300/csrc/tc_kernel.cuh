@@ -23,33 +23,36 @@
 //   * q8mv_tc_parts_kernel splits A into P once, in the shared-memory order
 //     the MMA reads (K-major core matrices of 8 rows x 8 k), 3 KiB per block
 //     of 32 k and pass of 16 rows, zero past M and past K.
-//   * q8mv_tc_kernel: one CTA per (128-column tile, K range, pass), ten
-//     warps with fixed roles, handing work over through mbarriers only:
-//       - the load warp keeps a kStages-deep shared-memory ring filled: per
-//         block, a 2D tensor copy of its 32 x 128 weight bytes (128-byte
-//         swizzle), one of its 128 scales and a bulk copy of its 3 KiB of
-//         activation parts, all completing on the stage's "full" mbarrier
-//         (rows past K and columns past N arrive as zeros); a stage is
-//         refilled once every compute warp has folded its block ("empty");
-//       - eight compute warps convert each block's weight bytes to bf16
-//         exactly (16 bytes a thread) into a tile laid out as MN-major core
-//         matrices (8 k x 8 n) and mark the tile converted ("conv"); kLag
-//         blocks later they wait for the block's MMAs ("done"), read 8 rows
-//         of their TMEM lane (one column n) with tcgen05.ld and fold the
-//         block with S[b, n] from the stage;
-//       - the MMA warp waits for a block's stage and converted tile, issues
-//         two tcgen05.mma (k 0..15, 16..31) of M = 128, N = 48, K = 16 into
-//         the tile's TMEM accumulator slot and commits them to "done".
-//     The bf16 tiles and accumulator slots rotate over kSlots = kLag + 1: a
-//     compute warp rewrites a tile only after folding the block whose MMA
-//     read it, and marks it converted only after that fold's TMEM reads.
+//   * q8mv_tc_kernel: one CTA per (128-column tile, K range, pass), fourteen
+//     warps with fixed roles that hand work over through mbarriers only.  The
+//     blocks go in steps of kPair:
+//       - the load warp keeps a ring of kPairStages steps in shared memory
+//         filled: per block, a 2D tensor copy of its 32 x 128 weight bytes
+//         (128-byte swizzle), one of its 128 scales and a bulk copy of its
+//         3 KiB of activation parts, a step's copies completing on one "full"
+//         mbarrier (rows past K and columns past N arrive as zeros); a stage
+//         is refilled once the fold warps are done with it ("empty");
+//       - eight convert warps turn each block's weight bytes into bf16
+//         exactly (16 bytes a thread) in a tile laid out as MN-major core
+//         matrices (8 k x 8 n), once the MMAs that last read the tile have
+//         completed, and mark the step converted ("conv");
+//       - the MMA warp waits for a step's stages, its converted tiles and the
+//         fold warps' release of its TMEM slot ("tfree"), issues two
+//         tcgen05.mma per block (k 0..15, 16..31) of M = 128, N = 48, K = 16
+//         into the slot and commits them to "done";
+//       - four fold warps, one per TMEM lane quarter, wait for "done", read
+//         their lanes' 48 columns per block with tcgen05.ld (8 rows at a
+//         time) and fold each block with S[b, n] from its stage, then release
+//         the slot and the stages.
+//     Tiles and TMEM slots rotate over kSlots steps.
 //
 // The weights come through the tensor-memory accelerator rather than a
 // register ring of per-thread loads: with loads issued eight blocks ahead
 // into registers, each block still cost a full memory latency (about 1 us per
 // block and CTA, measured on the attention projection).  The roles are split
 // because one thread issuing the MMAs and copies between CTA barriers put
-// about 500 cycles per block on every warp's path (measured with clock
+// about 500 cycles per block on every warp's path, and conversion and fold
+// in the same warps put their latencies in series (both measured with clock
 // stamps).
 //
 // Split-K CTAs of a column tile are summed in range order through the
@@ -72,14 +75,15 @@ constexpr int kRows = 16;               // activation rows per pass
 constexpr int kParts = 3;               // bf16 parts of each activation
 constexpr int kMmaN = kParts * kRows;   // 48: the MMA's N
 constexpr int kTileN = 128;             // weight columns per CTA: the MMA's M, one TMEM lane each
-constexpr int kWarps = 8;              // compute warps; w and w + 4 share TMEM lane quarter w % 4
-constexpr int kMmaWarp = kWarps;        // issues the MMAs (and owns the TMEM allocation)
-constexpr int kLoadWarp = kWarps + 1;   // keeps the shared-memory ring filled
-constexpr int kThreads = (kWarps + 2) * 32;
+constexpr int kConvWarps = 8;          // convert weight bytes to bf16 tiles (warp w: 16 columns)
+constexpr int kFoldWarps = 4;          // fold accumulators with the scales (warp: one TMEM lane quarter)
+constexpr int kMmaWarp = kConvWarps + kFoldWarps;  // issues the MMAs (and owns the TMEM allocation)
+constexpr int kLoadWarp = kMmaWarp + 1;            // keeps the shared-memory ring filled
+constexpr int kThreads = (kLoadWarp + 1) * 32;
 constexpr int kPair = 2;                // blocks per step of the compute and MMA warps
-constexpr int kLag = 1;                 // steps between a step's MMAs and its fold
-constexpr int kSlots = kLag + 1;        // steps of bf16 tiles and TMEM accumulators in flight
+constexpr int kSlots = 2;               // steps of bf16 tiles and TMEM accumulators in flight
 constexpr int kStages = 10;             // shared-memory ring of copied blocks (a multiple of kPair)
+constexpr int kPairStages = kStages / kPair;  // the ring in steps: one full / empty mbarrier each
 constexpr int kBlockCols = 64;          // TMEM columns per block's accumulator (48 used)
 constexpr int kSlotCols = kPair * kBlockCols;
 constexpr uint32_t kTmemCols = 256;     // allocated: a power of two >= kSlots * kSlotCols
@@ -101,7 +105,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 static_assert(kSlots * kSlotCols <= static_cast<int>(kTmemCols), "accumulator slots exceed the allocation");
 static_assert(kWRingOff % 1024 == 0 && kWStageBytes % 1024 == 0, "swizzled stages need 1024-byte alignment");
 static_assert(2 * (kSmemBytes + 2048) <= 228 * 1024, "two CTAs per SM (their TMEM fills the SM's 512 columns)");
-static_assert(kStages % kPair == 0 && kStages >= (kLag + 2) * kPair, "a step's stages share a phase");
+static_assert(kStages % kPair == 0 && kPairStages > kSlots, "a step's stages share an mbarrier");
 static_assert(kSlots == 2, "slot arithmetic below takes two slots");
 
 // error codes recorded in the device error word
@@ -328,31 +332,30 @@ __global__ void __launch_bounds__(256) q8mv_tc_parts_kernel(const float *A, uint
     }
 }
 
-// One thread: fill stage `st` with block b of the CTA's range: weights and
-// scales by tensor copies (before the dependency wait they are inputs no
-// earlier kernel writes), the activation parts by a bulk copy (only after it,
-// when `parts` is set).
+// One thread: copy block b of the CTA's range into stage `st`, completing on
+// `bar`: weights and scales by tensor copies (inputs no earlier kernel
+// writes, so they may be issued before the dependency wait), the activation
+// parts by a bulk copy (only after it).
 __device__ __forceinline__ void issue_inputs(const CUtensorMap *tmW, const CUtensorMap *tmS, uint32_t base,
-                                             uint64_t *full, int st, int64_t tile, int64_t b) {
-    mbar_arrive_expect_tx(full + st, kStageTx);
+                                             uint64_t *bar, int st, int64_t tile, int64_t b) {
     tma_load_2d(base + kWRingOff + st * kWStageBytes, tmW, static_cast<int>(tile * kTileN), static_cast<int>(b * kBlk),
-                full + st);
-    tma_load_2d(base + kSRingOff + st * kSStageBytes, tmS, static_cast<int>(tile * kTileN), static_cast<int>(b),
-                full + st);
+                bar);
+    tma_load_2d(base + kSRingOff + st * kSStageBytes, tmS, static_cast<int>(tile * kTileN), static_cast<int>(b), bar);
 }
-__device__ __forceinline__ void issue_parts(const Params &p, unsigned char *smem_base, uint64_t *full, int st, int z,
+__device__ __forceinline__ void issue_parts(const Params &p, unsigned char *smem_base, uint64_t *bar, int st, int z,
                                             int64_t b) {
     bulk_load(smem_base + kPartsOff + st * kPartBytes, p.P + (static_cast<int64_t>(z) * p.KB + b) * kPartBytes,
-              kPartBytes, full + st);
+              kPartBytes, bar);
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
     q8mv_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS, const Params p) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t s_full[kStages];   // stage landed (copies' transaction count)
-    __shared__ __align__(8) uint64_t s_empty[kStages];  // stage folded by every compute warp
-    __shared__ __align__(8) uint64_t s_conv[kSlots];    // tile converted by every compute warp
-    __shared__ __align__(8) uint64_t s_done[kSlots];    // the tile's MMAs completed
+    __shared__ __align__(8) uint64_t s_full[kPairStages];   // a step's stages landed (copies' transaction count)
+    __shared__ __align__(8) uint64_t s_empty[kPairStages];  // a step's stages folded by every fold warp
+    __shared__ __align__(8) uint64_t s_conv[kSlots];        // a step's tiles converted by every convert warp
+    __shared__ __align__(8) uint64_t s_done[kSlots];        // a step's MMAs completed
+    __shared__ __align__(8) uint64_t s_tfree[kSlots];       // a step's accumulators read by every fold warp
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     __shared__ unsigned s_is_last;
@@ -371,30 +374,36 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int64_t b_begin = static_cast<int64_t>(blockIdx.y) * p.bps;
     const int64_t b_end = b_begin + p.bps < p.KB ? b_begin + p.bps : static_cast<int64_t>(p.KB);
     const int nblocks = b_end > b_begin ? static_cast<int>(b_end - b_begin) : 0;
+    const int nsteps = (nblocks + kPair - 1) / kPair;
+    // blocks in step t (the last step of an odd range has one)
+    auto step_blocks = [&](int t) { return min(kPair, nblocks - kPair * t); };
 
-    // compute warps.  conversion: row k = lane of a block, the 16 columns of
-    // chunk c16 = warp; fold: TMEM lane quarter q (column n of the tile), rows
-    // 8 rh .. 8 rh + 7
-    const int c16 = warp;
-    const int ng = c16 * 2;  // the first of the two core-matrix columns this thread fills
-    const int q = warp & 3, rh = (warp >> 2) & 1;
+    // fold warps: TMEM lane quarter q = column n of the tile, all 16 rows
+    const bool folder = warp >= kConvWarps && warp < kConvWarps + kFoldWarps;
+    const int q = warp & 3;
     const int nl = q * 32 + lane;
     const int64_t n = tile * kTileN + nl;
-    const bool n_ok = warp < kWarps && n < p.N;
+    const bool n_ok = folder && n < p.N;
 
     if (warp == kLoadWarp && lane == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kPairStages; ++s) {
             mbar_init(s_full + s, 1);
-            mbar_init(s_empty + s, kWarps);
+            mbar_init(s_empty + s, kFoldWarps);
         }
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(s_conv + s, kWarps);
+            mbar_init(s_conv + s, kConvWarps);
             mbar_init(s_done + s, 1);
+            mbar_init(s_tfree + s, kFoldWarps);
         }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        for (int i = 0; i < kStages && i < nblocks; ++i) issue_inputs(&tmW, &tmS, base, s_full, i, tile, b_begin + i);
+        for (int t = 0; t < kPairStages && t < nsteps; ++t) {
+            const int nb = step_blocks(t);
+            mbar_arrive_expect_tx(s_full + t, nb * kStageTx);
+            for (int h = 0; h < nb; ++h)
+                issue_inputs(&tmW, &tmS, base, s_full + t, kPair * t + h, tile, b_begin + kPair * t + h);
+        }
     }
     if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
@@ -409,58 +418,62 @@ __global__ void __launch_bounds__(kThreads, 2)
     pdl_launch_dependents();
     pdl_wait();  // the activation parts come from the kernel launched just before
 
-    float2 acc[4];  // compute warps: rows 8 rh + 2 j, 8 rh + 2 j + 1 of column n
+    float2 acc[kRows / 2];  // fold warps: rows 2 j, 2 j + 1 of column n
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.0f, 0.0f);
+    for (int j = 0; j < kRows / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
     bool bad = false;  // warp-uniform
-    int last_issue[kStages];  // load warp: the last block issued into each stage (-1: none)
-    int issued_mma = 0;       // MMA warp: steps whose MMAs were issued
+    int last_issue[kPairStages];  // load warp: the last step issued into each stage pair (-1: none)
+    int issued_mma = 0;           // MMA warp: steps whose MMAs were issued
 
     if (warp == kLoadWarp) {
         if (lane == 0) {
 #pragma unroll
-            for (int s = 0; s < kStages; ++s) last_issue[s] = s < nblocks ? s : -1;
-            for (int i = 0; i < kStages && i < nblocks; ++i) issue_parts(p, smem, s_full, i, z, b_begin + i);
-            // block j into stage j % kStages once the compute warps folded block j - kStages
-            int st = 0;
+            for (int s = 0; s < kPairStages; ++s) last_issue[s] = s < nsteps ? s : -1;
+            for (int t = 0; t < kPairStages && t < nsteps; ++t)
+                for (int h = 0; h < step_blocks(t); ++h)
+                    issue_parts(p, smem, s_full + t, kPair * t + h, z, b_begin + kPair * t + h);
+            // step u into stage pair u % kPairStages once the fold warps folded step u - kPairStages
+            int ps = 0;
             uint32_t ph = 0;
-            for (int j = kStages; j < nblocks; ++j) {
-                if (!mbar_wait(s_empty + st, ph, abort_flag, p.wait_ns)) {
+            for (int u = kPairStages; u < nsteps; ++u) {
+                if (!mbar_wait(s_empty + ps, ph, abort_flag, p.wait_ns)) {
                     bad = true;
                     s_abort = 1;
                     atomicOr(p.err, kErrStageTimeout);
                     break;
                 }
-                issue_inputs(&tmW, &tmS, base, s_full, st, tile, b_begin + j);
-                issue_parts(p, smem, s_full, st, z, b_begin + j);
-                last_issue[st] = j;
-                if (++st == kStages) {
-                    st = 0;
+                const int nb = step_blocks(u);
+                mbar_arrive_expect_tx(s_full + ps, nb * kStageTx);
+                for (int h = 0; h < nb; ++h) {
+                    issue_inputs(&tmW, &tmS, base, s_full + ps, kPair * ps + h, tile, b_begin + kPair * u + h);
+                    issue_parts(p, smem, s_full + ps, kPair * ps + h, z, b_begin + kPair * u + h);
+                }
+                last_issue[ps] = u;
+                if (++ps == kPairStages) {
+                    ps = 0;
                     ph ^= 1u;
                 }
             }
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0) {
-            int st = 0, sl = 0;
-            uint32_t st_ph = 0, sl_ph = 0;
-            const int nsteps = (nblocks + kPair - 1) / kPair;
+            int ps = 0, sl = 0;
+            uint32_t ps_ph = 0, sl_ph = 0;
             for (int t = 0; t < nsteps; ++t) {
-                const bool two = kPair * t + 1 < nblocks;
-                // the step's parts landed, and every compute warp converted its weights
-                // (after folding the step that last used this accumulator slot)
-                if (!mbar_wait(s_full + st, st_ph, abort_flag, p.wait_ns) ||
-                    (two && !mbar_wait(s_full + st + 1, st_ph, abort_flag, p.wait_ns)) ||
-                    !mbar_wait(s_conv + sl, sl_ph, abort_flag, p.wait_ns)) {
+                // the step's parts landed; every convert warp filled its tiles; every fold
+                // warp read the accumulators of the step that last used this slot
+                if (!mbar_wait(s_full + ps, ps_ph, abort_flag, p.wait_ns) ||
+                    !mbar_wait(s_conv + sl, sl_ph, abort_flag, p.wait_ns) ||
+                    (t >= kSlots && !mbar_wait(s_tfree + sl, sl_ph ^ 1u, abort_flag, p.wait_ns))) {
                     bad = true;
                     s_abort = 1;
                     atomicOr(p.err, kErrStageTimeout);
                     break;
                 }
                 tc_fence_after();
-                for (int h = 0; h < (two ? 2 : 1); ++h) {
+                for (int h = 0; h < step_blocks(t); ++h) {
                     const uint32_t a0 = base + kTilesOff + (sl * kPair + h) * kWTileBytes;
-                    const uint32_t b0 = base + kPartsOff + (st + h) * kPartBytes;
+                    const uint32_t b0 = base + kPartsOff + (kPair * ps + h) * kPartBytes;
                     const uint32_t dt = tmem + sl * kSlotCols + h * kBlockCols;
                     mma_bf16(dt, smem_desc(a0, kWCoreK, 128), smem_desc(b0, kPCoreK, 128), 0u);
                     mma_bf16(dt, smem_desc(a0 + 2 * kWCoreK, kWCoreK, 128), smem_desc(b0 + 2 * kPCoreK, kPCoreK, 128),
@@ -468,114 +481,99 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 mma_commit(s_done + sl);
                 issued_mma = t + 1;
-                sl ^= 1;
-                if (sl == 0) sl_ph ^= 1u;
-                st += kPair;
-                if (st == kStages) {
-                    st = 0;
-                    st_ph ^= 1u;
+                if (++sl == kSlots) {
+                    sl = 0;
+                    sl_ph ^= 1u;
+                }
+                if (++ps == kPairStages) {
+                    ps = 0;
+                    ps_ph ^= 1u;
                 }
             }
         }
-    } else {
-        // stage and phase of step t's first block, slot of step t; stage, slot and
-        // phase of the folded step f = t - kLag
-        int st = 0, sl = 0, f_st = 0, f_sl = 0;
-        uint32_t st_ph = 0, f_ph = 0;
-        const int nsteps = (nblocks + kPair - 1) / kPair;
+    } else if (warp < kConvWarps) {
+        // row k = lane of each block, the 16 columns of chunk c16 = warp
+        const int c16 = warp;
         const int k = lane;
-        const int w_off = k * 128 + ((c16 ^ (k & 7)) << 4);                       // in a weight stage
-        const int t_off = (k >> 3) * kWCoreK + (k & 7) * 16 + ng * 128;            // in a bf16 tile
-        for (int t = 0; t < nsteps + kLag && !bad; ++t) {
-            if (t < nsteps) {
-                const bool two = kPair * t + 1 < nblocks;
-                bool waited = mbar_wait(s_full + st, st_ph, abort_flag, p.wait_ns);
-                if (two && waited) waited = mbar_wait(s_full + st + 1, st_ph, abort_flag, p.wait_ns);
-                if (!__all_sync(0xffffffffu, waited)) {
-                    bad = true;
-                    s_abort = 1;
-                    if (lane == 0) atomicOr(p.err, kErrStageTimeout);
-                    break;
-                }
-                // weights of the step's blocks -> bf16 tiles of slot sl (their last reader, the
-                // MMAs of step t - kSlots, was seen complete by this warp at that step's fold)
-                for (int h = 0; h < (two ? 2 : 1); ++h) {
-                    const uint4 w =
-                        *reinterpret_cast<const uint4 *>(smem + kWRingOff + (st + h) * kWStageBytes + w_off);
-                    uint4 lo, hi;
-                    convert16(w, lo, hi);
-                    unsigned char *row = smem + kTilesOff + (sl * kPair + h) * kWTileBytes + t_off;
-                    *reinterpret_cast<uint4 *>(row) = lo;
-                    *reinterpret_cast<uint4 *>(row + 128) = hi;
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_conv + sl);
-                sl ^= 1;
-                st += kPair;
-                if (st == kStages) {
-                    st = 0;
-                    st_ph ^= 1u;
-                }
+        const int w_off = k * 128 + ((c16 ^ (k & 7)) << 4);                     // in a weight stage
+        const int t_off = (k >> 3) * kWCoreK + (k & 7) * 16 + c16 * 2 * 128;     // in a bf16 tile
+        int ps = 0, sl = 0;
+        uint32_t ps_ph = 0, sl_ph = 0;
+        for (int t = 0; t < nsteps; ++t) {
+            // the step's weights landed, and the MMAs that last read this slot's tiles completed
+            bool waited = mbar_wait(s_full + ps, ps_ph, abort_flag, p.wait_ns);
+            if (waited && t >= kSlots) waited = mbar_wait(s_done + sl, sl_ph ^ 1u, abort_flag, p.wait_ns);
+            if (!__all_sync(0xffffffffu, waited)) {
+                bad = true;
+                s_abort = 1;
+                if (lane == 0) atomicOr(p.err, kErrStageTimeout);
+                break;
             }
-            const int f = t - kLag;  // the step folded now
-            if (f >= 0 && f < nsteps) {
-                const bool two = kPair * f + 1 < nblocks;
-                const bool waited = mbar_wait(s_done + f_sl, f_ph, abort_flag, p.wait_ns);
-                if (!__all_sync(0xffffffffu, waited)) {
-                    bad = true;
-                    s_abort = 1;
-                    if (lane == 0) atomicOr(p.err, kErrMmaTimeout);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + f_sl * kSlotCols + rh * 8;
-                const float *sring = reinterpret_cast<const float *>(smem + kSRingOff);
-                float d0[3][8], d1[3][8];
-                tmem_ld8(ta, d0[0]);
-                tmem_ld8(ta + kRows, d0[1]);
-                tmem_ld8(ta + 2 * kRows, d0[2]);
-                const float s0 = sring[f_st * (kSStageBytes / 4) + nl];
-                float s1 = 0.0f;
-                if (two) {
-                    tmem_ld8(ta + kBlockCols, d1[0]);
-                    tmem_ld8(ta + kBlockCols + kRows, d1[1]);
-                    tmem_ld8(ta + kBlockCols + 2 * kRows, d1[2]);
-                    s1 = sring[(f_st + 1) * (kSStageBytes / 4) + nl];
-                }
-                tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {  // the stages' last readers
-                    mbar_arrive(s_empty + f_st);
-                    if (two) mbar_arrive(s_empty + f_st + 1);
-                }
-                const float2 s02 = make_float2(s0, s0);
+            for (int h = 0; h < step_blocks(t); ++h) {
+                const uint4 w =
+                    *reinterpret_cast<const uint4 *>(smem + kWRingOff + (kPair * ps + h) * kWStageBytes + w_off);
+                uint4 lo, hi;
+                convert16(w, lo, hi);
+                unsigned char *row = smem + kTilesOff + (sl * kPair + h) * kWTileBytes + t_off;
+                *reinterpret_cast<uint4 *>(row) = lo;
+                *reinterpret_cast<uint4 *>(row + 128) = hi;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_conv + sl);
+            if (++sl == kSlots) {
+                sl = 0;
+                sl_ph ^= 1u;
+            }
+            if (++ps == kPairStages) {
+                ps = 0;
+                ps_ph ^= 1u;
+            }
+        }
+    } else if (folder) {
+        const float *sring = reinterpret_cast<const float *>(smem + kSRingOff);
+        int ps = 0, sl = 0;
+        uint32_t sl_ph = 0;
+        for (int t = 0; t < nsteps; ++t) {
+            const bool waited = mbar_wait(s_done + sl, sl_ph, abort_flag, p.wait_ns);
+            if (!__all_sync(0xffffffffu, waited)) {
+                bad = true;
+                s_abort = 1;
+                if (lane == 0) atomicOr(p.err, kErrMmaTimeout);
+                break;
+            }
+            tc_fence_after();
+            for (int h = 0; h < step_blocks(t); ++h) {
+                const float sv = sring[(kPair * ps + h) * (kSStageBytes / 4) + nl];
+                const float2 s2 = make_float2(sv, sv);
+                const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + sl * kSlotCols + h * kBlockCols;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 x = __fadd2_rn(__fadd2_rn(make_float2(d0[0][2 * j], d0[0][2 * j + 1]),
-                                                           make_float2(d0[1][2 * j], d0[1][2 * j + 1])),
-                                                make_float2(d0[2][2 * j], d0[2][2 * j + 1]));
-                    acc[j] = __ffma2_rn(x, s02, acc[j]);
-                }
-                if (two) {
-                    const float2 s12 = make_float2(s1, s1);
+                for (int r8 = 0; r8 < 2; ++r8) {  // rows 8 r8 .. 8 r8 + 7
+                    float dh[8], dm[8], dl[8];
+                    tmem_ld8(ta + r8 * 8, dh);
+                    tmem_ld8(ta + kRows + r8 * 8, dm);
+                    tmem_ld8(ta + 2 * kRows + r8 * 8, dl);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const float2 x = __fadd2_rn(__fadd2_rn(make_float2(d1[0][2 * j], d1[0][2 * j + 1]),
-                                                               make_float2(d1[1][2 * j], d1[1][2 * j + 1])),
-                                                    make_float2(d1[2][2 * j], d1[2][2 * j + 1]));
-                        acc[j] = __ffma2_rn(x, s12, acc[j]);
+                        const float2 x = __fadd2_rn(__fadd2_rn(make_float2(dh[2 * j], dh[2 * j + 1]),
+                                                               make_float2(dm[2 * j], dm[2 * j + 1])),
+                                                    make_float2(dl[2 * j], dl[2 * j + 1]));
+                        acc[r8 * 4 + j] = __ffma2_rn(x, s2, acc[r8 * 4 + j]);
                     }
                 }
             }
-            if (f >= 0) {
-                f_st += kPair;
-                if (f_st == kStages) f_st = 0;
-                f_sl ^= 1;
-                if (f_sl == 0) f_ph ^= 1u;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(s_tfree + sl);  // the slot's accumulators are read
+                mbar_arrive(s_empty + ps);  // the step's stages are used up
             }
+            if (++sl == kSlots) {
+                sl = 0;
+                sl_ph ^= 1u;
+            }
+            if (++ps == kPairStages) ps = 0;
         }
     }
 
@@ -584,11 +582,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         bool ok = true;
         if (warp == kMmaWarp && lane == 0 && issued_mma > 0)
             ok = mbar_wait(s_done + (issued_mma - 1) % kSlots, ((issued_mma - 1) / kSlots) & 1, nullptr, p.wait_ns);
-        // (issued_mma counts steps; each step committed once)
         if (warp == kLoadWarp && lane == 0) {
-            for (int s = 0; s < kStages && ok; ++s)
+            for (int s = 0; s < kPairStages && ok; ++s)
                 if (last_issue[s] >= 0)
-                    ok = mbar_wait(s_full + s, (last_issue[s] / kStages) & 1, nullptr, p.wait_ns);
+                    ok = mbar_wait(s_full + s, (last_issue[s] / kPairStages) & 1, nullptr, p.wait_ns);
         }
         if (!ok) atomicOr(p.err, kErrDrainTimeout);
         tc_fence_before();
@@ -605,14 +602,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == kMmaWarp)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 
-    // acc[j] holds rows 8 rh + 2 j, 8 rh + 2 j + 1 of column n
+    // fold warps: acc[j] holds rows 2 j, 2 j + 1 of column n
     if (p.split == 1) {
         if (n_ok) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kRows / 2; ++j) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int m = rh * 8 + 2 * j + h;
+                    const int m = 2 * j + h;
                     if (m < mrows) {
                         const int64_t idx = static_cast<int64_t>(m0 + m) * p.N + n;
                         p.C[idx] = q8epi::apply(p.epi, h ? acc[j].y : acc[j].x, p.C, idx, n);
@@ -628,10 +625,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *ws_row = p.ws + (static_cast<int64_t>(z) * p.split + blockIdx.y) * kRows * p.N;
     if (n_ok) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int m = rh * 8 + 2 * j;
-            if (m < mrows) ws_row[static_cast<int64_t>(m) * p.N + n] = acc[j].x;
-            if (m + 1 < mrows) ws_row[static_cast<int64_t>(m + 1) * p.N + n] = acc[j].y;
+        for (int j = 0; j < kRows / 2; ++j) {
+            if (2 * j < mrows) ws_row[static_cast<int64_t>(2 * j) * p.N + n] = acc[j].x;
+            if (2 * j + 1 < mrows) ws_row[static_cast<int64_t>(2 * j + 1) * p.N + n] = acc[j].y;
         }
     }
     unsigned *ticket = p.tickets + static_cast<int64_t>(z) * gridDim.x + tile;
@@ -642,14 +638,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!s_is_last) return;
     __threadfence();
     const float *ws_group = p.ws + static_cast<int64_t>(z) * p.split * kRows * p.N;
-    if (n_ok) {
-        for (int m = rh * 8; m < min(mrows, rh * 8 + 8); ++m) {
-            float v = __ldcg(ws_group + static_cast<int64_t>(m) * p.N + n);
+    // the sum is spread over every thread: thread i takes outputs i, i + kThreads, ...
+    for (int i = tid; i < mrows * kTileN; i += kThreads) {
+        const int m = i / kTileN;
+        const int64_t nn = tile * kTileN + (i - m * kTileN);
+        if (nn >= p.N) continue;
+        float v = __ldcg(ws_group + static_cast<int64_t>(m) * p.N + nn);
 #pragma unroll 4
-            for (int y = 1; y < p.split; ++y) v += __ldcg(ws_group + (static_cast<int64_t>(y) * kRows + m) * p.N + n);
-            const int64_t idx = static_cast<int64_t>(m0 + m) * p.N + n;
-            p.C[idx] = q8epi::apply(p.epi, v, p.C, idx, n);
-        }
+        for (int y = 1; y < p.split; ++y) v += __ldcg(ws_group + (static_cast<int64_t>(y) * kRows + m) * p.N + nn);
+        const int64_t idx = static_cast<int64_t>(m0 + m) * p.N + nn;
+        p.C[idx] = q8epi::apply(p.epi, v, p.C, idx, nn);
     }
     if (tid == 0) *ticket = 0u;
 }

@@ -382,7 +382,7 @@ def test_tc_planner_covers_every_row_column_and_block(q8, M, K, N):
     KB = (K + 31) // 32
     c = q8.choose_config_batched(M, K, N, 152, 2, 4, kernel=q8.KERNEL_TC)
     assert c["kernel"] == q8.KERNEL_TC and c["rows_per_pass"] == 16 and c["rows"] == M
-    assert c["threads_per_cta"] == 320 and c["tile_n"] == 128 and c["vec_bytes"] == 16
+    assert c["threads_per_cta"] == 448 and c["tile_n"] == 128 and c["vec_bytes"] == 16
     assert c["grid_z"] * 16 >= M and (c["grid_z"] - 1) * 16 < M
     assert c["grid_x"] * 128 >= N and (c["grid_x"] - 1) * 128 < N
     assert c["split_k"] * c["blocks_per_split"] >= KB and (c["split_k"] - 1) * c["blocks_per_split"] < KB
