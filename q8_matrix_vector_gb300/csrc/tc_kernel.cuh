@@ -471,7 +471,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                     break;
                 }
                 tc_fence_after();
-                for (int h = 0; h < step_blocks(t); ++h) {
+                const int nb = step_blocks(t);
+#pragma unroll
+                for (int h = 0; h < kPair; ++h) {
+                    if (h >= nb) break;
                     const uint32_t a0 = base + kTilesOff + (sl * kPair + h) * kWTileBytes;
                     const uint32_t b0 = base + kPartsOff + (kPair * ps + h) * kPartBytes;
                     const uint32_t dt = tmem + sl * kSlotCols + h * kBlockCols;
@@ -509,14 +512,22 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (lane == 0) atomicOr(p.err, kErrStageTimeout);
                 break;
             }
-            for (int h = 0; h < step_blocks(t); ++h) {
-                const uint4 w =
-                    *reinterpret_cast<const uint4 *>(smem + kWRingOff + (kPair * ps + h) * kWStageBytes + w_off);
-                uint4 lo, hi;
-                convert16(w, lo, hi);
-                unsigned char *row = smem + kTilesOff + (sl * kPair + h) * kWTileBytes + t_off;
-                *reinterpret_cast<uint4 *>(row) = lo;
-                *reinterpret_cast<uint4 *>(row + 128) = hi;
+            // both blocks' bytes first, so that their conversions interleave
+            const int nb = step_blocks(t);
+            uint4 w[kPair];
+#pragma unroll
+            for (int h = 0; h < kPair; ++h)
+                if (h < nb)
+                    w[h] = *reinterpret_cast<const uint4 *>(smem + kWRingOff + (kPair * ps + h) * kWStageBytes + w_off);
+#pragma unroll
+            for (int h = 0; h < kPair; ++h) {
+                if (h < nb) {
+                    uint4 lo, hi;
+                    convert16(w[h], lo, hi);
+                    unsigned char *row = smem + kTilesOff + (sl * kPair + h) * kWTileBytes + t_off;
+                    *reinterpret_cast<uint4 *>(row) = lo;
+                    *reinterpret_cast<uint4 *>(row + 128) = hi;
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -543,7 +554,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                 break;
             }
             tc_fence_after();
-            for (int h = 0; h < step_blocks(t); ++h) {
+            const int nb = step_blocks(t);
+#pragma unroll
+            for (int h = 0; h < kPair; ++h) {
+                if (h >= nb) break;
                 const float sv = sring[(kPair * ps + h) * (kSStageBytes / 4) + nl];
                 const float2 s2 = make_float2(sv, sv);
                 const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + sl * kSlotCols + h * kBlockCols;
