@@ -231,15 +231,18 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                  : "memory");
 }
 
-// 8 consecutive 32-bit TMEM columns of this thread's lane
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
-    uint32_t r[8];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr)
-                 : "memory");
+// 16 consecutive 32-bit TMEM columns of this thread's lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -561,20 +564,18 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const float sv = sring[(kPair * ps + h) * (kSStageBytes / 4) + nl];
                 const float2 s2 = make_float2(sv, sv);
                 const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + sl * kSlotCols + h * kBlockCols;
+                // the block's 48 columns of this lane in one round trip
+                float dh[16], dm[16], dl[16];
+                tmem_ld16(ta, dh);
+                tmem_ld16(ta + kRows, dm);
+                tmem_ld16(ta + 2 * kRows, dl);
+                tmem_wait_ld();
 #pragma unroll
-                for (int r8 = 0; r8 < 2; ++r8) {  // rows 8 r8 .. 8 r8 + 7
-                    float dh[8], dm[8], dl[8];
-                    tmem_ld8(ta + r8 * 8, dh);
-                    tmem_ld8(ta + kRows + r8 * 8, dm);
-                    tmem_ld8(ta + 2 * kRows + r8 * 8, dl);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float2 x = __fadd2_rn(__fadd2_rn(make_float2(dh[2 * j], dh[2 * j + 1]),
-                                                               make_float2(dm[2 * j], dm[2 * j + 1])),
-                                                    make_float2(dl[2 * j], dl[2 * j + 1]));
-                        acc[r8 * 4 + j] = __ffma2_rn(x, s2, acc[r8 * 4 + j]);
-                    }
+                for (int j = 0; j < kRows / 2; ++j) {
+                    const float2 x = __fadd2_rn(__fadd2_rn(make_float2(dh[2 * j], dh[2 * j + 1]),
+                                                           make_float2(dm[2 * j], dm[2 * j + 1])),
+                                                make_float2(dl[2 * j], dl[2 * j + 1]));
+                    acc[j] = __ffma2_rn(x, s2, acc[j]);
                 }
             }
             tc_fence_before();
