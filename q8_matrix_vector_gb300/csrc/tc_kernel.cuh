@@ -53,7 +53,9 @@
 // because one thread issuing the MMAs and copies between CTA barriers put
 // about 500 cycles per block on every warp's path, and conversion and fold
 // in the same warps put their latencies in series (both measured with clock
-// stamps).
+// stamps).  The activations are split once per call by their own kernel: a
+// split inside this kernel, where every column tile's CTA repeats it, measured
+// slower (70B FFN up, 16 rows: 162 us against 101 us).
 //
 // Split-K CTAs of a column tile are summed in range order through the
 // workspace by the CTA that takes the tile's last ticket.  Every mbarrier wait

@@ -174,3 +174,18 @@ def test_tc_back_to_back_calls_with_new_activations(q8, orc):
     for a, c in zip(rows, outs):
         ref, bound = orc.batched(a, W, S)
         check_rows(c.cpu().numpy().astype(np.float64), ref, bound, "chain")
+
+
+def test_default_batched_plans_pick_the_tcgen05_kernel_where_measured_faster(q8):
+    """16 rows per pass, and 8 rows on weights of K*N >= 2^25, plan the tcgen05
+    kernel; fewer rows, small weights at 8 rows, register-kernel overrides and
+    shapes it cannot take plan the register kernel."""
+    assert q8.Plan(4096, 4096, rows=16).info["kernel"] == q8.KERNEL_TC
+    assert q8.Plan(4096, 4096, rows=40).info["kernel"] == q8.KERNEL_TC
+    assert q8.Plan(8192, 28672, rows=8).info["kernel"] == q8.KERNEL_TC
+    assert q8.Plan(4096, 11008, rows=8).info["kernel"] == q8.KERNEL_TC
+    assert q8.Plan(4096, 4096, rows=8).info["kernel"] == q8.KERNEL_REGS
+    assert q8.Plan(8192, 28672, rows=4).info["kernel"] == q8.KERNEL_REGS
+    assert q8.Plan(4096, 4096, rows=16, vec_bytes=4).info["kernel"] == q8.KERNEL_REGS
+    assert q8.Plan(4096, 4100, rows=16).info["kernel"] == q8.KERNEL_REGS  # N % 16 != 0
+    assert q8.Plan(4096, 4096, rows=16, kernel=q8.KERNEL_MMA).info["kernel"] == q8.KERNEL_MMA
