@@ -304,7 +304,10 @@ q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t
  * Host-only planning for a batched plan of M rows: the configuration
  * q8mv_plan_batched would pick on a GPU with `sm_count` SMs, where registers
  * allow `ctas_per_sm` resident CTAs of the batched kernel, with weight loads
- * of `vec_bytes` (8, 4 or 1, dividing N).  Fills *info.
+ * of `vec_bytes` (8, 4 or 1, dividing N).  Fills *info.  With opts->kernel ==
+ * Q8MV_KERNEL_TC or Q8MV_KERNEL_MMA it plans that tensor-core kernel instead
+ * (`ctas_per_sm` its resident CTAs, `vec_bytes` ignored); INVALID_ARG when the
+ * shape cannot take it (TC: N % 16 != 0; MMA: N % 4 != 0).
  */
 q8mv_status_t q8mv_choose_config_batched(int64_t M, int64_t K, int64_t N, int32_t sm_count,
                                          int32_t ctas_per_sm, int32_t vec_bytes,
