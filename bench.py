@@ -1,9 +1,9 @@
 #!/usr/bin/env python
 """Throughput benchmark of the Q8_0 decode matvec on GB300.
 
-One step is one call of the whole path, C = matvec(A, W, S), on the 7B-class
-attention projection (K = 4096, N = 4096) unless ``--workload`` says
-otherwise; with ``--rows M`` a step is one batched call of M activation rows
+One step is one call of the whole path, C = matvec(A, W, S), on the LM head
+with a ragged K (K = 4100, N = 128256, the largest decode shape) unless
+``--workload`` says otherwise; with ``--rows M`` a step is one batched call of M activation rows
 against the same weights, with ``--epilogue ACT`` the call also applies the
 fused epilogue C = act(product + bias) + residual as it writes C, and with
 ``--transposed`` the weights are stored one output row per row (Wt [N, K],
@@ -15,8 +15,11 @@ every call streams its weights from HBM.
 Printed (rank 0, one JSON line): effective HBM GB/s over the algorithmic
 bytes K*N + 4*KB*N + 4*K + 4*N per call, microseconds per call, the roofline
 of the kernel against the measured HBM copy bandwidth, the fp64 CPU oracle
-timed on the host cores, an end-to-end figure with host buffers, the SM
-clocks seen during the timed region and the number of kernel launches.
+timed on the host cores (one core, and every core of the affinity mask), an
+end-to-end figure with host buffers, the SM clocks seen during the timed
+region, the number of kernel launches and, under ``per_config``, the same
+timing (microseconds per call, GB/s, fraction of the peak, plan, and the
+oracle on one core) for every decode shape.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload attn]
     python bench.py --impl reference ...   # the CPU oracle as the reference arm
@@ -32,6 +35,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -49,7 +53,10 @@ CSRC = os.path.join(ROOT, "q8_matrix_vector_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 GRAPH_CALLS = 1000  # calls captured per CUDA graph (rounded to the rotation length)
-CPU_BASELINE_SECONDS = 10.0
+CPU_BASELINE_SECONDS = 8.0        # single-thread oracle on the headline workload
+CPU_ALL_CORES_SECONDS = 4.0       # the oracle on every core of the affinity mask
+PER_CONFIG_ORACLE_SECONDS = 0.6   # single-thread oracle sample per config
+PER_CONFIG_TARGET_S = 0.03        # device time of one timed repetition per config
 
 
 # ----------------------------------------------------------------------------
@@ -365,11 +372,18 @@ def run_ours(args, rank, local_rank, world):
                                                 "grid_x", "grid_y")}}
         plan_plain.close()
 
+    table = None
+    if rank == 0 and world == 1 and not args.no_per_config:
+        del bufs, ptrs, epis, launch, g_full, g_rest
+        torch.cuda.empty_cache()
+        have = (args.workload, (A, W, S)) if (M == 1 and not args.transposed) else None
+        table = per_config(q8mv, dev, local_rank, stream, l2, peak, overlap, have)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(A, W, S, bytes_per_call, args.cpu_seconds, wl, M,
                            (bias_h, res_h, EPILOGUE_ACTS[args.epilogue]) if fused else None, args.transposed,
-                           args.a_int8)
+                           args.a_int8, all_core_seconds=args.all_core_seconds)
 
     if rank != 0:
         return None
@@ -407,6 +421,7 @@ def run_ours(args, rank, local_rank, world):
         "clocks": clocks,
         "gpu_launches": args.steps * launches_per_call(plan.info),
         "wall_s_timed_region": round(wall, 4),
+        "per_config": table,
     }
 
 
@@ -460,24 +475,51 @@ def time_calls(plan, ptrs, stream, calls, reps=3, epis=None):
     return best
 
 
-def cpu_baseline(A, W, S, bytes_per_call, seconds, wl, M=1, epilogue=None, transposed=False, a_int8=False):
-    """The fp64 oracle, as it stands, on the host cores: full calls for ~seconds."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
+def affinity_cores():
+    """The cores this process may run on."""
+    if hasattr(os, "sched_getaffinity"):
+        return sorted(os.sched_getaffinity(0))
+    return list(range(os.cpu_count() or 1))
+
+
+def oracle_product(orc, M=1, transposed=False, a_int8=False):
+    """The oracle function of the path being timed: (A, W, S) -> (C, bound)."""
+    if a_int8:
+        return lambda A, W, S: orc.i8(*orc.quantize(A.reshape(-1)), W, S)
+    if transposed:
+        return orc.transposed
+    return orc.factored if M == 1 else orc.batched
+
+
+def cpu_baseline(A, W, S, bytes_per_call, seconds, wl, M=1, epilogue=None, transposed=False, a_int8=False,
+                 all_core_seconds=CPU_ALL_CORES_SECONDS):
+    """The fp64 oracle, as it stands, on the host cores: full calls on one
+    core for ~seconds, then the same workload split by output columns over one
+    process per core of the affinity mask (``cores`` counts those processes)."""
     import oracle
 
     orc = oracle.load()
-    if a_int8:
-        product = lambda: orc.i8(*orc.quantize(A.reshape(-1)), W, S)  # noqa: E731
-    elif transposed:
-        product = lambda: orc.transposed(A, W, S)  # noqa: E731
-    else:
-        product = (lambda: orc.factored(A, W, S)) if M == 1 else (lambda: orc.batched(A, W, S))
+    product = oracle_product(orc, M, transposed, a_int8)
     if epilogue is None:
-        run = product
+        def run():
+            product(A, W, S)
     else:
         bias, residual, act = epilogue
 
         def run():
-            orc.epilogue(product()[0], bias=bias, residual=residual, act=act)
+            orc.epilogue(product(A, W, S)[0], bias=bias, residual=residual, act=act)
     run()  # page in
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -487,9 +529,185 @@ def cpu_baseline(A, W, S, bytes_per_call, seconds, wl, M=1, epilogue=None, trans
         if dt >= seconds:
             break
     rows = "" if M == 1 else f" of M={M} rows"
-    return {"value": round(reps * bytes_per_call / dt / 1e9, 4), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
-            "sample": f"{reps} full {wl.name} calls{rows} (K={wl.K}, N={wl.N}) in {dt:.1f} s, single thread, fp64"}
+    single = {"value": round(reps * bytes_per_call / dt / 1e9, 4), "unit": UNIT, "cores": 1,
+              "sample": f"{reps} full {wl.name} calls{rows} (K={wl.K}, N={wl.N}) in {dt:.1f} s, fp64"}
+    model = cpu_model()
+    multi = None
+    if all_core_seconds > 0 and epilogue is None:
+        try:
+            multi = cpu_all_cores(A, W, S, wl, M, all_core_seconds, transposed, a_int8)
+        except Exception as exc:  # noqa: BLE001  (report, do not lose the run)
+            multi = {"error": f"{type(exc).__name__}: {exc}"}
+    if multi and "value" in multi:
+        return {"value": multi["value"], "unit": UNIT, "cores": multi["cores"], "kind": "oracle",
+                "cpu_model": model,
+                "sample": multi["sample"], "single_thread": single}
+    out = dict(single)
+    out.update({"kind": "oracle", "cpu_model": model})
+    if multi:
+        out["all_cores"] = multi
+    return out
+
+
+def _oracle_chunk_worker(chunk, M, transposed, a_int8, seconds, core, barrier, out_q):
+    """One core's share of the all-core oracle run: the columns in ``chunk``
+    (A, W columns, S columns, bytes per call), repeated for ``seconds`` after
+    every worker is ready."""
+    try:
+        if hasattr(os, "sched_setaffinity"):
+            os.sched_setaffinity(0, {core})
+        import oracle
+
+        A, Wc, Sc, nbytes = chunk
+        product = oracle_product(oracle.load(), M, transposed, a_int8)
+        product(A, Wc, Sc)  # page in
+        barrier.wait(timeout=600)
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            product(A, Wc, Sc)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= seconds:
+                break
+        out_q.put((reps * nbytes, dt, reps))
+    except Exception as exc:  # noqa: BLE001
+        out_q.put(("error", repr(exc), 0))
+        try:
+            barrier.abort()
+        except Exception:  # noqa: BLE001
+            pass
+
+
+def cpu_all_cores(A, W, S, wl, M, seconds, transposed=False, a_int8=False):
+    """The unchanged single-thread oracle in one spawned process per core of
+    the affinity mask, each on its own contiguous range of output columns;
+    throughput = the bytes all processes finished / the longest run."""
+    import multiprocessing as mp
+
+    import numpy as np
+
+    cores = affinity_cores()
+    P = len(cores)
+    N = W.shape[0] if transposed else W.shape[1]
+    K = wl.K
+    KB = wl.KB
+    P = max(1, min(P, N))
+    ctx = mp.get_context("spawn")  # never fork a process that holds a CUDA context
+    barrier = ctx.Barrier(P)
+    out_q = ctx.Queue()
+    procs = []
+    for i in range(P):
+        c0, c1 = N * i // P, N * (i + 1) // P
+        if transposed:
+            Wc, Sc = np.ascontiguousarray(W[c0:c1]), np.ascontiguousarray(S[c0:c1])
+        else:
+            Wc, Sc = np.ascontiguousarray(W[:, c0:c1]), np.ascontiguousarray(S[:, c0:c1])
+        nc = c1 - c0
+        # this process's columns of W, S and C, and its share of A
+        nbytes = K * nc + 4 * KB * nc + 4 * M * nc + 4 * M * K * nc / N
+        proc = ctx.Process(target=_oracle_chunk_worker,
+                           args=((A, Wc, Sc, nbytes), M, transposed, a_int8, seconds, cores[i], barrier, out_q))
+        proc.start()
+        procs.append(proc)
+        del Wc, Sc
+    import queue
+
+    results = []
+    deadline = time.monotonic() + seconds + 600
+    try:
+        while len(results) < P:
+            try:
+                results.append(out_q.get(timeout=1.0))
+            except queue.Empty:
+                dead = [proc for proc in procs if proc.exitcode not in (None, 0)]
+                if dead:
+                    raise RuntimeError(f"oracle worker exited with code {dead[0].exitcode}")
+                if time.monotonic() > deadline:
+                    raise RuntimeError("oracle workers did not finish in time")
+    finally:
+        for proc in procs:
+            proc.join(timeout=60)
+            if proc.is_alive():
+                proc.kill()
+    errors = [r for r in results if r[0] == "error"]
+    if errors:
+        raise RuntimeError(errors[0][1])
+    total = sum(r[0] for r in results)
+    longest = max(r[1] for r in results)
+    calls = sum(r[2] for r in results) / P
+    return {"value": round(total / longest / 1e9, 4), "unit": UNIT, "cores": P,
+            "sample": f"{wl.name} (K={wl.K}, N={wl.N}" + (f", M={M} rows" if M > 1 else "")
+                      + f") split by output columns over {P} processes, one per core, "
+                      f"about {calls:.1f} passes over its columns each in {longest:.1f} s, fp64"}
+
+
+def oracle_sample_gbs(A, W, S, wl, seconds):
+    """The oracle on one core over a column sample of workload ``wl`` for
+    about ``seconds``: (GB/s, columns in the sample)."""
+    import numpy as np
+
+    import oracle
+
+    orc = oracle.load()
+    n_s = wl.N
+    t0 = time.perf_counter()
+    orc.factored(A, np.ascontiguousarray(W[:, :min(n_s, 256)]), np.ascontiguousarray(S[:, :min(n_s, 256)]))
+    t_256 = max(time.perf_counter() - t0, 1e-6)
+    # about a fifth of the budget per call
+    n_s = int(max(16, min(wl.N, 256 * (seconds / 5) / t_256)))
+    Ws, Ss = np.ascontiguousarray(W[:, :n_s]), np.ascontiguousarray(S[:, :n_s])
+    orc.factored(A, Ws, Ss)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        orc.factored(A, Ws, Ss)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return reps * workloads.batched_bytes(wl.K, n_s, 1) / dt / 1e9, n_s
+
+
+def per_config(q8mv, dev, local_rank, stream, l2, peak, overlap, have=None, oracle_seconds=PER_CONFIG_ORACLE_SECONDS):
+    """Every decode shape of ``workloads.ORDER`` with its default plan, timed
+    like the headline (back-to-back graph replays over rotating input copies
+    beyond twice the L2, best of three repetitions), with the oracle on one
+    core over a column sample of the same inputs next to it."""
+    import torch
+
+    table = {}
+    for name in workloads.ORDER:
+        wl = workloads.WORKLOADS[name]
+        if have is not None and have[0] == name:
+            A, W, S = have[1]
+        else:
+            A, W, S = workloads.make_inputs(wl)
+        nbytes = wl.algorithmic_bytes()
+        plan = q8mv.Plan(wl.K, wl.N, device=local_rank, overlap=int(overlap))
+        copies = max(2, math.ceil(2 * l2 / nbytes) + 1)
+        Ah, Wh, Sh = torch.from_numpy(A), torch.from_numpy(W), torch.from_numpy(S)
+        bufs = [(Ah.to(dev), Wh.to(dev), Sh.to(dev), torch.empty((1, wl.N), dtype=torch.float32, device=dev))
+                for _ in range(copies)]
+        ptrs = [(a.data_ptr(), w.data_ptr(), s.data_ptr(), c.data_ptr()) for a, w, s, c in bufs]
+        # about PER_CONFIG_TARGET_S of device time per repetition (launch-bound
+        # shapes counted at 3 us a call)
+        est = max(nbytes / (0.8 * peak * 1e9), 3e-6)
+        calls = int(min(20000, max(200, PER_CONFIG_TARGET_S / est)))
+        us = time_calls(plan, ptrs, stream, calls)
+        info = plan.info
+        plan.close()
+        del bufs, ptrs
+        gbs = nbytes / us / 1e3
+        cpu_gbs, n_s = oracle_sample_gbs(A, W, S, wl, oracle_seconds)
+        table[name] = {
+            "K": wl.K, "N": wl.N, "bytes_per_call": nbytes, "us_per_call": round(us, 3),
+            "gb_s": round(gbs, 1), "frac": round(gbs / peak, 4), "calls_timed": calls,
+            "plan": {k: info[k] for k in ("kernel", "vec_bytes", "threads_per_cta", "threads_n", "split_k",
+                                          "cluster", "grid_x", "grid_y", "stages")},
+            "oracle_1core_gb_s": round(cpu_gbs, 4),
+            "oracle_sample": f"first {n_s} of {wl.N} columns, one core, fp64",
+        }
+        torch.cuda.empty_cache()
+    return table
 
 
 # ----------------------------------------------------------------------------
@@ -563,7 +781,7 @@ def run_reference(args, rank, world):
                                + (", int8 activations (dp4a)" if args.a_int8 else ""),
                    "K": wl.K, "N": wl.N, "KB": wl.KB, "M": M, "epilogue": args.epilogue},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -571,7 +789,7 @@ def run_reference(args, rank, world):
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(workloads.WORKLOADS), default=workloads.HEADLINE)
@@ -588,6 +806,10 @@ def parse_args(argv=None):
     ap.add_argument("--reference-seconds", type=float, default=60.0,
                     help="CPU budget of the reference arm's timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all-core-seconds", type=float, default=CPU_ALL_CORES_SECONDS,
+                    help="seconds of the all-core oracle run in the CPU baseline (0 = single thread only)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-config table (every decode shape with its default plan)")
     ap.add_argument("--kernel", choices=["auto", "regs", "tma", "async", "mma", "tc"], default="auto",
                     help="plan override: kernel family (default: the plan's choice)")
     ap.add_argument("--split", type=int, default=0, help="plan override: K ranges per column tile")

@@ -350,7 +350,11 @@ int q8mv_version(void);
  *     can be refused.
  *   - The first call on each device looks up the scratch array's device
  *     address and the device's SM count and occupancy; make that first call
- *     before any stream capture begins on that device.
+ *     before any stream capture begins on that device.  A first call that
+ *     fails is not remembered: the next call repeats the set-up.  The address
+ *     is kept for the life of the process, so cudaDeviceReset on a device
+ *     after its first call here is not supported (later calls would use the
+ *     old context's address).
  *   - No cudaMalloc, cudaFree or other allocating routine is called.  Each
  *     call clears the counters it uses with cudaMemsetAsync on `stream` before
  *     its kernel, so a call never depends on what an earlier call left behind.

@@ -32,6 +32,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -1705,8 +1706,8 @@ constexpr int kNoallocMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
 
 struct NoallocDevice {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
+    std::mutex lock;                 // serialises the set-up
+    std::atomic<bool> ready{false};  // set-up done and succeeded on this device
     bool supported = false;
     unsigned char *scratch = nullptr;  // device address of g_noalloc_scratch on this device
     int sm_count = 0;
@@ -1718,30 +1719,27 @@ NoallocDevice g_noalloc_devices[kNoallocMaxDevices];
 
 // Set-up for one device (must be current): the scratch address, and the SM
 // count and occupancy the planner needs, queried the same way q8mv_plan does.
-void noalloc_setup(NoallocDevice &d, int device) {
+// Only a set-up that succeeded is kept; after an error the next call tries
+// again, so a transient failure does not disable the entry point for good.
+cudaError_t noalloc_setup(NoallocDevice &d, int device) {
     int major = 0, minor = 0;
     cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device);
-    if (e != cudaSuccess) {
-        d.err = e;
-        return;
-    }
+    if (e != cudaSuccess) return e;
     d.supported = (major == 10 && minor == 3);
-    if (!d.supported) return;
-    void *addr = nullptr;
-    e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
-    if (e != cudaSuccess || addr == nullptr) {
-        d.err = (e != cudaSuccess) ? e : cudaErrorInvalidSymbol;
-        return;
+    if (d.supported) {
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        if (addr == nullptr) return cudaErrorInvalidSymbol;
+        d.scratch = static_cast<unsigned char *>(addr);
+        e = query_occupancy(&d.occ);
+        if (e != cudaSuccess) return e;
+        d.max_cluster = query_max_cluster();
     }
-    d.scratch = static_cast<unsigned char *>(addr);
-    e = query_occupancy(&d.occ);
-    if (e != cudaSuccess) {
-        d.err = e;
-        return;
-    }
-    d.max_cluster = query_max_cluster();
+    d.ready.store(true, std::memory_order_release);
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -1758,8 +1756,13 @@ extern "C" q8mv_status_t q8mv_run_noalloc(int64_t K, int64_t N, const float *A, 
     if (st != Q8MV_OK) return st;
     if (dev < 0 || dev >= kNoallocMaxDevices) return Q8MV_ERR_UNSUPPORTED_DEVICE;
     NoallocDevice &d = g_noalloc_devices[dev];
-    std::call_once(d.once, noalloc_setup, std::ref(d), dev);
-    if (d.err != cudaSuccess) return cuda_status(d.err);
+    if (!d.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> guard(d.lock);
+        if (!d.ready.load(std::memory_order_relaxed)) {
+            st = cuda_status(noalloc_setup(d, dev));
+            if (st != Q8MV_OK) return st;
+        }
+    }
     if (!d.supported) return Q8MV_ERR_UNSUPPORTED_DEVICE;
 
     if (K == 0) return cuda_status(cudaMemsetAsync(C, 0, static_cast<size_t>(N) * sizeof(float), stream));

@@ -120,3 +120,17 @@ def test_tc_calls_count_two_launches():
 def test_bench_rejects_short_warmup():
     with pytest.raises(SystemExit):
         bench.parse_args(["--warmup", "2"])
+
+
+def test_all_core_oracle_baseline_runs_one_process_per_core():
+    import workloads
+
+    wl = workloads.WORKLOADS["tiny"]
+    A, W, S = workloads.make_inputs(wl)
+    rec = bench.cpu_all_cores(A, W, S, wl, 1, 0.2)
+    assert rec["cores"] == min(len(bench.affinity_cores()), wl.N)
+    assert rec["value"] > 0 and rec["unit"] == "GB/s"
+    full = bench.cpu_baseline(A, W, S, wl.algorithmic_bytes(), 0.2, wl, all_core_seconds=0.2)
+    assert full["kind"] == "oracle" and full["cpu_model"]
+    assert full["single_thread"]["cores"] == 1
+    assert full["cores"] == rec["cores"]

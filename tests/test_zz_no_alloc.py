@@ -48,7 +48,32 @@ def run_noalloc(q8, A, W, S, C):
     return q8.library().q8mv_run_noalloc(K, N, A.data_ptr(), W.data_ptr(), S.data_ptr(), C.data_ptr(), stream)
 
 
-@pytest.mark.parametrize("name,w_offset", [("attn", 0), ("tiny", 0), ("lm_head", 0), ("ffn_down", 3)])
+CASES = [("attn", 0), ("tiny", 0), ("lm_head", 0), ("ffn_down", 3)]
+
+
+def chosen_config(q8, K, N, w_offset):
+    """The register-kernel configuration the entry point picks for a W placed
+    w_offset bytes past a 256-byte boundary: a default plan shows it for the
+    widest load such a W allows (a forced width is used whenever W allows it)."""
+    if w_offset % 16 == 0:
+        return q8.Plan(K, N).info
+    widest = max(v for v in (8, 4, 2, 1) if w_offset % v == 0 and N % v == 0)
+    return q8.Plan(K, N, vec_bytes=widest).info
+
+
+def test_some_case_sends_partial_sums_through_the_scratch(q8):
+    # at least one case below must split K without a cluster, so that its
+    # partial sums and arrival counters live in the static array
+    through_scratch = []
+    for name, w_offset in CASES:
+        wl = workloads.WORKLOADS[name]
+        info = chosen_config(q8, wl.K, wl.N, w_offset)
+        if info["split_k"] > 1 and not info["cluster"]:
+            through_scratch.append(name)
+    assert through_scratch, "no case exercises the static split-K scratch"
+
+
+@pytest.mark.parametrize("name,w_offset", CASES)
 def test_noalloc_matches_plan_entry_point_twice(q8, orc, name, w_offset):
     import torch
 
@@ -64,17 +89,20 @@ def test_noalloc_matches_plan_entry_point_twice(q8, orc, name, w_offset):
     plan = q8.Plan(K, N)
     C_plan = plan(Ad, Wd, Sd)
     torch.cuda.synchronize()
-    ref_plan = C_plan.cpu().numpy().reshape(N).astype(np.float64)
-    _, bound = orc.factored(A, W, S)
+    C_plan = C_plan.cpu()
+    ref, bound = orc.factored(A, W, S)
 
-    # two calls in a row share the static scratch; both must match
+    # two calls in a row share the static scratch; both must give the plan's
+    # bits (same kernel, tile, split and summation order) and match the oracle
     for call in range(2):
         C = torch.full((1, N), float("nan"), device=dev)
         st = run_noalloc(q8, Ad, Wd, Sd, C)
         assert st == 0, q8.library().q8mv_status_string(st)
         torch.cuda.synchronize()
-        got = C.cpu().numpy().reshape(N).astype(np.float64)
-        assert_close(got, ref_plan, bound, f"{name} call {call}")
+        C = C.cpu()
+        assert torch.equal(C, C_plan), f"{name} call {call}: differs from q8mv_run's bits"
+        assert_close(C.numpy().reshape(N).astype(np.float64), ref.reshape(N), bound.reshape(N),
+                     f"{name} call {call}")
     plan.close()
 
 
