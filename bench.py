@@ -113,7 +113,7 @@ def kernel_source_hash(name: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()
 
 
-KERNEL_NAMES = {1: "regs", 2: "tma", 3: "async", 4: "rows", 5: "rows_i8", 6: "mma", 7: "tc"}
+KERNEL_NAMES = {1: "regs", 2: "stream", 4: "rows", 5: "rows_i8", 6: "mma", 7: "tc"}
 
 
 def traffic_key(workload: str, rows: int, transposed: bool = False, a_int8: bool = False, kernel: int = 1) -> str:
@@ -230,8 +230,8 @@ def run_ours(args, rank, local_rank, world):
     if args.transposed:
         W, S = np.ascontiguousarray(W.T), np.ascontiguousarray(S.T)
     bias_h, res_h = epilogue_inputs(N, M) if fused else (None, None)
-    kernel = {"auto": q8mv.KERNEL_AUTO, "regs": q8mv.KERNEL_REGS, "tma": q8mv.KERNEL_TMA,
-              "async": q8mv.KERNEL_ASYNC, "mma": q8mv.KERNEL_MMA,
+    kernel = {"auto": q8mv.KERNEL_AUTO, "regs": q8mv.KERNEL_REGS, "stream": q8mv.KERNEL_STREAM,
+              "mma": q8mv.KERNEL_MMA,
               "tc": q8mv.KERNEL_TC}[args.kernel]
     overlap = not args.no_overlap
     plan_opts = dict(kernel=kernel, split_k=args.split, stages=args.stages, threads_n=args.threads_n,
@@ -810,10 +810,10 @@ def parse_args(argv=None):
                     help="seconds of the all-core oracle run in the CPU baseline (0 = single thread only)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per-config table (every decode shape with its default plan)")
-    ap.add_argument("--kernel", choices=["auto", "regs", "tma", "async", "mma", "tc"], default="auto",
+    ap.add_argument("--kernel", choices=["auto", "regs", "stream", "mma", "tc"], default="auto",
                     help="plan override: kernel family (default: the plan's choice)")
     ap.add_argument("--split", type=int, default=0, help="plan override: K ranges per column tile")
-    ap.add_argument("--stages", type=int, default=0, help="plan override: TMA ring depth")
+    ap.add_argument("--stages", type=int, default=0, help="plan override: streaming kernel ring depth")
     ap.add_argument("--threads-n", type=int, default=0, help="plan override: threads along N per CTA")
     ap.add_argument("--cta-threads", type=int, default=0, help="plan override: threads per CTA (128 or 256)")
     ap.add_argument("--no-overlap", action="store_true",

@@ -35,8 +35,11 @@
  *
  * Errors: every call returns a q8mv_status_t.  Arguments are validated on the
  * host before anything is launched; q8mv_run reports launch-time errors only
- * (it does not synchronise).  No kernel in this library waits on a flag, so
- * none can hang.
+ * (it does not synchronise).  The register, rows and batched register kernels
+ * never wait on anything.  The streaming and tcgen05 kernels wait on
+ * shared-memory barriers for their copies and handoffs; every such wait is
+ * bounded (about 2 s), and a wait that runs out is recorded in the plan's
+ * device error word (q8mv_check) instead of hanging the GPU.
  */
 #ifndef Q8MV_H
 #define Q8MV_H
@@ -63,10 +66,12 @@ typedef enum {
 enum {
     Q8MV_KERNEL_AUTO = 0,
     Q8MV_KERNEL_REGS = 1, /* weights streamed through registers with vector loads; any alignment */
-    Q8MV_KERNEL_TMA = 2,  /* weights streamed by the tensor-memory accelerator into a shared-memory
-                             ring; needs N % 16 == 0, N >= 256, K >= 32 and 16-byte aligned A, W, S */
-    Q8MV_KERNEL_ASYNC = 3, /* each thread streams its weight strip through its own shared-memory ring
-                              with asynchronous 16-byte copies; needs N % 16 == 0 and 16-byte aligned W, S */
+    Q8MV_KERNEL_STREAM = 2, /* weights and scales streamed by the tensor-memory accelerator into a
+                               shared-memory ring, one CTA per SM taking at most half of it, so that
+                               the next call's CTAs become resident beside the running call and fill
+                               their rings while it computes (with overlap = 1); split-K summed through
+                               a thread-block cluster.  Needs N % 16 == 0, K <= 65536 and 16-byte
+                               aligned W and S, else the register kernel runs.  (Value 3 is retired.) */
     Q8MV_KERNEL_ROWS = 4,  /* weights stored one output row per row (q8mv_plan_transposed): a CTA owns
                               rows_per_cta outputs, its warps split K, lanes read 16 bytes of a row */
     Q8MV_KERNEL_ROWS_I8 = 5, /* as ROWS, with int8 activations: each 32-element block of A is quantized
@@ -91,15 +96,14 @@ typedef struct {
                           address allows it (narrower loads only as a fallback); 0 lets the
                           planner pick the width it expects to be fastest */
     int32_t threads_n; /* threads along N in one CTA: 32, 64, 128 or 256 */
-    int32_t split_k;   /* K ranges per column tile, each summed by one CTA (>= 1) */
-    int32_t stages;    /* ring depth: TMA kernel a multiple of 8 in 8 .. 32 stages of one block;
-                          async kernel 2, 3, 4 or 6 stages of 8 rows per thread */
+    int32_t split_k;   /* K ranges per column tile, each summed by one CTA (>= 1; the streaming
+                          kernel takes 1 .. 16, the cluster size) */
+    int32_t stages;    /* streaming kernel: ring depth, 1 .. 24 stages of one 32 x 256 block */
     int32_t overlap;   /* 1: launch with programmatic dependent launch, so a call starts while the
                           previous kernel in its stream finishes and reads W and S before that kernel
                           has completed (A is read and C written only after it).  Only for weights
-                          that the preceding work in the stream does not write.  Register and
-                          async kernels. */
-    int32_t cta_threads; /* register and async kernels: 128 or 256 threads per CTA */
+                          that the preceding work in the stream does not write. */
+    int32_t cta_threads; /* register kernel: 128 or 256 threads per CTA */
     int32_t rows_per_cta; /* transposed plans: output rows per CTA, 8 or 16 */
 } q8mv_opts_t;
 
@@ -107,14 +111,14 @@ typedef struct {
  * (the register kernel by default) and, for the register kernel, the weight
  * load width the planner expects to be fastest. */
 typedef struct {
-    int32_t kernel;           /* Q8MV_KERNEL_REGS, _TMA or _ASYNC */
+    int32_t kernel;           /* Q8MV_KERNEL_* the plan runs for 16-byte aligned tensors */
     int32_t vec_bytes;        /* weight bytes per thread per row */
     int32_t threads_n;        /* threads along N per CTA */
     int32_t groups_k;         /* thread groups along K per CTA (threads per CTA / threads_n) */
     int32_t threads_per_cta;
     int32_t split_k;          /* K ranges per column tile (partial rows summed in range order) */
     int32_t blocks_per_split; /* 32-row blocks in each K range */
-    int32_t stages;           /* TMA or async ring depth (0 for the register kernel) */
+    int32_t stages;           /* streaming kernel's ring depth (0 for the register kernel) */
     int32_t overlap;          /* programmatic dependent launch enabled */
     int32_t cluster;          /* split-K partial rows summed through a thread-block cluster's
                                  distributed shared memory (no workspace) */
@@ -262,22 +266,38 @@ typedef struct {
  * q8mv_run with the fused epilogue `epi` (NULL = q8mv_run).  Same rules as
  * q8mv_run; in addition bias and residual are 4-byte aligned device arrays of
  * the plan's device that do not overlap C, and act is one of Q8MV_ACT_*.
- * The register kernel (or, for a batched plan, the batched kernel) runs even
- * when the plan was made for the TMA or async kernel, and also when K == 0
- * (the product is then 0, so C = act(beta * C + bias) + residual).
+ * Every kernel applies the epilogue as it writes C; for K == 0 the register
+ * (or batched register) kernel runs it on a product of 0, so
+ * C = act(beta * C + bias) + residual.
  */
 q8mv_status_t q8mv_run_fused(q8mv_plan_t plan, const float *A, const int8_t *W, const float *S,
                              float *C, const q8mv_epilogue_t *epi, cudaStream_t stream);
 
 /*
  * Synchronise the plan's device and report in *device_error the error bits
- * its kernels recorded since the last check (0 = none; 1 = a weight stage
- * did not arrive in time, 2 = a ring slot was not released in time, 4 = a
- * copy in flight did not land in time).  A kernel that records an error stops
- * waiting and finishes; its output is then undefined.  The bits are cleared,
- * and the plan's split-K counters are reset when any was set.
+ * its kernels recorded since the last check (0 = none).  Streaming kernel:
+ * 1 = a ring stage's copies did not land in time, 2 = a ring stage was not
+ * released in time, 4 = copies in flight did not land in time at the end.
+ * tcgen05 kernel: 8 = a stage or handoff wait ran out, 16 = the MMAs did not
+ * complete in time, 32 = its final wait for copies and MMAs ran out.  A
+ * kernel that records an error stops waiting and finishes; its output is then
+ * undefined.  The bits are cleared, and the plan's split-K counters are reset
+ * when any was set.
  */
 q8mv_status_t q8mv_check(q8mv_plan_t plan, int32_t *device_error);
+
+/*
+ * For tests of the bounded-wait path only.  Sets the bound on every
+ * shared-memory barrier wait of the plan's streaming and tcgen05 kernels to
+ * wait_ns nanoseconds (0 restores the default of 2 s) and makes every ring
+ * stage's barrier expect extra_tx bytes more than its copies deliver (0 in
+ * normal use).  With extra_tx > 0 no stage ever completes, so the kernel's
+ * first wait runs out after wait_ns: it records its error bit (q8mv_check),
+ * stops issuing, waits at most wait_ns for what it issued, releases what it
+ * holds and returns, and the GPU stays usable.  Calls made after restoring
+ * (0, 0) compute normally.  INVALID_ARG for a NULL plan or wait_ns above 10 s.
+ */
+q8mv_status_t q8mv_plan_set_waits(q8mv_plan_t plan, uint64_t wait_ns, uint32_t extra_tx);
 
 /* Release the plan and its workspace.  NULL is accepted.  Synchronises the
  * plan's device first so that no launch still uses the workspace. */
@@ -290,8 +310,9 @@ q8mv_status_t q8mv_plan_info(q8mv_plan_t plan, q8mv_plan_info_t *info);
  * Host-only planning, no GPU needed: the configuration q8mv_plan would pick
  * for K, N on a GPU with `sm_count` SMs.  For the register kernel (opts NULL
  * or kernel REGS/AUTO): `ctas_per_sm` resident CTAs and weight loads of
- * `vec_bytes` (which must divide N).  For opts->kernel == Q8MV_KERNEL_TMA the
- * last two are ignored.  For opts->kernel == Q8MV_KERNEL_ROWS: the transposed
+ * `vec_bytes` (which must divide N).  For opts->kernel == Q8MV_KERNEL_STREAM
+ * the last two are ignored and an SM is taken to hold 228 KiB of shared
+ * memory with 1 KiB reserved per CTA.  For opts->kernel == Q8MV_KERNEL_ROWS: the transposed
  * plan's rows per CTA and warps along K, for `ctas_per_sm` resident CTAs of 16
  * rows and loads of `vec_bytes` (16, 4 or 1).  Fills *info (workspace_bytes of
  * partial rows).

@@ -27,8 +27,7 @@ Q8MV_ERR_CUDA = 4
 
 KERNEL_AUTO = 0
 KERNEL_REGS = 1
-KERNEL_TMA = 2
-KERNEL_ASYNC = 3
+KERNEL_STREAM = 2
 KERNEL_ROWS = 4
 KERNEL_ROWS_I8 = 5
 KERNEL_MMA = 6
@@ -98,6 +97,8 @@ def _load() -> ctypes.CDLL:
     lib.q8mv_run_fused.restype = ctypes.c_int
     lib.q8mv_check.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
     lib.q8mv_check.restype = ctypes.c_int
+    lib.q8mv_plan_set_waits.argtypes = [p, ctypes.c_uint64, ctypes.c_uint32]
+    lib.q8mv_plan_set_waits.restype = ctypes.c_int
     lib.q8mv_destroy.argtypes = [p]
     lib.q8mv_destroy.restype = ctypes.c_int
     lib.q8mv_plan_info.argtypes = [p, ctypes.POINTER(PlanInfo)]
@@ -271,6 +272,14 @@ class Plan:
         if st != Q8MV_OK:
             raise Q8mvError(st, "q8mv_check")
         return word.value
+
+    def set_waits(self, wait_ns: int = 0, extra_tx: int = 0) -> None:
+        """For tests of the bounded-wait path: the bound on each barrier wait of
+        the streaming and tcgen05 kernels (0 = the default) and extra bytes every
+        ring stage's barrier expects (0 = none; > 0 makes the first wait run out)."""
+        st = _lib.q8mv_plan_set_waits(self._h, int(wait_ns), int(extra_tx))
+        if st != Q8MV_OK:
+            raise Q8mvError(st, "q8mv_plan_set_waits")
 
     def close(self) -> None:
         if getattr(self, "_h", None) is not None and self._h.value:

@@ -514,7 +514,8 @@ q8mv_status_t choose_tc(int64_t M, int64_t K, int64_t N, const Device &dev, int 
 
 cudaError_t launch_tc(const TcConfig &c, const float *A, const CUtensorMap *wmap, const CUtensorMap *smap, float *C,
                       float *ws, unsigned *tickets, void *parts, int *err, int64_t M, int64_t K, int64_t N,
-                      const q8epi::Epilogue &epi, cudaStream_t stream, bool overlap) {
+                      const q8epi::Epilogue &epi, cudaStream_t stream, bool overlap, uint64_t wait_ns,
+                      uint32_t extra_tx) {
     const int KB = static_cast<int>(std::max<int64_t>(1, ceil_div(K, kBlk)));
     const int64_t total = c.groups * KB * 64;
     cudaLaunchAttribute pdl;
@@ -543,7 +544,8 @@ cudaError_t launch_tc(const TcConfig &c, const float *A, const CUtensorMap *wmap
     prm.KB = KB;
     prm.split = c.split;
     prm.bps = c.bps;
-    prm.wait_ns = tck::kWaitNs;
+    prm.wait_ns = wait_ns;
+    prm.extra_tx = extra_tx;
     prm.epi = epi;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(c.tiles), static_cast<unsigned>(c.split), static_cast<unsigned>(c.groups));

@@ -93,10 +93,13 @@ cudaError_t query_tc(int *cps);
 
 // Two launches: the activation parts into `parts`, then the product.  wmap:
 // W as a 2D tensor map [K rows][N bytes], box 32 rows x 128 columns, 128-byte
-// swizzle; smap: S [KB rows][N floats], box 1 row x 128 columns.
+// swizzle; smap: S [KB rows][N floats], box 1 row x 128 columns.  wait_ns
+// bounds each barrier wait; extra_tx (0 in normal use) is added to what each
+// ring stage's barrier expects, for tests of the expiry path.
 cudaError_t launch_tc(const TcConfig &c, const float *A, const CUtensorMap *wmap, const CUtensorMap *smap, float *C,
                       float *ws, unsigned *tickets, void *parts, int *err, int64_t M, int64_t K, int64_t N,
-                      const q8epi::Epilogue &epi, cudaStream_t stream, bool overlap);
+                      const q8epi::Epilogue &epi, cudaStream_t stream, bool overlap, uint64_t wait_ns,
+                      uint32_t extra_tx);
 
 q8mv_status_t choose_mma(int64_t M, int64_t K, int64_t N, const Device &dev, int cps, const int *resident_clusters,
                          const q8mv_opts_t *o, MmaConfig *out);

@@ -41,12 +41,11 @@
 #include <mutex>
 #include <new>
 
-#include "async_stream.cuh"
 #include "batched.h"
 #include "mma_kernel.cuh"
 #include "regs_kernel.cuh"
 #include "rows_kernel.cuh"
-#include "tma_stream.cuh"
+#include "stream_kernel.cuh"
 
 namespace {
 
@@ -399,7 +398,7 @@ bool encode_result(int which, CUresult r) {
 bool encode_w(CUtensorMap *m, const int8_t *W, int64_t K, int64_t N) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N)};
-    const cuuint32_t box[2] = {tmak::kUnitN, tmak::kBlk};
+    const cuuint32_t box[2] = {sk::kTileN, sk::kBlk};
     const cuuint32_t elem[2] = {1, 1};
     return encode_result(1, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(W), dims, strides,
                                         box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -410,7 +409,7 @@ bool encode_w(CUtensorMap *m, const int8_t *W, int64_t K, int64_t N) {
 bool encode_s(CUtensorMap *m, const float *S, int64_t KB, int64_t N) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(KB)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
-    const cuuint32_t box[2] = {tmak::kUnitN, 1};
+    const cuuint32_t box[2] = {sk::kTileN, 1};
     const cuuint32_t elem[2] = {1, 1};
     return encode_result(2, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(S), dims, strides,
                                         box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -440,165 +439,98 @@ bool encode_s_tc(CUtensorMap *m, const float *S, int64_t KB, int64_t N) {
                                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
 }
 
-// A as a 1D map [K floats], box 32.
-bool encode_a(CUtensorMap *m, const float *A, int64_t K) {
-    const cuuint64_t dims[1] = {static_cast<cuuint64_t>(K)};
-    const cuuint64_t strides[1] = {0};  // unused for rank 1, but the encoder rejects a null array
-    const cuuint32_t box[1] = {tmak::kBlk};
-    const cuuint32_t elem[1] = {1};
-    return encode_result(3, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, const_cast<float *>(A), dims, strides,
-                                        box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
-}
-
-size_t tma_smem_bytes(int stages) {
-    return static_cast<size_t>(stages) * tmak::kStageBytes + tmak::kRedBytes +
-           2 * tmak::kMaxStages * sizeof(uint64_t);
-}
-
-struct TmaConfig {
-    int64_t tiles = 0;
-    int split = 1;
-    int bps = 1;
-    int64_t items = 0;
-    int grid = 0;
-    int64_t ws_floats = 0;
+// ---------------------------------------------------------------------------
+// Co-resident streaming kernel: planning (pure)
+// ---------------------------------------------------------------------------
+struct StreamConfig {
+    bool usable = false;
+    int64_t tiles = 0;  // 256-column tiles
+    int split = 1;      // K ranges per tile (the cluster size when > 1)
+    int max_len = 0;    // blocks in the longest K range
+    int stages = 0;     // ring depth
+    size_t smem = 0;    // dynamic shared memory per CTA
 };
 
-// Split of each tile's K range for the TMA kernel.  Cost model as for the
-// register kernel: the weight bytes the busiest CTA (one per SM) streams, plus
-// the partial-row traffic of the split spread over all SMs.  Ties go to the
-// smaller split.
-TmaConfig choose_tma(int64_t K, int64_t N, int sm_count, int want_split) {
-    TmaConfig c;
-    const int64_t KB = ceil_div(K, kBlk);
-    c.tiles = ceil_div(N, tmak::kUnitN);
-    const int64_t unit_bytes = static_cast<int64_t>(kBlk) * tmak::kUnitN;
-    int64_t lo = 1, hi = std::min<int64_t>(KB, std::max<int64_t>(1, 16LL * sm_count));
-    if (want_split > 0) lo = hi = std::min<int64_t>(want_split, KB);
-    double best = -1.0;
-    for (int64_t split = lo; split <= hi; ++split) {
-        const int64_t bps = ceil_div(KB, split);
-        const int64_t split_eff = ceil_div(KB, bps);
-        if (split_eff != split && want_split <= 0) continue;
-        const int64_t items = c.tiles * split_eff;
-        const int64_t grid = std::min<int64_t>(sm_count, items);
-        const double per_cta = static_cast<double>(ceil_div(items, grid)) * bps * unit_bytes;
-        const double ws = split_eff > 1 ? 8.0 * split_eff * N / grid : 0.0;
-        const double cost = per_cta + ws;
-        if (best < 0 || cost < best * (1.0 - 1e-9)) {
-            best = cost;
-            c.split = static_cast<int>(split_eff);
-            c.bps = static_cast<int>(bps);
-            c.items = items;
-            c.grid = static_cast<int>(grid);
-            c.ws_floats = split_eff > 1 ? split_eff * N : 0;
-        }
-    }
-    return c;
+size_t stream_smem(int stages, int max_len) {
+    return static_cast<size_t>(sk::kBarBytes) + static_cast<size_t>(stages) * sk::kStageBytes +
+           static_cast<size_t>(max_len) * kBlk * sizeof(float);
 }
 
-}  // namespace
-
-// ---------------------------------------------------------------------------
-// Async-ring kernel: host side
-// ---------------------------------------------------------------------------
-namespace {
-
-
-using AsyncFn = void (*)(asyk::Params);
-
-AsyncFn async_kernel(int depth, int tpb) {
-    if (tpb == 128) {
-        switch (depth) {
-            case 2: return asyk::q8mv_async_kernel<2, 128>;
-            case 3: return asyk::q8mv_async_kernel<3, 128>;
-            case 4: return asyk::q8mv_async_kernel<4, 128>;
-            default: return asyk::q8mv_async_kernel<6, 128>;
-        }
-    }
-    switch (depth) {
-        case 2: return asyk::q8mv_async_kernel<2, 256>;
-        case 3: return asyk::q8mv_async_kernel<3, 256>;
-        case 4: return asyk::q8mv_async_kernel<4, 256>;
-        default: return asyk::q8mv_async_kernel<6, 256>;
-    }
+// Dynamic shared memory one CTA may use so that two fit an SM.
+size_t stream_budget(size_t smem_per_sm, size_t reserved_per_cta, size_t static_per_cta) {
+    const size_t half = smem_per_sm / 2;
+    return half > reserved_per_cta + static_per_cta ? half - reserved_per_cta - static_per_cta : 0;
 }
 
-size_t async_smem(int depth, int tpb) {
-    return static_cast<size_t>(depth) * asyk::kRows * tpb * asyk::kV + asyk::kABytes;
-}
-
-bool valid_async_depth(int d) { return d == 2 || d == 3 || d == 4 || d == 6; }
-
-// CTAs of this footprint that fit on one SM by shared memory (228 KiB, 1 KiB reserved per CTA)
-int async_cps(int depth, int tpb) {
-    return std::max(1, static_cast<int>((228 * 1024) / (async_smem(depth, tpb) + 1024)));
-}
-
-// Same cost model as the register kernel, over CTAs of 128 or 256 threads,
-// tiles of 8 .. 64 strips of 16 columns and ring depths 2 .. 6, with at most
-// kMaxBps blocks per CTA so that the CTA's activations fit in shared memory.
-// The depth is the smallest that keeps a thread's whole block (4 stages), or
-// 6 stages of a longer run, in flight.
-q8mv_status_t choose_async(int64_t K, int64_t N, int sm_count, const q8mv_opts_t *o, Config *out, int *depth_out) {
+// Split and ring depth of the streaming kernel for K, N.  One CTA per SM per
+// call, so that the next call's CTAs fit beside the running ones: the largest
+// split (at most 16, the largest cluster) with tiles * split <= sm_count, and
+// at least enough K ranges that one range's activations fit in 16 KiB.  When
+// `max_clusters` is given (max_clusters[s]: clusters of s CTAs that can be
+// resident at once), a split is taken only if two calls' clusters fit
+// together.  The ring is as deep as `budget` bytes of shared memory allow,
+// and never deeper than the longest range.
+q8mv_status_t choose_stream(int64_t K, int64_t N, int sm_count, size_t budget, const int *max_clusters,
+                            int want_split, int want_stages, StreamConfig *out) {
+    *out = StreamConfig{};
     if (K < 1 || N < 16 || N % 16 != 0 || sm_count <= 0) return Q8MV_ERR_INVALID_ARG;
-    const int want_tn = o ? o->threads_n : 0;
-    const int want_split = o ? o->split_k : 0;
-    const int want_depth = o ? o->stages : 0;
-    const int want_tpb = o ? o->cta_threads : 0;
-    if (want_depth != 0 && !valid_async_depth(want_depth)) return Q8MV_ERR_INVALID_ARG;
     const int64_t KB = ceil_div(K, kBlk);
-    const int64_t strips = N / asyk::kV;
-    Config best;
-    int best_depth = 0;
-    double best_cost = -1.0;
-    for (int tpb = 128; tpb <= 256; tpb *= 2) {
-        if (want_tpb != 0 && tpb != want_tpb) continue;
-        for (int tn = 8; tn <= 64; tn *= 2) {
-            if (want_tn != 0 && tn != want_tn) continue;
-            const int gk = tpb / tn;
-            const int64_t tile_n = static_cast<int64_t>(tn) * asyk::kV;
-            const int64_t tiles = ceil_div(strips, tn);
-            const int64_t min_split = ceil_div(KB, asyk::kMaxBps);
-            int64_t max_split = std::min<int64_t>(std::max<int64_t>(KB, 1), kMaxSplit);
-            max_split = std::min<int64_t>(max_split, std::max<int64_t>(min_split, 16LL * sm_count / tiles));
-            int64_t lo = min_split, hi = max_split;
-            if (want_split != 0) lo = hi = std::max<int64_t>(min_split, std::min<int64_t>(want_split, KB));
-            for (int64_t split = lo; split <= hi; ++split) {
-                const int64_t bps = ceil_div(KB, split);
-                const int64_t split_eff = ceil_div(KB, bps);
-                if (split_eff != split && want_split == 0) continue;
-                if (bps > asyk::kMaxBps) continue;
-                const int64_t blocks_per_thread = ceil_div(bps, gk);
-                const int depth = want_depth ? want_depth : (blocks_per_thread <= 1 ? 4 : 6);
-                const int cps = async_cps(depth, tpb);
-                const int64_t ctas = tiles * split_eff;
-                const int64_t busy = std::min<int64_t>(gk, bps) * blocks_per_thread;
-                const double per_sm = static_cast<double>(ceil_div(ctas, sm_count)) * std::max(bps, busy) * kBlk * tile_n;
-                const double ws = split_eff > 1 ? 8.0 * split_eff * N / sm_count : 0.0;
-                const double waves = static_cast<double>(ceil_div(ctas, static_cast<int64_t>(sm_count) * cps));
-                const double cost = per_sm + ws + 48.0 * 1024 * (waves - 1);
-                if (best_cost < 0 || cost < best_cost * (1.0 - 1e-9)) {
-                    best_cost = cost;
-                    best.vec = asyk::kV;
-                    best.tpb = tpb;
-                    best.tn = tn;
-                    best.gk = gk;
-                    best.split = static_cast<int>(split_eff);
-                    best.bps = static_cast<int>(bps);
-                    best.tiles = tiles;
-                    best.tile_n = tile_n;
-                    best.ws_floats = split_eff > 1 ? split_eff * N : 0;
-                    best_depth = depth;
-                }
-            }
+    StreamConfig c;
+    c.tiles = ceil_div(N, sk::kTileN);
+    const int64_t min_split = std::max<int64_t>(1, ceil_div(KB, sk::kMaxBlocksPerCta));
+    const int64_t max_split = std::min<int64_t>(sk::kMaxSplit, KB);
+    if (min_split > max_split) return Q8MV_ERR_INVALID_ARG;
+    int64_t split = min_split;
+    if (want_split != 0) {
+        if (want_split < min_split || want_split > max_split) return Q8MV_ERR_INVALID_ARG;
+        split = want_split;
+    } else {
+        for (int64_t sp = min_split; sp <= max_split; ++sp) {
+            if (c.tiles * sp > sm_count) break;
+            if (max_clusters != nullptr && sp > 1 && 2 * c.tiles > max_clusters[sp]) continue;
+            split = sp;
         }
     }
-    if (best_cost < 0) return Q8MV_ERR_INVALID_ARG;
-    *out = best;
-    *depth_out = best_depth;
+    c.split = static_cast<int>(split);
+    c.max_len = static_cast<int>(ceil_div(KB, split));
+    const size_t fixed = stream_smem(0, c.max_len);
+    int stages = 0;
+    if (want_stages != 0) {
+        if (want_stages < 1 || want_stages > sk::kMaxStages || stream_smem(want_stages, c.max_len) > budget)
+            return Q8MV_ERR_INVALID_ARG;
+        stages = want_stages;
+    } else {
+        if (fixed + sk::kStageBytes > budget) return Q8MV_ERR_INVALID_ARG;
+        stages = static_cast<int>(std::min<size_t>(sk::kMaxStages, (budget - fixed) / sk::kStageBytes));
+        stages = std::min(stages, c.max_len);
+    }
+    c.stages = stages;
+    c.smem = stream_smem(stages, c.max_len);
+    c.usable = true;
+    *out = c;
     return Q8MV_OK;
+}
+
+void fill_stream_info(const StreamConfig &c, int64_t KB, int sm_count, int64_t ws_bytes, q8mv_plan_info_t *info) {
+    std::memset(info, 0, sizeof(*info));
+    info->kernel = Q8MV_KERNEL_STREAM;
+    info->vec_bytes = sk::kLaneCols;
+    info->threads_n = 32;
+    info->groups_k = sk::kConsumerWarps;
+    info->threads_per_cta = sk::kThreads;
+    info->split_k = c.split;
+    info->blocks_per_split = static_cast<int32_t>(ceil_div(KB, c.split));
+    info->stages = c.stages;
+    info->cluster = c.split > 1 ? 1 : 0;
+    info->tile_n = sk::kTileN;
+    info->grid_x = c.tiles;
+    info->grid_y = c.split;
+    info->workspace_bytes = ws_bytes;
+    info->sm_count = sm_count;
+    info->ctas_per_sm = 2;
+    info->rows = 1;
+    info->rows_per_pass = 1;
+    info->grid_z = 1;
 }
 
 }  // namespace
@@ -686,16 +618,14 @@ struct q8mv_plan_s {
     int max_vec = 16;       // cap from opts
     bool forced_vec = false;  // opts named a width: use the widest legal one up to it
     Config cfg[5];          // register kernel, per weight-load width (16, 8, 4, 2, 1); vec == 0 if unusable
-    // TMA-stream kernel (used when enabled and A, W, S are 16-byte aligned)
-    bool async = false;     // async-ring kernel for 16-byte aligned W and S
     bool overlap = false;   // programmatic dependent launch
-    Config acfg;
-    int adepth = 0;         // async ring depth
-    bool tma = false;
-    TmaConfig tcfg;
-    int tma_stages = 0;
-    size_t tma_smem = 0;
-    MapCache wmaps, smaps, amaps;
+    // co-resident streaming kernel (used when asked for, or chosen, and W and
+    // S are 16-byte aligned)
+    bool stream = false;
+    StreamConfig scfg;
+    MapCache wmaps, smaps;
+    uint64_t wait_ns = sk::kWaitNs;  // bound on each mbarrier wait (streaming and tcgen05 kernels)
+    uint32_t extra_tx = 0;           // bytes a ring barrier expects beyond its copies (tests only)
     // batched plans (q8mv_plan_batched with M >= 2): rows per pass, and one
     // configuration per weight-load width (8, 4, 1 bytes; vec == 0 if unusable)
     int64_t M = 1;
@@ -720,6 +650,51 @@ struct q8mv_plan_s {
     int64_t n_tickets = 0;
     int64_t ws_bytes = 0;
 };
+
+// Plan the streaming kernel on the current device: the shared memory one CTA
+// may use so that two fit an SM, how many clusters of each size can be
+// resident at once, then the split and ring depth.  Sets p->stream when the
+// shape fits.
+static cudaError_t plan_stream(q8mv_plan_s *p, int want_split, int want_stages, int smem_optin) {
+    int smem_per_sm = 0, reserved = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, p->device);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, sk::q8mv_stream_kernel<true>);
+    if (e != cudaSuccess) return e;
+    size_t budget = stream_budget(static_cast<size_t>(smem_per_sm), static_cast<size_t>(reserved), fa.sharedSizeBytes);
+    budget = std::min(budget, static_cast<size_t>(smem_optin));
+    for (auto fn : {sk::q8mv_stream_kernel<true>, sk::q8mv_stream_kernel<false>}) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(budget));
+        if (e != cudaSuccess) return e;
+    }
+    e = cudaFuncSetAttribute(sk::q8mv_stream_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    int max_clusters[sk::kMaxSplit + 1] = {};
+    for (int s = 2; s <= sk::kMaxSplit; ++s) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, static_cast<unsigned>(s));
+        cfg.blockDim = dim3(sk::kThreads);
+        cfg.dynamicSmemBytes = budget;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 1;
+        attr.val.clusterDim.y = static_cast<unsigned>(s);
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, sk::q8mv_stream_kernel<true>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        max_clusters[s] = n;
+    }
+    const q8mv_status_t st =
+        choose_stream(p->K, p->N, p->sm_count, budget, max_clusters, want_split, want_stages, &p->scfg);
+    p->stream = (st == Q8MV_OK);
+    return cudaSuccess;
+}
 
 extern "C" {
 
@@ -754,39 +729,15 @@ q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t
         return Q8MV_OK;
     }
     if (opts && opts->kernel != Q8MV_KERNEL_AUTO && opts->kernel != Q8MV_KERNEL_REGS &&
-        opts->kernel != Q8MV_KERNEL_TMA && opts->kernel != Q8MV_KERNEL_ASYNC)
+        opts->kernel != Q8MV_KERNEL_STREAM)
         return Q8MV_ERR_INVALID_ARG;
-    if (opts && opts->kernel == Q8MV_KERNEL_ASYNC) {
-        Config c;
-        int depth = 0;
-        const q8mv_status_t st = choose_async(K, N, sm_count, opts, &c, &depth);
+    if (opts && opts->kernel == Q8MV_KERNEL_STREAM) {
+        // a GB300-class SM: 228 KiB of shared memory, 1 KiB reserved per CTA
+        StreamConfig c;
+        const q8mv_status_t st = choose_stream(K, N, sm_count, stream_budget(228 * 1024, 1024, 0), nullptr,
+                                               opts->split_k, opts->stages, &c);
         if (st != Q8MV_OK) return st;
-        fill_info(c, sm_count, async_cps(depth, c.tpb), c.ws_floats * static_cast<int64_t>(sizeof(float)), info);
-        info->kernel = Q8MV_KERNEL_ASYNC;
-        info->stages = depth;
-        return Q8MV_OK;
-    }
-    if (opts && opts->kernel == Q8MV_KERNEL_TMA) {
-        if (K < kBlk || N < tmak::kUnitN || N % 16 != 0 || sm_count <= 0 || opts->split_k < 0)
-            return Q8MV_ERR_INVALID_ARG;
-        const TmaConfig t = choose_tma(K, N, sm_count, opts->split_k);
-        std::memset(info, 0, sizeof(*info));
-        info->kernel = Q8MV_KERNEL_TMA;
-        info->vec_bytes = tmak::kLaneCols;
-        info->threads_n = 32;
-        info->groups_k = tmak::kConsumerWarps;
-        info->threads_per_cta = tmak::kThreads;
-        info->split_k = t.split;
-        info->blocks_per_split = t.bps;
-        info->tile_n = tmak::kUnitN;
-        info->grid_x = t.grid;
-        info->grid_y = 1;
-        info->workspace_bytes = t.ws_floats * static_cast<int64_t>(sizeof(float));
-        info->sm_count = sm_count;
-        info->ctas_per_sm = 1;
-        info->rows = 1;
-        info->rows_per_pass = 1;
-        info->grid_z = 1;
+        fill_stream_info(c, ceil_div(K, kBlk), sm_count, 0, info);
         return Q8MV_OK;
     }
     Config c;
@@ -810,8 +761,7 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
     if (N > 0 && K > ((1LL << 62) / N)) return Q8MV_ERR_INVALID_ARG;
     const int want_kernel = opts ? opts->kernel : Q8MV_KERNEL_AUTO;
     if (opts) {
-        if (want_kernel != Q8MV_KERNEL_AUTO && want_kernel != Q8MV_KERNEL_REGS && want_kernel != Q8MV_KERNEL_TMA &&
-            want_kernel != Q8MV_KERNEL_ASYNC)
+        if (want_kernel != Q8MV_KERNEL_AUTO && want_kernel != Q8MV_KERNEL_REGS && want_kernel != Q8MV_KERNEL_STREAM)
             return Q8MV_ERR_INVALID_ARG;
         if (opts->overlap != 0 && opts->overlap != 1) return Q8MV_ERR_INVALID_ARG;
         if (opts->vec_bytes != 0 && !valid_vec(opts->vec_bytes)) return Q8MV_ERR_INVALID_ARG;
@@ -821,21 +771,16 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
         if (opts->cta_threads != 0 && opts->cta_threads != 128 && opts->cta_threads != 256)
             return Q8MV_ERR_INVALID_ARG;
         if (opts->rows_per_cta != 0) return Q8MV_ERR_INVALID_ARG;
-        if (opts->stages != 0) {
-            const bool tma_ok = opts->stages >= tmak::kConsumerWarps && opts->stages <= tmak::kMaxStages &&
-                                opts->stages % tmak::kConsumerWarps == 0;
-            if (want_kernel == Q8MV_KERNEL_TMA && !tma_ok) return Q8MV_ERR_INVALID_ARG;
-            if (want_kernel == Q8MV_KERNEL_ASYNC && !valid_async_depth(opts->stages)) return Q8MV_ERR_INVALID_ARG;
-            if (want_kernel != Q8MV_KERNEL_TMA && want_kernel != Q8MV_KERNEL_ASYNC) return Q8MV_ERR_INVALID_ARG;
-        }
+        if (opts->stages != 0 && (want_kernel != Q8MV_KERNEL_STREAM || opts->stages < 1 ||
+                                  opts->stages > sk::kMaxStages))
+            return Q8MV_ERR_INVALID_ARG;
     }
-    // the TMA kernel needs 16-byte row pitches and whole boxes along each axis
+    // the streaming kernel needs 16-byte row pitches (tensor maps) and at most
+    // 16 K ranges of at most 128 blocks
     const int64_t KBl = ceil_div(K, kBlk);
-    const int64_t tma_tiles = ceil_div(N, tmak::kUnitN);
-    const bool tma_shape = (N % 16 == 0) && N >= tmak::kUnitN && K >= kBlk && (tma_tiles * KBl) < (1LL << 40);
-    if (want_kernel == Q8MV_KERNEL_TMA && !tma_shape) return Q8MV_ERR_INVALID_ARG;
-    const bool async_shape = (N % 16 == 0) && N >= 16 && K >= 1;
-    if (want_kernel == Q8MV_KERNEL_ASYNC && !async_shape) return Q8MV_ERR_INVALID_ARG;
+    const bool stream_shape = (N % 16 == 0) && N >= 16 && K >= 1 &&
+                              ceil_div(KBl, sk::kMaxBlocksPerCta) <= sk::kMaxSplit;
+    if (want_kernel == Q8MV_KERNEL_STREAM && !stream_shape) return Q8MV_ERR_INVALID_ARG;
 
     int prev = 0;
     q8mv_status_t st = cuda_status(cudaGetDevice(&prev));
@@ -893,17 +838,17 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
     // overrides each kernel family understands (the register kernel is also the
     // fallback for unaligned pointers, so it is planned whatever kernel is asked for)
     q8mv_opts_t regs_opts = {};
-    q8mv_opts_t async_opts = {};
     if (opts) {
         regs_opts = *opts;
-        async_opts = *opts;
+        regs_opts.stages = 0;
         if (!valid_tn(opts->threads_n)) regs_opts.threads_n = 0;
-        if (opts->threads_n > 64) async_opts.threads_n = 0;
-        if (want_kernel != Q8MV_KERNEL_REGS && want_kernel != Q8MV_KERNEL_AUTO) regs_opts.threads_n = 0;
+        if (want_kernel != Q8MV_KERNEL_REGS && want_kernel != Q8MV_KERNEL_AUTO) {
+            regs_opts.threads_n = 0;
+            regs_opts.split_k = 0;
+        }
     }
     if (want_kernel == Q8MV_KERNEL_REGS && opts && opts->threads_n != 0 && !valid_tn(opts->threads_n))
         return fail(Q8MV_ERR_INVALID_ARG);
-    if (want_kernel == Q8MV_KERNEL_ASYNC && opts && opts->threads_n > 64) return fail(Q8MV_ERR_INVALID_ARG);
 
     int64_t ws_floats = 0, max_tiles = 0;
     for (int i = 0; i < 5; ++i) {
@@ -918,46 +863,12 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
     }
     if (p->cfg[vec_index(1)].vec == 0 && N > 0) return fail(Q8MV_ERR_INVALID_ARG);  // needs the fallback
 
-    // async-ring kernel, on request (the register kernel measures faster on the decode shapes)
-    if (async_shape && want_kernel == Q8MV_KERNEL_ASYNC) {
-        if (choose_async(K, N, p->sm_count, &async_opts, &p->acfg, &p->adepth) != Q8MV_OK)
-            return fail(Q8MV_ERR_INVALID_ARG);
-        const size_t smem = async_smem(p->adepth, p->acfg.tpb);
-        if (smem + 1024 > static_cast<size_t>(smem_optin)) return fail(Q8MV_ERR_UNSUPPORTED_DEVICE);
-        st = cuda_status(cudaFuncSetAttribute(async_kernel(p->adepth, p->acfg.tpb),
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+    // co-resident streaming kernel
+    if (stream_shape && want_kernel == Q8MV_KERNEL_STREAM) {
+        if (encode_fn() == nullptr) return fail(Q8MV_ERR_UNSUPPORTED_DEVICE);
+        st = cuda_status(plan_stream(p, opts ? opts->split_k : 0, opts ? opts->stages : 0, smem_optin));
         if (st != Q8MV_OK) return fail(st);
-        p->async = true;
-        ws_floats = std::max(ws_floats, p->acfg.ws_floats);
-        if (p->acfg.split > 1) max_tiles = std::max(max_tiles, p->acfg.tiles);
-    }
-
-    // TMA-stream kernel: one persistent CTA per SM, ring as deep as shared memory allows
-    if (tma_shape && want_kernel == Q8MV_KERNEL_TMA && encode_fn() != nullptr) {
-        int stages = opts && opts->stages ? opts->stages : 0;
-        if (stages == 0) {
-            for (int r = tmak::kMaxStages; r >= tmak::kConsumerWarps; r -= tmak::kConsumerWarps) {
-                if (tma_smem_bytes(r) + 1024 <= static_cast<size_t>(smem_optin)) {
-                    stages = r;
-                    break;
-                }
-            }
-        }
-        if (stages != 0 && tma_smem_bytes(stages) + 1024 <= static_cast<size_t>(smem_optin)) {
-            p->tma_stages = stages;
-            p->tma_smem = tma_smem_bytes(stages);
-            p->tcfg = choose_tma(K, N, p->sm_count, opts ? opts->split_k : 0);
-            st = cuda_status(cudaFuncSetAttribute(tmak::q8mv_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  static_cast<int>(p->tma_smem)));
-            if (st != Q8MV_OK) return fail(st);
-            p->tma = true;
-            ws_floats = std::max<int64_t>(ws_floats, p->tcfg.ws_floats);
-            if (p->tcfg.split > 1) max_tiles = std::max(max_tiles, p->tcfg.tiles);
-        } else if (want_kernel == Q8MV_KERNEL_TMA) {
-            return fail(Q8MV_ERR_INVALID_ARG);
-        }
-    } else if (want_kernel == Q8MV_KERNEL_TMA) {
-        return fail(encode_fn() == nullptr ? Q8MV_ERR_UNSUPPORTED_DEVICE : Q8MV_ERR_INVALID_ARG);
+        if (!p->stream) return fail(Q8MV_ERR_INVALID_ARG);
     }
 
     if (ws_floats > 0) {
@@ -1083,31 +994,9 @@ q8mv_status_t q8mv_plan_info(q8mv_plan_t p, q8mv_plan_info_t *info) {
         info->overlap = p->overlap ? 1 : 0;
         return Q8MV_OK;
     }
-    if (p->async) {
-        fill_info(p->acfg, p->sm_count, async_cps(p->adepth, p->acfg.tpb), p->ws_bytes, info);
-        info->kernel = Q8MV_KERNEL_ASYNC;
-        info->stages = p->adepth;
+    if (p->stream) {
+        fill_stream_info(p->scfg, p->KB, p->sm_count, p->ws_bytes, info);
         info->overlap = p->overlap ? 1 : 0;
-        return Q8MV_OK;
-    }
-    if (p->tma) {
-        info->kernel = Q8MV_KERNEL_TMA;
-        info->vec_bytes = tmak::kLaneCols;
-        info->threads_n = 32;
-        info->groups_k = tmak::kConsumerWarps;
-        info->threads_per_cta = tmak::kThreads;
-        info->split_k = p->tcfg.split;
-        info->blocks_per_split = p->tcfg.bps;
-        info->stages = p->tma_stages;
-        info->tile_n = tmak::kUnitN;
-        info->grid_x = p->tcfg.grid;
-        info->grid_y = 1;
-        info->workspace_bytes = p->ws_bytes;
-        info->sm_count = p->sm_count;
-        info->ctas_per_sm = 1;
-        info->rows = 1;
-        info->rows_per_pass = 1;
-        info->grid_z = 1;
         return Q8MV_OK;
     }
     int idx = -1;
@@ -1134,8 +1023,10 @@ static bool overlaps(const void *a, int64_t a_bytes, const void *b, int64_t b_by
     return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
 }
 
-static q8mv_status_t run_tma(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
-                             cudaStream_t stream) {
+// Launch the streaming kernel (W and S 16-byte aligned): one CTA per tile and
+// K range, the ranges of a tile in one cluster.
+static q8mv_status_t run_stream(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
+                                const q8epi::Epilogue &epi, cudaStream_t stream) {
     const CUtensorMap *mw = p->wmaps.find(W);
     if (mw == nullptr) {
         CUtensorMap *m = p->wmaps.slot(W);
@@ -1150,62 +1041,42 @@ static q8mv_status_t run_tma(q8mv_plan_t p, const float *A, const int8_t *W, con
         p->smaps.commit(S);
         ms = m;
     }
-    const CUtensorMap *ma = p->amaps.find(A);
-    if (ma == nullptr) {
-        CUtensorMap *m = p->amaps.slot(A);
-        if (!encode_a(m, A, p->K)) return Q8MV_ERR_CUDA;
-        p->amaps.commit(A);
-        ma = m;
-    }
-    tmak::Params prm;
-    prm.C = C;
-    prm.ws = p->ws;
-    prm.tickets = p->tickets;
-    prm.err = p->err;
-    prm.N = p->N;
-    prm.KB = p->KB;
-    prm.tiles = p->tcfg.tiles;
-    prm.items = p->tcfg.items;
-    prm.split = p->tcfg.split;
-    prm.bps = p->tcfg.bps;
-    prm.grid = p->tcfg.grid;
-    prm.stages = p->tma_stages;
-    prm.wait_ns = tmak::kWaitNs;
-    tmak::q8mv_tma_kernel<<<p->tcfg.grid, tmak::kThreads, p->tma_smem, stream>>>(*mw, *ms, *ma, prm);
-    return cuda_status(cudaGetLastError());
-}
-
-static q8mv_status_t run_async(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
-                               cudaStream_t stream) {
-    const Config &c = p->acfg;
-    asyk::Params prm;
+    const StreamConfig &c = p->scfg;
+    sk::Params prm;
     prm.A = A;
-    prm.W = W;
-    prm.S = S;
     prm.C = C;
-    prm.ws = p->ws;
-    prm.tickets = p->tickets;
+    prm.err = p->err;
     prm.K = p->K;
     prm.N = p->N;
     prm.KB = p->KB;
-    prm.tn = c.tn;
-    prm.tn_log2 = log2_pow2(c.tn);
-    prm.gk = c.gk;
     prm.split = c.split;
-    prm.bps = c.bps;
+    prm.stages = c.stages;
+    prm.extra_tx = p->extra_tx;
+    prm.wait_ns = p->wait_ns;
+    prm.epi = epi;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(c.tiles), static_cast<unsigned>(c.split));
-    cfg.blockDim = dim3(static_cast<unsigned>(c.tpb));
-    cfg.dynamicSmemBytes = async_smem(p->adepth, c.tpb);
+    cfg.blockDim = dim3(sk::kThreads);
+    cfg.dynamicSmemBytes = c.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned n_attr = 0;
     if (p->overlap) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attr;
     }
-    return cuda_status(cudaLaunchKernelEx(&cfg, async_kernel(p->adepth, c.tpb), prm));
+    if (c.split > 1) {
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = 1;
+        attr[n_attr].val.clusterDim.y = static_cast<unsigned>(c.split);
+        attr[n_attr].val.clusterDim.z = 1;
+        ++n_attr;
+    }
+    cfg.attrs = n_attr ? attr : nullptr;
+    cfg.numAttrs = n_attr;
+    if (c.split > 1) return cuda_status(cudaLaunchKernelEx(&cfg, sk::q8mv_stream_kernel<true>, *mw, *ms, prm));
+    return cuda_status(cudaLaunchKernelEx(&cfg, sk::q8mv_stream_kernel<false>, *mw, *ms, prm));
 }
 
 static q8mv_status_t run_batched(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
@@ -1227,7 +1098,7 @@ static q8mv_status_t run_batched(q8mv_plan_t p, const float *A, const int8_t *W,
             ms = m;
         }
         return cuda_status(bk::launch_tc(p->tcc, A, mw, ms, C, p->ws, p->tickets, p->parts, p->err, p->M, p->K,
-                                         p->N, epi, stream, p->overlap));
+                                         p->N, epi, stream, p->overlap, p->wait_ns, p->extra_tx));
     }
     if (p->mma && p->mcfg.usable && reinterpret_cast<uintptr_t>(W) % 4 == 0)
         return cuda_status(bk::launch_mma(p->mcfg, A, W, S, C, p->ws, p->tickets, p->M, p->K, p->N, epi, stream,
@@ -1296,10 +1167,7 @@ static q8mv_status_t run_impl(q8mv_plan_t p, const float *A, const int8_t *W, co
 
     const uintptr_t waddr = reinterpret_cast<uintptr_t>(W);
     const uintptr_t saddr = reinterpret_cast<uintptr_t>(S);
-    const uintptr_t aaddr = reinterpret_cast<uintptr_t>(A);
-    if (!epi.on && p->async && waddr % 16 == 0 && saddr % 16 == 0) return run_async(p, A, W, S, C, stream);
-    if (!epi.on && p->tma && waddr % 16 == 0 && saddr % 16 == 0 && aaddr % 16 == 0)
-        return run_tma(p, A, W, S, C, stream);
+    if (p->stream && K > 0 && waddr % 16 == 0 && saddr % 16 == 0) return run_stream(p, A, W, S, C, epi, stream);
 
     // register kernel: of the weight-load widths that N, W's address and the
     // plan's cap allow, the one the planner expects to be fastest
@@ -1380,6 +1248,13 @@ q8mv_status_t q8mv_check(q8mv_plan_t p, int32_t *device_error) {
     *device_error = word;
     if (prev != p->device) cudaSetDevice(prev);
     return st;
+}
+
+q8mv_status_t q8mv_plan_set_waits(q8mv_plan_t p, uint64_t wait_ns, uint32_t extra_tx) {
+    if (p == nullptr || wait_ns > 10000000000ull) return Q8MV_ERR_INVALID_ARG;
+    p->wait_ns = wait_ns == 0 ? sk::kWaitNs : wait_ns;
+    p->extra_tx = extra_tx;
+    return Q8MV_OK;
 }
 
 q8mv_status_t q8mv_destroy(q8mv_plan_t p) {

@@ -1,0 +1,355 @@
+// q8mv co-resident streaming kernel (sm_103a): the Q8_0 matvec with the
+// weights brought into a shared-memory ring by the tensor-memory accelerator,
+// sized so that two consecutive calls share every SM.
+//
+//   C[0, n] = sum_b S[b, n] * ( sum_{k in block b} A[0, k] * W[k, n] )
+//
+// (Phobos docs, "Q8_0 matvec" example page: "The tensors", "Factoring out the
+// scale", "Line by line", "Bounds".)
+//
+// Why this shape.  In a decode chain every call reads the previous call's
+// output as its activations, so no call can multiply before the previous one
+// has finished; only its weight stream can start early.  A call of this
+// kernel occupies at most half of each SM (one CTA per SM, at most half the
+// shared memory and registers), so under programmatic dependent launch the
+// next call's CTAs become resident right away, alongside the running call,
+// and fill their rings with weights and scales while the running call
+// computes.  When the running call completes, the next call's weights are
+// already on chip; it stages its activations and multiplies.
+//
+// Work: CTA (t, q) owns the 256-column tile t (one TMA box wide) and the
+// contiguous block range [q*KB/split, (q+1)*KB/split) of its K.
+//   * One producer thread issues, per block, two 2D tensor copies into the
+//     next ring stage: W[32b .. 32b+32, 256t .. +256) (8 KiB) and
+//     S[b, 256t .. +256) (1 KiB), completing on the stage's "full" mbarrier.
+//     Rows at or past K and columns at or past N lie outside the tensor maps
+//     and arrive as zeros without being read.  The first ring's worth is
+//     issued before anything else; a stage is refilled once its consumer
+//     has released it ("empty").
+//   * Eight consumer warps wait for the previous grid (griddepcontrol.wait),
+//     stage the CTA's activations in shared memory (zeros past K) and take the
+//     blocks round-robin: warp w handles blocks w, w+8, ...  Lane l owns
+//     columns 8l .. 8l+7: it reads each of the block's 32 rows with one
+//     8-byte shared load, converts the bytes to f32 exactly, accumulates the
+//     block's sum in row order with packed f32x2 FMAs and folds the block's
+//     scale once per column into its accumulator.
+//   * At the end the warps' accumulators are summed in warp order through
+//     shared memory.  With split > 1 the tile's CTAs form one thread-block
+//     cluster: after a cluster barrier CTA r sums slice r of the columns over
+//     the cluster's CTAs in rank order through distributed shared memory, and
+//     writes C (with the fused epilogue, if any).  Every sum has an order
+//     fixed by the plan.
+//   * Every mbarrier wait is bounded (wait_ns of %globaltimer).  On expiry
+//     the CTA records an error bit in a device word, stops issuing and
+//     consuming, waits (bounded) for the copies it issued to land, and still
+//     takes part in both cluster barriers, so no CTA of the cluster waits for
+//     one that left.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda.h>
+#include <cstdint>
+
+#include "epilogue.cuh"
+
+namespace sk {
+
+constexpr int kBlk = 32;
+constexpr int kTileN = 256;                          // columns per CTA: one TMA box
+constexpr int kLaneCols = kTileN / 32;               // 8 columns per consumer lane
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;      // + one producer warp
+constexpr int kWBytes = kBlk * kTileN;               // 8192
+constexpr int kSBytes = kTileN * 4;                  // 1024
+constexpr int kStageBytes = kWBytes + kSBytes;       // 9216, a multiple of 128
+constexpr int kMaxStages = 24;
+constexpr int kBarBytes = 1024;                      // mbarriers, ahead of the ring
+constexpr int kMaxBlocksPerCta = 128;                // the CTA's activations, staged whole: <= 16 KiB
+constexpr int kMaxSplit = 16;                        // largest cluster (non-portable size)
+constexpr uint64_t kWaitNs = 2000000000ull;          // bound on any single wait
+
+// error bits recorded in the device error word
+constexpr int kErrFullTimeout = 1;   // a stage's copies did not land in time
+constexpr int kErrEmptyTimeout = 2;  // a stage was not released in time
+constexpr int kErrDrainTimeout = 4;  // copies in flight did not land in time at the end
+
+static_assert(kStageBytes % 128 == 0, "stages keep the 128-byte alignment of tensor copies");
+constexpr int kAbortOff = 2 * kMaxStages * 8;        // the CTA's abort word, after the mbarriers
+static_assert(kAbortOff + 4 <= kBarBytes, "mbarriers and the abort word fit their area");
+static_assert(kConsumerWarps * kTileN * 4 + kTileN * 4 <= kStageBytes, "the reduction fits the first stage");
+
+struct Params {
+    const float *A;
+    float *C;
+    int *err;           // device error word (0 = ok)
+    int64_t K, N;
+    int KB;
+    int split;          // K ranges per tile = cluster size along y
+    int stages;         // ring depth
+    uint32_t extra_tx;  // bytes a stage's barrier expects beyond its copies (0; tests of the expiry path only)
+    uint64_t wait_ns;   // bound on a single wait
+    q8epi::Epilogue epi;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase of the given parity.  False when the CTA is aborting
+// (abort_flag set, if given) or wait_ns of %globaltimer pass first.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort_flag,
+                                          uint64_t wait_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15u) == 0) {
+            if (abort_flag != nullptr && *abort_flag) return false;
+            if (global_ns() - t0 > wait_ns) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// barrier among the consumer warps only (the producer warp does not take part)
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+
+// Two signed bytes of `flipped` (selectors lo, hi) -> f32 exactly: the byte,
+// sign bit flipped, becomes the low mantissa byte of 2^23 (2^23 + u with u in
+// 0 .. 255), and 2^23 + 128 is subtracted.
+__device__ __forceinline__ float2 cvt2(uint32_t flipped, uint32_t sel_lo, uint32_t sel_hi) {
+    const float2 t = make_float2(__uint_as_float(__byte_perm(flipped, 0x4B000000u, sel_lo)),
+                                 __uint_as_float(__byte_perm(flipped, 0x4B000000u, sel_hi)));
+    return __fadd2_rn(t, make_float2(-8388736.0f, -8388736.0f));
+}
+
+// part[0..8) += a * (8 signed bytes in w)
+__device__ __forceinline__ void fma_row8(float a, uint2 w, float2 (&part)[4]) {
+    const float2 a2 = make_float2(a, a);
+    const uint32_t u0 = w.x ^ 0x80808080u;
+    const uint32_t u1 = w.y ^ 0x80808080u;
+    part[0] = __ffma2_rn(a2, cvt2(u0, 0x7440u, 0x7441u), part[0]);
+    part[1] = __ffma2_rn(a2, cvt2(u0, 0x7442u, 0x7443u), part[1]);
+    part[2] = __ffma2_rn(a2, cvt2(u1, 0x7440u, 0x7441u), part[2]);
+    part[3] = __ffma2_rn(a2, cvt2(u1, 0x7442u, 0x7443u), part[3]);
+}
+
+// Shared memory: [mbarriers: full[R], empty[R]; abort word] [ring: R stages of W, S]
+// [activations: the CTA's blocks, 128 bytes each].  The reduction at the end
+// reuses the first stage.
+template <bool CLUSTER>
+__global__ void __launch_bounds__(kThreads, 2)
+    q8mv_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
+                       const Params p) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int R = p.stages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + kMaxStages;
+    volatile int &s_abort = *reinterpret_cast<int *>(smem + kAbortOff);  // set by a role that gave up
+    unsigned char *ring = smem + kBarBytes;
+    float *a_s = reinterpret_cast<float *>(ring + static_cast<size_t>(R) * kStageBytes);
+    const volatile int *abort_flag = &s_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t t = blockIdx.x;
+    const int q = static_cast<int>(blockIdx.y);
+    const int b0 = static_cast<int>(static_cast<int64_t>(q) * p.KB / p.split);
+    const int b1 = static_cast<int>(static_cast<int64_t>(q + 1) * p.KB / p.split);
+    const int len = b1 - b0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < R; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // the next call may become resident now: it only reads its own weights
+    // before its own griddepcontrol.wait
+    pdl_launch_dependents();
+
+    float2 acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.0f, 0.0f);
+
+    if (warp == kConsumerWarps) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            prefetch_tensormap(&tmW);
+            prefetch_tensormap(&tmS);
+            const int x = static_cast<int>(t * kTileN);
+            int issued = 0;
+            int s = 0;
+            uint32_t use = 0;  // how many times stage s has been filled before
+            for (int j = 0; j < len; ++j) {
+                if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1u, abort_flag, p.wait_ns)) {
+                    if (!*abort_flag) atomicOr(p.err, kErrEmptyTimeout);
+                    s_abort = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
+                mbar_arrive_expect_tx(full + s, kStageBytes + p.extra_tx);
+                tma_load_2d(st, &tmW, x, (b0 + j) * kBlk, full + s);
+                tma_load_2d(st + kWBytes, &tmS, x, b0 + j, full + s);
+                ++issued;
+                if (++s == R) {
+                    s = 0;
+                    ++use;
+                }
+            }
+            // every copy this CTA issued lands before the CTA can finish
+            for (int j = (issued > R ? issued - R : 0); j < issued; ++j) {
+                if (!mbar_wait(full + (j % R), static_cast<uint32_t>(j / R) & 1u, nullptr, p.wait_ns)) {
+                    atomicOr(p.err, kErrDrainTimeout);
+                    break;
+                }
+            }
+        }
+    } else {
+        // -------------------------------------------------------- consumers
+        pdl_wait();
+        const int64_t k0 = static_cast<int64_t>(b0) * kBlk;
+        const int nk = len * kBlk;
+        for (int i = threadIdx.x; i < nk; i += kConsumerThreads)
+            a_s[i] = (k0 + i < p.K) ? __ldg(p.A + k0 + i) : 0.0f;
+        consumers_sync();
+
+        int s = warp;
+        uint32_t use = 0;
+        while (s >= R) {
+            s -= R;
+            ++use;
+        }
+        for (int j = warp; j < len; j += kConsumerWarps) {
+            if (*abort_flag || !mbar_wait(full + s, use & 1u, abort_flag, p.wait_ns)) {
+                if (!*abort_flag && lane == 0) atomicOr(p.err, kErrFullTimeout);
+                s_abort = 1;
+                break;
+            }
+            const unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
+            const uint2 *wl = reinterpret_cast<const uint2 *>(st) + lane;
+            const float4 *a4p = reinterpret_cast<const float4 *>(a_s + j * kBlk);
+            float2 part[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) part[c] = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int r = 0; r < kBlk; r += 4) {
+                const float4 a4 = a4p[r / 4];
+                fma_row8(a4.x, wl[(r + 0) * 32], part);
+                fma_row8(a4.y, wl[(r + 1) * 32], part);
+                fma_row8(a4.z, wl[(r + 2) * 32], part);
+                fma_row8(a4.w, wl[(r + 3) * 32], part);
+            }
+            const float4 *sl = reinterpret_cast<const float4 *>(st + kWBytes) + 2 * lane;
+            const float4 s0 = sl[0], s1 = sl[1];
+            acc[0] = __ffma2_rn(part[0], make_float2(s0.x, s0.y), acc[0]);
+            acc[1] = __ffma2_rn(part[1], make_float2(s0.z, s0.w), acc[1]);
+            acc[2] = __ffma2_rn(part[2], make_float2(s1.x, s1.y), acc[2]);
+            acc[3] = __ffma2_rn(part[3], make_float2(s1.z, s1.w), acc[3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + s);  // the stage may be refilled
+            s += kConsumerWarps;
+            while (s >= R) {
+                s -= R;
+                ++use;
+            }
+        }
+    }
+
+    // ---- sum the warps' accumulators in warp order (the first stage is free:
+    // every copy has landed and every stage has been consumed or abandoned)
+    __syncthreads();
+    float *red = reinterpret_cast<float *>(ring);  // [kConsumerWarps][kTileN]
+    if (warp < kConsumerWarps) {
+        float4 *mine = reinterpret_cast<float4 *>(red + warp * kTileN + lane * kLaneCols);
+        mine[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+        mine[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+    }
+    __syncthreads();
+    const int ct = threadIdx.x;  // column of the tile this thread sums (ct < kTileN)
+    float v = 0.0f;
+    if (ct < kTileN) {
+        v = red[ct];
+#pragma unroll
+        for (int w = 1; w < kConsumerWarps; ++w) v += red[w * kTileN + ct];
+    }
+    const int64_t col0 = t * kTileN;
+
+    if constexpr (CLUSTER) {
+        // CTA r of the tile's cluster sums slice r of the columns over the
+        // cluster's CTAs in rank order, reading their shared memory directly
+        namespace cg = cooperative_groups;
+        float *tile_sum = red + kConsumerWarps * kTileN;  // [kTileN]
+        if (ct < kTileN) tile_sum[ct] = v;
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        const int per = (kTileN + p.split - 1) / p.split;
+        const int c = q * per + ct;
+        if (ct < per && c < kTileN && col0 + c < p.N) {
+            float sum = *cluster.map_shared_rank(tile_sum + c, 0);
+            for (int r = 1; r < p.split; ++r) sum += *cluster.map_shared_rank(tile_sum + c, r);
+            const int64_t n = col0 + c;
+            p.C[n] = q8epi::apply(p.epi, sum, p.C, n, n);
+        }
+        cluster.sync();  // keep this CTA's sums alive until every CTA has read them
+    } else {
+        const int64_t n = col0 + ct;
+        if (ct < kTileN && n < p.N) p.C[n] = q8epi::apply(p.epi, v, p.C, n, n);
+    }
+}
+
+}  // namespace sk

@@ -134,6 +134,7 @@ struct Params {
     int split;
     int bps;               // blocks per K range
     uint64_t wait_ns;
+    uint32_t extra_tx;     // bytes a stage's barrier expects beyond its copies (0; tests of the expiry path only)
     q8epi::Epilogue epi;
 };
 
@@ -405,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         for (int t = 0; t < kPairStages && t < nsteps; ++t) {
             const int nb = step_blocks(t);
-            mbar_arrive_expect_tx(s_full + t, nb * kStageTx);
+            mbar_arrive_expect_tx(s_full + t, nb * kStageTx + p.extra_tx);
             for (int h = 0; h < nb; ++h)
                 issue_inputs(&tmW, &tmS, base, s_full + t, kPair * t + h, tile, b_begin + kPair * t + h);
         }
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     break;
                 }
                 const int nb = step_blocks(u);
-                mbar_arrive_expect_tx(s_full + ps, nb * kStageTx);
+                mbar_arrive_expect_tx(s_full + ps, nb * kStageTx + p.extra_tx);
                 for (int h = 0; h < nb; ++h) {
                     issue_inputs(&tmW, &tmS, base, s_full + ps, kPair * ps + h, tile, b_begin + kPair * u + h);
                     issue_parts(p, smem, s_full + ps, kPair * ps + h, z, b_begin + kPair * u + h);

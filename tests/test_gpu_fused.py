@@ -156,15 +156,23 @@ def test_fused_with_zero_k(q8, orc, M):
     check(C.cpu().numpy().astype(np.float64), ref, 1e-6 * mag + 1e-6, "K=0")
 
 
-def test_fused_on_tma_and_async_plans_uses_the_register_kernel(q8, orc):
-    A, W, S, bias, residual, c_old = inputs("attn", 1, seed=71)
+@pytest.mark.parametrize("name", ["attn", "ffn_up", "tiny"])
+@pytest.mark.parametrize("act", ["relu", "silu", "gelu_tanh"])
+def test_fused_on_streaming_plans(q8, orc, name, act):
+    A, W, S, bias, residual, c_old = inputs(name, 1, seed=71)
     K, N = W.shape
-    for kernel in (q8.KERNEL_TMA, q8.KERNEL_ASYNC):
-        plan = q8.Plan(K, N, kernel=kernel)
-        epi = dict(bias=bias, residual=residual, act="relu")
-        got = run_fused(plan, A, W, S, c_old, **epi)
-        ref, tol = reference(orc, A, W, S, c_old, **epi)
-        check(got, ref, tol, f"kernel {kernel}")
+    if N % 16:
+        N16 = N - N % 16
+        W, S, bias, residual, c_old = (W[:, :N16].copy(), S[:, :N16].copy(), bias[:N16].copy(),
+                                       residual[:, :N16].copy(), c_old[:, :N16].copy())
+        N = N16
+    plan = q8.Plan(K, N, kernel=q8.KERNEL_STREAM, overlap=1)
+    assert plan.info["kernel"] == q8.KERNEL_STREAM
+    epi = dict(bias=bias, residual=residual, act=act, beta=0.5)
+    got = run_fused(plan, A, W, S, c_old, **epi)
+    ref, tol = reference(orc, A, W, S, c_old, **epi)
+    check(got, ref, tol, f"{name} {act}")
+    assert plan.check() == 0
 
 
 def test_fused_rejects_bad_epilogues(q8):

@@ -178,41 +178,6 @@ def test_invalid_run_arguments(q8):
         plan(A, W.cpu(), S)
 
 
-TMA_K = [32, 33, 63, 100, 4100, 11008]
-TMA_N = [256, 272, 512, 528, 4096, 4112]
-
-
-@pytest.mark.parametrize("K", TMA_K)
-@pytest.mark.parametrize("N", TMA_N)
-def test_tma_kernel_shapes(q8, orc, K, N):
-    """TMA stream: ragged last tile (columns past N arrive as zeros), K tails, tiny unit counts."""
-    A, W, S = workloads.make_random(K, N, seed=K * 7 + N)
-    plan = q8.Plan(K, N, kernel=q8.KERNEL_TMA)
-    assert plan.info["kernel"] == q8.KERNEL_TMA
-    got, guards = run_plan(plan, A, W, S)
-    ref, bound = orc.factored(A, W, S)
-    assert guards
-    assert_close(got, ref, bound, f"tma K={K} N={N}")
-    assert plan.check() == 0
-
-
-@pytest.mark.parametrize("stages", [8, 16])
-@pytest.mark.parametrize("name", ["attn", "ffn_down", "lm_head"])
-def test_tma_ring_depths(q8, orc, stages, name):
-    A, W, S = workloads.make_inputs(name)
-    K, N = W.shape
-    plan = q8.Plan(K, N, kernel=q8.KERNEL_TMA, stages=stages)
-    assert plan.info["stages"] == stages
-    got, _ = run_plan(plan, A, W, S)
-    ref, bound = orc.factored(A, W, S)
-    assert_close(got, ref, bound, f"{name} stages={stages}")
-    Ai, Wi, Si = workloads.make_integer_exact(K, N, seed=3)
-    got_i, _ = run_plan(plan, Ai, Wi, Si)
-    ref_i, _ = orc.factored(Ai, Wi, Si)
-    assert np.array_equal(got_i, ref_i)
-    assert plan.check() == 0
-
-
 def test_default_plan_kernels(q8):
     for name in workloads.WORKLOADS:
         w = workloads.WORKLOADS[name]
@@ -226,57 +191,9 @@ def test_all_kernels_agree(q8, orc):
     A, W, S = workloads.make_inputs("ffn_up")
     K, N = W.shape
     ref, bound = orc.factored(A, W, S)
-    for kernel in (q8.KERNEL_REGS, q8.KERNEL_TMA, q8.KERNEL_ASYNC):
+    for kernel in (q8.KERNEL_REGS, q8.KERNEL_STREAM):
         got, _ = run_plan(q8.Plan(K, N, kernel=kernel), A, W, S)
         assert_close(got, ref, bound, f"kernel {kernel}")
-
-
-def test_tma_plan_rejects_shapes_it_cannot_stream(q8):
-    for K, N in ((31, 4096), (4096, 200), (4096, 128)):
-        with pytest.raises(q8.Q8mvError):
-            q8.Plan(K, N, kernel=q8.KERNEL_TMA)
-    with pytest.raises(q8.Q8mvError):
-        q8.Plan(4096, 4096, kernel=q8.KERNEL_TMA, stages=12)  # not a multiple of 8
-    with pytest.raises(q8.Q8mvError):
-        q8.Plan(4096, 4096, kernel=q8.KERNEL_TMA, stages=32)  # does not fit in shared memory
-
-
-ASYNC_K = [1, 31, 32, 33, 100, 4100, 11008]
-ASYNC_N = [16, 48, 256, 272, 4096, 4112]
-
-
-@pytest.mark.parametrize("K", ASYNC_K)
-@pytest.mark.parametrize("N", ASYNC_N)
-def test_async_kernel_shapes(q8, orc, K, N):
-    """Async ring: zero-filled rows past K, strips past N idle, splits from 1 to many."""
-    A, W, S = workloads.make_random(K, N, seed=K * 11 + N)
-    plan = q8.Plan(K, N, kernel=q8.KERNEL_ASYNC)
-    assert plan.info["kernel"] == q8.KERNEL_ASYNC
-    got, guards = run_plan(plan, A, W, S)
-    ref, bound = orc.factored(A, W, S)
-    assert guards
-    assert_close(got, ref, bound, f"async K={K} N={N}")
-
-
-@pytest.mark.parametrize("threads_n", [8, 16, 32, 64])
-@pytest.mark.parametrize("split_k", [1, 2, 5, 40])
-@pytest.mark.parametrize("stages,cta_threads", [(2, 128), (3, 256), (4, 128), (6, 256)])
-def test_async_forced_configurations(q8, orc, threads_n, split_k, stages, cta_threads):
-    K, N = 1251, 2048
-    A, W, S = workloads.make_random(K, N, seed=9)
-    if threads_n > cta_threads:
-        pytest.skip("tile wider than the CTA")
-    plan = q8.Plan(K, N, kernel=q8.KERNEL_ASYNC, threads_n=threads_n, split_k=split_k, stages=stages,
-                   cta_threads=cta_threads)
-    assert plan.info["threads_n"] == threads_n and plan.info["stages"] == stages
-    assert plan.info["threads_per_cta"] == cta_threads
-    got, _ = run_plan(plan, A, W, S)
-    ref, bound = orc.factored(A, W, S)
-    assert_close(got, ref, bound, f"async tn={threads_n} split={split_k}")
-    Ai, Wi, Si = workloads.make_integer_exact(K, N, seed=10)
-    got_i, _ = run_plan(plan, Ai, Wi, Si)
-    ref_i, _ = orc.factored(Ai, Wi, Si)
-    assert np.array_equal(got_i, ref_i)
 
 
 def test_overlapped_launches_respect_the_chain(q8):
@@ -307,10 +224,11 @@ def test_overlapped_launches_respect_the_chain(q8):
         stream.synchronize()
         return [b.cpu() for b in bufs]
 
-    plain = chain(q8.Plan(K, N, kernel=q8.KERNEL_ASYNC))
-    overlapped_plan = q8.Plan(K, N, kernel=q8.KERNEL_ASYNC, overlap=1)
-    assert overlapped_plan.info["overlap"] == 1
-    for _ in range(3):
-        over = chain(overlapped_plan)
-        for i in range(calls):
-            assert torch.equal(plain[i], over[i]), i
+    for kernel in (q8.KERNEL_REGS, q8.KERNEL_STREAM):
+        plain = chain(q8.Plan(K, N, kernel=kernel))
+        overlapped_plan = q8.Plan(K, N, kernel=kernel, overlap=1)
+        assert overlapped_plan.info["overlap"] == 1 and overlapped_plan.info["kernel"] == kernel
+        for _ in range(3):
+            over = chain(overlapped_plan)
+            for i in range(calls):
+                assert torch.equal(plain[i], over[i]), (kernel, i)

@@ -171,50 +171,50 @@ def test_planner_rejects_illegal_requests(q8):
         q8.choose_config(64, 256, 152, 1, 16, threads_n=96)
 
 
-TMA_SHAPES = [(4096, 4096), (4096, 11008), (11008, 4096), (8192, 28672), (4100, 128256),
-              (32, 256), (33, 272), (100000, 256), (64, 1 << 20)]
+STREAM_SHAPES = [(4096, 4096), (4096, 11008), (11008, 4096), (8192, 28672), (4100, 128256),
+                 (32, 256), (33, 272), (1, 16), (65536, 256), (64, 1 << 20)]
 
 
-@pytest.mark.parametrize("K,N", TMA_SHAPES)
-def test_tma_planner_covers_and_balances(q8, K, N):
+@pytest.mark.parametrize("K,N", STREAM_SHAPES)
+def test_stream_planner_fits_two_calls_per_sm(q8, K, N):
     KB = (K + 31) // 32
     tiles = -(-N // 256)
     for sms in (148, 152, 160):
-        c = q8.choose_config(K, N, sms, 0, 0, kernel=q8.KERNEL_TMA)
-        assert c["kernel"] == q8.KERNEL_TMA and c["tile_n"] == 256 and c["threads_per_cta"] == 288
+        c = q8.choose_config(K, N, sms, 0, 0, kernel=q8.KERNEL_STREAM)
+        assert c["kernel"] == q8.KERNEL_STREAM and c["tile_n"] == 256 and c["threads_per_cta"] == 288
         split, bps = c["split_k"], c["blocks_per_split"]
-        assert split * bps >= KB and (split - 1) * bps < KB  # every block in exactly one K range
-        items = tiles * split
-        assert c["grid_x"] == min(sms, items)
-        assert c["workspace_bytes"] == (4 * split * N if split > 1 else 0)
-        # the busiest CTA streams at most ~6% more units than an even share (or one item)
-        busiest = -(-items // c["grid_x"]) * bps
-        assert busiest <= max(1.06 * tiles * KB / c["grid_x"], bps) + bps
+        assert 1 <= split <= min(16, KB) and c["cluster"] == (1 if split > 1 else 0)
+        assert bps == -(-KB // split) and bps <= 128  # the CTA's activations fit 16 KiB
+        assert c["grid_x"] == tiles and c["grid_y"] == split and c["workspace_bytes"] == 0
+        # one CTA per SM and call whenever the smallest legal split allows it
+        min_split = -(-KB // 128)
+        if tiles * min_split <= sms:
+            assert tiles * split <= sms
+            # no larger split would still fit one CTA per SM
+            assert split == min(16, KB) or tiles * (split + 1) > sms
+        else:
+            assert split == min_split
+        # ring and activations within half of a 228 KiB SM (1 KiB reserved per CTA)
+        stages = c["stages"]
+        assert 1 <= stages <= min(24, bps)
+        assert 1024 + stages * 9216 + bps * 128 <= 228 * 1024 // 2 - 1024
 
 
-def test_tma_planner_rejects_shapes_it_cannot_stream(q8):
-    for K, N in ((31, 4096), (4096, 200), (4096, 128)):
+def test_stream_planner_rejects_shapes_it_cannot_stream(q8):
+    for K, N in ((0, 4096), (4096, 200), (4096, 8), (65536 + 32 * 128, 256)):
         with pytest.raises(q8.Q8mvError):
-            q8.choose_config(K, N, 152, 0, 0, kernel=q8.KERNEL_TMA)
-
-
-@pytest.mark.parametrize("K,N", [(4096, 4096), (4096, 11008), (11008, 4096), (8192, 28672), (4100, 128256),
-                                 (1, 16), (33, 48), (100000, 256)])
-def test_async_planner_covers_every_block(q8, K, N):
-    KB = (K + 31) // 32
-    for sms in (148, 152, 160):
-        c = q8.choose_config(K, N, sms, 0, 0, kernel=q8.KERNEL_ASYNC)
-        assert c["kernel"] == q8.KERNEL_ASYNC and c["vec_bytes"] == 16 and c["threads_per_cta"] in (128, 256)
-        assert c["threads_n"] in (8, 16, 32, 64) and c["tile_n"] == 16 * c["threads_n"]
-        assert c["stages"] in (2, 3, 4, 6)
-        assert c["grid_x"] * c["tile_n"] >= N and (c["grid_x"] - 1) * c["tile_n"] < N
-        assert c["blocks_per_split"] <= 128  # the CTA's activations fit in shared memory
-        assert c["split_k"] * c["blocks_per_split"] >= KB and (c["split_k"] - 1) * c["blocks_per_split"] < KB
-
-
-def test_async_planner_rejects_unaligned_rows(q8):
+            q8.choose_config(K, N, 152, 0, 0, kernel=q8.KERNEL_STREAM)
     with pytest.raises(q8.Q8mvError):
-        q8.choose_config(64, 200, 152, 0, 0, kernel=q8.KERNEL_ASYNC)
+        q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, split_k=17)
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, stages=25)
+    with pytest.raises(q8.Q8mvError):
+        q8.choose_config(64, 256, 152, 0, 0, kernel=3)  # a retired kernel family
+
+
+def test_stream_planner_takes_forced_split_and_stages(q8):
+    c = q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, split_k=4, stages=6)
+    assert c["split_k"] == 4 and c["stages"] == 6 and c["blocks_per_split"] == 32
 
 
 # ----------------------------------------------------------------------------
@@ -289,7 +289,7 @@ def test_batched_planner_rejects_illegal_requests(q8):
     with pytest.raises(q8.Q8mvError):
         q8.choose_config_batched(4, 64, 256, 152, 2, 4, cta_threads=128)
     with pytest.raises(q8.Q8mvError):
-        q8.choose_config_batched(4, 64, 256, 152, 2, 4, kernel=q8.KERNEL_TMA)
+        q8.choose_config_batched(4, 64, 256, 152, 2, 4, kernel=q8.KERNEL_STREAM)
 
 
 def test_batched_plan_rejects_bad_arguments_before_touching_a_device(q8):
@@ -350,7 +350,7 @@ def test_transposed_plan_rejects_bad_arguments_before_touching_a_device(q8):
     assert h.value is None
     assert lib.q8mv_plan_transposed(None, 64, 64, -1, None) == q8.Q8MV_ERR_INVALID_ARG
     for bad in (q8.Opts(0, 8, 0, 0, 0, 0, 0, 0), q8.Opts(0, 0, 32, 0, 0, 0, 0, 0), q8.Opts(0, 0, 0, 2, 0, 0, 0, 0),
-                q8.Opts(0, 0, 0, 0, 0, 0, 0, 12), q8.Opts(q8.KERNEL_TMA, 0, 0, 0, 0, 0, 0, 0)):
+                q8.Opts(0, 0, 0, 0, 0, 0, 0, 12), q8.Opts(q8.KERNEL_STREAM, 0, 0, 0, 0, 0, 0, 0)):
         assert lib.q8mv_plan_transposed(ctypes.byref(h), 64, 64, -1, ctypes.byref(bad)) == q8.Q8MV_ERR_INVALID_ARG
     # rows_per_cta belongs to transposed plans only
     bad = q8.Opts(0, 0, 0, 0, 0, 0, 0, 8)
