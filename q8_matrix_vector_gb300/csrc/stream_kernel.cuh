@@ -13,30 +13,41 @@
 // kernel occupies at most half of each SM (one CTA per SM, at most half the
 // shared memory and registers), so under programmatic dependent launch the
 // next call's CTAs become resident right away, alongside the running call,
-// and fill their rings with weights and scales while the running call
+// and bring their weights and scales on chip while the running call
 // computes.  When the running call completes, the next call's weights are
-// already on chip; it stages its activations and multiplies.
+// already there; it stages its activations and multiplies.  Weights a CTA
+// requests only after its activations are known would queue behind the next
+// call's early requests, so as much as possible is requested up front: a
+// ring of up to 24 half-blocks in shared memory, and 8 more half-blocks held
+// in the consumer warps' registers.
 //
-// Work: CTA (t, q) owns the 256-column tile t (one TMA box wide) and the
-// contiguous block range [q*KB/split, (q+1)*KB/split) of its K.
-//   * One producer thread issues, per block, two 2D tensor copies into the
-//     next ring stage: W[32b .. 32b+32, 256t .. +256) (8 KiB) and
-//     S[b, 256t .. +256) (1 KiB), completing on the stage's "full" mbarrier.
-//     Rows at or past K and columns at or past N lie outside the tensor maps
-//     and arrive as zeros without being read.  The first ring's worth is
-//     issued before anything else; a stage is refilled once its consumer
-//     has released it ("empty").
-//   * Eight consumer warps wait for the previous grid (griddepcontrol.wait),
-//     stage the CTA's activations in shared memory (zeros past K) and take the
-//     blocks round-robin: warp w handles blocks w, w+8, ...  Lane l owns
-//     columns 8l .. 8l+7: it reads each of the block's 32 rows with one
-//     8-byte shared load, converts the bytes to f32 exactly, accumulates the
-//     block's sum in row order with packed f32x2 FMAs and folds the block's
-//     scale once per column into its accumulator.
+// Work: CTA (t, q) owns the 256-column tile t and the contiguous block range
+// [q*KB/split, (q+1)*KB/split) of K.  Its items are half-blocks: item
+// i = 2j + h is rows 32(b0+j) .. +32 of the tile's column half h (128
+// columns), with their 128 scales.
+//   * Consumer warp w takes the items i = w, w+8, w+16, ... (so it always
+//     works on half h = w & 1); lane l owns columns 128h + 4l .. +3.  Items
+//     below R (the ring depth, a multiple of 8) come through the ring; the
+//     next 8 items are loaded by their warp straight into registers before
+//     the grid-dependency wait, and are the first each warp multiplies; any
+//     later item comes through the ring again.
+//   * One producer thread issues, per ring item, two 2D tensor copies into
+//     the item's stage: the 32 x 128 weight bytes (4 KiB) and the 128 scales
+//     (512 B), completing on the stage's "full" mbarrier.  Rows at or past K
+//     and columns at or past N lie outside the tensor maps and arrive as
+//     zeros without being read.  Ring item r sits in stage r % R; since R is a
+//     multiple of 8, a stage always belongs to the same warp, which takes its
+//     uses in order, so every parity wait is unambiguous.  A stage is refilled
+//     once its warp has released it ("empty").
+//   * The consumers wait for the previous grid (griddepcontrol.wait), stage
+//     the CTA's activations in shared memory (zeros past K) and then, per
+//     item, read each of the 32 rows with one 4-byte shared load, convert the
+//     bytes to f32 exactly, accumulate the block's sum in row order with
+//     packed f32x2 FMAs and fold the block's scale once per column.
 //   * At the end the warps' accumulators are summed in warp order through
 //     shared memory.  With split > 1 the tile's CTAs form one thread-block
 //     cluster: after a cluster barrier CTA r sums slice r of the columns over
-//     the cluster's CTAs in rank order through distributed shared memory, and
+//     the cluster's CTAs in rank order through distributed shared memory and
 //     writes C (with the fused epilogue, if any).  Every sum has an order
 //     fixed by the plan.
 //   * Every mbarrier wait is bounded (wait_ns of %globaltimer).  On expiry
@@ -55,16 +66,18 @@
 namespace sk {
 
 constexpr int kBlk = 32;
-constexpr int kTileN = 256;                          // columns per CTA: one TMA box
-constexpr int kLaneCols = kTileN / 32;               // 8 columns per consumer lane
+constexpr int kTileN = 256;                          // columns per CTA
+constexpr int kHalfN = 128;                          // columns per item: one TMA box
+constexpr int kLaneCols = kHalfN / 32;               // 4 columns per consumer lane
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;      // + one producer warp
-constexpr int kWBytes = kBlk * kTileN;               // 8192
-constexpr int kSBytes = kTileN * 4;                  // 1024
-constexpr int kStageBytes = kWBytes + kSBytes;       // 9216, a multiple of 128
-constexpr int kMaxStages = 24;
-constexpr int kBarBytes = 1024;                      // mbarriers, ahead of the ring
+constexpr int kWBytes = kBlk * kHalfN;               // 4096
+constexpr int kSBytes = kHalfN * 4;                  // 512
+constexpr int kStageBytes = kWBytes + kSBytes;       // 4608, a multiple of 128
+constexpr int kMaxStages = 24;                       // ring depth: a multiple of kConsumerWarps
+constexpr int kRegItems = kConsumerWarps;            // items held in registers, one per warp
+constexpr int kBarBytes = 1024;                      // mbarriers and the abort word, ahead of the ring
 constexpr int kMaxBlocksPerCta = 128;                // the CTA's activations, staged whole: <= 16 KiB
 constexpr int kMaxSplit = 16;                        // largest cluster (non-portable size)
 constexpr uint64_t kWaitNs = 2000000000ull;          // bound on any single wait
@@ -75,12 +88,16 @@ constexpr int kErrEmptyTimeout = 2;  // a stage was not released in time
 constexpr int kErrDrainTimeout = 4;  // copies in flight did not land in time at the end
 
 static_assert(kStageBytes % 128 == 0, "stages keep the 128-byte alignment of tensor copies");
+static_assert(kMaxStages % kConsumerWarps == 0, "a stage must always belong to one warp");
 constexpr int kAbortOff = 2 * kMaxStages * 8;        // the CTA's abort word, after the mbarriers
 static_assert(kAbortOff + 4 <= kBarBytes, "mbarriers and the abort word fit their area");
-static_assert(kConsumerWarps * kTileN * 4 + kTileN * 4 <= kStageBytes, "the reduction fits the first stage");
+// the reduction at the end reuses the first kConsumerWarps stages
+static_assert(kConsumerWarps * kHalfN * 4 + kTileN * 4 <= kConsumerWarps * kStageBytes, "reduction fits");
 
 struct Params {
     const float *A;
+    const int8_t *W;    // for the items held in registers (the rest come through the tensor maps)
+    const float *S;
     float *C;
     int *err;           // device error word (0 = ok)
     int64_t K, N;
@@ -173,20 +190,40 @@ __device__ __forceinline__ float2 cvt2(uint32_t flipped, uint32_t sel_lo, uint32
     return __fadd2_rn(t, make_float2(-8388736.0f, -8388736.0f));
 }
 
-// part[0..8) += a * (8 signed bytes in w)
-__device__ __forceinline__ void fma_row8(float a, uint2 w, float2 (&part)[4]) {
+// part[0..4) += a * (4 signed bytes in w)
+__device__ __forceinline__ void fma_row4(float a, uint32_t w, float2 (&part)[2]) {
     const float2 a2 = make_float2(a, a);
-    const uint32_t u0 = w.x ^ 0x80808080u;
-    const uint32_t u1 = w.y ^ 0x80808080u;
-    part[0] = __ffma2_rn(a2, cvt2(u0, 0x7440u, 0x7441u), part[0]);
-    part[1] = __ffma2_rn(a2, cvt2(u0, 0x7442u, 0x7443u), part[1]);
-    part[2] = __ffma2_rn(a2, cvt2(u1, 0x7440u, 0x7441u), part[2]);
-    part[3] = __ffma2_rn(a2, cvt2(u1, 0x7442u, 0x7443u), part[3]);
+    const uint32_t u = w ^ 0x80808080u;
+    part[0] = __ffma2_rn(a2, cvt2(u, 0x7440u, 0x7441u), part[0]);
+    part[1] = __ffma2_rn(a2, cvt2(u, 0x7442u, 0x7443u), part[1]);
 }
 
-// Shared memory: [mbarriers: full[R], empty[R]; abort word] [ring: R stages of W, S]
-// [activations: the CTA's blocks, 128 bytes each].  The reduction at the end
-// reuses the first stage.
+// A block's 32 rows of a lane's 4 columns (row r in w[r]) against the block's
+// activations a_blk, then acc += part * s: the block sum in row order, one
+// scale fold per column ("Factoring out the scale").
+__device__ __forceinline__ void block_dot(const float *a_blk, const uint32_t (&w)[kBlk], float4 s,
+                                          float2 (&acc)[2]) {
+    float2 part[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+#pragma unroll
+    for (int r = 0; r < kBlk; r += 4) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(a_blk + r);
+        fma_row4(a4.x, w[r + 0], part);
+        fma_row4(a4.y, w[r + 1], part);
+        fma_row4(a4.z, w[r + 2], part);
+        fma_row4(a4.w, w[r + 3], part);
+    }
+    acc[0] = __ffma2_rn(part[0], make_float2(s.x, s.y), acc[0]);
+    acc[1] = __ffma2_rn(part[1], make_float2(s.z, s.w), acc[1]);
+}
+
+__device__ __forceinline__ uint32_t ldg_stream_u32(const int8_t *p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Shared memory: [mbarriers full[R], empty[R]; abort word] [ring: R stages of
+// W and S half-blocks] [activations: the CTA's blocks, 128 bytes each].
 template <bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 2)
     q8mv_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
@@ -206,7 +243,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int q = static_cast<int>(blockIdx.y);
     const int b0 = static_cast<int>(static_cast<int64_t>(q) * p.KB / p.split);
     const int b1 = static_cast<int>(static_cast<int64_t>(q + 1) * p.KB / p.split);
-    const int len = b1 - b0;
+    const int items = 2 * (b1 - b0);
+    // items R .. R + n_reg - 1 are held in registers; the rest go through the ring
+    const int n_reg = min(kRegItems, max(0, items - R));
+    const int ring_items = items - n_reg;
+    const int64_t col0 = t * kTileN;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < R; ++s) {
@@ -221,30 +262,30 @@ __global__ void __launch_bounds__(kThreads, 2)
     // before its own griddepcontrol.wait
     pdl_launch_dependents();
 
-    float2 acc[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.0f, 0.0f);
+    float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             prefetch_tensormap(&tmW);
             prefetch_tensormap(&tmS);
-            const int x = static_cast<int>(t * kTileN);
             int issued = 0;
             int s = 0;
             uint32_t use = 0;  // how many times stage s has been filled before
-            for (int j = 0; j < len; ++j) {
+            for (int r = 0; r < ring_items; ++r) {
                 if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1u, abort_flag, p.wait_ns)) {
                     if (!*abort_flag) atomicOr(p.err, kErrEmptyTimeout);
                     s_abort = 1;
                     break;
                 }
                 if (*abort_flag) break;
+                const int i = r < R ? r : r + n_reg;  // the item: register items are skipped
+                const int x = static_cast<int>(col0) + (i & 1) * kHalfN;
+                const int b = b0 + (i >> 1);
                 unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
                 mbar_arrive_expect_tx(full + s, kStageBytes + p.extra_tx);
-                tma_load_2d(st, &tmW, x, (b0 + j) * kBlk, full + s);
-                tma_load_2d(st + kWBytes, &tmS, x, b0 + j, full + s);
+                tma_load_2d(st, &tmW, x, b * kBlk, full + s);
+                tma_load_2d(st + kWBytes, &tmS, x, b, full + s);
                 ++issued;
                 if (++s == R) {
                     s = 0;
@@ -252,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             // every copy this CTA issued lands before the CTA can finish
-            for (int j = (issued > R ? issued - R : 0); j < issued; ++j) {
-                if (!mbar_wait(full + (j % R), static_cast<uint32_t>(j / R) & 1u, nullptr, p.wait_ns)) {
+            for (int r = (issued > R ? issued - R : 0); r < issued; ++r) {
+                if (!mbar_wait(full + (r % R), static_cast<uint32_t>(r / R) & 1u, nullptr, p.wait_ns)) {
                     atomicOr(p.err, kErrDrainTimeout);
                     break;
                 }
@@ -261,79 +302,77 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // -------------------------------------------------------- consumers
+        const int h = warp & 1;
+        const int64_t n0 = col0 + h * kHalfN + lane * kLaneCols;
+        const bool cols_ok = n0 < p.N;  // N % 16 == 0: a lane's 4 columns are all in or all out
+        // this warp's register item (if any), requested before the wait
+        const int i_reg = R + warp;
+        const bool has_reg = warp < n_reg;
+        uint32_t wr[kBlk];
+        float4 sr = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (has_reg) {
+            const int b = b0 + (i_reg >> 1);
+            const int64_t k0 = static_cast<int64_t>(b) * kBlk;
+            const int8_t *wp = p.W + k0 * p.N + n0;
+#pragma unroll
+            for (int r = 0; r < kBlk; ++r)
+                wr[r] = (cols_ok && k0 + r < p.K) ? ldg_stream_u32(wp + static_cast<int64_t>(r) * p.N) : 0u;
+            if (cols_ok) sr = __ldg(reinterpret_cast<const float4 *>(p.S + static_cast<int64_t>(b) * p.N + n0));
+        }
         pdl_wait();
         const int64_t k0 = static_cast<int64_t>(b0) * kBlk;
-        const int nk = len * kBlk;
+        const int nk = (b1 - b0) * kBlk;
         for (int i = threadIdx.x; i < nk; i += kConsumerThreads)
             a_s[i] = (k0 + i < p.K) ? __ldg(p.A + k0 + i) : 0.0f;
         consumers_sync();
 
-        int s = warp;
-        uint32_t use = 0;
-        while (s >= R) {
-            s -= R;
-            ++use;
-        }
-        for (int j = warp; j < len; j += kConsumerWarps) {
+        // the register item first: it is on chip already, and its registers are
+        // free for the ring items afterwards
+        if (has_reg) block_dot(a_s + (i_reg >> 1) * kBlk, wr, sr, acc);
+        for (int i = warp; i < items; i += kConsumerWarps) {
+            if (i >= R && i < R + n_reg) continue;
+            const float *a_blk = a_s + (i >> 1) * kBlk;
+            const int r_item = i < R ? i : i - n_reg;
+            const int s = r_item % R;
+            const uint32_t use = static_cast<uint32_t>(r_item / R);
             if (*abort_flag || !mbar_wait(full + s, use & 1u, abort_flag, p.wait_ns)) {
                 if (!*abort_flag && lane == 0) atomicOr(p.err, kErrFullTimeout);
                 s_abort = 1;
                 break;
             }
             const unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
-            const uint2 *wl = reinterpret_cast<const uint2 *>(st) + lane;
-            const float4 *a4p = reinterpret_cast<const float4 *>(a_s + j * kBlk);
-            float2 part[4];
+            const uint32_t *wl = reinterpret_cast<const uint32_t *>(st) + lane;
+            uint32_t w[kBlk];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) part[c] = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int r = 0; r < kBlk; r += 4) {
-                const float4 a4 = a4p[r / 4];
-                fma_row8(a4.x, wl[(r + 0) * 32], part);
-                fma_row8(a4.y, wl[(r + 1) * 32], part);
-                fma_row8(a4.z, wl[(r + 2) * 32], part);
-                fma_row8(a4.w, wl[(r + 3) * 32], part);
-            }
-            const float4 *sl = reinterpret_cast<const float4 *>(st + kWBytes) + 2 * lane;
-            const float4 s0 = sl[0], s1 = sl[1];
-            acc[0] = __ffma2_rn(part[0], make_float2(s0.x, s0.y), acc[0]);
-            acc[1] = __ffma2_rn(part[1], make_float2(s0.z, s0.w), acc[1]);
-            acc[2] = __ffma2_rn(part[2], make_float2(s1.x, s1.y), acc[2]);
-            acc[3] = __ffma2_rn(part[3], make_float2(s1.z, s1.w), acc[3]);
+            for (int r = 0; r < kBlk; ++r) w[r] = wl[r * (kHalfN / 4)];
+            const float4 s4 = reinterpret_cast<const float4 *>(st + kWBytes)[lane];
+            block_dot(a_blk, w, s4, acc);
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + s);  // the stage may be refilled
-            s += kConsumerWarps;
-            while (s >= R) {
-                s -= R;
-                ++use;
-            }
         }
     }
 
-    // ---- sum the warps' accumulators in warp order (the first stage is free:
-    // every copy has landed and every stage has been consumed or abandoned)
+    // ---- sum the warps' accumulators in warp order (the first stages are
+    // free: every copy has landed and every stage has been consumed or abandoned)
     __syncthreads();
-    float *red = reinterpret_cast<float *>(ring);  // [kConsumerWarps][kTileN]
-    if (warp < kConsumerWarps) {
-        float4 *mine = reinterpret_cast<float4 *>(red + warp * kTileN + lane * kLaneCols);
-        mine[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
-        mine[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
-    }
+    float *red = reinterpret_cast<float *>(ring);  // [kConsumerWarps][kHalfN]
+    if (warp < kConsumerWarps)
+        reinterpret_cast<float4 *>(red + warp * kHalfN)[lane] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
     __syncthreads();
     const int ct = threadIdx.x;  // column of the tile this thread sums (ct < kTileN)
     float v = 0.0f;
     if (ct < kTileN) {
-        v = red[ct];
+        const int h = ct / kHalfN, c = ct % kHalfN;
+        v = red[h * kHalfN + c];
 #pragma unroll
-        for (int w = 1; w < kConsumerWarps; ++w) v += red[w * kTileN + ct];
+        for (int w = h + 2; w < kConsumerWarps; w += 2) v += red[w * kHalfN + c];
     }
-    const int64_t col0 = t * kTileN;
 
     if constexpr (CLUSTER) {
         // CTA r of the tile's cluster sums slice r of the columns over the
         // cluster's CTAs in rank order, reading their shared memory directly
         namespace cg = cooperative_groups;
-        float *tile_sum = red + kConsumerWarps * kTileN;  // [kTileN]
+        float *tile_sum = red + kConsumerWarps * kHalfN;  // [kTileN]
         if (ct < kTileN) tile_sum[ct] = v;
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();
