@@ -18,32 +18,36 @@
 // already there; it stages its activations and multiplies.  Weights a CTA
 // requests only after its activations are known would queue behind the next
 // call's early requests, so as much as possible is requested up front: a
-// ring of up to 24 half-blocks in shared memory, and 8 more half-blocks held
-// in the consumer warps' registers.
+// ring of up to 12 blocks in shared memory, and 4 more blocks held in the
+// consumer warps' registers.  One thread issuing tensor copies from DRAM
+// manages about one copy every 350 ns (measured), far below a CTA's share
+// of the bandwidth, so several lanes of the producer warp issue copies.
 //
 // Work: CTA (t, q) owns the 256-column tile t and the contiguous block range
-// [q*KB/split, (q+1)*KB/split) of K.  Its items are half-blocks: item
-// i = 2j + h is rows 32(b0+j) .. +32 of the tile's column half h (128
-// columns), with their 128 scales.
-//   * Consumer warp w takes the items i = w, w+8, w+16, ... (so it always
-//     works on half h = w & 1); lane l owns columns 128h + 4l .. +3.  Items
-//     below R (the ring depth, a multiple of 8) come through the ring; the
-//     next 8 items are loaded by their warp straight into registers before
+// [q*KB/split, (q+1)*KB/split) of K (blocks j = 0 .. len-1 of the range).
+//   * Consumer warps come in four pairs; warp w is in pair g = w / 2 and works
+//     on column half h = w % 2 of the tile (128 columns; lane l owns columns
+//     128h + 4l .. +3).  Pair g takes the blocks j = g, g+4, g+8, ...  Blocks
+//     below R (the ring depth, a multiple of 4) come through the ring; the
+//     next 4 blocks are loaded by their pair straight into registers before
 //     the grid-dependency wait, and are the first each warp multiplies; any
-//     later item comes through the ring again.
-//   * One producer thread issues, per ring item, two 2D tensor copies into
-//     the item's stage: the 32 x 128 weight bytes (4 KiB) and the 128 scales
-//     (512 B), completing on the stage's "full" mbarrier.  Rows at or past K
-//     and columns at or past N lie outside the tensor maps and arrive as
-//     zeros without being read.  Ring item r sits in stage r % R; since R is a
-//     multiple of 8, a stage always belongs to the same warp, which takes its
-//     uses in order, so every parity wait is unambiguous.  A stage is refilled
-//     once its warp has released it ("empty").
+//     later block comes through the ring again.
+//   * Producer lanes issue, per ring block, two 2D tensor copies into the
+//     block's stage: the 32 x 256 weight bytes (8 KiB) and the 256 scales
+//     (1 KiB), completing on the stage's "full" mbarrier.  Rows at or past K
+//     and columns at or past N lie outside the tensor maps and arrive as zeros
+//     without being read.  Ring block r sits in stage r % R.  Since R is a
+//     multiple of 4, a stage always belongs to the same warp pair, which
+//     takes its uses in order, and (R being a multiple of the number of
+//     issuing lanes) to the same issuing lane, so every parity wait is
+//     unambiguous.  A stage is refilled once both warps of its pair have
+//     released it ("empty").
 //   * The consumers wait for the previous grid (griddepcontrol.wait), stage
 //     the CTA's activations in shared memory (zeros past K) and then, per
-//     item, read each of the 32 rows with one 4-byte shared load, convert the
-//     bytes to f32 exactly, accumulate the block's sum in row order with
-//     packed f32x2 FMAs and fold the block's scale once per column.
+//     block, read each of the 32 rows of their half with one 4-byte shared
+//     load, convert the bytes to f32 exactly, accumulate the block's sum in
+//     row order with packed f32x2 FMAs and fold the block's scale once per
+//     column.
 //   * At the end the warps' accumulators are summed in warp order through
 //     shared memory.  With split > 1 the tile's CTAs form one thread-block
 //     cluster: after a cluster barrier CTA r sums slice r of the columns over
@@ -66,17 +70,19 @@
 namespace sk {
 
 constexpr int kBlk = 32;
-constexpr int kTileN = 256;                          // columns per CTA
-constexpr int kHalfN = 128;                          // columns per item: one TMA box
+constexpr int kTileN = 256;                          // columns per CTA: one TMA box wide
+constexpr int kHalfN = 128;                          // columns per consumer warp
 constexpr int kLaneCols = kHalfN / 32;               // 4 columns per consumer lane
 constexpr int kConsumerWarps = 8;
+constexpr int kPairs = kConsumerWarps / 2;           // warp pairs: the two halves of a block
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;      // + one producer warp
-constexpr int kWBytes = kBlk * kHalfN;               // 4096
-constexpr int kSBytes = kHalfN * 4;                  // 512
-constexpr int kStageBytes = kWBytes + kSBytes;       // 4608, a multiple of 128
-constexpr int kMaxStages = 24;                       // ring depth: a multiple of kConsumerWarps
-constexpr int kRegItems = kConsumerWarps;            // items held in registers, one per warp
+constexpr int kWBytes = kBlk * kTileN;               // 8192
+constexpr int kSBytes = kTileN * 4;                  // 1024
+constexpr int kStageBytes = kWBytes + kSBytes;       // 9216, a multiple of 128
+constexpr int kMaxStages = 24;                       // ring depth: a multiple of kPairs
+constexpr int kRegBlocks = kPairs;                   // blocks held in registers, one per pair
+constexpr int kMaxIssuers = 8;                       // producer lanes issuing copies
 constexpr int kBarBytes = 1024;                      // mbarriers and the abort word, ahead of the ring
 constexpr int kMaxBlocksPerCta = 128;                // the CTA's activations, staged whole: <= 16 KiB
 constexpr int kMaxSplit = 16;                        // largest cluster (non-portable size)
@@ -88,11 +94,17 @@ constexpr int kErrEmptyTimeout = 2;  // a stage was not released in time
 constexpr int kErrDrainTimeout = 4;  // copies in flight did not land in time at the end
 
 static_assert(kStageBytes % 128 == 0, "stages keep the 128-byte alignment of tensor copies");
-static_assert(kMaxStages % kConsumerWarps == 0, "a stage must always belong to one warp");
+static_assert(kMaxStages % kPairs == 0, "a stage must always belong to one warp pair");
 constexpr int kAbortOff = 2 * kMaxStages * 8;        // the CTA's abort word, after the mbarriers
 static_assert(kAbortOff + 4 <= kBarBytes, "mbarriers and the abort word fit their area");
-// the reduction at the end reuses the first kConsumerWarps stages
-static_assert(kConsumerWarps * kHalfN * 4 + kTileN * 4 <= kConsumerWarps * kStageBytes, "reduction fits");
+// the reduction at the end reuses the first stages
+static_assert(kConsumerWarps * kHalfN * 4 + kTileN * 4 <= kPairs * kStageBytes, "reduction fits");
+
+// Producer lanes that issue copies for a ring of R stages: the most (at most
+// kMaxIssuers) that divide R, so that every stage has one issuing lane.
+__host__ __device__ constexpr int issuers_for(int R) {
+    return R % 8 == 0 ? 8 : R % 6 == 0 ? 6 : R % 4 == 0 ? 4 : R % 3 == 0 ? 3 : R % 2 == 0 ? 2 : 1;
+}
 
 struct Params {
     const float *A;
@@ -223,7 +235,7 @@ __device__ __forceinline__ uint32_t ldg_stream_u32(const int8_t *p) {
 }
 
 // Shared memory: [mbarriers full[R], empty[R]; abort word] [ring: R stages of
-// W and S half-blocks] [activations: the CTA's blocks, 128 bytes each].
+// a block's W and S] [activations: the CTA's blocks, 128 bytes each].
 template <bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 2)
     q8mv_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
@@ -243,16 +255,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int q = static_cast<int>(blockIdx.y);
     const int b0 = static_cast<int>(static_cast<int64_t>(q) * p.KB / p.split);
     const int b1 = static_cast<int>(static_cast<int64_t>(q + 1) * p.KB / p.split);
-    const int items = 2 * (b1 - b0);
-    // items R .. R + n_reg - 1 are held in registers; the rest go through the ring
-    const int n_reg = min(kRegItems, max(0, items - R));
-    const int ring_items = items - n_reg;
+    const int len = b1 - b0;
+    // blocks R .. R + n_reg - 1 are held in registers; the rest go through the ring
+    const int n_reg = min(kRegBlocks, max(0, len - R));
+    const int ring_blocks = len - n_reg;
     const int64_t col0 = t * kTileN;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < R; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, 1);
+            mbar_init(empty + s, 2);  // both warps of the stage's pair release it
         }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -266,34 +278,32 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------------- producer
-        if (lane == 0) {
-            prefetch_tensormap(&tmW);
-            prefetch_tensormap(&tmS);
-            int issued = 0;
-            int s = 0;
-            uint32_t use = 0;  // how many times stage s has been filled before
-            for (int r = 0; r < ring_items; ++r) {
+        // lane l issues the ring blocks r = l, l + n_iss, ... (stages l, l + n_iss, ...)
+        const int n_iss = issuers_for(R);
+        if (lane < n_iss) {
+            if (lane == 0) {
+                prefetch_tensormap(&tmW);
+                prefetch_tensormap(&tmS);
+            }
+            int last = -1;
+            for (int r = lane; r < ring_blocks; r += n_iss) {
+                const int s = r % R;
+                const uint32_t use = static_cast<uint32_t>(r / R);
                 if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1u, abort_flag, p.wait_ns)) {
                     if (!*abort_flag) atomicOr(p.err, kErrEmptyTimeout);
                     s_abort = 1;
                     break;
                 }
                 if (*abort_flag) break;
-                const int i = r < R ? r : r + n_reg;  // the item: register items are skipped
-                const int x = static_cast<int>(col0) + (i & 1) * kHalfN;
-                const int b = b0 + (i >> 1);
+                const int b = b0 + (r < R ? r : r + n_reg);  // register blocks are skipped
                 unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
                 mbar_arrive_expect_tx(full + s, kStageBytes + p.extra_tx);
-                tma_load_2d(st, &tmW, x, b * kBlk, full + s);
-                tma_load_2d(st + kWBytes, &tmS, x, b, full + s);
-                ++issued;
-                if (++s == R) {
-                    s = 0;
-                    ++use;
-                }
+                tma_load_2d(st, &tmW, static_cast<int>(col0), b * kBlk, full + s);
+                tma_load_2d(st + kWBytes, &tmS, static_cast<int>(col0), b, full + s);
+                last = r;
             }
-            // every copy this CTA issued lands before the CTA can finish
-            for (int r = (issued > R ? issued - R : 0); r < issued; ++r) {
+            // every copy this lane issued lands before the CTA can finish
+            for (int r = last; r >= 0 && r > last - R; r -= n_iss) {
                 if (!mbar_wait(full + (r % R), static_cast<uint32_t>(r / R) & 1u, nullptr, p.wait_ns)) {
                     atomicOr(p.err, kErrDrainTimeout);
                     break;
@@ -302,16 +312,18 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // -------------------------------------------------------- consumers
+        const int g = warp >> 1;
         const int h = warp & 1;
-        const int64_t n0 = col0 + h * kHalfN + lane * kLaneCols;
+        const int n0_in = h * kHalfN + lane * kLaneCols;  // first column of this lane in the tile
+        const int64_t n0 = col0 + n0_in;
         const bool cols_ok = n0 < p.N;  // N % 16 == 0: a lane's 4 columns are all in or all out
-        // this warp's register item (if any), requested before the wait
-        const int i_reg = R + warp;
-        const bool has_reg = warp < n_reg;
+        // this pair's register block (if any), requested before the wait
+        const int j_reg = R + g;
+        const bool has_reg = g < n_reg;
         uint32_t wr[kBlk];
         float4 sr = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         if (has_reg) {
-            const int b = b0 + (i_reg >> 1);
+            const int b = b0 + j_reg;
             const int64_t k0 = static_cast<int64_t>(b) * kBlk;
             const int8_t *wp = p.W + k0 * p.N + n0;
 #pragma unroll
@@ -321,34 +333,33 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         pdl_wait();
         const int64_t k0 = static_cast<int64_t>(b0) * kBlk;
-        const int nk = (b1 - b0) * kBlk;
+        const int nk = len * kBlk;
         for (int i = threadIdx.x; i < nk; i += kConsumerThreads)
             a_s[i] = (k0 + i < p.K) ? __ldg(p.A + k0 + i) : 0.0f;
         consumers_sync();
 
-        // the register item first: it is on chip already, and its registers are
-        // free for the ring items afterwards
-        if (has_reg) block_dot(a_s + (i_reg >> 1) * kBlk, wr, sr, acc);
-        for (int i = warp; i < items; i += kConsumerWarps) {
-            if (i >= R && i < R + n_reg) continue;
-            const float *a_blk = a_s + (i >> 1) * kBlk;
-            const int r_item = i < R ? i : i - n_reg;
-            const int s = r_item % R;
-            const uint32_t use = static_cast<uint32_t>(r_item / R);
+        // the register block first: it is on chip already, and its registers are
+        // free for the ring blocks afterwards
+        if (has_reg) block_dot(a_s + j_reg * kBlk, wr, sr, acc);
+        for (int j = g; j < len; j += kPairs) {
+            if (j >= R && j < R + n_reg) continue;
+            const int r = j < R ? j : j - n_reg;
+            const int s = r % R;
+            const uint32_t use = static_cast<uint32_t>(r / R);
             if (*abort_flag || !mbar_wait(full + s, use & 1u, abort_flag, p.wait_ns)) {
                 if (!*abort_flag && lane == 0) atomicOr(p.err, kErrFullTimeout);
                 s_abort = 1;
                 break;
             }
             const unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
-            const uint32_t *wl = reinterpret_cast<const uint32_t *>(st) + lane;
+            const uint32_t *wl = reinterpret_cast<const uint32_t *>(st + n0_in);
             uint32_t w[kBlk];
 #pragma unroll
-            for (int r = 0; r < kBlk; ++r) w[r] = wl[r * (kHalfN / 4)];
-            const float4 s4 = reinterpret_cast<const float4 *>(st + kWBytes)[lane];
-            block_dot(a_blk, w, s4, acc);
+            for (int r = 0; r < kBlk; ++r) w[r] = wl[r * (kTileN / 4)];
+            const float4 s4 = *reinterpret_cast<const float4 *>(st + kWBytes + 4 * n0_in);
+            block_dot(a_s + j * kBlk, w, s4, acc);
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty + s);  // the stage may be refilled
+            if (lane == 0) mbar_arrive(empty + s);  // this warp's half of the stage may be refilled
         }
     }
 

@@ -35,11 +35,13 @@ def q8():
 @pytest.mark.parametrize("K,N,split", [(1024, 512, 1), (4100, 1024, 4)])
 def test_stream_wait_runs_out_and_the_next_call_is_clean(q8, orc, K, N, split):
     A, W, S = workloads.make_random(K, N, seed=K + N)
-    plan = q8.Plan(K, N, kernel=q8.KERNEL_STREAM, split_k=split, stages=8)
+    plan = q8.Plan(K, N, kernel=q8.KERNEL_STREAM, split_k=split, stages=4)
     plan.set_waits(wait_ns=1_000_000, extra_tx=16)
     run_plan(plan, A, W, S)  # the result is undefined; the call must return
     bits = plan.check()
-    assert bits & 1 and bits & 4, bits          # a stage never completed; the drain ran out too
+    # a stage never completed (seen first by a consumer, 1, or by the producer
+    # waiting for a stage to be released, 2); the final drain ran out too
+    assert bits & (1 | 2) and bits & 4, bits
     assert bits & ~STREAM_BITS == 0, bits
     plan.set_waits(0, 0)
     got, guards = run_plan(plan, A, W, S)

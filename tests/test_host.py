@@ -194,12 +194,12 @@ def test_stream_planner_fits_two_calls_per_sm(q8, K, N):
             assert split == min(16, KB) or tiles * (split + 1) > sms
         else:
             assert split == min_split
-        # a ring of half-block stages, a multiple of 8 deep, and the activations
+        # a ring of block stages, a multiple of 4 deep, and the activations
         # within half of a 228 KiB SM (1 KiB reserved per CTA)
         stages = c["stages"]
-        assert stages % 8 == 0 and 8 <= stages <= 24
-        assert stages <= max(8, -(-2 * bps // 8) * 8)
-        assert 1024 + stages * 4608 + bps * 128 <= 228 * 1024 // 2 - 1024
+        assert stages % 4 == 0 and 4 <= stages <= 24
+        assert stages <= max(4, -(-bps // 4) * 4)
+        assert 1024 + stages * 9216 + bps * 128 <= 228 * 1024 // 2 - 1024
 
 
 def test_stream_planner_rejects_shapes_it_cannot_stream(q8):
@@ -208,7 +208,7 @@ def test_stream_planner_rejects_shapes_it_cannot_stream(q8):
             q8.choose_config(K, N, 152, 0, 0, kernel=q8.KERNEL_STREAM)
     with pytest.raises(q8.Q8mvError):
         q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, split_k=17)
-    for stages in (4, 12, 25, 32):  # a multiple of 8, at most 24
+    for stages in (2, 6, 25, 28):  # a multiple of 4, at most 24
         with pytest.raises(q8.Q8mvError):
             q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, stages=stages)
     with pytest.raises(q8.Q8mvError):
@@ -216,8 +216,8 @@ def test_stream_planner_rejects_shapes_it_cannot_stream(q8):
 
 
 def test_stream_planner_takes_forced_split_and_stages(q8):
-    c = q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, split_k=4, stages=16)
-    assert c["split_k"] == 4 and c["stages"] == 16 and c["blocks_per_split"] == 32
+    c = q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, split_k=4, stages=8)
+    assert c["split_k"] == 4 and c["stages"] == 8 and c["blocks_per_split"] == 32
 
 
 # ----------------------------------------------------------------------------
