@@ -19,29 +19,35 @@
 // requests only after its activations are known would queue behind the next
 // call's early requests, so as much as possible is requested up front: a
 // ring of up to 12 blocks in shared memory, and 4 more blocks held in the
-// consumer warps' registers.  One thread issuing tensor copies from DRAM
-// manages about one copy every 350 ns (measured), far below a CTA's share
-// of the bandwidth, so several lanes of the producer warp issue copies.
+// consumer warps' registers.  The tensor-memory accelerator delivers about
+// 5 to 7 box copies per microsecond to an SM, and one issuing thread about
+// one copy every 350 ns (both measured), so copies are large (two blocks of
+// a 256-column tile, 16 KiB, and their 2 KiB of scales) and several lanes of
+// the producer warp issue them.  Waiting threads sleep in mbarrier.try_wait
+// (suspend-time hint) instead of spinning, so they do not take issue slots
+// from the call that is computing.
 //
 // Work: CTA (t, q) owns the 256-column tile t and the contiguous block range
-// [q*KB/split, (q+1)*KB/split) of K (blocks j = 0 .. len-1 of the range).
-//   * Consumer warps come in four pairs; warp w is in pair g = w / 2 and works
-//     on column half h = w % 2 of the tile (128 columns; lane l owns columns
-//     128h + 4l .. +3).  Pair g takes the blocks j = g, g+4, g+8, ...  Blocks
-//     below R (the ring depth, a multiple of 4) come through the ring; the
-//     next 4 blocks are loaded by their pair straight into registers before
-//     the grid-dependency wait, and are the first each warp multiplies; any
-//     later block comes through the ring again.
-//   * Producer lanes issue, per ring block, two 2D tensor copies into the
-//     block's stage: the 32 x 256 weight bytes (8 KiB) and the 256 scales
-//     (1 KiB), completing on the stage's "full" mbarrier.  Rows at or past K
+// [q*KB/split, (q+1)*KB/split) of K (blocks j = 0 .. len-1 of the range), in
+// units of two blocks (unit u = blocks 2u, 2u+1).
+//   * The consumer warps come in two groups of four; warp w is in group
+//     G = w / 4, takes block 2u + (w / 2) % 2 of each unit u it works on, and
+//     column half h = w % 2 of the tile (128 columns; lane l owns columns
+//     128h + 4l .. +3).  Group G takes the units u = G, G+2, G+4, ...  Units
+//     below R (the ring depth, even) come through the ring; the next 2 units
+//     are loaded by their group straight into registers before the
+//     grid-dependency wait, and are the first each warp multiplies; any later
+//     unit comes through the ring again.
+//   * Producer lanes issue, per ring unit, two 2D tensor copies into the
+//     unit's stage: the 64 x 256 weight bytes (16 KiB) and the 2 x 256 scales
+//     (2 KiB), completing on the stage's "full" mbarrier.  Rows at or past K
 //     and columns at or past N lie outside the tensor maps and arrive as zeros
-//     without being read.  Ring block r sits in stage r % R.  Since R is a
-//     multiple of 4, a stage always belongs to the same warp pair, which
-//     takes its uses in order, and (R being a multiple of the number of
-//     issuing lanes) to the same issuing lane, so every parity wait is
-//     unambiguous.  A stage is refilled once both warps of its pair have
-//     released it ("empty").
+//     without being read; a unit's second block past the range end is loaded
+//     but not used.  Ring unit r sits in stage r % R.  Since R is even, a
+//     stage always belongs to the same warp group, which takes its uses in
+//     order, and (R being a multiple of the number of issuing lanes) to the
+//     same issuing lane, so every parity wait is unambiguous.  A stage is
+//     refilled once all four warps of its group have released it ("empty").
 //   * The consumers wait for the previous grid (griddepcontrol.wait), stage
 //     the CTA's activations in shared memory (zeros past K) and then, per
 //     block, read each of the 32 rows of their half with one 4-byte shared
@@ -73,20 +79,23 @@ constexpr int kBlk = 32;
 constexpr int kTileN = 256;                          // columns per CTA: one TMA box wide
 constexpr int kHalfN = 128;                          // columns per consumer warp
 constexpr int kLaneCols = kHalfN / 32;               // 4 columns per consumer lane
+constexpr int kUnitBlocks = 2;                       // blocks per ring stage (one tensor copy)
 constexpr int kConsumerWarps = 8;
-constexpr int kPairs = kConsumerWarps / 2;           // warp pairs: the two halves of a block
+constexpr int kGroups = 2;                           // warp groups: a unit's two blocks x two halves each
+constexpr int kGroupWarps = kConsumerWarps / kGroups;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;      // + one producer warp
-constexpr int kWBytes = kBlk * kTileN;               // 8192
-constexpr int kSBytes = kTileN * 4;                  // 1024
-constexpr int kStageBytes = kWBytes + kSBytes;       // 9216, a multiple of 128
-constexpr int kMaxStages = 24;                       // ring depth: a multiple of kPairs
-constexpr int kRegBlocks = kPairs;                   // blocks held in registers, one per pair
+constexpr int kWBytes = kUnitBlocks * kBlk * kTileN; // 16384
+constexpr int kSBytes = kUnitBlocks * kTileN * 4;    // 2048
+constexpr int kStageBytes = kWBytes + kSBytes;       // 18432, a multiple of 128
+constexpr int kMaxStages = 12;                       // ring depth: a multiple of kGroups
+constexpr int kRegUnits = kGroups;                   // units held in registers, one per group
 constexpr int kMaxIssuers = 8;                       // producer lanes issuing copies
 constexpr int kBarBytes = 1024;                      // mbarriers and the abort word, ahead of the ring
 constexpr int kMaxBlocksPerCta = 128;                // the CTA's activations, staged whole: <= 16 KiB
 constexpr int kMaxSplit = 16;                        // largest cluster (non-portable size)
 constexpr uint64_t kWaitNs = 2000000000ull;          // bound on any single wait
+constexpr uint32_t kSuspendNs = 20000;               // a waiting thread sleeps up to this long per try
 
 // error bits recorded in the device error word
 constexpr int kErrFullTimeout = 1;   // a stage's copies did not land in time
@@ -94,16 +103,16 @@ constexpr int kErrEmptyTimeout = 2;  // a stage was not released in time
 constexpr int kErrDrainTimeout = 4;  // copies in flight did not land in time at the end
 
 static_assert(kStageBytes % 128 == 0, "stages keep the 128-byte alignment of tensor copies");
-static_assert(kMaxStages % kPairs == 0, "a stage must always belong to one warp pair");
+static_assert(kMaxStages % kGroups == 0, "a stage must always belong to one warp group");
 constexpr int kAbortOff = 2 * kMaxStages * 8;        // the CTA's abort word, after the mbarriers
 static_assert(kAbortOff + 4 <= kBarBytes, "mbarriers and the abort word fit their area");
-// the reduction at the end reuses the first stages
-static_assert(kConsumerWarps * kHalfN * 4 + kTileN * 4 <= kPairs * kStageBytes, "reduction fits");
+// the reduction at the end reuses the first stage
+static_assert(kConsumerWarps * kHalfN * 4 + kTileN * 4 <= kStageBytes, "reduction fits");
 
 // Producer lanes that issue copies for a ring of R stages: the most (at most
 // kMaxIssuers) that divide R, so that every stage has one issuing lane.
 __host__ __device__ constexpr int issuers_for(int R) {
-    return R % 8 == 0 ? 8 : R % 6 == 0 ? 6 : R % 4 == 0 ? 4 : R % 3 == 0 ? 3 : R % 2 == 0 ? 2 : 1;
+    return R % 8 == 0 ? 8 : R % 6 == 0 ? 6 : R % 5 == 0 ? 5 : R % 4 == 0 ? 4 : R % 3 == 0 ? 3 : R % 2 == 0 ? 2 : 1;
 }
 
 struct Params {
@@ -153,26 +162,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return done != 0;
 }
 
-// Wait for the phase of the given parity.  False when the CTA is aborting
-// (abort_flag set, if given) or wait_ns of %globaltimer pass first.
+// Wait for the phase of the given parity.  Each try sleeps until the phase
+// completes or kSuspendNs pass; between tries the CTA's abort word and the
+// bound are checked.  False when the CTA is aborting (abort_flag set, if
+// given) or wait_ns of %globaltimer pass first.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort_flag,
                                           uint64_t wait_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    for (uint32_t i = 1;; ++i) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15u) == 0) {
-            if (abort_flag != nullptr && *abort_flag) return false;
-            if (global_ns() - t0 > wait_ns) return false;
-        }
+        if (abort_flag != nullptr && *abort_flag) return false;
+        if (global_ns() - t0 > wait_ns) return false;
     }
 }
 
@@ -235,7 +244,7 @@ __device__ __forceinline__ uint32_t ldg_stream_u32(const int8_t *p) {
 }
 
 // Shared memory: [mbarriers full[R], empty[R]; abort word] [ring: R stages of
-// a block's W and S] [activations: the CTA's blocks, 128 bytes each].
+// a unit's W and S] [activations: the CTA's blocks, 128 bytes each].
 template <bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 2)
     q8mv_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
@@ -256,15 +265,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int b0 = static_cast<int>(static_cast<int64_t>(q) * p.KB / p.split);
     const int b1 = static_cast<int>(static_cast<int64_t>(q + 1) * p.KB / p.split);
     const int len = b1 - b0;
-    // blocks R .. R + n_reg - 1 are held in registers; the rest go through the ring
-    const int n_reg = min(kRegBlocks, max(0, len - R));
-    const int ring_blocks = len - n_reg;
+    const int units = (len + kUnitBlocks - 1) / kUnitBlocks;
+    // units R .. R + n_reg - 1 are held in registers; the rest go through the ring
+    const int n_reg = min(kRegUnits, max(0, units - R));
+    const int ring_units = units - n_reg;
     const int64_t col0 = t * kTileN;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < R; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, 2);  // both warps of the stage's pair release it
+            mbar_init(empty + s, kGroupWarps);  // every warp of the stage's group releases it
         }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -278,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------------- producer
-        // lane l issues the ring blocks r = l, l + n_iss, ... (stages l, l + n_iss, ...)
+        // lane l issues the ring units r = l, l + n_iss, ... (stages l, l + n_iss, ...)
         const int n_iss = issuers_for(R);
         if (lane < n_iss) {
             if (lane == 0) {
@@ -286,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 prefetch_tensormap(&tmS);
             }
             int last = -1;
-            for (int r = lane; r < ring_blocks; r += n_iss) {
+            for (int r = lane; r < ring_units; r += n_iss) {
                 const int s = r % R;
                 const uint32_t use = static_cast<uint32_t>(r / R);
                 if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1u, abort_flag, p.wait_ns)) {
@@ -295,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     break;
                 }
                 if (*abort_flag) break;
-                const int b = b0 + (r < R ? r : r + n_reg);  // register blocks are skipped
+                const int b = b0 + kUnitBlocks * (r < R ? r : r + n_reg);  // register units are skipped
                 unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
                 mbar_arrive_expect_tx(full + s, kStageBytes + p.extra_tx);
                 tma_load_2d(st, &tmW, static_cast<int>(col0), b * kBlk, full + s);
@@ -312,14 +322,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // -------------------------------------------------------- consumers
-        const int g = warp >> 1;
-        const int h = warp & 1;
+        const int G = warp / kGroupWarps;
+        const int bi = (warp >> 1) & 1;  // which block of a unit
+        const int h = warp & 1;          // which half of the tile
         const int n0_in = h * kHalfN + lane * kLaneCols;  // first column of this lane in the tile
         const int64_t n0 = col0 + n0_in;
         const bool cols_ok = n0 < p.N;  // N % 16 == 0: a lane's 4 columns are all in or all out
-        // this pair's register block (if any), requested before the wait
-        const int j_reg = R + g;
-        const bool has_reg = g < n_reg;
+        // this group's register unit (if any), requested before the wait
+        const int j_reg = kUnitBlocks * (R + G) + bi;
+        const bool has_reg = G < n_reg && j_reg < len;
         uint32_t wr[kBlk];
         float4 sr = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         if (has_reg) {
@@ -338,12 +349,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             a_s[i] = (k0 + i < p.K) ? __ldg(p.A + k0 + i) : 0.0f;
         consumers_sync();
 
-        // the register block first: it is on chip already, and its registers are
-        // free for the ring blocks afterwards
+        // the register unit first: it is on chip already, and its registers are
+        // free for the ring units afterwards
         if (has_reg) block_dot(a_s + j_reg * kBlk, wr, sr, acc);
-        for (int j = g; j < len; j += kPairs) {
-            if (j >= R && j < R + n_reg) continue;
-            const int r = j < R ? j : j - n_reg;
+        for (int u = G; u < units; u += kGroups) {
+            if (u >= R && u < R + n_reg) continue;
+            const int r = u < R ? u : u - n_reg;
             const int s = r % R;
             const uint32_t use = static_cast<uint32_t>(r / R);
             if (*abort_flag || !mbar_wait(full + s, use & 1u, abort_flag, p.wait_ns)) {
@@ -351,20 +362,23 @@ __global__ void __launch_bounds__(kThreads, 2)
                 s_abort = 1;
                 break;
             }
-            const unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
-            const uint32_t *wl = reinterpret_cast<const uint32_t *>(st + n0_in);
-            uint32_t w[kBlk];
+            const int j = kUnitBlocks * u + bi;
+            if (j < len) {
+                const unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
+                const uint32_t *wl = reinterpret_cast<const uint32_t *>(st + bi * (kBlk * kTileN) + n0_in);
+                uint32_t w[kBlk];
 #pragma unroll
-            for (int r = 0; r < kBlk; ++r) w[r] = wl[r * (kTileN / 4)];
-            const float4 s4 = *reinterpret_cast<const float4 *>(st + kWBytes + 4 * n0_in);
-            block_dot(a_s + j * kBlk, w, s4, acc);
+                for (int r = 0; r < kBlk; ++r) w[r] = wl[r * (kTileN / 4)];
+                const float4 s4 = *reinterpret_cast<const float4 *>(st + kWBytes + 4 * (bi * kTileN + n0_in));
+                block_dot(a_s + j * kBlk, w, s4, acc);
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty + s);  // this warp's half of the stage may be refilled
+            if (lane == 0) mbar_arrive(empty + s);  // this warp's part of the stage may be refilled
         }
     }
 
-    // ---- sum the warps' accumulators in warp order (the first stages are
-    // free: every copy has landed and every stage has been consumed or abandoned)
+    // ---- sum the warps' accumulators in warp order (the first stage is free:
+    // every copy has landed and every stage has been consumed or abandoned)
     __syncthreads();
     float *red = reinterpret_cast<float *>(ring);  // [kConsumerWarps][kHalfN]
     if (warp < kConsumerWarps)

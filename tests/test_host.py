@@ -194,12 +194,13 @@ def test_stream_planner_fits_two_calls_per_sm(q8, K, N):
             assert split == min(16, KB) or tiles * (split + 1) > sms
         else:
             assert split == min_split
-        # a ring of block stages, a multiple of 4 deep, and the activations
+        # a ring of two-block stages, an even number deep, and the activations
         # within half of a 228 KiB SM (1 KiB reserved per CTA)
         stages = c["stages"]
-        assert stages % 4 == 0 and 4 <= stages <= 24
-        assert stages <= max(4, -(-bps // 4) * 4)
-        assert 1024 + stages * 9216 + bps * 128 <= 228 * 1024 // 2 - 1024
+        units = -(-bps // 2)
+        assert stages % 2 == 0 and 2 <= stages <= 12
+        assert stages <= max(2, -(-units // 2) * 2)
+        assert 1024 + stages * 18432 + bps * 128 <= 228 * 1024 // 2 - 1024
 
 
 def test_stream_planner_rejects_shapes_it_cannot_stream(q8):
@@ -208,7 +209,7 @@ def test_stream_planner_rejects_shapes_it_cannot_stream(q8):
             q8.choose_config(K, N, 152, 0, 0, kernel=q8.KERNEL_STREAM)
     with pytest.raises(q8.Q8mvError):
         q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, split_k=17)
-    for stages in (2, 6, 25, 28):  # a multiple of 4, at most 24
+    for stages in (1, 3, 14, 24):  # even, at most 12
         with pytest.raises(q8.Q8mvError):
             q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, stages=stages)
     with pytest.raises(q8.Q8mvError):
@@ -216,8 +217,8 @@ def test_stream_planner_rejects_shapes_it_cannot_stream(q8):
 
 
 def test_stream_planner_takes_forced_split_and_stages(q8):
-    c = q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, split_k=4, stages=8)
-    assert c["split_k"] == 4 and c["stages"] == 8 and c["blocks_per_split"] == 32
+    c = q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, split_k=4, stages=4)
+    assert c["split_k"] == 4 and c["stages"] == 4 and c["blocks_per_split"] == 32
 
 
 # ----------------------------------------------------------------------------
