@@ -98,8 +98,8 @@ typedef struct {
     int32_t threads_n; /* threads along N in one CTA: 32, 64, 128 or 256 */
     int32_t split_k;   /* K ranges per column tile, each summed by one CTA (>= 1; the streaming
                           kernel takes 1 .. 16, the cluster size) */
-    int32_t stages;    /* streaming kernel: ring depth, an even number from 2 to 12 stages of two
-                          32 x 256 blocks */
+    int32_t stages;    /* streaming kernel: ring depth, 8, 16 or 24 stages of one 32 x 256 block
+                          (as shared memory allows) */
     int32_t overlap;   /* 1: launch with programmatic dependent launch, so a call starts while the
                           previous kernel in its stream finishes and reads W and S before that kernel
                           has completed (A is read and C written only after it).  Only for weights

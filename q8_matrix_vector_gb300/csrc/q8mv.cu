@@ -394,22 +394,22 @@ bool encode_result(int which, CUresult r) {
     return false;
 }
 
-// W as a 2D map [K rows][N bytes], box 64 rows x 256 columns (two blocks of a tile).
+// W as a 2D map [K rows][N bytes], box 32 rows x 256 columns (one block of a tile).
 bool encode_w(CUtensorMap *m, const int8_t *W, int64_t K, int64_t N) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N)};
-    const cuuint32_t box[2] = {sk::kTileN, sk::kUnitBlocks * sk::kBlk};
+    const cuuint32_t box[2] = {sk::kTileN, sk::kBlk};
     const cuuint32_t elem[2] = {1, 1};
     return encode_result(1, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(W), dims, strides,
                                         box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
 }
 
-// S as a 2D map [KB rows][N floats], box 2 rows x 256 columns.
+// S as a 2D map [KB rows][N floats], box 1 row x 256 columns.
 bool encode_s(CUtensorMap *m, const float *S, int64_t KB, int64_t N) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(KB)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
-    const cuuint32_t box[2] = {sk::kTileN, sk::kUnitBlocks};
+    const cuuint32_t box[2] = {sk::kTileN, 1};
     const cuuint32_t elem[2] = {1, 1};
     return encode_result(2, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(S), dims, strides,
                                         box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -468,9 +468,9 @@ size_t stream_budget(size_t smem_per_sm, size_t reserved_per_cta, size_t static_
 // at least enough K ranges that one range's activations fit in 16 KiB.  When
 // `max_clusters` is given (max_clusters[s]: clusters of s CTAs that can be
 // resident at once), a split is taken only if two calls' clusters fit
-// together.  The ring of two-block stages is an even number deep (each stage
-// belongs to one group of consumer warps), as deep as `budget` bytes of
-// shared memory allow, and no deeper than the longest range's units need.
+// together.  The ring of block stages is a multiple of 8 deep (each stage
+// belongs to one consumer warp), as deep as `budget` bytes of shared memory
+// allow, and no deeper than the longest range needs.
 q8mv_status_t choose_stream(int64_t K, int64_t N, int sm_count, size_t budget, const int *max_clusters,
                             int want_split, int want_stages, StreamConfig *out) {
     *out = StreamConfig{};
@@ -495,7 +495,7 @@ q8mv_status_t choose_stream(int64_t K, int64_t N, int sm_count, size_t budget, c
     c.split = static_cast<int>(split);
     c.max_len = static_cast<int>(ceil_div(KB, split));
     const size_t fixed = stream_smem(0, c.max_len);
-    constexpr int step = sk::kGroups;  // a stage always belongs to one group of consumer warps
+    constexpr int step = sk::kConsumerWarps;  // a stage always belongs to one consumer warp
     int stages = 0;
     if (want_stages != 0) {
         if (want_stages < step || want_stages > sk::kMaxStages || want_stages % step != 0 ||
@@ -506,9 +506,8 @@ q8mv_status_t choose_stream(int64_t K, int64_t N, int sm_count, size_t budget, c
         if (fixed + static_cast<size_t>(step) * sk::kStageBytes > budget) return Q8MV_ERR_INVALID_ARG;
         stages = static_cast<int>(std::min<size_t>(sk::kMaxStages, (budget - fixed) / sk::kStageBytes));
         stages -= stages % step;
-        // no deeper than the longest range's units need
-        const int64_t units = ceil_div(static_cast<int64_t>(c.max_len), sk::kUnitBlocks);
-        const int need = static_cast<int>(ceil_div(units, step) * step);
+        // no deeper than the longest range needs
+        const int need = static_cast<int>(ceil_div(static_cast<int64_t>(c.max_len), step) * step);
         stages = std::min(stages, std::max(step, need));
     }
     c.stages = stages;

@@ -18,42 +18,37 @@
 // already there; it stages its activations and multiplies.  Weights a CTA
 // requests only after its activations are known would queue behind the next
 // call's early requests, so as much as possible is requested up front: a
-// ring of up to 12 blocks in shared memory, and 4 more blocks held in the
-// consumer warps' registers.  The tensor-memory accelerator delivers about
-// 5 to 7 box copies per microsecond to an SM, and one issuing thread about
-// one copy every 350 ns (both measured), so copies are large (two blocks of
-// a 256-column tile, 16 KiB, and their 2 KiB of scales) and several lanes of
-// the producer warp issue them.  Waiting threads sleep in mbarrier.try_wait
+// ring of 8 blocks in shared memory, and 8 more blocks held in the consumer
+// warps' registers.  The tensor-memory accelerator delivers about one box
+// copy per 350 ns to each issuing thread (measured), so several lanes of the
+// producer warp issue them.  Waiting threads sleep in mbarrier.try_wait
 // (suspend-time hint) instead of spinning, so they do not take issue slots
-// from the call that is computing.
+// from the call that is computing.  Once the activations are known, the
+// multiply is the critical path; each consumer lane owns 8 columns, so it
+// runs four independent packed-FMA chains.
 //
 // Work: CTA (t, q) owns the 256-column tile t and the contiguous block range
-// [q*KB/split, (q+1)*KB/split) of K (blocks j = 0 .. len-1 of the range), in
-// units of two blocks (unit u = blocks 2u, 2u+1).
-//   * The consumer warps come in two groups of four; warp w is in group
-//     G = w / 4, takes block 2u + (w / 2) % 2 of each unit u it works on, and
-//     column half h = w % 2 of the tile (128 columns; lane l owns columns
-//     128h + 4l .. +3).  Group G takes the units u = G, G+2, G+4, ...  Units
-//     below R (the ring depth, even) come through the ring; the next 2 units
-//     are loaded by their group straight into registers before the
-//     grid-dependency wait, and are the first each warp multiplies; any later
-//     unit comes through the ring again.
-//   * Producer lanes issue, per ring unit, two 2D tensor copies into the
-//     unit's stage: the 64 x 256 weight bytes (16 KiB) and the 2 x 256 scales
-//     (2 KiB), completing on the stage's "full" mbarrier.  Rows at or past K
+// [q*KB/split, (q+1)*KB/split) of K (blocks j = 0 .. len-1 of the range).
+//   * Consumer warp w takes the blocks j = w, w+8, w+16, ...; lane l owns
+//     columns 8l .. 8l+7 of the tile.  Blocks below R (the ring depth, 8)
+//     come through the ring; the next 8 blocks are loaded by their warp
+//     straight into registers before the grid-dependency wait, and are the
+//     first each warp multiplies; any later block comes through the ring
+//     again.
+//   * Producer lanes issue, per ring block, two 2D tensor copies into the
+//     block's stage: the 32 x 256 weight bytes (8 KiB) and the 256 scales
+//     (1 KiB), completing on the stage's "full" mbarrier.  Rows at or past K
 //     and columns at or past N lie outside the tensor maps and arrive as zeros
-//     without being read; a unit's second block past the range end is loaded
-//     but not used.  Ring unit r sits in stage r % R.  Since R is even, a
-//     stage always belongs to the same warp group, which takes its uses in
-//     order, and (R being a multiple of the number of issuing lanes) to the
-//     same issuing lane, so every parity wait is unambiguous.  A stage is
-//     refilled once all four warps of its group have released it ("empty").
+//     without being read.  Ring block r sits in stage r % R.  Since R is a
+//     multiple of 8, a stage always belongs to the same warp, which takes its
+//     uses in order, and to the same issuing lane, so every parity wait is
+//     unambiguous.  A stage is refilled once its warp has released it
+//     ("empty").
 //   * The consumers wait for the previous grid (griddepcontrol.wait), stage
 //     the CTA's activations in shared memory (zeros past K) and then, per
-//     block, read each of the 32 rows of their half with one 4-byte shared
-//     load, convert the bytes to f32 exactly, accumulate the block's sum in
-//     row order with packed f32x2 FMAs and fold the block's scale once per
-//     column.
+//     block, read each of the 32 rows with one 8-byte shared load, convert
+//     the bytes to f32 exactly, accumulate the block's sum in row order with
+//     packed f32x2 FMAs and fold the block's scale once per column.
 //   * At the end the warps' accumulators are summed in warp order through
 //     shared memory.  With split > 1 the tile's CTAs form one thread-block
 //     cluster: after a cluster barrier CTA r sums slice r of the columns over
@@ -77,19 +72,15 @@ namespace sk {
 
 constexpr int kBlk = 32;
 constexpr int kTileN = 256;                          // columns per CTA: one TMA box wide
-constexpr int kHalfN = 128;                          // columns per consumer warp
-constexpr int kLaneCols = kHalfN / 32;               // 4 columns per consumer lane
-constexpr int kUnitBlocks = 2;                       // blocks per ring stage (one tensor copy)
+constexpr int kLaneCols = kTileN / 32;               // 8 columns per consumer lane
 constexpr int kConsumerWarps = 8;
-constexpr int kGroups = 2;                           // warp groups: a unit's two blocks x two halves each
-constexpr int kGroupWarps = kConsumerWarps / kGroups;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;      // + one producer warp
-constexpr int kWBytes = kUnitBlocks * kBlk * kTileN; // 16384
-constexpr int kSBytes = kUnitBlocks * kTileN * 4;    // 2048
-constexpr int kStageBytes = kWBytes + kSBytes;       // 18432, a multiple of 128
-constexpr int kMaxStages = 12;                       // ring depth: a multiple of kGroups
-constexpr int kRegUnits = kGroups;                   // units held in registers, one per group
+constexpr int kWBytes = kBlk * kTileN;               // 8192
+constexpr int kSBytes = kTileN * 4;                  // 1024
+constexpr int kStageBytes = kWBytes + kSBytes;       // 9216, a multiple of 128
+constexpr int kMaxStages = 24;                       // ring depth: a multiple of kConsumerWarps
+constexpr int kRegBlocks = kConsumerWarps;           // blocks held in registers, one per warp
 constexpr int kMaxIssuers = 8;                       // producer lanes issuing copies
 constexpr int kBarBytes = 1024;                      // mbarriers and the abort word, ahead of the ring
 constexpr int kMaxBlocksPerCta = 128;                // the CTA's activations, staged whole: <= 16 KiB
@@ -103,11 +94,11 @@ constexpr int kErrEmptyTimeout = 2;  // a stage was not released in time
 constexpr int kErrDrainTimeout = 4;  // copies in flight did not land in time at the end
 
 static_assert(kStageBytes % 128 == 0, "stages keep the 128-byte alignment of tensor copies");
-static_assert(kMaxStages % kGroups == 0, "a stage must always belong to one warp group");
+static_assert(kMaxStages % kConsumerWarps == 0, "a stage must always belong to one warp");
 constexpr int kAbortOff = 2 * kMaxStages * 8;        // the CTA's abort word, after the mbarriers
 static_assert(kAbortOff + 4 <= kBarBytes, "mbarriers and the abort word fit their area");
 // the reduction at the end reuses the first stage
-static_assert(kConsumerWarps * kHalfN * 4 + kTileN * 4 <= kStageBytes, "reduction fits");
+static_assert(kConsumerWarps * kTileN * 4 + kTileN * 4 <= kStageBytes, "reduction fits");
 
 // Producer lanes that issue copies for a ring of R stages: the most (at most
 // kMaxIssuers) that divide R, so that every stage has one issuing lane.
@@ -211,40 +202,74 @@ __device__ __forceinline__ float2 cvt2(uint32_t flipped, uint32_t sel_lo, uint32
     return __fadd2_rn(t, make_float2(-8388736.0f, -8388736.0f));
 }
 
-// part[0..4) += a * (4 signed bytes in w)
-__device__ __forceinline__ void fma_row4(float a, uint32_t w, float2 (&part)[2]) {
+// part[0..8) += a * (8 signed bytes in w)
+__device__ __forceinline__ void fma_row8(float a, uint2 w, float2 (&part)[4]) {
     const float2 a2 = make_float2(a, a);
-    const uint32_t u = w ^ 0x80808080u;
-    part[0] = __ffma2_rn(a2, cvt2(u, 0x7440u, 0x7441u), part[0]);
-    part[1] = __ffma2_rn(a2, cvt2(u, 0x7442u, 0x7443u), part[1]);
+    const uint32_t u0 = w.x ^ 0x80808080u;
+    const uint32_t u1 = w.y ^ 0x80808080u;
+    part[0] = __ffma2_rn(a2, cvt2(u0, 0x7440u, 0x7441u), part[0]);
+    part[1] = __ffma2_rn(a2, cvt2(u0, 0x7442u, 0x7443u), part[1]);
+    part[2] = __ffma2_rn(a2, cvt2(u1, 0x7440u, 0x7441u), part[2]);
+    part[3] = __ffma2_rn(a2, cvt2(u1, 0x7442u, 0x7443u), part[3]);
 }
 
-// A block's 32 rows of a lane's 4 columns (row r in w[r]) against the block's
+// A block's 32 rows of a lane's 8 columns (row r in w[r]) against the block's
 // activations a_blk, then acc += part * s: the block sum in row order, one
 // scale fold per column ("Factoring out the scale").
-__device__ __forceinline__ void block_dot(const float *a_blk, const uint32_t (&w)[kBlk], float4 s,
-                                          float2 (&acc)[2]) {
-    float2 part[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+__device__ __forceinline__ void block_dot(const float *a_blk, const uint2 (&w)[kBlk], float4 s0, float4 s1,
+                                          float2 (&acc)[4]) {
+    float2 part[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) part[c] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int r = 0; r < kBlk; r += 4) {
         const float4 a4 = *reinterpret_cast<const float4 *>(a_blk + r);
-        fma_row4(a4.x, w[r + 0], part);
-        fma_row4(a4.y, w[r + 1], part);
-        fma_row4(a4.z, w[r + 2], part);
-        fma_row4(a4.w, w[r + 3], part);
+        fma_row8(a4.x, w[r + 0], part);
+        fma_row8(a4.y, w[r + 1], part);
+        fma_row8(a4.z, w[r + 2], part);
+        fma_row8(a4.w, w[r + 3], part);
     }
-    acc[0] = __ffma2_rn(part[0], make_float2(s.x, s.y), acc[0]);
-    acc[1] = __ffma2_rn(part[1], make_float2(s.z, s.w), acc[1]);
+    acc[0] = __ffma2_rn(part[0], make_float2(s0.x, s0.y), acc[0]);
+    acc[1] = __ffma2_rn(part[1], make_float2(s0.z, s0.w), acc[1]);
+    acc[2] = __ffma2_rn(part[2], make_float2(s1.x, s1.y), acc[2]);
+    acc[3] = __ffma2_rn(part[3], make_float2(s1.z, s1.w), acc[3]);
 }
 
-__device__ __forceinline__ uint32_t ldg_stream_u32(const int8_t *p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.u32 %0, [%1];" : "=r"(v) : "l"(p));
+// The same for a block in a ring stage: rows r at wl[r * 32] (8-byte words),
+// read 8 rows at a time to keep few registers live.
+__device__ __forceinline__ void block_dot_smem(const float *a_blk, const uint2 *wl, float4 s0, float4 s1,
+                                               float2 (&acc)[4]) {
+    float2 part[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) part[c] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int r0 = 0; r0 < kBlk; r0 += 8) {
+        uint2 w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = wl[(r0 + i) * (kTileN / 8)];
+#pragma unroll
+        for (int i = 0; i < 8; i += 4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(a_blk + r0 + i);
+            fma_row8(a4.x, w[i + 0], part);
+            fma_row8(a4.y, w[i + 1], part);
+            fma_row8(a4.z, w[i + 2], part);
+            fma_row8(a4.w, w[i + 3], part);
+        }
+    }
+    acc[0] = __ffma2_rn(part[0], make_float2(s0.x, s0.y), acc[0]);
+    acc[1] = __ffma2_rn(part[1], make_float2(s0.z, s0.w), acc[1]);
+    acc[2] = __ffma2_rn(part[2], make_float2(s1.x, s1.y), acc[2]);
+    acc[3] = __ffma2_rn(part[3], make_float2(s1.z, s1.w), acc[3]);
+}
+
+__device__ __forceinline__ uint2 ldg_stream_u64(const int8_t *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
     return v;
 }
 
 // Shared memory: [mbarriers full[R], empty[R]; abort word] [ring: R stages of
-// a unit's W and S] [activations: the CTA's blocks, 128 bytes each].
+// a block's W and S] [activations: the CTA's blocks, 128 bytes each].
 template <bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, 2)
     q8mv_stream_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmS,
@@ -265,16 +290,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int b0 = static_cast<int>(static_cast<int64_t>(q) * p.KB / p.split);
     const int b1 = static_cast<int>(static_cast<int64_t>(q + 1) * p.KB / p.split);
     const int len = b1 - b0;
-    const int units = (len + kUnitBlocks - 1) / kUnitBlocks;
-    // units R .. R + n_reg - 1 are held in registers; the rest go through the ring
-    const int n_reg = min(kRegUnits, max(0, units - R));
-    const int ring_units = units - n_reg;
+    // blocks R .. R + n_reg - 1 are held in registers; the rest go through the ring
+    const int n_reg = min(kRegBlocks, max(0, len - R));
+    const int ring_blocks = len - n_reg;
     const int64_t col0 = t * kTileN;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < R; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, kGroupWarps);  // every warp of the stage's group releases it
+            mbar_init(empty + s, 1);
         }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -284,11 +308,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     // before its own griddepcontrol.wait
     pdl_launch_dependents();
 
-    float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+    float2 acc[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.0f, 0.0f);
 
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------------- producer
-        // lane l issues the ring units r = l, l + n_iss, ... (stages l, l + n_iss, ...)
+        // lane l issues the ring blocks r = l, l + n_iss, ... (stages l, l + n_iss, ...)
         const int n_iss = issuers_for(R);
         if (lane < n_iss) {
             if (lane == 0) {
@@ -296,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 prefetch_tensormap(&tmS);
             }
             int last = -1;
-            for (int r = lane; r < ring_units; r += n_iss) {
+            for (int r = lane; r < ring_blocks; r += n_iss) {
                 const int s = r % R;
                 const uint32_t use = static_cast<uint32_t>(r / R);
                 if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1u, abort_flag, p.wait_ns)) {
@@ -305,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     break;
                 }
                 if (*abort_flag) break;
-                const int b = b0 + kUnitBlocks * (r < R ? r : r + n_reg);  // register units are skipped
+                const int b = b0 + (r < R ? r : r + n_reg);  // register blocks are skipped
                 unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
                 mbar_arrive_expect_tx(full + s, kStageBytes + p.extra_tx);
                 tma_load_2d(st, &tmW, static_cast<int>(col0), b * kBlk, full + s);
@@ -322,25 +348,27 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // -------------------------------------------------------- consumers
-        const int G = warp / kGroupWarps;
-        const int bi = (warp >> 1) & 1;  // which block of a unit
-        const int h = warp & 1;          // which half of the tile
-        const int n0_in = h * kHalfN + lane * kLaneCols;  // first column of this lane in the tile
+        const int n0_in = lane * kLaneCols;  // first column of this lane in the tile
         const int64_t n0 = col0 + n0_in;
-        const bool cols_ok = n0 < p.N;  // N % 16 == 0: a lane's 4 columns are all in or all out
-        // this group's register unit (if any), requested before the wait
-        const int j_reg = kUnitBlocks * (R + G) + bi;
-        const bool has_reg = G < n_reg && j_reg < len;
-        uint32_t wr[kBlk];
-        float4 sr = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        const bool cols_ok = n0 < p.N;  // N % 16 == 0: a lane's 8 columns are all in or all out
+        // this warp's register block (if any), requested before the wait
+        const int j_reg = R + warp;
+        const bool has_reg = warp < n_reg;
+        uint2 wr[kBlk];
+        float4 sr0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), sr1 = sr0;
         if (has_reg) {
             const int b = b0 + j_reg;
             const int64_t k0 = static_cast<int64_t>(b) * kBlk;
             const int8_t *wp = p.W + k0 * p.N + n0;
 #pragma unroll
             for (int r = 0; r < kBlk; ++r)
-                wr[r] = (cols_ok && k0 + r < p.K) ? ldg_stream_u32(wp + static_cast<int64_t>(r) * p.N) : 0u;
-            if (cols_ok) sr = __ldg(reinterpret_cast<const float4 *>(p.S + static_cast<int64_t>(b) * p.N + n0));
+                wr[r] = (cols_ok && k0 + r < p.K) ? ldg_stream_u64(wp + static_cast<int64_t>(r) * p.N)
+                                                  : make_uint2(0u, 0u);
+            if (cols_ok) {
+                const float4 *sp = reinterpret_cast<const float4 *>(p.S + static_cast<int64_t>(b) * p.N + n0);
+                sr0 = __ldg(sp);
+                sr1 = __ldg(sp + 1);
+            }
         }
         pdl_wait();
         const int64_t k0 = static_cast<int64_t>(b0) * kBlk;
@@ -349,12 +377,12 @@ __global__ void __launch_bounds__(kThreads, 2)
             a_s[i] = (k0 + i < p.K) ? __ldg(p.A + k0 + i) : 0.0f;
         consumers_sync();
 
-        // the register unit first: it is on chip already, and its registers are
-        // free for the ring units afterwards
-        if (has_reg) block_dot(a_s + j_reg * kBlk, wr, sr, acc);
-        for (int u = G; u < units; u += kGroups) {
-            if (u >= R && u < R + n_reg) continue;
-            const int r = u < R ? u : u - n_reg;
+        // the register block first: it is on chip already, and its registers are
+        // free for the ring blocks afterwards
+        if (has_reg) block_dot(a_s + j_reg * kBlk, wr, sr0, sr1, acc);
+        for (int j = warp; j < len; j += kConsumerWarps) {
+            if (j >= R && j < R + n_reg) continue;
+            const int r = j < R ? j : j - n_reg;
             const int s = r % R;
             const uint32_t use = static_cast<uint32_t>(r / R);
             if (*abort_flag || !mbar_wait(full + s, use & 1u, abort_flag, p.wait_ns)) {
@@ -362,42 +390,38 @@ __global__ void __launch_bounds__(kThreads, 2)
                 s_abort = 1;
                 break;
             }
-            const int j = kUnitBlocks * u + bi;
-            if (j < len) {
-                const unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
-                const uint32_t *wl = reinterpret_cast<const uint32_t *>(st + bi * (kBlk * kTileN) + n0_in);
-                uint32_t w[kBlk];
-#pragma unroll
-                for (int r = 0; r < kBlk; ++r) w[r] = wl[r * (kTileN / 4)];
-                const float4 s4 = *reinterpret_cast<const float4 *>(st + kWBytes + 4 * (bi * kTileN + n0_in));
-                block_dot(a_s + j * kBlk, w, s4, acc);
-            }
+            const unsigned char *st = ring + static_cast<size_t>(s) * kStageBytes;
+            const uint2 *wl = reinterpret_cast<const uint2 *>(st + n0_in);
+            const float4 *sl = reinterpret_cast<const float4 *>(st + kWBytes + 4 * n0_in);
+            block_dot_smem(a_s + j * kBlk, wl, sl[0], sl[1], acc);
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty + s);  // this warp's part of the stage may be refilled
+            if (lane == 0) mbar_arrive(empty + s);  // the stage may be refilled
         }
     }
 
     // ---- sum the warps' accumulators in warp order (the first stage is free:
     // every copy has landed and every stage has been consumed or abandoned)
     __syncthreads();
-    float *red = reinterpret_cast<float *>(ring);  // [kConsumerWarps][kHalfN]
-    if (warp < kConsumerWarps)
-        reinterpret_cast<float4 *>(red + warp * kHalfN)[lane] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+    float *red = reinterpret_cast<float *>(ring);  // [kConsumerWarps][kTileN]
+    if (warp < kConsumerWarps) {
+        float4 *mine = reinterpret_cast<float4 *>(red + warp * kTileN + lane * kLaneCols);
+        mine[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+        mine[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+    }
     __syncthreads();
     const int ct = threadIdx.x;  // column of the tile this thread sums (ct < kTileN)
     float v = 0.0f;
     if (ct < kTileN) {
-        const int h = ct / kHalfN, c = ct % kHalfN;
-        v = red[h * kHalfN + c];
+        v = red[ct];
 #pragma unroll
-        for (int w = h + 2; w < kConsumerWarps; w += 2) v += red[w * kHalfN + c];
+        for (int w = 1; w < kConsumerWarps; ++w) v += red[w * kTileN + ct];
     }
 
     if constexpr (CLUSTER) {
         // CTA r of the tile's cluster sums slice r of the columns over the
         // cluster's CTAs in rank order, reading their shared memory directly
         namespace cg = cooperative_groups;
-        float *tile_sum = red + kConsumerWarps * kHalfN;  // [kTileN]
+        float *tile_sum = red + kConsumerWarps * kTileN;  // [kTileN]
         if (ct < kTileN) tile_sum[ct] = v;
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();

@@ -1,9 +1,9 @@
 """GPU parity of the co-resident streaming kernel (plans with kernel=KERNEL_STREAM).
 
-The kernel brings two blocks at a time of a 256-column tile of W (64 rows)
-and their scales into a shared-memory ring with tensor copies issued by
-several lanes (and up to 4 more blocks straight into registers), one CTA per
-SM and call, and sums the K ranges of a tile through a thread-block cluster.  Every result is checked
+The kernel brings each block of a 256-column tile of W (32 rows) and its 256
+scales into a shared-memory ring with tensor copies issued by several lanes
+(and up to 8 more blocks straight into registers), one CTA per SM and call,
+and sums the K ranges of a tile through a thread-block cluster.  Every result is checked
 against the fp64 oracle within |C_gpu - C_ref| <= 1e-5 sum|A W S| + 1e-6 per
 element; inputs whose result is exact in f32 must match bit for bit.
 """
@@ -67,7 +67,7 @@ def test_stream_workloads_full_size(q8, orc, name):
 
 
 @pytest.mark.parametrize("split", [1, 2, 3, 7, 8, 9, 16])
-@pytest.mark.parametrize("stages", [2, 4, 6])
+@pytest.mark.parametrize("stages", [8])
 def test_stream_forced_split_and_ring_depth(q8, orc, split, stages):
     K, N = 4100, 4112  # ragged K (last block of 4 rows) and a ragged last tile
     A, W, S = workloads.make_random(K, N, seed=split * 31 + stages)
@@ -116,7 +116,7 @@ def test_stream_plan_rejects_shapes_it_cannot_stream(q8):
     for K, N in ((0, 4096), (4096, 200), (4096, 8), (65536 + 4096, 256)):
         with pytest.raises(q8.Q8mvError):
             q8.Plan(K, N, kernel=q8.KERNEL_STREAM)
-    for stages in (1, 3, 14):  # even, at most 12
+    for stages in (4, 12, 16):  # a multiple of 8 that fits half an SM
         with pytest.raises(q8.Q8mvError):
             q8.Plan(4096, 4096, kernel=q8.KERNEL_STREAM, stages=stages)
     with pytest.raises(q8.Q8mvError):

@@ -35,7 +35,7 @@ def q8():
 @pytest.mark.parametrize("K,N,split", [(1024, 512, 1), (4100, 1024, 4)])
 def test_stream_wait_runs_out_and_the_next_call_is_clean(q8, orc, K, N, split):
     A, W, S = workloads.make_random(K, N, seed=K + N)
-    plan = q8.Plan(K, N, kernel=q8.KERNEL_STREAM, split_k=split, stages=2)
+    plan = q8.Plan(K, N, kernel=q8.KERNEL_STREAM, split_k=split, stages=8)
     plan.set_waits(wait_ns=1_000_000, extra_tx=16)
     run_plan(plan, A, W, S)  # the result is undefined; the call must return
     bits = plan.check()

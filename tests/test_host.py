@@ -194,13 +194,12 @@ def test_stream_planner_fits_two_calls_per_sm(q8, K, N):
             assert split == min(16, KB) or tiles * (split + 1) > sms
         else:
             assert split == min_split
-        # a ring of two-block stages, an even number deep, and the activations
+        # a ring of block stages, a multiple of 8 deep, and the activations
         # within half of a 228 KiB SM (1 KiB reserved per CTA)
         stages = c["stages"]
-        units = -(-bps // 2)
-        assert stages % 2 == 0 and 2 <= stages <= 12
-        assert stages <= max(2, -(-units // 2) * 2)
-        assert 1024 + stages * 18432 + bps * 128 <= 228 * 1024 // 2 - 1024
+        assert stages % 8 == 0 and 8 <= stages <= 24
+        assert stages <= max(8, -(-bps // 8) * 8)
+        assert 1024 + stages * 9216 + bps * 128 <= 228 * 1024 // 2 - 1024
 
 
 def test_stream_planner_rejects_shapes_it_cannot_stream(q8):
@@ -209,7 +208,7 @@ def test_stream_planner_rejects_shapes_it_cannot_stream(q8):
             q8.choose_config(K, N, 152, 0, 0, kernel=q8.KERNEL_STREAM)
     with pytest.raises(q8.Q8mvError):
         q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, split_k=17)
-    for stages in (1, 3, 14, 24):  # even, at most 12
+    for stages in (4, 12, 16, 32):  # a multiple of 8 that fits half an SM
         with pytest.raises(q8.Q8mvError):
             q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, stages=stages)
     with pytest.raises(q8.Q8mvError):
@@ -217,8 +216,8 @@ def test_stream_planner_rejects_shapes_it_cannot_stream(q8):
 
 
 def test_stream_planner_takes_forced_split_and_stages(q8):
-    c = q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, split_k=4, stages=4)
-    assert c["split_k"] == 4 and c["stages"] == 4 and c["blocks_per_split"] == 32
+    c = q8.choose_config(4096, 4096, 152, 0, 0, kernel=q8.KERNEL_STREAM, split_k=4, stages=8)
+    assert c["split_k"] == 4 and c["stages"] == 8 and c["blocks_per_split"] == 32
 
 
 # ----------------------------------------------------------------------------
