@@ -125,11 +125,8 @@ def traffic_key(workload: str, rows: int, transposed: bool = False, a_int8: bool
 
 
 def launches_per_call(info) -> int:
-    """Kernels one call launches (the plan says: the tcgen05 path splits the
-    activations into bf16 parts first, the L2 prefetch kernel runs ahead of
-    the register kernel)."""
-    if info.get("launches"):
-        return int(info["launches"])
+    """Kernels one call launches: the tcgen05 path splits the activations into
+    bf16 parts first."""
     return 2 if info.get("kernel") == 7 else 1
 
 
@@ -238,7 +235,7 @@ def run_ours(args, rank, local_rank, world):
               "tc": q8mv.KERNEL_TC}[args.kernel]
     overlap = not args.no_overlap
     plan_opts = dict(kernel=kernel, split_k=args.split, stages=args.stages, threads_n=args.threads_n,
-                     cta_threads=args.cta_threads, l2_prefetch=args.l2_prefetch)
+                     cta_threads=args.cta_threads)
     if args.transposed:
         plan_opts = dict(kernel=q8mv.KERNEL_ROWS_I8 if args.a_int8 else 0)
     plan = q8mv.Plan(K, N, device=local_rank, rows=M, transposed=args.transposed, overlap=int(overlap), **plan_opts)
@@ -366,9 +363,7 @@ def run_ours(args, rank, local_rank, world):
     # the same workload with plain launches, for comparison with the overlapped headline
     plain = None
     if overlap:
-        plain_opts = dict(plan_opts)
-        plain_opts.pop("l2_prefetch", None)  # the prefetch kernel needs overlapped launches
-        plan_plain = q8mv.Plan(K, N, device=local_rank, rows=M, transposed=args.transposed, overlap=0, **plain_opts)
+        plan_plain = q8mv.Plan(K, N, device=local_rank, rows=M, transposed=args.transposed, overlap=0, **plan_opts)
         us_plain = time_calls(plan_plain, ptrs, stream, min(args.steps, 20000), epis=epis)
         pinfo = plan_plain.info
         plain = {"us_per_call": round(us_plain, 3), "value": round(bytes_per_call / us_plain / 1e3, 2),
@@ -821,9 +816,6 @@ def parse_args(argv=None):
     ap.add_argument("--stages", type=int, default=0, help="plan override: streaming kernel ring depth")
     ap.add_argument("--threads-n", type=int, default=0, help="plan override: threads along N per CTA")
     ap.add_argument("--cta-threads", type=int, default=0, help="plan override: threads per CTA (128 or 256)")
-    ap.add_argument("--l2-prefetch", type=int, choices=[-1, 0, 1], default=0,
-                    help="plan override: 1 = launch the L2 prefetch kernel ahead of each call, -1 = never, "
-                         "0 = the plan decides")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain launches instead of programmatic dependent launch (the plan's overlap option, "
                          "on by default: decode weights are constant across calls)")

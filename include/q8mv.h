@@ -106,11 +106,6 @@ typedef struct {
                           that the preceding work in the stream does not write. */
     int32_t cta_threads; /* register kernel: 128 or 256 threads per CTA */
     int32_t rows_per_cta; /* transposed plans: output rows per CTA, 8 or 16 */
-    int32_t l2_prefetch;  /* single-row plans with overlap = 1 and the register kernel: 1 = each call
-                             first launches a one-warp-per-SM kernel that loads the call's W and S
-                             into L2 while the previous call runs (two launches per call), -1 = never,
-                             0 = the plan decides (when two calls' weights fit in L2).  Needs
-                             N % 16 == 0 and 16-byte aligned W and S; otherwise skipped. */
 } q8mv_opts_t;
 
 /* What a plan chose for 16-byte aligned tensors: the kernel family asked for
@@ -137,8 +132,6 @@ typedef struct {
     int32_t rows;             /* activation rows M of the plan (1 for q8mv_plan) */
     int32_t rows_per_pass;    /* activation rows one CTA serves (1, or 2, 4, 8, 16 when batched) */
     int64_t grid_z;           /* passes of rows_per_pass rows: ceil(rows / rows_per_pass) */
-    int32_t l2_prefetch;      /* 1: each call first launches the L2 prefetch kernel */
-    int32_t launches;         /* kernels one call launches (16-byte aligned tensors) */
 } q8mv_plan_info_t;
 
 typedef struct q8mv_plan_s *q8mv_plan_t;

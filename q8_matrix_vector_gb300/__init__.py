@@ -44,8 +44,7 @@ class Opts(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("vec_bytes", ctypes.c_int32),
                 ("threads_n", ctypes.c_int32), ("split_k", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("overlap", ctypes.c_int32),
-                ("cta_threads", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32),
-                ("l2_prefetch", ctypes.c_int32)]
+                ("cta_threads", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32)]
 
 
 class Epilogue(ctypes.Structure):
@@ -63,8 +62,7 @@ class PlanInfo(ctypes.Structure):
                 ("tile_n", ctypes.c_int64), ("grid_x", ctypes.c_int64), ("grid_y", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("sm_count", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("rows", ctypes.c_int32),
-                ("rows_per_pass", ctypes.c_int32), ("grid_z", ctypes.c_int64),
-                ("l2_prefetch", ctypes.c_int32), ("launches", ctypes.c_int32)]
+                ("rows_per_pass", ctypes.c_int32), ("grid_z", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -130,12 +128,10 @@ def library() -> ctypes.CDLL:
     return _lib
 
 
-def _opts(kernel=0, vec_bytes=0, threads_n=0, split_k=0, stages=0, overlap=0, cta_threads=0, rows_per_cta=0,
-          l2_prefetch=0):
-    if not (kernel or vec_bytes or threads_n or split_k or stages or overlap or cta_threads or rows_per_cta
-            or l2_prefetch):
+def _opts(kernel=0, vec_bytes=0, threads_n=0, split_k=0, stages=0, overlap=0, cta_threads=0, rows_per_cta=0):
+    if not (kernel or vec_bytes or threads_n or split_k or stages or overlap or cta_threads or rows_per_cta):
         return None
-    return Opts(kernel, vec_bytes, threads_n, split_k, stages, overlap, cta_threads, rows_per_cta, l2_prefetch)
+    return Opts(kernel, vec_bytes, threads_n, split_k, stages, overlap, cta_threads, rows_per_cta)
 
 
 def choose_config(K: int, N: int, sm_count: int, ctas_per_sm: int, vec_bytes: int, **opts) -> dict:

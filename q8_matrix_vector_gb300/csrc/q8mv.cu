@@ -44,7 +44,6 @@
 #include "batched.h"
 #include "mma_kernel.cuh"
 #include "regs_kernel.cuh"
-#include "prefetch_kernel.cuh"
 #include "rows_kernel.cuh"
 #include "stream_kernel.cuh"
 
@@ -55,9 +54,7 @@ using rk::kStageBlocks;
 using rk::Params;
 using rk::q8mv_regs_kernel;
 constexpr int kMaxSplit = 65535;    // gridDim.y limit
-constexpr int kVersion = 200;       // 0.2.0
-// whether plans turn the L2 prefetch kernel on by themselves (opts->l2_prefetch == 0)
-constexpr bool kL2PrefetchDefault = false;
+constexpr int kVersion = 100;       // 0.1.0
 
 thread_local int g_last_cuda_error = 0;
 
@@ -389,26 +386,6 @@ struct MapCache {
     }
 };
 
-// Box sizes of the L2 prefetch maps for an N-column tensor: 256 columns (or N
-// if smaller; N % 16 == 0) by up to 256 rows of W and 64 rows of S.
-struct PrefetchBoxes {
-    uint32_t cols, rows_w, rows_s;
-    int64_t w_boxes, s_boxes;
-    int tiles;
-};
-
-PrefetchBoxes prefetch_boxes(int64_t K, int64_t N) {
-    PrefetchBoxes b;
-    const int64_t KB = ceil_div(K, kBlk);
-    b.cols = static_cast<uint32_t>(std::min<int64_t>(pk::kBoxN, N));
-    b.rows_w = static_cast<uint32_t>(std::min<int64_t>(pk::kBoxRowsW, K));
-    b.rows_s = static_cast<uint32_t>(std::min<int64_t>(pk::kBoxRowsS, KB));
-    b.tiles = static_cast<int>(ceil_div(N, pk::kBoxN));
-    b.w_boxes = b.tiles * ceil_div(K, pk::kBoxRowsW);
-    b.s_boxes = b.tiles * ceil_div(KB, pk::kBoxRowsS);
-    return b;
-}
-
 // A failed encode is reported through q8mv_last_cuda_error as
 // -(1000 * which + CUresult), which = 1 for W, 2 for S, 3 for A.
 bool encode_result(int which, CUresult r) {
@@ -473,31 +450,6 @@ struct StreamConfig {
     int stages = 0;     // ring depth
     size_t smem = 0;    // dynamic shared memory per CTA
 };
-
-// W and S as the L2 prefetch kernel reads them: boxes of 256 columns by 256
-// rows of W and 64 rows of S (fewer for small tensors).
-bool encode_w_pf(CUtensorMap *m, const int8_t *W, int64_t K, int64_t N) {
-    const PrefetchBoxes b = prefetch_boxes(K, N);
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N)};
-    const cuuint32_t box[2] = {b.cols, b.rows_w};
-    const cuuint32_t elem[2] = {1, 1};
-    return encode_result(1, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(W), dims, strides,
-                                        box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
-}
-
-bool encode_s_pf(CUtensorMap *m, const float *S, int64_t K, int64_t N) {
-    const PrefetchBoxes b = prefetch_boxes(K, N);
-    const int64_t KB = ceil_div(K, kBlk);
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(KB)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
-    const cuuint32_t box[2] = {b.cols, b.rows_s};
-    const cuuint32_t elem[2] = {1, 1};
-    return encode_result(2, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(S), dims, strides,
-                                        box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
-}
 
 size_t stream_smem(int stages, int max_len) {
     return static_cast<size_t>(sk::kBarBytes) + static_cast<size_t>(stages) * sk::kStageBytes +
@@ -678,9 +630,6 @@ struct q8mv_plan_s {
     bool stream = false;
     StreamConfig scfg;
     MapCache wmaps, smaps;
-    // L2 prefetch kernel ahead of the register kernel (single-row, overlapped plans)
-    bool l2pf = false;
-    MapCache pf_wmaps, pf_smaps;
     uint64_t wait_ns = sk::kWaitNs;  // bound on each mbarrier wait (streaming and tcgen05 kernels)
     uint32_t extra_tx = 0;           // bytes a ring barrier expects beyond its copies (tests only)
     // batched plans (q8mv_plan_batched with M >= 2): rows per pass, and one
@@ -831,8 +780,6 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
         if (opts->stages != 0 && (want_kernel != Q8MV_KERNEL_STREAM || opts->stages < 1 ||
                                   opts->stages > sk::kMaxStages))
             return Q8MV_ERR_INVALID_ARG;
-        if (opts->l2_prefetch < -1 || opts->l2_prefetch > 1) return Q8MV_ERR_INVALID_ARG;
-        if (opts->l2_prefetch == 1 && opts->overlap != 1) return Q8MV_ERR_INVALID_ARG;
     }
     // the streaming kernel needs 16-byte row pitches (tensor maps) and at most
     // 16 K ranges of at most 128 blocks
@@ -921,19 +868,6 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device, cons
         max_tiles = std::max(max_tiles, c.tiles);
     }
     if (p->cfg[vec_index(1)].vec == 0 && N > 0) return fail(Q8MV_ERR_INVALID_ARG);  // needs the fallback
-
-    // L2 prefetch ahead of each call: asked for, or (by default, with overlap)
-    // when two calls' weights and scales fit in L2 with room to spare
-    {
-        int l2_bytes = 0;
-        st = cuda_status(cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, device));
-        if (st != Q8MV_OK) return fail(st);
-        const int want_pf = opts ? opts->l2_prefetch : 0;
-        const int64_t bytes = K * N + 4 * KBl * N;
-        const bool fits = 5 * bytes <= 2 * static_cast<int64_t>(l2_bytes);
-        p->l2pf = N % 16 == 0 && N >= 16 && K >= 1 && encode_fn() != nullptr && p->overlap &&
-                  (want_pf == 1 || (want_pf == 0 && kL2PrefetchDefault && fits));
-    }
 
     // co-resident streaming kernel
     if (stream_shape && want_kernel == Q8MV_KERNEL_STREAM) {
@@ -1040,15 +974,7 @@ static void fill_batched_info(const bk::Config &c, int sm_count, int64_t M, int6
     info->grid_z = c.groups;
 }
 
-static q8mv_status_t plan_info_impl(q8mv_plan_t p, q8mv_plan_info_t *info);
-
 q8mv_status_t q8mv_plan_info(q8mv_plan_t p, q8mv_plan_info_t *info) {
-    const q8mv_status_t st = plan_info_impl(p, info);
-    if (st == Q8MV_OK && info->launches == 0) info->launches = info->kernel == Q8MV_KERNEL_TC ? 2 : 1;
-    return st;
-}
-
-static q8mv_status_t plan_info_impl(q8mv_plan_t p, q8mv_plan_info_t *info) {
     if (p == nullptr || info == nullptr) return Q8MV_ERR_INVALID_ARG;
     std::memset(info, 0, sizeof(*info));
     if (p->rows) {
@@ -1086,8 +1012,6 @@ static q8mv_status_t plan_info_impl(q8mv_plan_t p, q8mv_plan_info_t *info) {
         fill_info(p->cfg[idx], p->sm_count, p->occ.get(vec_idx_of(p->cfg[idx].vec), p->cfg[idx].tpb), p->ws_bytes,
                   info);
         info->overlap = p->overlap ? 1 : 0;
-        info->l2_prefetch = p->l2pf ? 1 : 0;
-        info->launches = p->l2pf ? 2 : 1;
         return Q8MV_OK;
     }
     info->kernel = Q8MV_KERNEL_REGS;
@@ -1103,37 +1027,6 @@ static bool overlaps(const void *a, int64_t a_bytes, const void *b, int64_t b_by
     if (a_bytes <= 0 || b_bytes <= 0) return false;
     const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
     return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
-}
-
-// Launch the L2 prefetch kernel for this call's W and S (16-byte aligned):
-// one warp per SM, with programmatic dependent launch so that it runs beside
-// the previous kernel in the stream.
-static q8mv_status_t launch_l2_prefetch(q8mv_plan_t p, const int8_t *W, const float *S, cudaStream_t stream) {
-    const CUtensorMap *mw = p->pf_wmaps.find(W);
-    if (mw == nullptr) {
-        CUtensorMap *m = p->pf_wmaps.slot(W);
-        if (!encode_w_pf(m, W, p->K, p->N)) return Q8MV_ERR_CUDA;
-        p->pf_wmaps.commit(W);
-        mw = m;
-    }
-    const CUtensorMap *ms = p->pf_smaps.find(S);
-    if (ms == nullptr) {
-        CUtensorMap *m = p->pf_smaps.slot(S);
-        if (!encode_s_pf(m, S, p->K, p->N)) return Q8MV_ERR_CUDA;
-        p->pf_smaps.commit(S);
-        ms = m;
-    }
-    const PrefetchBoxes b = prefetch_boxes(p->K, p->N);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p->sm_count));
-    cfg.blockDim = dim3(pk::kThreads);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, pk::q8mv_l2_prefetch_kernel, *mw, *ms, b.w_boxes, b.s_boxes, b.tiles));
 }
 
 // Launch the streaming kernel (W and S 16-byte aligned): one CTA per tile and
@@ -1297,10 +1190,6 @@ static q8mv_status_t run_impl(q8mv_plan_t p, const float *A, const int8_t *W, co
     const Config &c = p->cfg[idx];
     const bool svec = (c.vec >= 4 && saddr % 16 == 0) || (c.vec == 2 && saddr % 8 == 0);
 
-    if (p->l2pf && waddr % 16 == 0 && saddr % 16 == 0) {
-        st = launch_l2_prefetch(p, W, S, stream);
-        if (st != Q8MV_OK) return st;
-    }
     Params prm;
     prm.A = A;
     prm.W = W;

@@ -201,8 +201,7 @@ def test_overlapped_launches_respect_the_chain(q8):
 
     The chain must give bit-identical results with and without overlap: a call
     may start early and read its weights, but it reads A only after the
-    previous kernel has completed.  With the L2 prefetch kernel a call is two
-    launches, and its product kernel still runs after the previous call.
+    previous kernel has completed.
     """
     import torch
 
@@ -225,45 +224,11 @@ def test_overlapped_launches_respect_the_chain(q8):
         stream.synchronize()
         return [b.cpu() for b in bufs]
 
-    for kernel, extra in ((q8.KERNEL_REGS, {}), (q8.KERNEL_REGS, {"l2_prefetch": 1}), (q8.KERNEL_STREAM, {})):
+    for kernel in (q8.KERNEL_REGS, q8.KERNEL_STREAM):
         plain = chain(q8.Plan(K, N, kernel=kernel))
-        overlapped_plan = q8.Plan(K, N, kernel=kernel, overlap=1, **extra)
-        info = overlapped_plan.info
-        assert info["overlap"] == 1 and info["kernel"] == kernel
-        assert info["l2_prefetch"] == extra.get("l2_prefetch", info["l2_prefetch"])
-        assert info["launches"] == (2 if info["l2_prefetch"] else 1)
+        overlapped_plan = q8.Plan(K, N, kernel=kernel, overlap=1)
+        assert overlapped_plan.info["overlap"] == 1 and overlapped_plan.info["kernel"] == kernel
         for _ in range(3):
             over = chain(overlapped_plan)
             for i in range(calls):
-                assert torch.equal(plain[i], over[i]), (kernel, extra, i)
-
-
-@pytest.mark.parametrize("name", ["attn", "ffn_up", "ffn_down", "tiny"])
-def test_l2_prefetch_plans(q8, orc, name):
-    """The L2 prefetch kernel changes no result: parity and the integer-exact bits."""
-    A, W, S = workloads.make_inputs(name)
-    K, N = W.shape
-    if N % 16:
-        W, S = np.ascontiguousarray(W[:, :N - N % 16]), np.ascontiguousarray(S[:, :N - N % 16])
-        N = W.shape[1]
-    plan = q8.Plan(K, N, overlap=1, l2_prefetch=1)
-    assert plan.info["l2_prefetch"] == 1 and plan.info["launches"] == 2
-    got, guards = run_plan(plan, A, W, S)
-    ref, bound = orc.factored(A, W, S)
-    assert guards
-    assert_close(got, ref, bound, name)
-    Ai, Wi, Si = workloads.make_integer_exact(K, N, seed=21)
-    got_i, _ = run_plan(plan, Ai, Wi, Si)
-    ref_i, _ = orc.factored(Ai, Wi, Si)
-    assert np.array_equal(got_i, ref_i)
-    # unaligned weights skip the prefetch and still give the right result
-    got_u, _ = run_plan(plan, A, W, S, w_offset=1)
-    assert_close(got_u, ref, bound, f"{name} unaligned")
-
-
-def test_l2_prefetch_needs_overlap(q8):
-    with pytest.raises(q8.Q8mvError):
-        q8.Plan(4096, 4096, l2_prefetch=1)
-    with pytest.raises(q8.Q8mvError):
-        q8.Plan(4096, 4096, overlap=1, l2_prefetch=2)
-    assert q8.Plan(4096, 4096, overlap=1, l2_prefetch=-1).info["l2_prefetch"] == 0
+                assert torch.equal(plain[i], over[i]), (kernel, i)
