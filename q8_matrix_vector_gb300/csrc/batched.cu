@@ -11,8 +11,6 @@
 #include "mma_kernel.cuh"
 #include "tc_kernel.cuh"
 
-static_assert(bk::kTcStepBlocks == tck::kPair, "the tensor maps' boxes are one step high");
-
 #include <cuda_runtime.h>
 
 #include <algorithm>

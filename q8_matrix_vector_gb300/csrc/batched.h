@@ -73,7 +73,6 @@ struct MmaConfig {
 constexpr int kTcThreads = 448;  // threads per CTA of the tcgen05 kernel
 constexpr int kTcTileN = 128;    // its columns per CTA
 constexpr int kTcRows = 16;      // its activation rows per pass
-constexpr int kTcStepBlocks = 2; // blocks per step: its tensor maps' boxes are this many blocks high
 
 struct TcConfig {
     int split = 0, bps = 0;

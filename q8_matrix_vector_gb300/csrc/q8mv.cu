@@ -416,14 +416,13 @@ bool encode_s(CUtensorMap *m, const float *S, int64_t KB, int64_t N) {
                                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE));
 }
 
-// The tcgen05 batched kernel's maps: W [K rows][N bytes], box 64 rows (two
-// blocks) x 128 columns, 128-byte swizzle (the kernel reads each row's 16-byte
-// chunks at chunk ^ (row % 8)); S [KB rows][N floats], box 2 rows x 128
-// columns.
+// The tcgen05 batched kernel's maps: W [K rows][N bytes], box 32 rows x 128
+// columns, 128-byte swizzle (the kernel reads each row's 16-byte chunks at
+// chunk ^ (row % 8)); S [KB rows][N floats], box 1 row x 128 columns.
 bool encode_w_tc(CUtensorMap *m, const int8_t *W, int64_t K, int64_t N) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N)};
-    const cuuint32_t box[2] = {128, 32 * bk::kTcStepBlocks};
+    const cuuint32_t box[2] = {128, 32};
     const cuuint32_t elem[2] = {1, 1};
     return encode_result(1, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t *>(W), dims, strides,
                                         box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -433,7 +432,7 @@ bool encode_w_tc(CUtensorMap *m, const int8_t *W, int64_t K, int64_t N) {
 bool encode_s_tc(CUtensorMap *m, const float *S, int64_t KB, int64_t N) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(KB)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 4};
-    const cuuint32_t box[2] = {128, bk::kTcStepBlocks};
+    const cuuint32_t box[2] = {128, 1};
     const cuuint32_t elem[2] = {1, 1};
     return encode_result(2, encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(S), dims, strides,
                                         box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

@@ -27,13 +27,11 @@
 //     warps with fixed roles that hand work over through mbarriers only.  The
 //     blocks go in steps of kPair:
 //       - the load warp keeps a ring of kPairStages steps in shared memory
-//         filled, lane l the steps of stage pair l: per step, a 2D tensor
-//         copy of its 64 x 128 weight bytes (128-byte swizzle), one of its
-//         2 x 128 scales and a bulk copy of its 3 KiB per block of activation
-//         parts, completing on the pair's "full" mbarrier (rows past K and
-//         columns past N arrive as zeros); a stage pair is refilled once the
-//         fold warps are done with it ("empty").  One thread issuing copies
-//         keeps only a few in flight, hence large copies and a lane per pair;
+//         filled: per block, a 2D tensor copy of its 32 x 128 weight bytes
+//         (128-byte swizzle), one of its 128 scales and a bulk copy of its
+//         3 KiB of activation parts, a step's copies completing on one "full"
+//         mbarrier (rows past K and columns past N arrive as zeros); a stage
+//         is refilled once the fold warps are done with it ("empty");
 //       - eight convert warps turn each block's weight bytes into bf16
 //         exactly (16 bytes a thread) in a tile laid out as MN-major core
 //         matrices (8 k x 8 n), once the MMAs that last read the tile have
@@ -95,9 +93,7 @@ constexpr int kWTileBytes = kBlk * kTileN * 2;   // 8192: one block of bf16 weig
 constexpr int kWStageBytes = kBlk * kTileN;      // 4096: one block of weight bytes
 constexpr int kSStageBytes = kTileN * 4;         // 512: one block of scales
 constexpr int kPartBytes = kBlk * kMmaN * 2;     // 3072: one block of activation parts
-// a step's weights and scales arrive by one tensor copy each (boxes of kPair
-// blocks), its activation parts by one bulk copy
-constexpr uint32_t kStepInputTx = kPair * (kWStageBytes + kSStageBytes);
+constexpr uint32_t kStageTx = kWStageBytes + kSStageBytes + kPartBytes;
 // shared memory (offsets from a 1024-byte aligned base): bf16 tiles, weight
 // stages (1024-byte aligned for the swizzle), part stages, scale stages
 constexpr int kTilesOff = 0;
@@ -342,24 +338,20 @@ __global__ void __launch_bounds__(256) q8mv_tc_parts_kernel(const float *A, uint
     }
 }
 
-// One thread: copy the kPair blocks from b on (a step) into stage pair ps,
-// completing on `bar`: weights and scales by one tensor copy each (inputs no
-// earlier kernel writes, so they may be issued before the dependency wait;
-// a step of one block still copies the whole box, and the second block's
-// rows, in the next K range or past K, are not used) ...
+// One thread: copy block b of the CTA's range into stage `st`, completing on
+// `bar`: weights and scales by tensor copies (inputs no earlier kernel
+// writes, so they may be issued before the dependency wait), the activation
+// parts by a bulk copy (only after it).
 __device__ __forceinline__ void issue_inputs(const CUtensorMap *tmW, const CUtensorMap *tmS, uint32_t base,
-                                             uint64_t *bar, int ps, int64_t tile, int64_t b) {
-    tma_load_2d(base + kWRingOff + kPair * ps * kWStageBytes, tmW, static_cast<int>(tile * kTileN),
-                static_cast<int>(b * kBlk), bar);
-    tma_load_2d(base + kSRingOff + kPair * ps * kSStageBytes, tmS, static_cast<int>(tile * kTileN),
-                static_cast<int>(b), bar);
+                                             uint64_t *bar, int st, int64_t tile, int64_t b) {
+    tma_load_2d(base + kWRingOff + st * kWStageBytes, tmW, static_cast<int>(tile * kTileN), static_cast<int>(b * kBlk),
+                bar);
+    tma_load_2d(base + kSRingOff + st * kSStageBytes, tmS, static_cast<int>(tile * kTileN), static_cast<int>(b), bar);
 }
-// ... and the step's nb blocks of activation parts by one bulk copy (only
-// after the dependency wait: the parts kernel writes them)
-__device__ __forceinline__ void issue_parts(const Params &p, unsigned char *smem_base, uint64_t *bar, int ps, int z,
-                                            int64_t b, int nb) {
-    bulk_load(smem_base + kPartsOff + kPair * ps * kPartBytes, p.P + (static_cast<int64_t>(z) * p.KB + b) * kPartBytes,
-              nb * kPartBytes, bar);
+__device__ __forceinline__ void issue_parts(const Params &p, unsigned char *smem_base, uint64_t *bar, int st, int z,
+                                            int64_t b) {
+    bulk_load(smem_base + kPartsOff + st * kPartBytes, p.P + (static_cast<int64_t>(z) * p.KB + b) * kPartBytes,
+              kPartBytes, bar);
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
@@ -412,16 +404,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    // lane l of the load warp owns stage pair l: one thread issuing copies
-    // keeps only a few in flight (measured), so the pairs are filled by
-    // their own lanes
-    if (warp == kLoadWarp) {
-        __syncwarp();
-        if (lane < kPairStages && lane < nsteps) {
-            const int nb = step_blocks(lane);
-            mbar_arrive_expect_tx(s_full + lane, kStepInputTx + nb * kPartBytes + p.extra_tx);
-            issue_inputs(&tmW, &tmS, base, s_full + lane, lane, tile, b_begin + kPair * lane);
+        for (int t = 0; t < kPairStages && t < nsteps; ++t) {
+            const int nb = step_blocks(t);
+            mbar_arrive_expect_tx(s_full + t, nb * kStageTx + p.extra_tx);
+            for (int h = 0; h < nb; ++h)
+                issue_inputs(&tmW, &tmS, base, s_full + t, kPair * t + h, tile, b_begin + kPair * t + h);
         }
     }
     if (warp == kMmaWarp) {
@@ -441,17 +428,20 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int j = 0; j < kRows / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
     bool bad = false;  // warp-uniform
-    int last_issue = -1;  // load warp lane l < kPairStages: the last step issued into stage pair l
-    int issued_mma = 0;   // MMA warp: steps whose MMAs were issued
+    int last_issue[kPairStages];  // load warp: the last step issued into each stage pair (-1: none)
+    int issued_mma = 0;           // MMA warp: steps whose MMAs were issued
 
     if (warp == kLoadWarp) {
-        if (lane < kPairStages && lane < nsteps) {
-            const int ps = lane;
-            issue_parts(p, smem, s_full + ps, ps, z, b_begin + kPair * ps, step_blocks(ps));
-            last_issue = ps;
-            // step u into stage pair ps = u % kPairStages once the fold warps folded step u - kPairStages
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < kPairStages; ++s) last_issue[s] = s < nsteps ? s : -1;
+            for (int t = 0; t < kPairStages && t < nsteps; ++t)
+                for (int h = 0; h < step_blocks(t); ++h)
+                    issue_parts(p, smem, s_full + t, kPair * t + h, z, b_begin + kPair * t + h);
+            // step u into stage pair u % kPairStages once the fold warps folded step u - kPairStages
+            int ps = 0;
             uint32_t ph = 0;
-            for (int u = ps + kPairStages; u < nsteps; u += kPairStages) {
+            for (int u = kPairStages; u < nsteps; ++u) {
                 if (!mbar_wait(s_empty + ps, ph, abort_flag, p.wait_ns)) {
                     bad = true;
                     s_abort = 1;
@@ -459,11 +449,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                     break;
                 }
                 const int nb = step_blocks(u);
-                mbar_arrive_expect_tx(s_full + ps, kStepInputTx + nb * kPartBytes + p.extra_tx);
-                issue_inputs(&tmW, &tmS, base, s_full + ps, ps, tile, b_begin + kPair * u);
-                issue_parts(p, smem, s_full + ps, ps, z, b_begin + kPair * u, nb);
-                last_issue = u;
-                ph ^= 1u;
+                mbar_arrive_expect_tx(s_full + ps, nb * kStageTx + p.extra_tx);
+                for (int h = 0; h < nb; ++h) {
+                    issue_inputs(&tmW, &tmS, base, s_full + ps, kPair * ps + h, tile, b_begin + kPair * u + h);
+                    issue_parts(p, smem, s_full + ps, kPair * ps + h, z, b_begin + kPair * u + h);
+                }
+                last_issue[ps] = u;
+                if (++ps == kPairStages) {
+                    ps = 0;
+                    ph ^= 1u;
+                }
             }
         }
     } else if (warp == kMmaWarp) {
@@ -605,8 +600,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         bool ok = true;
         if (warp == kMmaWarp && lane == 0 && issued_mma > 0)
             ok = mbar_wait(s_done + (issued_mma - 1) % kSlots, ((issued_mma - 1) / kSlots) & 1, nullptr, p.wait_ns);
-        if (warp == kLoadWarp && lane < kPairStages && last_issue >= 0)
-            ok = mbar_wait(s_full + lane, (last_issue / kPairStages) & 1, nullptr, p.wait_ns);
+        if (warp == kLoadWarp && lane == 0) {
+            for (int s = 0; s < kPairStages && ok; ++s)
+                if (last_issue[s] >= 0)
+                    ok = mbar_wait(s_full + s, (last_issue[s] / kPairStages) & 1, nullptr, p.wait_ns);
+        }
         if (!ok) atomicOr(p.err, kErrDrainTimeout);
         tc_fence_before();
         __syncthreads();
