@@ -581,6 +581,22 @@ RowsConfig choose_rows(int64_t K, int64_t N, int sm_count, int cps16, int want_r
     return c;
 }
 
+// A last partial block that would cost one warp a second step of its own:
+// K = whole 512-wide steps, a multiple of the warps, plus at most one block.
+// It is staged in shared memory (4-byte copies, so rows 4-byte aligned).
+struct RowsTail {
+    int64_t k_main;
+    int tail;
+};
+
+RowsTail rows_tail(int64_t K, int wk, int lv) {
+    const int64_t steps_full = K / tk::kStepK;
+    const int64_t tail = K - steps_full * tk::kStepK;
+    if (lv >= 4 && tail > 0 && tail <= kBlk && steps_full >= wk && steps_full % wk == 0)
+        return RowsTail{steps_full * tk::kStepK, static_cast<int>(tail)};
+    return RowsTail{K, 0};
+}
+
 // Widest load per lane that Wt's address, the row pitch K and the cap allow.
 int rows_lv(uintptr_t waddr, int64_t K, int cap) {
     if (cap >= 16 && waddr % 16 == 0 && K % 16 == 0) return 16;
@@ -1143,6 +1159,9 @@ static q8mv_status_t run_rows(q8mv_plan_t p, const float *A, const int8_t *W, co
         cfg.numAttrs = 1;
     }
     const int lv = rows_lv(reinterpret_cast<uintptr_t>(W), p->K, p->max_vec);
+    const RowsTail tl = rows_tail(p->K, c.wk, lv);
+    prm.k_main = tl.k_main;
+    prm.tail = tl.tail;
     return cuda_status(cudaLaunchKernelEx(&cfg, rows_kernel(lv, c.r, p->rows_i8), prm));
 }
 

@@ -18,6 +18,11 @@
 // once.  After its steps each warp sums its lanes per row (fixed butterfly), and
 // the CTA adds the warps in order in shared memory before writing C.
 //
+// A last partial block that would give one warp a second 512-wide step of its
+// own (K = 8 full steps plus a few k, as in a 4100-wide LM head) is instead
+// copied into shared memory with cp.async at the start, next to the first
+// step's loads, and folded in by one thread per row at the end.
+//
 // With int8 activations (I8A) the lane first turns its 16 activations into
 // codes of their 32-element block (the block's two lanes agree on its largest
 // magnitude through one shuffle): d = amax / 127, q = rint(a * (127 / amax)),
@@ -47,8 +52,17 @@ struct Params {
     int64_t K, N;
     int KB;
     int wk;          // warps per CTA along K
+    int64_t k_main;  // the warps' steps cover k < k_main (= K unless the tail is staged)
+    int tail;        // K - k_main: a last partial block staged in shared memory (0: none)
     q8epi::Epilogue epi;
 };
+
+// 4 bytes global -> shared without registers (both 4-byte aligned)
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
 
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -169,9 +183,46 @@ __device__ __forceinline__ void quantize_half_block(const float2 (&a2)[8], uint3
     }
 }
 
+// The staged tail block of row t (tail bytes of w, their activations a and
+// the row's scale s), folded into v the way a step folds a block: products in
+// two packed lanes, k in order within each, one scale fold; with int8
+// activations the tail's own codes (amax over its k), an exact i32 sum and one
+// fold with d * s.
+template <bool I8A>
+__device__ __forceinline__ float fold_tail(const uint32_t *w, const float *a, int tail, float s, float v) {
+    if constexpr (I8A) {
+        float amax = 0.0f;
+        for (int i = 0; i < tail; ++i) amax = fmaxf(amax, fabsf(a[i]));
+        const float d = __fdiv_rn(amax, 127.0f);
+        const float id = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+        constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+        int isum = 0;
+        for (int i = 0; i < tail; ++i) {
+            const int code = static_cast<int8_t>(__float_as_uint(__fadd_rn(__fmul_rn(a[i], id), kRound)) & 0xFFu);
+            const int wb = static_cast<int8_t>((w[i / 4] >> (8 * (i % 4))) & 0xFFu);
+            isum += code * wb;
+        }
+        return fmaf(static_cast<float>(isum), __fmul_rn(d, s), v);
+    } else {
+        float2 s2 = make_float2(0.0f, 0.0f);
+        for (int q = 0; 4 * q < tail; ++q) {
+            const uint32_t u = w[q] ^ 0x80808080u;
+            s2 = __ffma2_rn(make_float2(a[4 * q], a[4 * q + 1]), cvt2(u, 0x7440u, 0x7441u), s2);
+            s2 = __ffma2_rn(make_float2(a[4 * q + 2], a[4 * q + 3]), cvt2(u, 0x7442u, 0x7443u), s2);
+        }
+        return fmaf(s2.x + s2.y, s, v);
+    }
+}
+
 template <int LV, int R, bool I8A>
 __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_rows_kernel(const Params p) {
     __shared__ float part[kMaxWarps][R];
+    // a last partial block too short for a step of its own (tail > 0): its
+    // bytes and scales are copied at the start, next to the first step's
+    // loads, instead of costing one warp a second round trip
+    __shared__ uint32_t tail_w[R][kBlk / 4];
+    __shared__ float tail_s[R];
+    __shared__ float tail_a[kBlk];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const bool even = (lane & 1) == 0;
@@ -188,16 +239,27 @@ __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_row
     float s[R];
     int64_t k0 = static_cast<int64_t>(warp) * kStepK;
     load_step<LV, R>(p, w_base, s_base, nrows, k0 + lane * kLaneK, even, w, s);
+    if (p.tail > 0) {
+        // rows are 4-byte aligned here (K % 4 == 0); words past the tail are never read
+        const int t = threadIdx.x;
+        if (t < R * (kBlk / 4)) {
+            const int r = t / (kBlk / 4), q = t % (kBlk / 4);
+            if (r < nrows && 4 * q < p.tail) cp_async4(&tail_w[r][q], w_base + r * p.K + p.k_main + 4 * q);
+        }
+        if (t < nrows) cp_async4(&tail_s[t], s_base + t * p.KB + p.k_main / kBlk);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
     pdl_launch_dependents();
     pdl_wait();
     float2 a2[8];
     load_a(p, k0 + lane * kLaneK, a2);
+    if (p.tail > 0 && static_cast<int>(threadIdx.x) < p.tail) tail_a[threadIdx.x] = __ldg(p.A + p.k_main + threadIdx.x);
 
     float acc[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) acc[r] = 0.0f;
 
-    for (; k0 < p.K; k0 += step) {
+    for (; k0 < p.k_main; k0 += step) {
         if constexpr (I8A) {
             // per row: four dp4a into the exact i32 sum of the lane's 16
             // products, the block's other half by one shuffle, one fold with
@@ -233,7 +295,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_row
         }
         // the next step's loads, once this step's registers are free
         const int64_t kn = k0 + step + lane * kLaneK;
-        if (k0 + step < p.K) {
+        if (k0 + step < p.k_main) {
             load_step<LV, R>(p, w_base, s_base, nrows, kn, even, w, s);
             load_a(p, kn, a2);
         }
@@ -247,11 +309,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_row
         for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
         if (lane == 0) part[warp][r] = v;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     if (threadIdx.x < nrows) {
         const int t = threadIdx.x;
         float v = part[0][t];
         for (int q = 1; q < p.wk; ++q) v += part[q][t];
+        if (p.tail > 0) v = fold_tail<I8A>(tail_w[t], tail_a, p.tail, tail_s[t], v);
         const int64_t n = n0 + t;
         p.C[n] = q8epi::apply(p.epi, v, p.C, n, n);
     }

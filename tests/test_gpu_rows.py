@@ -178,3 +178,29 @@ def test_rows_zero_sizes(q8):
                torch.empty((0, 2), device=dev))
     torch.cuda.synchronize()
     assert out.shape == (1, 0)
+
+
+@pytest.mark.parametrize("K", [4100, 4104, 4112, 4128, 8196])
+@pytest.mark.parametrize("rows_per_cta", [8, 16])
+def test_rows_short_tail_staged_in_shared_memory(q8, orc, K, rows_per_cta):
+    """K = whole 512-wide steps (a multiple of the 8 warps) plus at most one
+    block: the last block is copied at the start and folded in at the end.
+    f32 and int8 activations, ragged last CTA, exact-integer data bit for bit."""
+    N = 1000 + K % 7
+    A, W, S = workloads.make_random(K, N, seed=K + rows_per_cta)
+    Wt, St = transpose(W, S)
+    plan = q8.Plan(K, N, transposed=True, rows_per_cta=rows_per_cta)
+    got, guards = run_rows(plan, A, Wt, St)
+    ref, bound = orc.transposed(A, Wt, St)
+    assert guards
+    assert_close(got, ref, bound, f"K={K} R={rows_per_cta}")
+    Ai, Wi, Si = workloads.make_integer_exact(K, N, seed=K)
+    Wti, Sti = transpose(Wi, Si)
+    got_i, _ = run_rows(plan, Ai, Wti, Sti)
+    ref_i, _ = orc.transposed(Ai, Wti, Sti)
+    assert np.array_equal(got_i, ref_i), np.flatnonzero(got_i != ref_i)[:10]
+    plan8 = q8.Plan(K, N, transposed=True, rows_per_cta=rows_per_cta, kernel=q8.KERNEL_ROWS_I8)
+    got8, _ = run_rows(plan8, A, Wt, St)
+    qa, da = orc.quantize(A.reshape(K))
+    ref8, bound8 = orc.i8(qa, da, Wt, St)
+    assert_close(got8, ref8, bound8, f"int8 K={K} R={rows_per_cta}")
