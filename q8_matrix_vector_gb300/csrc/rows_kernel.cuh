@@ -84,8 +84,10 @@ __device__ __forceinline__ uint32_t load_byte(const int8_t *p) {
 // The 16 bytes of `row` from byte k (k < K) into w, little-endian words;
 // bytes at or past K are 0 (they convert to 0) and are not read.
 //   LV = 16: one 16-byte load (rows 16-byte aligned), streamed past L1.
-//   LV = 4:  four 4-byte loads (rows 4-byte aligned), through L1 so that the
-//            warp's four loads of a 512-byte span reach L2 once.
+//   LV = 4:  rows 4-byte aligned: per row, by its own alignment, one 16-byte
+//            load, two 8-byte loads or four 4-byte loads, the narrow ones
+//            through L1 so that the warp's loads of a 512-byte span reach L2
+//            once.
 //   LV = 1:  sixteen byte loads (any alignment), through L1 likewise.
 template <int LV>
 __device__ __forceinline__ void load_chunk(const int8_t *row, int64_t k, int64_t K, uint32_t (&w)[4]) {
@@ -97,9 +99,23 @@ __device__ __forceinline__ void load_chunk(const int8_t *row, int64_t k, int64_t
                          : "l"(p)
                          : "memory");
         } else if constexpr (LV == 4) {
+            // the row's own alignment (the same for every lane of the warp, so
+            // the branch is uniform): rows of a 4-byte multiple K start 0, 4, 8
+            // or 12 bytes past a 16-byte boundary
+            const uintptr_t al = reinterpret_cast<uintptr_t>(p) & 15u;
+            if (al == 0) {
+                asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                             : "l"(p)
+                             : "memory");
+            } else if (al == 8) {
+                asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p) : "memory");
+                asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w[2]), "=r"(w[3]) : "l"(p + 8) : "memory");
+            } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(w[q]) : "l"(p + 4 * q) : "memory");
+                for (int q = 0; q < 4; ++q)
+                    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(w[q]) : "l"(p + 4 * q) : "memory");
+            }
         } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
