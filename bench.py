@@ -327,37 +327,38 @@ def run_ours(args, rank, local_rank, world):
         bias_d, res_d = epi_bufs[0]
         epi_copies = [(bias_d, bias_p), (res_d, res_p)]
         epi_kw = dict(bias=bias_d, residual=res_d, act=args.epilogue)
-    # the step's host-to-device copies are split over several streams (the same
-    # bytes; several copy engines share the host link), each waiting until the
-    # previous call has read the buffers, and the call waits for all of them
-    copier = SplitCopier([(Ad, Ap), (Wd, Wp), (Sd, Sp)] + epi_copies, args.e2e_streams, stream, dev)
-
-    def e2e_step():
-        copier.copy_in()
-        with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):
+        for _ in range(2):  # warm-up
+            Ad.copy_(Ap, non_blocking=True)
+            Wd.copy_(Wp, non_blocking=True)
+            Sd.copy_(Sp, non_blocking=True)
+            for dst, src in epi_copies:
+                dst.copy_(src, non_blocking=True)
             plan(Ad, Wd, Sd, out=Cd, stream=stream, **epi_kw)
             Cp.copy_(Cd, non_blocking=True)
-
-    for _ in range(2):  # warm-up
-        e2e_step()
     stream.synchronize()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     barrier(group)
-    e_start.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e_end.record(stream)
+    with torch.cuda.stream(stream):
+        e_start.record(stream)
+        for _ in range(e2e_steps):
+            Ad.copy_(Ap, non_blocking=True)
+            Wd.copy_(Wp, non_blocking=True)
+            Sd.copy_(Sp, non_blocking=True)
+            for dst, src in epi_copies:
+                dst.copy_(src, non_blocking=True)
+            plan(Ad, Wd, Sd, out=Cd, stream=stream, **epi_kw)
+            Cp.copy_(Cd, non_blocking=True)
+        e_end.record(stream)
     e_end.synchronize()
     e_ms = reduce_over_ranks(group, e_start.elapsed_time(e_end), "max", dev)
     e_bytes = reduce_over_ranks(group, float(bytes_per_call) * e2e_steps, "sum", dev)
     h2d = 4 * M * K + K * N + 4 * KB * N + ((4 * N + 4 * M * N) if fused else 0)
     e2e = {"value": round(e_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4 * M * N, "steps": e2e_steps,
-           "streams": args.e2e_streams,
            "what": "pinned host A, W, S" + (", bias, residual" if fused else "")
-                   + f" copied in (split over {args.e2e_streams} streams), "
-                   + ("q8mv_run_fused" if fused else "q8mv_run") + ", C copied out, every step"}
+                   + " copied in, " + ("q8mv_run_fused" if fused else "q8mv_run") + ", C copied out, every step"}
 
     # the same workload with plain launches, for comparison with the overlapped headline
     plain = None
@@ -422,58 +423,6 @@ def run_ours(args, rank, local_rank, world):
         "wall_s_timed_region": round(wall, 4),
         "per_config": table,
     }
-
-
-def split_pieces(pairs, n):
-    """Cut (destination, source) tensor pairs into contiguous pieces for n
-    streams, about the same number of bytes each: a list of n lists of
-    (destination view, source view)."""
-    flat = [(d.view(-1), h.view(-1)) for d, h in pairs]
-    total = sum(d.numel() * d.element_size() for d, _ in flat)
-    n = max(1, n)
-    share = max(1, -(-total // n))
-    pieces = [[] for _ in range(n)]
-    i, filled = 0, 0
-    for d, h in flat:
-        start, count, size = 0, d.numel(), d.element_size()
-        while start < count:
-            n_el = min(count - start, max(1, (share - filled) // size))
-            pieces[i].append((d[start:start + n_el], h[start:start + n_el]))
-            start += n_el
-            filled += n_el * size
-            if filled >= share and i + 1 < n:
-                i, filled = i + 1, 0
-    return pieces
-
-
-class SplitCopier:
-    """Host-to-device copies of (device, pinned host) tensor pairs, each cut
-    into contiguous pieces spread over `n` side streams.  copy_in() makes every
-    side stream wait for what `stream` has queued so far (the previous call must
-    be done reading the buffers), issues the pieces, and makes `stream` wait for
-    all of them."""
-
-    def __init__(self, pairs, n, stream, dev):
-        import torch
-
-        self.stream = stream
-        self.pieces = split_pieces(pairs, n)
-        self.sides = [torch.cuda.Stream(dev) for _ in self.pieces]
-        self.free = torch.cuda.Event()
-        self.done = [torch.cuda.Event() for _ in self.sides]
-
-    def copy_in(self):
-        import torch
-
-        self.free.record(self.stream)
-        for side, done, pieces in zip(self.sides, self.done, self.pieces):
-            side.wait_event(self.free)
-            with torch.cuda.stream(side):
-                for d, h in pieces:
-                    d.copy_(h, non_blocking=True)
-            done.record(side)
-        for done in self.done:
-            self.stream.wait_event(done)
 
 
 EPILOGUE_ACTS = {"none": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
@@ -853,8 +802,6 @@ def parse_args(argv=None):
     ap.add_argument("--a-int8", action="store_true",
                     help="with --transposed: int8 activations per 32-element block, dp4a products")
     ap.add_argument("--e2e-steps", type=int, default=100)
-    ap.add_argument("--e2e-streams", type=int, default=4,
-                    help="streams the end-to-end run's host-to-device copies are split over")
     ap.add_argument("--cpu-seconds", type=float, default=CPU_BASELINE_SECONDS)
     ap.add_argument("--reference-seconds", type=float, default=60.0,
                     help="CPU budget of the reference arm's timed steps")

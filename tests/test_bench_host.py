@@ -134,23 +134,3 @@ def test_all_core_oracle_baseline_runs_one_process_per_core():
     assert full["kind"] == "oracle" and full["cpu_model"]
     assert full["single_thread"]["cores"] == 1
     assert full["cores"] == rec["cores"]
-
-
-def test_split_pieces_cover_every_byte_once():
-    import torch
-
-    for n in (1, 3, 4, 8):
-        pairs = [(torch.zeros(10), torch.arange(10.0)),
-                 (torch.zeros(7, dtype=torch.int8), torch.arange(7, dtype=torch.int8)),
-                 (torch.zeros((3, 5)), torch.arange(15.0).view(3, 5))]
-        pieces = bench.split_pieces(pairs, n)
-        assert len(pieces) == n
-        for group in pieces:
-            for d, h in group:
-                assert d.numel() == h.numel() > 0
-                d.copy_(h)
-        for d, h in pairs:
-            assert torch.equal(d, h)
-        sizes = [sum(d.numel() * d.element_size() for d, _ in g) for g in pieces]
-        assert sum(sizes) == 40 + 7 + 60
-        assert max(sizes) <= -(-107 // n) + 4  # about an even share (one element of slack)
