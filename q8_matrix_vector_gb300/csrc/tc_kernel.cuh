@@ -478,15 +478,20 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 tc_fence_after();
                 const int nb = step_blocks(t);
+                // k 0..15 of every block of the step, then k 16..31: each block
+                // still accumulates its two halves in k order, and MMAs into
+                // different accumulators follow each other
 #pragma unroll
-                for (int h = 0; h < kPair; ++h) {
-                    if (h >= nb) break;
-                    const uint32_t a0 = base + kTilesOff + (sl * kPair + h) * kWTileBytes;
-                    const uint32_t b0 = base + kPartsOff + (kPair * ps + h) * kPartBytes;
-                    const uint32_t dt = tmem + sl * kSlotCols + h * kBlockCols;
-                    mma_bf16(dt, smem_desc(a0, kWCoreK, 128), smem_desc(b0, kPCoreK, 128), 0u);
-                    mma_bf16(dt, smem_desc(a0 + 2 * kWCoreK, kWCoreK, 128), smem_desc(b0 + 2 * kPCoreK, kPCoreK, 128),
-                             1u);
+                for (int kh = 0; kh < 2; ++kh) {
+#pragma unroll
+                    for (int h = 0; h < kPair; ++h) {
+                        if (h >= nb) break;
+                        const uint32_t a0 = base + kTilesOff + (sl * kPair + h) * kWTileBytes + 2 * kh * kWCoreK;
+                        const uint32_t b0 = base + kPartsOff + (kPair * ps + h) * kPartBytes + 2 * kh * kPCoreK;
+                        const uint32_t dt = tmem + sl * kSlotCols + h * kBlockCols;
+                        mma_bf16(dt, smem_desc(a0, kWCoreK, 128), smem_desc(b0, kPCoreK, 128),
+                                 static_cast<uint32_t>(kh));
+                    }
                 }
                 mma_commit(s_done + sl);
                 issued_mma = t + 1;
