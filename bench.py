@@ -121,7 +121,9 @@ def traffic_key(workload: str, rows: int, transposed: bool = False, a_int8: bool
     transposed layout) and, for batched calls, the kernel that ran."""
     if transposed:
         return f"{workload}_t" + ("8" if a_int8 else "")
-    return workload if rows == 1 else f"{workload}_m{rows}_{KERNEL_NAMES.get(kernel, str(kernel))}"
+    if rows == 1:
+        return f"{workload}_stream" if kernel == 2 else workload
+    return f"{workload}_m{rows}_{KERNEL_NAMES.get(kernel, str(kernel))}"
 
 
 def launches_per_call(info) -> int:
