@@ -47,4 +47,32 @@ __device__ __forceinline__ float apply(const Epilogue &e, float x, const float *
     return y;
 }
 
+// The inputs the statement reads for output (idx, n), loaded ahead of the
+// product so that their latency overlaps the reductions; apply_pre then gives
+// exactly what apply gives.
+struct Pre {
+    float c_old = 0.0f;
+    float bias = 0.0f;
+    float residual = 0.0f;
+};
+
+__device__ __forceinline__ Pre preload(const Epilogue &e, const float *c, int64_t idx, int64_t n) {
+    Pre q;
+    if (!e.on) return q;
+    if (e.beta != 0.0f) q.c_old = c[idx];
+    if (e.bias != nullptr) q.bias = __ldg(e.bias + n);
+    if (e.residual != nullptr) q.residual = __ldg(e.residual + idx);
+    return q;
+}
+
+__device__ __forceinline__ float apply_pre(const Epilogue &e, float x, const Pre &q) {
+    if (!e.on) return x;
+    float y = e.alpha * x;
+    if (e.beta != 0.0f) y = fmaf(e.beta, q.c_old, y);
+    if (e.bias != nullptr) y += q.bias;
+    y = activate(y, e.act);
+    if (e.residual != nullptr) y += q.residual;
+    return y;
+}
+
 }  // namespace q8epi

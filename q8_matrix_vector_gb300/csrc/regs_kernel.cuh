@@ -264,6 +264,22 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
         }
     }
 
+    // with the fused epilogue, the inputs of the one output column this thread
+    // writes after the split's reduction are loaded now, so that their latency
+    // overlaps the reductions (cluster splits whose slice fits the CTA, and
+    // unsplit tiles no wider than the CTA)
+    q8epi::Pre pre;
+    int64_t pre_n = -1;
+    if (p.epi.on) {
+        const int per = CLUSTER ? (tile_cols + p.split - 1) / p.split : tile_cols;
+        const int c_first = (CLUSTER ? static_cast<int>(blockIdx.y) * per : 0) + tid;
+        const int c_lim = CLUSTER ? min(tile_cols, (static_cast<int>(blockIdx.y) + 1) * per) : tile_cols;
+        if ((CLUSTER || p.split == 1) && per <= TPB && c_first < c_lim && col0 + c_first < p.N) {
+            pre_n = col0 + c_first;
+            pre = q8epi::preload(p.epi, p.C, pre_n, pre_n);
+        }
+    }
+
     // sum the K groups of this CTA: first the groups that share a warp, by a
     // butterfly of shuffles over the lane bits that number them (each pairwise
     // sum is commutative, so every lane ends with the same bits), then the
@@ -308,7 +324,7 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
             const int64_t n = col0 + c;
             float v = *cluster.map_shared_rank(mine + c, 0);
             for (int q = 1; q < p.split; ++q) v += *cluster.map_shared_rank(mine + c, q);
-            if (n < p.N) p.C[n] = q8epi::apply(p.epi, v, p.C, n, n);
+            if (n < p.N) p.C[n] = n == pre_n ? q8epi::apply_pre(p.epi, v, pre) : q8epi::apply(p.epi, v, p.C, n, n);
         }
         cluster.sync();  // keep this CTA's sums alive until every CTA has read them
         return;
@@ -323,7 +339,7 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
         if (split)
             p.ws[static_cast<int64_t>(blockIdx.y) * p.N + n] = v;
         else
-            p.C[n] = q8epi::apply(p.epi, v, p.C, n, n);
+            p.C[n] = n == pre_n ? q8epi::apply_pre(p.epi, v, pre) : q8epi::apply(p.epi, v, p.C, n, n);
     }
     if (!split) return;
 
