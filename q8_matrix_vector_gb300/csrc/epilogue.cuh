@@ -48,8 +48,8 @@ __device__ __forceinline__ float apply(const Epilogue &e, float x, const float *
 }
 
 // The inputs the statement reads for output (idx, n), loaded ahead of the
-// product so that their latency overlaps the reductions; apply_pre then gives
-// exactly what apply gives.
+// product so that their latency hides under the weight stream; apply_pre then
+// gives exactly what apply gives.
 struct Pre {
     float c_old = 0.0f;
     float bias = 0.0f;

@@ -212,6 +212,22 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
     pdl_launch_dependents();
     pdl_wait();
 
+    // with the fused epilogue, the inputs of the one output column this thread
+    // writes at the end (cluster splits whose slice fits the CTA, and unsplit
+    // tiles no wider than the CTA) are loaded now, so that their latency hides
+    // under the weight stream instead of sitting on the final write
+    q8epi::Pre pre;
+    int64_t pre_n = -1;
+    if (p.epi.on) {
+        const int per = CLUSTER ? (tile_cols + p.split - 1) / p.split : tile_cols;
+        const int c_first = (CLUSTER ? static_cast<int>(blockIdx.y) * per : 0) + tid;
+        const int c_lim = CLUSTER ? min(tile_cols, (static_cast<int>(blockIdx.y) + 1) * per) : tile_cols;
+        if ((CLUSTER || p.split == 1) && per <= TPB && c_first < c_lim && col0 + c_first < p.N) {
+            pre_n = col0 + c_first;
+            pre = q8epi::preload(p.epi, p.C, pre_n, pre_n);
+        }
+    }
+
     float acc[V];
 #pragma unroll
     for (int j = 0; j < V; ++j) acc[j] = 0.0f;
@@ -261,22 +277,6 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
             }
             if (!had_prefetch) load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
             fold_scale<V>(part, s, acc);
-        }
-    }
-
-    // with the fused epilogue, the inputs of the one output column this thread
-    // writes after the split's reduction are loaded now, so that their latency
-    // overlaps the reductions (cluster splits whose slice fits the CTA, and
-    // unsplit tiles no wider than the CTA)
-    q8epi::Pre pre;
-    int64_t pre_n = -1;
-    if (p.epi.on) {
-        const int per = CLUSTER ? (tile_cols + p.split - 1) / p.split : tile_cols;
-        const int c_first = (CLUSTER ? static_cast<int>(blockIdx.y) * per : 0) + tid;
-        const int c_lim = CLUSTER ? min(tile_cols, (static_cast<int>(blockIdx.y) + 1) * per) : tile_cols;
-        if ((CLUSTER || p.split == 1) && per <= TPB && c_first < c_lim && col0 + c_first < p.N) {
-            pre_n = col0 + c_first;
-            pre = q8epi::preload(p.epi, p.C, pre_n, pre_n);
         }
     }
 
