@@ -338,6 +338,91 @@ q8mv_status_t q8mv_choose_config_batched(int64_t M, int64_t K, int64_t N, int32_
 /* Static, human-readable text for a status code. */
 const char *q8mv_status_string(q8mv_status_t status);
 
+/*
+ * Feed-forward pair: the up and down matvecs of one feed-forward block, the
+ * down product reading the up product's output,
+ *
+ *     H[n] = epi_up(   sum_b S_up[b, n]   * ( sum_{k in b} A[k] * W_up[k, n] ) )     n < N_mid
+ *     C[n] = epi_down( sum_b S_down[b, n] * ( sum_{k in b} H[k] * W_down[k, n] ) )   n < N_out
+ *
+ * each product the Q8_0 matvec above ("Q8_0 matvec" page) and each epilogue
+ * the fused epilogue of q8mv_run_fused ("dot and tensor cores" page, "The
+ * fused epilogue"), fused into one launch ("fusing the matvec pair
+ * up -> down" of a feed-forward block).
+ *
+ * Tensors (device memory of the pair's GPU, contiguous, row-major):
+ *     A       f32 [K]                     activation row
+ *     W_up    i8  [K, N_mid]   S_up   f32 [ceil(K/32), N_mid]
+ *     H       f32 [N_mid]                 the up product's output (written, then read back)
+ *     W_down  i8  [N_mid, N_out]  S_down f32 [ceil(N_mid/32), N_out]
+ *     C       f32 [N_out]                 output, overwritten
+ *
+ * With mode Q8MV_PAIR_AUTO (0) one cooperative launch computes both products
+ * when N_mid and N_out are multiples of 8, W_up and W_down are 8-byte and
+ * S_up, S_down 4-byte aligned: every CTA is resident, takes one item of the up
+ * product, issues the first weight loads of its item of the down product,
+ * waits at a grid-wide barrier for H to be complete, then computes that item.
+ * Otherwise (or with Q8MV_PAIR_TWO_LAUNCHES) the two products run as two
+ * q8mv_run_fused calls of single-row plans.  Q8MV_PAIR_ONE_LAUNCH makes
+ * q8mv_pair_plan fail with INVALID_ARG when the one-launch kernel cannot be
+ * planned for the shapes.
+ *
+ * Rules: those of q8mv_run_fused for each product; in addition H may overlap
+ * none of A, W_up, S_up, W_down, S_down, C, nor epi_down's bias and residual,
+ * and C none of A, W_up, S_up.  The pair owns the workspace of both products
+ * and of its barrier; calls on one pair must be ordered, as for a plan.  The
+ * barrier's wait is bounded (about 2 s): if it runs out the kernel records
+ * error bit 1 (q8mv_pair_check) and finishes with C undefined.
+ */
+enum {
+    Q8MV_PAIR_AUTO = 0,
+    Q8MV_PAIR_ONE_LAUNCH = 1,
+    Q8MV_PAIR_TWO_LAUNCHES = 2
+};
+
+typedef struct q8mv_pair_s *q8mv_pair_t;
+
+typedef struct {
+    int32_t overlap;     /* 0 or 1: launches with programmatic dependent launch, as q8mv_opts_t */
+    int32_t split_up;    /* K ranges per column tile of the up product; 0 = planner (at most 64) */
+    int32_t split_down;  /* the same for the down product */
+    int32_t cta_threads; /* 128 or 256; 0 = 256 */
+    int32_t mode;        /* Q8MV_PAIR_* */
+} q8mv_pair_opts_t;
+
+typedef struct {
+    int32_t one_launch;       /* 1: q8mv_pair_run launches the pair kernel (pointers allowing) */
+    int32_t threads_per_cta;  /* the pair kernel's choices (0 when one_launch is 0) */
+    int32_t grid;             /* CTAs: the larger product's tiles x split */
+    int32_t ctas_per_sm;
+    int32_t split_up, split_down;
+    int32_t tiles_up, tiles_down;  /* 128-column tiles */
+    int64_t workspace_bytes;
+} q8mv_pair_info_t;
+
+/* Plan a pair for K, N_mid, N_out on `device` (-1 = current); opts may be NULL. */
+q8mv_status_t q8mv_pair_plan(q8mv_pair_t *out, int64_t K, int64_t N_mid, int64_t N_out, int device,
+                             const q8mv_pair_opts_t *opts);
+
+/* H = epi_up(A . W_up), then C = epi_down(H . W_down), asynchronously on
+ * `stream`; epi_up and epi_down may be NULL (plain products). */
+q8mv_status_t q8mv_pair_run(q8mv_pair_t pair, const float *A, const int8_t *W_up, const float *S_up, float *H,
+                            const q8mv_epilogue_t *epi_up, const int8_t *W_down, const float *S_down, float *C,
+                            const q8mv_epilogue_t *epi_down, cudaStream_t stream);
+
+q8mv_status_t q8mv_pair_info(q8mv_pair_t pair, q8mv_pair_info_t *info);
+
+/* As q8mv_check, for the pair kernel: bit 1 = its grid barrier's wait ran
+ * out.  Clears the bits, and resets the pair's counters when any was set. */
+q8mv_status_t q8mv_pair_check(q8mv_pair_t pair, int32_t *device_error);
+
+/* For tests of the bounded wait only: the grid barrier's bound in
+ * nanoseconds (0 restores about 2 s).  INVALID_ARG above 10 s. */
+q8mv_status_t q8mv_pair_set_wait(q8mv_pair_t pair, uint64_t wait_ns);
+
+/* Release the pair (synchronises its device first).  NULL is accepted. */
+q8mv_status_t q8mv_pair_destroy(q8mv_pair_t pair);
+
 /* The last CUDA runtime error code this library saw on the calling thread
  * (0 if none), for diagnosing Q8MV_ERR_CUDA. */
 int q8mv_last_cuda_error(void);

@@ -33,6 +33,10 @@ KERNEL_ROWS_I8 = 5
 KERNEL_MMA = 6
 KERNEL_TC = 7
 
+PAIR_AUTO = 0
+PAIR_ONE_LAUNCH = 1
+PAIR_TWO_LAUNCHES = 2
+
 ACT_NONE = 0
 ACT_RELU = 1
 ACT_SILU = 2
@@ -51,6 +55,20 @@ class Epilogue(ctypes.Structure):
     """q8mv_epilogue_t: y = alpha x + beta C_old + bias[n]; y = act(y); C = y + residual."""
     _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
                 ("residual", ctypes.c_void_p), ("act", ctypes.c_int32)]
+
+
+class PairOpts(ctypes.Structure):
+    _fields_ = [("overlap", ctypes.c_int32), ("split_up", ctypes.c_int32), ("split_down", ctypes.c_int32),
+                ("cta_threads", ctypes.c_int32), ("mode", ctypes.c_int32)]
+
+
+class PairInfo(ctypes.Structure):
+    _fields_ = [("one_launch", ctypes.c_int32), ("threads_per_cta", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("ctas_per_sm", ctypes.c_int32), ("split_up", ctypes.c_int32), ("split_down", ctypes.c_int32),
+                ("tiles_up", ctypes.c_int32), ("tiles_down", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class PlanInfo(ctypes.Structure):
@@ -117,6 +135,18 @@ def _load() -> ctypes.CDLL:
     lib.q8mv_last_cuda_error.restype = ctypes.c_int
     lib.q8mv_version.argtypes = []
     lib.q8mv_version.restype = ctypes.c_int
+    lib.q8mv_pair_plan.argtypes = [ctypes.POINTER(p), i64, i64, i64, ctypes.c_int, ctypes.POINTER(PairOpts)]
+    lib.q8mv_pair_plan.restype = ctypes.c_int
+    lib.q8mv_pair_run.argtypes = [p, p, p, p, p, ctypes.POINTER(Epilogue), p, p, p, ctypes.POINTER(Epilogue), p]
+    lib.q8mv_pair_run.restype = ctypes.c_int
+    lib.q8mv_pair_info.argtypes = [p, ctypes.POINTER(PairInfo)]
+    lib.q8mv_pair_info.restype = ctypes.c_int
+    lib.q8mv_pair_check.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
+    lib.q8mv_pair_check.restype = ctypes.c_int
+    lib.q8mv_pair_set_wait.argtypes = [p, ctypes.c_uint64]
+    lib.q8mv_pair_set_wait.restype = ctypes.c_int
+    lib.q8mv_pair_destroy.argtypes = [p]
+    lib.q8mv_pair_destroy.restype = ctypes.c_int
     return lib
 
 
@@ -287,6 +317,102 @@ class Plan:
             self._h = ctypes.c_void_p()
             if st != Q8MV_OK:
                 raise Q8mvError(st, "q8mv_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Pair:
+    """The up and down matvecs of a feed-forward block (``q8mv_pair_plan``):
+    H = epi_up(A . W_up) with W_up [K, N_mid], then C = epi_down(H . W_down)
+    with W_down [N_mid, N_out], in one launch when the shapes and pointers allow."""
+
+    def __init__(self, K: int, N_mid: int, N_out: int, device: int = -1, overlap: int = 0, split_up: int = 0,
+                 split_down: int = 0, cta_threads: int = 0, mode: int = PAIR_AUTO):
+        self.K, self.N_mid, self.N_out = int(K), int(N_mid), int(N_out)
+        handle = ctypes.c_void_p()
+        o = PairOpts(overlap, split_up, split_down, cta_threads, mode)
+        st = _lib.q8mv_pair_plan(ctypes.byref(handle), self.K, self.N_mid, self.N_out, int(device), ctypes.byref(o))
+        if st != Q8MV_OK:
+            raise Q8mvError(st, f"q8mv_pair_plan(K={K}, N_mid={N_mid}, N_out={N_out})")
+        self._h = handle
+        info = PairInfo()
+        st = _lib.q8mv_pair_info(self._h, ctypes.byref(info))
+        if st != Q8MV_OK:
+            raise Q8mvError(st, "q8mv_pair_info")
+        self.info = info.as_dict()
+
+    def run_ptr(self, A: int, W_up: int, S_up: int, H: int, W_down: int, S_down: int, C: int,
+                epi_up: "Epilogue" = None, epi_down: "Epilogue" = None, stream: int = 0) -> None:
+        """Enqueue the pair on raw device pointers (integers) and a raw stream."""
+        st = _lib.q8mv_pair_run(self._h, A, W_up, S_up, H, ctypes.byref(epi_up) if epi_up else None,
+                                W_down, S_down, C, ctypes.byref(epi_down) if epi_down else None, stream)
+        if st != Q8MV_OK:
+            raise Q8mvError(st, "q8mv_pair_run")
+
+    def __call__(self, A, W_up, S_up, W_down, S_down, H=None, out=None, *, act_up=None, bias_up=None,
+                 residual=None, bias_down=None):
+        """(H, C) on torch CUDA tensors, on the current stream: H = act_up(A . W_up + bias_up),
+        C = H . W_down + bias_down + residual."""
+        import torch
+
+        _check(A, torch.float32, (1, self.K), "A")
+        _check(W_up, torch.int8, (self.K, self.N_mid), "W_up")
+        _check(S_up, torch.float32, (num_blocks(self.K), self.N_mid), "S_up")
+        _check(W_down, torch.int8, (self.N_mid, self.N_out), "W_down")
+        _check(S_down, torch.float32, (num_blocks(self.N_mid), self.N_out), "S_down")
+        dev = W_up.device
+        for name, t in (("A", A), ("S_up", S_up), ("W_down", W_down), ("S_down", S_down)):
+            if t.device != dev:
+                raise ValueError(f"{name} is on {t.device}, W_up is on {dev}")
+        if H is None:
+            H = torch.empty((1, self.N_mid), dtype=torch.float32, device=dev)
+        if out is None:
+            out = torch.empty((1, self.N_out), dtype=torch.float32, device=dev)
+        _check(H, torch.float32, (1, self.N_mid), "out")
+        _check(out, torch.float32, (1, self.N_out), "out")
+        if act_up not in _ACTS:
+            raise ValueError(f"act_up must be one of {sorted(k for k in _ACTS if k)} or None, got {act_up!r}")
+        if bias_up is not None:
+            _check(bias_up, torch.float32, (self.N_mid,), "bias")
+        if bias_down is not None:
+            _check(bias_down, torch.float32, (self.N_out,), "bias")
+        if residual is not None:
+            _check(residual, torch.float32, (1, self.N_out), "residual")
+        eu = ed = None
+        if act_up is not None or bias_up is not None:
+            eu = Epilogue(1.0, 0.0, bias_up.data_ptr() if bias_up is not None else None, None, _ACTS[act_up])
+        if residual is not None or bias_down is not None:
+            ed = Epilogue(1.0, 0.0, bias_down.data_ptr() if bias_down is not None else None,
+                          residual.data_ptr() if residual is not None else None, ACT_NONE)
+        with torch.cuda.device(dev):
+            self.run_ptr(A.data_ptr(), W_up.data_ptr(), S_up.data_ptr(), H.data_ptr(), W_down.data_ptr(),
+                         S_down.data_ptr(), out.data_ptr(), eu, ed, torch.cuda.current_stream(dev).cuda_stream)
+        return H, out
+
+    def check(self) -> int:
+        """Synchronise and return (and clear) the pair kernel's error bits (1: barrier wait ran out)."""
+        word = ctypes.c_int32()
+        st = _lib.q8mv_pair_check(self._h, ctypes.byref(word))
+        if st != Q8MV_OK:
+            raise Q8mvError(st, "q8mv_pair_check")
+        return word.value
+
+    def set_wait(self, wait_ns: int = 0) -> None:
+        """For tests of the bounded wait: the grid barrier's bound (0 = the default)."""
+        st = _lib.q8mv_pair_set_wait(self._h, int(wait_ns))
+        if st != Q8MV_OK:
+            raise Q8mvError(st, "q8mv_pair_set_wait")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            st = _lib.q8mv_pair_destroy(self._h)
+            self._h = ctypes.c_void_p()
+            if st != Q8MV_OK:
+                raise Q8mvError(st, "q8mv_pair_destroy")
 
     def __del__(self):
         try:

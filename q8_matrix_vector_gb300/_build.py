@@ -1,7 +1,8 @@
 """Build step for the q8mv CUDA library (sm_103a only).
 
 Compiles the translation units under ``csrc/`` (``q8mv.cu``: the single-row
-kernels and the C ABI; ``batched.cu``: the batched kernel) in parallel with
+kernels and the C ABI; ``batched.cu``: the batched kernel; ``pair.cu``: the
+feed-forward pair kernel) in parallel with
 nvcc and links them into ``libq8mv.so`` inside the package directory.  Run
 ``python -m q8_matrix_vector_gb300._build`` or call ``build_library()``;
 nothing here needs a GPU.
@@ -16,7 +17,7 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-UNITS = [os.path.join(CSRC, "q8mv.cu"), os.path.join(CSRC, "batched.cu")]
+UNITS = [os.path.join(CSRC, "q8mv.cu"), os.path.join(CSRC, "batched.cu"), os.path.join(CSRC, "pair.cu")]
 SRC = UNITS[0]
 HDR = os.path.join(ROOT, "include", "q8mv.h")
 LIB = os.path.join(PKG, "libq8mv.so")

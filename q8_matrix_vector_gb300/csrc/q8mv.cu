@@ -43,6 +43,7 @@
 
 #include "batched.h"
 #include "mma_kernel.cuh"
+#include "pair.h"
 #include "regs_kernel.cuh"
 #include "rows_kernel.cuh"
 #include "stream_kernel.cuh"
@@ -1233,14 +1234,16 @@ q8mv_status_t q8mv_run(q8mv_plan_t p, const float *A, const int8_t *W, const flo
     return run_impl(p, A, W, S, C, q8epi::Epilogue{}, stream);
 }
 
-q8mv_status_t q8mv_run_fused(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
-                             const q8mv_epilogue_t *epi, cudaStream_t stream) {
-    if (epi == nullptr) return q8mv_run(p, A, W, S, C, stream);
-    if (p == nullptr || epi->act < Q8MV_ACT_NONE || epi->act > Q8MV_ACT_GELU_TANH) return Q8MV_ERR_INVALID_ARG;
+// The device form of a caller's epilogue for an output C of M rows of N,
+// after checking it (act in range, bias and residual 4-byte aligned and not
+// overlapping C).
+static q8mv_status_t make_epilogue(const q8mv_epilogue_t *epi, const float *C, int64_t M, int64_t N,
+                                   q8epi::Epilogue *out) {
+    if (epi->act < Q8MV_ACT_NONE || epi->act > Q8MV_ACT_GELU_TANH) return Q8MV_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(epi->bias) & 3u) || (reinterpret_cast<uintptr_t>(epi->residual) & 3u))
         return Q8MV_ERR_INVALID_ARG;
-    const int64_t c_bytes = 4 * p->M * p->N;
-    if (overlaps(C, c_bytes, epi->bias, 4 * p->N) || overlaps(C, c_bytes, epi->residual, c_bytes))
+    const int64_t c_bytes = 4 * M * N;
+    if (overlaps(C, c_bytes, epi->bias, 4 * N) || overlaps(C, c_bytes, epi->residual, c_bytes))
         return Q8MV_ERR_INVALID_ARG;
     q8epi::Epilogue e;
     e.on = 1;
@@ -1249,6 +1252,17 @@ q8mv_status_t q8mv_run_fused(q8mv_plan_t p, const float *A, const int8_t *W, con
     e.bias = epi->bias;
     e.residual = epi->residual;
     e.act = epi->act;
+    *out = e;
+    return Q8MV_OK;
+}
+
+q8mv_status_t q8mv_run_fused(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
+                             const q8mv_epilogue_t *epi, cudaStream_t stream) {
+    if (epi == nullptr) return q8mv_run(p, A, W, S, C, stream);
+    if (p == nullptr) return Q8MV_ERR_INVALID_ARG;
+    q8epi::Epilogue e;
+    const q8mv_status_t st = make_epilogue(epi, C, p->M, p->N, &e);
+    if (st != Q8MV_OK) return st;
     return run_impl(p, A, W, S, C, e, stream);
 }
 
@@ -1724,3 +1738,232 @@ extern "C" q8mv_status_t q8mv_run_noalloc(int64_t K, int64_t N, const float *A, 
     prm.bps = c.bps;
     return cuda_status(launch_regs(c, svec, smem_bytes(c), prm, stream, false));
 }
+
+// ---------------------------------------------------------------------------
+// Feed-forward pair: H = epi_up(A . W_up), C = epi_down(H . W_down)
+//
+// One launch of the pair kernel (pair_kernel.cuh) when the shapes and the
+// pointers allow it, else two launches of the single-row plans (which take any
+// shape and alignment).  The pair plan owns the pair kernel's workspace
+// (partial rows and counters of both products, the grid barrier and an error
+// word) and the two single-row plans.
+// ---------------------------------------------------------------------------
+struct q8mv_pair_s {
+    int64_t K = 0, n_mid = 0, n_out = 0;
+    int device = 0;
+    bool overlap = false;
+    int mode = Q8MV_PAIR_AUTO;
+    bool one = false;          // the pair kernel is planned
+    pk::Config cfg;
+    q8mv_plan_t up = nullptr, down = nullptr;
+    void *mem = nullptr;       // workspace of the pair kernel
+    float *ws_up = nullptr, *ws_down = nullptr;
+    unsigned *tickets_up = nullptr, *tickets_down = nullptr, *bar = nullptr;
+    int *err = nullptr;
+    size_t mem_bytes = 0;
+    uint64_t wait_ns = pk::kWaitNs;
+};
+
+extern "C" {
+
+q8mv_status_t q8mv_pair_destroy(q8mv_pair_t p) {
+    if (p == nullptr) return Q8MV_OK;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (prev != p->device) cudaSetDevice(p->device);
+    q8mv_status_t st = cuda_status(cudaDeviceSynchronize());
+    if (p->mem) cudaFree(p->mem);
+    if (prev != p->device) cudaSetDevice(prev);
+    const q8mv_status_t s1 = q8mv_destroy(p->up);
+    const q8mv_status_t s2 = q8mv_destroy(p->down);
+    delete p;
+    return st != Q8MV_OK ? st : (s1 != Q8MV_OK ? s1 : s2);
+}
+
+q8mv_status_t q8mv_pair_plan(q8mv_pair_t *out, int64_t K, int64_t n_mid, int64_t n_out, int device,
+                             const q8mv_pair_opts_t *opts) {
+    if (out == nullptr) return Q8MV_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (K < 0 || n_mid < 0 || n_out < 0) return Q8MV_ERR_INVALID_ARG;
+    q8mv_pair_opts_t o = {};
+    if (opts) o = *opts;
+    if (o.overlap != 0 && o.overlap != 1) return Q8MV_ERR_INVALID_ARG;
+    if (o.cta_threads != 0 && o.cta_threads != 128 && o.cta_threads != 256) return Q8MV_ERR_INVALID_ARG;
+    if (o.split_up < 0 || o.split_up > pk::kMaxSplitPair || o.split_down < 0 || o.split_down > pk::kMaxSplitPair)
+        return Q8MV_ERR_INVALID_ARG;
+    if (o.mode != Q8MV_PAIR_AUTO && o.mode != Q8MV_PAIR_ONE_LAUNCH && o.mode != Q8MV_PAIR_TWO_LAUNCHES)
+        return Q8MV_ERR_INVALID_ARG;
+
+    q8mv_pair_s *p = new (std::nothrow) q8mv_pair_s();
+    if (p == nullptr) return Q8MV_ERR_OUT_OF_MEMORY;
+    p->K = K;
+    p->n_mid = n_mid;
+    p->n_out = n_out;
+    p->overlap = o.overlap == 1;
+    p->mode = o.mode;
+
+    // the two single-row plans (two-launch mode, and the fallback)
+    q8mv_opts_t so = {};
+    so.overlap = o.overlap;
+    q8mv_status_t st = q8mv_plan(&p->up, K, n_mid, device, &so);
+    if (st == Q8MV_OK) st = q8mv_plan(&p->down, n_mid, n_out, device, &so);
+    if (st != Q8MV_OK) {
+        q8mv_pair_destroy(p);
+        return st;
+    }
+    p->device = p->up->device;
+
+    if (o.mode != Q8MV_PAIR_TWO_LAUNCHES) {
+        int prev = 0;
+        st = cuda_status(cudaGetDevice(&prev));
+        if (st == Q8MV_OK && prev != p->device) st = cuda_status(cudaSetDevice(p->device));
+        const int tpb = o.cta_threads ? o.cta_threads : 256;
+        int cps = 0;
+        if (st == Q8MV_OK) st = cuda_status(pk::occupancy(tpb, &cps));
+        if (st == Q8MV_OK && cps > 0)
+            p->one = pk::plan(K, n_mid, n_out, p->up->sm_count, cps, tpb, o.split_up, o.split_down, &p->cfg);
+        if (st == Q8MV_OK && p->one) {
+            const pk::Config &c = p->cfg;
+            auto up16 = [](size_t b) { return (b + 255) / 256 * 256; };
+            const size_t b_ws_up = up16(static_cast<size_t>(c.up.ws_floats) * sizeof(float));
+            const size_t b_ws_dn = up16(static_cast<size_t>(c.down.ws_floats) * sizeof(float));
+            const size_t b_t_up = up16(static_cast<size_t>(c.up.tiles) * sizeof(unsigned));
+            const size_t b_t_dn = up16(static_cast<size_t>(c.down.tiles) * sizeof(unsigned));
+            p->mem_bytes = b_ws_up + b_ws_dn + b_t_up + b_t_dn + 256;
+            st = cuda_status(cudaMalloc(&p->mem, p->mem_bytes));
+            if (st == Q8MV_OK) st = cuda_status(cudaMemset(p->mem, 0, p->mem_bytes));
+            if (st == Q8MV_OK) st = cuda_status(cudaDeviceSynchronize());
+            if (st == Q8MV_OK) {
+                char *m = static_cast<char *>(p->mem);
+                p->ws_up = reinterpret_cast<float *>(m);
+                p->ws_down = reinterpret_cast<float *>(m + b_ws_up);
+                p->tickets_up = reinterpret_cast<unsigned *>(m + b_ws_up + b_ws_dn);
+                p->tickets_down = reinterpret_cast<unsigned *>(m + b_ws_up + b_ws_dn + b_t_up);
+                p->bar = reinterpret_cast<unsigned *>(m + b_ws_up + b_ws_dn + b_t_up + b_t_dn);
+                p->err = reinterpret_cast<int *>(p->bar + 2);
+            }
+        }
+        if (prev != p->device) cudaSetDevice(prev);
+        if (st == Q8MV_OK && !p->one && o.mode == Q8MV_PAIR_ONE_LAUNCH) st = Q8MV_ERR_INVALID_ARG;
+        if (st != Q8MV_OK) {
+            q8mv_pair_destroy(p);
+            return st;
+        }
+    }
+    *out = p;
+    return Q8MV_OK;
+}
+
+q8mv_status_t q8mv_pair_info(q8mv_pair_t p, q8mv_pair_info_t *info) {
+    if (p == nullptr || info == nullptr) return Q8MV_ERR_INVALID_ARG;
+    std::memset(info, 0, sizeof(*info));
+    info->one_launch = p->one ? 1 : 0;
+    if (p->one) {
+        const pk::Config &c = p->cfg;
+        info->threads_per_cta = c.tpb;
+        info->grid = c.grid;
+        info->ctas_per_sm = c.cps;
+        info->split_up = c.up.split;
+        info->split_down = c.down.split;
+        info->tiles_up = c.up.tiles;
+        info->tiles_down = c.down.tiles;
+        info->workspace_bytes = static_cast<int64_t>(p->mem_bytes);
+    }
+    return Q8MV_OK;
+}
+
+q8mv_status_t q8mv_pair_run(q8mv_pair_t p, const float *A, const int8_t *W_up, const float *S_up, float *H,
+                            const q8mv_epilogue_t *epi_up, const int8_t *W_down, const float *S_down, float *C,
+                            const q8mv_epilogue_t *epi_down, cudaStream_t stream) {
+    if (p == nullptr) return Q8MV_ERR_INVALID_ARG;
+    const int64_t K = p->K, Nm = p->n_mid, No = p->n_out;
+    const int64_t KBu = ceil_div(K, kBlk), KBd = ceil_div(Nm, kBlk);
+    if (H == nullptr || C == nullptr || (reinterpret_cast<uintptr_t>(H) & 3u) || (reinterpret_cast<uintptr_t>(C) & 3u))
+        return Q8MV_ERR_INVALID_ARG;
+    // H is the up product's output and the down product's input: it may not
+    // overlap anything else the call reads or writes, nor C anything
+    if (overlaps(H, 4 * Nm, A, 4 * K) || overlaps(H, 4 * Nm, W_up, K * Nm) || overlaps(H, 4 * Nm, S_up, 4 * KBu * Nm) ||
+        overlaps(H, 4 * Nm, W_down, Nm * No) || overlaps(H, 4 * Nm, S_down, 4 * KBd * No) ||
+        overlaps(H, 4 * Nm, C, 4 * No) || overlaps(C, 4 * No, A, 4 * K) || overlaps(C, 4 * No, W_up, K * Nm) ||
+        overlaps(C, 4 * No, S_up, 4 * KBu * Nm))
+        return Q8MV_ERR_INVALID_ARG;
+    q8epi::Epilogue eu, ed;
+    if (epi_up) {
+        const q8mv_status_t st = make_epilogue(epi_up, H, 1, Nm, &eu);
+        if (st != Q8MV_OK) return st;
+        if (epi_up->residual && overlaps(epi_up->residual, 4 * Nm, C, 4 * No)) return Q8MV_ERR_INVALID_ARG;
+    }
+    if (epi_down) {
+        const q8mv_status_t st = make_epilogue(epi_down, C, 1, No, &ed);
+        if (st != Q8MV_OK) return st;
+        if ((epi_down->bias && overlaps(epi_down->bias, 4 * No, H, 4 * Nm)) ||
+            (epi_down->residual && overlaps(epi_down->residual, 4 * No, H, 4 * Nm)))
+            return Q8MV_ERR_INVALID_ARG;
+    }
+
+    const uintptr_t wu = reinterpret_cast<uintptr_t>(W_up), wd = reinterpret_cast<uintptr_t>(W_down);
+    const uintptr_t su = reinterpret_cast<uintptr_t>(S_up), sd = reinterpret_cast<uintptr_t>(S_down);
+    const bool one = p->one && wu % pk::kVec == 0 && wd % pk::kVec == 0 && su % 4 == 0 && sd % 4 == 0;
+    if (!one) {
+        q8mv_status_t st = run_impl(p->up, A, W_up, S_up, H, eu, stream);
+        if (st == Q8MV_OK) st = run_impl(p->down, H, W_down, S_down, C, ed, stream);
+        return st;
+    }
+    if (A == nullptr || W_up == nullptr || S_up == nullptr || W_down == nullptr || S_down == nullptr ||
+        (reinterpret_cast<uintptr_t>(A) & 3u))
+        return Q8MV_ERR_INVALID_ARG;
+    int dev = -1;
+    q8mv_status_t st = cuda_status(cudaGetDevice(&dev));
+    if (st != Q8MV_OK) return st;
+    if (dev != p->device) return Q8MV_ERR_INVALID_ARG;
+    pk::Args a;
+    a.A = A;
+    a.W_up = W_up;
+    a.S_up = S_up;
+    a.H = H;
+    a.W_down = W_down;
+    a.S_down = S_down;
+    a.C = C;
+    a.epi_up = eu;
+    a.epi_down = ed;
+    a.ws_up = p->ws_up;
+    a.ws_down = p->ws_down;
+    a.tickets_up = p->tickets_up;
+    a.tickets_down = p->tickets_down;
+    a.bar = p->bar;
+    a.err = p->err;
+    a.wait_ns = p->wait_ns;
+    const bool svec = su % 16 == 0 && sd % 16 == 0;
+    return cuda_status(pk::launch(p->cfg, a, svec, p->overlap, stream));
+}
+
+q8mv_status_t q8mv_pair_check(q8mv_pair_t p, int32_t *device_error) {
+    if (p == nullptr || device_error == nullptr) return Q8MV_ERR_INVALID_ARG;
+    *device_error = 0;
+    int prev = 0;
+    q8mv_status_t st = cuda_status(cudaGetDevice(&prev));
+    if (st != Q8MV_OK) return st;
+    if (prev != p->device) {
+        st = cuda_status(cudaSetDevice(p->device));
+        if (st != Q8MV_OK) return st;
+    }
+    int word = 0;
+    st = cuda_status(cudaDeviceSynchronize());
+    if (st == Q8MV_OK && p->err) st = cuda_status(cudaMemcpy(&word, p->err, sizeof(int), cudaMemcpyDeviceToHost));
+    if (st == Q8MV_OK && word != 0) {
+        // a barrier that gave up leaves the arrival count and the tickets behind: start clean
+        st = cuda_status(cudaMemset(p->mem, 0, p->mem_bytes));
+        if (st == Q8MV_OK) st = cuda_status(cudaDeviceSynchronize());
+    }
+    *device_error = word;
+    if (prev != p->device) cudaSetDevice(prev);
+    return st;
+}
+
+q8mv_status_t q8mv_pair_set_wait(q8mv_pair_t p, uint64_t wait_ns) {
+    if (p == nullptr || wait_ns > 10000000000ull) return Q8MV_ERR_INVALID_ARG;
+    p->wait_ns = wait_ns == 0 ? pk::kWaitNs : wait_ns;
+    return Q8MV_OK;
+}
+
+}  // extern "C"
