@@ -384,19 +384,24 @@ typedef struct q8mv_pair_s *q8mv_pair_t;
 
 typedef struct {
     int32_t overlap;     /* 0 or 1: launches with programmatic dependent launch, as q8mv_opts_t */
-    int32_t split_up;    /* K ranges per column tile of the up product; 0 = planner (at most 64) */
+    int32_t split_up;    /* with cluster == 1: K ranges per column tile of the up product; 0 = planner */
     int32_t split_down;  /* the same for the down product */
-    int32_t cta_threads; /* 128 or 256; 0 = 256 */
+    int32_t cta_threads; /* 128 or 256; 0 = planner */
     int32_t mode;        /* Q8MV_PAIR_* */
+    int32_t cluster;     /* 0 = planner; 1 = K ranges summed through the workspace (at most 64 per
+                            tile); 2 .. 8 = both products split this many ways, summed through
+                            thread-block clusters of that size */
 } q8mv_pair_opts_t;
 
 typedef struct {
     int32_t one_launch;       /* 1: q8mv_pair_run launches the pair kernel (pointers allowing) */
     int32_t threads_per_cta;  /* the pair kernel's choices (0 when one_launch is 0) */
     int32_t grid;             /* CTAs: the larger product's tiles x split */
-    int32_t ctas_per_sm;
+    int32_t resident_ctas;    /* CTAs of this shape the GPU holds at once */
+    int32_t cluster;          /* 1 = workspace sums, else the cluster size */
     int32_t split_up, split_down;
-    int32_t tiles_up, tiles_down;  /* 128-column tiles */
+    int32_t tiles_up, tiles_down;
+    int32_t tile_cols_up, tile_cols_down;  /* 128 or 64 */
     int64_t workspace_bytes;
 } q8mv_pair_info_t;
 

@@ -12,7 +12,7 @@
 namespace pk {
 
 constexpr int kVec = 8;                        // weight bytes per thread and row
-constexpr int kTn = 16;                        // threads along N: 128-column tiles
+constexpr int kMaxCluster = 8;                 // portable thread-block cluster size
 constexpr uint64_t kWaitNs = 2000000000ull;    // grid barrier bound
 constexpr int kErrBarrier = 1;                 // error bit: the grid barrier's wait ran out
 constexpr int kMaxSplitPair = 64;              // K ranges per column tile, per product
@@ -21,7 +21,9 @@ constexpr int kMaxSplitPair = 64;              // K ranges per column tile, per 
 struct PhaseConfig {
     int64_t K = 0, N = 0;
     int KB = 0;
-    int tiles = 0;        // 128-column tiles
+    int tn = 16;          // threads along N: tiles of tn * 8 columns
+    int gk = 0;           // thread groups along K
+    int tiles = 0;        // column tiles
     int split = 0;        // K ranges per tile
     int bps = 0;          // blocks per range
     int64_t ws_floats = 0;
@@ -29,23 +31,32 @@ struct PhaseConfig {
 
 struct Config {
     int tpb = 0;          // threads per CTA (128 or 256)
-    int gk = 0;           // thread groups along K
-    int cps = 0;          // resident CTAs per SM
+    int cluster = 1;      // > 1: both products split this many ways, summed through a cluster
+    int slots = 0;        // CTAs that can be resident at once
     int grid = 0;         // CTAs: the larger product's items
     size_t smem = 0;      // dynamic shared memory per CTA
     PhaseConfig up, down;
 };
 
-// Plan a pair on `sm_count` SMs with `cps` resident CTAs of `tpb` threads:
-// each product's split is the largest that keeps its items (tiles x split)
-// within one resident wave, unless want_up / want_down (> 0) fix it.  False
-// if the shapes cannot use the pair kernel (N_mid or N_out not a multiple of
-// 8, an empty product) or a wanted split does not fit.
-bool plan(int64_t K, int64_t n_mid, int64_t n_out, int sm_count, int cps, int tpb, int want_up, int want_down,
+// Dynamic shared memory of the pair kernel: the staged activations, or the K
+// groups' column sums (and, with a cluster, the CTA's own sums) for the
+// widest tile.
+size_t smem_bytes(int tpb, int cluster);
+
+// Plan a pair for `slots` resident CTAs of `tpb` threads.  cluster > 1:
+// both products take `cluster` K ranges per tile, summed through clusters of
+// that size, and each picks 128- or 64-column tiles (the wider unless the
+// narrower fills more of the slots).  cluster == 1: 128-column tiles, each
+// product's split the largest that keeps its items (tiles x split) within the
+// slots unless want_up / want_down (> 0) fix it, summed through the
+// workspace.  False if the shapes cannot use the pair kernel (N_mid or N_out
+// not a multiple of 8, an empty product) or the items do not fit.
+bool plan(int64_t K, int64_t n_mid, int64_t n_out, int slots, int tpb, int cluster, int want_up, int want_down,
           Config *out);
 
-// Resident CTAs per SM of the pair kernel with `tpb` threads.
-cudaError_t occupancy(int tpb, int *cps);
+// CTAs of the pair kernel (`tpb` threads, clusters of `cluster` CTAs, or none
+// for 1) that can be resident at once on the current device.
+cudaError_t resident_ctas(int tpb, int cluster, int *ctas);
 
 struct Args {
     const float *A;

@@ -31,6 +31,7 @@
 // bound is never reached in normal use.
 #pragma once
 
+#include <cooperative_groups.h>
 #include <cstdint>
 
 #include "epilogue.cuh"
@@ -49,7 +50,9 @@ struct Phase {
     unsigned *tickets;    // [tiles] arrival counters, zero between calls
     int64_t K, N;
     int KB;
-    int gk;               // thread groups along K (threads per CTA / kTn)
+    int tn;               // threads along N (tiles of tn * 8 columns)
+    int tn_log2;
+    int gk;               // thread groups along K (threads per CTA / tn)
     int split;            // K ranges per column tile
     int bps;              // blocks per K range
     int tiles;            // column tiles
@@ -75,8 +78,8 @@ template <bool SVEC>
 __device__ __forceinline__ bool prefetch_block(const Phase &p, int tile, int range,
                                                uint32_t (&w)[rk::kBlk][(kVec + 3) / 4], float (&s)[kVec]) {
     const int tid = threadIdx.x;
-    const int64_t n0 = static_cast<int64_t>(tile) * (kTn * kVec) + static_cast<int64_t>(tid & (kTn - 1)) * kVec;
-    const int b = range * p.bps + (tid / kTn);
+    const int64_t n0 = static_cast<int64_t>(tile) * (p.tn * kVec) + static_cast<int64_t>(tid & (p.tn - 1)) * kVec;
+    const int b = range * p.bps + (tid >> p.tn_log2);
     const int b_end = min(p.KB, range * p.bps + p.bps);
     if (n0 >= p.N || b >= b_end || static_cast<int64_t>(b + 1) * rk::kBlk > p.K) return false;
     const int8_t *w_ptr = p.W + static_cast<int64_t>(b) * rk::kBlk * p.N + n0;
@@ -88,15 +91,18 @@ __device__ __forceinline__ bool prefetch_block(const Phase &p, int tile, int ran
 
 // Item (tile, range) of phase p.  COHERENT: the activations were written
 // during this launch, so they are read through L2, not the read-only path.
-template <bool SVEC, int TPB, bool COHERENT>
+// CLUSTER: the tile's split CTAs form one thread-block cluster (rank = range)
+// and sum their K ranges through distributed shared memory in rank order;
+// otherwise through the workspace and the tile's tickets.
+template <bool SVEC, int TPB, bool COHERENT, bool CLUSTER>
 __device__ __forceinline__ void run_item(const Phase &p, int tile, int range, float *smem, unsigned &s_is_last,
                                          uint32_t (&w)[rk::kBlk][(kVec + 3) / 4], float (&s)[kVec],
                                          bool prefetched) {
     constexpr int V = kVec;
     const int tid = threadIdx.x;
-    const int tn_i = tid & (kTn - 1);
-    const int gk_i = tid / kTn;
-    constexpr int tile_cols = kTn * V;
+    const int tn_i = tid & (p.tn - 1);
+    const int gk_i = tid >> p.tn_log2;
+    const int tile_cols = p.tn * V;
     const int64_t col0 = static_cast<int64_t>(tile) * tile_cols;
     const int64_t n0 = col0 + static_cast<int64_t>(tn_i) * V;
     const bool active = n0 < p.N;  // V divides N, so an active strip is whole
@@ -161,6 +167,30 @@ __device__ __forceinline__ void run_item(const Phase &p, int tile, int range, fl
         for (int j = 0; j < V; ++j) red[gk_i * tile_cols + tn_i * V + j] = acc[j];
     }
     __syncthreads();
+    if constexpr (CLUSTER) {
+        // the CTA's column sums in its own shared memory; after a cluster
+        // barrier rank r adds up slice r of the columns over all ranks, in
+        // rank order, reading their shared memory directly
+        namespace cg = cooperative_groups;
+        float *mine = smem + p.gk * tile_cols;  // [tile_cols]
+        for (int c = tid; c < tile_cols; c += TPB) {
+            float v = red[c];
+            for (int g = 1; g < p.gk; ++g) v += red[g * tile_cols + c];
+            mine[c] = v;
+        }
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        const int per = (tile_cols + p.split - 1) / p.split;
+        const int c_end = min(tile_cols, (range + 1) * per);
+        for (int c = range * per + tid; c < c_end; c += TPB) {
+            const int64_t n = col0 + c;
+            float v = *cluster.map_shared_rank(mine + c, 0);
+            for (int q = 1; q < p.split; ++q) v += *cluster.map_shared_rank(mine + c, q);
+            if (n < p.N) p.C[n] = q8epi::apply(p.epi, v, p.C, n, n);
+        }
+        cluster.sync();  // keep this CTA's sums alive until every rank has read them
+        return;
+    }
     const bool split = p.split > 1;
     for (int c = tid; c < tile_cols; c += TPB) {
         const int64_t n = col0 + c;
@@ -222,7 +252,7 @@ __device__ __forceinline__ void grid_barrier(unsigned *bar, const Params &pp) {
     __syncthreads();
 }
 
-template <bool SVEC, int TPB>
+template <bool SVEC, int TPB, bool CLUSTER>
 __global__ void __launch_bounds__(TPB, rk::regs_min_blocks<kVec, TPB>()) q8mv_pair_kernel(const Params pp) {
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_is_last;
@@ -237,14 +267,14 @@ __global__ void __launch_bounds__(TPB, rk::regs_min_blocks<kVec, TPB>()) q8mv_pa
     bool pf = up && prefetch_block<SVEC>(pp.up, up_tile, up_range, w, s);
     rk::pdl_launch_dependents();
     rk::pdl_wait();
-    if (up) run_item<SVEC, TPB, false>(pp.up, up_tile, up_range, smem, s_is_last, w, s, pf);
+    if (up) run_item<SVEC, TPB, false, CLUSTER>(pp.up, up_tile, up_range, smem, s_is_last, w, s, pf);
 
     // down product: its first weight block before the grid barrier, H after it
     const bool down = item < pp.down.tiles * pp.down.split;
     const int dn_tile = down ? item / pp.down.split : 0, dn_range = down ? item % pp.down.split : 0;
     pf = down && prefetch_block<SVEC>(pp.down, dn_tile, dn_range, w, s);
     grid_barrier(pp.bar, pp);
-    if (down) run_item<SVEC, TPB, true>(pp.down, dn_tile, dn_range, smem, s_is_last, w, s, pf);
+    if (down) run_item<SVEC, TPB, true, CLUSTER>(pp.down, dn_tile, dn_range, smem, s_is_last, w, s, pf);
 }
 
 }  // namespace pk

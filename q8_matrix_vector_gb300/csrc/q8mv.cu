@@ -1791,6 +1791,8 @@ q8mv_status_t q8mv_pair_plan(q8mv_pair_t *out, int64_t K, int64_t n_mid, int64_t
     if (o.cta_threads != 0 && o.cta_threads != 128 && o.cta_threads != 256) return Q8MV_ERR_INVALID_ARG;
     if (o.split_up < 0 || o.split_up > pk::kMaxSplitPair || o.split_down < 0 || o.split_down > pk::kMaxSplitPair)
         return Q8MV_ERR_INVALID_ARG;
+    if (o.cluster < 0 || o.cluster > pk::kMaxCluster) return Q8MV_ERR_INVALID_ARG;
+    if ((o.split_up || o.split_down) && o.cluster != 1) return Q8MV_ERR_INVALID_ARG;
     if (o.mode != Q8MV_PAIR_AUTO && o.mode != Q8MV_PAIR_ONE_LAUNCH && o.mode != Q8MV_PAIR_TWO_LAUNCHES)
         return Q8MV_ERR_INVALID_ARG;
 
@@ -1817,11 +1819,19 @@ q8mv_status_t q8mv_pair_plan(q8mv_pair_t *out, int64_t K, int64_t n_mid, int64_t
         int prev = 0;
         st = cuda_status(cudaGetDevice(&prev));
         if (st == Q8MV_OK && prev != p->device) st = cuda_status(cudaSetDevice(p->device));
-        const int tpb = o.cta_threads ? o.cta_threads : 256;
-        int cps = 0;
-        if (st == Q8MV_OK) st = cuda_status(pk::occupancy(tpb, &cps));
-        if (st == Q8MV_OK && cps > 0)
-            p->one = pk::plan(K, n_mid, n_out, p->up->sm_count, cps, tpb, o.split_up, o.split_down, &p->cfg);
+        // the planner's default: 128-thread CTAs in clusters of the largest
+        // size (up to 8) whose up product still fits one resident wave
+        const int tpb = o.cta_threads ? o.cta_threads : 128;
+        const int c_lo = o.cluster ? o.cluster : 1, c_hi = o.cluster ? o.cluster : pk::kMaxCluster;
+        for (int cl = c_hi; st == Q8MV_OK && cl >= c_lo && !p->one; --cl) {
+            int slots = 0;
+            const cudaError_t e = pk::resident_ctas(tpb, cl, &slots);
+            if (e != cudaSuccess) {
+                cudaGetLastError();  // a cluster size this device cannot schedule
+                continue;
+            }
+            if (slots > 0) p->one = pk::plan(K, n_mid, n_out, slots, tpb, cl, o.split_up, o.split_down, &p->cfg);
+        }
         if (st == Q8MV_OK && p->one) {
             const pk::Config &c = p->cfg;
             auto up16 = [](size_t b) { return (b + 255) / 256 * 256; };
@@ -1862,11 +1872,14 @@ q8mv_status_t q8mv_pair_info(q8mv_pair_t p, q8mv_pair_info_t *info) {
         const pk::Config &c = p->cfg;
         info->threads_per_cta = c.tpb;
         info->grid = c.grid;
-        info->ctas_per_sm = c.cps;
+        info->resident_ctas = c.slots;
+        info->cluster = c.cluster;
         info->split_up = c.up.split;
         info->split_down = c.down.split;
         info->tiles_up = c.up.tiles;
         info->tiles_down = c.down.tiles;
+        info->tile_cols_up = c.up.tn * pk::kVec;
+        info->tile_cols_down = c.down.tn * pk::kVec;
         info->workspace_bytes = static_cast<int64_t>(p->mem_bytes);
     }
     return Q8MV_OK;

@@ -146,16 +146,34 @@ def test_pair_shapes(q8, orc, K, Nm, No, cta_threads):
 
 
 @pytest.mark.parametrize("split_up,split_down", [(1, 1), (2, 7), (7, 2), (15, 22)])
-def test_pair_forced_splits(q8, orc, split_up, split_down):
+def test_pair_forced_splits_through_the_workspace(q8, orc, split_up, split_down):
     K, Nm, No = 4100, 1376, 1024  # 129 and 43 blocks: ragged last ranges
     A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=split_up * 7 + split_down)
     try:
-        pair = q8.Pair(K, Nm, No, split_up=split_up, split_down=split_down, mode=q8.PAIR_ONE_LAUNCH)
+        pair = q8.Pair(K, Nm, No, split_up=split_up, split_down=split_down, cluster=1, mode=q8.PAIR_ONE_LAUNCH)
     except q8.Q8mvError:
         pytest.skip("split not legal for this shape")
-    assert pair.info["split_up"] == split_up and pair.info["split_down"] == split_down
+    info = pair.info
+    assert info["split_up"] == split_up and info["split_down"] == split_down and info["cluster"] == 1
     H, C, _ = run_pair(pair, A, Wu, Su, Wd, Sd, act_up="relu")
     check_pair(orc, A, Wu, Su, Wd, Sd, H, C, act_up="relu", what=f"splits {split_up}/{split_down}")
+
+
+@pytest.mark.parametrize("cluster", [2, 3, 5, 8])
+@pytest.mark.parametrize("cta_threads", [128, 256])
+@pytest.mark.parametrize("K,Nm,No", [(4100, 1376, 1000), (100, 264, 40)])
+def test_pair_cluster_sizes(q8, orc, cluster, cta_threads, K, Nm, No):
+    """Both products split `cluster` ways and summed through thread-block clusters; with
+    K = 100 (4 blocks) some of a tile's ranges are empty."""
+    A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=cluster * 3 + cta_threads + K)
+    pair = q8.Pair(K, Nm, No, cluster=cluster, cta_threads=cta_threads, mode=q8.PAIR_ONE_LAUNCH)
+    info = pair.info
+    assert info["cluster"] == cluster and info["split_up"] == cluster and info["split_down"] == cluster
+    assert info["grid"] <= info["resident_ctas"]
+    H, C, ok = run_pair(pair, A, Wu, Su, Wd, Sd, act_up="silu")
+    assert ok
+    check_pair(orc, A, Wu, Su, Wd, Sd, H, C, act_up="silu", what=f"cluster {cluster}, {cta_threads} threads")
+    assert pair.check() == 0
 
 
 def integer_pair(K, Nm, No, seed):
@@ -226,7 +244,7 @@ def test_pair_unaligned_weights_take_two_launches(q8, orc):
 
 def test_pair_shapes_the_kernel_cannot_take(q8, orc):
     # N_mid not a multiple of 8: two launches in auto mode, refused in one-launch mode
-    K, Nm, No = 256, 200, 64
+    K, Nm, No = 256, 204, 64
     with pytest.raises(q8.Q8mvError):
         q8.Pair(K, Nm, No, mode=q8.PAIR_ONE_LAUNCH)
     pair = q8.Pair(K, Nm, No)
@@ -234,7 +252,7 @@ def test_pair_shapes_the_kernel_cannot_take(q8, orc):
     A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=4)
     H, C, ok = run_pair(pair, A, Wu, Su, Wd, Sd)
     assert ok
-    check_pair(orc, A, Wu, Su, Wd, Sd, H, C, what="N_mid = 200")
+    check_pair(orc, A, Wu, Su, Wd, Sd, H, C, what="N_mid = 204")
 
 
 def test_pair_barrier_wait_runs_out_and_the_next_call_is_clean(q8, orc):
@@ -259,9 +277,13 @@ def test_pair_rejects_bad_arguments(q8):
     with pytest.raises(q8.Q8mvError):
         q8.Pair(256, 256, 256, cta_threads=64)
     with pytest.raises(q8.Q8mvError):
-        q8.Pair(256, 256, 256, split_up=65)
+        q8.Pair(256, 256, 256, cluster=1, split_up=65)
     with pytest.raises(q8.Q8mvError):
         q8.Pair(256, 256, 256, mode=3)
+    with pytest.raises(q8.Q8mvError):
+        q8.Pair(256, 256, 256, cluster=9)
+    with pytest.raises(q8.Q8mvError):  # splits are fixed by the cluster size
+        q8.Pair(256, 256, 256, cluster=4, split_up=2)
     pair = q8.Pair(256, 256, 256)
     A, Wu, Su, Wd, Sd = random_pair(256, 256, 256, seed=1)
     Ad, Wud, Sud, Wdd, Sdd = _dev(A.reshape(1, -1)), _dev(Wu), _dev(Su), _dev(Wd), _dev(Sd)
