@@ -359,9 +359,11 @@ const char *q8mv_status_string(q8mv_status_t status);
  *
  * With mode Q8MV_PAIR_AUTO (0) one cooperative launch computes both products
  * when N_mid and N_out are multiples of 8, W_up and W_down are 8-byte and
- * S_up, S_down 4-byte aligned: every CTA is resident, takes one item of the up
- * product, issues the first weight loads of its item of the down product,
- * waits at a grid-wide barrier for H to be complete, then computes that item.
+ * S_up, S_down 4-byte aligned: every CTA is resident and takes one item of
+ * each product.  While it computes its up item it already copies the first
+ * blocks of its down item into its shared memory (opts->prefetch), and it
+ * loads the next down block into registers before it waits at a grid-wide
+ * barrier for H to be complete; then it computes its down item.
  * Otherwise (or with Q8MV_PAIR_TWO_LAUNCHES) the two products run as two
  * q8mv_run_fused calls of single-row plans.  Q8MV_PAIR_ONE_LAUNCH makes
  * q8mv_pair_plan fail with INVALID_ARG when the one-launch kernel cannot be
@@ -384,24 +386,24 @@ typedef struct q8mv_pair_s *q8mv_pair_t;
 
 typedef struct {
     int32_t overlap;     /* 0 or 1: launches with programmatic dependent launch, as q8mv_opts_t */
-    int32_t split_up;    /* with cluster == 1: K ranges per column tile of the up product; 0 = planner */
+    int32_t split_up;    /* K ranges per column tile of the up product; 0 = planner (at most 64) */
     int32_t split_down;  /* the same for the down product */
-    int32_t cta_threads; /* 128 or 256; 0 = planner */
+    int32_t cta_threads; /* 128 or 256; 0 = 256 */
     int32_t mode;        /* Q8MV_PAIR_* */
-    int32_t cluster;     /* 0 = planner; 1 = K ranges summed through the workspace (at most 64 per
-                            tile); 2 .. 8 = both products split this many ways, summed through
-                            thread-block clusters of that size */
+    int32_t prefetch;    /* down blocks per CTA copied into shared memory during the up product:
+                            0 = as many as fit (needs N_out % 16 == 0 and, at run time, 16-byte
+                            aligned W_down and S_down), -1 = none, > 0 = at most that many */
 } q8mv_pair_opts_t;
 
 typedef struct {
     int32_t one_launch;       /* 1: q8mv_pair_run launches the pair kernel (pointers allowing) */
     int32_t threads_per_cta;  /* the pair kernel's choices (0 when one_launch is 0) */
     int32_t grid;             /* CTAs: the larger product's tiles x split */
-    int32_t resident_ctas;    /* CTAs of this shape the GPU holds at once */
-    int32_t cluster;          /* 1 = workspace sums, else the cluster size */
+    int32_t ctas_per_sm;      /* resident CTAs per SM (every CTA is resident) */
     int32_t split_up, split_down;
-    int32_t tiles_up, tiles_down;
-    int32_t tile_cols_up, tile_cols_down;  /* 128 or 64 */
+    int32_t tiles_up, tiles_down;  /* 128-column tiles */
+    int32_t prefetch_blocks;  /* down blocks per CTA in shared memory before the barrier */
+    int32_t smem_bytes;       /* dynamic shared memory per CTA */
     int64_t workspace_bytes;
 } q8mv_pair_info_t;
 

@@ -1791,8 +1791,7 @@ q8mv_status_t q8mv_pair_plan(q8mv_pair_t *out, int64_t K, int64_t n_mid, int64_t
     if (o.cta_threads != 0 && o.cta_threads != 128 && o.cta_threads != 256) return Q8MV_ERR_INVALID_ARG;
     if (o.split_up < 0 || o.split_up > pk::kMaxSplitPair || o.split_down < 0 || o.split_down > pk::kMaxSplitPair)
         return Q8MV_ERR_INVALID_ARG;
-    if (o.cluster < 0 || o.cluster > pk::kMaxCluster) return Q8MV_ERR_INVALID_ARG;
-    if ((o.split_up || o.split_down) && o.cluster != 1) return Q8MV_ERR_INVALID_ARG;
+    if (o.prefetch < -1) return Q8MV_ERR_INVALID_ARG;
     if (o.mode != Q8MV_PAIR_AUTO && o.mode != Q8MV_PAIR_ONE_LAUNCH && o.mode != Q8MV_PAIR_TWO_LAUNCHES)
         return Q8MV_ERR_INVALID_ARG;
 
@@ -1819,18 +1818,31 @@ q8mv_status_t q8mv_pair_plan(q8mv_pair_t *out, int64_t K, int64_t n_mid, int64_t
         int prev = 0;
         st = cuda_status(cudaGetDevice(&prev));
         if (st == Q8MV_OK && prev != p->device) st = cuda_status(cudaSetDevice(p->device));
-        // the planner's default: 128-thread CTAs in clusters of the largest
-        // size (up to 8) whose up product still fits one resident wave
-        const int tpb = o.cta_threads ? o.cta_threads : 128;
-        const int c_lo = o.cluster ? o.cluster : 1, c_hi = o.cluster ? o.cluster : pk::kMaxCluster;
-        for (int cl = c_hi; st == Q8MV_OK && cl >= c_lo && !p->one; --cl) {
-            int slots = 0;
-            const cudaError_t e = pk::resident_ctas(tpb, cl, &slots);
-            if (e != cudaSuccess) {
-                cudaGetLastError();  // a cluster size this device cannot schedule
-                continue;
+        // registers decide the resident CTAs per SM; the prefetch of the down
+        // product gets the shared memory they leave over
+        const int tpb = o.cta_threads ? o.cta_threads : 256;
+        int cps = 0, smem_sm = 0, reserved = 0;
+        if (st == Q8MV_OK) st = cuda_status(pk::occupancy(tpb, pk::base_smem(tpb), false, &cps));
+        if (st == Q8MV_OK)
+            st = cuda_status(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p->device));
+        if (st == Q8MV_OK)
+            st = cuda_status(cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, p->device));
+        if (st == Q8MV_OK && cps > 0) {
+            size_t budget = 0;
+            if (o.prefetch >= 0) {
+                const long long per_cta = smem_sm / cps - reserved - 64 - static_cast<long long>(pk::base_smem(tpb));
+                budget = per_cta > 0 ? static_cast<size_t>(per_cta) : 0;
+                if (o.prefetch > 0) budget = std::min(budget, static_cast<size_t>(o.prefetch) * pk::kPfBlockBytes);
             }
-            if (slots > 0) p->one = pk::plan(K, n_mid, n_out, slots, tpb, cl, o.split_up, o.split_down, &p->cfg);
+            p->one = pk::plan(K, n_mid, n_out, p->up->sm_count, cps, tpb, o.split_up, o.split_down, budget, &p->cfg);
+            // the prefetching kernel must keep the same CTAs per SM
+            while (st == Q8MV_OK && p->one && p->cfg.pf_blocks > 0) {
+                int cps_pf = 0;
+                st = cuda_status(pk::occupancy(tpb, p->cfg.smem, true, &cps_pf));
+                if (st != Q8MV_OK || cps_pf >= cps) break;
+                p->cfg.pf_blocks -= 1;
+                p->cfg.smem -= pk::kPfBlockBytes;
+            }
         }
         if (st == Q8MV_OK && p->one) {
             const pk::Config &c = p->cfg;
@@ -1872,14 +1884,13 @@ q8mv_status_t q8mv_pair_info(q8mv_pair_t p, q8mv_pair_info_t *info) {
         const pk::Config &c = p->cfg;
         info->threads_per_cta = c.tpb;
         info->grid = c.grid;
-        info->resident_ctas = c.slots;
-        info->cluster = c.cluster;
+        info->ctas_per_sm = c.cps;
         info->split_up = c.up.split;
         info->split_down = c.down.split;
         info->tiles_up = c.up.tiles;
         info->tiles_down = c.down.tiles;
-        info->tile_cols_up = c.up.tn * pk::kVec;
-        info->tile_cols_down = c.down.tn * pk::kVec;
+        info->prefetch_blocks = c.pf_blocks;
+        info->smem_bytes = static_cast<int32_t>(c.pf_blocks > 0 ? c.smem : c.pf_offset);
         info->workspace_bytes = static_cast<int64_t>(p->mem_bytes);
     }
     return Q8MV_OK;
@@ -1947,7 +1958,8 @@ q8mv_status_t q8mv_pair_run(q8mv_pair_t p, const float *A, const int8_t *W_up, c
     a.err = p->err;
     a.wait_ns = p->wait_ns;
     const bool svec = su % 16 == 0 && sd % 16 == 0;
-    return cuda_status(pk::launch(p->cfg, a, svec, p->overlap, stream));
+    const bool pf = wd % 16 == 0 && sd % 16 == 0;
+    return cuda_status(pk::launch(p->cfg, a, svec, pf, p->overlap, stream));
 }
 
 q8mv_status_t q8mv_pair_check(q8mv_pair_t p, int32_t *device_error) {

@@ -146,33 +146,54 @@ def test_pair_shapes(q8, orc, K, Nm, No, cta_threads):
 
 
 @pytest.mark.parametrize("split_up,split_down", [(1, 1), (2, 7), (7, 2), (15, 22)])
-def test_pair_forced_splits_through_the_workspace(q8, orc, split_up, split_down):
+def test_pair_forced_splits(q8, orc, split_up, split_down):
     K, Nm, No = 4100, 1376, 1024  # 129 and 43 blocks: ragged last ranges
     A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=split_up * 7 + split_down)
     try:
-        pair = q8.Pair(K, Nm, No, split_up=split_up, split_down=split_down, cluster=1, mode=q8.PAIR_ONE_LAUNCH)
+        pair = q8.Pair(K, Nm, No, split_up=split_up, split_down=split_down, mode=q8.PAIR_ONE_LAUNCH)
     except q8.Q8mvError:
         pytest.skip("split not legal for this shape")
     info = pair.info
-    assert info["split_up"] == split_up and info["split_down"] == split_down and info["cluster"] == 1
+    assert info["split_up"] == split_up and info["split_down"] == split_down
     H, C, _ = run_pair(pair, A, Wu, Su, Wd, Sd, act_up="relu")
     check_pair(orc, A, Wu, Su, Wd, Sd, H, C, act_up="relu", what=f"splits {split_up}/{split_down}")
 
 
-@pytest.mark.parametrize("cluster", [2, 3, 5, 8])
+@pytest.mark.parametrize("prefetch", [-1, 1, 5, 0])
 @pytest.mark.parametrize("cta_threads", [128, 256])
-@pytest.mark.parametrize("K,Nm,No", [(4100, 1376, 1000), (100, 264, 40)])
-def test_pair_cluster_sizes(q8, orc, cluster, cta_threads, K, Nm, No):
-    """Both products split `cluster` ways and summed through thread-block clusters; with
-    K = 100 (4 blocks) some of a tile's ranges are empty."""
-    A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=cluster * 3 + cta_threads + K)
-    pair = q8.Pair(K, Nm, No, cluster=cluster, cta_threads=cta_threads, mode=q8.PAIR_ONE_LAUNCH)
+@pytest.mark.parametrize("K,Nm,No", [(4100, 1376, 1008), (100, 264, 48), (512, 4104, 1024)])
+def test_pair_down_blocks_in_shared_memory(q8, orc, prefetch, cta_threads, K, Nm, No):
+    """The down product's first blocks copied into shared memory during the up product: none,
+    1, 5 or as many as fit; N_mid = 264 and 4104 end in a partial block, which is never copied."""
+    A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=prefetch * 3 + cta_threads + K)
+    pair = q8.Pair(K, Nm, No, prefetch=prefetch, cta_threads=cta_threads, mode=q8.PAIR_ONE_LAUNCH)
     info = pair.info
-    assert info["cluster"] == cluster and info["split_up"] == cluster and info["split_down"] == cluster
-    assert info["grid"] <= info["resident_ctas"]
+    if prefetch < 0:
+        assert info["prefetch_blocks"] == 0
+    elif prefetch > 0:
+        assert 0 < info["prefetch_blocks"] <= prefetch
+    else:
+        assert info["prefetch_blocks"] > 0
     H, C, ok = run_pair(pair, A, Wu, Su, Wd, Sd, act_up="silu")
     assert ok
-    check_pair(orc, A, Wu, Su, Wd, Sd, H, C, act_up="silu", what=f"cluster {cluster}, {cta_threads} threads")
+    check_pair(orc, A, Wu, Su, Wd, Sd, H, C, act_up="silu", what=f"prefetch {prefetch}, {cta_threads} threads")
+    assert pair.check() == 0
+
+
+def test_pair_prefetch_needs_16_byte_rows(q8, orc):
+    """N_out % 16 != 0: no shared-memory copy; W_down at an 8-byte offset: the kernel without it runs."""
+    K, Nm, No = 1024, 512, 1000
+    A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=2)
+    pair = q8.Pair(K, Nm, No, mode=q8.PAIR_ONE_LAUNCH)
+    assert pair.info["prefetch_blocks"] == 0
+    H, C, _ = run_pair(pair, A, Wu, Su, Wd, Sd)
+    check_pair(orc, A, Wu, Su, Wd, Sd, H, C, what="N_out = 1000")
+    No = 1024
+    A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=3)
+    pair = q8.Pair(K, Nm, No, mode=q8.PAIR_ONE_LAUNCH)
+    assert pair.info["prefetch_blocks"] > 0
+    H, C, _ = run_pair(pair, A, Wu, Su, Wd, Sd, w_offset=8)
+    check_pair(orc, A, Wu, Su, Wd, Sd, H, C, what="W at an 8-byte offset")
     assert pair.check() == 0
 
 
@@ -277,13 +298,11 @@ def test_pair_rejects_bad_arguments(q8):
     with pytest.raises(q8.Q8mvError):
         q8.Pair(256, 256, 256, cta_threads=64)
     with pytest.raises(q8.Q8mvError):
-        q8.Pair(256, 256, 256, cluster=1, split_up=65)
+        q8.Pair(256, 256, 256, split_up=65)
     with pytest.raises(q8.Q8mvError):
         q8.Pair(256, 256, 256, mode=3)
     with pytest.raises(q8.Q8mvError):
-        q8.Pair(256, 256, 256, cluster=9)
-    with pytest.raises(q8.Q8mvError):  # splits are fixed by the cluster size
-        q8.Pair(256, 256, 256, cluster=4, split_up=2)
+        q8.Pair(256, 256, 256, prefetch=-2)
     pair = q8.Pair(256, 256, 256)
     A, Wu, Su, Wd, Sd = random_pair(256, 256, 256, seed=1)
     Ad, Wud, Sud, Wdd, Sdd = _dev(A.reshape(1, -1)), _dev(Wu), _dev(Su), _dev(Wd), _dev(Sd)
