@@ -348,7 +348,7 @@ const char *q8mv_status_string(q8mv_status_t status);
  * each product the Q8_0 matvec above ("Q8_0 matvec" page) and each epilogue
  * the fused epilogue of q8mv_run_fused ("dot and tensor cores" page, "The
  * fused epilogue"), fused into one launch ("fusing the matvec pair
- * up -> down" of a feed-forward block).
+ * up -> down" of a feed-forward block) or chained as two.
  *
  * Tensors (device memory of the pair's GPU, contiguous, row-major):
  *     A       f32 [K]                     activation row
@@ -357,17 +357,18 @@ const char *q8mv_status_string(q8mv_status_t status);
  *     W_down  i8  [N_mid, N_out]  S_down f32 [ceil(N_mid/32), N_out]
  *     C       f32 [N_out]                 output, overwritten
  *
- * With mode Q8MV_PAIR_AUTO (0) one cooperative launch computes both products
- * when N_mid and N_out are multiples of 8, W_up and W_down are 8-byte and
- * S_up, S_down 4-byte aligned: every CTA is resident and takes one item of
- * each product.  While it computes its up item it already copies the first
- * blocks of its down item into its shared memory (opts->prefetch), and it
- * loads the next down block into registers before it waits at a grid-wide
- * barrier for H to be complete; then it computes its down item.
- * Otherwise (or with Q8MV_PAIR_TWO_LAUNCHES) the two products run as two
- * q8mv_run_fused calls of single-row plans.  Q8MV_PAIR_ONE_LAUNCH makes
- * q8mv_pair_plan fail with INVALID_ARG when the one-launch kernel cannot be
- * planned for the shapes.
+ * Modes.  Q8MV_PAIR_AUTO (0) and Q8MV_PAIR_TWO_LAUNCHES run the products as
+ * two q8mv_run_fused calls of single-row plans, the second launched with
+ * programmatic dependent launch when opts->overlap is 1 (its first weight
+ * loads then overlap the first call's tail).  Q8MV_PAIR_ONE_LAUNCH runs both
+ * in one cooperative launch of the pair kernel: every CTA is resident, takes
+ * one item of the up product, loads the first weight block of its item of
+ * the down product, waits at a grid-wide barrier for H to be complete, then
+ * computes that item; it needs N_mid and N_out to be multiples of 8
+ * (q8mv_pair_plan fails with INVALID_ARG otherwise) and, at run time, W_up and
+ * W_down 8-byte and S_up, S_down 4-byte aligned (else the call takes two
+ * launches).  AUTO takes two launches because they measured faster on GB300
+ * (7B FFN pair: 24.3 us against 26.1 us).
  *
  * Rules: those of q8mv_run_fused for each product; in addition H may overlap
  * none of A, W_up, S_up, W_down, S_down, C, nor epi_down's bias and residual,
@@ -390,20 +391,15 @@ typedef struct {
     int32_t split_down;  /* the same for the down product */
     int32_t cta_threads; /* 128 or 256; 0 = 256 */
     int32_t mode;        /* Q8MV_PAIR_* */
-    int32_t prefetch;    /* down blocks per CTA copied into shared memory during the up product:
-                            0 = as many as fit (needs N_out % 16 == 0 and, at run time, 16-byte
-                            aligned W_down and S_down), -1 = none, > 0 = at most that many */
 } q8mv_pair_opts_t;
 
 typedef struct {
     int32_t one_launch;       /* 1: q8mv_pair_run launches the pair kernel (pointers allowing) */
     int32_t threads_per_cta;  /* the pair kernel's choices (0 when one_launch is 0) */
     int32_t grid;             /* CTAs: the larger product's tiles x split */
-    int32_t ctas_per_sm;      /* resident CTAs per SM (every CTA is resident) */
+    int32_t ctas_per_sm;
     int32_t split_up, split_down;
     int32_t tiles_up, tiles_down;  /* 128-column tiles */
-    int32_t prefetch_blocks;  /* down blocks per CTA in shared memory before the barrier */
-    int32_t smem_bytes;       /* dynamic shared memory per CTA */
     int64_t workspace_bytes;
 } q8mv_pair_info_t;
 

@@ -59,14 +59,13 @@ class Epilogue(ctypes.Structure):
 
 class PairOpts(ctypes.Structure):
     _fields_ = [("overlap", ctypes.c_int32), ("split_up", ctypes.c_int32), ("split_down", ctypes.c_int32),
-                ("cta_threads", ctypes.c_int32), ("mode", ctypes.c_int32), ("prefetch", ctypes.c_int32)]
+                ("cta_threads", ctypes.c_int32), ("mode", ctypes.c_int32)]
 
 
 class PairInfo(ctypes.Structure):
     _fields_ = [("one_launch", ctypes.c_int32), ("threads_per_cta", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("split_up", ctypes.c_int32), ("split_down", ctypes.c_int32),
-                ("tiles_up", ctypes.c_int32), ("tiles_down", ctypes.c_int32), ("prefetch_blocks", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64)]
+                ("tiles_up", ctypes.c_int32), ("tiles_down", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -332,10 +331,10 @@ class Pair:
     with W_down [N_mid, N_out], in one launch when the shapes and pointers allow."""
 
     def __init__(self, K: int, N_mid: int, N_out: int, device: int = -1, overlap: int = 0, split_up: int = 0,
-                 split_down: int = 0, cta_threads: int = 0, mode: int = PAIR_AUTO, prefetch: int = 0):
+                 split_down: int = 0, cta_threads: int = 0, mode: int = PAIR_AUTO):
         self.K, self.N_mid, self.N_out = int(K), int(N_mid), int(N_out)
         handle = ctypes.c_void_p()
-        o = PairOpts(overlap, split_up, split_down, cta_threads, mode, prefetch)
+        o = PairOpts(overlap, split_up, split_down, cta_threads, mode)
         st = _lib.q8mv_pair_plan(ctypes.byref(handle), self.K, self.N_mid, self.N_out, int(device), ctypes.byref(o))
         if st != Q8MV_OK:
             raise Q8mvError(st, f"q8mv_pair_plan(K={K}, N_mid={N_mid}, N_out={N_out})")

@@ -11,23 +11,18 @@
 // can only start once every output of the up product is written.
 //
 // Design.  One cooperative grid of G CTAs, all resident at once, runs both
-// products.  CTA i takes item i of each product (column tile i / split, K
-// range i % split), computed as the register kernel computes a CTA of a split
-// that sums through the workspace: V = 8 bytes of a row per thread over
-// 128-column tiles, the activations staged in shared memory, the K groups
-// summed in shared memory in group order, and the K ranges of a tile summed in
-// range order by the CTA that takes the tile's last ticket.  A grid barrier
-// separates the products; H is read back through L2 (it was written during
-// this launch).
-//
-// What one launch adds over two: the down product's weights never depend on
-// H, and shared memory that the up product does not use stays with the CTA
-// across the barrier.  With PF, every CTA copies the first pf_blocks whole
-// blocks of its down range (weights and scales) into its shared memory with
-// cp.async as soon as it starts, and loads its first down block after those
-// into registers before it waits at the barrier.  The down product's weight
-// stream is then requested while the up product runs, and after the barrier
-// little but arithmetic is left.
+// products.  CTA i takes item i of the up product (column tile i / split_up,
+// K range i % split_up), computed exactly as the register kernel computes a
+// CTA of a split that sums through the workspace: V = 8 bytes of a row per
+// thread, the activations staged in shared memory, the K groups summed in
+// shared memory in group order, and the K ranges of a tile summed in range
+// order by the CTA that takes the tile's last ticket.  Before it waits at the
+// grid barrier that separates the products, the CTA already issues the loads
+// of the first weight block and scales of its item of the down product
+// (weights never depend on H), so the down product's weight stream starts
+// while the last up tiles finish and while the barrier resolves, instead of
+// after a second launch has found room on the SMs.  H is read back through L2
+// (it was written during this launch).
 //
 // The grid barrier waits for every CTA's arrival with a bounded spin (about
 // 2 s by default); if the bound runs out the CTA records error bit 1 in the
@@ -66,8 +61,6 @@ struct Params {
     unsigned *bar;        // [2]: arrivals, generation (zero arrivals between calls)
     int *err;             // error word (kErrBarrier)
     uint64_t wait_ns;
-    int pf_blocks;        // PF: down blocks per CTA copied into shared memory
-    int pf_offset;        // PF: byte offset of that copy in dynamic shared memory
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -76,18 +69,15 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-                 "l"(src)
-                 : "memory");
-}
-
-// Weights and scales of block b of this thread's strip in phase p, loaded
-// into registers, if the block is whole and the strip lies below N.
+// The first weight block and scales of this thread in item (tile, range) of
+// phase p, if the block is whole (the same rule as the register kernel).
 template <bool SVEC>
-__device__ __forceinline__ bool prefetch_block(const Phase &p, int tile, int b, int b_end,
+__device__ __forceinline__ bool prefetch_block(const Phase &p, int tile, int range,
                                                uint32_t (&w)[rk::kBlk][(kVec + 3) / 4], float (&s)[kVec]) {
-    const int64_t n0 = static_cast<int64_t>(tile) * kTileCols + static_cast<int64_t>(threadIdx.x % kTn) * kVec;
+    const int tid = threadIdx.x;
+    const int64_t n0 = static_cast<int64_t>(tile) * (kTn * kVec) + static_cast<int64_t>(tid & (kTn - 1)) * kVec;
+    const int b = range * p.bps + (tid / kTn);
+    const int b_end = min(p.KB, range * p.bps + p.bps);
     if (n0 >= p.N || b >= b_end || static_cast<int64_t>(b + 1) * rk::kBlk > p.K) return false;
     const int8_t *w_ptr = p.W + static_cast<int64_t>(b) * rk::kBlk * p.N + n0;
 #pragma unroll
@@ -96,45 +86,18 @@ __device__ __forceinline__ bool prefetch_block(const Phase &p, int tile, int b, 
     return true;
 }
 
-// Blocks b0 .. b0 + nb - 1 of tile `tile` (all whole; N a multiple of 16, W
-// and S 16-byte aligned) into shared memory: block j's 32 x 128 weight bytes
-// at dst + j * kPfBlockBytes, row-major, its 128 scales right after them.
-// Columns at or past N are not copied.
-template <int TPB>
-__device__ __forceinline__ void copy_blocks(const Phase &p, int tile, int b0, int nb, uint8_t *dst) {
-    const int64_t col0 = static_cast<int64_t>(tile) * kTileCols;
-    constexpr int w_chunks = rk::kBlk * kTileCols / 16;  // 256 per block
-    constexpr int s_chunks = kTileCols * 4 / 16;         // 32 per block
-    for (int i = threadIdx.x; i < nb * (w_chunks + s_chunks); i += TPB) {
-        const int j = i / (w_chunks + s_chunks);
-        const int q = i % (w_chunks + s_chunks);
-        uint8_t *blk = dst + j * kPfBlockBytes;
-        const int64_t b = b0 + j;
-        if (q < w_chunks) {
-            const int r = q / (kTileCols / 16), c = (q % (kTileCols / 16)) * 16;
-            if (col0 + c < p.N) cp_async16(blk + r * kTileCols + c, p.W + (b * rk::kBlk + r) * p.N + col0 + c);
-        } else {
-            const int c = (q - w_chunks) * 4;
-            if (col0 + c < p.N) cp_async16(blk + rk::kBlk * kTileCols + c * 4, p.S + b * p.N + col0 + c);
-        }
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
 // Item (tile, range) of phase p.  COHERENT: the activations were written
 // during this launch, so they are read through L2, not the read-only path.
-// pf_blocks > 0: the range's first pf_blocks blocks are in shared memory at
-// pf (copy_blocks).  `w`, `s` hold the thread's first block read from global
-// memory if `prefetched`.
 template <bool SVEC, int TPB, bool COHERENT>
 __device__ __forceinline__ void run_item(const Phase &p, int tile, int range, float *smem, unsigned &s_is_last,
                                          uint32_t (&w)[rk::kBlk][(kVec + 3) / 4], float (&s)[kVec],
-                                         bool prefetched, const uint8_t *pf, int pf_blocks) {
+                                         bool prefetched) {
     constexpr int V = kVec;
     const int tid = threadIdx.x;
-    const int tn_i = tid % kTn;
+    const int tn_i = tid & (kTn - 1);
     const int gk_i = tid / kTn;
-    const int64_t col0 = static_cast<int64_t>(tile) * kTileCols;
+    constexpr int tile_cols = kTn * V;
+    const int64_t col0 = static_cast<int64_t>(tile) * tile_cols;
     const int64_t n0 = col0 + static_cast<int64_t>(tn_i) * V;
     const bool active = n0 < p.N;  // V divides N, so an active strip is whole
     const int b_begin = range * p.bps;
@@ -157,35 +120,11 @@ __device__ __forceinline__ void run_item(const Phase &p, int tile, int range, fl
 
         for (; b < c_end; b += p.gk) {
             const float *a_blk = smem + (b - c_begin) * rk::kBlk;
+            const int8_t *w_ptr = p.W + static_cast<int64_t>(b) * rk::kBlk * p.N + n0;
+            const int64_t rows = min(static_cast<int64_t>(rk::kBlk), p.K - static_cast<int64_t>(b) * rk::kBlk);
             float part[V];
 #pragma unroll
             for (int j = 0; j < V; ++j) part[j] = 0.0f;
-            if (b - b_begin < pf_blocks) {
-                // a block copied into shared memory before the barrier
-                const uint8_t *blk = pf + (b - b_begin) * kPfBlockBytes;
-#pragma unroll
-                for (int r = 0; r < rk::kBlk; r += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(a_blk + r);
-                    uint32_t wr[4][2];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(blk + (r + q) * kTileCols + tn_i * V);
-                        wr[q][0] = v.x;
-                        wr[q][1] = v.y;
-                    }
-                    rk::fma_row<V>(a4.x, wr[0], part);
-                    rk::fma_row<V>(a4.y, wr[1], part);
-                    rk::fma_row<V>(a4.z, wr[2], part);
-                    rk::fma_row<V>(a4.w, wr[3], part);
-                }
-                const float4 *sp = reinterpret_cast<const float4 *>(blk + rk::kBlk * kTileCols) + 2 * tn_i;
-                const float4 s0 = sp[0], s1 = sp[1];
-                const float sb[V] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-                rk::fold_scale<V>(part, sb, acc);
-                continue;
-            }
-            const int8_t *w_ptr = p.W + static_cast<int64_t>(b) * rk::kBlk * p.N + n0;
-            const int64_t rows = min(static_cast<int64_t>(rk::kBlk), p.K - static_cast<int64_t>(b) * rk::kBlk);
             const bool had_prefetch = prefetched;
             if (rows == rk::kBlk) {
                 if (!prefetched) {
@@ -216,18 +155,18 @@ __device__ __forceinline__ void run_item(const Phase &p, int tile, int range, fl
 
     // the K groups of this CTA, summed in shared memory in group order
     __syncthreads();
-    float *red = smem;  // [gk][kTileCols]
+    float *red = smem;  // [gk][tile_cols]
     if (active) {
 #pragma unroll
-        for (int j = 0; j < V; ++j) red[gk_i * kTileCols + tn_i * V + j] = acc[j];
+        for (int j = 0; j < V; ++j) red[gk_i * tile_cols + tn_i * V + j] = acc[j];
     }
     __syncthreads();
     const bool split = p.split > 1;
-    for (int c = tid; c < kTileCols; c += TPB) {
+    for (int c = tid; c < tile_cols; c += TPB) {
         const int64_t n = col0 + c;
         if (n >= p.N) break;
         float v = red[c];
-        for (int g = 1; g < p.gk; ++g) v += red[g * kTileCols + c];
+        for (int g = 1; g < p.gk; ++g) v += red[g * tile_cols + c];
         if (split)
             p.ws[static_cast<int64_t>(range) * p.N + n] = v;
         else
@@ -245,7 +184,7 @@ __device__ __forceinline__ void run_item(const Phase &p, int tile, int range, fl
     __syncthreads();
     if (!s_is_last) return;
     __threadfence();
-    for (int c = tid; c < kTileCols; c += TPB) {
+    for (int c = tid; c < tile_cols; c += TPB) {
         const int64_t n = col0 + c;
         if (n >= p.N) break;
         float v = __ldcg(p.ws + n);
@@ -257,21 +196,21 @@ __device__ __forceinline__ void run_item(const Phase &p, int tile, int range, fl
 
 // Every CTA of the grid arrives once; the last to arrive resets the count and
 // advances the generation, which the others wait for (bounded).
-__device__ __forceinline__ void grid_barrier(const Params &pp) {
+__device__ __forceinline__ void grid_barrier(unsigned *bar, const Params &pp) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        volatile unsigned *gen = pp.bar + 1;
+        volatile unsigned *gen = bar + 1;
         const unsigned g0 = *gen;  // read before arriving: it cannot advance before this CTA arrives
         __threadfence();           // this CTA's H, partial rows and tickets before its arrival
-        const unsigned arrived = atomicAdd(pp.bar, 1u);
+        const unsigned arrived = atomicAdd(bar, 1u);
         if (arrived == gridDim.x - 1) {
-            atomicExch(pp.bar, 0u);
+            atomicExch(bar, 0u);
             __threadfence();
-            atomicAdd(pp.bar + 1, 1u);
+            atomicAdd(bar + 1, 1u);
         } else {
             const uint64_t t0 = globaltimer();
             while (*gen == g0) {
-                __nanosleep(64);
+                __nanosleep(100);
                 if (globaltimer() - t0 > pp.wait_ns) {
                     atomicOr(pp.err, kErrBarrier);
                     break;
@@ -283,53 +222,29 @@ __device__ __forceinline__ void grid_barrier(const Params &pp) {
     __syncthreads();
 }
 
-template <bool SVEC, int TPB, bool PF>
+template <bool SVEC, int TPB>
 __global__ void __launch_bounds__(TPB, rk::regs_min_blocks<kVec, TPB>()) q8mv_pair_kernel(const Params pp) {
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_is_last;
     uint32_t w[rk::kBlk][(kVec + 3) / 4];
     float s[kVec];
     const int item = static_cast<int>(blockIdx.x);
-    const int g = static_cast<int>(threadIdx.x) / kTn;
-
-    const bool up = item < pp.up.tiles * pp.up.split;
-    const int up_tile = up ? item / pp.up.split : 0, up_range = up ? item % pp.up.split : 0;
-    const int up_begin = up_range * pp.up.bps, up_end = min(pp.up.KB, up_begin + pp.up.bps);
-    const bool down = item < pp.down.tiles * pp.down.split;
-    const int dn_tile = down ? item / pp.down.split : 0, dn_range = down ? item % pp.down.split : 0;
-    const int dn_begin = dn_range * pp.down.bps, dn_end = min(pp.down.KB, dn_begin + pp.down.bps);
-    // whole blocks of the down range that go to shared memory (a partial last
-    // block of K is never copied)
-    int pf_blocks = 0;
-    uint8_t *pf = reinterpret_cast<uint8_t *>(smem) + pp.pf_offset;
-    if (PF && down) {
-        const int whole = static_cast<int>(min(static_cast<int64_t>(dn_end), pp.down.K / rk::kBlk)) - dn_begin;
-        pf_blocks = max(0, min(pp.pf_blocks, whole));
-    }
 
     // up product: the first weight block before the wait for the previous
-    // kernel in the stream (programmatic dependent launch), A after it; the
-    // down product's copy into shared memory starts alongside
-    const bool pf_up = up && prefetch_block<SVEC>(pp.up, up_tile, up_begin + g, up_end, w, s);
-    if (PF && pf_blocks > 0) copy_blocks<TPB>(pp.down, dn_tile, dn_begin, pf_blocks, pf);
+    // kernel in the stream (programmatic dependent launch), A after it
+    const bool up = item < pp.up.tiles * pp.up.split;
+    const int up_tile = up ? item / pp.up.split : 0, up_range = up ? item % pp.up.split : 0;
+    bool pf = up && prefetch_block<SVEC>(pp.up, up_tile, up_range, w, s);
     rk::pdl_launch_dependents();
     rk::pdl_wait();
-    if (up) run_item<SVEC, TPB, false>(pp.up, up_tile, up_range, smem, s_is_last, w, s, pf_up, nullptr, 0);
+    if (up) run_item<SVEC, TPB, false>(pp.up, up_tile, up_range, smem, s_is_last, w, s, pf);
 
-    // down product: the thread's first block after the shared-memory copy,
-    // into registers before the grid barrier, H after it
-    bool pf_dn = false;
-    if (down) {
-        int b = dn_begin + g;
-        if (pf_blocks > g) b += ((pf_blocks - g + pp.down.gk - 1) / pp.down.gk) * pp.down.gk;
-        pf_dn = prefetch_block<SVEC>(pp.down, dn_tile, b, dn_end, w, s);
-    }
-    grid_barrier(pp);
-    if (PF) {
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        __syncthreads();
-    }
-    if (down) run_item<SVEC, TPB, true>(pp.down, dn_tile, dn_range, smem, s_is_last, w, s, pf_dn, pf, pf_blocks);
+    // down product: its first weight block before the grid barrier, H after it
+    const bool down = item < pp.down.tiles * pp.down.split;
+    const int dn_tile = down ? item / pp.down.split : 0, dn_range = down ? item % pp.down.split : 0;
+    pf = down && prefetch_block<SVEC>(pp.down, dn_tile, dn_range, w, s);
+    grid_barrier(pp.bar, pp);
+    if (down) run_item<SVEC, TPB, true>(pp.down, dn_tile, dn_range, smem, s_is_last, w, s, pf);
 }
 
 }  // namespace pk

@@ -1742,9 +1742,10 @@ extern "C" q8mv_status_t q8mv_run_noalloc(int64_t K, int64_t N, const float *A, 
 // ---------------------------------------------------------------------------
 // Feed-forward pair: H = epi_up(A . W_up), C = epi_down(H . W_down)
 //
-// One launch of the pair kernel (pair_kernel.cuh) when the shapes and the
-// pointers allow it, else two launches of the single-row plans (which take any
-// shape and alignment).  The pair plan owns the pair kernel's workspace
+// Two launches of the single-row plans (any shape and alignment), chained by
+// programmatic dependent launch when the pair overlaps; or, when asked for,
+// one launch of the pair kernel (pair_kernel.cuh) where the shapes and the
+// pointers allow it.  The pair plan owns the pair kernel's workspace
 // (partial rows and counters of both products, the grid barrier and an error
 // word) and the two single-row plans.
 // ---------------------------------------------------------------------------
@@ -1791,7 +1792,6 @@ q8mv_status_t q8mv_pair_plan(q8mv_pair_t *out, int64_t K, int64_t n_mid, int64_t
     if (o.cta_threads != 0 && o.cta_threads != 128 && o.cta_threads != 256) return Q8MV_ERR_INVALID_ARG;
     if (o.split_up < 0 || o.split_up > pk::kMaxSplitPair || o.split_down < 0 || o.split_down > pk::kMaxSplitPair)
         return Q8MV_ERR_INVALID_ARG;
-    if (o.prefetch < -1) return Q8MV_ERR_INVALID_ARG;
     if (o.mode != Q8MV_PAIR_AUTO && o.mode != Q8MV_PAIR_ONE_LAUNCH && o.mode != Q8MV_PAIR_TWO_LAUNCHES)
         return Q8MV_ERR_INVALID_ARG;
 
@@ -1814,36 +1814,17 @@ q8mv_status_t q8mv_pair_plan(q8mv_pair_t *out, int64_t K, int64_t n_mid, int64_t
     }
     p->device = p->up->device;
 
-    if (o.mode != Q8MV_PAIR_TWO_LAUNCHES) {
+    // the one-launch kernel only when asked for: two launches chained by
+    // programmatic dependent launch measured faster on every shape tried
+    if (o.mode == Q8MV_PAIR_ONE_LAUNCH) {
         int prev = 0;
         st = cuda_status(cudaGetDevice(&prev));
         if (st == Q8MV_OK && prev != p->device) st = cuda_status(cudaSetDevice(p->device));
-        // registers decide the resident CTAs per SM; the prefetch of the down
-        // product gets the shared memory they leave over
         const int tpb = o.cta_threads ? o.cta_threads : 256;
-        int cps = 0, smem_sm = 0, reserved = 0;
-        if (st == Q8MV_OK) st = cuda_status(pk::occupancy(tpb, pk::base_smem(tpb), false, &cps));
-        if (st == Q8MV_OK)
-            st = cuda_status(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p->device));
-        if (st == Q8MV_OK)
-            st = cuda_status(cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, p->device));
-        if (st == Q8MV_OK && cps > 0) {
-            size_t budget = 0;
-            if (o.prefetch >= 0) {
-                const long long per_cta = smem_sm / cps - reserved - 64 - static_cast<long long>(pk::base_smem(tpb));
-                budget = per_cta > 0 ? static_cast<size_t>(per_cta) : 0;
-                if (o.prefetch > 0) budget = std::min(budget, static_cast<size_t>(o.prefetch) * pk::kPfBlockBytes);
-            }
-            p->one = pk::plan(K, n_mid, n_out, p->up->sm_count, cps, tpb, o.split_up, o.split_down, budget, &p->cfg);
-            // the prefetching kernel must keep the same CTAs per SM
-            while (st == Q8MV_OK && p->one && p->cfg.pf_blocks > 0) {
-                int cps_pf = 0;
-                st = cuda_status(pk::occupancy(tpb, p->cfg.smem, true, &cps_pf));
-                if (st != Q8MV_OK || cps_pf >= cps) break;
-                p->cfg.pf_blocks -= 1;
-                p->cfg.smem -= pk::kPfBlockBytes;
-            }
-        }
+        int cps = 0;
+        if (st == Q8MV_OK) st = cuda_status(pk::occupancy(tpb, &cps));
+        if (st == Q8MV_OK && cps > 0)
+            p->one = pk::plan(K, n_mid, n_out, p->up->sm_count, cps, tpb, o.split_up, o.split_down, &p->cfg);
         if (st == Q8MV_OK && p->one) {
             const pk::Config &c = p->cfg;
             auto up16 = [](size_t b) { return (b + 255) / 256 * 256; };
@@ -1889,8 +1870,6 @@ q8mv_status_t q8mv_pair_info(q8mv_pair_t p, q8mv_pair_info_t *info) {
         info->split_down = c.down.split;
         info->tiles_up = c.up.tiles;
         info->tiles_down = c.down.tiles;
-        info->prefetch_blocks = c.pf_blocks;
-        info->smem_bytes = static_cast<int32_t>(c.pf_blocks > 0 ? c.smem : c.pf_offset);
         info->workspace_bytes = static_cast<int64_t>(p->mem_bytes);
     }
     return Q8MV_OK;
@@ -1958,8 +1937,7 @@ q8mv_status_t q8mv_pair_run(q8mv_pair_t p, const float *A, const int8_t *W_up, c
     a.err = p->err;
     a.wait_ns = p->wait_ns;
     const bool svec = su % 16 == 0 && sd % 16 == 0;
-    const bool pf = wd % 16 == 0 && sd % 16 == 0;
-    return cuda_status(pk::launch(p->cfg, a, svec, pf, p->overlap, stream));
+    return cuda_status(pk::launch(p->cfg, a, svec, p->overlap, stream));
 }
 
 q8mv_status_t q8mv_pair_check(q8mv_pair_t p, int32_t *device_error) {

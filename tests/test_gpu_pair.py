@@ -1,7 +1,8 @@
 """GPU parity of the feed-forward pair (q8mv_pair_plan / q8mv_pair_run).
 
 H = epi_up(A . W_up) and C = epi_down(H . W_down), in one cooperative launch
-(the pair kernel) or as two single-row calls.  H is checked against the fp64
+(the pair kernel, mode PAIR_ONE_LAUNCH) or as two single-row calls (the
+default).  H is checked against the fp64
 oracle's product of A and its epilogue; C against the oracle's product of the
 GPU's own H (exact in fp64) and its epilogue, each within
 ``oracle.epilogue_tolerance`` (1.13 (1e-5 sum|x w s| + 1e-6) + 1e-6 of the
@@ -116,12 +117,13 @@ def random_pair(K, Nm, No, seed):
     return A, Wu, Su, Wd, Sd
 
 
-@pytest.mark.parametrize("mode", [0, 2])
-def test_pair_7b_ffn(q8, orc, mode):
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("overlap", [0, 1])
+def test_pair_7b_ffn(q8, orc, mode, overlap):
     """7B FFN up (4096 x 11008, SiLU + bias) then down (11008 x 4096, + residual)."""
     A, Wu, Su, Wd, Sd, bias_up, residual = ffn_inputs()
-    pair = q8.Pair(4096, 11008, 4096, mode=mode)
-    assert pair.info["one_launch"] == (1 if mode == 0 else 0)
+    pair = q8.Pair(4096, 11008, 4096, mode=mode, overlap=overlap)
+    assert pair.info["one_launch"] == (1 if mode == 1 else 0)
     H, C, ok = run_pair(pair, A, Wu, Su, Wd, Sd, act_up="silu", bias_up=bias_up, residual=residual)
     assert ok
     check_pair(orc, A, Wu, Su, Wd, Sd, H, C, act_up="silu", bias_up=bias_up, residual=residual,
@@ -135,7 +137,7 @@ def test_pair_7b_ffn(q8, orc, mode):
 def test_pair_shapes(q8, orc, K, Nm, No, cta_threads):
     """Ragged K (partial last blocks in both products), ragged last column tiles, one-block products."""
     A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=K + Nm + No)
-    pair = q8.Pair(K, Nm, No, cta_threads=cta_threads)
+    pair = q8.Pair(K, Nm, No, cta_threads=cta_threads, mode=q8.PAIR_ONE_LAUNCH)
     info = pair.info
     assert info["one_launch"] == 1 and info["threads_per_cta"] == cta_threads
     assert info["grid"] == max(info["tiles_up"] * info["split_up"], info["tiles_down"] * info["split_down"])
@@ -153,48 +155,9 @@ def test_pair_forced_splits(q8, orc, split_up, split_down):
         pair = q8.Pair(K, Nm, No, split_up=split_up, split_down=split_down, mode=q8.PAIR_ONE_LAUNCH)
     except q8.Q8mvError:
         pytest.skip("split not legal for this shape")
-    info = pair.info
-    assert info["split_up"] == split_up and info["split_down"] == split_down
+    assert pair.info["split_up"] == split_up and pair.info["split_down"] == split_down
     H, C, _ = run_pair(pair, A, Wu, Su, Wd, Sd, act_up="relu")
     check_pair(orc, A, Wu, Su, Wd, Sd, H, C, act_up="relu", what=f"splits {split_up}/{split_down}")
-
-
-@pytest.mark.parametrize("prefetch", [-1, 1, 5, 0])
-@pytest.mark.parametrize("cta_threads", [128, 256])
-@pytest.mark.parametrize("K,Nm,No", [(4100, 1376, 1008), (100, 264, 48), (512, 4104, 1024)])
-def test_pair_down_blocks_in_shared_memory(q8, orc, prefetch, cta_threads, K, Nm, No):
-    """The down product's first blocks copied into shared memory during the up product: none,
-    1, 5 or as many as fit; N_mid = 264 and 4104 end in a partial block, which is never copied."""
-    A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=prefetch * 3 + cta_threads + K)
-    pair = q8.Pair(K, Nm, No, prefetch=prefetch, cta_threads=cta_threads, mode=q8.PAIR_ONE_LAUNCH)
-    info = pair.info
-    if prefetch < 0:
-        assert info["prefetch_blocks"] == 0
-    elif prefetch > 0:
-        assert 0 < info["prefetch_blocks"] <= prefetch
-    else:
-        assert info["prefetch_blocks"] > 0
-    H, C, ok = run_pair(pair, A, Wu, Su, Wd, Sd, act_up="silu")
-    assert ok
-    check_pair(orc, A, Wu, Su, Wd, Sd, H, C, act_up="silu", what=f"prefetch {prefetch}, {cta_threads} threads")
-    assert pair.check() == 0
-
-
-def test_pair_prefetch_needs_16_byte_rows(q8, orc):
-    """N_out % 16 != 0: no shared-memory copy; W_down at an 8-byte offset: the kernel without it runs."""
-    K, Nm, No = 1024, 512, 1000
-    A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=2)
-    pair = q8.Pair(K, Nm, No, mode=q8.PAIR_ONE_LAUNCH)
-    assert pair.info["prefetch_blocks"] == 0
-    H, C, _ = run_pair(pair, A, Wu, Su, Wd, Sd)
-    check_pair(orc, A, Wu, Su, Wd, Sd, H, C, what="N_out = 1000")
-    No = 1024
-    A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=3)
-    pair = q8.Pair(K, Nm, No, mode=q8.PAIR_ONE_LAUNCH)
-    assert pair.info["prefetch_blocks"] > 0
-    H, C, _ = run_pair(pair, A, Wu, Su, Wd, Sd, w_offset=8)
-    check_pair(orc, A, Wu, Su, Wd, Sd, H, C, what="W at an 8-byte offset")
-    assert pair.check() == 0
 
 
 def integer_pair(K, Nm, No, seed):
@@ -208,7 +171,7 @@ def integer_pair(K, Nm, No, seed):
     return A, Wu, Su, Wd, Sd
 
 
-@pytest.mark.parametrize("mode", [0, 2])
+@pytest.mark.parametrize("mode", [1, 2])
 def test_pair_integer_data_bit_exact(q8, orc, mode):
     K, Nm, No = 1000, 1504, 1032
     A, Wu, Su, Wd, Sd = integer_pair(K, Nm, No, seed=11)
@@ -223,19 +186,20 @@ def test_pair_integer_data_bit_exact(q8, orc, mode):
 
 def test_pair_repeated_calls_are_bit_identical(q8):
     A, Wu, Su, Wd, Sd, bias_up, residual = ffn_inputs(seed=5)
-    pair = q8.Pair(4096, 11008, 4096, overlap=1)
+    pair = q8.Pair(4096, 11008, 4096, overlap=1, mode=q8.PAIR_ONE_LAUNCH)
     H1, C1, _ = run_pair(pair, A, Wu, Su, Wd, Sd, act_up="silu", bias_up=bias_up, residual=residual)
     H2, C2, _ = run_pair(pair, A, Wu, Su, Wd, Sd, act_up="silu", bias_up=bias_up, residual=residual, calls=5)
     assert np.array_equal(H1, H2) and np.array_equal(C1, C2)
     assert pair.check() == 0
 
 
-def test_pair_dependent_chain_with_overlap(q8, orc):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_pair_dependent_chain_with_overlap(q8, orc, mode):
     """Back-to-back overlapped pairs where each call's A is the previous call's C."""
     import torch
 
     A, Wu, Su, Wd, Sd, bias_up, residual = ffn_inputs(seed=9)
-    pair = q8.Pair(4096, 11008, 4096, overlap=1)
+    pair = q8.Pair(4096, 11008, 4096, overlap=1, mode=mode)
     Wud, Sud, Wdd, Sdd = _dev(Wu), _dev(Su), _dev(Wd), _dev(Sd)
     bu, res = _dev(bias_up), _dev(residual.reshape(1, -1))
     steps = 6
@@ -256,7 +220,7 @@ def test_pair_dependent_chain_with_overlap(q8, orc):
 def test_pair_unaligned_weights_take_two_launches(q8, orc):
     K, Nm, No = 512, 1024, 256
     A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=21)
-    pair = q8.Pair(K, Nm, No)
+    pair = q8.Pair(K, Nm, No, mode=q8.PAIR_ONE_LAUNCH)
     assert pair.info["one_launch"] == 1
     H, C, ok = run_pair(pair, A, Wu, Su, Wd, Sd, act_up="silu", w_offset=3)
     assert ok
@@ -281,7 +245,7 @@ def test_pair_barrier_wait_runs_out_and_the_next_call_is_clean(q8, orc):
     bit 1 and finishes; with the bound restored the next call is correct."""
     K, Nm, No = 4096, 2048, 1024
     A, Wu, Su, Wd, Sd = random_pair(K, Nm, No, seed=8)
-    pair = q8.Pair(K, Nm, No)
+    pair = q8.Pair(K, Nm, No, mode=q8.PAIR_ONE_LAUNCH)
     pair.set_wait(1)
     run_pair(pair, A, Wu, Su, Wd, Sd)  # H and C undefined; the call must return
     assert pair.check() == 1
@@ -301,8 +265,6 @@ def test_pair_rejects_bad_arguments(q8):
         q8.Pair(256, 256, 256, split_up=65)
     with pytest.raises(q8.Q8mvError):
         q8.Pair(256, 256, 256, mode=3)
-    with pytest.raises(q8.Q8mvError):
-        q8.Pair(256, 256, 256, prefetch=-2)
     pair = q8.Pair(256, 256, 256)
     A, Wu, Su, Wd, Sd = random_pair(256, 256, 256, seed=1)
     Ad, Wud, Sud, Wdd, Sdd = _dev(A.reshape(1, -1)), _dev(Wu), _dev(Su), _dev(Wd), _dev(Sd)
