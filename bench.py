@@ -429,6 +429,127 @@ def run_ours(args, rank, local_rank, world):
 
 EPILOGUE_ACTS = {"none": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
 
+PAIR_UP, PAIR_DOWN = "ffn_up", "ffn_down"
+
+
+def run_pair(args, rank, local_rank, world):
+    """``--pair``: one step is the 7B FFN pair through q8mv_pair_run,
+    H = silu(A . W_up + bias) then C = H . W_down + residual, in the default
+    mode (two launches chained by programmatic dependent launch) and, for
+    comparison, the one-launch pair kernel.  Bytes: both products' algorithmic
+    bytes plus the bias and the residual."""
+    import numpy as np
+    import torch
+
+    import q8_matrix_vector_gb300 as q8mv
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for the q8mv arm")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    group = init_group(world, "nccl")
+    up, down = workloads.WORKLOADS[PAIR_UP], workloads.WORKLOADS[PAIR_DOWN]
+    K, Nm, No = up.K, up.N, down.N
+    bytes_per_step = up.algorithmic_bytes() + down.algorithmic_bytes() + 4 * Nm + 4 * No
+    A, Wu, Su = workloads.make_inputs(up)
+    _, Wd, Sd = workloads.make_inputs(down)
+    rng = np.random.Generator(np.random.PCG64(2024))
+    bias = rng.standard_normal(Nm).astype(np.float32)
+    residual = (20.0 * rng.standard_normal(No)).astype(np.float32)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or 126 * 1024 * 1024
+    copies = max(2, math.ceil(2 * l2 / bytes_per_step) + 1)
+    host = [torch.from_numpy(x) for x in (A.reshape(1, K), Wu, Su, Wd, Sd, bias, residual.reshape(1, No))]
+    bufs = [[t.to(dev) for t in host] + [torch.empty((1, Nm), device=dev), torch.empty((1, No), device=dev)]
+            for _ in range(copies)]
+    stream = torch.cuda.Stream(dev)
+
+    def make(mode):
+        pair = q8mv.Pair(K, Nm, No, device=local_rank, overlap=0 if args.no_overlap else 1, mode=mode)
+        calls = []
+        for Ad, Wud, Sud, Wdd, Sdd, bd, rd, Hd, Cd in bufs:
+            eu = q8mv.Epilogue(1.0, 0.0, bd.data_ptr(), None, q8mv.ACT_SILU)
+            ed = q8mv.Epilogue(1.0, 0.0, None, rd.data_ptr(), q8mv.ACT_NONE)
+            calls.append((Ad.data_ptr(), Wud.data_ptr(), Sud.data_ptr(), Hd.data_ptr(), Wdd.data_ptr(),
+                          Sdd.data_ptr(), Cd.data_ptr(), eu, ed))
+
+        def launch(i, st):
+            pair.run_ptr(*calls[i % copies][:7], calls[i % copies][7], calls[i % copies][8], st)
+        return pair, launch
+
+    def timed(launch, steps, sample_clocks):
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                launch(i, stream.cuda_stream)
+        stream.synchronize()
+        chunk = max(copies, (min(GRAPH_CALLS, max(steps, 1)) // copies) * copies)
+        full, rest = divmod(steps, chunk)
+        graphs = []
+        for n in ([chunk] if full else []) + ([rest] if rest else []):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                cs = torch.cuda.current_stream().cuda_stream
+                for i in range(n):
+                    launch(i, cs)
+            graphs.append(g)
+        with torch.cuda.stream(stream):
+            for g in graphs:
+                g.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(group)
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(local_rank) if sample_clocks else None
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(full):
+                graphs[0].replay()
+            if rest:
+                graphs[-1].replay()
+            e1.record(stream)
+        e1.synchronize()
+        barrier(group)
+        clocks = sampler.stop() if sampler else None
+        return reduce_over_ranks(group, e0.elapsed_time(e1), "max", dev), chunk, clocks
+
+    pair, launch = make(q8mv.PAIR_AUTO)
+    ms, chunk, clocks = timed(launch, args.steps, True)
+    pair1, launch1 = make(q8mv.PAIR_ONE_LAUNCH)
+    ms1, _, _ = timed(launch1, args.steps, False)
+    for p in (pair, pair1):
+        if p.check() != 0:
+            raise RuntimeError("pair kernel recorded a device error")
+    if rank != 0:
+        return None
+    steps = max(args.steps, 1)
+    us, us1 = ms * 1e3 / steps, ms1 * 1e3 / steps
+    value = world * bytes_per_step * steps / (ms * 1e-3) / 1e9 if ms > 0 else 0.0
+    peak, peak_kind = read_hbm_peak()
+    achieved = bytes_per_step / (us * 1e-6) / 1e9
+    info1 = pair1.info
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / steps, 6),
+        "us_per_call": round(us, 3), "pct_of_peak": round(100.0 * achieved / peak, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"ffn_pair: {up.description} (SiLU + bias) then {down.description} (+ residual), "
+                               "q8mv_pair_run",
+                   "K": K, "N_mid": Nm, "N_out": No, "bytes_per_call": bytes_per_step,
+                   "l2": f"inputs larger than L2: {copies} rotating input copies "
+                         f"({copies * bytes_per_step / 1e6:.0f} MB) vs {l2 / 1e6:.0f} MB L2",
+                   "timing": f"CUDA events around graph replays of {chunk} back-to-back pair calls"
+                             + ("" if args.no_overlap else ", programmatic dependent launch"),
+                   "mode": "two launches (the default)", "parallelism": "single GPU" if world == 1 else
+                   f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} copy bandwidth",
+                     "traffic": None, "algorithmic_bytes_per_launch": bytes_per_step},
+        "one_launch": {"us_per_call": round(us1, 3), "value": round(bytes_per_step / us1 / 1e3, 2), "unit": UNIT,
+                       "plan": {k: info1[k] for k in ("threads_per_cta", "grid", "ctas_per_sm", "split_up",
+                                                      "split_down")}},
+        "cpu_baseline": None, "e2e": None, "clocks": clocks,
+        "gpu_launches": args.steps * 2,
+    }
+
 
 def epilogue_inputs(N, M):
     """Seeded bias [N] and residual [M, N] for a fused-epilogue run."""
@@ -818,6 +939,8 @@ def parse_args(argv=None):
     ap.add_argument("--stages", type=int, default=0, help="plan override: streaming kernel ring depth")
     ap.add_argument("--threads-n", type=int, default=0, help="plan override: threads along N per CTA")
     ap.add_argument("--cta-threads", type=int, default=0, help="plan override: threads per CTA (128 or 256)")
+    ap.add_argument("--pair", action="store_true",
+                    help="time the 7B FFN pair (up with SiLU + bias, down with residual) through q8mv_pair_run")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain launches instead of programmatic dependent launch (the plan's overlap option, "
                          "on by default: decode weights are constant across calls)")
@@ -842,6 +965,8 @@ def main(argv=None):
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
     if args.impl == "reference":
         line = run_reference(args, rank, world)
+    elif args.pair:
+        line = run_pair(args, rank, local_rank, world)
     else:
         line = run_ours(args, rank, local_rank, world)
     if line is not None:
