@@ -275,35 +275,6 @@ q8mv_status_t q8mv_run_fused(q8mv_plan_t plan, const float *A, const int8_t *W, 
                              float *C, const q8mv_epilogue_t *epi, cudaStream_t stream);
 
 /*
- * Regions of device memory that the NEXT call will read (its W and S, say).
- * Unused entries have bytes == 0.
- */
-#define Q8MV_MAX_PREFETCH 4
-typedef struct {
-    const void *ptr[Q8MV_MAX_PREFETCH];
-    int64_t bytes[Q8MV_MAX_PREFETCH];
-} q8mv_prefetch_t;
-
-/*
- * q8mv_run_fused (epi may be NULL) that also asks L2 to fetch the regions in
- * `next` while this call runs, so that a following call that reads them (the
- * next projection of a decode step, whose weights are known in advance)
- * finds them on chip instead of waiting for HBM after this call completes.
- * Each CTA issues bulk L2 prefetches for an equal slice of each region, right
- * after its own first weight loads; nothing waits for them and no result
- * depends on them (a hint: the regions are trimmed to their 16-byte-aligned
- * interior and may be evicted before use).  Every call still reads its own
- * weights from wherever they are; the prefetch moves the next call's HBM
- * reads earlier, it does not remove them.  Honoured by the register kernel
- * (single-row plans); other kernels ignore `next`.  The regions must stay
- * valid until this call completes and must not be written by work that
- * overlaps it.  INVALID_ARG for a negative size or a NULL pointer with a
- * positive size.  next == NULL is q8mv_run_fused.
- */
-q8mv_status_t q8mv_run_prefetch(q8mv_plan_t plan, const float *A, const int8_t *W, const float *S, float *C,
-                                const q8mv_epilogue_t *epi, const q8mv_prefetch_t *next, cudaStream_t stream);
-
-/*
  * Synchronise the plan's device and report in *device_error the error bits
  * its kernels recorded since the last check (0 = none).  Streaming kernel:
  * 1 = a ring stage's copies did not land in time, 2 = a ring stage was not

@@ -57,26 +57,6 @@ class Epilogue(ctypes.Structure):
                 ("residual", ctypes.c_void_p), ("act", ctypes.c_int32)]
 
 
-MAX_PREFETCH = 4
-
-
-class Prefetch(ctypes.Structure):
-    """q8mv_prefetch_t: up to four device regions the next call will read."""
-    _fields_ = [("ptr", ctypes.c_void_p * MAX_PREFETCH), ("bytes", ctypes.c_int64 * MAX_PREFETCH)]
-
-    @classmethod
-    def of(cls, regions) -> "Prefetch":
-        """From a list of (device pointer, bytes) pairs (at most four)."""
-        regions = list(regions)
-        if len(regions) > MAX_PREFETCH:
-            raise ValueError(f"at most {MAX_PREFETCH} prefetch regions")
-        p = cls()
-        for i, (ptr, n) in enumerate(regions):
-            p.ptr[i] = ptr
-            p.bytes[i] = int(n)
-        return p
-
-
 class PairOpts(ctypes.Structure):
     _fields_ = [("overlap", ctypes.c_int32), ("split_up", ctypes.c_int32), ("split_down", ctypes.c_int32),
                 ("cta_threads", ctypes.c_int32), ("mode", ctypes.c_int32)]
@@ -133,8 +113,6 @@ def _load() -> ctypes.CDLL:
     lib.q8mv_run.restype = ctypes.c_int
     lib.q8mv_run_fused.argtypes = [p, p, p, p, p, ctypes.POINTER(Epilogue), p]
     lib.q8mv_run_fused.restype = ctypes.c_int
-    lib.q8mv_run_prefetch.argtypes = [p, p, p, p, p, ctypes.POINTER(Epilogue), ctypes.POINTER(Prefetch), p]
-    lib.q8mv_run_prefetch.restype = ctypes.c_int
     lib.q8mv_check.argtypes = [p, ctypes.POINTER(ctypes.c_int32)]
     lib.q8mv_check.restype = ctypes.c_int
     lib.q8mv_plan_set_waits.argtypes = [p, ctypes.c_uint64, ctypes.c_uint32]
@@ -262,16 +240,6 @@ class Plan:
         st = _lib.q8mv_run_fused(self._h, A, W, S, C, ctypes.byref(epilogue), stream)
         if st != Q8MV_OK:
             raise Q8mvError(st, "q8mv_run_fused")
-
-    def run_prefetch_ptr(self, A: int, W: int, S: int, C: int, next_regions, epilogue: "Epilogue" = None,
-                         stream: int = 0) -> None:
-        """Enqueue the matvec (with an optional epilogue) and ask L2 to fetch the
-        (pointer, bytes) regions the next call will read (``q8mv_run_prefetch``)."""
-        nx = next_regions if isinstance(next_regions, Prefetch) else Prefetch.of(next_regions)
-        st = _lib.q8mv_run_prefetch(self._h, A, W, S, C, ctypes.byref(epilogue) if epilogue else None,
-                                    ctypes.byref(nx), stream)
-        if st != Q8MV_OK:
-            raise Q8mvError(st, "q8mv_run_prefetch")
 
     def __call__(self, A, W, S, out=None, stream=None, *, alpha=None, beta=None, bias=None, residual=None,
                  act=None):

@@ -1169,8 +1169,7 @@ static q8mv_status_t run_rows(q8mv_plan_t p, const float *A, const int8_t *W, co
 // The run path of q8mv_run and q8mv_run_fused.  With an epilogue the register
 // (or batched) kernel always runs, also for K == 0 (the product is then 0).
 static q8mv_status_t run_impl(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
-                              const q8epi::Epilogue &epi, cudaStream_t stream,
-                              const rk::L2Prefetch *next = nullptr) {
+                              const q8epi::Epilogue &epi, cudaStream_t stream) {
     if (p == nullptr) return Q8MV_ERR_INVALID_ARG;
     const int64_t K = p->K, N = p->N, M = p->M;
     if (N == 0) return Q8MV_OK;
@@ -1227,7 +1226,6 @@ static q8mv_status_t run_impl(q8mv_plan_t p, const float *A, const int8_t *W, co
     prm.split = c.split;
     prm.bps = c.bps;
     prm.epi = epi;
-    if (next) prm.next = *next;
     return cuda_status(launch_regs(c, svec, smem_bytes(c), prm, stream, p->overlap));
 }
 
@@ -1266,31 +1264,6 @@ q8mv_status_t q8mv_run_fused(q8mv_plan_t p, const float *A, const int8_t *W, con
     const q8mv_status_t st = make_epilogue(epi, C, p->M, p->N, &e);
     if (st != Q8MV_OK) return st;
     return run_impl(p, A, W, S, C, e, stream);
-}
-
-q8mv_status_t q8mv_run_prefetch(q8mv_plan_t p, const float *A, const int8_t *W, const float *S, float *C,
-                                const q8mv_epilogue_t *epi, const q8mv_prefetch_t *next, cudaStream_t stream) {
-    if (p == nullptr) return Q8MV_ERR_INVALID_ARG;
-    q8epi::Epilogue e;
-    if (epi) {
-        const q8mv_status_t st = make_epilogue(epi, C, p->M, p->N, &e);
-        if (st != Q8MV_OK) return st;
-    }
-    if (next == nullptr) return run_impl(p, A, W, S, C, e, stream);
-    // each region trimmed to its 16-byte-aligned interior (bulk prefetches
-    // take 16-byte units)
-    rk::L2Prefetch nx;
-    for (int r = 0; r < Q8MV_MAX_PREFETCH; ++r) {
-        if (next->bytes[r] < 0 || (next->bytes[r] > 0 && next->ptr[r] == nullptr)) return Q8MV_ERR_INVALID_ARG;
-        if (next->bytes[r] == 0) continue;
-        const uintptr_t a = reinterpret_cast<uintptr_t>(next->ptr[r]);
-        const uintptr_t lo = (a + 15) & ~static_cast<uintptr_t>(15);
-        const uintptr_t hi = (a + static_cast<uintptr_t>(next->bytes[r])) & ~static_cast<uintptr_t>(15);
-        if (hi <= lo) continue;
-        nx.ptr[r] = reinterpret_cast<const uint8_t *>(lo);
-        nx.bytes[r] = static_cast<int64_t>(hi - lo);
-    }
-    return run_impl(p, A, W, S, C, e, stream, &nx);
 }
 
 q8mv_status_t q8mv_check(q8mv_plan_t p, int32_t *device_error) {

@@ -16,16 +16,6 @@ namespace rk {
 
 constexpr int kBlk = 32;            // Q8_0 block length along K
 constexpr int kStageBlocks = 64;    // activation blocks staged in shared memory at a time
-constexpr int kMaxPrefetch = 4;     // regions a call may ask L2 to fetch for the next call
-constexpr int kPrefetchPiece = 65536;  // bytes per bulk prefetch instruction
-
-// Device memory the next call will read (its weights and scales, say), which
-// this call asks L2 to fetch while it runs: 16-byte aligned regions whose
-// sizes are multiples of 16; bytes == 0 marks an unused entry.
-struct L2Prefetch {
-    const uint8_t *ptr[kMaxPrefetch] = {};
-    int64_t bytes[kMaxPrefetch] = {};
-};
 
 // ---------------------------------------------------------------------------
 // Kernel parameters
@@ -45,7 +35,6 @@ struct Params {
     int split;            // CTAs per tile along K
     int bps;              // blocks per split
     q8epi::Epilogue epi;  // applied as C is written (off by default)
-    L2Prefetch next;      // fetched into L2 for the next call (none by default)
 };
 
 // ---------------------------------------------------------------------------
@@ -167,27 +156,6 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// This CTA's share of every region in `nx`: the grid's CTAs split each
-// region into equal 16-byte-aligned slices, and one thread asks L2 to fetch
-// its CTA's slice in bulk prefetches of at most 64 KiB.  Only a hint: nothing
-// waits for it and no result depends on it.
-__device__ __forceinline__ void prefetch_next_l2(const L2Prefetch &nx) {
-    const int64_t ctas = static_cast<int64_t>(gridDim.x) * gridDim.y;
-    const int64_t c = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
-#pragma unroll
-    for (int r = 0; r < kMaxPrefetch; ++r) {
-        const int64_t bytes = nx.bytes[r];
-        if (bytes <= 0) continue;
-        const int64_t per = ((bytes + ctas - 1) / ctas + 15) / 16 * 16;
-        const int64_t lo = c * per;
-        const int64_t hi = min(bytes, lo + per);
-        for (int64_t off = lo; off < hi; off += kPrefetchPiece) {
-            const uint32_t len = static_cast<uint32_t>(min(static_cast<int64_t>(kPrefetchPiece), hi - off));
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(nx.ptr[r] + off), "r"(len) : "memory");
-        }
-    }
-}
-
 template <int V>
 __device__ __forceinline__ void load_w_volatile(const int8_t *p, uint32_t (&w)[(V + 3) / 4]) {
     // same loads as load_w, but kept in program order so that a block's 32
@@ -241,7 +209,6 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
         load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
         prefetched = true;
     }
-    if (tid == 0) prefetch_next_l2(p.next);
     pdl_launch_dependents();
     pdl_wait();
 
