@@ -31,6 +31,7 @@ path; the process group only provides the barrier and the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -219,6 +220,10 @@ def run_ours(args, rank, local_rank, world):
     dev = torch.device("cuda", local_rank)
     group = init_group(world, "nccl")
     wl = workloads.WORKLOADS[args.workload]
+    if args.limit_k:
+        # the workload's recipe (distributions, seed, N) at a smaller K: a smaller case for profiling
+        wl = dataclasses.replace(wl, K=args.limit_k, name=f"{wl.name}_k{args.limit_k}",
+                                 description=f"{wl.description}, drawn at K={args.limit_k} instead")
     K, N, KB = wl.K, wl.N, wl.KB
     M = args.rows
     bytes_per_call = workloads.batched_bytes(K, N, M)
@@ -237,7 +242,7 @@ def run_ours(args, rank, local_rank, world):
               "tc": q8mv.KERNEL_TC}[args.kernel]
     overlap = not args.no_overlap
     plan_opts = dict(kernel=kernel, split_k=args.split, stages=args.stages, threads_n=args.threads_n,
-                     cta_threads=args.cta_threads)
+                     cta_threads=args.cta_threads, vec_bytes=args.vec_bytes)
     if args.transposed:
         plan_opts = dict(kernel=q8mv.KERNEL_ROWS_I8 if args.a_int8 else 0)
     plan = q8mv.Plan(K, N, device=local_rank, rows=M, transposed=args.transposed, overlap=int(overlap), **plan_opts)
@@ -939,6 +944,9 @@ def parse_args(argv=None):
     ap.add_argument("--stages", type=int, default=0, help="plan override: streaming kernel ring depth")
     ap.add_argument("--threads-n", type=int, default=0, help="plan override: threads along N per CTA")
     ap.add_argument("--cta-threads", type=int, default=0, help="plan override: threads per CTA (128 or 256)")
+    ap.add_argument("--vec-bytes", type=int, default=0, help="plan override: widest weight load per thread and row")
+    ap.add_argument("--limit-k", type=int, default=0,
+                    help="draw the workload at K = LIMIT_K instead (a smaller case of the same recipe, for profiling)")
     ap.add_argument("--pair", action="store_true",
                     help="time the 7B FFN pair (up with SiLU + bias, down with residual) through q8mv_pair_run")
     ap.add_argument("--no-overlap", action="store_true",
@@ -947,6 +955,8 @@ def parse_args(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.limit_k < 0:
+        ap.error("--limit-k must be positive")
     if args.steps < 1:
         ap.error("--steps must be at least 1")
     if not 1 <= args.rows <= 1 << 19:
