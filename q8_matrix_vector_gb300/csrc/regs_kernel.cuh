@@ -268,12 +268,16 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
                     fma_row<V>(a4.w, w[r + 3], part);
                 }
             } else {
-                // masked remainder: rows at or past K are never read
-                for (int r = 0; r < rows; ++r) {
-                    uint32_t wr[VW];
-                    load_w<V>(w_ptr + r * p.N, wr);
-                    fma_row<V>(a_blk[r], wr, part);
-                }
+                // masked remainder: rows at or past K are never read; the rows
+                // below K are all requested before the first is used (one round
+                // trip, not one per row), into the registers of a whole block
+#pragma unroll
+                for (int r = 0; r < kBlk; ++r)
+                    if (r < rows) load_w_volatile<V>(w_ptr + r * p.N, w[r]);
+                prefetched = false;
+#pragma unroll
+                for (int r = 0; r < kBlk; ++r)
+                    if (r < rows) fma_row<V>(a_blk[r], w[r], part);
             }
             if (!had_prefetch) load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
             fold_scale<V>(part, s, acc);
