@@ -47,31 +47,32 @@ __device__ __forceinline__ float apply(const Epilogue &e, float x, const float *
     return y;
 }
 
-// The inputs the statement reads for output (idx, n), loaded ahead of the
-// product so that their latency hides under the weight stream; apply_pre then
-// gives exactly what apply gives.
-struct Pre {
-    float c_old = 0.0f;
-    float bias = 0.0f;
-    float residual = 0.0f;
-};
-
-__device__ __forceinline__ Pre preload(const Epilogue &e, const float *c, int64_t idx, int64_t n) {
-    Pre q;
-    if (!e.on) return q;
-    if (e.beta != 0.0f) q.c_old = c[idx];
-    if (e.bias != nullptr) q.bias = __ldg(e.bias + n);
-    if (e.residual != nullptr) q.residual = __ldg(e.residual + idx);
-    return q;
+// The inputs the statement reads for output (idx, n), copied ahead of the
+// product into this thread's three shared-memory slots q[0..2] (old C, bias,
+// residual) with cp.async, so that their latency hides under the weight stream
+// and no register holds them meanwhile.  After cp.async.wait_all, apply_pre
+// gives exactly what apply gives.  All pointers 4-byte aligned.
+__device__ __forceinline__ void cp_async_f32(float *dst, const float *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
 }
 
-__device__ __forceinline__ float apply_pre(const Epilogue &e, float x, const Pre &q) {
+__device__ __forceinline__ void preload_async(const Epilogue &e, const float *c, int64_t idx, int64_t n, float *q) {
+    if (e.beta != 0.0f) cp_async_f32(q + 0, c + idx);
+    if (e.bias != nullptr) cp_async_f32(q + 1, e.bias + n);
+    if (e.residual != nullptr) cp_async_f32(q + 2, e.residual + idx);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ float apply_pre(const Epilogue &e, float x, const float *q) {
     if (!e.on) return x;
+    asm volatile("cp.async.wait_all;" ::: "memory");
     float y = e.alpha * x;
-    if (e.beta != 0.0f) y = fmaf(e.beta, q.c_old, y);
-    if (e.bias != nullptr) y += q.bias;
+    if (e.beta != 0.0f) y = fmaf(e.beta, q[0], y);
+    if (e.bias != nullptr) y += q[1];
     y = activate(y, e.act);
-    if (e.residual != nullptr) y += q.residual;
+    if (e.residual != nullptr) y += q[2];
     return y;
 }
 

@@ -283,8 +283,26 @@ int query_max_cluster() {
     return clusters >= 1 ? 8 : 1;
 }
 
+// Every register-kernel variant may use up to 64 KiB of dynamic shared memory:
+// the largest tile's column sums (32 KiB) next to up to 20 KiB of static
+// arrays (per-thread scale slots, epilogue inputs) exceed the default 48 KiB.
+cudaError_t allow_regs_smem() {
+    const int vecs[5] = {16, 8, 4, 2, 1};
+    for (int i = 0; i < 5; ++i)
+        for (int t = 0; t < 2; ++t)
+            for (int sv = 0; sv < 2; ++sv)
+                for (int cl = 0; cl < (cluster_capable(vecs[i]) ? 2 : 1); ++cl) {
+                    const cudaError_t e = cudaFuncSetAttribute(kernel_for(vecs[i], sv != 0, t == 0 ? 128 : 256, cl != 0),
+                                                               cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+                    if (e != cudaSuccess) return e;
+                }
+    return cudaSuccess;
+}
+
 // Resident CTAs per SM of every register-kernel variant on the current device.
 cudaError_t query_occupancy(Occupancy *occ) {
+    const cudaError_t ea = allow_regs_smem();
+    if (ea != cudaSuccess) return ea;
     const int vecs[5] = {16, 8, 4, 2, 1};
     for (int i = 0; i < 5; ++i) {
         for (int t = 0; t < 2; ++t) {

@@ -127,6 +127,39 @@ __device__ __forceinline__ void load_s(const float *p, float (&s)[V]) {
     }
 }
 
+// With SVEC and V >= 4, a block's V scales travel to the thread's own slot in
+// shared memory with cp.async (16-byte pieces), issued with the block's weight
+// loads and read back after the arithmetic, so that no register holds them
+// while the 32 rows are in flight.
+template <int V, bool SVEC>
+__host__ __device__ constexpr bool scales_async() {
+    return SVEC && V >= 4;
+}
+
+template <int V>
+__device__ __forceinline__ void load_s_async(const float *p, float *slot) {
+#pragma unroll
+    for (int q = 0; q < V / 4; ++q)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(
+                         slot + 4 * q))),
+                     "l"(p + 4 * q)
+                     : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int V>
+__device__ __forceinline__ void read_s_slot(const float *slot, float (&s)[V]) {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+#pragma unroll
+    for (int q = 0; q < V / 4; ++q) {
+        const float4 v = *reinterpret_cast<const float4 *>(slot + 4 * q);
+        s[4 * q + 0] = v.x;
+        s[4 * q + 1] = v.y;
+        s[4 * q + 2] = v.z;
+        s[4 * q + 3] = v.w;
+    }
+}
+
 // acc += part * s, one fused multiply-add per column ("Factoring out the scale").
 template <int V>
 __device__ __forceinline__ void fold_scale(const float (&part)[V], const float (&s)[V], float (&acc)[V]) {
@@ -178,10 +211,25 @@ constexpr int regs_min_blocks() {
     return V >= 16 ? 1 : (TPB == 256 ? 2 : 4);
 }
 
+// The output column (absolute index) whose fused-epilogue inputs this thread
+// copies ahead: its first column of the cluster slice this CTA sums, or of an
+// unsplit tile, when the slice or tile is no wider than the CTA; -1 otherwise.
+template <int TPB, bool CLUSTER>
+__device__ __forceinline__ int64_t pre_column(const Params &p, int tile_cols, int64_t col0) {
+    const int tid = static_cast<int>(threadIdx.x);
+    const int per = CLUSTER ? (tile_cols + p.split - 1) / p.split : tile_cols;
+    const int c_first = (CLUSTER ? static_cast<int>(blockIdx.y) * per : 0) + tid;
+    const int c_lim = CLUSTER ? min(tile_cols, (static_cast<int>(blockIdx.y) + 1) * per) : tile_cols;
+    if ((CLUSTER || p.split == 1) && per <= TPB && c_first < c_lim && col0 + c_first < p.N) return col0 + c_first;
+    return -1;
+}
+
 template <int V, bool SVEC, int TPB, bool CLUSTER>
 __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kernel(const Params p) {
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_is_last;
+    __shared__ float s_pre[3 * TPB];  // fused epilogue inputs of each thread's output column
+    __shared__ __align__(16) float s_scale[scales_async<V, SVEC>() ? TPB * V : 4];  // each thread's block scales
     constexpr int VW = (V + 3) / 4;
 
     const int tid = threadIdx.x;
@@ -206,7 +254,10 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
         const int8_t *w_ptr = p.W + static_cast<int64_t>(b) * kBlk * p.N + n0;
 #pragma unroll
         for (int r = 0; r < kBlk; ++r) load_w_volatile<V>(w_ptr + r * p.N, w[r]);
-        load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
+        if constexpr (scales_async<V, SVEC>())
+            load_s_async<V>(p.S + static_cast<int64_t>(b) * p.N + n0, s_scale + tid * V);
+        else
+            load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
         prefetched = true;
     }
     pdl_launch_dependents();
@@ -214,18 +265,12 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
 
     // with the fused epilogue, the inputs of the one output column this thread
     // writes at the end (cluster splits whose slice fits the CTA, and unsplit
-    // tiles no wider than the CTA) are loaded now, so that their latency hides
-    // under the weight stream instead of sitting on the final write
-    q8epi::Pre pre;
-    int64_t pre_n = -1;
+    // tiles no wider than the CTA) are copied into shared memory now, so that
+    // their latency hides under the weight stream instead of sitting on the
+    // final write
     if (p.epi.on) {
-        const int per = CLUSTER ? (tile_cols + p.split - 1) / p.split : tile_cols;
-        const int c_first = (CLUSTER ? static_cast<int>(blockIdx.y) * per : 0) + tid;
-        const int c_lim = CLUSTER ? min(tile_cols, (static_cast<int>(blockIdx.y) + 1) * per) : tile_cols;
-        if ((CLUSTER || p.split == 1) && per <= TPB && c_first < c_lim && col0 + c_first < p.N) {
-            pre_n = col0 + c_first;
-            pre = q8epi::preload(p.epi, p.C, pre_n, pre_n);
-        }
+        const int64_t pn = pre_column<TPB, CLUSTER>(p, tile_cols, col0);
+        if (pn >= 0) q8epi::preload_async(p.epi, p.C, pn, pn, s_pre + 3 * tid);
     }
 
     float acc[V];
@@ -251,12 +296,16 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
 #pragma unroll
             for (int j = 0; j < V; ++j) part[j] = 0.0f;
 
-            const bool had_prefetch = prefetched;
             if (rows == kBlk) {
-                // whole block: all 32 row loads are issued before the arithmetic
+                // whole block: all 32 row loads and the scales are issued
+                // before the arithmetic
                 if (!prefetched) {
 #pragma unroll
                     for (int r = 0; r < kBlk; ++r) load_w_volatile<V>(w_ptr + r * p.N, w[r]);
+                    if constexpr (scales_async<V, SVEC>())
+                        load_s_async<V>(p.S + static_cast<int64_t>(b) * p.N + n0, s_scale + tid * V);
+                    else
+                        load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
                 }
                 prefetched = false;
 #pragma unroll
@@ -274,12 +323,16 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
 #pragma unroll
                 for (int r = 0; r < kBlk; ++r)
                     if (r < rows) load_w_volatile<V>(w_ptr + r * p.N, w[r]);
+                if constexpr (scales_async<V, SVEC>())
+                    load_s_async<V>(p.S + static_cast<int64_t>(b) * p.N + n0, s_scale + tid * V);
+                else
+                    load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
                 prefetched = false;
 #pragma unroll
                 for (int r = 0; r < kBlk; ++r)
                     if (r < rows) fma_row<V>(a_blk[r], w[r], part);
             }
-            if (!had_prefetch) load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
+            if constexpr (scales_async<V, SVEC>()) read_s_slot<V>(s_scale + tid * V, s);
             fold_scale<V>(part, s, acc);
         }
     }
@@ -328,7 +381,10 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
             const int64_t n = col0 + c;
             float v = *cluster.map_shared_rank(mine + c, 0);
             for (int q = 1; q < p.split; ++q) v += *cluster.map_shared_rank(mine + c, q);
-            if (n < p.N) p.C[n] = n == pre_n ? q8epi::apply_pre(p.epi, v, pre) : q8epi::apply(p.epi, v, p.C, n, n);
+            if (n < p.N)
+                p.C[n] = p.epi.on && n == pre_column<TPB, CLUSTER>(p, tile_cols, col0)
+                             ? q8epi::apply_pre(p.epi, v, s_pre + 3 * tid)
+                             : q8epi::apply(p.epi, v, p.C, n, n);
         }
         cluster.sync();  // keep this CTA's sums alive until every CTA has read them
         return;
@@ -343,7 +399,9 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
         if (split)
             p.ws[static_cast<int64_t>(blockIdx.y) * p.N + n] = v;
         else
-            p.C[n] = n == pre_n ? q8epi::apply_pre(p.epi, v, pre) : q8epi::apply(p.epi, v, p.C, n, n);
+            p.C[n] = p.epi.on && n == pre_column<TPB, CLUSTER>(p, tile_cols, col0)
+                         ? q8epi::apply_pre(p.epi, v, s_pre + 3 * tid)
+                         : q8epi::apply(p.epi, v, p.C, n, n);
     }
     if (!split) return;
 
