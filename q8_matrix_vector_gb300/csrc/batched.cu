@@ -34,6 +34,12 @@ int log2_pow2(int x) {
 
 int vec_slot(int v) { return v == 8 ? 0 : v == 4 ? 1 : v == 1 ? 2 : -1; }
 
+// Static shared memory of the batched register kernel: each thread's scale
+// slot (kThreads x vec floats, below 4 rows per pass) and the last-ticket flag.
+size_t static_smem(int mb, int vec) {
+    return (mb < 4 ? static_cast<size_t>(kThreads) * vec * sizeof(float) : 4) + 16;
+}
+
 // Cost model (microseconds) of one call, checked against GB300 sweeps of the
 // decode shapes at 2 to 16 rows.
 //   Streaming: the bytes in flight per resident thread (32 rows of a block)
@@ -222,7 +228,8 @@ q8mv_status_t choose(int64_t M, int64_t K, int64_t N, const Device &dev, int vec
                 const size_t red = static_cast<size_t>(red_rows + (c.cluster ? 1 : 0)) * mb * tile_n * sizeof(float);
                 c.smem = std::max(a_bytes, red);
                 if (c.smem > static_cast<size_t>(dev.smem_per_cta)) continue;
-                c.cps = std::min<int>(cps_regs, static_cast<int>(dev.smem_per_sm / (c.smem + 1024)));
+                c.cps = std::min<int>(cps_regs,
+                                      static_cast<int>(dev.smem_per_sm / (c.smem + static_smem(mb, vec) + 1024)));
                 if (c.cps < 1) continue;
                 if (c.cluster && tiles * groups > resident_clusters(dev, vec_slot(vec), static_cast<int>(split_eff), c.cps))
                     continue;
@@ -288,8 +295,8 @@ cudaError_t query_device(int mb, Device *dev) {
 }
 
 cudaError_t prepare(const Config &c) {
-    if (c.smem <= 48 * 1024) return cudaSuccess;
-    // only ever raise the kernel's limit: plans made earlier may need more
+    // only ever raise the kernel's limit: plans made earlier may need more (the
+    // default limit already leaves room for the kernel's static arrays)
     const KernelFn fn = kernel_for(c.mb, c.vec, c.cluster);
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, fn);

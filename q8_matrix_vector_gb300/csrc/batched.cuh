@@ -196,6 +196,7 @@ template <int MB, int V, int TPB, bool CLUSTER>
 __global__ void __launch_bounds__(TPB, min_blocks<MB, V>()) q8mv_batched_kernel(const Params p) {
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_is_last;
+    __shared__ float s_scale[MB < 4 ? TPB * V : 1];  // each thread's scales of its current block (below 4 rows)
     constexpr int VW = (V + 3) / 4;
 
     const int tid = threadIdx.x;
@@ -256,6 +257,21 @@ __global__ void __launch_bounds__(TPB, min_blocks<MB, V>()) q8mv_batched_kernel(
             for (int m = 0; m < MB; ++m)
 #pragma unroll
                 for (int j = 0; j < V; ++j) part[m][j] = 0.0f;
+            // below 4 rows the block's scales are requested before its
+            // arithmetic, so that they arrive while it runs: copied into this
+            // thread's shared-memory slot, so that no register holds them
+            // meanwhile (from 4 rows on the arithmetic is long enough to
+            // leave them after it)
+            if constexpr (MB < 4) {
+                const float *sp = p.S + static_cast<int64_t>(b) * p.N + n0;
+#pragma unroll
+                for (int j = 0; j < V; ++j)
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(
+                                     __cvta_generic_to_shared(s_scale + tid * V + j))),
+                                 "l"(sp + j)
+                                 : "memory");
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            }
 
             if (rows == kBlk) {
                 if (!prefetched) {
@@ -298,7 +314,13 @@ __global__ void __launch_bounds__(TPB, min_blocks<MB, V>()) q8mv_batched_kernel(
             }
             // the block's scale, once per block, column and activation row
             float s[V];
-            load_s<V, false>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
+            if constexpr (MB < 4) {
+                asm volatile("cp.async.wait_all;" ::: "memory");
+#pragma unroll
+                for (int j = 0; j < V; ++j) s[j] = s_scale[tid * V + j];
+            } else {
+                load_s<V, false>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
+            }
 #pragma unroll
             for (int m = 0; m < MB; ++m)
 #pragma unroll
