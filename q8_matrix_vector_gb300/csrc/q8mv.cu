@@ -324,7 +324,7 @@ cudaError_t launch_regs(const Config &c, bool svec, size_t smem, const Params &p
                         bool overlap);
 
 size_t smem_bytes(const Config &c) {
-    const size_t stage = static_cast<size_t>(kStageBlocks) * kBlk * sizeof(float);
+    const size_t stage = static_cast<size_t>(std::min(c.bps, kStageBlocks)) * kBlk * sizeof(float);
     const size_t red = static_cast<size_t>(c.gk + (c.cluster ? 1 : 0)) * c.tile_n * sizeof(float);
     return std::max(stage, red);
 }

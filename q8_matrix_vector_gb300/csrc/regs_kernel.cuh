@@ -15,7 +15,8 @@
 namespace rk {
 
 constexpr int kBlk = 32;            // Q8_0 block length along K
-constexpr int kStageBlocks = 64;    // activation blocks staged in shared memory at a time
+constexpr int kStageBlocks = 160;   // activation blocks staged in shared memory at a time (20 KiB: a
+                                    // CTA's whole K range on every decode shape, fetched once)
 
 // ---------------------------------------------------------------------------
 // Kernel parameters
