@@ -73,7 +73,8 @@ __device__ __forceinline__ uint64_t globaltimer() {
 // phase p, if the block is whole (the same rule as the register kernel).
 template <bool SVEC>
 __device__ __forceinline__ bool prefetch_block(const Phase &p, int tile, int range,
-                                               uint32_t (&w)[rk::kBlk][(kVec + 3) / 4], float (&s)[kVec]) {
+                                               uint32_t (&w)[rk::kBlk][(kVec + 3) / 4], float (&s)[kVec],
+                                               float *s_slot) {
     const int tid = threadIdx.x;
     const int64_t n0 = static_cast<int64_t>(tile) * (kTn * kVec) + static_cast<int64_t>(tid & (kTn - 1)) * kVec;
     const int b = range * p.bps + (tid / kTn);
@@ -82,7 +83,10 @@ __device__ __forceinline__ bool prefetch_block(const Phase &p, int tile, int ran
     const int8_t *w_ptr = p.W + static_cast<int64_t>(b) * rk::kBlk * p.N + n0;
 #pragma unroll
     for (int r = 0; r < rk::kBlk; ++r) rk::load_w_volatile<kVec>(w_ptr + r * p.N, w[r]);
-    rk::load_s<kVec, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
+    if constexpr (SVEC)
+        rk::load_s_async<kVec>(p.S + static_cast<int64_t>(b) * p.N + n0, s_slot);
+    else
+        rk::load_s<kVec, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
     return true;
 }
 
@@ -91,7 +95,7 @@ __device__ __forceinline__ bool prefetch_block(const Phase &p, int tile, int ran
 template <bool SVEC, int TPB, bool COHERENT>
 __device__ __forceinline__ void run_item(const Phase &p, int tile, int range, float *smem, unsigned &s_is_last,
                                          uint32_t (&w)[rk::kBlk][(kVec + 3) / 4], float (&s)[kVec],
-                                         bool prefetched) {
+                                         bool prefetched, float *s_slot) {
     constexpr int V = kVec;
     const int tid = threadIdx.x;
     const int tn_i = tid & (kTn - 1);
@@ -127,9 +131,13 @@ __device__ __forceinline__ void run_item(const Phase &p, int tile, int range, fl
             for (int j = 0; j < V; ++j) part[j] = 0.0f;
             const bool had_prefetch = prefetched;
             if (rows == rk::kBlk) {
+                // with 16-byte-aligned scales the block's rows and scales are
+                // all requested before its arithmetic (the scales through the
+                // thread's shared-memory slot)
                 if (!prefetched) {
 #pragma unroll
                     for (int r = 0; r < rk::kBlk; ++r) rk::load_w_volatile<V>(w_ptr + r * p.N, w[r]);
+                    if constexpr (SVEC) rk::load_s_async<V>(p.S + static_cast<int64_t>(b) * p.N + n0, s_slot);
                 }
                 prefetched = false;
 #pragma unroll
@@ -141,14 +149,21 @@ __device__ __forceinline__ void run_item(const Phase &p, int tile, int range, fl
                     rk::fma_row<V>(a4.w, w[r + 3], part);
                 }
             } else {
-                // masked remainder: rows at or past K are never read
-                for (int r = 0; r < rows; ++r) {
-                    uint32_t wr[(V + 3) / 4];
-                    rk::load_w<V>(w_ptr + r * p.N, wr);
-                    rk::fma_row<V>(a_blk[r], wr, part);
-                }
+                // masked remainder: rows at or past K are never read; the rows
+                // below K are requested together
+#pragma unroll
+                for (int r = 0; r < rk::kBlk; ++r)
+                    if (r < rows) rk::load_w_volatile<V>(w_ptr + r * p.N, w[r]);
+                if constexpr (SVEC) rk::load_s_async<V>(p.S + static_cast<int64_t>(b) * p.N + n0, s_slot);
+                prefetched = false;
+#pragma unroll
+                for (int r = 0; r < rk::kBlk; ++r)
+                    if (r < rows) rk::fma_row<V>(a_blk[r], w[r], part);
             }
-            if (!had_prefetch) rk::load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
+            if constexpr (SVEC)
+                rk::read_s_slot<V>(s_slot, s);
+            else if (!had_prefetch)
+                rk::load_s<V, SVEC>(p.S + static_cast<int64_t>(b) * p.N + n0, s);
             rk::fold_scale<V>(part, s, acc);
         }
     }
@@ -226,6 +241,8 @@ template <bool SVEC, int TPB>
 __global__ void __launch_bounds__(TPB, rk::regs_min_blocks<kVec, TPB>()) q8mv_pair_kernel(const Params pp) {
     extern __shared__ __align__(16) float smem[];
     __shared__ unsigned s_is_last;
+    __shared__ __align__(16) float s_scale[SVEC ? TPB * kVec : 4];  // each thread's block scales
+    float *s_slot = s_scale + (SVEC ? threadIdx.x * kVec : 0);
     uint32_t w[rk::kBlk][(kVec + 3) / 4];
     float s[kVec];
     const int item = static_cast<int>(blockIdx.x);
@@ -234,17 +251,17 @@ __global__ void __launch_bounds__(TPB, rk::regs_min_blocks<kVec, TPB>()) q8mv_pa
     // kernel in the stream (programmatic dependent launch), A after it
     const bool up = item < pp.up.tiles * pp.up.split;
     const int up_tile = up ? item / pp.up.split : 0, up_range = up ? item % pp.up.split : 0;
-    bool pf = up && prefetch_block<SVEC>(pp.up, up_tile, up_range, w, s);
+    bool pf = up && prefetch_block<SVEC>(pp.up, up_tile, up_range, w, s, s_slot);
     rk::pdl_launch_dependents();
     rk::pdl_wait();
-    if (up) run_item<SVEC, TPB, false>(pp.up, up_tile, up_range, smem, s_is_last, w, s, pf);
+    if (up) run_item<SVEC, TPB, false>(pp.up, up_tile, up_range, smem, s_is_last, w, s, pf, s_slot);
 
     // down product: its first weight block before the grid barrier, H after it
     const bool down = item < pp.down.tiles * pp.down.split;
     const int dn_tile = down ? item / pp.down.split : 0, dn_range = down ? item % pp.down.split : 0;
-    pf = down && prefetch_block<SVEC>(pp.down, dn_tile, dn_range, w, s);
+    pf = down && prefetch_block<SVEC>(pp.down, dn_tile, dn_range, w, s, s_slot);
     grid_barrier(pp.bar, pp);
-    if (down) run_item<SVEC, TPB, true>(pp.down, dn_tile, dn_range, smem, s_is_last, w, s, pf);
+    if (down) run_item<SVEC, TPB, true>(pp.down, dn_tile, dn_range, smem, s_is_last, w, s, pf, s_slot);
 }
 
 }  // namespace pk
