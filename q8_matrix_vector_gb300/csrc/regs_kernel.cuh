@@ -378,6 +378,26 @@ __global__ void __launch_bounds__(TPB, regs_min_blocks<V, TPB>()) q8mv_regs_kern
         const int rank = static_cast<int>(blockIdx.y);
         const int per = (tile_cols + p.split - 1) / p.split;
         const int c_end = min(tile_cols, (rank + 1) * per);
+        if (per <= TPB) {
+            // one column per thread: read the ranks' sums, tell the cluster
+            // that this CTA is done reading (the arrive takes the finished sum
+            // as an operand, so every read has completed), then write, and
+            // only then wait for the others before the shared memory goes
+            const int c = rank * per + tid;
+            const int64_t n = col0 + c;
+            float v = 0.0f;
+            if (c < c_end) {
+                v = *cluster.map_shared_rank(mine + c, 0);
+                for (int q = 1; q < p.split; ++q) v += *cluster.map_shared_rank(mine + c, q);
+            }
+            asm volatile("barrier.cluster.arrive.relaxed.aligned; // %0" ::"f"(v) : "memory");
+            if (c < c_end && n < p.N)
+                p.C[n] = p.epi.on && n == pre_column<TPB, CLUSTER>(p, tile_cols, col0)
+                             ? q8epi::apply_pre(p.epi, v, s_pre + 3 * tid)
+                             : q8epi::apply(p.epi, v, p.C, n, n);
+            asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+            return;
+        }
         for (int c = rank * per + tid; c < c_end; c += TPB) {
             const int64_t n = col0 + c;
             float v = *cluster.map_shared_rank(mine + c, 0);
