@@ -386,6 +386,28 @@ __global__ void __launch_bounds__(TPB, min_blocks<MB, V>()) q8mv_batched_kernel(
         const int rank = static_cast<int>(blockIdx.y);
         const int per = (outs + p.split - 1) / p.split;
         const int i_end = min(outs, (rank + 1) * per);
+        if (per <= TPB) {
+            // one output per thread: read the ranks' sums, tell the cluster
+            // that this CTA is done reading (the arrive takes the finished sum
+            // as an operand, so every read has completed), write, and only
+            // then wait for the others before the shared memory goes
+            const int i = rank * per + tid;
+            const int m = i / tile_cols;
+            const int64_t n = col0 + (i - m * tile_cols);
+            const bool mine_out = i < i_end && m < mrows && n < p.N;
+            float v = 0.0f;
+            if (mine_out) {
+                v = *cluster.map_shared_rank(mine + i, 0);
+                for (int q = 1; q < p.split; ++q) v += *cluster.map_shared_rank(mine + i, q);
+            }
+            asm volatile("barrier.cluster.arrive.relaxed.aligned; // %0" ::"f"(v) : "memory");
+            if (mine_out) {
+                const int64_t idx = static_cast<int64_t>(m0 + m) * p.N + n;
+                p.C[idx] = q8epi::apply(p.epi, v, p.C, idx, n);
+            }
+            asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+            return;
+        }
         for (int i = rank * per + tid; i < i_end; i += TPB) {
             const int m = i / tile_cols;
             const int64_t n = col0 + (i - m * tile_cols);

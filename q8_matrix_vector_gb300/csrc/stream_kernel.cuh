@@ -427,13 +427,21 @@ __global__ void __launch_bounds__(kThreads, 2)
         cluster.sync();
         const int per = (kTileN + p.split - 1) / p.split;
         const int c = q * per + ct;
-        if (ct < per && c < kTileN && col0 + c < p.N) {
-            float sum = *cluster.map_shared_rank(tile_sum + c, 0);
+        const bool mine = ct < per && c < kTileN && col0 + c < p.N;
+        float sum = 0.0f;
+        if (mine) {
+            sum = *cluster.map_shared_rank(tile_sum + c, 0);
             for (int r = 1; r < p.split; ++r) sum += *cluster.map_shared_rank(tile_sum + c, r);
+        }
+        // done reading the other CTAs' sums (the arrive takes the finished sum
+        // as an operand, so every read has completed); write, then wait for
+        // the others before this CTA's shared memory goes
+        asm volatile("barrier.cluster.arrive.relaxed.aligned; // %0" ::"f"(sum) : "memory");
+        if (mine) {
             const int64_t n = col0 + c;
             p.C[n] = q8epi::apply(p.epi, sum, p.C, n, n);
         }
-        cluster.sync();  // keep this CTA's sums alive until every CTA has read them
+        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     } else {
         const int64_t n = col0 + ct;
         if (ct < kTileN && n < p.N) p.C[n] = q8epi::apply(p.epi, v, p.C, n, n);
