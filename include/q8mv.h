@@ -426,6 +426,17 @@ q8mv_status_t q8mv_pair_set_wait(q8mv_pair_t pair, uint64_t wait_ns);
 /* Release the pair (synchronises its device first).  NULL is accepted. */
 q8mv_status_t q8mv_pair_destroy(q8mv_pair_t pair);
 
+/*
+ * Host-only planning, no GPU needed: the one-launch configuration that
+ * q8mv_pair_plan would pick (mode Q8MV_PAIR_ONE_LAUNCH) on a GPU with
+ * `sm_count` SMs holding `ctas_per_sm` pair-kernel CTAs each.  Fills *info
+ * (workspace_bytes: the split sums' partial rows and counters, without the
+ * barrier words); INVALID_ARG if the shapes cannot use the pair kernel.
+ */
+q8mv_status_t q8mv_pair_choose_config(int64_t K, int64_t N_mid, int64_t N_out, int32_t sm_count,
+                                      int32_t ctas_per_sm, const q8mv_pair_opts_t *opts,
+                                      q8mv_pair_info_t *info);
+
 /* The last CUDA runtime error code this library saw on the calling thread
  * (0 if none), for diagnosing Q8MV_ERR_CUDA. */
 int q8mv_last_cuda_error(void);

@@ -147,6 +147,9 @@ def _load() -> ctypes.CDLL:
     lib.q8mv_pair_set_wait.restype = ctypes.c_int
     lib.q8mv_pair_destroy.argtypes = [p]
     lib.q8mv_pair_destroy.restype = ctypes.c_int
+    lib.q8mv_pair_choose_config.argtypes = [i64, i64, i64, i32, i32, ctypes.POINTER(PairOpts),
+                                            ctypes.POINTER(PairInfo)]
+    lib.q8mv_pair_choose_config.restype = ctypes.c_int
     return lib
 
 
@@ -184,6 +187,16 @@ def choose_config_batched(M: int, K: int, N: int, sm_count: int, ctas_per_sm: in
                                          ctypes.byref(o) if o else None, ctypes.byref(info))
     if st != Q8MV_OK:
         raise Q8mvError(st, "q8mv_choose_config_batched")
+    return info.as_dict()
+
+
+def choose_pair_config(K: int, N_mid: int, N_out: int, sm_count: int, ctas_per_sm: int, **opts) -> dict:
+    """Host-only planner of the one-launch FFN pair kernel (``q8mv_pair_choose_config``)."""
+    info = PairInfo()
+    o = PairOpts(0, opts.get("split_up", 0), opts.get("split_down", 0), opts.get("cta_threads", 0), PAIR_ONE_LAUNCH)
+    st = _lib.q8mv_pair_choose_config(K, N_mid, N_out, sm_count, ctas_per_sm, ctypes.byref(o), ctypes.byref(info))
+    if st != Q8MV_OK:
+        raise Q8mvError(st, "q8mv_pair_choose_config")
     return info.as_dict()
 
 

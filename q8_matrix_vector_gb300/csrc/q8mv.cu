@@ -1875,6 +1875,39 @@ q8mv_status_t q8mv_pair_plan(q8mv_pair_t *out, int64_t K, int64_t n_mid, int64_t
     return Q8MV_OK;
 }
 
+static void fill_pair_info(const pk::Config &c, int64_t mem_bytes, q8mv_pair_info_t *info) {
+    info->one_launch = 1;
+    info->threads_per_cta = c.tpb;
+    info->grid = c.grid;
+    info->ctas_per_sm = c.cps;
+    info->split_up = c.up.split;
+    info->split_down = c.down.split;
+    info->tiles_up = c.up.tiles;
+    info->tiles_down = c.down.tiles;
+    info->workspace_bytes = mem_bytes;
+}
+
+q8mv_status_t q8mv_pair_choose_config(int64_t K, int64_t n_mid, int64_t n_out, int32_t sm_count,
+                                      int32_t ctas_per_sm, const q8mv_pair_opts_t *opts,
+                                      q8mv_pair_info_t *info) {
+    if (info == nullptr || sm_count <= 0 || ctas_per_sm <= 0 || K < 0 || n_mid < 0 || n_out < 0)
+        return Q8MV_ERR_INVALID_ARG;
+    q8mv_pair_opts_t o = {};
+    if (opts) o = *opts;
+    if (o.cta_threads != 0 && o.cta_threads != 128 && o.cta_threads != 256) return Q8MV_ERR_INVALID_ARG;
+    if (o.split_up < 0 || o.split_up > pk::kMaxSplitPair || o.split_down < 0 || o.split_down > pk::kMaxSplitPair)
+        return Q8MV_ERR_INVALID_ARG;
+    std::memset(info, 0, sizeof(*info));
+    pk::Config c;
+    if (!pk::plan(K, n_mid, n_out, sm_count, ctas_per_sm, o.cta_threads ? o.cta_threads : 256, o.split_up,
+                  o.split_down, &c))
+        return Q8MV_ERR_INVALID_ARG;
+    const int64_t ws = (c.up.ws_floats + c.down.ws_floats) * static_cast<int64_t>(sizeof(float)) +
+                       static_cast<int64_t>(c.up.tiles + c.down.tiles) * static_cast<int64_t>(sizeof(unsigned));
+    fill_pair_info(c, ws, info);
+    return Q8MV_OK;
+}
+
 q8mv_status_t q8mv_pair_info(q8mv_pair_t p, q8mv_pair_info_t *info) {
     if (p == nullptr || info == nullptr) return Q8MV_ERR_INVALID_ARG;
     std::memset(info, 0, sizeof(*info));
