@@ -81,8 +81,7 @@ __device__ __forceinline__ uint32_t load_byte(const int8_t *p) {
     return v & 0xFFu;
 }
 
-// The 16 bytes of `row` from byte k (k < K) into w, little-endian words;
-// bytes at or past K are 0 (they convert to 0) and are not read.
+// The 16 bytes at p (all below K) into w, little-endian words:
 //   LV = 16: one 16-byte load (rows 16-byte aligned), streamed past L1.
 //   LV = 4:  rows 4-byte aligned: per row, by its own alignment, one 16-byte
 //            load, two 8-byte loads or four 4-byte loads, the narrow ones
@@ -90,38 +89,45 @@ __device__ __forceinline__ uint32_t load_byte(const int8_t *p) {
 //            once.
 //   LV = 1:  sixteen byte loads (any alignment), through L1 likewise.
 template <int LV>
-__device__ __forceinline__ void load_chunk(const int8_t *row, int64_t k, int64_t K, uint32_t (&w)[4]) {
-    const int8_t *p = row + k;
-    if (k + kLaneK <= K) {
-        if constexpr (LV == 16) {
+__device__ __forceinline__ void load_chunk_whole(const int8_t *p, uint32_t (&w)[4]) {
+    if constexpr (LV == 16) {
+        asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "l"(p)
+                     : "memory");
+    } else if constexpr (LV == 4) {
+        // the row's own alignment (the same for every lane of the warp, so
+        // the branch is uniform): rows of a 4-byte multiple K start 0, 4, 8
+        // or 12 bytes past a 16-byte boundary
+        const uintptr_t al = reinterpret_cast<uintptr_t>(p) & 15u;
+        if (al == 0) {
             asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
                          : "l"(p)
                          : "memory");
-        } else if constexpr (LV == 4) {
-            // the row's own alignment (the same for every lane of the warp, so
-            // the branch is uniform): rows of a 4-byte multiple K start 0, 4, 8
-            // or 12 bytes past a 16-byte boundary
-            const uintptr_t al = reinterpret_cast<uintptr_t>(p) & 15u;
-            if (al == 0) {
-                asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                             : "l"(p)
-                             : "memory");
-            } else if (al == 8) {
-                asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p) : "memory");
-                asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w[2]), "=r"(w[3]) : "l"(p + 8) : "memory");
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(w[q]) : "l"(p + 4 * q) : "memory");
-            }
+        } else if (al == 8) {
+            asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p) : "memory");
+            asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(w[2]), "=r"(w[3]) : "l"(p + 8) : "memory");
         } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                w[q] = load_byte(p + 4 * q) | (load_byte(p + 4 * q + 1) << 8) | (load_byte(p + 4 * q + 2) << 16) |
-                       (load_byte(p + 4 * q + 3) << 24);
+                asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(w[q]) : "l"(p + 4 * q) : "memory");
         }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            w[q] = load_byte(p + 4 * q) | (load_byte(p + 4 * q + 1) << 8) | (load_byte(p + 4 * q + 2) << 16) |
+                   (load_byte(p + 4 * q + 3) << 24);
+    }
+}
+
+// The 16 bytes of `row` from byte k (k < K) into w; bytes at or past K are 0
+// (they convert to 0) and are not read.
+template <int LV>
+__device__ __forceinline__ void load_chunk(const int8_t *row, int64_t k, int64_t K, uint32_t (&w)[4]) {
+    const int8_t *p = row + k;
+    if (k + kLaneK <= K) {
+        load_chunk_whole<LV>(p, w);
     } else {
         // the row's ragged end: only bytes below K (unrolled, so that w stays in registers)
 #pragma unroll
@@ -147,6 +153,30 @@ __device__ __forceinline__ void load_step(const Params &p, const int8_t *w_base,
             w[r][0] = w[r][1] = w[r][2] = w[r][3] = 0u;
             s[r] = 0.0f;
         }
+    }
+}
+
+// A step's loads when the CTA has all R rows and the warp's 512-wide step lies
+// below K: the same loads as load_step without its bounds checks, so that the
+// steady state of the step loop issues no code for ragged edges.
+template <int LV, int R>
+__device__ __forceinline__ void load_step_whole(const Params &p, const int8_t *w_base, const float *s_base, int64_t k,
+                                                bool even, uint32_t (&w)[R][4], float (&s)[R]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        load_chunk_whole<LV>(w_base + r * p.K + k, w[r]);
+        s[r] = even ? __ldg(s_base + r * p.KB + k / kBlk) : 0.0f;
+    }
+}
+
+// The lane's 16 activations from k when they lie below K and A + k is 16-byte
+// aligned: four vector loads.
+__device__ __forceinline__ void load_a_whole(const Params &p, int64_t k, float2 (&a2)[8]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 t = __ldg(reinterpret_cast<const float4 *>(p.A + k) + q);
+        a2[2 * q] = make_float2(t.x, t.y);
+        a2[2 * q + 1] = make_float2(t.z, t.w);
     }
 }
 
@@ -253,8 +283,25 @@ __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_row
     // step before it (three CTAs per SM keep other warps' loads in flight)
     uint32_t w[R][4];
     float s[R];
+    float2 a2[8];
+    // a step whose 512 k lie below K, in a CTA with all R rows, loads without
+    // bounds checks (the branch is uniform over the warp)
+    const bool whole_rows = nrows == R;
+    const bool a_vec = (reinterpret_cast<uintptr_t>(p.A) & 15u) == 0;
+    auto step_loads = [&](int64_t kb) {
+        if (whole_rows && kb + kStepK <= p.K)
+            load_step_whole<LV, R>(p, w_base, s_base, kb + lane * kLaneK, even, w, s);
+        else
+            load_step<LV, R>(p, w_base, s_base, nrows, kb + lane * kLaneK, even, w, s);
+    };
+    auto step_acts = [&](int64_t kb) {
+        if (a_vec && kb + kStepK <= p.K)
+            load_a_whole(p, kb + lane * kLaneK, a2);
+        else
+            load_a(p, kb + lane * kLaneK, a2);
+    };
     int64_t k0 = static_cast<int64_t>(warp) * kStepK;
-    load_step<LV, R>(p, w_base, s_base, nrows, k0 + lane * kLaneK, even, w, s);
+    step_loads(k0);
     if (p.tail > 0) {
         // rows are 4-byte aligned here (K % 4 == 0); words past the tail are never read
         const int t = threadIdx.x;
@@ -267,8 +314,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_row
     }
     pdl_launch_dependents();
     pdl_wait();
-    float2 a2[8];
-    load_a(p, k0 + lane * kLaneK, a2);
+    step_acts(k0);
     if (p.tail > 0 && static_cast<int>(threadIdx.x) < p.tail) tail_a[threadIdx.x] = __ldg(p.A + p.k_main + threadIdx.x);
 
     float acc[R];
@@ -310,10 +356,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_row
             }
         }
         // the next step's loads, once this step's registers are free
-        const int64_t kn = k0 + step + lane * kLaneK;
         if (k0 + step < p.k_main) {
-            load_step<LV, R>(p, w_base, s_base, nrows, kn, even, w, s);
-            load_a(p, kn, a2);
+            step_loads(k0 + step);
+            step_acts(k0 + step);
         }
     }
 
