@@ -104,7 +104,8 @@ typedef struct {
                           previous kernel in its stream finishes and reads W and S before that kernel
                           has completed (A is read and C written only after it).  Only for weights
                           that the preceding work in the stream does not write. */
-    int32_t cta_threads; /* register kernel: 128 or 256 threads per CTA */
+    int32_t cta_threads; /* register kernel: 128 or 256 threads per CTA; transposed plans: 32, 64,
+                            128 or 256 (the warps splitting K, at most one per 512-wide step) */
     int32_t rows_per_cta; /* transposed plans: output rows per CTA, 8 or 16 */
 } q8mv_opts_t;
 
@@ -159,7 +160,10 @@ q8mv_status_t q8mv_plan(q8mv_plan_t *out, int64_t K, int64_t N, int device,
  * linear layer stores its weights).  q8mv_run and q8mv_run_fused then take Wt
  * and St in place of W and S.  Limits as for q8mv_plan.  Accepted overrides:
  * vec_bytes (16, 4 or 1: load per lane and step, used when K and Wt's address
- * allow it, narrower loads as the fallback), rows_per_cta (8 or 16), overlap,
+ * allow it, narrower loads as the fallback), rows_per_cta (8 or 16), cta_threads
+ * (32, 64, 128 or 256: warps along K; by default the fewest, at least 2 with
+ * int8 activations, that still give every SM 32 warps, 12 with int8
+ * activations), overlap,
  * and kernel = Q8MV_KERNEL_ROWS_I8 for int8 activations (below); any other
  * non-zero field gives INVALID_ARG.  Each output's blocks are summed in order
  * within a fixed interleave, so a plan is bitwise repeatable.

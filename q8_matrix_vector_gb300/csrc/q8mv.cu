@@ -586,17 +586,36 @@ struct RowsConfig {
     int64_t ctas = 0;  // grid
 };
 
-// One warp per 512-wide step of K, at most 8 (warps then take every 8th step).
+// Warps along K per 8-row CTA: the fewest (1, 2, 4 or 8; int8 activations at
+// least 2) whose grid still gives every SM kRowsWarpsPerSm warps (int8:
+// kRowsWarpsPerSmI8), at most one per 512-wide step.  Fewer warps give each
+// more steps, so a CTA's fixed work (its row sums, the reduction over warps,
+// the prologue) is spread over more bytes; measured on the decode shapes
+// (warps 1 / 2 / 4 / 8, us): LM head 107.6 / 109.6 / 113.2 / 124.8, 70B FFN
+// up 41.8 / 40.2 / 40.1 / 44.0, FFN up 18.4 / 10.6 / 10.3 / 10.8, attention
+// 17.8 / 9.8 / 5.6 / 5.3; int8: LM head 104.9 / 102.3 / 108.3 / 125.3, FFN
+// down 37.2 / 20.3 / 12.0 / 12.9.
+constexpr int64_t kRowsWarpsPerSm = 32;
+constexpr int64_t kRowsWarpsPerSmI8 = 12;
+
 // 8 rows per CTA unless asked otherwise: three 8-row CTAs per SM measured
 // faster than one 16-row CTA on every decode shape (e.g. 70B FFN up 54 us vs
-// 83 us).
-RowsConfig choose_rows(int64_t K, int64_t N, int sm_count, int cps16, int want_r) {
-    (void)sm_count;
-    (void)cps16;
+// 83 us).  16-row CTAs keep one warp per step (at most 8).  want_threads
+// (32, 64, 128 or 256) fixes the warps along K.
+RowsConfig choose_rows(int64_t K, int64_t N, int sm_count, int want_r, int want_threads, bool i8a) {
     RowsConfig c;
-    c.wk = static_cast<int>(std::min<int64_t>(tk::kMaxWarps, std::max<int64_t>(1, ceil_div(K, tk::kStepK))));
+    const int64_t steps = std::max<int64_t>(1, ceil_div(K, tk::kStepK));
     c.r = want_r != 0 ? want_r : 8;
     c.ctas = std::max<int64_t>(1, ceil_div(N, c.r));
+    int wk = tk::kMaxWarps;
+    if (want_threads != 0) {
+        wk = want_threads / 32;
+    } else if (c.r == 8) {
+        const int64_t need = (i8a ? kRowsWarpsPerSmI8 : kRowsWarpsPerSm) * std::max(1, sm_count);
+        wk = i8a ? 2 : 1;
+        while (wk < tk::kMaxWarps && c.ctas * wk < need) wk *= 2;
+    }
+    c.wk = static_cast<int>(std::min<int64_t>(wk, steps));
     return c;
 }
 
@@ -764,7 +783,11 @@ q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t
         if (vec_bytes != 16 && vec_bytes != 4 && vec_bytes != 1) return Q8MV_ERR_INVALID_ARG;
         if (opts->rows_per_cta != 0 && opts->rows_per_cta != 8 && opts->rows_per_cta != 16)
             return Q8MV_ERR_INVALID_ARG;
-        const RowsConfig c = choose_rows(K, N, sm_count, ctas_per_sm, opts->rows_per_cta);
+        if (opts->cta_threads != 0 && opts->cta_threads != 32 && opts->cta_threads != 64 &&
+            opts->cta_threads != 128 && opts->cta_threads != 256)
+            return Q8MV_ERR_INVALID_ARG;
+        const RowsConfig c = choose_rows(K, N, sm_count, opts->rows_per_cta, opts->cta_threads,
+                                         opts->kernel == Q8MV_KERNEL_ROWS_I8);
         fill_rows_info(c, K, vec_bytes, sm_count, ctas_per_sm, 0, info);
         info->kernel = opts->kernel;
         return Q8MV_OK;
@@ -1502,7 +1525,10 @@ q8mv_status_t q8mv_plan_transposed(q8mv_plan_t *out, int64_t K, int64_t N, int d
         if (opts->rows_per_cta != 0 && opts->rows_per_cta != 8 && opts->rows_per_cta != 16)
             return Q8MV_ERR_INVALID_ARG;
         if (opts->overlap != 0 && opts->overlap != 1) return Q8MV_ERR_INVALID_ARG;
-        if (opts->threads_n != 0 || opts->split_k != 0 || opts->stages != 0 || opts->cta_threads != 0)
+        if (opts->cta_threads != 0 && opts->cta_threads != 32 && opts->cta_threads != 64 &&
+            opts->cta_threads != 128 && opts->cta_threads != 256)
+            return Q8MV_ERR_INVALID_ARG;
+        if (opts->threads_n != 0 || opts->split_k != 0 || opts->stages != 0)
             return Q8MV_ERR_INVALID_ARG;
     }
     int prev = 0;
@@ -1545,14 +1571,11 @@ q8mv_status_t q8mv_plan_transposed(q8mv_plan_t *out, int64_t K, int64_t N, int d
     if (st == Q8MV_OK) st = cuda_status(cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, device));
     if (st != Q8MV_OK) return fail(st);
     if (major != 10 || minor != 3) return fail(Q8MV_ERR_UNSUPPORTED_DEVICE);
-    int cps16 = 1;
-    st = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cps16, rows_kernel(16, 16), 256, 0));
-    if (st != Q8MV_OK) return fail(st == Q8MV_ERR_CUDA ? Q8MV_ERR_UNSUPPORTED_DEVICE : st);
-    p->rcfg = choose_rows(K, N, p->sm_count, cps16, opts ? opts->rows_per_cta : 0);
+    p->rcfg = choose_rows(K, N, p->sm_count, opts ? opts->rows_per_cta : 0, opts ? opts->cta_threads : 0, p->rows_i8);
     int cps = 1;
     st = cuda_status(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cps, rows_kernel(16, p->rcfg.r, p->rows_i8),
                                                                    32 * p->rcfg.wk, 0));
-    if (st != Q8MV_OK) return fail(st);
+    if (st != Q8MV_OK) return fail(st == Q8MV_ERR_CUDA ? Q8MV_ERR_UNSUPPORTED_DEVICE : st);
     p->rows_cps = cps;
     st = cuda_status(cudaMalloc(&p->err, sizeof(int)));
     if (st == Q8MV_OK) st = cuda_status(cudaMemset(p->err, 0, sizeof(int)));

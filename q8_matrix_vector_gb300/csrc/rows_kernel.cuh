@@ -15,8 +15,9 @@
 // (byte permute into the mantissa of 2^23, packed subtract) and multiplies them
 // with its 16 activations in packed f32x2 FMAs; the two lanes of a block add
 // their halves with one shuffle, and the even lane applies the block's scale
-// once.  After its steps each warp sums its lanes per row (fixed butterfly), and
-// the CTA adds the warps in order in shared memory before writing C.
+// once.  After its steps each warp sums its lanes for all rows at once (a fixed
+// tree in which a lane keeps half of its rows at each level), and the CTA adds
+// the warps in order in shared memory before writing C.
 //
 // A last partial block that would give one warp a second 512-wide step of its
 // own (K = 8 full steps plus a few k, as in a 4100-wide LM head) is instead
@@ -199,6 +200,34 @@ __device__ __forceinline__ void load_a(const Params &p, int64_t k, float2 (&a2)[
     }
 }
 
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// The warp's sums of v[r] over its 32 lanes for all R rows at once (R = 8 or
+// 16): at each of log2(R) halving levels (lane masks 16, 8, ...) a lane keeps
+// half of its rows and sends the other half to its partner, adding what it
+// receives; the remaining levels add whole.  Afterwards lane l holds the total
+// of row l / (32 / R) (every lane of that span the same value).  A fixed
+// tree, so the sums are bitwise repeatable.
+template <int R>
+__device__ __forceinline__ float warp_sum_rows(float (&v)[R], int lane) {
+    constexpr int kLevels = ilog2(R);
+#pragma unroll
+    for (int lv = 0; lv < kLevels; ++lv) {
+        const int h = R >> (lv + 1), mask = 16 >> lv;
+        const bool up = (lane & mask) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = up ? v[i] : v[i + h];
+            const float keep = up ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (int mask = 16 >> kLevels; mask >= 1; mask >>= 1) t += __shfl_xor_sync(0xffffffffu, t, mask);
+    return t;
+}
+
 // 8-row CTAs fit three per SM in registers (measured best); 16-row CTAs hold
 // twice the loads in flight per thread and take the register file of one CTA
 // per SM.
@@ -304,12 +333,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_row
     step_loads(k0);
     if (p.tail > 0) {
         // rows are 4-byte aligned here (K % 4 == 0); words past the tail are never read
-        const int t = threadIdx.x;
-        if (t < R * (kBlk / 4)) {
-            const int r = t / (kBlk / 4), q = t % (kBlk / 4);
+        // (a CTA of 1 to 8 warps: each thread takes every blockDim.x-th word)
+        for (int i = threadIdx.x; i < R * (kBlk / 4); i += blockDim.x) {
+            const int r = i / (kBlk / 4), q = i % (kBlk / 4);
             if (r < nrows && 4 * q < p.tail) cp_async4(&tail_w[r][q], w_base + r * p.K + p.k_main + 4 * q);
         }
-        if (t < nrows) cp_async4(&tail_s[t], s_base + t * p.KB + p.k_main / kBlk);
+        for (int r = threadIdx.x; r < nrows; r += blockDim.x) cp_async4(&tail_s[r], s_base + r * p.KB + p.k_main / kBlk);
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
     pdl_launch_dependents();
@@ -362,13 +391,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, rows_min_blocks<R>()) q8mv_row
         }
     }
 
-    // lanes of the warp per row (fixed butterfly), then the warps in order
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        float v = acc[r];
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == 0) part[warp][r] = v;
+    // lanes of the warp for all rows at once (fixed tree), then the warps in order
+    {
+        const float v = warp_sum_rows<R>(acc, lane);
+        if ((lane & (32 / R - 1)) == 0) part[warp][lane / (32 / R)] = v;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();

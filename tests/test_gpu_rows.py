@@ -109,16 +109,21 @@ def test_rows_misaligned_bases(q8, orc, w_offset, a_offset):
 
 @pytest.mark.parametrize("vec", [16, 4, 1])
 @pytest.mark.parametrize("rows_per_cta", [8, 16])
+@pytest.mark.parametrize("cta_threads", [0, 32, 64, 128, 256])
 @pytest.mark.parametrize("K,N", [(4096, 1000), (11008, 129), (4100, 77)])
-def test_rows_forced_configurations(q8, orc, vec, rows_per_cta, K, N):
+def test_rows_forced_configurations(q8, orc, vec, rows_per_cta, cta_threads, K, N):
+    """Every load width, rows per CTA and warps along K (1 to 8 warps, each
+    taking every wk-th 512-wide step), against the oracle."""
     A, W, S = workloads.make_random(K, N, seed=K + N)
     Wt, St = transpose(W, S)
-    plan = q8.Plan(K, N, transposed=True, vec_bytes=vec, rows_per_cta=rows_per_cta)
+    plan = q8.Plan(K, N, transposed=True, vec_bytes=vec, rows_per_cta=rows_per_cta, cta_threads=cta_threads)
     assert plan.info["tile_n"] == rows_per_cta
+    if cta_threads:
+        assert plan.info["groups_k"] == min(cta_threads // 32, -(-K // 512))
     got, guards = run_rows(plan, A, Wt, St)
     ref, bound = orc.transposed(A, Wt, St)
     assert guards
-    assert_close(got, ref, bound, f"vec={vec} R={rows_per_cta} K={K} N={N}")
+    assert_close(got, ref, bound, f"vec={vec} R={rows_per_cta} wk={plan.info['groups_k']} K={K} N={N}")
 
 
 @pytest.mark.parametrize("act", [None, "silu"])
@@ -182,14 +187,17 @@ def test_rows_zero_sizes(q8):
 
 @pytest.mark.parametrize("K", [4100, 4104, 4112, 4128, 8196])
 @pytest.mark.parametrize("rows_per_cta", [8, 16])
-def test_rows_short_tail_staged_in_shared_memory(q8, orc, K, rows_per_cta):
-    """K = whole 512-wide steps (a multiple of the 8 warps) plus at most one
-    block: the last block is copied at the start and folded in at the end.
-    f32 and int8 activations, ragged last CTA, exact-integer data bit for bit."""
+@pytest.mark.parametrize("cta_threads", [0, 32, 64, 256])
+def test_rows_short_tail_staged_in_shared_memory(q8, orc, K, rows_per_cta, cta_threads):
+    """K = whole 512-wide steps (a multiple of the warps along K) plus at most
+    one block: the last block is copied at the start (by CTAs of 1 to 8 warps)
+    and folded in at the end.  f32 and int8 activations, ragged last CTA,
+    exact-integer data bit for bit."""
     N = 1000 + K % 7
     A, W, S = workloads.make_random(K, N, seed=K + rows_per_cta)
     Wt, St = transpose(W, S)
-    plan = q8.Plan(K, N, transposed=True, rows_per_cta=rows_per_cta)
+    opts = dict(rows_per_cta=rows_per_cta, cta_threads=cta_threads)
+    plan = q8.Plan(K, N, transposed=True, **opts)
     got, guards = run_rows(plan, A, Wt, St)
     ref, bound = orc.transposed(A, Wt, St)
     assert guards
@@ -199,7 +207,7 @@ def test_rows_short_tail_staged_in_shared_memory(q8, orc, K, rows_per_cta):
     got_i, _ = run_rows(plan, Ai, Wti, Sti)
     ref_i, _ = orc.transposed(Ai, Wti, Sti)
     assert np.array_equal(got_i, ref_i), np.flatnonzero(got_i != ref_i)[:10]
-    plan8 = q8.Plan(K, N, transposed=True, rows_per_cta=rows_per_cta, kernel=q8.KERNEL_ROWS_I8)
+    plan8 = q8.Plan(K, N, transposed=True, kernel=q8.KERNEL_ROWS_I8, **opts)
     got8, _ = run_rows(plan8, A, Wt, St)
     qa, da = orc.quantize(A.reshape(K))
     ref8, bound8 = orc.i8(qa, da, Wt, St)

@@ -326,10 +326,34 @@ def test_rows_planner_covers_every_row_and_step(q8, K, N):
             assert c["kernel"] == q8.KERNEL_ROWS and c["vec_bytes"] == vec
             assert c["tile_n"] in (8, 16) and (r == 0 or c["tile_n"] == r)
             assert c["grid_x"] * c["tile_n"] >= N and (c["grid_x"] - 1) * c["tile_n"] < max(N, 1)
-            # one warp per 512-wide step of K, at most 8
+            # 1, 2, 4 or 8 warps along K, at most one per 512-wide step; 16-row CTAs take 8
             steps = max(1, (K + 511) // 512)
-            assert c["groups_k"] == min(8, steps) and c["threads_per_cta"] == 32 * c["groups_k"]
+            assert c["groups_k"] <= min(8, steps) and c["threads_per_cta"] == 32 * c["groups_k"]
+            assert c["groups_k"] in (1, 2, 4, 8) or c["groups_k"] == steps
+            if c["tile_n"] == 16:
+                assert c["groups_k"] == min(8, steps)
             assert c["split_k"] == 1 and c["workspace_bytes"] == 0
+
+
+def test_rows_planner_warps_along_k(q8):
+    # the fewest warps along K (int8 activations: at least 2) whose grid gives
+    # every SM 32 warps (int8: 12), at most one per 512-wide step
+    def wk(K, N, i8=False, **kw):
+        kern = q8.KERNEL_ROWS_I8 if i8 else q8.KERNEL_ROWS
+        return q8.choose_config(K, N, 152, 3, 16, kernel=kern, **kw)["groups_k"]
+
+    assert wk(4100, 128256) == 1 and wk(8192, 28672) == 2 and wk(4096, 14336) == 4
+    assert wk(14336, 4096) == 8 and wk(4096, 4096) == 8 and wk(4096, 11008) == 4
+    assert wk(4100, 128256, True) == 2 and wk(4096, 14336, True) == 2 and wk(14336, 4096, True) == 4
+    assert wk(4096, 4096, True) == 4 and wk(8192, 28672, True) == 2
+    assert wk(1024, 200) == 2 and wk(100, 200) == 1  # capped by the steps of K
+    for t in (32, 64, 128, 256):
+        assert wk(4100, 128256, cta_threads=t) == t // 32
+        assert wk(600, 1000, cta_threads=t) == min(t // 32, 2)
+    assert wk(4096, 4096, rows_per_cta=16) == 8
+    for bad in (16, 96, 512):
+        with pytest.raises(q8.Q8mvError):
+            wk(4096, 4096, cta_threads=bad)
 
 
 def test_rows_planner_picks_rows_per_cta(q8):
@@ -363,7 +387,7 @@ def test_transposed_plan_rejects_bad_arguments_before_touching_a_device(q8):
 
 def test_int8_activation_planner_and_quantize_arguments(q8):
     c = q8.choose_config(4096, 4096, 152, 3, 16, kernel=q8.KERNEL_ROWS_I8)
-    assert c["kernel"] == q8.KERNEL_ROWS_I8 and c["tile_n"] == 8 and c["groups_k"] == 8
+    assert c["kernel"] == q8.KERNEL_ROWS_I8 and c["tile_n"] == 8 and c["groups_k"] == 4
     lib = q8.library()
     assert lib.q8mv_quantize_rows(-1, 64, None, None, None, None) == q8.Q8MV_ERR_INVALID_ARG
     assert lib.q8mv_quantize_rows(2, -1, None, None, None, None) == q8.Q8MV_ERR_INVALID_ARG
