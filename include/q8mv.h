@@ -317,9 +317,10 @@ q8mv_status_t q8mv_plan_info(q8mv_plan_t plan, q8mv_plan_info_t *info);
  * or kernel REGS/AUTO): `ctas_per_sm` resident CTAs and weight loads of
  * `vec_bytes` (which must divide N).  For opts->kernel == Q8MV_KERNEL_STREAM
  * the last two are ignored and an SM is taken to hold 228 KiB of shared
- * memory with 1 KiB reserved per CTA.  For opts->kernel == Q8MV_KERNEL_ROWS: the transposed
- * plan's rows per CTA and warps along K, for `ctas_per_sm` resident CTAs of 16
- * rows and loads of `vec_bytes` (16, 4 or 1).  Fills *info (workspace_bytes of
+ * memory with 1 KiB reserved per CTA.  For opts->kernel == Q8MV_KERNEL_ROWS or
+ * Q8MV_KERNEL_ROWS_I8: the transposed plan's rows per CTA and warps along K
+ * (which depend on sm_count, not on ctas_per_sm, which is only reported back)
+ * for loads of `vec_bytes` (16, 4 or 1).  Fills *info (workspace_bytes of
  * partial rows).
  */
 q8mv_status_t q8mv_choose_config(int64_t K, int64_t N, int32_t sm_count, int32_t ctas_per_sm,
