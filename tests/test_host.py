@@ -154,6 +154,29 @@ def test_planner_fills_the_gpu_for_the_attention_projection(q8):
     assert c["split_k"] > 1 and c["cluster"] == 1 and c["workspace_bytes"] == 0
 
 
+def test_planner_ties_go_to_256_thread_ctas(q8):
+    # a plan and the one with half the threads per CTA and half the columns per
+    # thread group hold the same resident warps and cost the same in the
+    # planner's model; the 256-thread CTAs win (measured faster on the LM head,
+    # 70B FFN up and FFN up).  8-byte loads, overlapped launches, 2 resident
+    # 256-thread CTAs per SM (4 of 128 threads), as on the device
+    def pick(K, N):
+        c = q8.choose_config(K, N, 152, 2, 8, overlap=1)
+        return c["threads_per_cta"], c["threads_n"], c["split_k"]
+
+    assert pick(4100, 128256) == (256, 64, 1)
+    assert pick(8192, 28672) == (256, 64, 5)
+    assert pick(4096, 11008) == (256, 16, 3)
+    assert pick(4096, 4096) == (256, 16, 8) and pick(11008, 4096) == (256, 16, 8)
+    # each tie's other half is a legal plan of the same modelled cost
+    for K, N in ((4100, 128256), (8192, 28672)):
+        a = q8.choose_config(K, N, 152, 2, 8, overlap=1)
+        b = q8.choose_config(K, N, 152, 2, 8, overlap=1, cta_threads=128, threads_n=a["threads_n"] // 2,
+                             split_k=a["split_k"])
+        assert b["threads_per_cta"] == 128 and b["groups_k"] == a["groups_k"]
+        assert b["tile_n"] * 2 == a["tile_n"] and b["grid_x"] * b["tile_n"] >= N
+
+
 def test_planner_honours_overrides(q8):
     c = q8.choose_config(4096, 4096, 152, 1, 16, threads_n=128, split_k=4)
     assert c["threads_n"] == 128 and c["split_k"] == 4 and c["blocks_per_split"] == 32
