@@ -168,7 +168,7 @@ def test_planner_ties_go_to_256_thread_ctas(q8):
     assert pick(8192, 28672) == (256, 64, 5)
     assert pick(4096, 11008) == (256, 16, 3)
     assert pick(4096, 4096) == (256, 16, 8) and pick(11008, 4096) == (256, 16, 8)
-    # each tie's other half is a legal plan of the same modelled cost
+    # the other half of each tie is a legal plan with the same thread groups along K
     for K, N in ((4100, 128256), (8192, 28672)):
         a = q8.choose_config(K, N, 152, 2, 8, overlap=1)
         b = q8.choose_config(K, N, 152, 2, 8, overlap=1, cta_threads=128, threads_n=a["threads_n"] // 2,
